@@ -1,0 +1,166 @@
+"""CPU oracle for the selective-scan layer core -- TEST INFRASTRUCTURE ONLY.
+
+The arithmetic lives in ``m3scan_oracle.c`` (plain float64 C, single
+threaded).  This module compiles it with gcc, loads it with ctypes and wraps
+it for NumPy arrays.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import it; the CUDA library never does,
+and nothing here imports the CUDA library.
+
+Every function takes the same (already dtype-rounded) inputs the GPU sees,
+promoted to float64, and returns float64 results.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import sys
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "m3scan_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "libm3oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_dp = ctypes.POINTER(ctypes.c_double)
+_u8p = ctypes.POINTER(ctypes.c_uint8)
+_i64 = ctypes.c_int64
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into a shared library (IEEE float64, no fast-math)."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-fPIC", "-shared", "-std=c11", "-fno-fast-math",
+           "-ffp-contract=off", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            lib.m3o_forward.restype = ctypes.c_int
+            lib.m3o_forward.argtypes = [_i64] * 5 + [_dp] * 10 + [_u8p] + [_dp] * 5 + [_i64]
+            lib.m3o_backward.restype = ctypes.c_int
+            lib.m3o_backward.argtypes = ([_i64] * 5 + [_dp] * 11 + [_u8p, _i64]
+                                         + [_dp] * 11)
+            _lib = lib
+    return _lib
+
+
+def _c64(a):
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def _ptr(a):
+    if a is None:
+        return None
+    return a.ctypes.data_as(_dp)
+
+
+def _mask_ptr(mask):
+    if mask is None:
+        return None, None
+    m = np.ascontiguousarray(np.asarray(mask, dtype=np.uint8))
+    return m, m.ctypes.data_as(_u8p)
+
+
+def _common(inp):
+    """Unpack an ``Inputs``-like mapping into float64 arrays and sizes."""
+    x = _c64(inp["x"])
+    Bsz, T, D = x.shape
+    Bm = _c64(inp["B"])
+    N = Bm.shape[-1]
+    conv_w = _c64(inp["conv_w"])
+    W = conv_w.shape[-1]
+    arrs = dict(x=x, delta_raw=_c64(inp["delta_raw"]), z=_c64(inp["z"]), B=Bm,
+                C=_c64(inp["C"]), conv_w=conv_w, conv_b=_c64(inp["conv_b"]),
+                dt_bias=_c64(inp["dt_bias"]), a_log=_c64(inp["a_log"]),
+                D=_c64(inp["D"]))
+    return (Bsz, T, D, N, W), arrs
+
+
+def forward(inp, chan_mask=None, ckpt_chunk: int = 0):
+    """Oracle forward.
+
+    Returns a dict with ``gated``, ``y``, ``u``, ``delta`` ([B,T,D]) and, if
+    ``ckpt_chunk`` > 0, ``ckpt`` ([B, ceil(T/K), N, D], the state before each
+    chunk).  Channels outside ``chan_mask`` are left as zeros.
+    """
+    lib = _load()
+    (Bsz, T, D, N, W), a = _common(inp)
+    gated = np.zeros((Bsz, T, D))
+    y = np.zeros((Bsz, T, D))
+    u = np.zeros((Bsz, T, D))
+    delta = np.zeros((Bsz, T, D))
+    ckpt = None
+    if ckpt_chunk > 0:
+        nc = (T + ckpt_chunk - 1) // ckpt_chunk
+        ckpt = np.zeros((Bsz, nc, N, D))
+    _m, mp = _mask_ptr(chan_mask)
+    rc = lib.m3o_forward(Bsz, T, D, N, W, _ptr(a["x"]), _ptr(a["delta_raw"]),
+                         _ptr(a["z"]), _ptr(a["B"]), _ptr(a["C"]),
+                         _ptr(a["conv_w"]), _ptr(a["conv_b"]), _ptr(a["dt_bias"]),
+                         _ptr(a["a_log"]), _ptr(a["D"]), mp, _ptr(gated), _ptr(y),
+                         _ptr(u), _ptr(delta), _ptr(ckpt), int(ckpt_chunk))
+    if rc != 0:
+        raise MemoryError("oracle forward: allocation failed")
+    out = dict(gated=gated, y=y, u=u, delta=delta)
+    if ckpt is not None:
+        out["ckpt"] = ckpt
+    return out
+
+
+GRAD_NAMES = ("d_x", "d_delta_raw", "dz", "du", "dB", "dC", "d_conv_w",
+              "d_conv_b", "d_dt_bias", "d_a_log", "dD")
+
+
+def backward(inp, d_gated=None, chan_mask=None, chunk: int = 0):
+    """Oracle backward of L = sum(gated * d_gated).
+
+    ``chunk`` = 0 keeps every state (sequential); ``chunk`` > 0 recomputes
+    states chunk by chunk from chunk-start states.  Returns a dict of float64
+    gradients named as in ``GRAD_NAMES``.
+    """
+    lib = _load()
+    (Bsz, T, D, N, W), a = _common(inp)
+    g = _c64(inp["d_gated"] if d_gated is None else d_gated)
+    out = {k: np.zeros((Bsz, T, D)) for k in ("d_x", "d_delta_raw", "dz", "du")}
+    out["dB"] = np.zeros((Bsz, T, N))
+    out["dC"] = np.zeros((Bsz, T, N))
+    out["d_conv_w"] = np.zeros((D, W))
+    out["d_conv_b"] = np.zeros(D)
+    out["d_dt_bias"] = np.zeros(D)
+    out["d_a_log"] = np.zeros((D, N))
+    out["dD"] = np.zeros(D)
+    _m, mp = _mask_ptr(chan_mask)
+    rc = lib.m3o_backward(Bsz, T, D, N, W, _ptr(a["x"]), _ptr(a["delta_raw"]),
+                          _ptr(a["z"]), _ptr(a["B"]), _ptr(a["C"]),
+                          _ptr(a["conv_w"]), _ptr(a["conv_b"]), _ptr(a["dt_bias"]),
+                          _ptr(a["a_log"]), _ptr(a["D"]), _ptr(g), mp, int(chunk),
+                          *[_ptr(out[k]) for k in GRAD_NAMES])
+    if rc != 0:
+        raise MemoryError("oracle backward: allocation failed")
+    return out
+
+
+def loss(inp, d_gated=None) -> float:
+    """L = sum(gated * d_gated), the scalar whose gradient ``backward`` gives."""
+    g = _c64(inp["d_gated"] if d_gated is None else d_gated)
+    return float(np.sum(forward(inp)["gated"] * g))
+
+
+if __name__ == "__main__":  # pragma: no cover
+    print(build(force="--force" in sys.argv))
