@@ -1,0 +1,152 @@
+/*
+ * m3scan.h -- C ABI of the GB300 selective-scan layer core (Mamba-1).
+ *
+ * The layer core, forward (the per-layer loop of
+ * gpu_forward_mamba_backbone_mixed on the mamba-rs 0.3.1 page
+ * src/mamba_ssm/gpu/forward_mixed.rs, steps F4a conv1d, F4c softplus,
+ * F4d selective scan, F4e gating):
+ *
+ *   c[t]     = conv_b + sum_{k<4} conv_w[k] * x[t-3+k]       (x = 0 for t < 0)
+ *   u[t]     = c[t] * sigmoid(c[t])
+ *   delta[t] = softplus(delta_raw[t] + dt_bias)
+ *   A[n]     = -exp(a_log[n])                 (trainer.rs 0.7.3, recompute_a_neg_all)
+ *   h_t[n]   = exp(delta[t] * A[n]) * h_{t-1}[n] + delta[t] * B_t[n] * u[t],  h_{-1} = 0
+ *   y[t]     = sum_n C_t[n] * h_t[n] + D * u[t]
+ *   gated[t] = y[t] * z[t] * sigmoid(z[t])
+ *
+ * per (batch b, channel d); B_t and C_t are shared by every channel of a
+ * token.  The backward is the reverse-time derivative of
+ * L = sum gated * d_gated, giving the gradients the backward scratch of the
+ * same page names (d_u, d_delta, d_B, d_C reduced over d_inner, d_D, d_a_log,
+ * softplus and conv1d backward).
+ *
+ * Layouts (row-major, channel fastest; every pointer is a DEVICE pointer):
+ *   x, delta_raw, z, gated, y_dbg, d_gated, d_x, d_delta_raw, dz, du_dbg
+ *                       : [batch, seq_len, d_inner]  activation dtype
+ *   Bm, Cm              : [batch, seq_len, d_state]  activation dtype
+ *   dB, dC              : [batch, seq_len, d_state]  float32
+ *   conv_w, d_conv_w    : [d_inner, d_conv]          float32
+ *   a_log, d_a_log      : [d_inner, d_state]         float32
+ *   conv_b, dt_bias, D and their grads : [d_inner]   float32
+ *   ckpt                : [batch, n_chunks, d_state, d_inner] float32, where
+ *                         ckpt[b, c, n, d] is h before step c * chunk.
+ *
+ * Ownership: the caller allocates and frees every buffer, including the
+ * workspace sized by m3scan_plan.  The library never allocates, frees or
+ * synchronises; all work is enqueued on `stream` in order.  Buffers must
+ * stay valid until that work completes.  Calls on one workspace must not
+ * overlap on the GPU.
+ *
+ * Errors: arguments are validated before anything is enqueued; a failed
+ * validation returns a status and enqueues nothing.  A failed launch
+ * returns M3_ERR_CUDA (the CUDA error is cleared with cudaGetLastError).
+ * Unsupported shapes return M3_ERR_UNSUPPORTED; there is no fallback path.
+ */
+#ifndef M3SCAN_H
+#define M3SCAN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t (NULL = the legacy default stream). */
+typedef struct CUstream_st* m3_stream_t;
+
+typedef enum {
+    M3_F32 = 0,  /* activations stored as float32 */
+    M3_BF16 = 1  /* activations stored as bfloat16 (state, params, grads f32) */
+} m3_dtype;
+
+typedef enum {
+    M3_OK = 0,
+    M3_ERR_NULL = 1,        /* a required pointer is NULL */
+    M3_ERR_DIMS = 2,        /* a size is negative or out of range */
+    M3_ERR_UNSUPPORTED = 3, /* d_state != 16, d_conv != 4, d_inner % 8 != 0, dtype */
+    M3_ERR_ALIGN = 4,       /* a pointer is not aligned as required */
+    M3_ERR_WORKSPACE = 5,   /* workspace missing or smaller than planned */
+    M3_ERR_CUDA = 6         /* a CUDA runtime call or launch failed */
+} m3_status;
+
+typedef struct {
+    int64_t batch, seq_len, d_inner, d_state, d_conv;
+    /* Checkpoint interval K in steps (1..64); 0 = library default (16). */
+    int64_t chunk;
+    /* Number of time segments scanned in parallel (each segment is a run of
+       whole chunks); 0 = chosen from the shape and the current device. */
+    int64_t segments;
+    /* 1: param grads are added to the output buffers; 0: overwritten. */
+    int32_t accumulate_param_grads;
+    int32_t reserved;
+} m3_dims;
+
+typedef struct {
+    int64_t chunk;              /* K actually used */
+    int64_t n_chunks;           /* ceil(seq_len / K) */
+    int64_t fwd_segments;       /* time segments of the forward */
+    int64_t bwd_segments;       /* time segments of the backward */
+    int64_t ckpt_bytes;         /* size of ckpt */
+    int64_t workspace_bytes;    /* size of the workspace both calls need */
+    int32_t fwd_launches;       /* kernels one m3scan_fwd enqueues */
+    int32_t bwd_launches;       /* kernels one m3scan_bwd enqueues (memsets excluded) */
+} m3_plan;
+
+/*
+ * Resolve defaults and size the caller-owned buffers.  With
+ * dims->segments == 0 it queries the current CUDA device (SM count and
+ * kernel occupancy); with an explicit segment count it touches no device.
+ * Returns M3_OK and fills *plan, or a validation status.
+ */
+m3_status m3scan_plan(const m3_dims* dims, m3_dtype act, m3_plan* plan);
+
+/*
+ * Forward.  Writes gated (and y_dbg = y when non-NULL) and the chunk
+ * checkpoints ckpt that m3scan_bwd reads.  Activation pointers must be
+ * 16-byte aligned; float32 pointers 4-byte aligned; workspace 256-byte
+ * aligned with workspace_bytes >= plan.workspace_bytes.
+ */
+m3_status m3scan_fwd(const m3_dims* dims, m3_dtype act,
+                     const void* x, const void* delta_raw, const void* z,
+                     const void* Bm, const void* Cm,
+                     const float* conv_w, const float* conv_b,
+                     const float* dt_bias, const float* a_log, const float* D,
+                     void* gated, void* y_dbg, float* ckpt,
+                     void* workspace, size_t workspace_bytes,
+                     m3_stream_t stream);
+
+/*
+ * Backward of L = sum(gated * d_gated), from the forward's inputs and its
+ * checkpoints.  Writes d_x, d_delta_raw, dz (and du_dbg = dL/du through the
+ * D skip and the recurrence, when non-NULL) in the activation dtype;
+ * overwrites dB and dC (float32, reduced over d_inner); writes or adds the
+ * float32 parameter grads d_conv_w, d_conv_b, d_dt_bias, d_a_log, dD per
+ * dims->accumulate_param_grads.  dims->chunk must equal the chunk the
+ * forward that wrote ckpt used; the segment counts of the two calls are
+ * independent of each other.
+ */
+m3_status m3scan_bwd(const m3_dims* dims, m3_dtype act,
+                     const void* x, const void* delta_raw, const void* z,
+                     const void* Bm, const void* Cm,
+                     const float* conv_w, const float* conv_b,
+                     const float* dt_bias, const float* a_log, const float* D,
+                     const float* ckpt, const void* d_gated,
+                     void* d_x, void* d_delta_raw, void* dz, void* du_dbg,
+                     float* dB, float* dC,
+                     float* d_conv_w, float* d_conv_b, float* d_dt_bias,
+                     float* d_a_log, float* dD,
+                     void* workspace, size_t workspace_bytes,
+                     m3_stream_t stream);
+
+/* A static, human-readable name for a status code. */
+const char* m3scan_status_string(m3_status status);
+
+/* Library version as major * 10000 + minor * 100 + patch. */
+int32_t m3scan_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* M3SCAN_H */

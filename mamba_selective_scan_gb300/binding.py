@@ -1,0 +1,285 @@
+"""Thin Python binding of the m3scan C ABI (include/m3scan.h).
+
+Argument marshalling only: every step of the layer core runs in the CUDA
+library.  PyTorch supplies device memory and the stream; outputs that the
+caller does not pass are allocated here with ``torch.empty``.  If the
+library cannot be loaded the calls raise -- there is no other path.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+M3_F32 = 0
+M3_BF16 = 1
+
+STATUS = {
+    0: "M3_OK",
+    1: "M3_ERR_NULL",
+    2: "M3_ERR_DIMS",
+    3: "M3_ERR_UNSUPPORTED",
+    4: "M3_ERR_ALIGN",
+    5: "M3_ERR_WORKSPACE",
+    6: "M3_ERR_CUDA",
+}
+
+# every symbol include/m3scan.h declares
+EXPORTS = ("m3scan_plan", "m3scan_fwd", "m3scan_bwd", "m3scan_status_string",
+           "m3scan_version")
+
+
+class M3Error(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = _lib_handle().m3scan_status_string(status).decode() if _LIB else STATUS.get(status)
+        super().__init__(f"{where}: {msg}")
+
+
+class M3Dims(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int64), ("seq_len", ctypes.c_int64),
+                ("d_inner", ctypes.c_int64), ("d_state", ctypes.c_int64),
+                ("d_conv", ctypes.c_int64), ("chunk", ctypes.c_int64),
+                ("segments", ctypes.c_int64),
+                ("accumulate_param_grads", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
+
+
+class M3Plan(ctypes.Structure):
+    _fields_ = [("chunk", ctypes.c_int64), ("n_chunks", ctypes.c_int64),
+                ("fwd_segments", ctypes.c_int64), ("bwd_segments", ctypes.c_int64),
+                ("ckpt_bytes", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64),
+                ("fwd_launches", ctypes.c_int32), ("bwd_launches", ctypes.c_int32)]
+
+    def as_dict(self):
+        return {k: getattr(self, k) for k, _ in self._fields_}
+
+
+_LIB = None
+_LOCK = threading.Lock()
+_vp = ctypes.c_void_p
+_fp = ctypes.c_void_p  # float* passed as an address
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def _lib_handle(build_if_missing: bool = True):
+    global _LIB
+    with _LOCK:
+        if _LIB is None:
+            path = _build.LIB_PATH
+            if build_if_missing and not os.path.exists(path):
+                _build.build()
+            if not os.path.exists(path):
+                raise RuntimeError(f"libm3scan not built: {path} is missing")
+            lib = ctypes.CDLL(path)
+            lib.m3scan_plan.restype = ctypes.c_int
+            lib.m3scan_plan.argtypes = [ctypes.POINTER(M3Dims), ctypes.c_int,
+                                        ctypes.POINTER(M3Plan)]
+            lib.m3scan_fwd.restype = ctypes.c_int
+            lib.m3scan_fwd.argtypes = ([ctypes.POINTER(M3Dims), ctypes.c_int] + [_vp] * 5
+                                       + [_fp] * 5 + [_vp, _vp, _fp, _vp, ctypes.c_size_t, _vp])
+            lib.m3scan_bwd.restype = ctypes.c_int
+            lib.m3scan_bwd.argtypes = ([ctypes.POINTER(M3Dims), ctypes.c_int] + [_vp] * 5
+                                       + [_fp] * 5 + [_fp, _vp] + [_vp] * 4 + [_fp] * 2
+                                       + [_fp] * 5 + [_vp, ctypes.c_size_t, _vp])
+            lib.m3scan_status_string.restype = ctypes.c_char_p
+            lib.m3scan_status_string.argtypes = [ctypes.c_int]
+            lib.m3scan_version.restype = ctypes.c_int32
+            lib.m3scan_version.argtypes = []
+            _LIB = lib
+    return _LIB
+
+
+def load():
+    """Load libm3scan (building it first if it is missing)."""
+    return _lib_handle()
+
+
+def make_dims(batch, seq_len, d_inner, d_state=16, d_conv=4, chunk=0, segments=0,
+              accumulate_param_grads=False) -> M3Dims:
+    return M3Dims(int(batch), int(seq_len), int(d_inner), int(d_state), int(d_conv),
+                  int(chunk), int(segments), int(bool(accumulate_param_grads)), 0)
+
+
+def m3scan_plan(dims: M3Dims, act: int) -> M3Plan:
+    out = M3Plan()
+    st = _lib_handle().m3scan_plan(ctypes.byref(dims), int(act), ctypes.byref(out))
+    if st != 0:
+        raise M3Error(st, "m3scan_plan")
+    return out
+
+
+def m3scan_status_string(status: int) -> str:
+    return _lib_handle().m3scan_status_string(int(status)).decode()
+
+
+def m3scan_version() -> int:
+    return int(_lib_handle().m3scan_version())
+
+
+def raw_fwd(dims, act, x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D,
+            gated, y_dbg, ckpt, workspace, workspace_bytes, stream) -> int:
+    """Call m3scan_fwd with integer addresses; returns the status code."""
+    return _lib_handle().m3scan_fwd(ctypes.byref(dims), int(act), x, delta_raw, z, Bm, Cm,
+                                    conv_w, conv_b, dt_bias, a_log, D, gated, y_dbg, ckpt,
+                                    workspace, int(workspace_bytes), stream)
+
+
+def raw_bwd(dims, act, x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D, ckpt,
+            d_gated, d_x, d_delta_raw, dz, du_dbg, dB, dC, d_conv_w, d_conv_b, d_dt_bias,
+            d_a_log, dD, workspace, workspace_bytes, stream) -> int:
+    """Call m3scan_bwd with integer addresses; returns the status code."""
+    return _lib_handle().m3scan_bwd(ctypes.byref(dims), int(act), x, delta_raw, z, Bm, Cm,
+                                    conv_w, conv_b, dt_bias, a_log, D, ckpt, d_gated, d_x,
+                                    d_delta_raw, dz, du_dbg, dB, dC, d_conv_w, d_conv_b,
+                                    d_dt_bias, d_a_log, dD, workspace, int(workspace_bytes),
+                                    stream)
+
+
+# ---------------------------------------------------------------------------
+# torch-tensor wrappers (allocation and pointer marshalling only)
+# ---------------------------------------------------------------------------
+
+def _torch():
+    import torch
+    return torch
+
+
+def _act_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.bfloat16:
+        return M3_BF16
+    if t.dtype == torch.float32:
+        return M3_F32
+    raise TypeError(f"activation dtype must be bfloat16 or float32, got {t.dtype}")
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _check(t, name, dtype=None, device=None):
+    if t is None:
+        return
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def _stream_handle(stream):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+class Workspace:
+    """A device workspace sized for a plan (reusable across calls)."""
+
+    def __init__(self, nbytes: int, device):
+        torch = _torch()
+        self.nbytes = max(int(nbytes), 256)
+        self.buf = torch.empty(self.nbytes, dtype=torch.uint8, device=device)
+
+    @property
+    def ptr(self):
+        return self.buf.data_ptr()
+
+
+def plan_for(x, chunk=0, segments=0):
+    Bsz, T, D = x.shape
+    dims = make_dims(Bsz, T, D, chunk=chunk, segments=segments)
+    return dims, m3scan_plan(dims, _act_code(x))
+
+
+def m3scan_fwd(x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D, *, chunk=0,
+               segments=0, gated=None, y_dbg=None, want_y=False, ckpt=None, workspace=None,
+               stream=None):
+    """Forward of the layer core.  Returns (gated, ckpt, y_dbg or None)."""
+    torch = _torch()
+    act = x.dtype
+    dev = x.device
+    for n, t in (("x", x), ("delta_raw", delta_raw), ("z", z), ("B", Bm), ("C", Cm)):
+        _check(t, n, act, dev)
+    for n, t in (("conv_w", conv_w), ("conv_b", conv_b), ("dt_bias", dt_bias),
+                 ("a_log", a_log), ("D", D)):
+        _check(t, n, torch.float32, dev)
+    Bsz, T, Dn = x.shape
+    dims = make_dims(Bsz, T, Dn, d_state=Bm.shape[-1], d_conv=conv_w.shape[-1], chunk=chunk,
+                     segments=segments)
+    code = _act_code(x)
+    pl = m3scan_plan(dims, code)
+    if gated is None:
+        gated = torch.empty_like(x)
+    if want_y and y_dbg is None:
+        y_dbg = torch.empty_like(x)
+    if ckpt is None:
+        ckpt = torch.empty((Bsz, pl.n_chunks, Bm.shape[-1], Dn), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = Workspace(pl.workspace_bytes, dev)
+    st = raw_fwd(dims, code, _ptr(x), _ptr(delta_raw), _ptr(z), _ptr(Bm), _ptr(Cm),
+                 _ptr(conv_w), _ptr(conv_b), _ptr(dt_bias), _ptr(a_log), _ptr(D),
+                 _ptr(gated), _ptr(y_dbg), _ptr(ckpt), workspace.ptr, workspace.nbytes,
+                 _stream_handle(stream))
+    if st != 0:
+        raise M3Error(st, "m3scan_fwd")
+    return gated, ckpt, y_dbg
+
+
+def m3scan_bwd(x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D, ckpt, d_gated, *,
+               chunk=0, segments=0, want_du=False, accumulate_param_grads=False, out=None,
+               workspace=None, stream=None):
+    """Backward of the layer core.  Returns a dict of gradients (tensors)."""
+    torch = _torch()
+    act = x.dtype
+    dev = x.device
+    for n, t in (("x", x), ("delta_raw", delta_raw), ("z", z), ("B", Bm), ("C", Cm),
+                 ("d_gated", d_gated)):
+        _check(t, n, act, dev)
+    for n, t in (("conv_w", conv_w), ("conv_b", conv_b), ("dt_bias", dt_bias),
+                 ("a_log", a_log), ("D", D), ("ckpt", ckpt)):
+        _check(t, n, torch.float32, dev)
+    Bsz, T, Dn = x.shape
+    N = Bm.shape[-1]
+    W = conv_w.shape[-1]
+    dims = make_dims(Bsz, T, Dn, d_state=N, d_conv=W, chunk=chunk, segments=segments,
+                     accumulate_param_grads=accumulate_param_grads)
+    code = _act_code(x)
+    pl = m3scan_plan(dims, code)
+    o = dict(out or {})
+    o.setdefault("d_x", torch.empty_like(x))
+    o.setdefault("d_delta_raw", torch.empty_like(x))
+    o.setdefault("dz", torch.empty_like(x))
+    if want_du:
+        o.setdefault("du", torch.empty_like(x))
+    f32 = dict(dtype=torch.float32, device=dev)
+    o.setdefault("dB", torch.empty((Bsz, T, N), **f32))
+    o.setdefault("dC", torch.empty((Bsz, T, N), **f32))
+    o.setdefault("d_conv_w", torch.zeros((Dn, W), **f32))
+    o.setdefault("d_conv_b", torch.zeros((Dn,), **f32))
+    o.setdefault("d_dt_bias", torch.zeros((Dn,), **f32))
+    o.setdefault("d_a_log", torch.zeros((Dn, N), **f32))
+    o.setdefault("dD", torch.zeros((Dn,), **f32))
+    for k, v in o.items():
+        _check(v, k, None, dev)
+    if workspace is None:
+        workspace = Workspace(pl.workspace_bytes, dev)
+    st = raw_bwd(dims, code, _ptr(x), _ptr(delta_raw), _ptr(z), _ptr(Bm), _ptr(Cm),
+                 _ptr(conv_w), _ptr(conv_b), _ptr(dt_bias), _ptr(a_log), _ptr(D), _ptr(ckpt),
+                 _ptr(d_gated), _ptr(o["d_x"]), _ptr(o["d_delta_raw"]), _ptr(o["dz"]),
+                 _ptr(o.get("du")), _ptr(o["dB"]), _ptr(o["dC"]), _ptr(o["d_conv_w"]),
+                 _ptr(o["d_conv_b"]), _ptr(o["d_dt_bias"]), _ptr(o["d_a_log"]), _ptr(o["dD"]),
+                 workspace.ptr, workspace.nbytes, _stream_handle(stream))
+    if st != 0:
+        raise M3Error(st, "m3scan_bwd")
+    return o

@@ -1,0 +1,1165 @@
+// m3scan.cu -- selective-scan layer core (Mamba-1), forward and backward, for
+// sm_103a.  The C ABI is declared in include/m3scan.h.
+//
+// What is computed follows the mamba-rs pages: src/mamba_ssm/gpu/
+// forward_mixed.rs (0.3.1), steps F4a conv1d + SiLU, F4c softplus, F4d the
+// selective scan with the D skip, F4e gating, and the backward scratch list
+// of the same page; A = -exp(a_log) from trainer.rs (0.7.3),
+// recompute_a_neg_all.  The design is not the pages': they save the f32
+// state before every step (h_saved, B*(T+1)*d_inner*d_state) and the
+// discretisation da_exp per step.  Here the forward keeps the 16 state lanes
+// of one channel in registers and writes only the state at the start of each
+// chunk of K steps; the backward recomputes one chunk at a time into shared
+// memory and runs the reverse-time pass from there.
+//
+// Work decomposition.  A block owns (batch b, a group of 64 channels, one
+// time segment); a thread owns one channel and all 16 lanes of its state.
+// When batch * channel groups alone cannot fill the GPU, time is split into
+// S segments of whole chunks.  The scan is linear in the state, so a
+// segment's effect on the next one is (decay, local end state): an
+// aggregate kernel computes it per segment, a carry kernel chains the
+// segments, and the main kernel reruns each segment from its true start.
+// The backward does the same in reverse time for the adjoint state.
+//
+// dB and dC are sums over channels: each warp reduces its 32 channels with
+// a shuffle reduce-scatter, warps combine in shared memory, and each block
+// adds one float per (t, n) to the f32 output with a global reduction.
+// Parameter gradients are written as per-(batch, segment) partials and
+// summed in a fixed order by a finalize kernel (deterministic).
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "../../include/m3scan.h"
+
+namespace {
+
+constexpr int NS = 16;      // d_state lanes per channel
+constexpr int WC = 4;       // conv taps
+constexpr int G = 64;       // channels (= threads) per block
+constexpr int NW = G / 32;  // warps per block
+constexpr int KMAX = 64;    // largest chunk (the backward may allow less)
+constexpr int KDEF = 16;    // default chunk
+constexpr int NPART = 24;   // per-channel parameter partials (23 used)
+constexpr float LOG2E = 1.4426950408889634f;
+constexpr float LN2 = 0.6931471805599453f;
+
+// ---------------------------------------------------------------------------
+// small device helpers
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ float ex2(float v) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
+  return r;
+}
+
+__device__ __forceinline__ float sigmoid_f(float v) {
+  return __frcp_rn(1.0f + __expf(-v));
+}
+
+// log(1 + e^v) = max(v, 0) + log1p(e^-|v|)
+__device__ __forceinline__ float softplus_f(float v) {
+  return fmaxf(v, 0.0f) + log1pf(__expf(-fabsf(v)));
+}
+
+template <typename T> struct Act;
+template <> struct Act<float> {
+  static __device__ __forceinline__ float ld(const float* p) { return *p; }
+  static __device__ __forceinline__ void st(float* p, float v) { *p = v; }
+};
+template <> struct Act<__nv_bfloat16> {
+  static __device__ __forceinline__ float ld(const __nv_bfloat16* p) {
+    return __bfloat162float(*p);
+  }
+  static __device__ __forceinline__ void st(__nv_bfloat16* p, float v) {
+    *p = __float2bfloat16_rn(v);
+  }
+};
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, bool valid) {
+  unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+  int n = valid ? 16 : 0;  // 0 bytes read: the 16 bytes are zero-filled
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(s), "l"(gmem), "r"(n));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+template <int N> __device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
+}
+
+// Stage rows [t_first, t_first + rows) x channels [d0, d0 + G) of a
+// [B, T, D] activation tensor into dst[rows][G]; out-of-range rows and
+// channels read as zero.
+template <typename T>
+__device__ __forceinline__ void stage_act(T* dst, const T* src, int b, int t_first, int rows,
+                                          int T_, int D, int d0, int tid) {
+  constexpr int EPC = 16 / sizeof(T);
+  constexpr int CPR = G / EPC;
+  const int n = rows * CPR;
+  for (int i = tid; i < n; i += G) {
+    const int r = i / CPR, cc = i - r * CPR;
+    const int t = t_first + r, dd = d0 + cc * EPC;
+    const bool ok = (t >= 0) && (t < T_) && (dd < D);
+    const T* g = ok ? src + ((size_t)b * T_ + t) * D + dd : src;
+    cp_async16(dst + r * G + cc * EPC, g, ok);
+  }
+}
+
+// Stage rows [t_first, t_first + rows) of a [B, T, 16] tensor into dst[rows][16].
+template <typename T>
+__device__ __forceinline__ void stage_bc(T* dst, const T* src, int b, int t_first, int rows,
+                                         int T_, int tid) {
+  constexpr int CPR = NS * sizeof(T) / 16;
+  const int n = rows * CPR;
+  for (int i = tid; i < n; i += G) {
+    const int r = i / CPR, cc = i - r * CPR;
+    const int t = t_first + r;
+    const bool ok = (t >= 0) && (t < T_);
+    const T* g = ok ? src + ((size_t)b * T_ + t) * NS + cc * (16 / sizeof(T)) : src;
+    cp_async16(dst + r * NS + cc * (16 / sizeof(T)), g, ok);
+  }
+}
+
+// Sum of v[lane'] over all lanes lane' of the warp, for value index = lane:
+// a butterfly reduce-scatter (31 shuffles).
+__device__ __forceinline__ float warp_reduce_scatter32(float (&v)[32], int lane) {
+#pragma unroll
+  for (int half = 16; half >= 1; half >>= 1) {
+    const bool up = (lane & half) != 0;
+#pragma unroll
+    for (int i = 0; i < half; ++i) {
+      const float send = up ? v[i] : v[i + half];
+      const float keep = up ? v[i + half] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, half);
+    }
+  }
+  return v[0];
+}
+
+// ---------------------------------------------------------------------------
+// geometry and kernel arguments
+// ---------------------------------------------------------------------------
+
+struct Geo {
+  int B, T, D, K, nc, S, m;  // S segments of m chunks (the last may be short)
+};
+
+__host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+struct FwdArgs {
+  Geo g;
+  const void *x, *dr, *z, *Bm, *Cm;
+  const float *conv_w, *conv_b, *dt_bias, *a_log, *Dp;
+  void *gated, *y_dbg;
+  float* ckpt;
+  float *agg_h, *agg_s;
+};
+
+struct BwdArgs {
+  Geo g;
+  const void *x, *dr, *z, *Bm, *Cm, *dg;
+  const float *conv_w, *conv_b, *dt_bias, *a_log, *Dp, *ckpt;
+  void *dx, *ddr, *dz, *du_dbg;
+  float *dB, *dC;
+  float *q, *sd, *gin, *dxpart, *dchead, *partials;
+  float *d_conv_w, *d_conv_b, *d_dt_bias, *d_a_log, *dD;
+  int accumulate;
+};
+
+// Forward shared memory: two tile buffers {x, delta_raw, z: [K][G] act;
+// B, C: [K][16] act} and the current chunk's B, C as float [K][16].
+struct FwdSmem {
+  size_t x, dr, z, Bt, Ct, tile, fB, fC, total;
+};
+__host__ __device__ inline FwdSmem fwd_smem(int K, int es) {
+  FwdSmem s;
+  s.x = 0;
+  s.dr = s.x + align_up((size_t)K * G * es, 128);
+  s.z = s.dr + align_up((size_t)K * G * es, 128);
+  s.Bt = s.z + align_up((size_t)K * G * es, 128);
+  s.Ct = s.Bt + align_up((size_t)K * NS * es, 128);
+  s.tile = s.Ct + align_up((size_t)K * NS * es, 128);
+  s.fB = 2 * s.tile;
+  s.fC = s.fB + align_up((size_t)K * NS * 4, 128);
+  s.total = s.fC + align_up((size_t)K * NS * 4, 128);
+  return s;
+}
+
+// Backward shared memory: two tile buffers {x: [K+3][G] (three halo rows
+// before the chunk), delta_raw, z, d_gated: [K][G]; B, C: [K][16]}, float B
+// and C of the current chunk, the recomputed states hist[K][G][16] f32, the
+// per-step scalars (u, delta, conv pre-activation, y) [K][G] float4, and the
+// per-warp dB/dC sums red[K][NW][32].
+struct BwdSmem {
+  size_t x, dr, z, dg, Bt, Ct, tile, fB, fC, hist, scal, red, total;
+};
+__host__ __device__ inline BwdSmem bwd_smem(int K, int es) {
+  BwdSmem s;
+  s.x = 0;
+  s.dr = s.x + align_up((size_t)(K + 3) * G * es, 128);
+  s.z = s.dr + align_up((size_t)K * G * es, 128);
+  s.dg = s.z + align_up((size_t)K * G * es, 128);
+  s.Bt = s.dg + align_up((size_t)K * G * es, 128);
+  s.Ct = s.Bt + align_up((size_t)K * NS * es, 128);
+  s.tile = s.Ct + align_up((size_t)K * NS * es, 128);
+  s.fB = 2 * s.tile;
+  s.fC = s.fB + align_up((size_t)K * NS * 4, 128);
+  s.hist = s.fC + align_up((size_t)K * NS * 4, 128);
+  s.scal = s.hist + (size_t)K * G * NS * 4;
+  s.red = s.scal + (size_t)K * G * 16;
+  s.total = s.red + (size_t)K * NW * 32 * 4;
+  return s;
+}
+
+// Backward aggregate shared memory: two buffers {delta_raw, z, d_gated:
+// [K][G]; C: [K][16]} and float C.
+struct AggSmem {
+  size_t dr, z, dg, Ct, tile, fC, total;
+};
+__host__ __device__ inline AggSmem agg_smem(int K, int es) {
+  AggSmem s;
+  s.dr = 0;
+  s.z = s.dr + align_up((size_t)K * G * es, 128);
+  s.dg = s.z + align_up((size_t)K * G * es, 128);
+  s.Ct = s.dg + align_up((size_t)K * G * es, 128);
+  s.tile = s.Ct + align_up((size_t)K * NS * es, 128);
+  s.fC = 2 * s.tile;
+  s.total = s.fC + align_up((size_t)K * NS * 4, 128);
+  return s;
+}
+
+// Per-channel parameters: A2 = A * log2(e) with A = -exp(a_log).
+struct ChanParams {
+  float A2[NS];
+  float w[WC];
+  float cb, dtb, Dd;
+};
+__device__ __forceinline__ void load_params(ChanParams& p, const float* conv_w, const float* conv_b,
+                                            const float* dt_bias, const float* a_log,
+                                            const float* Dp, int d, bool active) {
+#pragma unroll
+  for (int n = 0; n < NS; ++n) p.A2[n] = active ? -expf(a_log[(size_t)d * NS + n]) * LOG2E : 0.0f;
+#pragma unroll
+  for (int k = 0; k < WC; ++k) p.w[k] = active ? conv_w[(size_t)d * WC + k] : 0.0f;
+  p.cb = active ? conv_b[d] : 0.0f;
+  p.dtb = active ? dt_bias[d] : 0.0f;
+  p.Dd = active ? Dp[d] : 0.0f;
+}
+
+// ---------------------------------------------------------------------------
+// forward: FINAL = rerun from the true segment start, write gated (+y) and
+// the chunk checkpoints; !FINAL = local pass from zero over segments
+// 0..S-2 writing only the end state and the summed step size.
+// ---------------------------------------------------------------------------
+
+template <typename T, bool FINAL>
+__global__ void __launch_bounds__(G) m3_fwd_kernel(FwdArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const Geo g = a.g;
+  const int tid = threadIdx.x;
+  const int d0 = blockIdx.x * G;
+  const int s = blockIdx.y;
+  const int b = blockIdx.z;
+  const int d = d0 + tid;
+  const bool active = d < g.D;
+  const int c_begin = s * g.m;
+  const int c_end = min(c_begin + g.m, g.nc);
+  const int t_begin = c_begin * g.K;
+  const int K = g.K;
+  const FwdSmem L = fwd_smem(K, sizeof(T));
+  const T* xg = static_cast<const T*>(a.x);
+  const T* drg = static_cast<const T*>(a.dr);
+  const T* zg = static_cast<const T*>(a.z);
+  const T* Bg = static_cast<const T*>(a.Bm);
+  const T* Cg = static_cast<const T*>(a.Cm);
+  float* fB = reinterpret_cast<float*>(smem + L.fB);
+  float* fC = reinterpret_cast<float*>(smem + L.fC);
+
+  ChanParams P;
+  load_params(P, a.conv_w, a.conv_b, a.dt_bias, a.a_log, a.Dp, d, active);
+
+  float h[NS];
+#pragma unroll
+  for (int n = 0; n < NS; ++n)
+    h[n] = (FINAL && s > 0 && active)
+               ? a.ckpt[(((size_t)b * g.nc + c_begin) * NS + n) * g.D + d]
+               : 0.0f;
+
+  // conv window x[t-3], x[t-2], x[t-1]
+  float xm3 = 0.f, xm2 = 0.f, xm1 = 0.f;
+  if (active) {
+    if (t_begin >= 3) xm3 = Act<T>::ld(xg + ((size_t)b * g.T + t_begin - 3) * g.D + d);
+    if (t_begin >= 2) xm2 = Act<T>::ld(xg + ((size_t)b * g.T + t_begin - 2) * g.D + d);
+    if (t_begin >= 1) xm1 = Act<T>::ld(xg + ((size_t)b * g.T + t_begin - 1) * g.D + d);
+  }
+  float sdelta = 0.f;
+
+  auto stage = [&](int c, int buf) {
+    unsigned char* base = smem + (size_t)buf * L.tile;
+    const int t0 = c * K;
+    stage_act<T>(reinterpret_cast<T*>(base + L.x), xg, b, t0, K, g.T, g.D, d0, tid);
+    stage_act<T>(reinterpret_cast<T*>(base + L.dr), drg, b, t0, K, g.T, g.D, d0, tid);
+    stage_bc<T>(reinterpret_cast<T*>(base + L.Bt), Bg, b, t0, K, g.T, tid);
+    if (FINAL) {
+      stage_act<T>(reinterpret_cast<T*>(base + L.z), zg, b, t0, K, g.T, g.D, d0, tid);
+      stage_bc<T>(reinterpret_cast<T*>(base + L.Ct), Cg, b, t0, K, g.T, tid);
+    }
+    cp_async_commit();
+  };
+
+  stage(c_begin, 0);
+  for (int c = c_begin; c < c_end; ++c) {
+    const int buf = (c - c_begin) & 1;
+    if (c + 1 < c_end) {
+      stage(c + 1, buf ^ 1);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();
+    const unsigned char* base = smem + (size_t)buf * L.tile;
+    const T* Bt = reinterpret_cast<const T*>(base + L.Bt);
+    const T* Ct = reinterpret_cast<const T*>(base + L.Ct);
+    for (int i = tid; i < K * NS; i += G) {
+      fB[i] = Act<T>::ld(Bt + i);
+      if (FINAL) fC[i] = Act<T>::ld(Ct + i);
+    }
+    __syncthreads();
+
+    if (FINAL && active && (c > c_begin || s == 0)) {
+#pragma unroll
+      for (int n = 0; n < NS; ++n) a.ckpt[(((size_t)b * g.nc + c) * NS + n) * g.D + d] = h[n];
+    }
+    const T* xt = reinterpret_cast<const T*>(base + L.x);
+    const T* drt = reinterpret_cast<const T*>(base + L.dr);
+    const T* zt = reinterpret_cast<const T*>(base + L.z);
+    const int steps = min(K, g.T - c * K);
+    for (int j = 0; j < steps; ++j) {
+      const float xv = Act<T>::ld(xt + j * G + tid);
+      const float cpre = fmaf(P.w[0], xm3, fmaf(P.w[1], xm2, fmaf(P.w[2], xm1, fmaf(P.w[3], xv, P.cb))));
+      xm3 = xm2;
+      xm2 = xm1;
+      xm1 = xv;
+      const float u = cpre * sigmoid_f(cpre);
+      const float delta = softplus_f(Act<T>::ld(drt + j * G + tid) + P.dtb);
+      const float du = delta * u;
+      const float4* B4 = reinterpret_cast<const float4*>(fB + j * NS);
+      float Bv[NS];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float4 v = B4[q];
+        Bv[4 * q] = v.x; Bv[4 * q + 1] = v.y; Bv[4 * q + 2] = v.z; Bv[4 * q + 3] = v.w;
+      }
+#pragma unroll
+      for (int n = 0; n < NS; ++n) h[n] = fmaf(ex2(delta * P.A2[n]), h[n], du * Bv[n]);
+      if (FINAL) {
+        const float4* C4 = reinterpret_cast<const float4*>(fC + j * NS);
+        float y0 = 0.f, y1 = 0.f, y2 = 0.f, y3 = 0.f;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float4 v = C4[q];
+          y0 = fmaf(v.x, h[4 * q], y0);
+          y1 = fmaf(v.y, h[4 * q + 1], y1);
+          y2 = fmaf(v.z, h[4 * q + 2], y2);
+          y3 = fmaf(v.w, h[4 * q + 3], y3);
+        }
+        const float y = fmaf(P.Dd, u, (y0 + y1) + (y2 + y3));
+        const float zv = Act<T>::ld(zt + j * G + tid);
+        if (active) {
+          const size_t i = ((size_t)b * g.T + c * K + j) * g.D + d;
+          Act<T>::st(static_cast<T*>(a.gated) + i, y * zv * sigmoid_f(zv));
+          if (a.y_dbg) Act<T>::st(static_cast<T*>(a.y_dbg) + i, y);
+        }
+      } else {
+        sdelta += delta;
+      }
+    }
+    __syncthreads();
+  }
+  if (!FINAL && active) {
+#pragma unroll
+    for (int n = 0; n < NS; ++n) a.agg_h[(((size_t)b * g.S + s) * NS + n) * g.D + d] = h[n];
+    a.agg_s[((size_t)b * g.S + s) * g.D + d] = sdelta;
+  }
+}
+
+// Chain the forward segments: start(0) = 0, start(s+1) = decay(s) * start(s)
+// + local_end(s), with decay(s) = exp(A * sum of delta over segment s).
+// Writes each segment's start state into the checkpoint of its first chunk.
+__global__ void m3_fwd_carry_kernel(FwdArgs a) {
+  const Geo g = a.g;
+  const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const size_t total = (size_t)g.B * NS * g.D;
+  if (idx >= total) return;
+  const int d = (int)(idx % g.D);
+  const int n = (int)((idx / g.D) % NS);
+  const int b = (int)(idx / ((size_t)g.D * NS));
+  const float A2 = -expf(a.a_log[(size_t)d * NS + n]) * LOG2E;
+  float h = 0.f;
+  for (int s = 0; s < g.S; ++s) {
+    a.ckpt[(((size_t)b * g.nc + (size_t)s * g.m) * NS + n) * g.D + d] = h;
+    if (s + 1 < g.S) {
+      const size_t bs = (size_t)b * g.S + s;
+      h = fmaf(ex2(A2 * a.agg_s[bs * g.D + d]), h, a.agg_h[(bs * NS + n) * g.D + d]);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// backward aggregate (segments 1..S-1): the adjoint carry a segment passes to
+// its predecessor when nothing enters it from the right,
+//   carry_t = exp(delta_t A) * (dy_t C_t + carry_{t+1}),
+// and the summed step size (the segment's total decay).
+// ---------------------------------------------------------------------------
+
+template <typename T>
+__global__ void __launch_bounds__(G) m3_bwd_agg_kernel(BwdArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const Geo g = a.g;
+  const int tid = threadIdx.x;
+  const int d0 = blockIdx.x * G;
+  const int s = blockIdx.y + 1;
+  const int b = blockIdx.z;
+  const int d = d0 + tid;
+  const bool active = d < g.D;
+  const int c_begin = s * g.m;
+  const int c_end = min(c_begin + g.m, g.nc);
+  const int K = g.K;
+  const AggSmem L = agg_smem(K, sizeof(T));
+  float* fC = reinterpret_cast<float*>(smem + L.fC);
+
+  float A2[NS];
+#pragma unroll
+  for (int n = 0; n < NS; ++n) A2[n] = active ? -expf(a.a_log[(size_t)d * NS + n]) * LOG2E : 0.f;
+  const float dtb = active ? a.dt_bias[d] : 0.f;
+  float carry[NS];
+#pragma unroll
+  for (int n = 0; n < NS; ++n) carry[n] = 0.f;
+  float sdelta = 0.f;
+
+  auto stage = [&](int c, int buf) {
+    unsigned char* base = smem + (size_t)buf * L.tile;
+    const int t0 = c * K;
+    stage_act<T>(reinterpret_cast<T*>(base + L.dr), static_cast<const T*>(a.dr), b, t0, K, g.T, g.D, d0, tid);
+    stage_act<T>(reinterpret_cast<T*>(base + L.z), static_cast<const T*>(a.z), b, t0, K, g.T, g.D, d0, tid);
+    stage_act<T>(reinterpret_cast<T*>(base + L.dg), static_cast<const T*>(a.dg), b, t0, K, g.T, g.D, d0, tid);
+    stage_bc<T>(reinterpret_cast<T*>(base + L.Ct), static_cast<const T*>(a.Cm), b, t0, K, g.T, tid);
+    cp_async_commit();
+  };
+
+  stage(c_end - 1, 0);
+  for (int c = c_end - 1; c >= c_begin; --c) {
+    const int buf = (c_end - 1 - c) & 1;
+    if (c - 1 >= c_begin) {
+      stage(c - 1, buf ^ 1);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();
+    const unsigned char* base = smem + (size_t)buf * L.tile;
+    const T* Ct = reinterpret_cast<const T*>(base + L.Ct);
+    for (int i = tid; i < K * NS; i += G) fC[i] = Act<T>::ld(Ct + i);
+    __syncthreads();
+    const T* drt = reinterpret_cast<const T*>(base + L.dr);
+    const T* zt = reinterpret_cast<const T*>(base + L.z);
+    const T* dgt = reinterpret_cast<const T*>(base + L.dg);
+    const int steps = min(K, g.T - c * K);
+    for (int j = steps - 1; j >= 0; --j) {
+      const float zv = Act<T>::ld(zt + j * G + tid);
+      const float dy = Act<T>::ld(dgt + j * G + tid) * zv * sigmoid_f(zv);
+      const float delta = softplus_f(Act<T>::ld(drt + j * G + tid) + dtb);
+      sdelta += delta;
+      const float4* C4 = reinterpret_cast<const float4*>(fC + j * NS);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float4 v = C4[q];
+        carry[4 * q + 0] = ex2(delta * A2[4 * q + 0]) * fmaf(dy, v.x, carry[4 * q + 0]);
+        carry[4 * q + 1] = ex2(delta * A2[4 * q + 1]) * fmaf(dy, v.y, carry[4 * q + 1]);
+        carry[4 * q + 2] = ex2(delta * A2[4 * q + 2]) * fmaf(dy, v.z, carry[4 * q + 2]);
+        carry[4 * q + 3] = ex2(delta * A2[4 * q + 3]) * fmaf(dy, v.w, carry[4 * q + 3]);
+      }
+    }
+    __syncthreads();
+  }
+  if (active) {
+    const size_t bs = (size_t)b * g.S + s;
+#pragma unroll
+    for (int n = 0; n < NS; ++n) a.q[(bs * NS + n) * g.D + d] = carry[n];
+    a.sd[bs * g.D + d] = sdelta;
+  }
+}
+
+// Chain the backward segments right to left: in(S-1) = 0,
+// in(s-1) = decay(s) * in(s) + local(s).
+__global__ void m3_bwd_carry_kernel(BwdArgs a) {
+  const Geo g = a.g;
+  const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const size_t total = (size_t)g.B * NS * g.D;
+  if (idx >= total) return;
+  const int d = (int)(idx % g.D);
+  const int n = (int)((idx / g.D) % NS);
+  const int b = (int)(idx / ((size_t)g.D * NS));
+  const float A2 = -expf(a.a_log[(size_t)d * NS + n]) * LOG2E;
+  float c = 0.f;
+  for (int s = g.S - 1; s >= 0; --s) {
+    const size_t bs = (size_t)b * g.S + s;
+    a.gin[(bs * NS + n) * g.D + d] = c;
+    if (s >= 1) c = fmaf(ex2(A2 * a.sd[bs * g.D + d]), c, a.q[(bs * NS + n) * g.D + d]);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// backward main kernel
+// ---------------------------------------------------------------------------
+
+template <typename T>
+__global__ void __launch_bounds__(G) m3_bwd_kernel(BwdArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const Geo g = a.g;
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  const int d0 = blockIdx.x * G;
+  const int s = blockIdx.y;
+  const int b = blockIdx.z;
+  const int d = d0 + tid;
+  const bool active = d < g.D;
+  const int c_begin = s * g.m;
+  const int c_end = min(c_begin + g.m, g.nc);
+  const int t_begin = c_begin * g.K;
+  const int t_end = min(c_end * g.K, g.T);
+  const int K = g.K;
+  const BwdSmem L = bwd_smem(K, sizeof(T));
+  float* fB = reinterpret_cast<float*>(smem + L.fB);
+  float* fC = reinterpret_cast<float*>(smem + L.fC);
+  float4* hist = reinterpret_cast<float4*>(smem + L.hist);
+  float4* scal = reinterpret_cast<float4*>(smem + L.scal);
+  float* red = reinterpret_cast<float*>(smem + L.red);
+  const int swz = (tid >> 1) & 3;  // conflict-free float4 stores of 64-byte rows
+
+  ChanParams P;
+  load_params(P, a.conv_w, a.conv_b, a.dt_bias, a.a_log, a.Dp, d, active);
+
+  // adjoint carry entering the segment's last step from the right:
+  // exp(delta_{t+1} A) * dh_{t+1}
+  float carry[NS];
+#pragma unroll
+  for (int n = 0; n < NS; ++n)
+    carry[n] = (g.S > 1 && active) ? a.gin[(((size_t)b * g.S + s) * NS + n) * g.D + d] : 0.f;
+
+  float dAp[NS];  // dL/dA per lane
+#pragma unroll
+  for (int n = 0; n < NS; ++n) dAp[n] = 0.f;
+  float dD_acc = 0.f, ddtb_acc = 0.f, dcb_acc = 0.f;
+  float dcw[WC] = {0.f, 0.f, 0.f, 0.f};
+  float dc1 = 0.f, dc2 = 0.f, dc3 = 0.f;  // dc at t+1, t+2, t+3
+
+  const T* xg = static_cast<const T*>(a.x);
+  auto stage = [&](int c, int buf) {
+    unsigned char* base = smem + (size_t)buf * L.tile;
+    const int t0 = c * K;
+    stage_act<T>(reinterpret_cast<T*>(base + L.x), xg, b, t0 - 3, K + 3, g.T, g.D, d0, tid);
+    stage_act<T>(reinterpret_cast<T*>(base + L.dr), static_cast<const T*>(a.dr), b, t0, K, g.T, g.D, d0, tid);
+    stage_act<T>(reinterpret_cast<T*>(base + L.z), static_cast<const T*>(a.z), b, t0, K, g.T, g.D, d0, tid);
+    stage_act<T>(reinterpret_cast<T*>(base + L.dg), static_cast<const T*>(a.dg), b, t0, K, g.T, g.D, d0, tid);
+    stage_bc<T>(reinterpret_cast<T*>(base + L.Bt), static_cast<const T*>(a.Bm), b, t0, K, g.T, tid);
+    stage_bc<T>(reinterpret_cast<T*>(base + L.Ct), static_cast<const T*>(a.Cm), b, t0, K, g.T, tid);
+    cp_async_commit();
+  };
+
+  stage(c_end - 1, 0);
+  for (int c = c_end - 1; c >= c_begin; --c) {
+    const int buf = (c_end - 1 - c) & 1;
+    if (c - 1 >= c_begin) {
+      stage(c - 1, buf ^ 1);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();
+    const unsigned char* base = smem + (size_t)buf * L.tile;
+    {
+      const T* Bt = reinterpret_cast<const T*>(base + L.Bt);
+      const T* Ct = reinterpret_cast<const T*>(base + L.Ct);
+      for (int i = tid; i < K * NS; i += G) {
+        fB[i] = Act<T>::ld(Bt + i);
+        fC[i] = Act<T>::ld(Ct + i);
+      }
+    }
+    __syncthreads();
+    const T* xt = reinterpret_cast<const T*>(base + L.x);  // row r is step c*K - 3 + r
+    const T* drt = reinterpret_cast<const T*>(base + L.dr);
+    const T* zt = reinterpret_cast<const T*>(base + L.z);
+    const T* dgt = reinterpret_cast<const T*>(base + L.dg);
+    const int steps = min(K, g.T - c * K);
+
+    // ---- recompute the chunk forward from its checkpoint ----
+    {
+      float h[NS];
+#pragma unroll
+      for (int n = 0; n < NS; ++n)
+        h[n] = active ? a.ckpt[(((size_t)b * g.nc + c) * NS + n) * g.D + d] : 0.f;
+      float xm3 = Act<T>::ld(xt + 0 * G + tid);
+      float xm2 = Act<T>::ld(xt + 1 * G + tid);
+      float xm1 = Act<T>::ld(xt + 2 * G + tid);
+      for (int j = 0; j < steps; ++j) {
+        const float xv = Act<T>::ld(xt + (j + 3) * G + tid);
+        const float cpre = fmaf(P.w[0], xm3, fmaf(P.w[1], xm2, fmaf(P.w[2], xm1, fmaf(P.w[3], xv, P.cb))));
+        xm3 = xm2;
+        xm2 = xm1;
+        xm1 = xv;
+        const float u = cpre * sigmoid_f(cpre);
+        const float delta = softplus_f(Act<T>::ld(drt + j * G + tid) + P.dtb);
+        const float du = delta * u;
+        const float4* B4 = reinterpret_cast<const float4*>(fB + j * NS);
+        const float4* C4 = reinterpret_cast<const float4*>(fC + j * NS);
+        float y0 = 0.f, y1 = 0.f, y2 = 0.f, y3 = 0.f;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float4 bv = B4[q];
+          const float4 cv = C4[q];
+          h[4 * q + 0] = fmaf(ex2(delta * P.A2[4 * q + 0]), h[4 * q + 0], du * bv.x);
+          h[4 * q + 1] = fmaf(ex2(delta * P.A2[4 * q + 1]), h[4 * q + 1], du * bv.y);
+          h[4 * q + 2] = fmaf(ex2(delta * P.A2[4 * q + 2]), h[4 * q + 2], du * bv.z);
+          h[4 * q + 3] = fmaf(ex2(delta * P.A2[4 * q + 3]), h[4 * q + 3], du * bv.w);
+          y0 = fmaf(cv.x, h[4 * q + 0], y0);
+          y1 = fmaf(cv.y, h[4 * q + 1], y1);
+          y2 = fmaf(cv.z, h[4 * q + 2], y2);
+          y3 = fmaf(cv.w, h[4 * q + 3], y3);
+          hist[(j * G + tid) * 4 + (q ^ swz)] =
+              make_float4(h[4 * q + 0], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
+        }
+        const float y = fmaf(P.Dd, u, (y0 + y1) + (y2 + y3));
+        scal[j * G + tid] = make_float4(u, delta, cpre, y);
+      }
+    }
+
+    // ---- reverse-time pass over the chunk ----
+    for (int j = steps - 1; j >= 0; --j) {
+      const int t = c * K + j;
+      const float4 sc = scal[j * G + tid];
+      const float u = sc.x, delta = sc.y, cpre = sc.z, y = sc.w;
+      const float gv = Act<T>::ld(dgt + j * G + tid);
+      const float zv = Act<T>::ld(zt + j * G + tid);
+      const float drv = Act<T>::ld(drt + j * G + tid);
+      const float szv = sigmoid_f(zv);
+      const float dy = gv * zv * szv;
+      const float dzv = gv * y * (szv + zv * szv * (1.f - szv));
+      const float du_ = delta * u;
+      float sumB = 0.f, sumAq = 0.f;
+      float pv[32];
+      const float4* B4 = reinterpret_cast<const float4*>(fB + j * NS);
+      const float4* C4 = reinterpret_cast<const float4*>(fC + j * NS);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float4 hv4 = hist[(j * G + tid) * 4 + (q ^ swz)];
+        const float4 bv4 = B4[q];
+        const float4 cv4 = C4[q];
+        const float hv[4] = {hv4.x, hv4.y, hv4.z, hv4.w};
+        const float bv[4] = {bv4.x, bv4.y, bv4.z, bv4.w};
+        const float cv[4] = {cv4.x, cv4.y, cv4.z, cv4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int n = 4 * q + e;
+          const float dh = fmaf(dy, cv[e], carry[n]);   // dL/dh_t
+          pv[16 + n] = dy * hv[e];                      // dC partial
+          pv[n] = dh * du_;                             // dB partial
+          const float r = fmaf(-du_, bv[e], hv[e]);     // exp(delta A) h_{t-1}
+          sumB = fmaf(dh, bv[e], sumB);
+          const float qn = dh * r;
+          dAp[n] = fmaf(delta, qn, dAp[n]);
+          sumAq = fmaf(P.A2[n], qn, sumAq);
+          carry[n] = ex2(delta * P.A2[n]) * dh;
+        }
+      }
+      const float du = fmaf(dy, P.Dd, delta * sumB);
+      const float ddelta = fmaf(u, sumB, LN2 * sumAq);
+      dD_acc = fmaf(dy, u, dD_acc);
+      const float ddr = ddelta * sigmoid_f(drv + P.dtb);
+      ddtb_acc += ddr;
+      const float scp = sigmoid_f(cpre);
+      const float dc = du * (scp + cpre * scp * (1.f - scp));
+      dcb_acc += dc;
+#pragma unroll
+      for (int k = 0; k < WC; ++k) dcw[k] = fmaf(dc, Act<T>::ld(xt + (j + k) * G + tid), dcw[k]);
+      const float dxv = fmaf(dc, P.w[3], fmaf(dc1, P.w[2], fmaf(dc2, P.w[1], dc3 * P.w[0])));
+      dc3 = dc2;
+      dc2 = dc1;
+      dc1 = dc;
+      if (active) {
+        const size_t i = ((size_t)b * g.T + t) * g.D + d;
+        Act<T>::st(static_cast<T*>(a.ddr) + i, ddr);
+        Act<T>::st(static_cast<T*>(a.dz) + i, dzv);
+        if (a.du_dbg) Act<T>::st(static_cast<T*>(a.du_dbg) + i, du);
+        if (s + 1 < g.S && t >= t_end - 3)
+          a.dxpart[(((size_t)b * g.S + s) * 3 + (t - (t_end - 3))) * g.D + d] = dxv;
+        else
+          Act<T>::st(static_cast<T*>(a.dx) + i, dxv);
+        if (s > 0 && t < t_begin + 3)
+          a.dchead[(((size_t)b * g.S + s) * 3 + (t - t_begin)) * g.D + d] = dc;
+      } else {
+#pragma unroll
+        for (int n = 0; n < 32; ++n) pv[n] = 0.f;
+      }
+      red[(j * NW + warp) * 32 + lane] = warp_reduce_scatter32(pv, lane);
+    }
+    __syncthreads();
+    // one global reduction per (t, n) per block for dB and dC
+    for (int i = tid; i < steps * 32; i += G) {
+      const int j = i >> 5, l = i & 31;
+      float v = 0.f;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) v += red[(j * NW + w) * 32 + l];
+      float* dst = (l < NS ? a.dB : a.dC) + ((size_t)b * g.T + c * K + j) * NS + (l & (NS - 1));
+      atomicAdd(dst, v);
+    }
+    __syncthreads();
+  }
+
+  if (active) {
+    float* Pp = a.partials + ((size_t)b * g.S + s) * NPART * g.D;
+#pragma unroll
+    for (int n = 0; n < NS; ++n) Pp[(size_t)n * g.D + d] = dAp[n];
+    Pp[(size_t)16 * g.D + d] = dD_acc;
+    Pp[(size_t)17 * g.D + d] = ddtb_acc;
+    Pp[(size_t)18 * g.D + d] = dcb_acc;
+#pragma unroll
+    for (int k = 0; k < WC; ++k) Pp[(size_t)(19 + k) * g.D + d] = dcw[k];
+  }
+}
+
+// d_x at the last three steps of segment s needs dc from the first three
+// steps of segment s+1: complete and store them.
+template <typename T>
+__global__ void m3_bwd_fixup_kernel(BwdArgs a) {
+  const Geo g = a.g;
+  const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const size_t total = (size_t)g.B * (g.S - 1) * 3 * g.D;
+  if (idx >= total) return;
+  const int d = (int)(idx % g.D);
+  size_t rest = idx / g.D;
+  const int j = (int)(rest % 3);
+  rest /= 3;
+  const int s = (int)(rest % (g.S - 1));
+  const int b = (int)(rest / (g.S - 1));
+  const int t_end = min((s + 1) * g.m * g.K, g.T);
+  const int t = t_end - 3 + j;
+  float v = a.dxpart[(((size_t)b * g.S + s) * 3 + j) * g.D + d];
+  for (int k = 0; k < WC; ++k) {
+    const int tp = t + 3 - k;
+    if (tp >= t_end && tp < g.T)
+      v = fmaf(a.dchead[(((size_t)b * g.S + s + 1) * 3 + (tp - t_end)) * g.D + d],
+               a.conv_w[(size_t)d * WC + k], v);
+  }
+  Act<T>::st(static_cast<T*>(a.dx) + ((size_t)b * g.T + t) * g.D + d, v);
+}
+
+// Sum the per-(batch, segment) parameter partials in a fixed order.
+__global__ void m3_bwd_finalize_kernel(BwdArgs a, int rows) {
+  const Geo g = a.g;
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= 23 * g.D) return;
+  const int jj = idx / g.D, d = idx - jj * g.D;
+  float v = 0.f;
+  for (int r = 0; r < rows; ++r) v += a.partials[((size_t)r * NPART + jj) * g.D + d];
+  float* dst;
+  if (jj < NS) {
+    v *= -expf(a.a_log[(size_t)d * NS + jj]);  // dL/da_log = dL/dA * A
+    dst = a.d_a_log + (size_t)d * NS + jj;
+  } else if (jj == 16) {
+    dst = a.dD + d;
+  } else if (jj == 17) {
+    dst = a.d_dt_bias + d;
+  } else if (jj == 18) {
+    dst = a.d_conv_b + d;
+  } else {
+    dst = a.d_conv_w + (size_t)d * WC + (jj - 19);
+  }
+  *dst = a.accumulate ? *dst + v : v;
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+
+constexpr size_t SMEM_CAP = 227 * 1024;  // opt-in shared memory per block
+
+// Largest chunk whose backward footprint fits one block's shared memory.
+__host__ inline int kmax_for(int es) {
+  int k = KMAX;
+  while (k > 1 && bwd_smem(k, es).total > SMEM_CAP) --k;
+  return k;
+}
+
+struct DevInfo {
+  bool attrs = false;
+  int sms = 0;
+  int occ_fwd[2][KMAX + 1];  // [dtype][chunk] blocks per SM, 0 = not yet queried
+  int occ_bwd[2][KMAX + 1];
+};
+
+std::mutex g_mu;
+DevInfo g_dev[64];
+
+template <typename T>
+cudaError_t set_attrs() {
+  const int es = sizeof(T);
+  cudaError_t e;
+  e = cudaFuncSetAttribute(m3_fwd_kernel<T, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)fwd_smem(KMAX, es).total);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(m3_fwd_kernel<T, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)fwd_smem(KMAX, es).total);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(m3_bwd_agg_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)agg_smem(KMAX, es).total);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(m3_bwd_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)bwd_smem(kmax_for(es), es).total);
+}
+
+// Device facts for the current device: kernel attributes are set once per
+// device (with that device current), occupancy is queried once per chunk.
+cudaError_t device_info(int chunk, int ai, int* sms, int* occ_f, int* occ_b) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DevInfo& di = g_dev[dev];
+  if (!di.attrs) {
+    e = set_attrs<float>();
+    if (e != cudaSuccess) return e;
+    e = set_attrs<__nv_bfloat16>();
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    for (int a = 0; a < 2; ++a)
+      for (int k = 0; k <= KMAX; ++k) di.occ_fwd[a][k] = di.occ_bwd[a][k] = 0;
+    di.attrs = true;
+  }
+  if (occ_f && di.occ_fwd[ai][chunk] == 0) {
+    int of = 0, ob = 0;
+    if (ai == 1) {
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&of, m3_fwd_kernel<__nv_bfloat16, true>, G,
+                                                        fwd_smem(chunk, 2).total);
+      if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ob, m3_bwd_kernel<__nv_bfloat16>, G,
+                                                          bwd_smem(chunk, 2).total);
+    } else {
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&of, m3_fwd_kernel<float, true>, G,
+                                                        fwd_smem(chunk, 4).total);
+      if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ob, m3_bwd_kernel<float>, G,
+                                                          bwd_smem(chunk, 4).total);
+    }
+    if (e != cudaSuccess) return e;
+    di.occ_fwd[ai][chunk] = of > 0 ? of : 1;
+    di.occ_bwd[ai][chunk] = ob > 0 ? ob : 1;
+  }
+  if (sms) *sms = di.sms;
+  if (occ_f) *occ_f = di.occ_fwd[ai][chunk];
+  if (occ_b) *occ_b = di.occ_bwd[ai][chunk];
+  return cudaSuccess;
+}
+
+struct Plan {
+  int B, T, D, K, nc;
+  int Sf, mf, Sb, mb;
+  size_t ckpt_bytes, ws_bytes;
+  // workspace offsets (bytes)
+  size_t f_aggh, f_aggs;
+  size_t b_part, b_q, b_sd, b_gin, b_dxpart, b_dchead;
+  int fwd_launches, bwd_launches;
+};
+
+// Segments of whole chunks; every segment but the last spans >= 4 steps so
+// that the conv's three-step reach crosses at most one segment boundary.
+void fix_segments(int nc, int K, int want, int* S, int* m) {
+  int m_min = (4 + K - 1) / K;
+  if (want < 1) want = 1;
+  int mm = (nc + want - 1) / want;
+  if (mm < m_min) mm = m_min;
+  if (mm < 1) mm = 1;
+  int ss = (nc + mm - 1) / mm;
+  if (ss < 1) ss = 1;
+  if (ss > 65535) {
+    ss = 65535;
+    mm = (nc + ss - 1) / ss;
+    ss = (nc + mm - 1) / mm;
+  }
+  *S = ss;
+  *m = mm;
+}
+
+m3_status validate_dims(const m3_dims* dm, m3_dtype act) {
+  if (!dm) return M3_ERR_NULL;
+  if (act != M3_F32 && act != M3_BF16) return M3_ERR_UNSUPPORTED;
+  if (dm->batch < 0 || dm->seq_len < 0 || dm->d_inner < 0 || dm->chunk < 0 || dm->segments < 0)
+    return M3_ERR_DIMS;
+  if (dm->d_state != NS || dm->d_conv != WC) return M3_ERR_UNSUPPORTED;
+  if (dm->d_inner % 8 != 0) return M3_ERR_UNSUPPORTED;
+  if (dm->chunk > KMAX) return M3_ERR_DIMS;
+  if (dm->chunk > kmax_for(act == M3_BF16 ? 2 : 4)) return M3_ERR_UNSUPPORTED;
+  if (dm->batch > 65535 || dm->seq_len > (int64_t)1 << 30 || dm->d_inner > (int64_t)1 << 24)
+    return M3_ERR_DIMS;
+  if (dm->segments > 65535) return M3_ERR_DIMS;
+  if (dm->batch * dm->d_inner > ((int64_t)1 << 27)) return M3_ERR_DIMS;  // 1-D grids of the carry passes
+  return M3_OK;
+}
+
+m3_status make_plan(const m3_dims* dm, m3_dtype act, Plan* p) {
+  m3_status st = validate_dims(dm, act);
+  if (st != M3_OK) return st;
+  p->B = (int)dm->batch;
+  p->T = (int)dm->seq_len;
+  p->D = (int)dm->d_inner;
+  p->K = dm->chunk ? (int)dm->chunk : KDEF;
+  p->nc = (p->T + p->K - 1) / p->K;
+  const int groups = (p->D + G - 1) / G;
+  int want_f = 1, want_b = 1;
+  if (dm->segments > 0) {
+    want_f = want_b = (int)dm->segments;
+  } else if ((int64_t)p->B * p->T * p->D > 0) {
+    int sms = 0, of = 0, ob = 0;
+    if (device_info(p->K, act == M3_BF16 ? 1 : 0, &sms, &of, &ob) != cudaSuccess) {
+      cudaGetLastError();
+      return M3_ERR_CUDA;
+    }
+    const int64_t bg = (int64_t)p->B * groups;
+    const int64_t cap_f = (int64_t)sms * of;
+    const int64_t cap_b = (int64_t)sms * ob;
+    want_f = (int)((cap_f + bg - 1) / bg);
+    want_b = (int)((cap_b + bg - 1) / bg);
+  }
+  if (p->nc == 0) {
+    p->Sf = p->Sb = 1;
+    p->mf = p->mb = 0;
+  } else {
+    fix_segments(p->nc, p->K, want_f, &p->Sf, &p->mf);
+    fix_segments(p->nc, p->K, want_b, &p->Sb, &p->mb);
+  }
+  const size_t B = p->B, D = p->D;
+  p->ckpt_bytes = B * p->nc * NS * D * 4;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off = align_up(off + bytes, 256);
+    return o;
+  };
+  // forward section
+  off = 0;
+  p->f_aggh = p->f_aggs = 0;
+  if (p->Sf > 1) {
+    p->f_aggh = take(B * p->Sf * NS * D * 4);
+    p->f_aggs = take(B * p->Sf * D * 4);
+  }
+  size_t fwd_total = off;
+  // backward section (reuses the same bytes)
+  off = 0;
+  p->b_part = take(B * p->Sb * NPART * D * 4);
+  p->b_q = p->b_sd = p->b_gin = p->b_dxpart = p->b_dchead = 0;
+  if (p->Sb > 1) {
+    p->b_q = take(B * p->Sb * NS * D * 4);
+    p->b_sd = take(B * p->Sb * D * 4);
+    p->b_gin = take(B * p->Sb * NS * D * 4);
+    p->b_dxpart = take(B * p->Sb * 3 * D * 4);
+    p->b_dchead = take(B * p->Sb * 3 * D * 4);
+  }
+  size_t bwd_total = off;
+  p->ws_bytes = fwd_total > bwd_total ? fwd_total : bwd_total;
+  if (p->ws_bytes < 256) p->ws_bytes = 256;
+  const bool empty = (size_t)p->B * p->T * p->D == 0;
+  p->fwd_launches = empty ? 0 : (p->Sf > 1 ? 3 : 1);
+  p->bwd_launches = empty ? 0 : (p->Sb > 1 ? 5 : 2);
+  return M3_OK;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+template <typename T>
+m3_status launch_fwd(const Plan& p, FwdArgs a, cudaStream_t st) {
+  const int groups = (p.D + G - 1) / G;
+  const size_t smem = fwd_smem(p.K, sizeof(T)).total;
+  a.g = Geo{p.B, p.T, p.D, p.K, p.nc, p.Sf, p.mf};
+  if (p.Sf > 1) {
+    m3_fwd_kernel<T, false><<<dim3(groups, p.Sf - 1, p.B), G, smem, st>>>(a);
+    const size_t n = (size_t)p.B * NS * p.D;
+    m3_fwd_carry_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(a);
+  }
+  m3_fwd_kernel<T, true><<<dim3(groups, p.Sf, p.B), G, smem, st>>>(a);
+  return cudaGetLastError() == cudaSuccess ? M3_OK : M3_ERR_CUDA;
+}
+
+template <typename T>
+m3_status launch_bwd(const Plan& p, BwdArgs a, cudaStream_t st) {
+  const int groups = (p.D + G - 1) / G;
+  a.g = Geo{p.B, p.T, p.D, p.K, p.nc, p.Sb, p.mb};
+  if (cudaMemsetAsync(a.dB, 0, (size_t)p.B * p.T * NS * 4, st) != cudaSuccess) return M3_ERR_CUDA;
+  if (cudaMemsetAsync(a.dC, 0, (size_t)p.B * p.T * NS * 4, st) != cudaSuccess) return M3_ERR_CUDA;
+  if (p.Sb > 1) {
+    m3_bwd_agg_kernel<T><<<dim3(groups, p.Sb - 1, p.B), G, agg_smem(p.K, sizeof(T)).total, st>>>(a);
+    const size_t n = (size_t)p.B * NS * p.D;
+    m3_bwd_carry_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(a);
+  }
+  m3_bwd_kernel<T><<<dim3(groups, p.Sb, p.B), G, bwd_smem(p.K, sizeof(T)).total, st>>>(a);
+  if (p.Sb > 1) {
+    const size_t n = (size_t)p.B * (p.Sb - 1) * 3 * p.D;
+    m3_bwd_fixup_kernel<T><<<(unsigned)((n + 255) / 256), 256, 0, st>>>(a);
+  }
+  const int nf = 23 * p.D;
+  m3_bwd_finalize_kernel<<<(nf + 255) / 256, 256, 0, st>>>(a, p.B * p.Sb);
+  return cudaGetLastError() == cudaSuccess ? M3_OK : M3_ERR_CUDA;
+}
+
+// The device must have this library's kernels registered: fail early and
+// cleanly when the attribute setup cannot run (no device, wrong arch).
+m3_status ensure_device(int chunk) {
+  if (device_info(chunk, 0, nullptr, nullptr, nullptr) != cudaSuccess) {
+    cudaGetLastError();
+    return M3_ERR_CUDA;
+  }
+  return M3_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* m3scan_status_string(m3_status s) {
+  switch (s) {
+    case M3_OK: return "M3_OK";
+    case M3_ERR_NULL: return "M3_ERR_NULL: a required pointer is NULL";
+    case M3_ERR_DIMS: return "M3_ERR_DIMS: a size is negative or out of range";
+    case M3_ERR_UNSUPPORTED:
+      return "M3_ERR_UNSUPPORTED: needs d_state 16, d_conv 4, d_inner % 8 == 0, dtype f32 or bf16";
+    case M3_ERR_ALIGN: return "M3_ERR_ALIGN: a pointer is not aligned as required";
+    case M3_ERR_WORKSPACE: return "M3_ERR_WORKSPACE: workspace missing or too small";
+    case M3_ERR_CUDA: return "M3_ERR_CUDA: a CUDA call or kernel launch failed";
+  }
+  return "unknown m3_status";
+}
+
+int32_t m3scan_version(void) { return 100; }
+
+m3_status m3scan_plan(const m3_dims* dims, m3_dtype act, m3_plan* out) {
+  if (!out) return M3_ERR_NULL;
+  Plan p;
+  m3_status st = make_plan(dims, act, &p);
+  if (st != M3_OK) return st;
+  out->chunk = p.K;
+  out->n_chunks = p.nc;
+  out->fwd_segments = p.Sf;
+  out->bwd_segments = p.Sb;
+  out->ckpt_bytes = (int64_t)p.ckpt_bytes;
+  out->workspace_bytes = (int64_t)p.ws_bytes;
+  out->fwd_launches = p.fwd_launches;
+  out->bwd_launches = p.bwd_launches;
+  return M3_OK;
+}
+
+m3_status m3scan_fwd(const m3_dims* dims, m3_dtype act, const void* x, const void* delta_raw,
+                     const void* z, const void* Bm, const void* Cm, const float* conv_w,
+                     const float* conv_b, const float* dt_bias, const float* a_log, const float* D,
+                     void* gated, void* y_dbg, float* ckpt, void* workspace, size_t workspace_bytes,
+                     m3_stream_t stream) {
+  Plan p;
+  m3_status st = make_plan(dims, act, &p);
+  if (st != M3_OK) return st;
+  if ((size_t)p.B * p.T * p.D == 0) return M3_OK;
+  if (!x || !delta_raw || !z || !Bm || !Cm || !conv_w || !conv_b || !dt_bias || !a_log || !D ||
+      !gated || !ckpt)
+    return M3_ERR_NULL;
+  const void* act_ptrs[] = {x, delta_raw, z, Bm, Cm, gated, y_dbg};
+  for (const void* q : act_ptrs)
+    if (q && !aligned(q, 16)) return M3_ERR_ALIGN;
+  const void* f_ptrs[] = {conv_w, conv_b, dt_bias, a_log, D, ckpt};
+  for (const void* q : f_ptrs)
+    if (!aligned(q, 4)) return M3_ERR_ALIGN;
+  if (p.Sf > 1) {
+    if (!workspace) return M3_ERR_WORKSPACE;
+    if (workspace_bytes < p.ws_bytes) return M3_ERR_WORKSPACE;
+    if (!aligned(workspace, 256)) return M3_ERR_ALIGN;
+  }
+  if (ensure_device(p.K) != M3_OK) return M3_ERR_CUDA;
+  FwdArgs a{};
+  a.x = x; a.dr = delta_raw; a.z = z; a.Bm = Bm; a.Cm = Cm;
+  a.conv_w = conv_w; a.conv_b = conv_b; a.dt_bias = dt_bias; a.a_log = a_log; a.Dp = D;
+  a.gated = gated; a.y_dbg = y_dbg; a.ckpt = ckpt;
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  a.agg_h = p.Sf > 1 ? reinterpret_cast<float*>(ws + p.f_aggh) : nullptr;
+  a.agg_s = p.Sf > 1 ? reinterpret_cast<float*>(ws + p.f_aggs) : nullptr;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  return act == M3_BF16 ? launch_fwd<__nv_bfloat16>(p, a, s) : launch_fwd<float>(p, a, s);
+}
+
+m3_status m3scan_bwd(const m3_dims* dims, m3_dtype act, const void* x, const void* delta_raw,
+                     const void* z, const void* Bm, const void* Cm, const float* conv_w,
+                     const float* conv_b, const float* dt_bias, const float* a_log, const float* D,
+                     const float* ckpt, const void* d_gated, void* d_x, void* d_delta_raw, void* dz,
+                     void* du_dbg, float* dB, float* dC, float* d_conv_w, float* d_conv_b,
+                     float* d_dt_bias, float* d_a_log, float* dD, void* workspace,
+                     size_t workspace_bytes, m3_stream_t stream) {
+  Plan p;
+  m3_status st = make_plan(dims, act, &p);
+  if (st != M3_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if ((size_t)p.B * p.T * p.D == 0) {
+    // no elements: parameter grads are zero (or unchanged when accumulating)
+    if (p.D > 0 && !dims->accumulate_param_grads) {
+      if (!d_conv_w || !d_conv_b || !d_dt_bias || !d_a_log || !dD) return M3_ERR_NULL;
+      const size_t D_ = p.D;
+      if (cudaMemsetAsync(d_conv_w, 0, D_ * WC * 4, s) != cudaSuccess ||
+          cudaMemsetAsync(d_conv_b, 0, D_ * 4, s) != cudaSuccess ||
+          cudaMemsetAsync(d_dt_bias, 0, D_ * 4, s) != cudaSuccess ||
+          cudaMemsetAsync(d_a_log, 0, D_ * NS * 4, s) != cudaSuccess ||
+          cudaMemsetAsync(dD, 0, D_ * 4, s) != cudaSuccess) {
+        cudaGetLastError();
+        return M3_ERR_CUDA;
+      }
+    }
+    return M3_OK;
+  }
+  if (!x || !delta_raw || !z || !Bm || !Cm || !conv_w || !conv_b || !dt_bias || !a_log || !D ||
+      !ckpt || !d_gated || !d_x || !d_delta_raw || !dz || !dB || !dC || !d_conv_w || !d_conv_b ||
+      !d_dt_bias || !d_a_log || !dD)
+    return M3_ERR_NULL;
+  const void* act_ptrs[] = {x, delta_raw, z, Bm, Cm, d_gated, d_x, d_delta_raw, dz, du_dbg};
+  for (const void* q : act_ptrs)
+    if (q && !aligned(q, 16)) return M3_ERR_ALIGN;
+  const void* f_ptrs[] = {conv_w, conv_b, dt_bias, a_log, D, ckpt, dB, dC,
+                          d_conv_w, d_conv_b, d_dt_bias, d_a_log, dD};
+  for (const void* q : f_ptrs)
+    if (!aligned(q, 4)) return M3_ERR_ALIGN;
+  if (!workspace) return M3_ERR_WORKSPACE;
+  if (workspace_bytes < p.ws_bytes) return M3_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return M3_ERR_ALIGN;
+  if (ensure_device(p.K) != M3_OK) return M3_ERR_CUDA;
+  BwdArgs a{};
+  a.x = x; a.dr = delta_raw; a.z = z; a.Bm = Bm; a.Cm = Cm; a.dg = d_gated;
+  a.conv_w = conv_w; a.conv_b = conv_b; a.dt_bias = dt_bias; a.a_log = a_log; a.Dp = D;
+  a.ckpt = ckpt;
+  a.dx = d_x; a.ddr = d_delta_raw; a.dz = dz; a.du_dbg = du_dbg;
+  a.dB = dB; a.dC = dC;
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  a.partials = reinterpret_cast<float*>(ws + p.b_part);
+  if (p.Sb > 1) {
+    a.q = reinterpret_cast<float*>(ws + p.b_q);
+    a.sd = reinterpret_cast<float*>(ws + p.b_sd);
+    a.gin = reinterpret_cast<float*>(ws + p.b_gin);
+    a.dxpart = reinterpret_cast<float*>(ws + p.b_dxpart);
+    a.dchead = reinterpret_cast<float*>(ws + p.b_dchead);
+  }
+  a.d_conv_w = d_conv_w; a.d_conv_b = d_conv_b; a.d_dt_bias = d_dt_bias; a.d_a_log = d_a_log;
+  a.dD = dD;
+  a.accumulate = dims->accumulate_param_grads ? 1 : 0;
+  m3_status r = act == M3_BF16 ? launch_bwd<__nv_bfloat16>(p, a, s) : launch_bwd<float>(p, a, s);
+  if (r != M3_OK) cudaGetLastError();
+  return r;
+}
+
+}  // extern "C"

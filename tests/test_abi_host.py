@@ -1,0 +1,170 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds for
+sm_103a, loads, exports every function include/m3scan.h declares, and its
+argument validation rejects bad calls before anything is enqueued.
+
+Every call here that passes addresses is built to fail validation (NULL,
+misaligned, unsupported or undersized arguments), so nothing ever reaches a
+device even where one is present.
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from mamba_selective_scan_gb300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load()
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "m3scan.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(m3scan_\w+)\s*\(", src)))
+
+
+def test_header_declares_what_the_binding_exports():
+    assert _declared_functions() == sorted(binding.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_version_and_status_strings(lib):
+    assert binding.m3scan_version() == 100
+    for code, name in binding.STATUS.items():
+        assert binding.m3scan_status_string(code).startswith(name)
+    assert "unknown" in binding.m3scan_status_string(99)
+
+
+def _plan(dims, act=binding.M3_BF16):
+    out = binding.M3Plan()
+    st = binding.load().m3scan_plan(ctypes.byref(dims), act, ctypes.byref(out))
+    return st, out
+
+
+def test_plan_with_explicit_segments_needs_no_device(lib):
+    dims = binding.make_dims(8, 2048, 1536, chunk=16, segments=4)
+    st, p = _plan(dims)
+    assert st == 0
+    assert p.chunk == 16 and p.n_chunks == 128
+    assert p.fwd_segments == 4 and p.bwd_segments == 4
+    assert p.ckpt_bytes == 8 * 128 * 16 * 1536 * 4
+    assert p.fwd_launches == 3 and p.bwd_launches == 5
+    # one segment: the main kernel plus the parameter-gradient finalize
+    st, p1 = _plan(binding.make_dims(8, 2048, 1536, chunk=16, segments=1))
+    assert st == 0 and p1.fwd_launches == 1 and p1.bwd_launches == 2
+    assert p1.workspace_bytes >= 8 * 24 * 1536 * 4
+
+
+def test_segments_are_whole_chunks_of_at_least_four_steps(lib):
+    st, p = _plan(binding.make_dims(1, 10, 8, chunk=1, segments=10))
+    assert st == 0
+    # chunk 1 -> at least 4 chunks per segment -> ceil(10 / 4) = 3 segments
+    assert p.fwd_segments == 3 and p.bwd_segments == 3
+    st, p = _plan(binding.make_dims(1, 10, 8, chunk=16, segments=7))
+    assert st == 0 and p.fwd_segments == 1
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(d_state=8), "M3_ERR_UNSUPPORTED"),
+    (dict(d_conv=3), "M3_ERR_UNSUPPORTED"),
+    (dict(d_inner=36), "M3_ERR_UNSUPPORTED"),
+    (dict(batch=-1), "M3_ERR_DIMS"),
+    (dict(seq_len=-5), "M3_ERR_DIMS"),
+    (dict(chunk=65), "M3_ERR_DIMS"),
+    (dict(chunk=64), "M3_ERR_UNSUPPORTED"),  # backward footprint too large
+    (dict(segments=-1), "M3_ERR_DIMS"),
+    (dict(batch=70000), "M3_ERR_DIMS"),
+])
+def test_plan_rejects_bad_dims(lib, kw, status):
+    base = dict(batch=2, seq_len=64, d_inner=64, d_state=16, d_conv=4, chunk=16, segments=1)
+    base.update(kw)
+    st, _ = _plan(binding.make_dims(**base))
+    assert binding.STATUS[st] == status
+
+
+def test_plan_rejects_unknown_dtype_and_null(lib):
+    st, _ = _plan(binding.make_dims(1, 8, 8, segments=1), act=7)
+    assert binding.STATUS[st] == "M3_ERR_UNSUPPORTED"
+    assert binding.STATUS[lib.m3scan_plan(None, 1, None)] == "M3_ERR_NULL"
+
+
+def test_f32_chunk_limit_is_lower_than_bf16(lib):
+    st_b, _ = _plan(binding.make_dims(1, 64, 64, chunk=32, segments=1), binding.M3_BF16)
+    st_f, _ = _plan(binding.make_dims(1, 64, 64, chunk=32, segments=1), binding.M3_F32)
+    assert st_b == 0
+    assert binding.STATUS[st_f] == "M3_ERR_UNSUPPORTED"
+
+
+A = 1 << 20  # a 256-byte aligned fake address; never dereferenced
+
+
+def _fwd_args(**over):
+    a = dict(x=A, delta_raw=A, z=A, Bm=A, Cm=A, conv_w=A, conv_b=A, dt_bias=A, a_log=A,
+             D=A, gated=A, y_dbg=None, ckpt=A, workspace=A, workspace_bytes=1 << 30,
+             stream=None)
+    a.update(over)
+    return a
+
+
+def _fwd(dims, act=binding.M3_BF16, **over):
+    a = _fwd_args(**over)
+    return binding.STATUS[binding.raw_fwd(dims, act, a["x"], a["delta_raw"], a["z"], a["Bm"],
+                                          a["Cm"], a["conv_w"], a["conv_b"], a["dt_bias"],
+                                          a["a_log"], a["D"], a["gated"], a["y_dbg"],
+                                          a["ckpt"], a["workspace"], a["workspace_bytes"],
+                                          a["stream"])]
+
+
+def test_fwd_rejects_null_and_misaligned_before_any_launch(lib):
+    dims = binding.make_dims(2, 64, 64, chunk=16, segments=2)
+    assert _fwd(dims, x=None) == "M3_ERR_NULL"
+    assert _fwd(dims, ckpt=None) == "M3_ERR_NULL"
+    assert _fwd(dims, gated=None) == "M3_ERR_NULL"
+    assert _fwd(dims, x=A + 2) == "M3_ERR_ALIGN"
+    assert _fwd(dims, Cm=A + 8) == "M3_ERR_ALIGN"
+    assert _fwd(dims, y_dbg=A + 4) == "M3_ERR_ALIGN"
+    assert _fwd(dims, conv_w=A + 1) == "M3_ERR_ALIGN"
+    assert _fwd(dims, workspace=None) == "M3_ERR_WORKSPACE"
+    assert _fwd(dims, workspace_bytes=16) == "M3_ERR_WORKSPACE"
+    assert _fwd(dims, workspace=A + 16) == "M3_ERR_ALIGN"
+    assert _fwd(binding.make_dims(2, 64, 60, segments=1)) == "M3_ERR_UNSUPPORTED"
+
+
+def test_empty_forward_is_a_no_op(lib):
+    # zero elements: nothing to do, nothing is touched, pointers may be NULL
+    dims = binding.make_dims(0, 64, 64, segments=1)
+    assert _fwd(dims, x=None, gated=None, ckpt=None) == "M3_OK"
+
+
+def _bwd(dims, act=binding.M3_BF16, **over):
+    a = dict(x=A, delta_raw=A, z=A, Bm=A, Cm=A, conv_w=A, conv_b=A, dt_bias=A, a_log=A, D=A,
+             ckpt=A, d_gated=A, d_x=A, d_delta_raw=A, dz=A, du_dbg=None, dB=A, dC=A,
+             d_conv_w=A, d_conv_b=A, d_dt_bias=A, d_a_log=A, dD=A, workspace=A,
+             workspace_bytes=1 << 30, stream=None)
+    a.update(over)
+    return binding.STATUS[binding.raw_bwd(dims, act, *a.values())]
+
+
+def test_bwd_rejects_bad_arguments_before_any_launch(lib):
+    dims = binding.make_dims(2, 64, 64, chunk=16, segments=1)
+    assert _bwd(dims, d_gated=None) == "M3_ERR_NULL"
+    assert _bwd(dims, dB=None) == "M3_ERR_NULL"
+    assert _bwd(dims, dD=None) == "M3_ERR_NULL"
+    assert _bwd(dims, d_x=A + 2) == "M3_ERR_ALIGN"
+    assert _bwd(dims, du_dbg=A + 2) == "M3_ERR_ALIGN"
+    assert _bwd(dims, dC=A + 2) == "M3_ERR_ALIGN"
+    assert _bwd(dims, workspace=None) == "M3_ERR_WORKSPACE"
+    assert _bwd(dims, workspace_bytes=255) == "M3_ERR_WORKSPACE"
+    assert _bwd(dims, workspace=A + 128) == "M3_ERR_ALIGN"
+    assert _bwd(binding.make_dims(2, 64, 64, d_state=32, segments=1)) == "M3_ERR_UNSUPPORTED"
