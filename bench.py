@@ -1,0 +1,628 @@
+#!/usr/bin/env python
+"""Throughput of the selective-scan layer core (forward + backward) on GB300.
+
+One step = one forward (m3scan_fwd) and one backward (m3scan_bwd) of the
+layer core over one batch of the workload, through the C ABI.  Prints ONE
+JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the CPU oracle, timed on host cores
+
+Timing: inputs resident in HBM; each step is two CUDA-graph replays (forward
+graph, backward graph) bracketed by CUDA events on the launching stream;
+L2 is flushed (256 MiB memset) between steps, outside the events.  The
+end-to-end number repeats the step through the Python binding with inputs
+copied from pinned host memory and results copied back inside the timed
+region.  Multi-GPU runs are independent replicas (weak scaling).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from mamba_selective_scan_gb300.inputs import WORKLOADS, make_workload_inputs  # noqa: E402
+
+METRIC = "selective-scan fwd+bwd Gelem/s (B*T*d_inner) and % of GB300 HBM roofline"
+UNIT = "Gelem/s"
+DEFAULT_WORKLOAD = "trainer_b8_t128_d512"
+EXTRA_WORKLOADS = ("m130m_b8_t2048_d1536", "longseq_b1_t65536_d2048", "m2p8b_b4_t4096_d5120")
+HBM_TARGET_GBS = 8000.0  # the roofline bandwidth the metric is defined with
+ROOFLINE_CHUNK = 128     # chunk length of the metric's minimum-bytes formula
+NS = 16
+
+
+def algorithmic_bytes(batch, T, D, es, chunk=ROOFLINE_CHUNK):
+    """Minimum bytes the fused design moves (per call), with checkpoints every
+    `chunk` steps: forward reads x, delta_raw, z, B, C and writes gated and the
+    checkpoints; backward reads x, delta_raw, z, d_gated, B, C and the
+    checkpoints and writes d_x, d_delta_raw, dz, dB, dC (f32)."""
+    E = batch * T * D
+    nc = -(-T // chunk)
+    bc = batch * T * 2 * NS
+    ck = batch * nc * NS * D * 4
+    fwd = E * 4 * es + bc * es + ck
+    bwd = E * 7 * es + bc * es + bc * 4 + ck
+    return fwd, bwd
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def source_hash():
+    h = hashlib.sha256()
+    with open(os.path.join(ROOT, "mamba_selective_scan_gb300", "csrc", "m3scan.cu"), "rb") as f:
+        h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload, kernel):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    if d.get("source_sha256_16") != source_hash():
+        return None
+    return d.get("traffic", {}).get(workload, {}).get(kernel)
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"m3scan_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append(dict(sm=float(parts[1]), smax=float(parts[2]),
+                                     power=float(parts[3]) if parts[3] not in ("[N/A]", "") else None,
+                                     hw=parts[5], hwt=parts[6], swt=parts[7], pcap=parts[8]))
+                except ValueError:
+                    continue
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        if not rows:
+            return None
+        reasons = set()
+        for r in rows:
+            for k, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                            ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
+                if r[k].lower().startswith("active"):
+                    reasons.add(name)
+        powers = [r["power"] for r in rows if r["power"] is not None]
+        return {"sm_mhz": statistics.median(r["sm"] for r in rows),
+                "sm_max_mhz": max(r["smax"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows),
+                "power_w_max": max(powers) if powers else None}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+class Layer:
+    """Device buffers, plan and captured graphs for one layer-core instance."""
+
+    def __init__(self, torch, binding, tensors, chunk=0, segments=0):
+        self.t = tensors
+        x = tensors["x"]
+        self.act = binding.M3_BF16 if x.dtype == torch.bfloat16 else binding.M3_F32
+        Bsz, T, D = x.shape
+        self.shape = (Bsz, T, D)
+        self.dims = binding.make_dims(Bsz, T, D, chunk=chunk, segments=segments)
+        self.plan = binding.m3scan_plan(self.dims, self.act)
+        dev = x.device
+        f32 = dict(dtype=torch.float32, device=dev)
+        self.o = {
+            "gated": torch.empty_like(x),
+            "ckpt": torch.empty((Bsz, self.plan.n_chunks, NS, D), **f32),
+            "d_x": torch.empty_like(x), "d_delta_raw": torch.empty_like(x),
+            "dz": torch.empty_like(x),
+            "dB": torch.empty((Bsz, T, NS), **f32), "dC": torch.empty((Bsz, T, NS), **f32),
+            "d_conv_w": torch.empty((D, 4), **f32), "d_conv_b": torch.empty((D,), **f32),
+            "d_dt_bias": torch.empty((D,), **f32), "d_a_log": torch.empty((D, NS), **f32),
+            "dD": torch.empty((D,), **f32),
+        }
+        self.ws = torch.empty(max(int(self.plan.workspace_bytes), 256), dtype=torch.uint8,
+                              device=dev)
+        self.binding = binding
+
+    def fwd(self, stream):
+        t, o, b = self.t, self.o, self.binding
+        st = b.raw_fwd(self.dims, self.act, t["x"].data_ptr(), t["delta_raw"].data_ptr(),
+                       t["z"].data_ptr(), t["B"].data_ptr(), t["C"].data_ptr(),
+                       t["conv_w"].data_ptr(), t["conv_b"].data_ptr(), t["dt_bias"].data_ptr(),
+                       t["a_log"].data_ptr(), t["D"].data_ptr(), o["gated"].data_ptr(), None,
+                       o["ckpt"].data_ptr(), self.ws.data_ptr(), self.ws.numel(), stream)
+        if st != 0:
+            raise b.M3Error(st, "m3scan_fwd")
+
+    def bwd(self, stream):
+        t, o, b = self.t, self.o, self.binding
+        st = b.raw_bwd(self.dims, self.act, t["x"].data_ptr(), t["delta_raw"].data_ptr(),
+                       t["z"].data_ptr(), t["B"].data_ptr(), t["C"].data_ptr(),
+                       t["conv_w"].data_ptr(), t["conv_b"].data_ptr(), t["dt_bias"].data_ptr(),
+                       t["a_log"].data_ptr(), t["D"].data_ptr(), o["ckpt"].data_ptr(),
+                       t["d_gated"].data_ptr(), o["d_x"].data_ptr(), o["d_delta_raw"].data_ptr(),
+                       o["dz"].data_ptr(), None, o["dB"].data_ptr(), o["dC"].data_ptr(),
+                       o["d_conv_w"].data_ptr(), o["d_conv_b"].data_ptr(),
+                       o["d_dt_bias"].data_ptr(), o["d_a_log"].data_ptr(), o["dD"].data_ptr(),
+                       self.ws.data_ptr(), self.ws.numel(), stream)
+        if st != 0:
+            raise b.M3Error(st, "m3scan_bwd")
+
+
+def host_inputs_to_device(torch, inp, device):
+    import numpy as np
+    from mamba_selective_scan_gb300.inputs import bf16_bits
+    out = {}
+    for k, v in inp.arrays.items():
+        if k in ("x", "delta_raw", "z", "B", "C", "d_gated") and inp.act == "bf16":
+            out[k] = torch.from_numpy(bf16_bits(v).view(np.int16)).view(torch.bfloat16).to(device)
+        else:
+            out[k] = torch.from_numpy(np.ascontiguousarray(v, dtype=np.float32)).to(device)
+    return out
+
+
+def device_inputs(torch, w, device, seed_offset=0):
+    """Inputs drawn on the device with the recipe's distributions (used for
+    the large extra workloads, where drawing with NumPy on the host would
+    dominate the run time)."""
+    g = torch.Generator(device=device)
+    g.manual_seed(1_000_003 * (w.seed + 1) + seed_offset)
+    Bsz, T, D = w.batch, w.seq_len, w.d_inner
+    act = torch.bfloat16 if w.act == "bf16" else torch.float32
+    f32 = dict(dtype=torch.float32, device=device)
+
+    def normal(shape, std=1.0):
+        return (torch.randn(shape, generator=g, **f32) * std).to(act)
+
+    def softplus_inv(y):
+        return torch.log(torch.expm1(y.double())).float()
+    t = {"x": normal((Bsz, T, D)), "z": normal((Bsz, T, D)), "d_gated": normal((Bsz, T, D))}
+    t["conv_w"] = torch.rand((D, 4), generator=g, **f32) - 0.5
+    dt_bias = softplus_inv(0.001 + 0.099 * torch.rand((D,), generator=g, **f32))
+    if w.slow_delta:
+        tgt = 0.001 + 0.009 * torch.rand((Bsz, T, D), generator=g, **f32)
+        t["delta_raw"] = (softplus_inv(tgt) - dt_bias).to(act)
+        del tgt
+    else:
+        t["delta_raw"] = normal((Bsz, T, D), 0.5)
+    t["dt_bias"] = dt_bias
+    t["B"] = normal((Bsz, T, NS))
+    t["C"] = normal((Bsz, T, NS))
+    t["conv_b"] = torch.zeros((D,), **f32)
+    t["a_log"] = torch.log(torch.arange(1, NS + 1, **f32)).repeat(D, 1).contiguous()
+    t["D"] = torch.ones((D,), **f32)
+    return t
+
+
+def capture(torch, layer_list, stream):
+    """Capture the forward of every layer (in order) and the backward (in
+    reverse order) as two CUDA graphs."""
+    gf, gb = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gf, stream=stream):
+        for L in layer_list:
+            L.fwd(torch.cuda.current_stream().cuda_stream)
+    with torch.cuda.graph(gb, stream=stream):
+        for L in reversed(layer_list):
+            L.bwd(torch.cuda.current_stream().cuda_stream)
+    return gf, gb
+
+
+def time_steps(torch, gf, gb, steps, flush):
+    """Per-step forward and backward device times (ms) with L2 flushed
+    before every step."""
+    s = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for i in range(steps):
+        if flush is not None:
+            flush.zero_()
+        e0, e1, e2 = ev[i]
+        e0.record(s)
+        gf.replay()
+        e1.record(s)
+        gb.replay()
+        e2.record(s)
+    torch.cuda.synchronize()
+    f = [a.elapsed_time(b) for a, b, _ in ev]
+    bw = [b.elapsed_time(c) for _, b, c in ev]
+    return f, bw
+
+
+def gpu_arm(args):
+    import torch
+    from mamba_selective_scan_gb300 import binding, build
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    if rank == 0 or world == 1:
+        build.build()
+    if dist is not None:
+        dist.barrier()
+    binding.load()
+
+    w = WORKLOADS[args.workload]
+    es = 2 if w.act == "bf16" else 4
+    inp = make_workload_inputs(args.workload)
+    tensors = host_inputs_to_device(torch, inp, device)
+    layer = Layer(torch, binding, tensors, chunk=args.chunk, segments=args.segments)
+    stream = torch.cuda.Stream(device)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+
+    # warm-up (eager), then capture
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 1)):
+            layer.fwd(stream.cuda_stream)
+            layer.bwd(stream.cuda_stream)
+    torch.cuda.synchronize()
+    gf, gb = capture(torch, [layer], stream)
+    for _ in range(args.warmup):
+        gf.replay()
+        gb.replay()
+    torch.cuda.synchronize()
+
+    # keep the GPU busy briefly so the clock samples see steady state
+    sampler = ClockSampler(local)
+    sampler.start()
+    t_end = time.time() + 0.3
+    while time.time() < t_end:
+        for _ in range(20):
+            gf.replay()
+            gb.replay()
+        torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    f_ms, b_ms = time_steps(torch, gf, gb, args.steps, flush)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    clocks = sampler.stop()
+
+    total_ms = sum(f_ms) + sum(b_ms)
+    if dist is not None:
+        tt = torch.tensor([total_ms], device=device, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    E = w.elems
+    value = world * E * args.steps / (total_ms * 1e-3) / 1e9
+    fwd_avg = sum(f_ms) / len(f_ms)
+    bwd_avg = sum(b_ms) / len(b_ms)
+    fb, bb = algorithmic_bytes(w.batch, w.seq_len, w.d_inner, es)
+    peak, peak_kind = measured_peaks()
+    step_s = (fwd_avg + bwd_avg) * 1e-3
+    bwd_achieved = bb / (bwd_avg * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "kernel": "m3scan_bwd (m3_bwd_kernel + finalize)",
+                "achieved": round(bwd_achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(bwd_achieved / peak, 4), "peak_kind": peak_kind,
+                "traffic": ncu_traffic(args.workload, "bwd"),
+                "algorithmic_bytes_per_launch": bb}
+    hbm = {"min_bytes_fwd_bwd": fb + bb, "chunk_for_min_bytes": ROOFLINE_CHUNK,
+           "frac_of_8TBs": round((fb + bb) / HBM_TARGET_GBS / 1e9 / step_s, 4),
+           "frac_of_measured": round((fb + bb) / peak / 1e9 / step_s, 4),
+           "fwd_gelem_s": round(E / (fwd_avg * 1e-3) / 1e9, 2),
+           "bwd_gelem_s": round(E / (bwd_avg * 1e-3) / 1e9, 2)}
+
+    # end to end through the public binding with pinned host buffers
+    e2e = None
+    if rank == 0 or world > 1:
+        e2e = e2e_measure(torch, binding, layer, tensors, min(args.steps, 50), device)
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total_ms / args.steps, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "batch": w.batch, "seq_len": w.seq_len,
+                   "d_inner": w.d_inner, "d_state": NS, "d_conv": 4, "act_storage": w.act,
+                   "chunk": int(layer.plan.chunk), "fwd_segments": int(layer.plan.fwd_segments),
+                   "bwd_segments": int(layer.plan.bwd_segments),
+                   "l2": "flushed before every step (256 MiB memset outside the events)",
+                   "timing": "CUDA graphs (fwd, bwd) per step, CUDA events per graph",
+                   "parallelism": f"replicas x{world}"},
+        "hbm_roofline": hbm,
+        "roofline": roofline,
+        "e2e": e2e,
+        "gpu_launches": int(args.steps * (layer.plan.fwd_launches + layer.plan.bwd_launches)),
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(inp, args.cpu_seconds)
+    if rank == 0 and not args.no_extras:
+        line["extra"] = extras(torch, binding, device, args, flush, stream)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def e2e_measure(torch, binding, layer, tensors, steps, device):
+    """Same step through the public binding, with the step's inputs copied
+    from pinned host memory and its results copied back inside the events."""
+    ins = ("x", "delta_raw", "z", "B", "C", "d_gated", "conv_w", "conv_b", "dt_bias",
+           "a_log", "D")
+    outs = ("gated", "d_x", "d_delta_raw", "dz", "dB", "dC", "d_conv_w", "d_conv_b",
+            "d_dt_bias", "d_a_log", "dD")
+    h_in = {k: tensors[k].cpu().pin_memory() for k in ins}
+    d_in = {k: torch.empty_like(tensors[k]) for k in ins}
+    h_out = {k: torch.empty(layer.o[k].shape, dtype=layer.o[k].dtype, pin_memory=True)
+             for k in outs}
+    bi = sum(v.numel() * v.element_size() for v in h_in.values())
+    bo = sum(v.numel() * v.element_size() for v in h_out.values())
+    ws = layer.ws
+    s = torch.cuda.current_stream()
+    E = layer.shape[0] * layer.shape[1] * layer.shape[2]
+
+    def step():
+        for k in ins:
+            d_in[k].copy_(h_in[k], non_blocking=True)
+        gated, ckpt, _ = binding.m3scan_fwd(
+            d_in["x"], d_in["delta_raw"], d_in["z"], d_in["B"], d_in["C"], d_in["conv_w"],
+            d_in["conv_b"], d_in["dt_bias"], d_in["a_log"], d_in["D"], chunk=int(layer.plan.chunk),
+            gated=layer.o["gated"], ckpt=layer.o["ckpt"],
+            workspace=_WS(ws), stream=s)
+        g = binding.m3scan_bwd(
+            d_in["x"], d_in["delta_raw"], d_in["z"], d_in["B"], d_in["C"], d_in["conv_w"],
+            d_in["conv_b"], d_in["dt_bias"], d_in["a_log"], d_in["D"], ckpt, d_in["d_gated"],
+            chunk=int(layer.plan.chunk), out={k: layer.o[k] for k in outs if k != "gated"},
+            workspace=_WS(ws), stream=s)
+        h_out["gated"].copy_(gated, non_blocking=True)
+        for k in outs[1:]:
+            h_out[k].copy_(g[k], non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(steps):
+        step()
+    e1.record(s)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    return {"value": round(E * steps / (ms * 1e-3) / 1e9, 3), "unit": UNIT,
+            "h2d_bytes_per_step": int(bi), "d2h_bytes_per_step": int(bo),
+            "ms_per_step": round(ms / steps, 5), "steps": steps}
+
+
+class _WS:
+    def __init__(self, buf):
+        self.buf = buf
+        self.nbytes = buf.numel()
+        self.ptr = buf.data_ptr()
+
+
+def extras(torch, binding, device, args, flush, stream):
+    """The larger workloads at full size (device-drawn inputs, same recipe
+    distributions), and the 24-layer stack of the Mamba-2.8B-like core."""
+    out = {}
+    for name in EXTRA_WORKLOADS:
+        w = WORKLOADS[name]
+        es = 2 if w.act == "bf16" else 4
+        t = device_inputs(torch, w, device)
+        L = Layer(torch, binding, t)
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                L.fwd(stream.cuda_stream)
+                L.bwd(stream.cuda_stream)
+        torch.cuda.synchronize()
+        gf, gb = capture(torch, [L], stream)
+        for _ in range(2):
+            gf.replay()
+            gb.replay()
+        f_ms, b_ms = time_steps(torch, gf, gb, args.extra_steps, flush)
+        fa, ba = sum(f_ms) / len(f_ms), sum(b_ms) / len(b_ms)
+        fb, bb = algorithmic_bytes(w.batch, w.seq_len, w.d_inner, es)
+        E = w.elems
+        out[name] = {"gelem_s": round(E / ((fa + ba) * 1e-3) / 1e9, 2),
+                     "fwd_gelem_s": round(E / (fa * 1e-3) / 1e9, 2),
+                     "bwd_gelem_s": round(E / (ba * 1e-3) / 1e9, 2),
+                     "ms_fwd": round(fa, 4), "ms_bwd": round(ba, 4),
+                     "frac_of_8TBs": round((fb + bb) / HBM_TARGET_GBS / 1e9 / ((fa + ba) * 1e-3), 4),
+                     "fwd_segments": int(L.plan.fwd_segments),
+                     "bwd_segments": int(L.plan.bwd_segments), "chunk": int(L.plan.chunk)}
+        del gf, gb, L, t
+        torch.cuda.empty_cache()
+    if not args.no_stack:
+        out["m2p8b_stack24"] = stack24(torch, binding, device, args, stream)
+    return out
+
+
+def stack24(torch, binding, device, args, stream):
+    name = "m2p8b_b4_t4096_d5120"
+    w = WORKLOADS[name]
+    layers = [Layer(torch, binding, device_inputs(torch, w, device, seed_offset=l))
+              for l in range(24)]
+    with torch.cuda.stream(stream):
+        for L in layers:
+            L.fwd(stream.cuda_stream)
+        for L in reversed(layers):
+            L.bwd(stream.cuda_stream)
+    torch.cuda.synchronize()
+    gf, gb = capture(torch, layers, stream)
+    gf.replay()
+    gb.replay()
+    torch.cuda.synchronize()
+    f_ms, b_ms = time_steps(torch, gf, gb, max(2, args.extra_steps // 4), None)
+    fa, ba = sum(f_ms) / len(f_ms), sum(b_ms) / len(b_ms)
+    fb, bb = algorithmic_bytes(w.batch, w.seq_len, w.d_inner, 2)
+    E = 24 * w.elems
+    res = {"gelem_s": round(E / ((fa + ba) * 1e-3) / 1e9, 2), "ms_fwd": round(fa, 3),
+           "ms_bwd": round(ba, 3),
+           "frac_of_8TBs": round(24 * (fb + bb) / HBM_TARGET_GBS / 1e9 / ((fa + ba) * 1e-3), 4),
+           "note": "24 independent layer cores, fwd 0..23 then bwd 23..0, one graph each"}
+    del gf, gb, layers
+    torch.cuda.empty_cache()
+    return res
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (baseline and reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_sample_rate(inp, channels):
+    """Time the oracle's forward + backward on the first `channels`
+    channels (all batches and steps) of the workload; returns (elements, s)."""
+    import numpy as np
+
+    import oracle
+    mask = np.zeros(inp.d_inner, dtype=np.uint8)
+    mask[:channels] = 1
+    t0 = time.perf_counter()
+    oracle.forward(inp, chan_mask=mask)
+    oracle.backward(inp, chan_mask=mask)
+    dt = time.perf_counter() - t0
+    return inp.batch * inp.seq_len * channels, dt
+
+
+def pick_channels(inp, seconds):
+    """Channels whose oracle fwd+bwd takes about `seconds` (fixed per-call
+    overhead measured separately and excluded from the per-channel cost)."""
+    oracle_sample_rate(inp, 1)  # load the library, warm caches
+    k = min(8, inp.d_inner)
+    _, t1 = oracle_sample_rate(inp, 1)
+    _, tk = oracle_sample_rate(inp, k)
+    per_chan = max((tk - t1) / max(k - 1, 1), tk / k / 4, 1e-6)
+    fixed = max(t1 - per_chan, 0.0)
+    ch = int(max(seconds - fixed, 0.0) / per_chan)
+    return max(1, min(inp.d_inner, ch)), per_chan
+
+
+def cpu_baseline(inp, seconds):
+    import oracle
+    oracle.build()
+    ch, _ = pick_channels(inp, seconds)
+    e, dt = oracle_sample_rate(inp, ch)
+    return {"value": round(e / dt / 1e9, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"first {ch} of {inp.d_inner} channels, all batches and steps, "
+                      f"fwd+bwd, float64 C, single thread ({dt:.1f} s)"}
+
+
+def reference_arm(args):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    w = WORKLOADS[args.workload]
+    inp = make_workload_inputs(args.workload)
+    total_steps = args.steps + args.warmup
+    budget = 90.0 / max(total_steps, 1)
+    ch, _ = pick_channels(inp, budget)
+    for _ in range(args.warmup):
+        oracle_sample_rate(inp, ch)
+    times = []
+    elems = 0
+    for _ in range(args.steps):
+        e, dt = oracle_sample_rate(inp, ch)
+        times.append(dt)
+        elems += e
+    tot = sum(times)
+    value = elems / tot / 1e9
+    sample = (f"first {ch} of {w.d_inner} channels per step, all batches and steps, "
+              f"fwd+bwd, float64 C, single thread")
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(tot / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "batch": w.batch, "seq_len": w.seq_len,
+                       "d_inner": w.d_inner, "d_state": NS, "d_conv": 4, "act_storage": w.act},
+            "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": 1,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--chunk", type=int, default=0)
+    ap.add_argument("--segments", type=int, default=0)
+    ap.add_argument("--extra-steps", type=int, default=20)
+    ap.add_argument("--no-extras", action="store_true")
+    ap.add_argument("--no-stack", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        reference_arm(args)
+    else:
+        gpu_arm(args)
+
+
+if __name__ == "__main__":
+    main()
