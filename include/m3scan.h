@@ -139,6 +139,50 @@ m3_status m3scan_bwd(const m3_dims* dims, m3_dtype act,
                      void* workspace, size_t workspace_bytes,
                      m3_stream_t stream);
 
+/*
+ * Size in bytes of the scratch array the library keeps on every GPU that
+ * loads it, for m3scan_bwd_noalloc.
+ */
+#define M3SCAN_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/*
+ * The paper has no counterpart to this entry point: it is an addition for
+ * callers that cannot allocate device memory -- for example a plugin or host
+ * application that hands the library a fixed device-memory budget and
+ * forbids allocation inside its execution path, or a latency-critical caller
+ * that cannot accept the implicit device synchronisation of cudaMalloc and
+ * cudaFree.
+ *
+ * Same computation, arguments and results as m3scan_bwd, without the
+ * workspace arguments: the scratch is a fixed array of
+ * M3SCAN_NOALLOC_SCRATCH_BYTES inside the library.  Neither this call nor
+ * anything it calls allocates or frees memory.  The caller still passes
+ * (and owns) every input and output.
+ *
+ * - A shape whose plan needs more scratch than M3SCAN_NOALLOC_SCRATCH_BYTES
+ *   (m3scan_plan's workspace_bytes) is rejected with M3_ERR_WORKSPACE before
+ *   anything is enqueued; use m3scan_bwd with a workspace for it.
+ * - The first call on a device, with that device current, looks up the
+ *   array's device address (cudaGetSymbolAddress) and caches it; make that
+ *   first call before any stream capture on that device.
+ * - Every call on a device shares the one array, and the array keeps what
+ *   the last call left in it (nothing in it needs to start at zero).  Calls
+ *   that overlap on the GPU -- on different streams, or from different host
+ *   threads without ordering -- race on it and give wrong results; order
+ *   them on one stream or with events.
+ */
+m3_status m3scan_bwd_noalloc(const m3_dims* dims, m3_dtype act,
+                             const void* x, const void* delta_raw, const void* z,
+                             const void* Bm, const void* Cm,
+                             const float* conv_w, const float* conv_b,
+                             const float* dt_bias, const float* a_log, const float* D,
+                             const float* ckpt, const void* d_gated,
+                             void* d_x, void* d_delta_raw, void* dz, void* du_dbg,
+                             float* dB, float* dC,
+                             float* d_conv_w, float* d_conv_b, float* d_dt_bias,
+                             float* d_a_log, float* dD,
+                             m3_stream_t stream);
+
 /* A static, human-readable name for a status code. */
 const char* m3scan_status_string(m3_status status);
 

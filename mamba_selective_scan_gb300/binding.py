@@ -28,8 +28,11 @@ STATUS = {
 }
 
 # every symbol include/m3scan.h declares
-EXPORTS = ("m3scan_plan", "m3scan_fwd", "m3scan_bwd", "m3scan_status_string",
-           "m3scan_version")
+EXPORTS = ("m3scan_plan", "m3scan_fwd", "m3scan_bwd", "m3scan_bwd_noalloc",
+           "m3scan_status_string", "m3scan_version")
+
+# size of the library's own scratch array used by m3scan_bwd_noalloc
+NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
 class M3Error(RuntimeError):
@@ -88,6 +91,10 @@ def _lib_handle(build_if_missing: bool = True):
             lib.m3scan_bwd.argtypes = ([ctypes.POINTER(M3Dims), ctypes.c_int] + [_vp] * 5
                                        + [_fp] * 5 + [_fp, _vp] + [_vp] * 4 + [_fp] * 2
                                        + [_fp] * 5 + [_vp, ctypes.c_size_t, _vp])
+            lib.m3scan_bwd_noalloc.restype = ctypes.c_int
+            lib.m3scan_bwd_noalloc.argtypes = ([ctypes.POINTER(M3Dims), ctypes.c_int] + [_vp] * 5
+                                               + [_fp] * 5 + [_fp, _vp] + [_vp] * 4
+                                               + [_fp] * 2 + [_fp] * 5 + [_vp])
             lib.m3scan_status_string.restype = ctypes.c_char_p
             lib.m3scan_status_string.argtypes = [ctypes.c_int]
             lib.m3scan_version.restype = ctypes.c_int32
@@ -140,6 +147,18 @@ def raw_bwd(dims, act, x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, 
                                     d_delta_raw, dz, du_dbg, dB, dC, d_conv_w, d_conv_b,
                                     d_dt_bias, d_a_log, dD, workspace, int(workspace_bytes),
                                     stream)
+
+
+def raw_bwd_noalloc(dims, act, x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D,
+                    ckpt, d_gated, d_x, d_delta_raw, dz, du_dbg, dB, dC, d_conv_w, d_conv_b,
+                    d_dt_bias, d_a_log, dD, stream) -> int:
+    """Call m3scan_bwd_noalloc (no workspace; the library's fixed scratch
+    array is used) with integer addresses; returns the status code.  For
+    callers that cannot allocate device memory themselves."""
+    return _lib_handle().m3scan_bwd_noalloc(ctypes.byref(dims), int(act), x, delta_raw, z, Bm,
+                                            Cm, conv_w, conv_b, dt_bias, a_log, D, ckpt,
+                                            d_gated, d_x, d_delta_raw, dz, du_dbg, dB, dC,
+                                            d_conv_w, d_conv_b, d_dt_bias, d_a_log, dD, stream)
 
 
 # ---------------------------------------------------------------------------

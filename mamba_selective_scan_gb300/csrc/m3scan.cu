@@ -35,6 +35,12 @@
 
 #include "../../include/m3scan.h"
 
+// Backward scratch owned by the library itself, for m3scan_bwd_noalloc.
+// Every GPU that loads this library holds these bytes until the process
+// exits.  Host code must not use the name as an address: it is fetched per
+// device with cudaGetSymbolAddress.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[M3SCAN_NOALLOC_SCRATCH_BYTES];
+
 namespace {
 
 constexpr int NS = 16;      // d_state lanes per channel
@@ -1160,6 +1166,66 @@ m3_status m3scan_bwd(const m3_dims* dims, m3_dtype act, const void* x, const voi
   m3_status r = act == M3_BF16 ? launch_bwd<__nv_bfloat16>(p, a, s) : launch_bwd<float>(p, a, s);
   if (r != M3_OK) cudaGetLastError();
   return r;
+}
+
+
+}  // extern "C"
+
+namespace {
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[64];  // device address of g_noalloc_scratch, per device
+
+// Set-up for m3scan_bwd_noalloc, once per device with that device current:
+// look up the device address of the library's scratch array.
+m3_status noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return M3_ERR_CUDA;
+  }
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_addr[dev]) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || p == nullptr) {
+      cudaGetLastError();
+      return M3_ERR_CUDA;
+    }
+    g_noalloc_addr[dev] = p;
+  }
+  *out = g_noalloc_addr[dev];
+  return M3_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+// The backward of m3scan_bwd, run on the library's own fixed scratch array
+// instead of a caller-provided workspace; it allocates nothing.  Nothing in
+// the scratch has to start at zero: every byte the kernels read in one call
+// is written earlier in the same call.
+m3_status m3scan_bwd_noalloc(const m3_dims* dims, m3_dtype act, const void* x,
+                             const void* delta_raw, const void* z, const void* Bm,
+                             const void* Cm, const float* conv_w, const float* conv_b,
+                             const float* dt_bias, const float* a_log, const float* D,
+                             const float* ckpt, const void* d_gated, void* d_x,
+                             void* d_delta_raw, void* dz, void* du_dbg, float* dB, float* dC,
+                             float* d_conv_w, float* d_conv_b, float* d_dt_bias,
+                             float* d_a_log, float* dD, m3_stream_t stream) {
+  Plan p;
+  m3_status st = make_plan(dims, act, &p);
+  if (st != M3_OK) return st;
+  if (p.ws_bytes > (size_t)M3SCAN_NOALLOC_SCRATCH_BYTES) return M3_ERR_WORKSPACE;
+  void* ws = nullptr;
+  if ((size_t)p.B * p.T * p.D > 0) {
+    st = noalloc_scratch(&ws);
+    if (st != M3_OK) return st;
+  }
+  return m3scan_bwd(dims, act, x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D, ckpt,
+                    d_gated, d_x, d_delta_raw, dz, du_dbg, dB, dC, d_conv_w, d_conv_b, d_dt_bias,
+                    d_a_log, dD, ws, (size_t)M3SCAN_NOALLOC_SCRATCH_BYTES, stream);
 }
 
 }  // extern "C"
