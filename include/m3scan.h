@@ -72,7 +72,9 @@ typedef enum {
 
 typedef struct {
     int64_t batch, seq_len, d_inner, d_state, d_conv;
-    /* Checkpoint interval K in steps (1..64); 0 = library default (16). */
+    /* Checkpoint interval K in steps; 0 = library default (8).  At most 64,
+       and small enough for the backward's shared memory (32 for bf16
+       activations, 28 for f32); larger values give M3_ERR_UNSUPPORTED. */
     int64_t chunk;
     /* Number of time segments scanned in parallel (each segment is a run of
        whole chunks); 0 = chosen from the shape and the current device. */
@@ -103,9 +105,9 @@ m3_status m3scan_plan(const m3_dims* dims, m3_dtype act, m3_plan* plan);
 
 /*
  * Forward.  Writes gated (and y_dbg = y when non-NULL) and the chunk
- * checkpoints ckpt that m3scan_bwd reads.  Activation pointers must be
- * 16-byte aligned; float32 pointers 4-byte aligned; workspace 256-byte
- * aligned with workspace_bytes >= plan.workspace_bytes.
+ * checkpoints ckpt that m3scan_bwd reads.  Activation pointers and ckpt
+ * must be 16-byte aligned; the other float32 pointers 4-byte aligned;
+ * workspace 256-byte aligned with workspace_bytes >= plan.workspace_bytes.
  */
 m3_status m3scan_fwd(const m3_dims* dims, m3_dtype act,
                      const void* x, const void* delta_raw, const void* z,

@@ -43,13 +43,15 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[M3SCAN_NOALLOC_
 
 namespace {
 
-constexpr int NS = 16;      // d_state lanes per channel
-constexpr int WC = 4;       // conv taps
-constexpr int G = 64;       // channels (= threads) per block
-constexpr int NW = G / 32;  // warps per block
-constexpr int KMAX = 64;    // largest chunk (the backward may allow less)
-constexpr int KDEF = 16;    // default chunk
-constexpr int NPART = 24;   // per-channel parameter partials (23 used)
+constexpr int NS = 16;        // d_state lanes per channel
+constexpr int WC = 4;         // conv taps
+constexpr int GF = 128;       // forward: channels (= threads) per block
+constexpr int GB = 64;        // backward: channels (= threads) per block
+constexpr int NWB = GB / 32;  // backward warps per block
+constexpr int TT = 32;        // forward / aggregate staging tile (steps)
+constexpr int KMAX = 64;      // largest chunk (the backward may allow less)
+constexpr int KDEF = 8;       // default chunk
+constexpr int NPART = 24;     // per-channel parameter partials (23 used)
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
 
@@ -62,14 +64,30 @@ __device__ __forceinline__ float ex2(float v) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
   return r;
 }
-
-__device__ __forceinline__ float sigmoid_f(float v) {
-  return __frcp_rn(1.0f + __expf(-v));
+__device__ __forceinline__ float rcp_a(float v) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
+  return r;
 }
+__device__ __forceinline__ float lg2_a(float v) {
+  float r;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
+  return r;
+}
+__device__ __forceinline__ float2 ex2x2(float2 v) { return make_float2(ex2(v.x), ex2(v.y)); }
+__device__ __forceinline__ float2 f2b(float v) { return make_float2(v, v); }
 
-// log(1 + e^v) = max(v, 0) + log1p(e^-|v|)
+// 1 / (1 + e^-v)
+__device__ __forceinline__ float sigmoid_f(float v) { return rcp_a(1.0f + ex2(-v * LOG2E)); }
+
+// log(1 + e^v) = max(v, 0) + log1p(e^-|v|); log1p(e) for e in (0, 1] from
+// the series e - e^2/2 + e^3/3 below 2^-6 (truncation < e^3/4 relative),
+// else log2(1 + e) ln 2.
 __device__ __forceinline__ float softplus_f(float v) {
-  return fmaxf(v, 0.0f) + log1pf(__expf(-fabsf(v)));
+  const float e = ex2(-fabsf(v) * LOG2E);
+  const float series = e * fmaf(e, fmaf(e, 0.33333334f, -0.5f), 1.0f);
+  const float lg = lg2_a(1.0f + e) * LN2;
+  return fmaxf(v, 0.0f) + (e < 0.015625f ? series : lg);
 }
 
 template <typename T> struct Act;
@@ -97,52 +115,38 @@ template <int N> __device__ __forceinline__ void cp_async_wait() {
 }
 
 // Stage rows [t_first, t_first + rows) x channels [d0, d0 + G) of a
-// [B, T, D] activation tensor into dst[rows][G]; out-of-range rows and
-// channels read as zero.
-template <typename T>
-__device__ __forceinline__ void stage_act(T* dst, const T* src, int b, int t_first, int rows,
-                                          int T_, int D, int d0, int tid) {
+// [B, T_, D] tensor of element type T into dst[rows][G]; rows outside
+// [0, t_limit) and channels >= D read as zero.  NT threads cooperate.
+template <typename T, int G, int NT>
+__device__ __forceinline__ void stage_rows(T* dst, const T* src, int b, int t_first, int rows,
+                                           int T_, int t_limit, int D, int d0, int tid) {
   constexpr int EPC = 16 / sizeof(T);
   constexpr int CPR = G / EPC;
   const int n = rows * CPR;
-  for (int i = tid; i < n; i += G) {
+  for (int i = tid; i < n; i += NT) {
     const int r = i / CPR, cc = i - r * CPR;
     const int t = t_first + r, dd = d0 + cc * EPC;
-    const bool ok = (t >= 0) && (t < T_) && (dd < D);
+    const bool ok = (t >= 0) && (t < t_limit) && (dd < D);
     const T* g = ok ? src + ((size_t)b * T_ + t) * D + dd : src;
     cp_async16(dst + r * G + cc * EPC, g, ok);
   }
 }
 
-// Stage rows [t_first, t_first + rows) of a [B, T, 16] tensor into dst[rows][16].
-template <typename T>
+// Stage rows [t_first, t_first + rows) of a [B, T_, 16] tensor into
+// dst[rows][16]; rows outside [0, t_limit) read as zero.
+template <typename T, int NT>
 __device__ __forceinline__ void stage_bc(T* dst, const T* src, int b, int t_first, int rows,
-                                         int T_, int tid) {
-  constexpr int CPR = NS * sizeof(T) / 16;
+                                         int T_, int t_limit, int tid) {
+  constexpr int EPC = 16 / sizeof(T);
+  constexpr int CPR = NS / EPC;
   const int n = rows * CPR;
-  for (int i = tid; i < n; i += G) {
+  for (int i = tid; i < n; i += NT) {
     const int r = i / CPR, cc = i - r * CPR;
     const int t = t_first + r;
-    const bool ok = (t >= 0) && (t < T_);
-    const T* g = ok ? src + ((size_t)b * T_ + t) * NS + cc * (16 / sizeof(T)) : src;
-    cp_async16(dst + r * NS + cc * (16 / sizeof(T)), g, ok);
+    const bool ok = (t >= 0) && (t < t_limit);
+    const T* g = ok ? src + ((size_t)b * T_ + t) * NS + cc * EPC : src;
+    cp_async16(dst + r * NS + cc * EPC, g, ok);
   }
-}
-
-// Sum of v[lane'] over all lanes lane' of the warp, for value index = lane:
-// a butterfly reduce-scatter (31 shuffles).
-__device__ __forceinline__ float warp_reduce_scatter32(float (&v)[32], int lane) {
-#pragma unroll
-  for (int half = 16; half >= 1; half >>= 1) {
-    const bool up = (lane & half) != 0;
-#pragma unroll
-    for (int i = 0; i < half; ++i) {
-      const float send = up ? v[i] : v[i + half];
-      const float keep = up ? v[i + half] : v[i];
-      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, half);
-    }
-  }
-  return v[0];
 }
 
 // ---------------------------------------------------------------------------
@@ -175,98 +179,83 @@ struct BwdArgs {
   int accumulate;
 };
 
-// Forward shared memory: two tile buffers {x, delta_raw, z: [K][G] act;
-// B, C: [K][16] act} and the current chunk's B, C as float [K][16].
+// Forward shared memory: two staging buffers {x, delta_raw, z: [TT][GF]
+// act; B, C: [TT][16] act} and B, C of the current tile as float [TT][16].
 struct FwdSmem {
   size_t x, dr, z, Bt, Ct, tile, fB, fC, total;
 };
-__host__ __device__ inline FwdSmem fwd_smem(int K, int es) {
+__host__ __device__ inline FwdSmem fwd_smem(int es) {
   FwdSmem s;
   s.x = 0;
-  s.dr = s.x + align_up((size_t)K * G * es, 128);
-  s.z = s.dr + align_up((size_t)K * G * es, 128);
-  s.Bt = s.z + align_up((size_t)K * G * es, 128);
-  s.Ct = s.Bt + align_up((size_t)K * NS * es, 128);
-  s.tile = s.Ct + align_up((size_t)K * NS * es, 128);
+  s.dr = s.x + align_up((size_t)TT * GF * es, 128);
+  s.z = s.dr + align_up((size_t)TT * GF * es, 128);
+  s.Bt = s.z + align_up((size_t)TT * GF * es, 128);
+  s.Ct = s.Bt + align_up((size_t)TT * NS * es, 128);
+  s.tile = s.Ct + align_up((size_t)TT * NS * es, 128);
   s.fB = 2 * s.tile;
-  s.fC = s.fB + align_up((size_t)K * NS * 4, 128);
-  s.total = s.fC + align_up((size_t)K * NS * 4, 128);
+  s.fC = s.fB + (size_t)TT * NS * 4;
+  s.total = s.fC + (size_t)TT * NS * 4;
   return s;
 }
 
-// Backward shared memory: two tile buffers {x: [K+3][G] (three halo rows
-// before the chunk), delta_raw, z, d_gated: [K][G]; B, C: [K][16]}, float B
-// and C of the current chunk, the recomputed states hist[K][G][16] f32, the
-// per-step scalars (u, delta, conv pre-activation, y) [K][G] float4, and the
-// per-warp dB/dC sums red[K][NW][32].
+// Backward shared memory: two staging buffers {x: [K+3][GB] (three halo rows
+// before the chunk), delta_raw, z, d_gated: [K][GB] act; B, C: [K][16] act;
+// the chunk's start state ck: [16][GB] f32}; B and C of the current chunk as
+// float; the recomputed states hist[K+1][GB][16] f32 (row 0 = chunk start);
+// per-step scalars scal[K][GB] float4 (sigmoid(c), delta, c, y); per-warp
+// dB/dC sums red[K][NWB][32].
 struct BwdSmem {
-  size_t x, dr, z, dg, Bt, Ct, tile, fB, fC, hist, scal, red, total;
+  size_t x, dr, z, dg, Bt, Ct, ck, tile, fB, fC, hist, scal, red, total;
 };
 __host__ __device__ inline BwdSmem bwd_smem(int K, int es) {
   BwdSmem s;
   s.x = 0;
-  s.dr = s.x + align_up((size_t)(K + 3) * G * es, 128);
-  s.z = s.dr + align_up((size_t)K * G * es, 128);
-  s.dg = s.z + align_up((size_t)K * G * es, 128);
-  s.Bt = s.dg + align_up((size_t)K * G * es, 128);
+  s.dr = s.x + align_up((size_t)(K + 3) * GB * es, 128);
+  s.z = s.dr + align_up((size_t)K * GB * es, 128);
+  s.dg = s.z + align_up((size_t)K * GB * es, 128);
+  s.Bt = s.dg + align_up((size_t)K * GB * es, 128);
   s.Ct = s.Bt + align_up((size_t)K * NS * es, 128);
-  s.tile = s.Ct + align_up((size_t)K * NS * es, 128);
+  s.ck = s.Ct + align_up((size_t)K * NS * es, 128);
+  s.tile = s.ck + (size_t)NS * GB * 4;
   s.fB = 2 * s.tile;
-  s.fC = s.fB + align_up((size_t)K * NS * 4, 128);
-  s.hist = s.fC + align_up((size_t)K * NS * 4, 128);
-  s.scal = s.hist + (size_t)K * G * NS * 4;
-  s.red = s.scal + (size_t)K * G * 16;
-  s.total = s.red + (size_t)K * NW * 32 * 4;
+  s.fC = s.fB + (size_t)K * NS * 4;
+  s.hist = s.fC + (size_t)K * NS * 4;
+  s.scal = s.hist + (size_t)(K + 1) * GB * NS * 4;
+  s.red = s.scal + (size_t)K * GB * 16;
+  s.total = s.red + (size_t)K * NWB * 32 * 4;
   return s;
 }
 
 // Backward aggregate shared memory: two buffers {delta_raw, z, d_gated:
-// [K][G]; C: [K][16]} and float C.
+// [TT][GB]; C: [TT][16]} and float C.
 struct AggSmem {
   size_t dr, z, dg, Ct, tile, fC, total;
 };
-__host__ __device__ inline AggSmem agg_smem(int K, int es) {
+__host__ __device__ inline AggSmem agg_smem(int es) {
   AggSmem s;
   s.dr = 0;
-  s.z = s.dr + align_up((size_t)K * G * es, 128);
-  s.dg = s.z + align_up((size_t)K * G * es, 128);
-  s.Ct = s.dg + align_up((size_t)K * G * es, 128);
-  s.tile = s.Ct + align_up((size_t)K * NS * es, 128);
+  s.z = s.dr + align_up((size_t)TT * GB * es, 128);
+  s.dg = s.z + align_up((size_t)TT * GB * es, 128);
+  s.Ct = s.dg + align_up((size_t)TT * GB * es, 128);
+  s.tile = s.Ct + align_up((size_t)TT * NS * es, 128);
   s.fC = 2 * s.tile;
-  s.total = s.fC + align_up((size_t)K * NS * 4, 128);
+  s.total = s.fC + (size_t)TT * NS * 4;
   return s;
 }
 
-// Per-channel parameters: A2 = A * log2(e) with A = -exp(a_log).
-struct ChanParams {
-  float A2[NS];
-  float w[WC];
-  float cb, dtb, Dd;
-};
-__device__ __forceinline__ void load_params(ChanParams& p, const float* conv_w, const float* conv_b,
-                                            const float* dt_bias, const float* a_log,
-                                            const float* Dp, int d, bool active) {
-#pragma unroll
-  for (int n = 0; n < NS; ++n) p.A2[n] = active ? -expf(a_log[(size_t)d * NS + n]) * LOG2E : 0.0f;
-#pragma unroll
-  for (int k = 0; k < WC; ++k) p.w[k] = active ? conv_w[(size_t)d * WC + k] : 0.0f;
-  p.cb = active ? conv_b[d] : 0.0f;
-  p.dtb = active ? dt_bias[d] : 0.0f;
-  p.Dd = active ? Dp[d] : 0.0f;
-}
-
 // ---------------------------------------------------------------------------
-// forward: FINAL = rerun from the true segment start, write gated (+y) and
-// the chunk checkpoints; !FINAL = local pass from zero over segments
-// 0..S-2 writing only the end state and the summed step size.
+// forward: FINAL = run each segment from its true start state, write gated
+// (+y) and a checkpoint every K steps; !FINAL = local pass from zero over
+// segments 0..S-2 writing only the end state and the summed step size.
+// Lanes are handled in pairs with packed f32x2 arithmetic.
 // ---------------------------------------------------------------------------
 
 template <typename T, bool FINAL>
-__global__ void __launch_bounds__(G) m3_fwd_kernel(FwdArgs a) {
+__global__ void __launch_bounds__(GF) m3_fwd_kernel(FwdArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   const Geo g = a.g;
   const int tid = threadIdx.x;
-  const int d0 = blockIdx.x * G;
+  const int d0 = blockIdx.x * GF;
   const int s = blockIdx.y;
   const int b = blockIdx.z;
   const int d = d0 + tid;
@@ -274,8 +263,8 @@ __global__ void __launch_bounds__(G) m3_fwd_kernel(FwdArgs a) {
   const int c_begin = s * g.m;
   const int c_end = min(c_begin + g.m, g.nc);
   const int t_begin = c_begin * g.K;
-  const int K = g.K;
-  const FwdSmem L = fwd_smem(K, sizeof(T));
+  const int t_end = min(c_end * g.K, g.T);
+  const FwdSmem L = fwd_smem(sizeof(T));
   const T* xg = static_cast<const T*>(a.x);
   const T* drg = static_cast<const T*>(a.dr);
   const T* zg = static_cast<const T*>(a.z);
@@ -284,18 +273,31 @@ __global__ void __launch_bounds__(G) m3_fwd_kernel(FwdArgs a) {
   float* fB = reinterpret_cast<float*>(smem + L.fB);
   float* fC = reinterpret_cast<float*>(smem + L.fC);
 
-  ChanParams P;
-  load_params(P, a.conv_w, a.conv_b, a.dt_bias, a.a_log, a.Dp, d, active);
-
-  float h[NS];
+  float2 a2[NS / 2];  // A log2(e) for lanes (2i, 2i+1)
 #pragma unroll
-  for (int n = 0; n < NS; ++n)
-    h[n] = (FINAL && s > 0 && active)
-               ? a.ckpt[(((size_t)b * g.nc + c_begin) * NS + n) * g.D + d]
-               : 0.0f;
+  for (int i = 0; i < NS / 2; ++i) {
+    a2[i].x = active ? -expf(a.a_log[(size_t)d * NS + 2 * i]) * LOG2E : 0.f;
+    a2[i].y = active ? -expf(a.a_log[(size_t)d * NS + 2 * i + 1]) * LOG2E : 0.f;
+  }
+  float w[WC];
+#pragma unroll
+  for (int k = 0; k < WC; ++k) w[k] = active ? a.conv_w[(size_t)d * WC + k] : 0.f;
+  const float cb = active ? a.conv_b[d] : 0.f;
+  const float dtb = active ? a.dt_bias[d] : 0.f;
+  const float Dd = active ? a.Dp[d] : 0.f;
 
-  // conv window x[t-3], x[t-2], x[t-1]
-  float xm3 = 0.f, xm2 = 0.f, xm1 = 0.f;
+  float2 h[NS / 2];
+#pragma unroll
+  for (int i = 0; i < NS / 2; ++i) {
+    if (FINAL && s > 0 && active) {
+      const float* ck = a.ckpt + (((size_t)b * g.nc + c_begin) * NS + 2 * i) * g.D + d;
+      h[i] = make_float2(ck[0], ck[g.D]);
+    } else {
+      h[i] = make_float2(0.f, 0.f);
+    }
+  }
+
+  float xm3 = 0.f, xm2 = 0.f, xm1 = 0.f;  // conv window x[t-3], x[t-2], x[t-1]
   if (active) {
     if (t_begin >= 3) xm3 = Act<T>::ld(xg + ((size_t)b * g.T + t_begin - 3) * g.D + d);
     if (t_begin >= 2) xm2 = Act<T>::ld(xg + ((size_t)b * g.T + t_begin - 2) * g.D + d);
@@ -303,91 +305,111 @@ __global__ void __launch_bounds__(G) m3_fwd_kernel(FwdArgs a) {
   }
   float sdelta = 0.f;
 
-  auto stage = [&](int c, int buf) {
+  auto stage = [&](int t0, int buf) {
     unsigned char* base = smem + (size_t)buf * L.tile;
-    const int t0 = c * K;
-    stage_act<T>(reinterpret_cast<T*>(base + L.x), xg, b, t0, K, g.T, g.D, d0, tid);
-    stage_act<T>(reinterpret_cast<T*>(base + L.dr), drg, b, t0, K, g.T, g.D, d0, tid);
-    stage_bc<T>(reinterpret_cast<T*>(base + L.Bt), Bg, b, t0, K, g.T, tid);
+    stage_rows<T, GF, GF>(reinterpret_cast<T*>(base + L.x), xg, b, t0, TT, g.T, t_end, g.D, d0, tid);
+    stage_rows<T, GF, GF>(reinterpret_cast<T*>(base + L.dr), drg, b, t0, TT, g.T, t_end, g.D, d0, tid);
+    stage_bc<T, GF>(reinterpret_cast<T*>(base + L.Bt), Bg, b, t0, TT, g.T, t_end, tid);
     if (FINAL) {
-      stage_act<T>(reinterpret_cast<T*>(base + L.z), zg, b, t0, K, g.T, g.D, d0, tid);
-      stage_bc<T>(reinterpret_cast<T*>(base + L.Ct), Cg, b, t0, K, g.T, tid);
+      stage_rows<T, GF, GF>(reinterpret_cast<T*>(base + L.z), zg, b, t0, TT, g.T, t_end, g.D, d0, tid);
+      stage_bc<T, GF>(reinterpret_cast<T*>(base + L.Ct), Cg, b, t0, TT, g.T, t_end, tid);
     }
     cp_async_commit();
   };
 
-  stage(c_begin, 0);
-  for (int c = c_begin; c < c_end; ++c) {
-    const int buf = (c - c_begin) & 1;
-    if (c + 1 < c_end) {
-      stage(c + 1, buf ^ 1);
+  int kc = 0;  // steps left until the next checkpoint
+  stage(t_begin, 0);
+  for (int t0 = t_begin, it = 0; t0 < t_end; t0 += TT, ++it) {
+    const int buf = it & 1;
+    if (t0 + TT < t_end) {
+      stage(t0 + TT, buf ^ 1);
       cp_async_wait<1>();
     } else {
       cp_async_wait<0>();
     }
     __syncthreads();
     const unsigned char* base = smem + (size_t)buf * L.tile;
-    const T* Bt = reinterpret_cast<const T*>(base + L.Bt);
-    const T* Ct = reinterpret_cast<const T*>(base + L.Ct);
-    for (int i = tid; i < K * NS; i += G) {
-      fB[i] = Act<T>::ld(Bt + i);
-      if (FINAL) fC[i] = Act<T>::ld(Ct + i);
+    {
+      const T* Bt = reinterpret_cast<const T*>(base + L.Bt);
+      const T* Ct = reinterpret_cast<const T*>(base + L.Ct);
+      for (int i = tid; i < TT * NS; i += GF) {
+        fB[i] = Act<T>::ld(Bt + i);
+        if (FINAL) fC[i] = Act<T>::ld(Ct + i);
+      }
     }
     __syncthreads();
-
-    if (FINAL && active && (c > c_begin || s == 0)) {
-#pragma unroll
-      for (int n = 0; n < NS; ++n) a.ckpt[(((size_t)b * g.nc + c) * NS + n) * g.D + d] = h[n];
-    }
     const T* xt = reinterpret_cast<const T*>(base + L.x);
     const T* drt = reinterpret_cast<const T*>(base + L.dr);
     const T* zt = reinterpret_cast<const T*>(base + L.z);
-    const int steps = min(K, g.T - c * K);
+    const int steps = min(TT, t_end - t0);
     for (int j = 0; j < steps; ++j) {
-      const float xv = Act<T>::ld(xt + j * G + tid);
-      const float cpre = fmaf(P.w[0], xm3, fmaf(P.w[1], xm2, fmaf(P.w[2], xm1, fmaf(P.w[3], xv, P.cb))));
+      if (FINAL) {
+        if (kc == 0) {
+          const int t = t0 + j;
+          if (active && (t > t_begin || s == 0)) {
+            float* ck = a.ckpt + (((size_t)b * g.nc + t / g.K) * NS) * g.D + d;
+#pragma unroll
+            for (int i = 0; i < NS / 2; ++i) {
+              ck[(size_t)(2 * i) * g.D] = h[i].x;
+              ck[(size_t)(2 * i + 1) * g.D] = h[i].y;
+            }
+          }
+          kc = g.K;
+        }
+        --kc;
+      }
+      const float xv = Act<T>::ld(xt + j * GF + tid);
+      const float cpre = fmaf(w[0], xm3, fmaf(w[1], xm2, fmaf(w[2], xm1, fmaf(w[3], xv, cb))));
       xm3 = xm2;
       xm2 = xm1;
       xm1 = xv;
       const float u = cpre * sigmoid_f(cpre);
-      const float delta = softplus_f(Act<T>::ld(drt + j * G + tid) + P.dtb);
-      const float du = delta * u;
+      const float delta = softplus_f(Act<T>::ld(drt + j * GF + tid) + dtb);
+      const float2 dl2 = f2b(delta);
+      const float2 du2 = f2b(delta * u);
       const float4* B4 = reinterpret_cast<const float4*>(fB + j * NS);
-      float Bv[NS];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float4 v = B4[q];
-        Bv[4 * q] = v.x; Bv[4 * q + 1] = v.y; Bv[4 * q + 2] = v.z; Bv[4 * q + 3] = v.w;
-      }
-#pragma unroll
-      for (int n = 0; n < NS; ++n) h[n] = fmaf(ex2(delta * P.A2[n]), h[n], du * Bv[n]);
       if (FINAL) {
         const float4* C4 = reinterpret_cast<const float4*>(fC + j * NS);
-        float y0 = 0.f, y1 = 0.f, y2 = 0.f, y3 = 0.f;
+        float2 y01 = make_float2(0.f, 0.f), y23 = make_float2(0.f, 0.f);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const float4 v = C4[q];
-          y0 = fmaf(v.x, h[4 * q], y0);
-          y1 = fmaf(v.y, h[4 * q + 1], y1);
-          y2 = fmaf(v.z, h[4 * q + 2], y2);
-          y3 = fmaf(v.w, h[4 * q + 3], y3);
+          const float4 bv = B4[q];
+          const float4 cv = C4[q];
+          const float2 dA0 = ex2x2(__fmul2_rn(dl2, a2[2 * q]));
+          const float2 dA1 = ex2x2(__fmul2_rn(dl2, a2[2 * q + 1]));
+          h[2 * q] = __ffma2_rn(dA0, h[2 * q], __fmul2_rn(du2, make_float2(bv.x, bv.y)));
+          h[2 * q + 1] = __ffma2_rn(dA1, h[2 * q + 1], __fmul2_rn(du2, make_float2(bv.z, bv.w)));
+          y01 = __ffma2_rn(make_float2(cv.x, cv.y), h[2 * q], y01);
+          y23 = __ffma2_rn(make_float2(cv.z, cv.w), h[2 * q + 1], y23);
         }
-        const float y = fmaf(P.Dd, u, (y0 + y1) + (y2 + y3));
-        const float zv = Act<T>::ld(zt + j * G + tid);
+        const float y = fmaf(Dd, u, (y01.x + y01.y) + (y23.x + y23.y));
+        const float zv = Act<T>::ld(zt + j * GF + tid);
         if (active) {
-          const size_t i = ((size_t)b * g.T + c * K + j) * g.D + d;
+          const size_t i = ((size_t)b * g.T + t0 + j) * g.D + d;
           Act<T>::st(static_cast<T*>(a.gated) + i, y * zv * sigmoid_f(zv));
           if (a.y_dbg) Act<T>::st(static_cast<T*>(a.y_dbg) + i, y);
         }
       } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float4 bv = B4[q];
+          const float2 dA0 = ex2x2(__fmul2_rn(dl2, a2[2 * q]));
+          const float2 dA1 = ex2x2(__fmul2_rn(dl2, a2[2 * q + 1]));
+          h[2 * q] = __ffma2_rn(dA0, h[2 * q], __fmul2_rn(du2, make_float2(bv.x, bv.y)));
+          h[2 * q + 1] = __ffma2_rn(dA1, h[2 * q + 1], __fmul2_rn(du2, make_float2(bv.z, bv.w)));
+        }
         sdelta += delta;
       }
     }
     __syncthreads();
   }
   if (!FINAL && active) {
+    float* ah = a.agg_h + (((size_t)b * g.S + s) * NS) * g.D + d;
 #pragma unroll
-    for (int n = 0; n < NS; ++n) a.agg_h[(((size_t)b * g.S + s) * NS + n) * g.D + d] = h[n];
+    for (int i = 0; i < NS / 2; ++i) {
+      ah[(size_t)(2 * i) * g.D] = h[i].x;
+      ah[(size_t)(2 * i + 1) * g.D] = h[i].y;
+    }
     a.agg_s[((size_t)b * g.S + s) * g.D + d] = sdelta;
   }
 }
@@ -422,71 +444,80 @@ __global__ void m3_fwd_carry_kernel(FwdArgs a) {
 // ---------------------------------------------------------------------------
 
 template <typename T>
-__global__ void __launch_bounds__(G) m3_bwd_agg_kernel(BwdArgs a) {
+__global__ void __launch_bounds__(GB) m3_bwd_agg_kernel(BwdArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   const Geo g = a.g;
   const int tid = threadIdx.x;
-  const int d0 = blockIdx.x * G;
+  const int d0 = blockIdx.x * GB;
   const int s = blockIdx.y + 1;
   const int b = blockIdx.z;
   const int d = d0 + tid;
   const bool active = d < g.D;
-  const int c_begin = s * g.m;
-  const int c_end = min(c_begin + g.m, g.nc);
-  const int K = g.K;
-  const AggSmem L = agg_smem(K, sizeof(T));
+  const int t_begin = s * g.m * g.K;
+  const int t_end = min((s + 1) * g.m * g.K, g.T);
+  const AggSmem L = agg_smem(sizeof(T));
   float* fC = reinterpret_cast<float*>(smem + L.fC);
 
-  float A2[NS];
+  float2 a2[NS / 2];
 #pragma unroll
-  for (int n = 0; n < NS; ++n) A2[n] = active ? -expf(a.a_log[(size_t)d * NS + n]) * LOG2E : 0.f;
+  for (int i = 0; i < NS / 2; ++i) {
+    a2[i].x = active ? -expf(a.a_log[(size_t)d * NS + 2 * i]) * LOG2E : 0.f;
+    a2[i].y = active ? -expf(a.a_log[(size_t)d * NS + 2 * i + 1]) * LOG2E : 0.f;
+  }
   const float dtb = active ? a.dt_bias[d] : 0.f;
-  float carry[NS];
+  float2 carry[NS / 2];
 #pragma unroll
-  for (int n = 0; n < NS; ++n) carry[n] = 0.f;
+  for (int i = 0; i < NS / 2; ++i) carry[i] = make_float2(0.f, 0.f);
   float sdelta = 0.f;
 
-  auto stage = [&](int c, int buf) {
+  const int ntiles = (t_end - t_begin + TT - 1) / TT;
+  auto tile_start = [&](int i) { return max(t_begin, t_end - (i + 1) * TT); };
+  auto stage = [&](int i, int buf) {
     unsigned char* base = smem + (size_t)buf * L.tile;
-    const int t0 = c * K;
-    stage_act<T>(reinterpret_cast<T*>(base + L.dr), static_cast<const T*>(a.dr), b, t0, K, g.T, g.D, d0, tid);
-    stage_act<T>(reinterpret_cast<T*>(base + L.z), static_cast<const T*>(a.z), b, t0, K, g.T, g.D, d0, tid);
-    stage_act<T>(reinterpret_cast<T*>(base + L.dg), static_cast<const T*>(a.dg), b, t0, K, g.T, g.D, d0, tid);
-    stage_bc<T>(reinterpret_cast<T*>(base + L.Ct), static_cast<const T*>(a.Cm), b, t0, K, g.T, tid);
+    const int t0 = tile_start(i);
+    const int rows = (t_end - i * TT) - t0;
+    stage_rows<T, GB, GB>(reinterpret_cast<T*>(base + L.dr), static_cast<const T*>(a.dr), b, t0, rows, g.T, g.T, g.D, d0, tid);
+    stage_rows<T, GB, GB>(reinterpret_cast<T*>(base + L.z), static_cast<const T*>(a.z), b, t0, rows, g.T, g.T, g.D, d0, tid);
+    stage_rows<T, GB, GB>(reinterpret_cast<T*>(base + L.dg), static_cast<const T*>(a.dg), b, t0, rows, g.T, g.T, g.D, d0, tid);
+    stage_bc<T, GB>(reinterpret_cast<T*>(base + L.Ct), static_cast<const T*>(a.Cm), b, t0, rows, g.T, g.T, tid);
     cp_async_commit();
   };
 
-  stage(c_end - 1, 0);
-  for (int c = c_end - 1; c >= c_begin; --c) {
-    const int buf = (c_end - 1 - c) & 1;
-    if (c - 1 >= c_begin) {
-      stage(c - 1, buf ^ 1);
+  stage(0, 0);
+  for (int i = 0; i < ntiles; ++i) {
+    const int buf = i & 1;
+    if (i + 1 < ntiles) {
+      stage(i + 1, buf ^ 1);
       cp_async_wait<1>();
     } else {
       cp_async_wait<0>();
     }
     __syncthreads();
     const unsigned char* base = smem + (size_t)buf * L.tile;
-    const T* Ct = reinterpret_cast<const T*>(base + L.Ct);
-    for (int i = tid; i < K * NS; i += G) fC[i] = Act<T>::ld(Ct + i);
+    const int t0 = tile_start(i);
+    const int steps = (t_end - i * TT) - t0;
+    {
+      const T* Ct = reinterpret_cast<const T*>(base + L.Ct);
+      for (int k = tid; k < steps * NS; k += GB) fC[k] = Act<T>::ld(Ct + k);
+    }
     __syncthreads();
     const T* drt = reinterpret_cast<const T*>(base + L.dr);
     const T* zt = reinterpret_cast<const T*>(base + L.z);
     const T* dgt = reinterpret_cast<const T*>(base + L.dg);
-    const int steps = min(K, g.T - c * K);
     for (int j = steps - 1; j >= 0; --j) {
-      const float zv = Act<T>::ld(zt + j * G + tid);
-      const float dy = Act<T>::ld(dgt + j * G + tid) * zv * sigmoid_f(zv);
-      const float delta = softplus_f(Act<T>::ld(drt + j * G + tid) + dtb);
+      const float zv = Act<T>::ld(zt + j * GB + tid);
+      const float2 dy2 = f2b(Act<T>::ld(dgt + j * GB + tid) * zv * sigmoid_f(zv));
+      const float delta = softplus_f(Act<T>::ld(drt + j * GB + tid) + dtb);
+      const float2 dl2 = f2b(delta);
       sdelta += delta;
       const float4* C4 = reinterpret_cast<const float4*>(fC + j * NS);
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const float4 v = C4[q];
-        carry[4 * q + 0] = ex2(delta * A2[4 * q + 0]) * fmaf(dy, v.x, carry[4 * q + 0]);
-        carry[4 * q + 1] = ex2(delta * A2[4 * q + 1]) * fmaf(dy, v.y, carry[4 * q + 1]);
-        carry[4 * q + 2] = ex2(delta * A2[4 * q + 2]) * fmaf(dy, v.z, carry[4 * q + 2]);
-        carry[4 * q + 3] = ex2(delta * A2[4 * q + 3]) * fmaf(dy, v.w, carry[4 * q + 3]);
+        carry[2 * q] = __fmul2_rn(ex2x2(__fmul2_rn(dl2, a2[2 * q])),
+                                  __ffma2_rn(dy2, make_float2(v.x, v.y), carry[2 * q]));
+        carry[2 * q + 1] = __fmul2_rn(ex2x2(__fmul2_rn(dl2, a2[2 * q + 1])),
+                                      __ffma2_rn(dy2, make_float2(v.z, v.w), carry[2 * q + 1]));
       }
     }
     __syncthreads();
@@ -494,7 +525,10 @@ __global__ void __launch_bounds__(G) m3_bwd_agg_kernel(BwdArgs a) {
   if (active) {
     const size_t bs = (size_t)b * g.S + s;
 #pragma unroll
-    for (int n = 0; n < NS; ++n) a.q[(bs * NS + n) * g.D + d] = carry[n];
+    for (int i = 0; i < NS / 2; ++i) {
+      a.q[(bs * NS + 2 * i) * g.D + d] = carry[i].x;
+      a.q[(bs * NS + 2 * i + 1) * g.D + d] = carry[i].y;
+    }
     a.sd[bs * g.D + d] = sdelta;
   }
 }
@@ -520,16 +554,47 @@ __global__ void m3_bwd_carry_kernel(BwdArgs a) {
 
 // ---------------------------------------------------------------------------
 // backward main kernel
+//
+// Each thread keeps its 16 state lanes in 4 quads whose order is rotated by
+// the lane's two low bits: register quad qs holds state quad qs ^ (lane & 3).
+// The dB/dC sum over the warp's 32 channels then starts with two
+// butterfly levels that need no selects (partners hold the same state lane
+// in the same register), as the reduce-scatter below relies on.
 // ---------------------------------------------------------------------------
 
+// Sum over the 32 lanes of v[0..15] (v[s] holds state lane
+// 4 * ((s >> 2) ^ (lane & 3)) + (s & 3)); returns the total for state lane
+// 4 * (lane & 3) + 2 * ((lane >> 3) & 1) + ((lane >> 2) & 1).
+__device__ __forceinline__ float warp_sum16_rotated(float (&v)[NS], int lane) {
+#pragma unroll
+  for (int s = 0; s < 8; ++s) v[s] += __shfl_xor_sync(0xffffffffu, v[s + 8], 2);
+#pragma unroll
+  for (int s = 0; s < 4; ++s) v[s] += __shfl_xor_sync(0xffffffffu, v[s + 4], 1);
+  {
+    const bool up = (lane & 8) != 0;
+    const float s0 = up ? v[0] : v[2], s1 = up ? v[1] : v[3];
+    const float k0 = up ? v[2] : v[0], k1 = up ? v[3] : v[1];
+    v[0] = k0 + __shfl_xor_sync(0xffffffffu, s0, 8);
+    v[1] = k1 + __shfl_xor_sync(0xffffffffu, s1, 8);
+  }
+  {
+    const bool up = (lane & 4) != 0;
+    const float s0 = up ? v[0] : v[1];
+    const float k0 = up ? v[1] : v[0];
+    v[0] = k0 + __shfl_xor_sync(0xffffffffu, s0, 4);
+  }
+  return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 16);
+}
+
 template <typename T>
-__global__ void __launch_bounds__(G) m3_bwd_kernel(BwdArgs a) {
+__global__ void __launch_bounds__(GB) m3_bwd_kernel(BwdArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   const Geo g = a.g;
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
-  const int d0 = blockIdx.x * G;
+  const int rot = lane & 3;
+  const int d0 = blockIdx.x * GB;
   const int s = blockIdx.y;
   const int b = blockIdx.z;
   const int d = d0 + tid;
@@ -545,35 +610,58 @@ __global__ void __launch_bounds__(G) m3_bwd_kernel(BwdArgs a) {
   float4* hist = reinterpret_cast<float4*>(smem + L.hist);
   float4* scal = reinterpret_cast<float4*>(smem + L.scal);
   float* red = reinterpret_cast<float*>(smem + L.red);
-  const int swz = (tid >> 1) & 3;  // conflict-free float4 stores of 64-byte rows
+  const int swz = (tid >> 1) & 3;  // conflict-free float4 rows of 64 bytes
+  // state lane of register slot 2*i (pair i): quad (i >> 1) ^ rot, offset 2*(i & 1)
+  auto lane_of = [&](int i) { return 4 * ((i >> 1) ^ rot) + 2 * (i & 1); };
 
-  ChanParams P;
-  load_params(P, a.conv_w, a.conv_b, a.dt_bias, a.a_log, a.Dp, d, active);
+  float2 a2[NS / 2];
+  float w[WC];
+  float cb = 0.f, dtb = 0.f, Dd = 0.f;
+#pragma unroll
+  for (int i = 0; i < NS / 2; ++i) {
+    const int n = lane_of(i);
+    a2[i].x = active ? -expf(a.a_log[(size_t)d * NS + n]) * LOG2E : 0.f;
+    a2[i].y = active ? -expf(a.a_log[(size_t)d * NS + n + 1]) * LOG2E : 0.f;
+  }
+#pragma unroll
+  for (int k = 0; k < WC; ++k) w[k] = active ? a.conv_w[(size_t)d * WC + k] : 0.f;
+  if (active) {
+    cb = a.conv_b[d];
+    dtb = a.dt_bias[d];
+    Dd = a.Dp[d];
+  }
 
   // adjoint carry entering the segment's last step from the right:
-  // exp(delta_{t+1} A) * dh_{t+1}
-  float carry[NS];
+  // exp(delta_{t+1} A) dh_{t+1}
+  float2 carry[NS / 2];
 #pragma unroll
-  for (int n = 0; n < NS; ++n)
-    carry[n] = (g.S > 1 && active) ? a.gin[(((size_t)b * g.S + s) * NS + n) * g.D + d] : 0.f;
-
-  float dAp[NS];  // dL/dA per lane
+  for (int i = 0; i < NS / 2; ++i) {
+    carry[i] = make_float2(0.f, 0.f);
+    if (g.S > 1 && active) {
+      const float* gi = a.gin + (((size_t)b * g.S + s) * NS + lane_of(i)) * g.D + d;
+      carry[i] = make_float2(gi[0], gi[g.D]);
+    }
+  }
+  float2 dAp[NS / 2];  // dL/dA per lane
 #pragma unroll
-  for (int n = 0; n < NS; ++n) dAp[n] = 0.f;
+  for (int i = 0; i < NS / 2; ++i) dAp[i] = make_float2(0.f, 0.f);
   float dD_acc = 0.f, ddtb_acc = 0.f, dcb_acc = 0.f;
   float dcw[WC] = {0.f, 0.f, 0.f, 0.f};
-  float dc1 = 0.f, dc2 = 0.f, dc3 = 0.f;  // dc at t+1, t+2, t+3
+  float dc1 = 0.f, dc2 = 0.f, dc3 = 0.f;  // conv-input gradient at t+1, t+2, t+3
 
   const T* xg = static_cast<const T*>(a.x);
   auto stage = [&](int c, int buf) {
     unsigned char* base = smem + (size_t)buf * L.tile;
     const int t0 = c * K;
-    stage_act<T>(reinterpret_cast<T*>(base + L.x), xg, b, t0 - 3, K + 3, g.T, g.D, d0, tid);
-    stage_act<T>(reinterpret_cast<T*>(base + L.dr), static_cast<const T*>(a.dr), b, t0, K, g.T, g.D, d0, tid);
-    stage_act<T>(reinterpret_cast<T*>(base + L.z), static_cast<const T*>(a.z), b, t0, K, g.T, g.D, d0, tid);
-    stage_act<T>(reinterpret_cast<T*>(base + L.dg), static_cast<const T*>(a.dg), b, t0, K, g.T, g.D, d0, tid);
-    stage_bc<T>(reinterpret_cast<T*>(base + L.Bt), static_cast<const T*>(a.Bm), b, t0, K, g.T, tid);
-    stage_bc<T>(reinterpret_cast<T*>(base + L.Ct), static_cast<const T*>(a.Cm), b, t0, K, g.T, tid);
+    stage_rows<T, GB, GB>(reinterpret_cast<T*>(base + L.x), xg, b, t0 - 3, K + 3, g.T, g.T, g.D, d0, tid);
+    stage_rows<T, GB, GB>(reinterpret_cast<T*>(base + L.dr), static_cast<const T*>(a.dr), b, t0, K, g.T, g.T, g.D, d0, tid);
+    stage_rows<T, GB, GB>(reinterpret_cast<T*>(base + L.z), static_cast<const T*>(a.z), b, t0, K, g.T, g.T, g.D, d0, tid);
+    stage_rows<T, GB, GB>(reinterpret_cast<T*>(base + L.dg), static_cast<const T*>(a.dg), b, t0, K, g.T, g.T, g.D, d0, tid);
+    stage_bc<T, GB>(reinterpret_cast<T*>(base + L.Bt), static_cast<const T*>(a.Bm), b, t0, K, g.T, g.T, tid);
+    stage_bc<T, GB>(reinterpret_cast<T*>(base + L.Ct), static_cast<const T*>(a.Cm), b, t0, K, g.T, g.T, tid);
+    // chunk start state: 16 rows of GB floats from ckpt[b, c, :, d0:d0+GB]
+    stage_rows<float, GB, GB>(reinterpret_cast<float*>(base + L.ck), a.ckpt + ((size_t)b * g.nc + c) * NS * g.D,
+                              0, 0, NS, NS, NS, g.D, d0, tid);
     cp_async_commit();
   };
 
@@ -591,7 +679,7 @@ __global__ void __launch_bounds__(G) m3_bwd_kernel(BwdArgs a) {
     {
       const T* Bt = reinterpret_cast<const T*>(base + L.Bt);
       const T* Ct = reinterpret_cast<const T*>(base + L.Ct);
-      for (int i = tid; i < K * NS; i += G) {
+      for (int i = tid; i < K * NS; i += GB) {
         fB[i] = Act<T>::ld(Bt + i);
         fC[i] = Act<T>::ld(Ct + i);
       }
@@ -601,98 +689,125 @@ __global__ void __launch_bounds__(G) m3_bwd_kernel(BwdArgs a) {
     const T* drt = reinterpret_cast<const T*>(base + L.dr);
     const T* zt = reinterpret_cast<const T*>(base + L.z);
     const T* dgt = reinterpret_cast<const T*>(base + L.dg);
+    const float* ckt = reinterpret_cast<const float*>(base + L.ck);
     const int steps = min(K, g.T - c * K);
 
-    // ---- recompute the chunk forward from its checkpoint ----
+    // ---- recompute the chunk forward from its start state ----
     {
-      float h[NS];
+      float2 h[NS / 2];
 #pragma unroll
-      for (int n = 0; n < NS; ++n)
-        h[n] = active ? a.ckpt[(((size_t)b * g.nc + c) * NS + n) * g.D + d] : 0.f;
-      float xm3 = Act<T>::ld(xt + 0 * G + tid);
-      float xm2 = Act<T>::ld(xt + 1 * G + tid);
-      float xm1 = Act<T>::ld(xt + 2 * G + tid);
+      for (int i = 0; i < NS / 2; ++i) {
+        const int n = lane_of(i);
+        h[i] = make_float2(ckt[n * GB + tid], ckt[(n + 1) * GB + tid]);
+      }
+#pragma unroll
+      for (int qs = 0; qs < 4; ++qs)
+        hist[tid * 4 + (qs ^ swz)] = make_float4(h[2 * qs].x, h[2 * qs].y, h[2 * qs + 1].x, h[2 * qs + 1].y);
+      float xm3 = Act<T>::ld(xt + 0 * GB + tid);
+      float xm2 = Act<T>::ld(xt + 1 * GB + tid);
+      float xm1 = Act<T>::ld(xt + 2 * GB + tid);
       for (int j = 0; j < steps; ++j) {
-        const float xv = Act<T>::ld(xt + (j + 3) * G + tid);
-        const float cpre = fmaf(P.w[0], xm3, fmaf(P.w[1], xm2, fmaf(P.w[2], xm1, fmaf(P.w[3], xv, P.cb))));
+        const float xv = Act<T>::ld(xt + (j + 3) * GB + tid);
+        const float cpre = fmaf(w[0], xm3, fmaf(w[1], xm2, fmaf(w[2], xm1, fmaf(w[3], xv, cb))));
         xm3 = xm2;
         xm2 = xm1;
         xm1 = xv;
-        const float u = cpre * sigmoid_f(cpre);
-        const float delta = softplus_f(Act<T>::ld(drt + j * G + tid) + P.dtb);
-        const float du = delta * u;
+        const float sc = sigmoid_f(cpre);
+        const float u = cpre * sc;
+        const float delta = softplus_f(Act<T>::ld(drt + j * GB + tid) + dtb);
+        const float2 dl2 = f2b(delta);
+        const float2 du2 = f2b(delta * u);
         const float4* B4 = reinterpret_cast<const float4*>(fB + j * NS);
         const float4* C4 = reinterpret_cast<const float4*>(fC + j * NS);
-        float y0 = 0.f, y1 = 0.f, y2 = 0.f, y3 = 0.f;
+        float2 y01 = make_float2(0.f, 0.f), y23 = make_float2(0.f, 0.f);
+        float4* hrow = hist + (size_t)(j + 1) * GB * 4 + tid * 4;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float4 bv = B4[q];
-          const float4 cv = C4[q];
-          h[4 * q + 0] = fmaf(ex2(delta * P.A2[4 * q + 0]), h[4 * q + 0], du * bv.x);
-          h[4 * q + 1] = fmaf(ex2(delta * P.A2[4 * q + 1]), h[4 * q + 1], du * bv.y);
-          h[4 * q + 2] = fmaf(ex2(delta * P.A2[4 * q + 2]), h[4 * q + 2], du * bv.z);
-          h[4 * q + 3] = fmaf(ex2(delta * P.A2[4 * q + 3]), h[4 * q + 3], du * bv.w);
-          y0 = fmaf(cv.x, h[4 * q + 0], y0);
-          y1 = fmaf(cv.y, h[4 * q + 1], y1);
-          y2 = fmaf(cv.z, h[4 * q + 2], y2);
-          y3 = fmaf(cv.w, h[4 * q + 3], y3);
-          hist[(j * G + tid) * 4 + (q ^ swz)] =
-              make_float4(h[4 * q + 0], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
+        for (int qs = 0; qs < 4; ++qs) {
+          const float4 bv = B4[qs ^ rot];
+          const float4 cv = C4[qs ^ rot];
+          const float2 dA0 = ex2x2(__fmul2_rn(dl2, a2[2 * qs]));
+          const float2 dA1 = ex2x2(__fmul2_rn(dl2, a2[2 * qs + 1]));
+          h[2 * qs] = __ffma2_rn(dA0, h[2 * qs], __fmul2_rn(du2, make_float2(bv.x, bv.y)));
+          h[2 * qs + 1] = __ffma2_rn(dA1, h[2 * qs + 1], __fmul2_rn(du2, make_float2(bv.z, bv.w)));
+          y01 = __ffma2_rn(make_float2(cv.x, cv.y), h[2 * qs], y01);
+          y23 = __ffma2_rn(make_float2(cv.z, cv.w), h[2 * qs + 1], y23);
+          hrow[qs ^ swz] = make_float4(h[2 * qs].x, h[2 * qs].y, h[2 * qs + 1].x, h[2 * qs + 1].y);
         }
-        const float y = fmaf(P.Dd, u, (y0 + y1) + (y2 + y3));
-        scal[j * G + tid] = make_float4(u, delta, cpre, y);
+        const float y = fmaf(Dd, u, (y01.x + y01.y) + (y23.x + y23.y));
+        scal[j * GB + tid] = make_float4(sc, delta, cpre, y);
       }
     }
 
     // ---- reverse-time pass over the chunk ----
+    float2 hn[NS / 2];  // h_t (state after step t)
+    {
+      const float4* hrow = hist + (size_t)steps * GB * 4 + tid * 4;
+#pragma unroll
+      for (int qs = 0; qs < 4; ++qs) {
+        const float4 v = hrow[qs ^ swz];
+        hn[2 * qs] = make_float2(v.x, v.y);
+        hn[2 * qs + 1] = make_float2(v.z, v.w);
+      }
+    }
     for (int j = steps - 1; j >= 0; --j) {
       const int t = c * K + j;
-      const float4 sc = scal[j * G + tid];
-      const float u = sc.x, delta = sc.y, cpre = sc.z, y = sc.w;
-      const float gv = Act<T>::ld(dgt + j * G + tid);
-      const float zv = Act<T>::ld(zt + j * G + tid);
-      const float drv = Act<T>::ld(drt + j * G + tid);
-      const float szv = sigmoid_f(zv);
-      const float dy = gv * zv * szv;
-      const float dzv = gv * y * (szv + zv * szv * (1.f - szv));
-      const float du_ = delta * u;
-      float sumB = 0.f, sumAq = 0.f;
-      float pv[32];
+      const float4 sv = scal[j * GB + tid];
+      const float sc = sv.x, delta = sv.y, cpre = sv.z, y = sv.w;
+      const float u = cpre * sc;
+      const float gv = Act<T>::ld(dgt + j * GB + tid);
+      const float zv = Act<T>::ld(zt + j * GB + tid);
+      const float drv = Act<T>::ld(drt + j * GB + tid);
+      const float sz = sigmoid_f(zv);
+      const float dy = gv * zv * sz;
+      const float dzv = gv * y * (sz * fmaf(zv, 1.f - sz, 1.f));
+      const float2 dy2 = f2b(dy);
+      const float2 dl2 = f2b(delta);
+      const float2 du2 = f2b(delta * u);
+      float2 sB = make_float2(0.f, 0.f), sAq = make_float2(0.f, 0.f);
+      float pB[NS], pC[NS];
+      float2 hp[NS / 2];  // h_{t-1}
+      const float4* hrow = hist + (size_t)j * GB * 4 + tid * 4;
       const float4* B4 = reinterpret_cast<const float4*>(fB + j * NS);
       const float4* C4 = reinterpret_cast<const float4*>(fC + j * NS);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float4 hv4 = hist[(j * G + tid) * 4 + (q ^ swz)];
-        const float4 bv4 = B4[q];
-        const float4 cv4 = C4[q];
-        const float hv[4] = {hv4.x, hv4.y, hv4.z, hv4.w};
-        const float bv[4] = {bv4.x, bv4.y, bv4.z, bv4.w};
-        const float cv[4] = {cv4.x, cv4.y, cv4.z, cv4.w};
+      for (int qs = 0; qs < 4; ++qs) {
+        const float4 hv = hrow[qs ^ swz];
+        hp[2 * qs] = make_float2(hv.x, hv.y);
+        hp[2 * qs + 1] = make_float2(hv.z, hv.w);
+        const float4 bv = B4[qs ^ rot];
+        const float4 cv = C4[qs ^ rot];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int n = 4 * q + e;
-          const float dh = fmaf(dy, cv[e], carry[n]);   // dL/dh_t
-          pv[16 + n] = dy * hv[e];                      // dC partial
-          pv[n] = dh * du_;                             // dB partial
-          const float r = fmaf(-du_, bv[e], hv[e]);     // exp(delta A) h_{t-1}
-          sumB = fmaf(dh, bv[e], sumB);
-          const float qn = dh * r;
-          dAp[n] = fmaf(delta, qn, dAp[n]);
-          sumAq = fmaf(P.A2[n], qn, sumAq);
-          carry[n] = ex2(delta * P.A2[n]) * dh;
+        for (int e = 0; e < 2; ++e) {
+          const int i = 2 * qs + e;
+          const float2 bb = e ? make_float2(bv.z, bv.w) : make_float2(bv.x, bv.y);
+          const float2 cc = e ? make_float2(cv.z, cv.w) : make_float2(cv.x, cv.y);
+          const float2 dh = __ffma2_rn(dy2, cc, carry[i]);       // dL/dh_t
+          const float2 pc = __fmul2_rn(dy2, hn[i]);               // dC partial
+          const float2 pb = __fmul2_rn(dh, du2);                  // dB partial
+          sB = __ffma2_rn(dh, bb, sB);
+          carry[i] = __fmul2_rn(ex2x2(__fmul2_rn(dl2, a2[i])), dh);  // exp(delta A) dh
+          const float2 qv = __fmul2_rn(carry[i], hp[i]);          // dh exp(delta A) h_{t-1}
+          dAp[i] = __ffma2_rn(dl2, qv, dAp[i]);
+          sAq = __ffma2_rn(a2[i], qv, sAq);
+          pB[2 * i] = pb.x;
+          pB[2 * i + 1] = pb.y;
+          pC[2 * i] = pc.x;
+          pC[2 * i + 1] = pc.y;
         }
       }
-      const float du = fmaf(dy, P.Dd, delta * sumB);
-      const float ddelta = fmaf(u, sumB, LN2 * sumAq);
+#pragma unroll
+      for (int i = 0; i < NS / 2; ++i) hn[i] = hp[i];
+      const float sumB = sB.x + sB.y;
+      const float du = fmaf(dy, Dd, delta * sumB);
+      const float ddelta = fmaf(u, sumB, LN2 * (sAq.x + sAq.y));
       dD_acc = fmaf(dy, u, dD_acc);
-      const float ddr = ddelta * sigmoid_f(drv + P.dtb);
+      const float ddr = ddelta * sigmoid_f(drv + dtb);
       ddtb_acc += ddr;
-      const float scp = sigmoid_f(cpre);
-      const float dc = du * (scp + cpre * scp * (1.f - scp));
+      const float dc = du * (sc * fmaf(cpre, 1.f - sc, 1.f));
       dcb_acc += dc;
 #pragma unroll
-      for (int k = 0; k < WC; ++k) dcw[k] = fmaf(dc, Act<T>::ld(xt + (j + k) * G + tid), dcw[k]);
-      const float dxv = fmaf(dc, P.w[3], fmaf(dc1, P.w[2], fmaf(dc2, P.w[1], dc3 * P.w[0])));
+      for (int k = 0; k < WC; ++k) dcw[k] = fmaf(dc, Act<T>::ld(xt + (j + k) * GB + tid), dcw[k]);
+      const float dxv = fmaf(dc, w[3], fmaf(dc1, w[2], fmaf(dc2, w[1], dc3 * w[0])));
       dc3 = dc2;
       dc2 = dc1;
       dc1 = dc;
@@ -709,17 +824,20 @@ __global__ void __launch_bounds__(G) m3_bwd_kernel(BwdArgs a) {
           a.dchead[(((size_t)b * g.S + s) * 3 + (t - t_begin)) * g.D + d] = dc;
       } else {
 #pragma unroll
-        for (int n = 0; n < 32; ++n) pv[n] = 0.f;
+        for (int n = 0; n < NS; ++n) pB[n] = pC[n] = 0.f;
       }
-      red[(j * NW + warp) * 32 + lane] = warp_reduce_scatter32(pv, lane);
+      const float rb = warp_sum16_rotated(pB, lane);
+      const float rc = warp_sum16_rotated(pC, lane);
+      const int nf = 4 * rot + 2 * ((lane >> 3) & 1) + ((lane >> 2) & 1);
+      red[(j * NWB + warp) * 32 + (lane < 16 ? nf : 16 + nf)] = lane < 16 ? rb : rc;
     }
     __syncthreads();
     // one global reduction per (t, n) per block for dB and dC
-    for (int i = tid; i < steps * 32; i += G) {
+    for (int i = tid; i < steps * 32; i += GB) {
       const int j = i >> 5, l = i & 31;
       float v = 0.f;
 #pragma unroll
-      for (int w = 0; w < NW; ++w) v += red[(j * NW + w) * 32 + l];
+      for (int ww = 0; ww < NWB; ++ww) v += red[(j * NWB + ww) * 32 + l];
       float* dst = (l < NS ? a.dB : a.dC) + ((size_t)b * g.T + c * K + j) * NS + (l & (NS - 1));
       atomicAdd(dst, v);
     }
@@ -729,7 +847,11 @@ __global__ void __launch_bounds__(G) m3_bwd_kernel(BwdArgs a) {
   if (active) {
     float* Pp = a.partials + ((size_t)b * g.S + s) * NPART * g.D;
 #pragma unroll
-    for (int n = 0; n < NS; ++n) Pp[(size_t)n * g.D + d] = dAp[n];
+    for (int i = 0; i < NS / 2; ++i) {
+      const int n = lane_of(i);
+      Pp[(size_t)n * g.D + d] = dAp[i].x;
+      Pp[(size_t)(n + 1) * g.D + d] = dAp[i].y;
+    }
     Pp[(size_t)16 * g.D + d] = dD_acc;
     Pp[(size_t)17 * g.D + d] = ddtb_acc;
     Pp[(size_t)18 * g.D + d] = dcb_acc;
@@ -793,6 +915,8 @@ __global__ void m3_bwd_finalize_kernel(BwdArgs a, int rows) {
 // ---------------------------------------------------------------------------
 
 constexpr size_t SMEM_CAP = 227 * 1024;  // opt-in shared memory per block
+constexpr int FWD_WARPS_PER_SM = 8;       // forward time split target
+constexpr int BWD_WAVES = 4;              // backward time split target
 
 // Largest chunk whose backward footprint fits one block's shared memory.
 __host__ inline int kmax_for(int es) {
@@ -816,13 +940,13 @@ cudaError_t set_attrs() {
   const int es = sizeof(T);
   cudaError_t e;
   e = cudaFuncSetAttribute(m3_fwd_kernel<T, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)fwd_smem(KMAX, es).total);
+                           (int)fwd_smem(es).total);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(m3_fwd_kernel<T, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)fwd_smem(KMAX, es).total);
+                           (int)fwd_smem(es).total);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(m3_bwd_agg_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)agg_smem(KMAX, es).total);
+                           (int)agg_smem(es).total);
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(m3_bwd_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)bwd_smem(kmax_for(es), es).total);
@@ -851,16 +975,16 @@ cudaError_t device_info(int chunk, int ai, int* sms, int* occ_f, int* occ_b) {
   if (occ_f && di.occ_fwd[ai][chunk] == 0) {
     int of = 0, ob = 0;
     if (ai == 1) {
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&of, m3_fwd_kernel<__nv_bfloat16, true>, G,
-                                                        fwd_smem(chunk, 2).total);
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&of, m3_fwd_kernel<__nv_bfloat16, true>, GF,
+                                                        fwd_smem(2).total);
       if (e == cudaSuccess)
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ob, m3_bwd_kernel<__nv_bfloat16>, G,
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ob, m3_bwd_kernel<__nv_bfloat16>, GB,
                                                           bwd_smem(chunk, 2).total);
     } else {
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&of, m3_fwd_kernel<float, true>, G,
-                                                        fwd_smem(chunk, 4).total);
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&of, m3_fwd_kernel<float, true>, GF,
+                                                        fwd_smem(4).total);
       if (e == cudaSuccess)
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ob, m3_bwd_kernel<float>, G,
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ob, m3_bwd_kernel<float>, GB,
                                                           bwd_smem(chunk, 4).total);
     }
     if (e != cudaSuccess) return e;
@@ -926,7 +1050,8 @@ m3_status make_plan(const m3_dims* dm, m3_dtype act, Plan* p) {
   p->D = (int)dm->d_inner;
   p->K = dm->chunk ? (int)dm->chunk : KDEF;
   p->nc = (p->T + p->K - 1) / p->K;
-  const int groups = (p->D + G - 1) / G;
+  const int groups_f = (p->D + GF - 1) / GF;
+  const int groups_b = (p->D + GB - 1) / GB;
   int want_f = 1, want_b = 1;
   if (dm->segments > 0) {
     want_f = want_b = (int)dm->segments;
@@ -936,11 +1061,17 @@ m3_status make_plan(const m3_dims* dm, m3_dtype act, Plan* p) {
       cudaGetLastError();
       return M3_ERR_CUDA;
     }
-    const int64_t bg = (int64_t)p->B * groups;
-    const int64_t cap_f = (int64_t)sms * of;
-    const int64_t cap_b = (int64_t)sms * ob;
-    want_f = (int)((cap_f + bg - 1) / bg);
-    want_b = (int)((cap_b + bg - 1) / bg);
+    // Forward: a segment boundary costs a second pass over the earlier
+    // segments, so split time only until about FWD_WARPS_PER_SM warps are
+    // resident.  Backward: the aggregate pass is cheap next to the main
+    // kernel, so split until about BWD_WAVES waves of resident blocks.
+    const int64_t fwd_warps = (int64_t)p->B * groups_f * (GF / 32);
+    const int64_t want_fw = (int64_t)FWD_WARPS_PER_SM * sms;
+    want_f = (int)((want_fw + fwd_warps - 1) / fwd_warps);
+    const int64_t bblocks = (int64_t)p->B * groups_b;
+    const int64_t cap_b = (int64_t)sms * ob * BWD_WAVES;
+    want_b = (int)((cap_b + bblocks - 1) / bblocks);
+    (void)of;
   }
   if (p->nc == 0) {
     p->Sf = p->Sb = 1;
@@ -989,30 +1120,30 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 template <typename T>
 m3_status launch_fwd(const Plan& p, FwdArgs a, cudaStream_t st) {
-  const int groups = (p.D + G - 1) / G;
-  const size_t smem = fwd_smem(p.K, sizeof(T)).total;
+  const int groups = (p.D + GF - 1) / GF;
+  const size_t smem = fwd_smem(sizeof(T)).total;
   a.g = Geo{p.B, p.T, p.D, p.K, p.nc, p.Sf, p.mf};
   if (p.Sf > 1) {
-    m3_fwd_kernel<T, false><<<dim3(groups, p.Sf - 1, p.B), G, smem, st>>>(a);
+    m3_fwd_kernel<T, false><<<dim3(groups, p.Sf - 1, p.B), GF, smem, st>>>(a);
     const size_t n = (size_t)p.B * NS * p.D;
     m3_fwd_carry_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(a);
   }
-  m3_fwd_kernel<T, true><<<dim3(groups, p.Sf, p.B), G, smem, st>>>(a);
+  m3_fwd_kernel<T, true><<<dim3(groups, p.Sf, p.B), GF, smem, st>>>(a);
   return cudaGetLastError() == cudaSuccess ? M3_OK : M3_ERR_CUDA;
 }
 
 template <typename T>
 m3_status launch_bwd(const Plan& p, BwdArgs a, cudaStream_t st) {
-  const int groups = (p.D + G - 1) / G;
+  const int groups = (p.D + GB - 1) / GB;
   a.g = Geo{p.B, p.T, p.D, p.K, p.nc, p.Sb, p.mb};
   if (cudaMemsetAsync(a.dB, 0, (size_t)p.B * p.T * NS * 4, st) != cudaSuccess) return M3_ERR_CUDA;
   if (cudaMemsetAsync(a.dC, 0, (size_t)p.B * p.T * NS * 4, st) != cudaSuccess) return M3_ERR_CUDA;
   if (p.Sb > 1) {
-    m3_bwd_agg_kernel<T><<<dim3(groups, p.Sb - 1, p.B), G, agg_smem(p.K, sizeof(T)).total, st>>>(a);
+    m3_bwd_agg_kernel<T><<<dim3(groups, p.Sb - 1, p.B), GB, agg_smem(sizeof(T)).total, st>>>(a);
     const size_t n = (size_t)p.B * NS * p.D;
     m3_bwd_carry_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(a);
   }
-  m3_bwd_kernel<T><<<dim3(groups, p.Sb, p.B), G, bwd_smem(p.K, sizeof(T)).total, st>>>(a);
+  m3_bwd_kernel<T><<<dim3(groups, p.Sb, p.B), GB, bwd_smem(p.K, sizeof(T)).total, st>>>(a);
   if (p.Sb > 1) {
     const size_t n = (size_t)p.B * (p.Sb - 1) * 3 * p.D;
     m3_bwd_fixup_kernel<T><<<(unsigned)((n + 255) / 256), 256, 0, st>>>(a);
@@ -1083,9 +1214,10 @@ m3_status m3scan_fwd(const m3_dims* dims, m3_dtype act, const void* x, const voi
   const void* act_ptrs[] = {x, delta_raw, z, Bm, Cm, gated, y_dbg};
   for (const void* q : act_ptrs)
     if (q && !aligned(q, 16)) return M3_ERR_ALIGN;
-  const void* f_ptrs[] = {conv_w, conv_b, dt_bias, a_log, D, ckpt};
+  const void* f_ptrs[] = {conv_w, conv_b, dt_bias, a_log, D};
   for (const void* q : f_ptrs)
     if (!aligned(q, 4)) return M3_ERR_ALIGN;
+  if (!aligned(ckpt, 16)) return M3_ERR_ALIGN;
   if (p.Sf > 1) {
     if (!workspace) return M3_ERR_WORKSPACE;
     if (workspace_bytes < p.ws_bytes) return M3_ERR_WORKSPACE;
@@ -1137,10 +1269,11 @@ m3_status m3scan_bwd(const m3_dims* dims, m3_dtype act, const void* x, const voi
   const void* act_ptrs[] = {x, delta_raw, z, Bm, Cm, d_gated, d_x, d_delta_raw, dz, du_dbg};
   for (const void* q : act_ptrs)
     if (q && !aligned(q, 16)) return M3_ERR_ALIGN;
-  const void* f_ptrs[] = {conv_w, conv_b, dt_bias, a_log, D, ckpt, dB, dC,
+  const void* f_ptrs[] = {conv_w, conv_b, dt_bias, a_log, D, dB, dC,
                           d_conv_w, d_conv_b, d_dt_bias, d_a_log, dD};
   for (const void* q : f_ptrs)
     if (!aligned(q, 4)) return M3_ERR_ALIGN;
+  if (!aligned(ckpt, 16)) return M3_ERR_ALIGN;
   if (!workspace) return M3_ERR_WORKSPACE;
   if (workspace_bytes < p.ws_bytes) return M3_ERR_WORKSPACE;
   if (!aligned(workspace, 256)) return M3_ERR_ALIGN;
