@@ -73,8 +73,8 @@ typedef enum {
 typedef struct {
     int64_t batch, seq_len, d_inner, d_state, d_conv;
     /* Checkpoint interval K in steps; 0 = library default (8).  At most 64,
-       and small enough for the backward's shared memory (32 for bf16
-       activations, 28 for f32); larger values give M3_ERR_UNSUPPORTED. */
+       and small enough for the backward's shared memory (30 for bf16
+       activations, 23 for f32); larger values give M3_ERR_UNSUPPORTED. */
     int64_t chunk;
     /* Number of time segments scanned in parallel (each segment is a run of
        whole chunks); 0 = chosen from the shape and the current device. */
@@ -187,6 +187,11 @@ m3_status m3scan_bwd_noalloc(const m3_dims* dims, m3_dtype act,
 
 /* A static, human-readable name for a status code. */
 const char* m3scan_status_string(m3_status status);
+
+/* Name of the last CUDA error this thread's calls into the library met
+ * (the detail behind M3_ERR_CUDA), e.g. "cudaErrorInvalidValue";
+ * "cudaSuccess" if none. */
+const char* m3scan_last_cuda_error(void);
 
 /* Library version as major * 10000 + minor * 100 + patch. */
 int32_t m3scan_version(void);

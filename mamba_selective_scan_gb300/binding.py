@@ -29,7 +29,7 @@ STATUS = {
 
 # every symbol include/m3scan.h declares
 EXPORTS = ("m3scan_plan", "m3scan_fwd", "m3scan_bwd", "m3scan_bwd_noalloc",
-           "m3scan_status_string", "m3scan_version")
+           "m3scan_status_string", "m3scan_last_cuda_error", "m3scan_version")
 
 # size of the library's own scratch array used by m3scan_bwd_noalloc
 NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -39,6 +39,8 @@ class M3Error(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
         msg = _lib_handle().m3scan_status_string(status).decode() if _LIB else STATUS.get(status)
+        if status == 6 and _LIB:
+            msg += f" ({_LIB.m3scan_last_cuda_error().decode()})"
         super().__init__(f"{where}: {msg}")
 
 
@@ -97,6 +99,8 @@ def _lib_handle(build_if_missing: bool = True):
                                                + [_fp] * 2 + [_fp] * 5 + [_vp])
             lib.m3scan_status_string.restype = ctypes.c_char_p
             lib.m3scan_status_string.argtypes = [ctypes.c_int]
+            lib.m3scan_last_cuda_error.restype = ctypes.c_char_p
+            lib.m3scan_last_cuda_error.argtypes = []
             lib.m3scan_version.restype = ctypes.c_int32
             lib.m3scan_version.argtypes = []
             _LIB = lib

@@ -46,9 +46,11 @@ namespace {
 constexpr int NS = 16;        // d_state lanes per channel
 constexpr int WC = 4;         // conv taps
 constexpr int GF = 128;       // forward: channels (= threads) per block
-constexpr int GB = 64;        // backward: channels (= threads) per block
+constexpr int GB = 128;       // backward: channels (= threads) per block = 4 warps,
+                              // one per tensor-memory lane quadrant
 constexpr int NWB = GB / 32;  // backward warps per block
-constexpr int TT = 32;        // forward / aggregate staging tile (steps)
+constexpr int TT = 16;        // forward / aggregate staging tile (steps)
+constexpr int SUB = 8;        // forward scalar sub-tile (steps)
 constexpr int KMAX = 64;      // largest chunk (the backward may allow less)
 constexpr int KDEF = 8;       // default chunk
 constexpr int NPART = 24;     // per-channel parameter partials (23 used)
@@ -114,6 +116,44 @@ template <int N> __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
 }
 
+// ---- tensor memory (tcgen05): per-thread row storage ----
+// A CTA of 4 warps owns tensor-memory lanes 0..127 (warp w: lanes 32w..32w+31,
+// one lane per thread).  32x32b accesses move 16 consecutive 32-bit columns
+// of the calling thread's lane.
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {  // whole warp
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)),
+               "r"(ncols) : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {  // whole warp
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tmem_fence_before_sync() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_fence_after_sync() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float2 (&v)[NS / 2]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+      ::"r"(taddr), "f"(v[0].x), "f"(v[0].y), "f"(v[1].x), "f"(v[1].y), "f"(v[2].x), "f"(v[2].y),
+      "f"(v[3].x), "f"(v[3].y), "f"(v[4].x), "f"(v[4].y), "f"(v[5].x), "f"(v[5].y), "f"(v[6].x),
+      "f"(v[6].y), "f"(v[7].x), "f"(v[7].y) : "memory");
+}
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float2 (&v)[NS / 2]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=f"(v[0].x), "=f"(v[0].y), "=f"(v[1].x), "=f"(v[1].y), "=f"(v[2].x), "=f"(v[2].y),
+        "=f"(v[3].x), "=f"(v[3].y), "=f"(v[4].x), "=f"(v[4].y), "=f"(v[5].x), "=f"(v[5].y),
+        "=f"(v[6].x), "=f"(v[6].y), "=f"(v[7].x), "=f"(v[7].y) : "r"(taddr) : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
 // Stage rows [t_first, t_first + rows) x channels [d0, d0 + G) of a
 // [B, T_, D] tensor of element type T into dst[rows][G]; rows outside
 // [0, t_limit) and channels >= D read as zero.  NT threads cooperate.
@@ -177,12 +217,15 @@ struct BwdArgs {
   float *q, *sd, *gin, *dxpart, *dchead, *partials;
   float *d_conv_w, *d_conv_b, *d_dt_bias, *d_a_log, *dD;
   int accumulate;
+  uint32_t tcols;  // tensor-memory columns per CTA for the state history
 };
 
 // Forward shared memory: two staging buffers {x, delta_raw, z: [TT][GF]
-// act; B, C: [TT][16] act} and B, C of the current tile as float [TT][16].
+// act; B, C: [TT][16] act}, B and C of the current tile as float [TT][16],
+// and per-step scalars of one sub-tile sc[SUB][GF] float4 (thread-private
+// slots: delta, delta*u, D*u, silu(z)).
 struct FwdSmem {
-  size_t x, dr, z, Bt, Ct, tile, fB, fC, total;
+  size_t x, dr, z, Bt, Ct, tile, fB, fC, sc, total;
 };
 __host__ __device__ inline FwdSmem fwd_smem(int es) {
   FwdSmem s;
@@ -194,18 +237,21 @@ __host__ __device__ inline FwdSmem fwd_smem(int es) {
   s.tile = s.Ct + align_up((size_t)TT * NS * es, 128);
   s.fB = 2 * s.tile;
   s.fC = s.fB + (size_t)TT * NS * 4;
-  s.total = s.fC + (size_t)TT * NS * 4;
+  s.sc = s.fC + (size_t)TT * NS * 4;
+  s.total = s.sc + (size_t)SUB * GF * 16;
   return s;
 }
 
 // Backward shared memory: two staging buffers {x: [K+3][GB] (three halo rows
 // before the chunk), delta_raw, z, d_gated: [K][GB] act; B, C: [K][16] act;
 // the chunk's start state ck: [16][GB] f32}; B and C of the current chunk as
-// float; the recomputed states hist[K+1][GB][16] f32 (row 0 = chunk start);
-// per-step scalars scal[K][GB] float4 (sigmoid(c), delta, c, y); per-warp
-// dB/dC sums red[K][NWB][32].
+// float (the recomputed states live in tensor memory, see m3_bwd_kernel);
+// per-step scalars, two thread-private float4 slots per step: s0[K][GB] =
+// (delta, delta*u, dy, dz factor -> sum_n A dh exp(delta A) h_{t-1}) and
+// s1[K][GB] = (D*u -> sum_n dh B, sigmoid(delta_raw + dt_bias), sigmoid(c),
+// c); per-warp dB/dC sums red[K][NWB][32].
 struct BwdSmem {
-  size_t x, dr, z, dg, Bt, Ct, ck, tile, fB, fC, hist, scal, red, total;
+  size_t x, dr, z, dg, Bt, Ct, ck, tile, fB, fC, scal, red, total;
 };
 __host__ __device__ inline BwdSmem bwd_smem(int K, int es) {
   BwdSmem s;
@@ -219,17 +265,16 @@ __host__ __device__ inline BwdSmem bwd_smem(int K, int es) {
   s.tile = s.ck + (size_t)NS * GB * 4;
   s.fB = 2 * s.tile;
   s.fC = s.fB + (size_t)K * NS * 4;
-  s.hist = s.fC + (size_t)K * NS * 4;
-  s.scal = s.hist + (size_t)(K + 1) * GB * NS * 4;
-  s.red = s.scal + (size_t)K * GB * 16;
+  s.scal = s.fC + (size_t)K * NS * 4;
+  s.red = s.scal + (size_t)2 * K * GB * 16;
   s.total = s.red + (size_t)K * NWB * 32 * 4;
   return s;
 }
 
 // Backward aggregate shared memory: two buffers {delta_raw, z, d_gated:
-// [TT][GB]; C: [TT][16]} and float C.
+// [TT][GB]; C: [TT][16]}, float C and per-step (delta, dy) [TT][GB] float2.
 struct AggSmem {
-  size_t dr, z, dg, Ct, tile, fC, total;
+  size_t dr, z, dg, Ct, tile, fC, sc, total;
 };
 __host__ __device__ inline AggSmem agg_smem(int es) {
   AggSmem s;
@@ -239,7 +284,8 @@ __host__ __device__ inline AggSmem agg_smem(int es) {
   s.Ct = s.dg + align_up((size_t)TT * GB * es, 128);
   s.tile = s.Ct + align_up((size_t)TT * NS * es, 128);
   s.fC = 2 * s.tile;
-  s.total = s.fC + (size_t)TT * NS * 4;
+  s.sc = s.fC + (size_t)TT * NS * 4;
+  s.total = s.sc + (size_t)TT * GB * 8;
   return s;
 }
 
@@ -317,6 +363,7 @@ __global__ void __launch_bounds__(GF) m3_fwd_kernel(FwdArgs a) {
     cp_async_commit();
   };
 
+  float4* scs = reinterpret_cast<float4*>(smem + L.sc) + tid;  // this thread's slots, stride GF
   int kc = 0;  // steps left until the next checkpoint
   stage(t_begin, 0);
   for (int t0 = t_begin, it = 0; t0 < t_end; t0 += TT, ++it) {
@@ -342,63 +389,77 @@ __global__ void __launch_bounds__(GF) m3_fwd_kernel(FwdArgs a) {
     const T* drt = reinterpret_cast<const T*>(base + L.dr);
     const T* zt = reinterpret_cast<const T*>(base + L.z);
     const int steps = min(TT, t_end - t0);
-    for (int j = 0; j < steps; ++j) {
-      if (FINAL) {
-        if (kc == 0) {
-          const int t = t0 + j;
-          if (active && (t > t_begin || s == 0)) {
-            float* ck = a.ckpt + (((size_t)b * g.nc + t / g.K) * NS) * g.D + d;
-#pragma unroll
-            for (int i = 0; i < NS / 2; ++i) {
-              ck[(size_t)(2 * i) * g.D] = h[i].x;
-              ck[(size_t)(2 * i + 1) * g.D] = h[i].y;
-            }
-          }
-          kc = g.K;
+    for (int j0 = 0; j0 < steps; j0 += SUB) {
+      const int ns = min(SUB, steps - j0);
+      // scalar pass: independent per step (conv, SiLU, softplus, gate factor)
+      for (int j = 0; j < ns; ++j) {
+        const float xv = Act<T>::ld(xt + (j0 + j) * GF + tid);
+        const float cpre = fmaf(w[0], xm3, fmaf(w[1], xm2, fmaf(w[2], xm1, fmaf(w[3], xv, cb))));
+        xm3 = xm2;
+        xm2 = xm1;
+        xm1 = xv;
+        const float u = cpre * sigmoid_f(cpre);
+        const float delta = softplus_f(Act<T>::ld(drt + (j0 + j) * GF + tid) + dtb);
+        float gz = 0.f;
+        if (FINAL) {
+          const float zv = Act<T>::ld(zt + (j0 + j) * GF + tid);
+          gz = zv * sigmoid_f(zv);
+        } else {
+          sdelta += delta;
         }
-        --kc;
+        scs[j * GF] = make_float4(delta, delta * u, Dd * u, gz);
       }
-      const float xv = Act<T>::ld(xt + j * GF + tid);
-      const float cpre = fmaf(w[0], xm3, fmaf(w[1], xm2, fmaf(w[2], xm1, fmaf(w[3], xv, cb))));
-      xm3 = xm2;
-      xm2 = xm1;
-      xm1 = xv;
-      const float u = cpre * sigmoid_f(cpre);
-      const float delta = softplus_f(Act<T>::ld(drt + j * GF + tid) + dtb);
-      const float2 dl2 = f2b(delta);
-      const float2 du2 = f2b(delta * u);
-      const float4* B4 = reinterpret_cast<const float4*>(fB + j * NS);
-      if (FINAL) {
-        const float4* C4 = reinterpret_cast<const float4*>(fC + j * NS);
-        float2 y01 = make_float2(0.f, 0.f), y23 = make_float2(0.f, 0.f);
+      // state pass: the only loop-carried dependence is h
+      for (int j = 0; j < ns; ++j) {
+        if (FINAL) {
+          if (kc == 0) {
+            const int t = t0 + j0 + j;
+            if (active && (t > t_begin || s == 0)) {
+              float* ck = a.ckpt + (((size_t)b * g.nc + t / g.K) * NS) * g.D + d;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float4 bv = B4[q];
-          const float4 cv = C4[q];
-          const float2 dA0 = ex2x2(__fmul2_rn(dl2, a2[2 * q]));
-          const float2 dA1 = ex2x2(__fmul2_rn(dl2, a2[2 * q + 1]));
-          h[2 * q] = __ffma2_rn(dA0, h[2 * q], __fmul2_rn(du2, make_float2(bv.x, bv.y)));
-          h[2 * q + 1] = __ffma2_rn(dA1, h[2 * q + 1], __fmul2_rn(du2, make_float2(bv.z, bv.w)));
-          y01 = __ffma2_rn(make_float2(cv.x, cv.y), h[2 * q], y01);
-          y23 = __ffma2_rn(make_float2(cv.z, cv.w), h[2 * q + 1], y23);
+              for (int i = 0; i < NS / 2; ++i) {
+                ck[(size_t)(2 * i) * g.D] = h[i].x;
+                ck[(size_t)(2 * i + 1) * g.D] = h[i].y;
+              }
+            }
+            kc = g.K;
+          }
+          --kc;
         }
-        const float y = fmaf(Dd, u, (y01.x + y01.y) + (y23.x + y23.y));
-        const float zv = Act<T>::ld(zt + j * GF + tid);
-        if (active) {
-          const size_t i = ((size_t)b * g.T + t0 + j) * g.D + d;
-          Act<T>::st(static_cast<T*>(a.gated) + i, y * zv * sigmoid_f(zv));
-          if (a.y_dbg) Act<T>::st(static_cast<T*>(a.y_dbg) + i, y);
-        }
-      } else {
+        const float4 v = scs[j * GF];
+        const float2 dl2 = f2b(v.x);
+        const float2 du2 = f2b(v.y);
+        const float4* B4 = reinterpret_cast<const float4*>(fB + (j0 + j) * NS);
+        if (FINAL) {
+          const float4* C4 = reinterpret_cast<const float4*>(fC + (j0 + j) * NS);
+          float2 y01 = make_float2(0.f, 0.f), y23 = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float4 bv = B4[q];
-          const float2 dA0 = ex2x2(__fmul2_rn(dl2, a2[2 * q]));
-          const float2 dA1 = ex2x2(__fmul2_rn(dl2, a2[2 * q + 1]));
-          h[2 * q] = __ffma2_rn(dA0, h[2 * q], __fmul2_rn(du2, make_float2(bv.x, bv.y)));
-          h[2 * q + 1] = __ffma2_rn(dA1, h[2 * q + 1], __fmul2_rn(du2, make_float2(bv.z, bv.w)));
+          for (int q = 0; q < 4; ++q) {
+            const float4 bv = B4[q];
+            const float4 cv = C4[q];
+            const float2 dA0 = ex2x2(__fmul2_rn(dl2, a2[2 * q]));
+            const float2 dA1 = ex2x2(__fmul2_rn(dl2, a2[2 * q + 1]));
+            h[2 * q] = __ffma2_rn(dA0, h[2 * q], __fmul2_rn(du2, make_float2(bv.x, bv.y)));
+            h[2 * q + 1] = __ffma2_rn(dA1, h[2 * q + 1], __fmul2_rn(du2, make_float2(bv.z, bv.w)));
+            y01 = __ffma2_rn(make_float2(cv.x, cv.y), h[2 * q], y01);
+            y23 = __ffma2_rn(make_float2(cv.z, cv.w), h[2 * q + 1], y23);
+          }
+          const float y = ((y01.x + y01.y) + (y23.x + y23.y)) + v.z;
+          if (active) {
+            const size_t i = ((size_t)b * g.T + t0 + j0 + j) * g.D + d;
+            Act<T>::st(static_cast<T*>(a.gated) + i, y * v.w);
+            if (a.y_dbg) Act<T>::st(static_cast<T*>(a.y_dbg) + i, y);
+          }
+        } else {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float4 bv = B4[q];
+            const float2 dA0 = ex2x2(__fmul2_rn(dl2, a2[2 * q]));
+            const float2 dA1 = ex2x2(__fmul2_rn(dl2, a2[2 * q + 1]));
+            h[2 * q] = __ffma2_rn(dA0, h[2 * q], __fmul2_rn(du2, make_float2(bv.x, bv.y)));
+            h[2 * q + 1] = __ffma2_rn(dA1, h[2 * q + 1], __fmul2_rn(du2, make_float2(bv.z, bv.w)));
+          }
         }
-        sdelta += delta;
       }
     }
     __syncthreads();
@@ -504,20 +565,26 @@ __global__ void __launch_bounds__(GB) m3_bwd_agg_kernel(BwdArgs a) {
     const T* drt = reinterpret_cast<const T*>(base + L.dr);
     const T* zt = reinterpret_cast<const T*>(base + L.z);
     const T* dgt = reinterpret_cast<const T*>(base + L.dg);
-    for (int j = steps - 1; j >= 0; --j) {
+    float2* scs = reinterpret_cast<float2*>(smem + L.sc) + tid;  // thread-private, stride GB
+    for (int j = 0; j < steps; ++j) {  // scalar pass
       const float zv = Act<T>::ld(zt + j * GB + tid);
-      const float2 dy2 = f2b(Act<T>::ld(dgt + j * GB + tid) * zv * sigmoid_f(zv));
+      const float dy = Act<T>::ld(dgt + j * GB + tid) * zv * sigmoid_f(zv);
       const float delta = softplus_f(Act<T>::ld(drt + j * GB + tid) + dtb);
-      const float2 dl2 = f2b(delta);
       sdelta += delta;
+      scs[j * GB] = make_float2(delta, dy);
+    }
+    for (int j = steps - 1; j >= 0; --j) {  // state pass
+      const float2 v = scs[j * GB];
+      const float2 dl2 = f2b(v.x);
+      const float2 dy2 = f2b(v.y);
       const float4* C4 = reinterpret_cast<const float4*>(fC + j * NS);
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        const float4 v = C4[q];
+        const float4 c4 = C4[q];
         carry[2 * q] = __fmul2_rn(ex2x2(__fmul2_rn(dl2, a2[2 * q])),
-                                  __ffma2_rn(dy2, make_float2(v.x, v.y), carry[2 * q]));
+                                  __ffma2_rn(dy2, make_float2(c4.x, c4.y), carry[2 * q]));
         carry[2 * q + 1] = __fmul2_rn(ex2x2(__fmul2_rn(dl2, a2[2 * q + 1])),
-                                      __ffma2_rn(dy2, make_float2(v.z, v.w), carry[2 * q + 1]));
+                                      __ffma2_rn(dy2, make_float2(c4.z, c4.w), carry[2 * q + 1]));
       }
     }
     __syncthreads();
@@ -587,7 +654,7 @@ __device__ __forceinline__ float warp_sum16_rotated(float (&v)[NS], int lane) {
 }
 
 template <typename T>
-__global__ void __launch_bounds__(GB) m3_bwd_kernel(BwdArgs a) {
+__global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(BwdArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   const Geo g = a.g;
   const int tid = threadIdx.x;
@@ -607,12 +674,20 @@ __global__ void __launch_bounds__(GB) m3_bwd_kernel(BwdArgs a) {
   const BwdSmem L = bwd_smem(K, sizeof(T));
   float* fB = reinterpret_cast<float*>(smem + L.fB);
   float* fC = reinterpret_cast<float*>(smem + L.fC);
-  float4* hist = reinterpret_cast<float4*>(smem + L.hist);
   float4* scal = reinterpret_cast<float4*>(smem + L.scal);
   float* red = reinterpret_cast<float*>(smem + L.red);
-  const int swz = (tid >> 1) & 3;  // conflict-free float4 rows of 64 bytes
   // state lane of register slot 2*i (pair i): quad (i >> 1) ^ rot, offset 2*(i & 1)
   auto lane_of = [&](int i) { return 4 * ((i >> 1) ^ rot) + 2 * (i & 1); };
+
+  // The recomputed states of a chunk (K rows of 16 f32 per channel) live in
+  // tensor memory: row j of this thread = columns [16 j, 16 j + 16) of its
+  // lane.  Warp 0 allocates for the CTA; every exit path below deallocates.
+  __shared__ uint32_t tmem_slot;
+  if (warp == 0) tmem_alloc(&tmem_slot, a.tcols);
+  tmem_fence_before_sync();
+  __syncthreads();
+  tmem_fence_after_sync();
+  const uint32_t trow = tmem_slot + ((uint32_t)(warp * 32) << 16);
 
   float2 a2[NS / 2];
   float w[WC];
@@ -692,17 +767,11 @@ __global__ void __launch_bounds__(GB) m3_bwd_kernel(BwdArgs a) {
     const float* ckt = reinterpret_cast<const float*>(base + L.ck);
     const int steps = min(K, g.T - c * K);
 
-    // ---- recompute the chunk forward from its start state ----
+    float4* s0 = reinterpret_cast<float4*>(smem + L.scal) + tid;  // thread-private, stride GB
+    float4* s1 = s0 + (size_t)K * GB;
+
+    // ---- scalar pass: everything per step that does not need the state ----
     {
-      float2 h[NS / 2];
-#pragma unroll
-      for (int i = 0; i < NS / 2; ++i) {
-        const int n = lane_of(i);
-        h[i] = make_float2(ckt[n * GB + tid], ckt[(n + 1) * GB + tid]);
-      }
-#pragma unroll
-      for (int qs = 0; qs < 4; ++qs)
-        hist[tid * 4 + (qs ^ swz)] = make_float4(h[2 * qs].x, h[2 * qs].y, h[2 * qs + 1].x, h[2 * qs + 1].y);
       float xm3 = Act<T>::ld(xt + 0 * GB + tid);
       float xm2 = Act<T>::ld(xt + 1 * GB + tid);
       float xm1 = Act<T>::ld(xt + 2 * GB + tid);
@@ -714,13 +783,35 @@ __global__ void __launch_bounds__(GB) m3_bwd_kernel(BwdArgs a) {
         xm1 = xv;
         const float sc = sigmoid_f(cpre);
         const float u = cpre * sc;
-        const float delta = softplus_f(Act<T>::ld(drt + j * GB + tid) + dtb);
-        const float2 dl2 = f2b(delta);
-        const float2 du2 = f2b(delta * u);
+        const float v = Act<T>::ld(drt + j * GB + tid) + dtb;
+        const float delta = softplus_f(v);
+        const float sv = sigmoid_f(v);
+        const float zv = Act<T>::ld(zt + j * GB + tid);
+        const float gv = Act<T>::ld(dgt + j * GB + tid);
+        const float sz = sigmoid_f(zv);
+        const float dy = gv * zv * sz;                           // dL/dy
+        const float dzf = gv * (sz * fmaf(zv, 1.f - sz, 1.f));    // dL/dz = y * dzf
+        s0[j * GB] = make_float4(delta, delta * u, dy, dzf);
+        s1[j * GB] = make_float4(Dd * u, sv, sc, cpre);
+      }
+    }
+
+    // ---- recompute the chunk's states from its start state; dz needs y ----
+    {
+      float2 h[NS / 2];
+#pragma unroll
+      for (int i = 0; i < NS / 2; ++i) {
+        const int n = lane_of(i);
+        h[i] = make_float2(ckt[n * GB + tid], ckt[(n + 1) * GB + tid]);
+      }
+      for (int j = 0; j < steps; ++j) {
+        const float4 v0 = s0[j * GB];
+        const float Du = s1[j * GB].x;
+        const float2 dl2 = f2b(v0.x);
+        const float2 du2 = f2b(v0.y);
         const float4* B4 = reinterpret_cast<const float4*>(fB + j * NS);
         const float4* C4 = reinterpret_cast<const float4*>(fC + j * NS);
         float2 y01 = make_float2(0.f, 0.f), y23 = make_float2(0.f, 0.f);
-        float4* hrow = hist + (size_t)(j + 1) * GB * 4 + tid * 4;
 #pragma unroll
         for (int qs = 0; qs < 4; ++qs) {
           const float4 bv = B4[qs ^ rot];
@@ -731,77 +822,90 @@ __global__ void __launch_bounds__(GB) m3_bwd_kernel(BwdArgs a) {
           h[2 * qs + 1] = __ffma2_rn(dA1, h[2 * qs + 1], __fmul2_rn(du2, make_float2(bv.z, bv.w)));
           y01 = __ffma2_rn(make_float2(cv.x, cv.y), h[2 * qs], y01);
           y23 = __ffma2_rn(make_float2(cv.z, cv.w), h[2 * qs + 1], y23);
-          hrow[qs ^ swz] = make_float4(h[2 * qs].x, h[2 * qs].y, h[2 * qs + 1].x, h[2 * qs + 1].y);
         }
-        const float y = fmaf(Dd, u, (y01.x + y01.y) + (y23.x + y23.y));
-        scal[j * GB + tid] = make_float4(sc, delta, cpre, y);
+        tmem_st16(trow + 16u * (uint32_t)j, h);
+        const float y = ((y01.x + y01.y) + (y23.x + y23.y)) + Du;
+        if (active)
+          Act<T>::st(static_cast<T*>(a.dz) + ((size_t)b * g.T + c * K + j) * g.D + d, y * v0.w);
+      }
+      tmem_wait_st();
+    }
+
+    // ---- reverse-time pass over the chunk: adjoint state, dA, dB/dC ----
+    {
+      float2 hn[NS / 2];  // h_t (state after step t)
+      tmem_ld16(trow + 16u * (uint32_t)(steps - 1), hn);
+      tmem_wait_ld();
+      for (int j = steps - 1; j >= 0; --j) {
+        const float4 v0 = s0[j * GB];
+        const float2 dl2 = f2b(v0.x);
+        const float2 du2 = f2b(v0.y);
+        const float2 dy2 = f2b(v0.z);
+        float2 sB = make_float2(0.f, 0.f), sAq = make_float2(0.f, 0.f);
+        float pB[NS], pC[NS];
+        float2 hp[NS / 2];  // h_{t-1}
+        if (j > 0) {
+          tmem_ld16(trow + 16u * (uint32_t)(j - 1), hp);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int i = 0; i < NS / 2; ++i) {
+            const int n = lane_of(i);
+            hp[i] = make_float2(ckt[n * GB + tid], ckt[(n + 1) * GB + tid]);
+          }
+        }
+        const float4* B4 = reinterpret_cast<const float4*>(fB + j * NS);
+        const float4* C4 = reinterpret_cast<const float4*>(fC + j * NS);
+#pragma unroll
+        for (int qs = 0; qs < 4; ++qs) {
+          const float4 bv = B4[qs ^ rot];
+          const float4 cv = C4[qs ^ rot];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int i = 2 * qs + e;
+            const float2 bb = e ? make_float2(bv.z, bv.w) : make_float2(bv.x, bv.y);
+            const float2 cc = e ? make_float2(cv.z, cv.w) : make_float2(cv.x, cv.y);
+            const float2 dh = __ffma2_rn(dy2, cc, carry[i]);            // dL/dh_t
+            const float2 pc = __fmul2_rn(dy2, hn[i]);                    // dC partial
+            const float2 pb = __fmul2_rn(dh, du2);                       // dB partial
+            sB = __ffma2_rn(dh, bb, sB);
+            carry[i] = __fmul2_rn(ex2x2(__fmul2_rn(dl2, a2[i])), dh);    // exp(delta A) dh
+            const float2 qv = __fmul2_rn(carry[i], hp[i]);               // dh exp(delta A) h_{t-1}
+            dAp[i] = __ffma2_rn(dl2, qv, dAp[i]);
+            sAq = __ffma2_rn(a2[i], qv, sAq);
+            pB[2 * i] = pb.x;
+            pB[2 * i + 1] = pb.y;
+            pC[2 * i] = pc.x;
+            pC[2 * i + 1] = pc.y;
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < NS / 2; ++i) hn[i] = hp[i];
+        // the scalar pass below reads these two sums
+        reinterpret_cast<float*>(s0 + j * GB)[3] = sAq.x + sAq.y;
+        reinterpret_cast<float*>(s1 + j * GB)[0] = sB.x + sB.y;
+        if (!active) {
+#pragma unroll
+          for (int n = 0; n < NS; ++n) pB[n] = pC[n] = 0.f;
+        }
+        const float rb = warp_sum16_rotated(pB, lane);
+        const float rc = warp_sum16_rotated(pC, lane);
+        const int nf = 4 * rot + 2 * ((lane >> 3) & 1) + ((lane >> 2) & 1);
+        red[(j * NWB + warp) * 32 + (lane < 16 ? nf : 16 + nf)] = lane < 16 ? rb : rc;
       }
     }
 
-    // ---- reverse-time pass over the chunk ----
-    float2 hn[NS / 2];  // h_t (state after step t)
-    {
-      const float4* hrow = hist + (size_t)steps * GB * 4 + tid * 4;
-#pragma unroll
-      for (int qs = 0; qs < 4; ++qs) {
-        const float4 v = hrow[qs ^ swz];
-        hn[2 * qs] = make_float2(v.x, v.y);
-        hn[2 * qs + 1] = make_float2(v.z, v.w);
-      }
-    }
+    // ---- scalar pass: du, d delta, softplus, SiLU and conv backward ----
     for (int j = steps - 1; j >= 0; --j) {
       const int t = c * K + j;
-      const float4 sv = scal[j * GB + tid];
-      const float sc = sv.x, delta = sv.y, cpre = sv.z, y = sv.w;
+      const float4 v0 = s0[j * GB];
+      const float4 v1 = s1[j * GB];
+      const float delta = v0.x, dy = v0.z, sAq = v0.w;
+      const float sumB = v1.x, sv = v1.y, sc = v1.z, cpre = v1.w;
       const float u = cpre * sc;
-      const float gv = Act<T>::ld(dgt + j * GB + tid);
-      const float zv = Act<T>::ld(zt + j * GB + tid);
-      const float drv = Act<T>::ld(drt + j * GB + tid);
-      const float sz = sigmoid_f(zv);
-      const float dy = gv * zv * sz;
-      const float dzv = gv * y * (sz * fmaf(zv, 1.f - sz, 1.f));
-      const float2 dy2 = f2b(dy);
-      const float2 dl2 = f2b(delta);
-      const float2 du2 = f2b(delta * u);
-      float2 sB = make_float2(0.f, 0.f), sAq = make_float2(0.f, 0.f);
-      float pB[NS], pC[NS];
-      float2 hp[NS / 2];  // h_{t-1}
-      const float4* hrow = hist + (size_t)j * GB * 4 + tid * 4;
-      const float4* B4 = reinterpret_cast<const float4*>(fB + j * NS);
-      const float4* C4 = reinterpret_cast<const float4*>(fC + j * NS);
-#pragma unroll
-      for (int qs = 0; qs < 4; ++qs) {
-        const float4 hv = hrow[qs ^ swz];
-        hp[2 * qs] = make_float2(hv.x, hv.y);
-        hp[2 * qs + 1] = make_float2(hv.z, hv.w);
-        const float4 bv = B4[qs ^ rot];
-        const float4 cv = C4[qs ^ rot];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int i = 2 * qs + e;
-          const float2 bb = e ? make_float2(bv.z, bv.w) : make_float2(bv.x, bv.y);
-          const float2 cc = e ? make_float2(cv.z, cv.w) : make_float2(cv.x, cv.y);
-          const float2 dh = __ffma2_rn(dy2, cc, carry[i]);       // dL/dh_t
-          const float2 pc = __fmul2_rn(dy2, hn[i]);               // dC partial
-          const float2 pb = __fmul2_rn(dh, du2);                  // dB partial
-          sB = __ffma2_rn(dh, bb, sB);
-          carry[i] = __fmul2_rn(ex2x2(__fmul2_rn(dl2, a2[i])), dh);  // exp(delta A) dh
-          const float2 qv = __fmul2_rn(carry[i], hp[i]);          // dh exp(delta A) h_{t-1}
-          dAp[i] = __ffma2_rn(dl2, qv, dAp[i]);
-          sAq = __ffma2_rn(a2[i], qv, sAq);
-          pB[2 * i] = pb.x;
-          pB[2 * i + 1] = pb.y;
-          pC[2 * i] = pc.x;
-          pC[2 * i + 1] = pc.y;
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < NS / 2; ++i) hn[i] = hp[i];
-      const float sumB = sB.x + sB.y;
       const float du = fmaf(dy, Dd, delta * sumB);
-      const float ddelta = fmaf(u, sumB, LN2 * (sAq.x + sAq.y));
+      const float ddr = fmaf(u, sumB, LN2 * sAq) * sv;
       dD_acc = fmaf(dy, u, dD_acc);
-      const float ddr = ddelta * sigmoid_f(drv + dtb);
       ddtb_acc += ddr;
       const float dc = du * (sc * fmaf(cpre, 1.f - sc, 1.f));
       dcb_acc += dc;
@@ -814,7 +918,6 @@ __global__ void __launch_bounds__(GB) m3_bwd_kernel(BwdArgs a) {
       if (active) {
         const size_t i = ((size_t)b * g.T + t) * g.D + d;
         Act<T>::st(static_cast<T*>(a.ddr) + i, ddr);
-        Act<T>::st(static_cast<T*>(a.dz) + i, dzv);
         if (a.du_dbg) Act<T>::st(static_cast<T*>(a.du_dbg) + i, du);
         if (s + 1 < g.S && t >= t_end - 3)
           a.dxpart[(((size_t)b * g.S + s) * 3 + (t - (t_end - 3))) * g.D + d] = dxv;
@@ -822,14 +925,7 @@ __global__ void __launch_bounds__(GB) m3_bwd_kernel(BwdArgs a) {
           Act<T>::st(static_cast<T*>(a.dx) + i, dxv);
         if (s > 0 && t < t_begin + 3)
           a.dchead[(((size_t)b * g.S + s) * 3 + (t - t_begin)) * g.D + d] = dc;
-      } else {
-#pragma unroll
-        for (int n = 0; n < NS; ++n) pB[n] = pC[n] = 0.f;
       }
-      const float rb = warp_sum16_rotated(pB, lane);
-      const float rc = warp_sum16_rotated(pC, lane);
-      const int nf = 4 * rot + 2 * ((lane >> 3) & 1) + ((lane >> 2) & 1);
-      red[(j * NWB + warp) * 32 + (lane < 16 ? nf : 16 + nf)] = lane < 16 ? rb : rc;
     }
     __syncthreads();
     // one global reduction per (t, n) per block for dB and dC
@@ -858,6 +954,9 @@ __global__ void __launch_bounds__(GB) m3_bwd_kernel(BwdArgs a) {
 #pragma unroll
     for (int k = 0; k < WC; ++k) Pp[(size_t)(19 + k) * g.D + d] = dcw[k];
   }
+  tmem_fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem_slot, a.tcols);
 }
 
 // d_x at the last three steps of segment s needs dc from the first three
@@ -914,26 +1013,58 @@ __global__ void m3_bwd_finalize_kernel(BwdArgs a, int rows) {
 // host side
 // ---------------------------------------------------------------------------
 
-constexpr size_t SMEM_CAP = 227 * 1024;  // opt-in shared memory per block
+// opt-in shared memory per block, less 1 KB kept for static shared memory
+constexpr size_t SMEM_CAP = 227 * 1024 - 1024;
 constexpr int FWD_WARPS_PER_SM = 8;       // forward time split target
 constexpr int BWD_WAVES = 4;              // backward time split target
 
-// Largest chunk whose backward footprint fits one block's shared memory.
+// Tensor-memory columns a backward CTA allocates for K rows of 16 states:
+// a power of two >= 32 (the allocation granularity), at most 512.
+__host__ inline uint32_t tmem_cols_for(int K) {
+  uint32_t c = 32;
+  while (c < (uint32_t)K * NS) c <<= 1;
+  return c;
+}
+
+// Largest chunk whose backward fits: 16 K tensor-memory columns <= 512 and
+// the shared-memory footprint within one block's limit.
 __host__ inline int kmax_for(int es) {
   int k = KMAX;
-  while (k > 1 && bwd_smem(k, es).total > SMEM_CAP) --k;
+  while (k > 1 && (bwd_smem(k, es).total > SMEM_CAP || tmem_cols_for(k) > 512)) --k;
   return k;
+}
+
+// Shared memory to request per backward CTA: its footprint, raised if needed
+// so that no more CTAs fit on one SM than tensor memory can serve at once
+// (512 columns / tcols), so no allocation ever has to wait.
+__host__ inline size_t bwd_launch_smem(int K, int es, int smem_per_sm) {
+  const int max_ctas = 512 / (int)tmem_cols_for(K);
+  size_t need = bwd_smem(K, es).total;
+  const size_t floor_bytes = (size_t)smem_per_sm / (max_ctas + 1) + 1;  // > 1/(max+1) of the SM
+  if (need < floor_bytes) need = floor_bytes;
+  return align_up(need, 128);
 }
 
 struct DevInfo {
   bool attrs = false;
   int sms = 0;
+  int smem_per_sm = 0;
   int occ_fwd[2][KMAX + 1];  // [dtype][chunk] blocks per SM, 0 = not yet queried
   int occ_bwd[2][KMAX + 1];
 };
 
 std::mutex g_mu;
 DevInfo g_dev[64];
+thread_local cudaError_t g_last_cuda = cudaSuccess;  // last CUDA error this thread saw
+
+// Record a failed CUDA call (and clear the runtime's sticky-free error state).
+inline cudaError_t note(cudaError_t e) {
+  if (e != cudaSuccess) {
+    g_last_cuda = e;
+    cudaGetLastError();
+  }
+  return e;
+}
 
 template <typename T>
 cudaError_t set_attrs() {
@@ -949,12 +1080,12 @@ cudaError_t set_attrs() {
                            (int)agg_smem(es).total);
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(m3_bwd_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)bwd_smem(kmax_for(es), es).total);
+                              (int)SMEM_CAP);
 }
 
 // Device facts for the current device: kernel attributes are set once per
 // device (with that device current), occupancy is queried once per chunk.
-cudaError_t device_info(int chunk, int ai, int* sms, int* occ_f, int* occ_b) {
+cudaError_t device_info(int chunk, int ai, int* sms, int* occ_f, int* occ_b, int* smem_sm = nullptr) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -968,6 +1099,8 @@ cudaError_t device_info(int chunk, int ai, int* sms, int* occ_f, int* occ_b) {
     if (e != cudaSuccess) return e;
     e = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&di.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    if (e != cudaSuccess) return e;
     for (int a = 0; a < 2; ++a)
       for (int k = 0; k <= KMAX; ++k) di.occ_fwd[a][k] = di.occ_bwd[a][k] = 0;
     di.attrs = true;
@@ -979,19 +1112,22 @@ cudaError_t device_info(int chunk, int ai, int* sms, int* occ_f, int* occ_b) {
                                                         fwd_smem(2).total);
       if (e == cudaSuccess)
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ob, m3_bwd_kernel<__nv_bfloat16>, GB,
-                                                          bwd_smem(chunk, 2).total);
+                                                          bwd_launch_smem(chunk, 2, di.smem_per_sm));
     } else {
       e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&of, m3_fwd_kernel<float, true>, GF,
                                                         fwd_smem(4).total);
       if (e == cudaSuccess)
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ob, m3_bwd_kernel<float>, GB,
-                                                          bwd_smem(chunk, 4).total);
+                                                          bwd_launch_smem(chunk, 4, di.smem_per_sm));
     }
     if (e != cudaSuccess) return e;
+    // the tensor-memory budget must cover every resident backward CTA
+    if (ob * (int)tmem_cols_for(chunk) > 512) return cudaErrorInvalidConfiguration;
     di.occ_fwd[ai][chunk] = of > 0 ? of : 1;
     di.occ_bwd[ai][chunk] = ob > 0 ? ob : 1;
   }
   if (sms) *sms = di.sms;
+  if (smem_sm) *smem_sm = di.smem_per_sm;
   if (occ_f) *occ_f = di.occ_fwd[ai][chunk];
   if (occ_b) *occ_b = di.occ_bwd[ai][chunk];
   return cudaSuccess;
@@ -1057,10 +1193,8 @@ m3_status make_plan(const m3_dims* dm, m3_dtype act, Plan* p) {
     want_f = want_b = (int)dm->segments;
   } else if ((int64_t)p->B * p->T * p->D > 0) {
     int sms = 0, of = 0, ob = 0;
-    if (device_info(p->K, act == M3_BF16 ? 1 : 0, &sms, &of, &ob) != cudaSuccess) {
-      cudaGetLastError();
+    if (note(device_info(p->K, act == M3_BF16 ? 1 : 0, &sms, &of, &ob)) != cudaSuccess)
       return M3_ERR_CUDA;
-    }
     // Forward: a segment boundary costs a second pass over the earlier
     // segments, so split time only until about FWD_WARPS_PER_SM warps are
     // resident.  Backward: the aggregate pass is cheap next to the main
@@ -1129,37 +1263,36 @@ m3_status launch_fwd(const Plan& p, FwdArgs a, cudaStream_t st) {
     m3_fwd_carry_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(a);
   }
   m3_fwd_kernel<T, true><<<dim3(groups, p.Sf, p.B), GF, smem, st>>>(a);
-  return cudaGetLastError() == cudaSuccess ? M3_OK : M3_ERR_CUDA;
+  return note(cudaGetLastError()) == cudaSuccess ? M3_OK : M3_ERR_CUDA;
 }
 
 template <typename T>
-m3_status launch_bwd(const Plan& p, BwdArgs a, cudaStream_t st) {
+m3_status launch_bwd(const Plan& p, BwdArgs a, cudaStream_t st, int smem_per_sm) {
   const int groups = (p.D + GB - 1) / GB;
   a.g = Geo{p.B, p.T, p.D, p.K, p.nc, p.Sb, p.mb};
-  if (cudaMemsetAsync(a.dB, 0, (size_t)p.B * p.T * NS * 4, st) != cudaSuccess) return M3_ERR_CUDA;
-  if (cudaMemsetAsync(a.dC, 0, (size_t)p.B * p.T * NS * 4, st) != cudaSuccess) return M3_ERR_CUDA;
+  if (note(cudaMemsetAsync(a.dB, 0, (size_t)p.B * p.T * NS * 4, st)) != cudaSuccess) return M3_ERR_CUDA;
+  if (note(cudaMemsetAsync(a.dC, 0, (size_t)p.B * p.T * NS * 4, st)) != cudaSuccess) return M3_ERR_CUDA;
   if (p.Sb > 1) {
     m3_bwd_agg_kernel<T><<<dim3(groups, p.Sb - 1, p.B), GB, agg_smem(sizeof(T)).total, st>>>(a);
     const size_t n = (size_t)p.B * NS * p.D;
     m3_bwd_carry_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(a);
   }
-  m3_bwd_kernel<T><<<dim3(groups, p.Sb, p.B), GB, bwd_smem(p.K, sizeof(T)).total, st>>>(a);
+  a.tcols = tmem_cols_for(p.K);
+  m3_bwd_kernel<T><<<dim3(groups, p.Sb, p.B), GB, bwd_launch_smem(p.K, sizeof(T), smem_per_sm), st>>>(a);
   if (p.Sb > 1) {
     const size_t n = (size_t)p.B * (p.Sb - 1) * 3 * p.D;
     m3_bwd_fixup_kernel<T><<<(unsigned)((n + 255) / 256), 256, 0, st>>>(a);
   }
   const int nf = 23 * p.D;
   m3_bwd_finalize_kernel<<<(nf + 255) / 256, 256, 0, st>>>(a, p.B * p.Sb);
-  return cudaGetLastError() == cudaSuccess ? M3_OK : M3_ERR_CUDA;
+  return note(cudaGetLastError()) == cudaSuccess ? M3_OK : M3_ERR_CUDA;
 }
 
 // The device must have this library's kernels registered: fail early and
 // cleanly when the attribute setup cannot run (no device, wrong arch).
-m3_status ensure_device(int chunk) {
-  if (device_info(chunk, 0, nullptr, nullptr, nullptr) != cudaSuccess) {
-    cudaGetLastError();
-    return M3_ERR_CUDA;
-  }
+m3_status ensure_device(int chunk, int ai, int* smem_sm) {
+  int of = 0, ob = 0;
+  if (note(device_info(chunk, ai, nullptr, &of, &ob, smem_sm)) != cudaSuccess) return M3_ERR_CUDA;
   return M3_OK;
 }
 
@@ -1182,6 +1315,8 @@ const char* m3scan_status_string(m3_status s) {
 }
 
 int32_t m3scan_version(void) { return 100; }
+
+const char* m3scan_last_cuda_error(void) { return cudaGetErrorName(g_last_cuda); }
 
 m3_status m3scan_plan(const m3_dims* dims, m3_dtype act, m3_plan* out) {
   if (!out) return M3_ERR_NULL;
@@ -1223,7 +1358,8 @@ m3_status m3scan_fwd(const m3_dims* dims, m3_dtype act, const void* x, const voi
     if (workspace_bytes < p.ws_bytes) return M3_ERR_WORKSPACE;
     if (!aligned(workspace, 256)) return M3_ERR_ALIGN;
   }
-  if (ensure_device(p.K) != M3_OK) return M3_ERR_CUDA;
+  int smem_sm = 0;
+  if (ensure_device(p.K, act == M3_BF16 ? 1 : 0, &smem_sm) != M3_OK) return M3_ERR_CUDA;
   FwdArgs a{};
   a.x = x; a.dr = delta_raw; a.z = z; a.Bm = Bm; a.Cm = Cm;
   a.conv_w = conv_w; a.conv_b = conv_b; a.dt_bias = dt_bias; a.a_log = a_log; a.Dp = D;
@@ -1256,7 +1392,7 @@ m3_status m3scan_bwd(const m3_dims* dims, m3_dtype act, const void* x, const voi
           cudaMemsetAsync(d_dt_bias, 0, D_ * 4, s) != cudaSuccess ||
           cudaMemsetAsync(d_a_log, 0, D_ * NS * 4, s) != cudaSuccess ||
           cudaMemsetAsync(dD, 0, D_ * 4, s) != cudaSuccess) {
-        cudaGetLastError();
+        note(cudaGetLastError());
         return M3_ERR_CUDA;
       }
     }
@@ -1277,7 +1413,8 @@ m3_status m3scan_bwd(const m3_dims* dims, m3_dtype act, const void* x, const voi
   if (!workspace) return M3_ERR_WORKSPACE;
   if (workspace_bytes < p.ws_bytes) return M3_ERR_WORKSPACE;
   if (!aligned(workspace, 256)) return M3_ERR_ALIGN;
-  if (ensure_device(p.K) != M3_OK) return M3_ERR_CUDA;
+  int smem_sm = 0;
+  if (ensure_device(p.K, act == M3_BF16 ? 1 : 0, &smem_sm) != M3_OK) return M3_ERR_CUDA;
   BwdArgs a{};
   a.x = x; a.dr = delta_raw; a.z = z; a.Bm = Bm; a.Cm = Cm; a.dg = d_gated;
   a.conv_w = conv_w; a.conv_b = conv_b; a.dt_bias = dt_bias; a.a_log = a_log; a.Dp = D;
@@ -1296,7 +1433,8 @@ m3_status m3scan_bwd(const m3_dims* dims, m3_dtype act, const void* x, const voi
   a.d_conv_w = d_conv_w; a.d_conv_b = d_conv_b; a.d_dt_bias = d_dt_bias; a.d_a_log = d_a_log;
   a.dD = dD;
   a.accumulate = dims->accumulate_param_grads ? 1 : 0;
-  m3_status r = act == M3_BF16 ? launch_bwd<__nv_bfloat16>(p, a, s) : launch_bwd<float>(p, a, s);
+  m3_status r = act == M3_BF16 ? launch_bwd<__nv_bfloat16>(p, a, s, smem_sm)
+                                : launch_bwd<float>(p, a, s, smem_sm);
   if (r != M3_OK) cudaGetLastError();
   return r;
 }
@@ -1322,7 +1460,7 @@ m3_status noalloc_scratch(void** out) {
     void* p = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess || p == nullptr) {
-      cudaGetLastError();
+      note(e != cudaSuccess ? e : cudaErrorInvalidSymbol);
       return M3_ERR_CUDA;
     }
     g_noalloc_addr[dev] = p;

@@ -99,11 +99,13 @@ def test_plan_rejects_unknown_dtype_and_null(lib):
     assert binding.STATUS[lib.m3scan_plan(None, 1, None)] == "M3_ERR_NULL"
 
 
-def test_f32_chunk_limit_is_lower_than_bf16(lib):
-    st_b, _ = _plan(binding.make_dims(1, 64, 64, chunk=32, segments=1), binding.M3_BF16)
-    st_f, _ = _plan(binding.make_dims(1, 64, 64, chunk=32, segments=1), binding.M3_F32)
-    assert st_b == 0
-    assert binding.STATUS[st_f] == "M3_ERR_UNSUPPORTED"
+def test_chunk_limits_follow_the_backward_shared_memory(lib):
+    def st(chunk, act):
+        return binding.STATUS[_plan(binding.make_dims(1, 64, 64, chunk=chunk, segments=1), act)[0]]
+    assert st(30, binding.M3_BF16) == "M3_OK"
+    assert st(31, binding.M3_BF16) == "M3_ERR_UNSUPPORTED"
+    assert st(23, binding.M3_F32) == "M3_OK"
+    assert st(24, binding.M3_F32) == "M3_ERR_UNSUPPORTED"
 
 
 A = 1 << 20  # a 256-byte aligned fake address; never dereferenced

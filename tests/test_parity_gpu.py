@@ -47,7 +47,9 @@ SMALL = [
     (1, 2, 8, "bf16", 0, 0),
     (3, 3, 16, "f32", 1, 0),
     (1, 7, 64, "f32", 2, 3),
-    (2, 97, 72, "bf16", 32, 2),
+    (2, 97, 72, "bf16", 28, 2),
+    (2, 97, 72, "f32", 23, 3),
+    (2, 97, 72, "bf16", 30, 3),
     (1, 130, 200, "f32", 7, 5),
     (4, 33, 520, "bf16", 16, 2),
 ]
