@@ -214,7 +214,7 @@ struct BwdArgs {
   const float *conv_w, *conv_b, *dt_bias, *a_log, *Dp, *ckpt;
   void *dx, *ddr, *dz, *du_dbg;
   float *dB, *dC;
-  float *q, *sd, *gin, *dxpart, *dchead, *partials;
+  float *q, *sd, *dxpart, *dchead, *partials;
   float *d_conv_w, *d_conv_b, *d_dt_bias, *d_a_log, *dD;
   int accumulate;
   uint32_t tcols;  // tensor-memory columns per CTA for the state history
@@ -334,12 +334,23 @@ __global__ void __launch_bounds__(GF) m3_fwd_kernel(FwdArgs a) {
 
   float2 h[NS / 2];
 #pragma unroll
-  for (int i = 0; i < NS / 2; ++i) {
-    if (FINAL && s > 0 && active) {
-      const float* ck = a.ckpt + (((size_t)b * g.nc + c_begin) * NS + 2 * i) * g.D + d;
-      h[i] = make_float2(ck[0], ck[g.D]);
-    } else {
-      h[i] = make_float2(0.f, 0.f);
+  for (int i = 0; i < NS / 2; ++i) h[i] = make_float2(0.f, 0.f);
+  if (FINAL && s > 0) {
+    // The scan is linear in the state: chain the earlier segments' local end
+    // states with their decays, start(s'+1) = exp(A sum delta_s') start(s') +
+    // local_end(s'), to get this segment's true start state.
+    const float* __restrict__ agg_s = a.agg_s;
+    const float* __restrict__ agg_h = a.agg_h;
+#pragma unroll 2
+    for (int sp = 0; sp < s; ++sp) {
+      const size_t bs = (size_t)b * g.S + sp;
+      const float2 dl2 = f2b(active ? agg_s[bs * g.D + d] : 0.f);
+#pragma unroll
+      for (int i = 0; i < NS / 2; ++i) {
+        const float* ah = agg_h + (bs * NS + 2 * i) * g.D + d;
+        const float2 loc = active ? make_float2(ah[0], ah[g.D]) : make_float2(0.f, 0.f);
+        h[i] = __ffma2_rn(ex2x2(__fmul2_rn(dl2, a2[i])), h[i], loc);
+      }
     }
   }
 
@@ -414,7 +425,7 @@ __global__ void __launch_bounds__(GF) m3_fwd_kernel(FwdArgs a) {
         if (FINAL) {
           if (kc == 0) {
             const int t = t0 + j0 + j;
-            if (active && (t > t_begin || s == 0)) {
+            if (active) {
               float* ck = a.ckpt + (((size_t)b * g.nc + t / g.K) * NS) * g.D + d;
 #pragma unroll
               for (int i = 0; i < NS / 2; ++i) {
@@ -475,28 +486,6 @@ __global__ void __launch_bounds__(GF) m3_fwd_kernel(FwdArgs a) {
   }
 }
 
-// Chain the forward segments: start(0) = 0, start(s+1) = decay(s) * start(s)
-// + local_end(s), with decay(s) = exp(A * sum of delta over segment s).
-// Writes each segment's start state into the checkpoint of its first chunk.
-__global__ void m3_fwd_carry_kernel(FwdArgs a) {
-  const Geo g = a.g;
-  const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const size_t total = (size_t)g.B * NS * g.D;
-  if (idx >= total) return;
-  const int d = (int)(idx % g.D);
-  const int n = (int)((idx / g.D) % NS);
-  const int b = (int)(idx / ((size_t)g.D * NS));
-  const float A2 = -expf(a.a_log[(size_t)d * NS + n]) * LOG2E;
-  float h = 0.f;
-  for (int s = 0; s < g.S; ++s) {
-    a.ckpt[(((size_t)b * g.nc + (size_t)s * g.m) * NS + n) * g.D + d] = h;
-    if (s + 1 < g.S) {
-      const size_t bs = (size_t)b * g.S + s;
-      h = fmaf(ex2(A2 * a.agg_s[bs * g.D + d]), h, a.agg_h[(bs * NS + n) * g.D + d]);
-    }
-  }
-}
-
 // ---------------------------------------------------------------------------
 // backward aggregate (segments 1..S-1): the adjoint carry a segment passes to
 // its predecessor when nothing enters it from the right,
@@ -531,6 +520,17 @@ __global__ void __launch_bounds__(GB) m3_bwd_agg_kernel(BwdArgs a) {
   for (int i = 0; i < NS / 2; ++i) carry[i] = make_float2(0.f, 0.f);
   float sdelta = 0.f;
 
+  {
+    // dB and dC are sums over channel groups (global reductions in the main
+    // kernel): this kernel runs before it, so it clears them.
+    const size_t ncta = (size_t)gridDim.x * gridDim.y * gridDim.z;
+    const size_t cid = blockIdx.x + (size_t)gridDim.x * (blockIdx.y + (size_t)gridDim.y * blockIdx.z);
+    const size_t total = (size_t)g.B * g.T * NS;
+    for (size_t i = cid * GB + tid; i < total; i += ncta * GB) {
+      a.dB[i] = 0.f;
+      a.dC[i] = 0.f;
+    }
+  }
   const int ntiles = (t_end - t_begin + TT - 1) / TT;
   auto tile_start = [&](int i) { return max(t_begin, t_end - (i + 1) * TT); };
   auto stage = [&](int i, int buf) {
@@ -600,25 +600,6 @@ __global__ void __launch_bounds__(GB) m3_bwd_agg_kernel(BwdArgs a) {
   }
 }
 
-// Chain the backward segments right to left: in(S-1) = 0,
-// in(s-1) = decay(s) * in(s) + local(s).
-__global__ void m3_bwd_carry_kernel(BwdArgs a) {
-  const Geo g = a.g;
-  const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const size_t total = (size_t)g.B * NS * g.D;
-  if (idx >= total) return;
-  const int d = (int)(idx % g.D);
-  const int n = (int)((idx / g.D) % NS);
-  const int b = (int)(idx / ((size_t)g.D * NS));
-  const float A2 = -expf(a.a_log[(size_t)d * NS + n]) * LOG2E;
-  float c = 0.f;
-  for (int s = g.S - 1; s >= 0; --s) {
-    const size_t bs = (size_t)b * g.S + s;
-    a.gin[(bs * NS + n) * g.D + d] = c;
-    if (s >= 1) c = fmaf(ex2(A2 * a.sd[bs * g.D + d]), c, a.q[(bs * NS + n) * g.D + d]);
-  }
-}
-
 // ---------------------------------------------------------------------------
 // backward main kernel
 //
@@ -674,7 +655,6 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(BwdArgs a) {
   const BwdSmem L = bwd_smem(K, sizeof(T));
   float* fB = reinterpret_cast<float*>(smem + L.fB);
   float* fC = reinterpret_cast<float*>(smem + L.fC);
-  float4* scal = reinterpret_cast<float4*>(smem + L.scal);
   float* red = reinterpret_cast<float*>(smem + L.red);
   // state lane of register slot 2*i (pair i): quad (i >> 1) ^ rot, offset 2*(i & 1)
   auto lane_of = [&](int i) { return 4 * ((i >> 1) ^ rot) + 2 * (i & 1); };
@@ -710,11 +690,22 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(BwdArgs a) {
   // exp(delta_{t+1} A) dh_{t+1}
   float2 carry[NS / 2];
 #pragma unroll
-  for (int i = 0; i < NS / 2; ++i) {
-    carry[i] = make_float2(0.f, 0.f);
-    if (g.S > 1 && active) {
-      const float* gi = a.gin + (((size_t)b * g.S + s) * NS + lane_of(i)) * g.D + d;
-      carry[i] = make_float2(gi[0], gi[g.D]);
+  for (int i = 0; i < NS / 2; ++i) carry[i] = make_float2(0.f, 0.f);
+  if (s + 1 < g.S) {
+    // chain the later segments right to left: in(s'-1) = exp(A sum delta_s')
+    // in(s') + local(s'), with in(S-1) = 0
+    const float* __restrict__ sd = a.sd;
+    const float* __restrict__ q = a.q;
+#pragma unroll 2
+    for (int sp = g.S - 1; sp > s; --sp) {
+      const size_t bs = (size_t)b * g.S + sp;
+      const float2 dl2 = f2b(active ? sd[bs * g.D + d] : 0.f);
+#pragma unroll
+      for (int i = 0; i < NS / 2; ++i) {
+        const float* qq = q + (bs * NS + lane_of(i)) * g.D + d;
+        const float2 loc = active ? make_float2(qq[0], qq[g.D]) : make_float2(0.f, 0.f);
+        carry[i] = __ffma2_rn(ex2x2(__fmul2_rn(dl2, a2[i])), carry[i], loc);
+      }
     }
   }
   float2 dAp[NS / 2];  // dL/dA per lane
@@ -769,164 +760,170 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(BwdArgs a) {
 
     float4* s0 = reinterpret_cast<float4*>(smem + L.scal) + tid;  // thread-private, stride GB
     float4* s1 = s0 + (size_t)K * GB;
+    T* const dz_c = static_cast<T*>(a.dz) + ((size_t)b * g.T + (size_t)c * K) * g.D + d;
+    T* const ddr_c = static_cast<T*>(a.ddr) + ((size_t)b * g.T + (size_t)c * K) * g.D + d;
+    T* const dx_c = static_cast<T*>(a.dx) + ((size_t)b * g.T + (size_t)c * K) * g.D + d;
+    T* const du_c = a.du_dbg ? static_cast<T*>(a.du_dbg) + ((size_t)b * g.T + (size_t)c * K) * g.D + d
+                             : nullptr;
 
-    // ---- scalar pass: everything per step that does not need the state ----
+    // The four passes over the chunk.
     {
-      float xm3 = Act<T>::ld(xt + 0 * GB + tid);
-      float xm2 = Act<T>::ld(xt + 1 * GB + tid);
-      float xm1 = Act<T>::ld(xt + 2 * GB + tid);
-      for (int j = 0; j < steps; ++j) {
-        const float xv = Act<T>::ld(xt + (j + 3) * GB + tid);
-        const float cpre = fmaf(w[0], xm3, fmaf(w[1], xm2, fmaf(w[2], xm1, fmaf(w[3], xv, cb))));
-        xm3 = xm2;
-        xm2 = xm1;
-        xm1 = xv;
-        const float sc = sigmoid_f(cpre);
-        const float u = cpre * sc;
-        const float v = Act<T>::ld(drt + j * GB + tid) + dtb;
-        const float delta = softplus_f(v);
-        const float sv = sigmoid_f(v);
-        const float zv = Act<T>::ld(zt + j * GB + tid);
-        const float gv = Act<T>::ld(dgt + j * GB + tid);
-        const float sz = sigmoid_f(zv);
-        const float dy = gv * zv * sz;                           // dL/dy
-        const float dzf = gv * (sz * fmaf(zv, 1.f - sz, 1.f));    // dL/dz = y * dzf
-        s0[j * GB] = make_float4(delta, delta * u, dy, dzf);
-        s1[j * GB] = make_float4(Dd * u, sv, sc, cpre);
-      }
-    }
+      const int nst = steps;
 
-    // ---- recompute the chunk's states from its start state; dz needs y ----
-    {
-      float2 h[NS / 2];
-#pragma unroll
-      for (int i = 0; i < NS / 2; ++i) {
-        const int n = lane_of(i);
-        h[i] = make_float2(ckt[n * GB + tid], ckt[(n + 1) * GB + tid]);
-      }
-      for (int j = 0; j < steps; ++j) {
-        const float4 v0 = s0[j * GB];
-        const float Du = s1[j * GB].x;
-        const float2 dl2 = f2b(v0.x);
-        const float2 du2 = f2b(v0.y);
-        const float4* B4 = reinterpret_cast<const float4*>(fB + j * NS);
-        const float4* C4 = reinterpret_cast<const float4*>(fC + j * NS);
-        float2 y01 = make_float2(0.f, 0.f), y23 = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int qs = 0; qs < 4; ++qs) {
-          const float4 bv = B4[qs ^ rot];
-          const float4 cv = C4[qs ^ rot];
-          const float2 dA0 = ex2x2(__fmul2_rn(dl2, a2[2 * qs]));
-          const float2 dA1 = ex2x2(__fmul2_rn(dl2, a2[2 * qs + 1]));
-          h[2 * qs] = __ffma2_rn(dA0, h[2 * qs], __fmul2_rn(du2, make_float2(bv.x, bv.y)));
-          h[2 * qs + 1] = __ffma2_rn(dA1, h[2 * qs + 1], __fmul2_rn(du2, make_float2(bv.z, bv.w)));
-          y01 = __ffma2_rn(make_float2(cv.x, cv.y), h[2 * qs], y01);
-          y23 = __ffma2_rn(make_float2(cv.z, cv.w), h[2 * qs + 1], y23);
+      // ---- scalar pass: everything per step that does not need the state ----
+      {
+        float xm3 = Act<T>::ld(xt + 0 * GB + tid);
+        float xm2 = Act<T>::ld(xt + 1 * GB + tid);
+        float xm1 = Act<T>::ld(xt + 2 * GB + tid);
+        for (int j = 0; j < nst; ++j) {
+          const float xv = Act<T>::ld(xt + (j + 3) * GB + tid);
+          const float cpre = fmaf(w[0], xm3, fmaf(w[1], xm2, fmaf(w[2], xm1, fmaf(w[3], xv, cb))));
+          xm3 = xm2;
+          xm2 = xm1;
+          xm1 = xv;
+          const float sc = sigmoid_f(cpre);
+          const float u = cpre * sc;
+          const float v = Act<T>::ld(drt + j * GB + tid) + dtb;
+          const float delta = softplus_f(v);
+          const float sv = sigmoid_f(v);
+          const float zv = Act<T>::ld(zt + j * GB + tid);
+          const float gv = Act<T>::ld(dgt + j * GB + tid);
+          const float sz = sigmoid_f(zv);
+          const float dy = gv * zv * sz;                           // dL/dy
+          const float dzf = gv * (sz * fmaf(zv, 1.f - sz, 1.f));    // dL/dz = y * dzf
+          s0[j * GB] = make_float4(delta, delta * u, dy, dzf);
+          s1[j * GB] = make_float4(Dd * u, sv, sc, cpre);
         }
-        tmem_st16(trow + 16u * (uint32_t)j, h);
-        const float y = ((y01.x + y01.y) + (y23.x + y23.y)) + Du;
-        if (active)
-          Act<T>::st(static_cast<T*>(a.dz) + ((size_t)b * g.T + c * K + j) * g.D + d, y * v0.w);
       }
-      tmem_wait_st();
-    }
 
-    // ---- reverse-time pass over the chunk: adjoint state, dA, dB/dC ----
-    {
-      float2 hn[NS / 2];  // h_t (state after step t)
-      tmem_ld16(trow + 16u * (uint32_t)(steps - 1), hn);
-      tmem_wait_ld();
-      for (int j = steps - 1; j >= 0; --j) {
-        const float4 v0 = s0[j * GB];
-        const float2 dl2 = f2b(v0.x);
-        const float2 du2 = f2b(v0.y);
-        const float2 dy2 = f2b(v0.z);
-        float2 sB = make_float2(0.f, 0.f), sAq = make_float2(0.f, 0.f);
-        float pB[NS], pC[NS];
-        float2 hp[NS / 2];  // h_{t-1}
-        if (j > 0) {
-          tmem_ld16(trow + 16u * (uint32_t)(j - 1), hp);
-          tmem_wait_ld();
-        } else {
+      // ---- recompute the chunk's states from its start state ----
+      {
+        float2 h[NS / 2];
+#pragma unroll
+        for (int i = 0; i < NS / 2; ++i) {
+          const int n = lane_of(i);
+          h[i] = make_float2(ckt[n * GB + tid], ckt[(n + 1) * GB + tid]);
+        }
+        for (int j = 0; j < nst; ++j) {
+          const float4 v0 = s0[j * GB];
+          const float2 dl2 = f2b(v0.x);
+          const float2 du2 = f2b(v0.y);
+          const float4* B4 = reinterpret_cast<const float4*>(fB + j * NS);
+#pragma unroll
+          for (int qs = 0; qs < 4; ++qs) {
+            const float4 bv = B4[qs ^ rot];
+            const float2 dA0 = ex2x2(__fmul2_rn(dl2, a2[2 * qs]));
+            const float2 dA1 = ex2x2(__fmul2_rn(dl2, a2[2 * qs + 1]));
+            h[2 * qs] = __ffma2_rn(dA0, h[2 * qs], __fmul2_rn(du2, make_float2(bv.x, bv.y)));
+            h[2 * qs + 1] = __ffma2_rn(dA1, h[2 * qs + 1], __fmul2_rn(du2, make_float2(bv.z, bv.w)));
+          }
+          tmem_st16(trow + 16u * (uint32_t)j, h);
+        }
+        tmem_wait_st();
+      }
+
+      // ---- reverse-time pass: y and dz, adjoint state, dA, dB/dC ----
+      {
+        float2 hn[NS / 2];  // h_t (state after step t)
+        tmem_ld16(trow + 16u * (uint32_t)(nst - 1), hn);
+        tmem_wait_ld();
+        for (int j = nst - 1; j >= 0; --j) {
+          const float4 v0 = s0[j * GB];
+          const float Du = reinterpret_cast<const float*>(s1 + j * GB)[0];
+          const float2 dl2 = f2b(v0.x);
+          const float2 du2 = f2b(v0.y);
+          const float2 dy2 = f2b(v0.z);
+          float2 sB = make_float2(0.f, 0.f), sAq = make_float2(0.f, 0.f);
+          float2 y01 = make_float2(0.f, 0.f), y23 = make_float2(0.f, 0.f);
+          float2 pB[NS / 2], pC[NS / 2];
+          float2 hp[NS / 2];  // h_{t-1}
+          if (j > 0) {
+            tmem_ld16(trow + 16u * (uint32_t)(j - 1), hp);
+            tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int i = 0; i < NS / 2; ++i) {
+              const int n = lane_of(i);
+              hp[i] = make_float2(ckt[n * GB + tid], ckt[(n + 1) * GB + tid]);
+            }
+          }
+          const float4* B4 = reinterpret_cast<const float4*>(fB + j * NS);
+          const float4* C4 = reinterpret_cast<const float4*>(fC + j * NS);
+#pragma unroll
+          for (int qs = 0; qs < 4; ++qs) {
+            const float4 bv = B4[qs ^ rot];
+            const float4 cv = C4[qs ^ rot];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int i = 2 * qs + e;
+              const float2 bb = e ? make_float2(bv.z, bv.w) : make_float2(bv.x, bv.y);
+              const float2 cc = e ? make_float2(cv.z, cv.w) : make_float2(cv.x, cv.y);
+              if (e) y23 = __ffma2_rn(cc, hn[i], y23); else y01 = __ffma2_rn(cc, hn[i], y01);
+              const float2 dh = __ffma2_rn(dy2, cc, carry[i]);            // dL/dh_t
+              pC[i] = __fmul2_rn(dy2, hn[i]);                              // dC partial
+              pB[i] = __fmul2_rn(dh, du2);                                 // dB partial
+              sB = __ffma2_rn(dh, bb, sB);
+              carry[i] = __fmul2_rn(ex2x2(__fmul2_rn(dl2, a2[i])), dh);    // exp(delta A) dh
+              const float2 qv = __fmul2_rn(carry[i], hp[i]);               // dh exp(delta A) h_{t-1}
+              dAp[i] = __ffma2_rn(dl2, qv, dAp[i]);
+              sAq = __ffma2_rn(a2[i], qv, sAq);
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < NS / 2; ++i) hn[i] = hp[i];
+          const float y = ((y01.x + y01.y) + (y23.x + y23.y)) + Du;
+          if (active) Act<T>::st(dz_c + (size_t)j * g.D, y * v0.w);
+          // the scalar pass below reads these two sums
+          reinterpret_cast<float*>(s0 + j * GB)[3] = sAq.x + sAq.y;
+          reinterpret_cast<float*>(s1 + j * GB)[0] = sB.x + sB.y;
+          float vb[NS], vc[NS];
 #pragma unroll
           for (int i = 0; i < NS / 2; ++i) {
-            const int n = lane_of(i);
-            hp[i] = make_float2(ckt[n * GB + tid], ckt[(n + 1) * GB + tid]);
+            vb[2 * i] = active ? pB[i].x : 0.f;
+            vb[2 * i + 1] = active ? pB[i].y : 0.f;
+            vc[2 * i] = active ? pC[i].x : 0.f;
+            vc[2 * i + 1] = active ? pC[i].y : 0.f;
           }
+          const float rb = warp_sum16_rotated(vb, lane);
+          const float rc = warp_sum16_rotated(vc, lane);
+          const int nf = 4 * rot + 2 * ((lane >> 3) & 1) + ((lane >> 2) & 1);
+          red[(j * NWB + warp) * 32 + (lane < 16 ? nf : 16 + nf)] = lane < 16 ? rb : rc;
         }
-        const float4* B4 = reinterpret_cast<const float4*>(fB + j * NS);
-        const float4* C4 = reinterpret_cast<const float4*>(fC + j * NS);
+      }
+
+      // ---- scalar pass: du, d delta, softplus, SiLU and conv backward ----
+      for (int j = nst - 1; j >= 0; --j) {
+        const int t = c * K + j;
+        const float4 v0 = s0[j * GB];
+        const float4 v1 = s1[j * GB];
+        const float delta = v0.x, dy = v0.z, sAq = v0.w;
+        const float sumB = v1.x, sv = v1.y, sc = v1.z, cpre = v1.w;
+        const float u = cpre * sc;
+        const float du = fmaf(dy, Dd, delta * sumB);
+        const float ddr = fmaf(u, sumB, LN2 * sAq) * sv;
+        dD_acc = fmaf(dy, u, dD_acc);
+        ddtb_acc += ddr;
+        const float dc = du * (sc * fmaf(cpre, 1.f - sc, 1.f));
+        dcb_acc += dc;
 #pragma unroll
-        for (int qs = 0; qs < 4; ++qs) {
-          const float4 bv = B4[qs ^ rot];
-          const float4 cv = C4[qs ^ rot];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int i = 2 * qs + e;
-            const float2 bb = e ? make_float2(bv.z, bv.w) : make_float2(bv.x, bv.y);
-            const float2 cc = e ? make_float2(cv.z, cv.w) : make_float2(cv.x, cv.y);
-            const float2 dh = __ffma2_rn(dy2, cc, carry[i]);            // dL/dh_t
-            const float2 pc = __fmul2_rn(dy2, hn[i]);                    // dC partial
-            const float2 pb = __fmul2_rn(dh, du2);                       // dB partial
-            sB = __ffma2_rn(dh, bb, sB);
-            carry[i] = __fmul2_rn(ex2x2(__fmul2_rn(dl2, a2[i])), dh);    // exp(delta A) dh
-            const float2 qv = __fmul2_rn(carry[i], hp[i]);               // dh exp(delta A) h_{t-1}
-            dAp[i] = __ffma2_rn(dl2, qv, dAp[i]);
-            sAq = __ffma2_rn(a2[i], qv, sAq);
-            pB[2 * i] = pb.x;
-            pB[2 * i + 1] = pb.y;
-            pC[2 * i] = pc.x;
-            pC[2 * i + 1] = pc.y;
-          }
+        for (int k = 0; k < WC; ++k) dcw[k] = fmaf(dc, Act<T>::ld(xt + (j + k) * GB + tid), dcw[k]);
+        const float dxv = fmaf(dc, w[3], fmaf(dc1, w[2], fmaf(dc2, w[1], dc3 * w[0])));
+        dc3 = dc2;
+        dc2 = dc1;
+        dc1 = dc;
+        if (active) {
+          Act<T>::st(ddr_c + (size_t)j * g.D, ddr);
+          if (du_c) Act<T>::st(du_c + (size_t)j * g.D, du);
+          if (s + 1 < g.S && t >= t_end - 3)
+            a.dxpart[(((size_t)b * g.S + s) * 3 + (t - (t_end - 3))) * g.D + d] = dxv;
+          else
+            Act<T>::st(dx_c + (size_t)j * g.D, dxv);
+          if (s > 0 && t < t_begin + 3)
+            a.dchead[(((size_t)b * g.S + s) * 3 + (t - t_begin)) * g.D + d] = dc;
         }
-#pragma unroll
-        for (int i = 0; i < NS / 2; ++i) hn[i] = hp[i];
-        // the scalar pass below reads these two sums
-        reinterpret_cast<float*>(s0 + j * GB)[3] = sAq.x + sAq.y;
-        reinterpret_cast<float*>(s1 + j * GB)[0] = sB.x + sB.y;
-        if (!active) {
-#pragma unroll
-          for (int n = 0; n < NS; ++n) pB[n] = pC[n] = 0.f;
-        }
-        const float rb = warp_sum16_rotated(pB, lane);
-        const float rc = warp_sum16_rotated(pC, lane);
-        const int nf = 4 * rot + 2 * ((lane >> 3) & 1) + ((lane >> 2) & 1);
-        red[(j * NWB + warp) * 32 + (lane < 16 ? nf : 16 + nf)] = lane < 16 ? rb : rc;
       }
     }
 
-    // ---- scalar pass: du, d delta, softplus, SiLU and conv backward ----
-    for (int j = steps - 1; j >= 0; --j) {
-      const int t = c * K + j;
-      const float4 v0 = s0[j * GB];
-      const float4 v1 = s1[j * GB];
-      const float delta = v0.x, dy = v0.z, sAq = v0.w;
-      const float sumB = v1.x, sv = v1.y, sc = v1.z, cpre = v1.w;
-      const float u = cpre * sc;
-      const float du = fmaf(dy, Dd, delta * sumB);
-      const float ddr = fmaf(u, sumB, LN2 * sAq) * sv;
-      dD_acc = fmaf(dy, u, dD_acc);
-      ddtb_acc += ddr;
-      const float dc = du * (sc * fmaf(cpre, 1.f - sc, 1.f));
-      dcb_acc += dc;
-#pragma unroll
-      for (int k = 0; k < WC; ++k) dcw[k] = fmaf(dc, Act<T>::ld(xt + (j + k) * GB + tid), dcw[k]);
-      const float dxv = fmaf(dc, w[3], fmaf(dc1, w[2], fmaf(dc2, w[1], dc3 * w[0])));
-      dc3 = dc2;
-      dc2 = dc1;
-      dc1 = dc;
-      if (active) {
-        const size_t i = ((size_t)b * g.T + t) * g.D + d;
-        Act<T>::st(static_cast<T*>(a.ddr) + i, ddr);
-        if (a.du_dbg) Act<T>::st(static_cast<T*>(a.du_dbg) + i, du);
-        if (s + 1 < g.S && t >= t_end - 3)
-          a.dxpart[(((size_t)b * g.S + s) * 3 + (t - (t_end - 3))) * g.D + d] = dxv;
-        else
-          Act<T>::st(static_cast<T*>(a.dx) + i, dxv);
-        if (s > 0 && t < t_begin + 3)
-          a.dchead[(((size_t)b * g.S + s) * 3 + (t - t_begin)) * g.D + d] = dc;
-      }
-    }
     __syncthreads();
     // one global reduction per (t, n) per block for dB and dC
     for (int i = tid; i < steps * 32; i += GB) {
@@ -959,40 +956,54 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(BwdArgs a) {
   if (warp == 0) tmem_dealloc(tmem_slot, a.tcols);
 }
 
-// d_x at the last three steps of segment s needs dc from the first three
-// steps of segment s+1: complete and store them.
+// The backward's last kernel, two roles by block index.
+//  - blocks [0, nfin): parameter gradients, the per-(batch, segment) partials
+//    summed in a fixed order (one warp per output: lane l sums rows l, l+32,
+//    ..., then a fixed shuffle tree), so the result is deterministic;
+//  - blocks [nfin, ...): d_x at the last three steps of each segment but the
+//    last, which needs the conv gradient of the next segment's first steps.
 template <typename T>
-__global__ void m3_bwd_fixup_kernel(BwdArgs a) {
+__global__ void m3_bwd_tail_kernel(BwdArgs a, int rows, int nfin) {
   const Geo g = a.g;
-  const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const size_t total = (size_t)g.B * (g.S - 1) * 3 * g.D;
-  if (idx >= total) return;
-  const int d = (int)(idx % g.D);
-  size_t rest = idx / g.D;
-  const int j = (int)(rest % 3);
-  rest /= 3;
-  const int s = (int)(rest % (g.S - 1));
-  const int b = (int)(rest / (g.S - 1));
-  const int t_end = min((s + 1) * g.m * g.K, g.T);
-  const int t = t_end - 3 + j;
-  float v = a.dxpart[(((size_t)b * g.S + s) * 3 + j) * g.D + d];
-  for (int k = 0; k < WC; ++k) {
-    const int tp = t + 3 - k;
-    if (tp >= t_end && tp < g.T)
-      v = fmaf(a.dchead[(((size_t)b * g.S + s + 1) * 3 + (tp - t_end)) * g.D + d],
-               a.conv_w[(size_t)d * WC + k], v);
+  if ((int)blockIdx.x >= nfin) {
+    const size_t idx = (size_t)(blockIdx.x - nfin) * blockDim.x + threadIdx.x;
+    const size_t total = (size_t)g.B * (g.S - 1) * 3 * g.D;
+    if (idx >= total) return;
+    const int d = (int)(idx % g.D);
+    size_t rest = idx / g.D;
+    const int j = (int)(rest % 3);
+    rest /= 3;
+    const int s = (int)(rest % (g.S - 1));
+    const int b = (int)(rest / (g.S - 1));
+    const int t_end = min((s + 1) * g.m * g.K, g.T);
+    const int t = t_end - 3 + j;
+    float v = a.dxpart[(((size_t)b * g.S + s) * 3 + j) * g.D + d];
+    for (int k = 0; k < WC; ++k) {
+      const int tp = t + 3 - k;
+      if (tp >= t_end && tp < g.T)
+        v = fmaf(a.dchead[(((size_t)b * g.S + s + 1) * 3 + (tp - t_end)) * g.D + d],
+                 a.conv_w[(size_t)d * WC + k], v);
+    }
+    Act<T>::st(static_cast<T*>(a.dx) + ((size_t)b * g.T + t) * g.D + d, v);
+    return;
   }
-  Act<T>::st(static_cast<T*>(a.dx) + ((size_t)b * g.T + t) * g.D + d, v);
-}
-
-// Sum the per-(batch, segment) parameter partials in a fixed order.
-__global__ void m3_bwd_finalize_kernel(BwdArgs a, int rows) {
-  const Geo g = a.g;
-  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= 23 * g.D) return;
-  const int jj = idx / g.D, d = idx - jj * g.D;
-  float v = 0.f;
-  for (int r = 0; r < rows; ++r) v += a.partials[((size_t)r * NPART + jj) * g.D + d];
+  const int widx = (int)(((size_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (widx >= 23 * g.D) return;  // whole warps exit together
+  const int jj = widx / g.D, d = widx - jj * g.D;
+  const float* __restrict__ P = a.partials + (size_t)jj * g.D + d;
+  const size_t stride = (size_t)NPART * g.D;
+  float v0 = 0.f, v1 = 0.f;
+  int r = lane;
+  for (; r + 32 < rows; r += 64) {
+    v0 += P[(size_t)r * stride];
+    v1 += P[(size_t)(r + 32) * stride];
+  }
+  if (r < rows) v0 += P[(size_t)r * stride];
+  float v = v0 + v1;
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  if (lane != 0) return;
   float* dst;
   if (jj < NS) {
     v *= -expf(a.a_log[(size_t)d * NS + jj]);  // dL/da_log = dL/dA * A
@@ -1015,8 +1026,6 @@ __global__ void m3_bwd_finalize_kernel(BwdArgs a, int rows) {
 
 // opt-in shared memory per block, less 1 KB kept for static shared memory
 constexpr size_t SMEM_CAP = 227 * 1024 - 1024;
-constexpr int FWD_WARPS_PER_SM = 8;       // forward time split target
-constexpr int BWD_WAVES = 4;              // backward time split target
 
 // Tensor-memory columns a backward CTA allocates for K rows of 16 states:
 // a power of two >= 32 (the allocation granularity), at most 512.
@@ -1070,17 +1079,27 @@ template <typename T>
 cudaError_t set_attrs() {
   const int es = sizeof(T);
   cudaError_t e;
+  // every kernel here wants all of the unified L1/shared storage as shared
+  // memory, so that the occupancy the runtime reports is the one it launches
   e = cudaFuncSetAttribute(m3_fwd_kernel<T, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)fwd_smem(es).total);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(m3_fwd_kernel<T, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)fwd_smem(es).total);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(m3_bwd_agg_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)agg_smem(es).total);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(m3_bwd_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)SMEM_CAP);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(m3_fwd_kernel<T, true>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(m3_fwd_kernel<T, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)fwd_smem(es).total);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(m3_fwd_kernel<T, false>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(m3_bwd_agg_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)agg_smem(es).total);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(m3_bwd_agg_kernel<T>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(m3_bwd_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_CAP);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(m3_bwd_kernel<T>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+  return e;
 }
 
 // Device facts for the current device: kernel attributes are set once per
@@ -1139,7 +1158,7 @@ struct Plan {
   size_t ckpt_bytes, ws_bytes;
   // workspace offsets (bytes)
   size_t f_aggh, f_aggs;
-  size_t b_part, b_q, b_sd, b_gin, b_dxpart, b_dchead;
+  size_t b_part, b_q, b_sd, b_dxpart, b_dchead;
   int fwd_launches, bwd_launches;
 };
 
@@ -1162,6 +1181,22 @@ void fix_segments(int nc, int K, int want, int* S, int* m) {
   *m = mm;
 }
 
+// Segment count: the largest split whose CTAs fit in `waves` waves of
+// resident CTAs, with at least two chunks per segment (measured on GB300:
+// the forward gains little beyond a wave or two, since its aggregate pass
+// repeats most of its work; the backward keeps gaining up to several waves).
+int choose_segments(int nc, int K, int64_t groups, int64_t cap, int waves) {
+  if (groups < 1) groups = 1;
+  int64_t want = waves * cap / groups;
+  if (want < 1) want = 1;
+  const int64_t max_s = (nc + 1) / 2;  // >= 2 chunks per segment
+  if (want > max_s) want = max_s;
+  if (want < 1) want = 1;
+  int S = 1, m = 1;
+  fix_segments(nc, K, (int)want, &S, &m);
+  return S;
+}
+
 m3_status validate_dims(const m3_dims* dm, m3_dtype act) {
   if (!dm) return M3_ERR_NULL;
   if (act != M3_F32 && act != M3_BF16) return M3_ERR_UNSUPPORTED;
@@ -1174,7 +1209,7 @@ m3_status validate_dims(const m3_dims* dm, m3_dtype act) {
   if (dm->batch > 65535 || dm->seq_len > (int64_t)1 << 30 || dm->d_inner > (int64_t)1 << 24)
     return M3_ERR_DIMS;
   if (dm->segments > 65535) return M3_ERR_DIMS;
-  if (dm->batch * dm->d_inner > ((int64_t)1 << 27)) return M3_ERR_DIMS;  // 1-D grids of the carry passes
+  if (dm->batch * dm->d_inner > ((int64_t)1 << 27)) return M3_ERR_DIMS;  // 1-D grid of the tail kernel
   return M3_OK;
 }
 
@@ -1195,17 +1230,8 @@ m3_status make_plan(const m3_dims* dm, m3_dtype act, Plan* p) {
     int sms = 0, of = 0, ob = 0;
     if (note(device_info(p->K, act == M3_BF16 ? 1 : 0, &sms, &of, &ob)) != cudaSuccess)
       return M3_ERR_CUDA;
-    // Forward: a segment boundary costs a second pass over the earlier
-    // segments, so split time only until about FWD_WARPS_PER_SM warps are
-    // resident.  Backward: the aggregate pass is cheap next to the main
-    // kernel, so split until about BWD_WAVES waves of resident blocks.
-    const int64_t fwd_warps = (int64_t)p->B * groups_f * (GF / 32);
-    const int64_t want_fw = (int64_t)FWD_WARPS_PER_SM * sms;
-    want_f = (int)((want_fw + fwd_warps - 1) / fwd_warps);
-    const int64_t bblocks = (int64_t)p->B * groups_b;
-    const int64_t cap_b = (int64_t)sms * ob * BWD_WAVES;
-    want_b = (int)((cap_b + bblocks - 1) / bblocks);
-    (void)of;
+    want_f = choose_segments(p->nc, p->K, (int64_t)p->B * groups_f, (int64_t)sms * of, 2);
+    want_b = choose_segments(p->nc, p->K, (int64_t)p->B * groups_b, (int64_t)sms * ob, 8);
   }
   if (p->nc == 0) {
     p->Sf = p->Sb = 1;
@@ -1233,11 +1259,10 @@ m3_status make_plan(const m3_dims* dm, m3_dtype act, Plan* p) {
   // backward section (reuses the same bytes)
   off = 0;
   p->b_part = take(B * p->Sb * NPART * D * 4);
-  p->b_q = p->b_sd = p->b_gin = p->b_dxpart = p->b_dchead = 0;
+  p->b_q = p->b_sd = p->b_dxpart = p->b_dchead = 0;
   if (p->Sb > 1) {
     p->b_q = take(B * p->Sb * NS * D * 4);
     p->b_sd = take(B * p->Sb * D * 4);
-    p->b_gin = take(B * p->Sb * NS * D * 4);
     p->b_dxpart = take(B * p->Sb * 3 * D * 4);
     p->b_dchead = take(B * p->Sb * 3 * D * 4);
   }
@@ -1245,8 +1270,8 @@ m3_status make_plan(const m3_dims* dm, m3_dtype act, Plan* p) {
   p->ws_bytes = fwd_total > bwd_total ? fwd_total : bwd_total;
   if (p->ws_bytes < 256) p->ws_bytes = 256;
   const bool empty = (size_t)p->B * p->T * p->D == 0;
-  p->fwd_launches = empty ? 0 : (p->Sf > 1 ? 3 : 1);
-  p->bwd_launches = empty ? 0 : (p->Sb > 1 ? 5 : 2);
+  p->fwd_launches = empty ? 0 : (p->Sf > 1 ? 2 : 1);
+  p->bwd_launches = empty ? 0 : (p->Sb > 1 ? 3 : 2);
   return M3_OK;
 }
 
@@ -1257,11 +1282,7 @@ m3_status launch_fwd(const Plan& p, FwdArgs a, cudaStream_t st) {
   const int groups = (p.D + GF - 1) / GF;
   const size_t smem = fwd_smem(sizeof(T)).total;
   a.g = Geo{p.B, p.T, p.D, p.K, p.nc, p.Sf, p.mf};
-  if (p.Sf > 1) {
-    m3_fwd_kernel<T, false><<<dim3(groups, p.Sf - 1, p.B), GF, smem, st>>>(a);
-    const size_t n = (size_t)p.B * NS * p.D;
-    m3_fwd_carry_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(a);
-  }
+  if (p.Sf > 1) m3_fwd_kernel<T, false><<<dim3(groups, p.Sf - 1, p.B), GF, smem, st>>>(a);
   m3_fwd_kernel<T, true><<<dim3(groups, p.Sf, p.B), GF, smem, st>>>(a);
   return note(cudaGetLastError()) == cudaSuccess ? M3_OK : M3_ERR_CUDA;
 }
@@ -1270,21 +1291,18 @@ template <typename T>
 m3_status launch_bwd(const Plan& p, BwdArgs a, cudaStream_t st, int smem_per_sm) {
   const int groups = (p.D + GB - 1) / GB;
   a.g = Geo{p.B, p.T, p.D, p.K, p.nc, p.Sb, p.mb};
-  if (note(cudaMemsetAsync(a.dB, 0, (size_t)p.B * p.T * NS * 4, st)) != cudaSuccess) return M3_ERR_CUDA;
-  if (note(cudaMemsetAsync(a.dC, 0, (size_t)p.B * p.T * NS * 4, st)) != cudaSuccess) return M3_ERR_CUDA;
   if (p.Sb > 1) {
+    // also clears dB and dC before the main kernel's reductions into them
     m3_bwd_agg_kernel<T><<<dim3(groups, p.Sb - 1, p.B), GB, agg_smem(sizeof(T)).total, st>>>(a);
-    const size_t n = (size_t)p.B * NS * p.D;
-    m3_bwd_carry_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(a);
+  } else {
+    if (note(cudaMemsetAsync(a.dB, 0, (size_t)p.B * p.T * NS * 4, st)) != cudaSuccess) return M3_ERR_CUDA;
+    if (note(cudaMemsetAsync(a.dC, 0, (size_t)p.B * p.T * NS * 4, st)) != cudaSuccess) return M3_ERR_CUDA;
   }
   a.tcols = tmem_cols_for(p.K);
   m3_bwd_kernel<T><<<dim3(groups, p.Sb, p.B), GB, bwd_launch_smem(p.K, sizeof(T), smem_per_sm), st>>>(a);
-  if (p.Sb > 1) {
-    const size_t n = (size_t)p.B * (p.Sb - 1) * 3 * p.D;
-    m3_bwd_fixup_kernel<T><<<(unsigned)((n + 255) / 256), 256, 0, st>>>(a);
-  }
-  const int nf = 23 * p.D;
-  m3_bwd_finalize_kernel<<<(nf + 255) / 256, 256, 0, st>>>(a, p.B * p.Sb);
+  const size_t nfin = ((size_t)23 * p.D * 32 + 255) / 256;             // one warp per output
+  const size_t nfix = p.Sb > 1 ? ((size_t)p.B * (p.Sb - 1) * 3 * p.D + 255) / 256 : 0;
+  m3_bwd_tail_kernel<T><<<(unsigned)(nfin + nfix), 256, 0, st>>>(a, p.B * p.Sb, (int)nfin);
   return note(cudaGetLastError()) == cudaSuccess ? M3_OK : M3_ERR_CUDA;
 }
 
@@ -1426,7 +1444,6 @@ m3_status m3scan_bwd(const m3_dims* dims, m3_dtype act, const void* x, const voi
   if (p.Sb > 1) {
     a.q = reinterpret_cast<float*>(ws + p.b_q);
     a.sd = reinterpret_cast<float*>(ws + p.b_sd);
-    a.gin = reinterpret_cast<float*>(ws + p.b_gin);
     a.dxpart = reinterpret_cast<float*>(ws + p.b_dxpart);
     a.dchead = reinterpret_cast<float*>(ws + p.b_dchead);
   }

@@ -59,8 +59,8 @@ def test_plan_with_explicit_segments_needs_no_device(lib):
     assert p.chunk == 16 and p.n_chunks == 128
     assert p.fwd_segments == 4 and p.bwd_segments == 4
     assert p.ckpt_bytes == 8 * 128 * 16 * 1536 * 4
-    assert p.fwd_launches == 3 and p.bwd_launches == 5
-    # one segment: the main kernel plus the parameter-gradient finalize
+    assert p.fwd_launches == 2 and p.bwd_launches == 3
+    # one segment: the main kernel plus the parameter-gradient tail kernel
     st, p1 = _plan(binding.make_dims(8, 2048, 1536, chunk=16, segments=1))
     assert st == 0 and p1.fwd_launches == 1 and p1.bwd_launches == 2
     assert p1.workspace_bytes >= 8 * 24 * 1536 * 4
