@@ -827,6 +827,7 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(BwdArgs a) {
         float2 hn[NS / 2];  // h_t (state after step t)
         tmem_ld16(trow + 16u * (uint32_t)(nst - 1), hn);
         tmem_wait_ld();
+#pragma unroll 2
         for (int j = nst - 1; j >= 0; --j) {
           const float4 v0 = s0[j * GB];
           const float Du = reinterpret_cast<const float*>(s1 + j * GB)[0];
@@ -876,13 +877,15 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(BwdArgs a) {
           // the scalar pass below reads these two sums
           reinterpret_cast<float*>(s0 + j * GB)[3] = sAq.x + sAq.y;
           reinterpret_cast<float*>(s1 + j * GB)[0] = sB.x + sB.y;
+          // Channels past d_inner run on zero-filled inputs and parameters, so
+          // their partials are exactly zero and need no masking.
           float vb[NS], vc[NS];
 #pragma unroll
           for (int i = 0; i < NS / 2; ++i) {
-            vb[2 * i] = active ? pB[i].x : 0.f;
-            vb[2 * i + 1] = active ? pB[i].y : 0.f;
-            vc[2 * i] = active ? pC[i].x : 0.f;
-            vc[2 * i + 1] = active ? pC[i].y : 0.f;
+            vb[2 * i] = pB[i].x;
+            vb[2 * i + 1] = pB[i].y;
+            vc[2 * i] = pC[i].x;
+            vc[2 * i + 1] = pC[i].y;
           }
           const float rb = warp_sum16_rotated(vb, lane);
           const float rc = warp_sum16_rotated(vc, lane);
