@@ -319,6 +319,19 @@ __global__ void __launch_bounds__(GF) m3_fwd_kernel(FwdArgs a) {
   float* fB = reinterpret_cast<float*>(smem + L.fB);
   float* fC = reinterpret_cast<float*>(smem + L.fC);
 
+  auto stage = [&](int t0, int buf) {
+    unsigned char* base = smem + (size_t)buf * L.tile;
+    stage_rows<T, GF, GF>(reinterpret_cast<T*>(base + L.x), xg, b, t0, TT, g.T, t_end, g.D, d0, tid);
+    stage_rows<T, GF, GF>(reinterpret_cast<T*>(base + L.dr), drg, b, t0, TT, g.T, t_end, g.D, d0, tid);
+    stage_bc<T, GF>(reinterpret_cast<T*>(base + L.Bt), Bg, b, t0, TT, g.T, t_end, tid);
+    if (FINAL) {
+      stage_rows<T, GF, GF>(reinterpret_cast<T*>(base + L.z), zg, b, t0, TT, g.T, t_end, g.D, d0, tid);
+      stage_bc<T, GF>(reinterpret_cast<T*>(base + L.Ct), Cg, b, t0, TT, g.T, t_end, tid);
+    }
+    cp_async_commit();
+  };
+  stage(t_begin, 0);  // first tile in flight while the parameters and carries load
+
   float2 a2[NS / 2];  // A log2(e) for lanes (2i, 2i+1)
 #pragma unroll
   for (int i = 0; i < NS / 2; ++i) {
@@ -341,7 +354,7 @@ __global__ void __launch_bounds__(GF) m3_fwd_kernel(FwdArgs a) {
     // local_end(s'), to get this segment's true start state.
     const float* __restrict__ agg_s = a.agg_s;
     const float* __restrict__ agg_h = a.agg_h;
-#pragma unroll 2
+#pragma unroll 4
     for (int sp = 0; sp < s; ++sp) {
       const size_t bs = (size_t)b * g.S + sp;
       const float2 dl2 = f2b(active ? agg_s[bs * g.D + d] : 0.f);
@@ -362,21 +375,9 @@ __global__ void __launch_bounds__(GF) m3_fwd_kernel(FwdArgs a) {
   }
   float sdelta = 0.f;
 
-  auto stage = [&](int t0, int buf) {
-    unsigned char* base = smem + (size_t)buf * L.tile;
-    stage_rows<T, GF, GF>(reinterpret_cast<T*>(base + L.x), xg, b, t0, TT, g.T, t_end, g.D, d0, tid);
-    stage_rows<T, GF, GF>(reinterpret_cast<T*>(base + L.dr), drg, b, t0, TT, g.T, t_end, g.D, d0, tid);
-    stage_bc<T, GF>(reinterpret_cast<T*>(base + L.Bt), Bg, b, t0, TT, g.T, t_end, tid);
-    if (FINAL) {
-      stage_rows<T, GF, GF>(reinterpret_cast<T*>(base + L.z), zg, b, t0, TT, g.T, t_end, g.D, d0, tid);
-      stage_bc<T, GF>(reinterpret_cast<T*>(base + L.Ct), Cg, b, t0, TT, g.T, t_end, tid);
-    }
-    cp_async_commit();
-  };
 
   float4* scs = reinterpret_cast<float4*>(smem + L.sc) + tid;  // this thread's slots, stride GF
   int kc = 0;  // steps left until the next checkpoint
-  stage(t_begin, 0);
   for (int t0 = t_begin, it = 0; t0 < t_end; t0 += TT, ++it) {
     const int buf = it & 1;
     if (t0 + TT < t_end) {
@@ -507,6 +508,20 @@ __global__ void __launch_bounds__(GB) m3_bwd_agg_kernel(BwdArgs a) {
   const int t_end = min((s + 1) * g.m * g.K, g.T);
   const AggSmem L = agg_smem(sizeof(T));
   float* fC = reinterpret_cast<float*>(smem + L.fC);
+  const int ntiles = (t_end - t_begin + TT - 1) / TT;
+  auto tile_start = [&](int i) { return max(t_begin, t_end - (i + 1) * TT); };
+  auto stage = [&](int i, int buf) {
+    unsigned char* base = smem + (size_t)buf * L.tile;
+    const int t0 = tile_start(i);
+    const int rows = (t_end - i * TT) - t0;
+    stage_rows<T, GB, GB>(reinterpret_cast<T*>(base + L.dr), static_cast<const T*>(a.dr), b, t0, rows, g.T, g.T, g.D, d0, tid);
+    stage_rows<T, GB, GB>(reinterpret_cast<T*>(base + L.z), static_cast<const T*>(a.z), b, t0, rows, g.T, g.T, g.D, d0, tid);
+    stage_rows<T, GB, GB>(reinterpret_cast<T*>(base + L.dg), static_cast<const T*>(a.dg), b, t0, rows, g.T, g.T, g.D, d0, tid);
+    stage_bc<T, GB>(reinterpret_cast<T*>(base + L.Ct), static_cast<const T*>(a.Cm), b, t0, rows, g.T, g.T, tid);
+    cp_async_commit();
+  };
+
+  stage(0, 0);  // first tile in flight while the parameters load
 
   float2 a2[NS / 2];
 #pragma unroll
@@ -531,20 +546,6 @@ __global__ void __launch_bounds__(GB) m3_bwd_agg_kernel(BwdArgs a) {
       a.dC[i] = 0.f;
     }
   }
-  const int ntiles = (t_end - t_begin + TT - 1) / TT;
-  auto tile_start = [&](int i) { return max(t_begin, t_end - (i + 1) * TT); };
-  auto stage = [&](int i, int buf) {
-    unsigned char* base = smem + (size_t)buf * L.tile;
-    const int t0 = tile_start(i);
-    const int rows = (t_end - i * TT) - t0;
-    stage_rows<T, GB, GB>(reinterpret_cast<T*>(base + L.dr), static_cast<const T*>(a.dr), b, t0, rows, g.T, g.T, g.D, d0, tid);
-    stage_rows<T, GB, GB>(reinterpret_cast<T*>(base + L.z), static_cast<const T*>(a.z), b, t0, rows, g.T, g.T, g.D, d0, tid);
-    stage_rows<T, GB, GB>(reinterpret_cast<T*>(base + L.dg), static_cast<const T*>(a.dg), b, t0, rows, g.T, g.T, g.D, d0, tid);
-    stage_bc<T, GB>(reinterpret_cast<T*>(base + L.Ct), static_cast<const T*>(a.Cm), b, t0, rows, g.T, g.T, tid);
-    cp_async_commit();
-  };
-
-  stage(0, 0);
   for (int i = 0; i < ntiles; ++i) {
     const int buf = i & 1;
     if (i + 1 < ntiles) {
@@ -961,8 +962,9 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(BwdArgs a) {
 
 // The backward's last kernel, two roles by block index.
 //  - blocks [0, nfin): parameter gradients, the per-(batch, segment) partials
-//    summed in a fixed order (one warp per output: lane l sums rows l, l+32,
-//    ..., then a fixed shuffle tree), so the result is deterministic;
+//    summed in a fixed order (one thread per output, consecutive threads on
+//    consecutive channels so the row reads coalesce), so the result is
+//    deterministic;
 //  - blocks [nfin, ...): d_x at the last three steps of each segment but the
 //    last, which needs the conv gradient of the next segment's first steps.
 template <typename T>
@@ -990,23 +992,25 @@ __global__ void m3_bwd_tail_kernel(BwdArgs a, int rows, int nfin) {
     Act<T>::st(static_cast<T*>(a.dx) + ((size_t)b * g.T + t) * g.D + d, v);
     return;
   }
-  const int widx = (int)(((size_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5);
-  const int lane = threadIdx.x & 31;
-  if (widx >= 23 * g.D) return;  // whole warps exit together
-  const int jj = widx / g.D, d = widx - jj * g.D;
+  const int oidx = (int)((size_t)blockIdx.x * blockDim.x + threadIdx.x);
+  if (oidx >= 23 * g.D) return;
+  const int jj = oidx / g.D, d = oidx - jj * g.D;
   const float* __restrict__ P = a.partials + (size_t)jj * g.D + d;
   const size_t stride = (size_t)NPART * g.D;
-  float v0 = 0.f, v1 = 0.f;
-  int r = lane;
-  for (; r + 32 < rows; r += 64) {
+  // four accumulators over rows r = 0 mod 4, 1 mod 4, ...; combined in a
+  // fixed order
+  float v0 = 0.f, v1 = 0.f, v2 = 0.f, v3 = 0.f;
+  int r = 0;
+  for (; r + 3 < rows; r += 4) {
     v0 += P[(size_t)r * stride];
-    v1 += P[(size_t)(r + 32) * stride];
+    v1 += P[(size_t)(r + 1) * stride];
+    v2 += P[(size_t)(r + 2) * stride];
+    v3 += P[(size_t)(r + 3) * stride];
   }
   if (r < rows) v0 += P[(size_t)r * stride];
-  float v = v0 + v1;
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  if (lane != 0) return;
+  if (r + 1 < rows) v1 += P[(size_t)(r + 1) * stride];
+  if (r + 2 < rows) v2 += P[(size_t)(r + 2) * stride];
+  float v = (v0 + v1) + (v2 + v3);
   float* dst;
   if (jj < NS) {
     v *= -expf(a.a_log[(size_t)d * NS + jj]);  // dL/da_log = dL/dA * A
@@ -1303,7 +1307,7 @@ m3_status launch_bwd(const Plan& p, BwdArgs a, cudaStream_t st, int smem_per_sm)
   }
   a.tcols = tmem_cols_for(p.K);
   m3_bwd_kernel<T><<<dim3(groups, p.Sb, p.B), GB, bwd_launch_smem(p.K, sizeof(T), smem_per_sm), st>>>(a);
-  const size_t nfin = ((size_t)23 * p.D * 32 + 255) / 256;             // one warp per output
+  const size_t nfin = ((size_t)23 * p.D + 255) / 256;                  // one thread per output
   const size_t nfix = p.Sb > 1 ? ((size_t)p.B * (p.Sb - 1) * 3 * p.D + 255) / 256 : 0;
   m3_bwd_tail_kernel<T><<<(unsigned)(nfin + nfix), 256, 0, st>>>(a, p.B * p.Sb, (int)nfin);
   return note(cudaGetLastError()) == cudaSuccess ? M3_OK : M3_ERR_CUDA;
