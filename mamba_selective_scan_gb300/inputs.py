@@ -158,6 +158,31 @@ def make_inputs(batch, seq_len, d_inner, act="bf16", seed=0, d_state=D_STATE,
     return Inputs(batch, seq_len, d_inner, d_state, d_conv, act, arrays)
 
 
+STATE_NAMES = ("ssm_state", "conv_state", "d_ssm_state_out", "d_conv_state_out")
+
+
+def make_state_inputs(batch, d_inner, act="bf16", seed=0, d_state=D_STATE,
+                      d_conv=D_CONV) -> dict:
+    """Seeded carried state for a window that continues an earlier one.
+
+    ``ssm_state`` [batch, d_state, d_inner] (float32) and ``conv_state``
+    [batch, d_conv - 1, d_inner] (activation dtype: it holds earlier conv
+    inputs), plus the upstream gradients of the window's state outputs,
+    ``d_ssm_state_out`` (float32) and ``d_conv_state_out`` (activation
+    dtype), all ~ N(0, 1) and drawn in that order from a stream of its own
+    (``default_rng([seed, 1])``), so the activation draws of ``make_inputs``
+    with the same seed are unchanged.
+    """
+    rng = np.random.default_rng([seed, 1])
+    h = rng.standard_normal((batch, d_state, d_inner), dtype=np.float32)
+    c = rng.standard_normal((batch, d_conv - 1, d_inner), dtype=np.float32)
+    gh = rng.standard_normal((batch, d_state, d_inner), dtype=np.float32)
+    gc = rng.standard_normal((batch, d_conv - 1, d_inner), dtype=np.float32)
+    if act == "bf16":
+        c, gc = round_to_bf16(c), round_to_bf16(gc)
+    return dict(ssm_state=h, conv_state=c, d_ssm_state_out=gh, d_conv_state_out=gc)
+
+
 def make_workload_inputs(name: str) -> Inputs:
     w = WORKLOADS[name]
     return make_inputs(w.batch, w.seq_len, w.d_inner, w.act, w.seed,

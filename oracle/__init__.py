@@ -52,10 +52,11 @@ def _load():
         if _lib is None:
             lib = ctypes.CDLL(build())
             lib.m3o_forward.restype = ctypes.c_int
-            lib.m3o_forward.argtypes = [_i64] * 5 + [_dp] * 10 + [_u8p] + [_dp] * 5 + [_i64]
+            lib.m3o_forward.argtypes = ([_i64] * 5 + [_dp] * 10 + [_u8p] + [_dp] * 5
+                                        + [_i64] + [_dp] * 4)
             lib.m3o_backward.restype = ctypes.c_int
             lib.m3o_backward.argtypes = ([_i64] * 5 + [_dp] * 11 + [_u8p, _i64]
-                                         + [_dp] * 11)
+                                         + [_dp] * 11 + [_dp] * 6)
             _lib = lib
     return _lib
 
@@ -68,6 +69,10 @@ def _ptr(a):
     if a is None:
         return None
     return a.ctypes.data_as(_dp)
+
+
+def _opt64(a):
+    return None if a is None else _c64(a)
 
 
 def _mask_ptr(mask):
@@ -92,15 +97,23 @@ def _common(inp):
     return (Bsz, T, D, N, W), arrs
 
 
-def forward(inp, chan_mask=None, ckpt_chunk: int = 0):
+def forward(inp, chan_mask=None, ckpt_chunk: int = 0, ssm_state=None, conv_state=None):
     """Oracle forward.
 
-    Returns a dict with ``gated``, ``y``, ``u``, ``delta`` ([B,T,D]) and, if
-    ``ckpt_chunk`` > 0, ``ckpt`` ([B, ceil(T/K), N, D], the state before each
-    chunk).  Channels outside ``chan_mask`` are left as zeros.
+    Returns a dict with ``gated``, ``y``, ``u``, ``delta`` ([B,T,D]),
+    ``ssm_state_out`` ([B,N,D], the state after the last step) and
+    ``conv_state_out`` ([B,W-1,D], the conv inputs of the last W-1 steps,
+    oldest first) and, if ``ckpt_chunk`` > 0, ``ckpt`` ([B, ceil(T/K), N, D],
+    the state before each chunk).  ``ssm_state`` ([B,N,D]) and
+    ``conv_state`` ([B,W-1,D]) are the carried state the sequence starts
+    from (None = zero).  Channels outside ``chan_mask`` are left as zeros.
     """
     lib = _load()
     (Bsz, T, D, N, W), a = _common(inp)
+    h0 = _opt64(ssm_state)
+    c0 = _opt64(conv_state)
+    h_out = np.zeros((Bsz, N, D))
+    c_out = np.zeros((Bsz, W - 1, D))
     gated = np.zeros((Bsz, T, D))
     y = np.zeros((Bsz, T, D))
     u = np.zeros((Bsz, T, D))
@@ -114,10 +127,12 @@ def forward(inp, chan_mask=None, ckpt_chunk: int = 0):
                          _ptr(a["z"]), _ptr(a["B"]), _ptr(a["C"]),
                          _ptr(a["conv_w"]), _ptr(a["conv_b"]), _ptr(a["dt_bias"]),
                          _ptr(a["a_log"]), _ptr(a["D"]), mp, _ptr(gated), _ptr(y),
-                         _ptr(u), _ptr(delta), _ptr(ckpt), int(ckpt_chunk))
+                         _ptr(u), _ptr(delta), _ptr(ckpt), int(ckpt_chunk),
+                         _ptr(h0), _ptr(c0), _ptr(h_out), _ptr(c_out))
     if rc != 0:
         raise MemoryError("oracle forward: allocation failed")
-    out = dict(gated=gated, y=y, u=u, delta=delta)
+    out = dict(gated=gated, y=y, u=u, delta=delta, ssm_state_out=h_out,
+               conv_state_out=c_out)
     if ckpt is not None:
         out["ckpt"] = ckpt
     return out
@@ -127,16 +142,25 @@ GRAD_NAMES = ("d_x", "d_delta_raw", "dz", "du", "dB", "dC", "d_conv_w",
               "d_conv_b", "d_dt_bias", "d_a_log", "dD")
 
 
-def backward(inp, d_gated=None, chan_mask=None, chunk: int = 0):
-    """Oracle backward of L = sum(gated * d_gated).
+STATE_GRAD_NAMES = ("d_ssm_state", "d_conv_state")
+
+
+def backward(inp, d_gated=None, chan_mask=None, chunk: int = 0, ssm_state=None,
+             conv_state=None, d_ssm_state_out=None, d_conv_state_out=None):
+    """Oracle backward of
+    L = sum(gated * d_gated) + sum(ssm_state_out * d_ssm_state_out)
+        + sum(conv_state_out * d_conv_state_out).
 
     ``chunk`` = 0 keeps every state (sequential); ``chunk`` > 0 recomputes
-    states chunk by chunk from chunk-start states.  Returns a dict of float64
-    gradients named as in ``GRAD_NAMES``.
+    states chunk by chunk from chunk-start states.  The carried-state
+    arguments are as in ``forward`` (None = zero).  Returns a dict of float64
+    gradients named as in ``GRAD_NAMES`` and ``STATE_GRAD_NAMES``.
     """
     lib = _load()
     (Bsz, T, D, N, W), a = _common(inp)
     g = _c64(inp["d_gated"] if d_gated is None else d_gated)
+    h0, c0 = _opt64(ssm_state), _opt64(conv_state)
+    gh, gc = _opt64(d_ssm_state_out), _opt64(d_conv_state_out)
     out = {k: np.zeros((Bsz, T, D)) for k in ("d_x", "d_delta_raw", "dz", "du")}
     out["dB"] = np.zeros((Bsz, T, N))
     out["dC"] = np.zeros((Bsz, T, N))
@@ -145,21 +169,32 @@ def backward(inp, d_gated=None, chan_mask=None, chunk: int = 0):
     out["d_dt_bias"] = np.zeros(D)
     out["d_a_log"] = np.zeros((D, N))
     out["dD"] = np.zeros(D)
+    out["d_ssm_state"] = np.zeros((Bsz, N, D))
+    out["d_conv_state"] = np.zeros((Bsz, W - 1, D))
     _m, mp = _mask_ptr(chan_mask)
     rc = lib.m3o_backward(Bsz, T, D, N, W, _ptr(a["x"]), _ptr(a["delta_raw"]),
                           _ptr(a["z"]), _ptr(a["B"]), _ptr(a["C"]),
                           _ptr(a["conv_w"]), _ptr(a["conv_b"]), _ptr(a["dt_bias"]),
                           _ptr(a["a_log"]), _ptr(a["D"]), _ptr(g), mp, int(chunk),
-                          *[_ptr(out[k]) for k in GRAD_NAMES])
+                          *[_ptr(out[k]) for k in GRAD_NAMES],
+                          _ptr(h0), _ptr(c0), _ptr(gh), _ptr(gc),
+                          _ptr(out["d_ssm_state"]), _ptr(out["d_conv_state"]))
     if rc != 0:
         raise MemoryError("oracle backward: allocation failed")
     return out
 
 
-def loss(inp, d_gated=None) -> float:
-    """L = sum(gated * d_gated), the scalar whose gradient ``backward`` gives."""
+def loss(inp, d_gated=None, ssm_state=None, conv_state=None, d_ssm_state_out=None,
+         d_conv_state_out=None) -> float:
+    """The scalar whose gradient ``backward`` gives (see ``backward``)."""
     g = _c64(inp["d_gated"] if d_gated is None else d_gated)
-    return float(np.sum(forward(inp)["gated"] * g))
+    f = forward(inp, ssm_state=ssm_state, conv_state=conv_state)
+    L = float(np.sum(f["gated"] * g))
+    if d_ssm_state_out is not None:
+        L += float(np.sum(f["ssm_state_out"] * _c64(d_ssm_state_out)))
+    if d_conv_state_out is not None:
+        L += float(np.sum(f["conv_state_out"] * _c64(d_conv_state_out)))
+    return L
 
 
 if __name__ == "__main__":  # pragma: no cover

@@ -26,8 +26,11 @@
  * written out step by step (no autograd, no fusion).
  *
  * Readings where the pages are silent (each is listed in the design notes):
- *  - conv taps: c[t] = conv_b + sum_k w[k] * x[t-(W-1)+k], x = 0 before t=0
- *    (w[W-1] multiplies the current token; zero initial conv state).
+ *  - conv taps: c[t] = conv_b + sum_k w[k] * x[t-(W-1)+k] (w[W-1] multiplies
+ *    the current token); x before t=0 is the carried conv state, zero when
+ *    none is given.
+ *  - the recurrent state before step 0 is the carried SSM state, zero when
+ *    none is given (the trainer's reset_state).
  *  - the input term of the recurrence is delta*B*u (Euler for B, zero-order
  *    hold for A); y_t reads the state after the t-th update.
  *  - softplus(v) = log(1 + e^v) exactly, no threshold.
@@ -39,6 +42,15 @@
  * and d_conv_w are [D, W]; a_log and d_a_log are [D, N]; conv_b, dt_bias,
  * Dp and their grads are [D].  ckpt is [B, nc, N, D] with nc = ceil(T/K):
  * ckpt[b, c, :, d] is the state before step c*K.
+ *
+ * Carried state (all nullable; NULL inputs mean zero, NULL outputs are not
+ * written).  ssm_state [B, N, D] is the state before step 0 (h_{-1});
+ * conv_state [B, W-1, D] holds the conv inputs of the W-1 steps before step
+ * 0, oldest first (row r is step r-(W-1)).  ssm_state_out and conv_state_out
+ * have the same layouts and hold h_{T-1} and the inputs of steps T-W+1..T-1,
+ * so that a sequence cut in two windows and run window by window, each
+ * window starting from the previous one's outputs, gives the same results as
+ * one run over the whole sequence.
  *
  * chan_mask (nullable, [D] bytes): when given, only channels with a nonzero
  * mask byte are computed; the others keep whatever the caller put in the
@@ -70,9 +82,19 @@ static int channel_on(const uint8_t* mask, int64_t d) {
     return mask == NULL || mask[d] != 0;
 }
 
+/* The conv input of channel d at step s >= -(W-1): x for s >= 0, else the
+   carried conv state (row s + W - 1), zero when there is none. */
+static double x_at(const double* x, const double* conv_state, int64_t b,
+                   int64_t s, int64_t d, int64_t T, int64_t D, int64_t W) {
+    if (s >= 0) return x[IDX3(b, s, d, T, D)];
+    if (conv_state == NULL) return 0.0;
+    return conv_state[IDX3(b, s + (W - 1), d, W - 1, D)];
+}
+
 /* Per-channel forward quantities along time (conv output c, u, delta). */
 static void channel_inputs(int64_t b, int64_t d, int64_t T, int64_t D, int64_t W,
-                           const double* x, const double* delta_raw,
+                           const double* x, const double* conv_state,
+                           const double* delta_raw,
                            const double* conv_w, const double* conv_b,
                            const double* dt_bias, double* c, double* u,
                            double* delta) {
@@ -80,7 +102,7 @@ static void channel_inputs(int64_t b, int64_t d, int64_t T, int64_t D, int64_t W
         double acc = conv_b[d];
         for (int64_t k = 0; k < W; ++k) {
             int64_t s = t - (W - 1) + k;
-            if (s >= 0) acc += conv_w[d * W + k] * x[IDX3(b, s, d, T, D)];
+            acc += conv_w[d * W + k] * x_at(x, conv_state, b, s, d, T, D, W);
         }
         c[t] = acc;
         u[t] = silu(acc);
@@ -107,7 +129,9 @@ static double scan_output(int64_t N, const double* Ct, const double* h,
 /*
  * Forward.  gated, y, u_out, delta_out: [B,T,D] (y, u_out, delta_out and
  * ckpt nullable).  K is the checkpoint interval used for ckpt (ignored when
- * ckpt is NULL).  Returns 0, or -1 on an allocation failure.
+ * ckpt is NULL).  ssm_state, conv_state, ssm_state_out, conv_state_out: the
+ * carried state described above (nullable).  Returns 0, or -1 on an
+ * allocation failure.
  */
 int m3o_forward(int64_t B, int64_t T, int64_t D, int64_t N, int64_t W,
                 const double* x, const double* delta_raw, const double* z,
@@ -115,7 +139,9 @@ int m3o_forward(int64_t B, int64_t T, int64_t D, int64_t N, int64_t W,
                 const double* conv_b, const double* dt_bias,
                 const double* a_log, const double* Dp,
                 const uint8_t* chan_mask, double* gated, double* y_out,
-                double* u_out, double* delta_out, double* ckpt, int64_t K) {
+                double* u_out, double* delta_out, double* ckpt, int64_t K,
+                const double* ssm_state, const double* conv_state,
+                double* ssm_state_out, double* conv_state_out) {
     double* c = malloc(sizeof(double) * (size_t)(T > 0 ? T : 1));
     double* u = malloc(sizeof(double) * (size_t)(T > 0 ? T : 1));
     double* delta = malloc(sizeof(double) * (size_t)(T > 0 ? T : 1));
@@ -131,9 +157,10 @@ int m3o_forward(int64_t B, int64_t T, int64_t D, int64_t N, int64_t W,
         for (int64_t d = 0; d < D; ++d) {
             if (!channel_on(chan_mask, d)) continue;
             for (int64_t n = 0; n < N; ++n) A[n] = -exp(a_log[d * N + n]);
-            channel_inputs(b, d, T, D, W, x, delta_raw, conv_w, conv_b, dt_bias,
-                           c, u, delta);
-            for (int64_t n = 0; n < N; ++n) h[n] = 0.0;
+            channel_inputs(b, d, T, D, W, x, conv_state, delta_raw, conv_w,
+                           conv_b, dt_bias, c, u, delta);
+            for (int64_t n = 0; n < N; ++n)
+                h[n] = ssm_state ? ssm_state[(b * N + n) * D + d] : 0.0;
             for (int64_t t = 0; t < T; ++t) {
                 if (nc > 0 && t % K == 0) {
                     int64_t ci = t / K;
@@ -151,6 +178,13 @@ int m3o_forward(int64_t B, int64_t T, int64_t D, int64_t N, int64_t W,
                 if (u_out) u_out[i] = u[t];
                 if (delta_out) delta_out[i] = delta[t];
             }
+            if (ssm_state_out)
+                for (int64_t n = 0; n < N; ++n)
+                    ssm_state_out[(b * N + n) * D + d] = h[n];
+            if (conv_state_out)
+                for (int64_t r = 0; r < W - 1; ++r)
+                    conv_state_out[IDX3(b, r, d, W - 1, D)] =
+                        x_at(x, conv_state, b, T - (W - 1) + r, d, T, D, W);
         }
     }
     free(c); free(u); free(delta); free(A); free(h); free(hn);
@@ -170,6 +204,12 @@ int m3o_forward(int64_t B, int64_t T, int64_t D, int64_t N, int64_t W,
  * dB, dC: [B,T,N], accumulated into (the caller zeroes them).
  * Parameter grads d_conv_w [D,W], d_conv_b [D], d_dt_bias [D], d_a_log
  * [D,N], dD [D]: overwritten for every computed channel.
+ *
+ * With carried state the loss gains the terms of the state outputs,
+ *     L += sum ssm_state_out * d_ssm_state_out
+ *        + sum conv_state_out * d_conv_state_out,
+ * (d_ssm_state_out, d_conv_state_out nullable = zero), and d_ssm_state,
+ * d_conv_state (nullable) receive dL/d ssm_state and dL/d conv_state.
  */
 int m3o_backward(int64_t B, int64_t T, int64_t D, int64_t N, int64_t W,
                  const double* x, const double* delta_raw, const double* z,
@@ -179,7 +219,10 @@ int m3o_backward(int64_t B, int64_t T, int64_t D, int64_t N, int64_t W,
                  const uint8_t* chan_mask, int64_t K, double* d_x,
                  double* d_delta_raw, double* dz, double* du_out, double* dB,
                  double* dC, double* d_conv_w, double* d_conv_b,
-                 double* d_dt_bias, double* d_a_log, double* dD) {
+                 double* d_dt_bias, double* d_a_log, double* dD,
+                 const double* ssm_state, const double* conv_state,
+                 const double* d_ssm_state_out, const double* d_conv_state_out,
+                 double* d_ssm_state, double* d_conv_state) {
     int64_t Tm = T > 0 ? T : 1;
     int64_t span = (K > 0) ? K : Tm;         /* states held at once */
     int64_t nc = (K > 0) ? (T + K - 1) / K : 1;
@@ -205,11 +248,12 @@ int m3o_backward(int64_t B, int64_t T, int64_t D, int64_t N, int64_t W,
         for (int64_t d = 0; d < D; ++d) {
             if (!channel_on(chan_mask, d)) continue;
             for (int64_t n = 0; n < N; ++n) A[n] = -exp(a_log[d * N + n]);
-            channel_inputs(b, d, T, D, W, x, delta_raw, conv_w, conv_b, dt_bias,
-                           c, u, delta);
+            channel_inputs(b, d, T, D, W, x, conv_state, delta_raw, conv_w,
+                           conv_b, dt_bias, c, u, delta);
 
             /* forward sweep: keep the state before each span */
-            for (int64_t n = 0; n < N; ++n) h[n] = 0.0;
+            for (int64_t n = 0; n < N; ++n)
+                h[n] = ssm_state ? ssm_state[(b * N + n) * D + d] : 0.0;
             for (int64_t t = 0; t < T; ++t) {
                 if (t % span == 0)
                     memcpy(starts + (t / span) * N, h, sizeof(double) * (size_t)N);
@@ -219,8 +263,11 @@ int m3o_backward(int64_t B, int64_t T, int64_t D, int64_t N, int64_t W,
 
             double dD_acc = 0.0, ddtb_acc = 0.0;
             for (int64_t n = 0; n < N; ++n) {
-                dh_next[n] = 0.0;  /* dL/dh_{t+1}, zero after the last step */
-                dA_next[n] = 0.0;  /* exp(delta_{t+1} A), unused at t = T-1 */
+                /* dA_next[n] * dh_next[n] is the gradient reaching h_t from
+                   later steps; after the last step that is the upstream
+                   gradient of the state output (zero when none) */
+                dh_next[n] = d_ssm_state_out ? d_ssm_state_out[(b * N + n) * D + d] : 0.0;
+                dA_next[n] = 1.0;
                 dAp[n] = 0.0;      /* dL/dA[n] */
             }
             for (int64_t s = (T + span - 1) / span - 1; s >= 0; --s) {
@@ -270,6 +317,11 @@ int m3o_backward(int64_t B, int64_t T, int64_t D, int64_t N, int64_t W,
                 }
             }
 
+            /* h_{-1} = ssm_state feeds h_0 = exp(delta_0 A) h_{-1} + ... */
+            if (d_ssm_state)
+                for (int64_t n = 0; n < N; ++n)
+                    d_ssm_state[(b * N + n) * D + d] = dA_next[n] * dh_next[n];
+
             /* conv1d backward: c[t] = conv_b + sum_k w[k] x[t-(W-1)+k] */
             double dcb = 0.0;
             for (int64_t t = 0; t < T; ++t) dcb += dc[t];
@@ -279,18 +331,27 @@ int m3o_backward(int64_t B, int64_t T, int64_t D, int64_t N, int64_t W,
                 double acc = 0.0;
                 for (int64_t t = 0; t < T; ++t) {
                     int64_t s2 = t - (W - 1) + k;
-                    if (s2 >= 0) acc += dc[t] * x[IDX3(b, s2, d, T, D)];
+                    acc += dc[t] * x_at(x, conv_state, b, s2, d, T, D, W);
                 }
                 if (b == 0) d_conv_w[d * W + k] = 0.0;
                 d_conv_w[d * W + k] += acc;
             }
-            for (int64_t s2 = 0; s2 < T; ++s2) {
+            /* the conv input at step s2 >= -(W-1) reaches the conv outputs
+               of steps s2..s2+W-1 and, for s2 >= T-(W-1), the conv state
+               output row s2-(T-(W-1)) */
+            for (int64_t s2 = -(W - 1); s2 < T; ++s2) {
                 double acc = 0.0;
                 for (int64_t k = 0; k < W; ++k) {
                     int64_t t = s2 + (W - 1) - k;
-                    if (t < T) acc += dc[t] * conv_w[d * W + k];
+                    if (t >= 0 && t < T) acc += dc[t] * conv_w[d * W + k];
                 }
-                d_x[IDX3(b, s2, d, T, D)] = acc;
+                int64_t r = s2 - (T - (W - 1));
+                if (d_conv_state_out && r >= 0)
+                    acc += d_conv_state_out[IDX3(b, r, d, W - 1, D)];
+                if (s2 >= 0)
+                    d_x[IDX3(b, s2, d, T, D)] = acc;
+                else if (d_conv_state)
+                    d_conv_state[IDX3(b, s2 + (W - 1), d, W - 1, D)] = acc;
             }
             /* A = -exp(a_log): dL/da_log = dL/dA * A */
             for (int64_t n = 0; n < N; ++n) {
