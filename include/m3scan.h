@@ -6,11 +6,13 @@
  * src/mamba_ssm/gpu/forward_mixed.rs, steps F4a conv1d, F4c softplus,
  * F4d selective scan, F4e gating):
  *
- *   c[t]     = conv_b + sum_{k<4} conv_w[k] * x[t-3+k]       (x = 0 for t < 0)
+ *   c[t]     = conv_b + sum_{k<4} conv_w[k] * x[t-3+k]
+ *              (x = 0 for t < 0, or a carried conv state, m3scan_fwd_state)
  *   u[t]     = c[t] * sigmoid(c[t])
  *   delta[t] = softplus(delta_raw[t] + dt_bias)
  *   A[n]     = -exp(a_log[n])                 (trainer.rs 0.7.3, recompute_a_neg_all)
- *   h_t[n]   = exp(delta[t] * A[n]) * h_{t-1}[n] + delta[t] * B_t[n] * u[t],  h_{-1} = 0
+ *   h_t[n]   = exp(delta[t] * A[n]) * h_{t-1}[n] + delta[t] * B_t[n] * u[t],
+ *              h_{-1} = 0 (or a carried state, m3scan_fwd_state)
  *   y[t]     = sum_n C_t[n] * h_t[n] + D * u[t]
  *   gated[t] = y[t] * z[t] * sigmoid(z[t])
  *
@@ -140,6 +142,87 @@ m3_status m3scan_bwd(const m3_dims* dims, m3_dtype act,
                      float* d_a_log, float* dD,
                      void* workspace, size_t workspace_bytes,
                      m3_stream_t stream);
+
+/*
+ * Carried state.  The mamba-rs pages carry two pieces of recurrent state
+ * from one call to the next: the conv1d of step F4a reads and updates a
+ * per-layer conv state (the last d_conv-1 conv inputs of each channel), and
+ * the selective scan of step F4d reads and writes the SSM state h through a
+ * state pointer (forward_mixed.rs 0.3.1, the per-layer loop of
+ * gpu_forward_mamba_backbone_mixed); the trainer (trainer.rs 0.7.3) keeps
+ * them between windows of a long sequence and zeroes them in reset_state.
+ * With these structs a window starts from a given state and returns its
+ * final one, so that running a sequence window by window, each window from
+ * the previous one's outputs, gives the results of one call over the whole
+ * sequence (and the backward chains the same way, in reverse order).
+ *
+ * Layouts (DEVICE pointers, channel fastest):
+ *   ssm_state, ssm_state_out, d_ssm_state, d_ssm_state_out
+ *        : [batch, d_state, d_inner] float32; ssm_state is h_{-1} (the state
+ *          before step 0), ssm_state_out is h_{seq_len-1};
+ *   conv_state, conv_state_out, d_conv_state, d_conv_state_out
+ *        : [batch, d_conv-1, d_inner] activation dtype, oldest step first;
+ *          conv_state row r is the conv input x of step r-(d_conv-1), and
+ *          conv_state_out row r that of step seq_len-(d_conv-1)+r (taken
+ *          from conv_state where that step is negative).
+ * Every pointer may be NULL: a NULL input state means zero (the
+ * reset_state case), a NULL upstream gradient means zero, a NULL output is
+ * not written.  float32 pointers must be 4-byte aligned, activation-dtype
+ * ones aligned to their element.  A window of seq_len 0 copies each state
+ * input to its output (and each upstream gradient to the state gradient).
+ */
+typedef struct {
+    const float* ssm_state;      /* in, nullable */
+    const void* conv_state;      /* in, nullable */
+    float* ssm_state_out;        /* out, nullable */
+    void* conv_state_out;        /* out, nullable */
+} m3_fwd_state;
+
+typedef struct {
+    const void* conv_state;        /* in: the conv_state the forward used */
+    const float* d_ssm_state_out;  /* in: dL/d ssm_state_out, nullable */
+    const void* d_conv_state_out;  /* in: dL/d conv_state_out, nullable */
+    float* d_ssm_state;            /* out: dL/d ssm_state, nullable */
+    void* d_conv_state;            /* out: dL/d conv_state, nullable */
+} m3_bwd_state;
+
+/*
+ * m3scan_fwd starting from a carried state and writing the final one.  The
+ * checkpoints it writes start at ssm_state (ckpt[:, 0] = ssm_state), so
+ * m3scan_bwd_state needs only the conv_state among the state inputs.
+ * state must not be NULL (M3_ERR_NULL).
+ */
+m3_status m3scan_fwd_state(const m3_dims* dims, m3_dtype act,
+                           const void* x, const void* delta_raw, const void* z,
+                           const void* Bm, const void* Cm,
+                           const float* conv_w, const float* conv_b,
+                           const float* dt_bias, const float* a_log, const float* D,
+                           void* gated, void* y_dbg, float* ckpt,
+                           const m3_fwd_state* state,
+                           void* workspace, size_t workspace_bytes,
+                           m3_stream_t stream);
+
+/*
+ * m3scan_bwd of the loss
+ *   L = sum gated * d_gated + sum ssm_state_out * d_ssm_state_out
+ *       + sum conv_state_out * d_conv_state_out,
+ * from a forward made by m3scan_fwd_state.  Besides m3scan_bwd's outputs
+ * it writes d_ssm_state and d_conv_state when they are non-NULL (the
+ * latter in the activation dtype).  state must not be NULL (M3_ERR_NULL).
+ */
+m3_status m3scan_bwd_state(const m3_dims* dims, m3_dtype act,
+                           const void* x, const void* delta_raw, const void* z,
+                           const void* Bm, const void* Cm,
+                           const float* conv_w, const float* conv_b,
+                           const float* dt_bias, const float* a_log, const float* D,
+                           const float* ckpt, const void* d_gated,
+                           void* d_x, void* d_delta_raw, void* dz, void* du_dbg,
+                           float* dB, float* dC,
+                           float* d_conv_w, float* d_conv_b, float* d_dt_bias,
+                           float* d_a_log, float* dD,
+                           const m3_bwd_state* state,
+                           void* workspace, size_t workspace_bytes,
+                           m3_stream_t stream);
 
 /*
  * Size in bytes of the scratch array the library keeps on every GPU that

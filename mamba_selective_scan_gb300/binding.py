@@ -28,8 +28,9 @@ STATUS = {
 }
 
 # every symbol include/m3scan.h declares
-EXPORTS = ("m3scan_plan", "m3scan_fwd", "m3scan_bwd", "m3scan_bwd_noalloc",
-           "m3scan_status_string", "m3scan_last_cuda_error", "m3scan_version")
+EXPORTS = ("m3scan_plan", "m3scan_fwd", "m3scan_bwd", "m3scan_fwd_state", "m3scan_bwd_state",
+           "m3scan_bwd_noalloc", "m3scan_status_string", "m3scan_last_cuda_error",
+           "m3scan_version")
 
 # size of the library's own scratch array used by m3scan_bwd_noalloc
 NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -63,6 +64,20 @@ class M3Plan(ctypes.Structure):
         return {k: getattr(self, k) for k, _ in self._fields_}
 
 
+class M3FwdState(ctypes.Structure):
+    """m3_fwd_state: carried state in and out of a forward window."""
+    _fields_ = [("ssm_state", ctypes.c_void_p), ("conv_state", ctypes.c_void_p),
+                ("ssm_state_out", ctypes.c_void_p), ("conv_state_out", ctypes.c_void_p)]
+
+
+class M3BwdState(ctypes.Structure):
+    """m3_bwd_state: the conv state the forward used, the upstream gradients of
+    the state outputs and the gradients of the state inputs."""
+    _fields_ = [("conv_state", ctypes.c_void_p), ("d_ssm_state_out", ctypes.c_void_p),
+                ("d_conv_state_out", ctypes.c_void_p), ("d_ssm_state", ctypes.c_void_p),
+                ("d_conv_state", ctypes.c_void_p)]
+
+
 _LIB = None
 _LOCK = threading.Lock()
 _vp = ctypes.c_void_p
@@ -93,6 +108,16 @@ def _lib_handle(build_if_missing: bool = True):
             lib.m3scan_bwd.argtypes = ([ctypes.POINTER(M3Dims), ctypes.c_int] + [_vp] * 5
                                        + [_fp] * 5 + [_fp, _vp] + [_vp] * 4 + [_fp] * 2
                                        + [_fp] * 5 + [_vp, ctypes.c_size_t, _vp])
+            lib.m3scan_fwd_state.restype = ctypes.c_int
+            lib.m3scan_fwd_state.argtypes = ([ctypes.POINTER(M3Dims), ctypes.c_int] + [_vp] * 5
+                                             + [_fp] * 5 + [_vp, _vp, _fp]
+                                             + [ctypes.POINTER(M3FwdState)]
+                                             + [_vp, ctypes.c_size_t, _vp])
+            lib.m3scan_bwd_state.restype = ctypes.c_int
+            lib.m3scan_bwd_state.argtypes = ([ctypes.POINTER(M3Dims), ctypes.c_int] + [_vp] * 5
+                                             + [_fp] * 5 + [_fp, _vp] + [_vp] * 4 + [_fp] * 2
+                                             + [_fp] * 5 + [ctypes.POINTER(M3BwdState)]
+                                             + [_vp, ctypes.c_size_t, _vp])
             lib.m3scan_bwd_noalloc.restype = ctypes.c_int
             lib.m3scan_bwd_noalloc.argtypes = ([ctypes.POINTER(M3Dims), ctypes.c_int] + [_vp] * 5
                                                + [_fp] * 5 + [_fp, _vp] + [_vp] * 4
@@ -151,6 +176,29 @@ def raw_bwd(dims, act, x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, 
                                     d_delta_raw, dz, du_dbg, dB, dC, d_conv_w, d_conv_b,
                                     d_dt_bias, d_a_log, dD, workspace, int(workspace_bytes),
                                     stream)
+
+
+def raw_fwd_state(dims, act, x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D,
+                  gated, y_dbg, ckpt, state, workspace, workspace_bytes, stream) -> int:
+    """Call m3scan_fwd_state (``state`` an M3FwdState or None); returns the
+    status code."""
+    sp = ctypes.byref(state) if state is not None else None
+    return _lib_handle().m3scan_fwd_state(ctypes.byref(dims), int(act), x, delta_raw, z, Bm, Cm,
+                                          conv_w, conv_b, dt_bias, a_log, D, gated, y_dbg, ckpt,
+                                          sp, workspace, int(workspace_bytes), stream)
+
+
+def raw_bwd_state(dims, act, x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D, ckpt,
+                  d_gated, d_x, d_delta_raw, dz, du_dbg, dB, dC, d_conv_w, d_conv_b, d_dt_bias,
+                  d_a_log, dD, state, workspace, workspace_bytes, stream) -> int:
+    """Call m3scan_bwd_state (``state`` an M3BwdState or None); returns the
+    status code."""
+    sp = ctypes.byref(state) if state is not None else None
+    return _lib_handle().m3scan_bwd_state(ctypes.byref(dims), int(act), x, delta_raw, z, Bm, Cm,
+                                          conv_w, conv_b, dt_bias, a_log, D, ckpt, d_gated, d_x,
+                                          d_delta_raw, dz, du_dbg, dB, dC, d_conv_w, d_conv_b,
+                                          d_dt_bias, d_a_log, dD, sp, workspace,
+                                          int(workspace_bytes), stream)
 
 
 def raw_bwd_noalloc(dims, act, x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D,
@@ -229,6 +277,37 @@ def m3scan_fwd(x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D, *, ch
                segments=0, gated=None, y_dbg=None, want_y=False, ckpt=None, workspace=None,
                stream=None):
     """Forward of the layer core.  Returns (gated, ckpt, y_dbg or None)."""
+    return _fwd(x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D, chunk, segments,
+                gated, y_dbg, want_y, ckpt, workspace, stream, None)[:3]
+
+
+def m3scan_fwd_state(x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D, *,
+                     ssm_state=None, conv_state=None, chunk=0, segments=0, gated=None,
+                     y_dbg=None, want_y=False, ckpt=None, ssm_state_out=None,
+                     conv_state_out=None, workspace=None, stream=None):
+    """Forward of one window from a carried state (None = zero).  Returns
+    (gated, ckpt, y_dbg or None, ssm_state_out [B,16,D] f32,
+    conv_state_out [B,3,D] activation dtype)."""
+    torch = _torch()
+    Bsz, _, Dn = x.shape
+    N, W = Bm.shape[-1], conv_w.shape[-1]
+    if ssm_state_out is None:
+        ssm_state_out = torch.empty((Bsz, N, Dn), dtype=torch.float32, device=x.device)
+    if conv_state_out is None:
+        conv_state_out = torch.empty((Bsz, W - 1, Dn), dtype=x.dtype, device=x.device)
+    _check(ssm_state, "ssm_state", torch.float32, x.device)
+    _check(conv_state, "conv_state", x.dtype, x.device)
+    _check(ssm_state_out, "ssm_state_out", torch.float32, x.device)
+    _check(conv_state_out, "conv_state_out", x.dtype, x.device)
+    st = M3FwdState(_ptr(ssm_state), _ptr(conv_state), _ptr(ssm_state_out),
+                    _ptr(conv_state_out))
+    gated, ckpt, y_dbg = _fwd(x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D, chunk,
+                              segments, gated, y_dbg, want_y, ckpt, workspace, stream, st)[:3]
+    return gated, ckpt, y_dbg, ssm_state_out, conv_state_out
+
+
+def _fwd(x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D, chunk, segments, gated,
+         y_dbg, want_y, ckpt, workspace, stream, state):
     torch = _torch()
     act = x.dtype
     dev = x.device
@@ -250,12 +329,16 @@ def m3scan_fwd(x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D, *, ch
         ckpt = torch.empty((Bsz, pl.n_chunks, Bm.shape[-1], Dn), dtype=torch.float32, device=dev)
     if workspace is None:
         workspace = Workspace(pl.workspace_bytes, dev)
-    st = raw_fwd(dims, code, _ptr(x), _ptr(delta_raw), _ptr(z), _ptr(Bm), _ptr(Cm),
-                 _ptr(conv_w), _ptr(conv_b), _ptr(dt_bias), _ptr(a_log), _ptr(D),
-                 _ptr(gated), _ptr(y_dbg), _ptr(ckpt), workspace.ptr, workspace.nbytes,
-                 _stream_handle(stream))
+    args = (dims, code, _ptr(x), _ptr(delta_raw), _ptr(z), _ptr(Bm), _ptr(Cm),
+            _ptr(conv_w), _ptr(conv_b), _ptr(dt_bias), _ptr(a_log), _ptr(D),
+            _ptr(gated), _ptr(y_dbg), _ptr(ckpt))
+    tail = (workspace.ptr, workspace.nbytes, _stream_handle(stream))
+    if state is None:
+        st = raw_fwd(*args, *tail)
+    else:
+        st = raw_fwd_state(*args, state, *tail)
     if st != 0:
-        raise M3Error(st, "m3scan_fwd")
+        raise M3Error(st, "m3scan_fwd" if state is None else "m3scan_fwd_state")
     return gated, ckpt, y_dbg
 
 
@@ -263,6 +346,36 @@ def m3scan_bwd(x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D, ckpt,
                chunk=0, segments=0, want_du=False, accumulate_param_grads=False, out=None,
                workspace=None, stream=None):
     """Backward of the layer core.  Returns a dict of gradients (tensors)."""
+    return _bwd(x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D, ckpt, d_gated,
+                chunk, segments, want_du, accumulate_param_grads, out, workspace, stream, None)
+
+
+def m3scan_bwd_state(x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D, ckpt, d_gated,
+                     *, conv_state=None, d_ssm_state_out=None, d_conv_state_out=None, chunk=0,
+                     segments=0, want_du=False, accumulate_param_grads=False, out=None,
+                     workspace=None, stream=None):
+    """Backward of one window made by ``m3scan_fwd_state``.  Returns the
+    gradients of ``m3scan_bwd`` plus ``d_ssm_state`` [B,16,D] f32 and
+    ``d_conv_state`` [B,3,D] (activation dtype)."""
+    torch = _torch()
+    Bsz, _, Dn = x.shape
+    N, W = Bm.shape[-1], conv_w.shape[-1]
+    o = dict(out or {})
+    o.setdefault("d_ssm_state", torch.empty((Bsz, N, Dn), dtype=torch.float32, device=x.device))
+    o.setdefault("d_conv_state", torch.empty((Bsz, W - 1, Dn), dtype=x.dtype, device=x.device))
+    _check(conv_state, "conv_state", x.dtype, x.device)
+    _check(d_ssm_state_out, "d_ssm_state_out", torch.float32, x.device)
+    _check(d_conv_state_out, "d_conv_state_out", x.dtype, x.device)
+    _check(o["d_ssm_state"], "d_ssm_state", torch.float32, x.device)
+    _check(o["d_conv_state"], "d_conv_state", x.dtype, x.device)
+    st = M3BwdState(_ptr(conv_state), _ptr(d_ssm_state_out), _ptr(d_conv_state_out),
+                    _ptr(o["d_ssm_state"]), _ptr(o["d_conv_state"]))
+    return _bwd(x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D, ckpt, d_gated,
+                chunk, segments, want_du, accumulate_param_grads, o, workspace, stream, st)
+
+
+def _bwd(x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D, ckpt, d_gated, chunk,
+         segments, want_du, accumulate_param_grads, out, workspace, stream, state):
     torch = _torch()
     act = x.dtype
     dev = x.device
@@ -297,12 +410,16 @@ def m3scan_bwd(x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D, ckpt,
         _check(v, k, None, dev)
     if workspace is None:
         workspace = Workspace(pl.workspace_bytes, dev)
-    st = raw_bwd(dims, code, _ptr(x), _ptr(delta_raw), _ptr(z), _ptr(Bm), _ptr(Cm),
-                 _ptr(conv_w), _ptr(conv_b), _ptr(dt_bias), _ptr(a_log), _ptr(D), _ptr(ckpt),
-                 _ptr(d_gated), _ptr(o["d_x"]), _ptr(o["d_delta_raw"]), _ptr(o["dz"]),
-                 _ptr(o.get("du")), _ptr(o["dB"]), _ptr(o["dC"]), _ptr(o["d_conv_w"]),
-                 _ptr(o["d_conv_b"]), _ptr(o["d_dt_bias"]), _ptr(o["d_a_log"]), _ptr(o["dD"]),
-                 workspace.ptr, workspace.nbytes, _stream_handle(stream))
+    args = (dims, code, _ptr(x), _ptr(delta_raw), _ptr(z), _ptr(Bm), _ptr(Cm),
+            _ptr(conv_w), _ptr(conv_b), _ptr(dt_bias), _ptr(a_log), _ptr(D), _ptr(ckpt),
+            _ptr(d_gated), _ptr(o["d_x"]), _ptr(o["d_delta_raw"]), _ptr(o["dz"]),
+            _ptr(o.get("du")), _ptr(o["dB"]), _ptr(o["dC"]), _ptr(o["d_conv_w"]),
+            _ptr(o["d_conv_b"]), _ptr(o["d_dt_bias"]), _ptr(o["d_a_log"]), _ptr(o["dD"]))
+    tail = (workspace.ptr, workspace.nbytes, _stream_handle(stream))
+    if state is None:
+        st = raw_bwd(*args, *tail)
+    else:
+        st = raw_bwd_state(*args, state, *tail)
     if st != 0:
-        raise M3Error(st, "m3scan_bwd")
+        raise M3Error(st, "m3scan_bwd" if state is None else "m3scan_bwd_state")
     return o

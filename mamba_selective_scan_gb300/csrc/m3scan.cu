@@ -206,6 +206,12 @@ struct FwdArgs {
   void *gated, *y_dbg;
   float* ckpt;
   float *agg_h, *agg_s;
+  // carried state (all nullable): h before step 0 [B, 16, D] f32, the conv
+  // inputs of steps -3..-1 [B, 3, D] act, and the same two after the window
+  const float* h_in;
+  const void* conv_in;
+  float* h_out;
+  void* conv_out;
 };
 
 struct BwdArgs {
@@ -216,6 +222,15 @@ struct BwdArgs {
   float *dB, *dC;
   float *q, *sd, *dxpart, *dchead, *partials;
   float *d_conv_w, *d_conv_b, *d_dt_bias, *d_a_log, *dD;
+  // carried state (all nullable): the forward's conv inputs of steps -3..-1
+  // [B, 3, D] act; upstream gradients of the window's state outputs
+  // (g_h [B, 16, D] f32, g_conv [B, 3, D] act); gradients of the state
+  // inputs (d_h_in f32, d_conv_in act)
+  const void* conv_in;
+  const float* g_h;
+  const void* g_conv;
+  float* d_h_in;
+  void* d_conv_in;
   int accumulate;
   uint32_t tcols;  // tensor-memory columns per CTA for the state history
 };
@@ -348,6 +363,11 @@ __global__ void __launch_bounds__(GF) m3_fwd_kernel(FwdArgs a) {
   float2 h[NS / 2];
 #pragma unroll
   for (int i = 0; i < NS / 2; ++i) h[i] = make_float2(0.f, 0.f);
+  if (FINAL && a.h_in && active) {  // the local passes start from zero
+    const float* h0 = a.h_in + (size_t)b * NS * g.D + d;
+#pragma unroll
+    for (int i = 0; i < NS / 2; ++i) h[i] = make_float2(h0[(size_t)(2 * i) * g.D], h0[(size_t)(2 * i + 1) * g.D]);
+  }
   if (FINAL && s > 0) {
     // The scan is linear in the state: chain the earlier segments' local end
     // states with their decays, start(s'+1) = exp(A sum delta_s') start(s') +
@@ -367,11 +387,18 @@ __global__ void __launch_bounds__(GF) m3_fwd_kernel(FwdArgs a) {
     }
   }
 
-  float xm3 = 0.f, xm2 = 0.f, xm1 = 0.f;  // conv window x[t-3], x[t-2], x[t-1]
+  // conv window x[t-3], x[t-2], x[t-1]; steps before 0 come from the
+  // carried conv inputs (row step + 3), zero without them
+  auto x_at = [&](int t) -> float {
+    if (t >= 0) return Act<T>::ld(xg + ((size_t)b * g.T + t) * g.D + d);
+    if (a.conv_in) return Act<T>::ld(static_cast<const T*>(a.conv_in) + ((size_t)b * 3 + t + 3) * g.D + d);
+    return 0.f;
+  };
+  float xm3 = 0.f, xm2 = 0.f, xm1 = 0.f;
   if (active) {
-    if (t_begin >= 3) xm3 = Act<T>::ld(xg + ((size_t)b * g.T + t_begin - 3) * g.D + d);
-    if (t_begin >= 2) xm2 = Act<T>::ld(xg + ((size_t)b * g.T + t_begin - 2) * g.D + d);
-    if (t_begin >= 1) xm1 = Act<T>::ld(xg + ((size_t)b * g.T + t_begin - 1) * g.D + d);
+    xm3 = x_at(t_begin - 3);
+    xm2 = x_at(t_begin - 2);
+    xm1 = x_at(t_begin - 1);
   }
   float sdelta = 0.f;
 
@@ -475,6 +502,22 @@ __global__ void __launch_bounds__(GF) m3_fwd_kernel(FwdArgs a) {
       }
     }
     __syncthreads();
+  }
+  if (FINAL && s == g.S - 1 && active) {
+    if (a.h_out) {
+      float* ho = a.h_out + (size_t)b * NS * g.D + d;
+#pragma unroll
+      for (int i = 0; i < NS / 2; ++i) {
+        ho[(size_t)(2 * i) * g.D] = h[i].x;
+        ho[(size_t)(2 * i + 1) * g.D] = h[i].y;
+      }
+    }
+    if (a.conv_out) {  // the window now holds x[T-3], x[T-2], x[T-1]
+      T* co = static_cast<T*>(a.conv_out) + (size_t)b * 3 * g.D + d;
+      Act<T>::st(co, xm3);
+      Act<T>::st(co + g.D, xm2);
+      Act<T>::st(co + 2 * (size_t)g.D, xm1);
+    }
   }
   if (!FINAL && active) {
     float* ah = a.agg_h + (((size_t)b * g.S + s) * NS) * g.D + d;
@@ -692,6 +735,14 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(BwdArgs a) {
   float2 carry[NS / 2];
 #pragma unroll
   for (int i = 0; i < NS / 2; ++i) carry[i] = make_float2(0.f, 0.f);
+  if (a.g_h && active) {  // the gradient of the state output enters after the last step
+    const float* gh = a.g_h + (size_t)b * NS * g.D + d;
+#pragma unroll
+    for (int i = 0; i < NS / 2; ++i) {
+      const int n = lane_of(i);
+      carry[i] = make_float2(gh[(size_t)n * g.D], gh[(size_t)(n + 1) * g.D]);
+    }
+  }
   if (s + 1 < g.S) {
     // chain the later segments right to left: in(s'-1) = exp(A sum delta_s')
     // in(s') + local(s'), with in(S-1) = 0
@@ -743,6 +794,13 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(BwdArgs a) {
     }
     __syncthreads();
     const unsigned char* base = smem + (size_t)buf * L.tile;
+    if (a.conv_in && c * K < 3 && active) {
+      // halo rows before step 0 (staged as zeros): the carried conv inputs.
+      // Only this thread reads its column of the x tile.
+      T* xw = reinterpret_cast<T*>(smem + (size_t)buf * L.tile + L.x);
+      const T* ci = static_cast<const T*>(a.conv_in) + (size_t)b * 3 * g.D + d;
+      for (int r = 0; r < 3 - c * K; ++r) xw[r * GB + tid] = ci[(size_t)(c * K + r) * g.D];
+    }
     {
       const T* Bt = reinterpret_cast<const T*>(base + L.Bt);
       const T* Ct = reinterpret_cast<const T*>(base + L.Ct);
@@ -911,7 +969,9 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(BwdArgs a) {
         dcb_acc += dc;
 #pragma unroll
         for (int k = 0; k < WC; ++k) dcw[k] = fmaf(dc, Act<T>::ld(xt + (j + k) * GB + tid), dcw[k]);
-        const float dxv = fmaf(dc, w[3], fmaf(dc1, w[2], fmaf(dc2, w[1], dc3 * w[0])));
+        float dxv = fmaf(dc, w[3], fmaf(dc1, w[2], fmaf(dc2, w[1], dc3 * w[0])));
+        if (a.g_conv && t >= g.T - 3 && active)  // x[t] is also a conv-state output
+          dxv += Act<T>::ld(static_cast<const T*>(a.g_conv) + ((size_t)b * 3 + t - (g.T - 3)) * g.D + d);
         dc3 = dc2;
         dc2 = dc1;
         dc1 = dc;
@@ -941,6 +1001,34 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(BwdArgs a) {
     __syncthreads();
   }
 
+  if (s == 0 && active) {
+    if (a.d_h_in) {  // carry = exp(delta_0 A) dL/dh_0 = dL/dh_{-1}
+      float* dh0 = a.d_h_in + (size_t)b * NS * g.D + d;
+#pragma unroll
+      for (int i = 0; i < NS / 2; ++i) {
+        const int n = lane_of(i);
+        dh0[(size_t)n * g.D] = carry[i].x;
+        dh0[(size_t)(n + 1) * g.D] = carry[i].y;
+      }
+    }
+    if (a.d_conv_in) {
+      // conv inputs of steps -1, -2, -3 reach the conv outputs of steps
+      // 0..2 (dc1 = dc_0, dc2 = dc_1, dc3 = dc_2; zero past the sequence),
+      // and, when T < 3, the conv-state output too
+      float v[3];
+      v[2] = fmaf(dc1, w[2], fmaf(dc2, w[1], dc3 * w[0]));
+      v[1] = fmaf(dc1, w[1], dc2 * w[0]);
+      v[0] = dc1 * w[0];
+      T* dci = static_cast<T*>(a.d_conv_in) + (size_t)b * 3 * g.D + d;
+#pragma unroll
+      for (int r = 0; r < 3; ++r) {
+        const int ro = r - g.T;  // row of the conv-state output holding step r - 3
+        if (a.g_conv && ro >= 0)
+          v[r] += Act<T>::ld(static_cast<const T*>(a.g_conv) + ((size_t)b * 3 + ro) * g.D + d);
+        Act<T>::st(dci + (size_t)r * g.D, v[r]);
+      }
+    }
+  }
   if (active) {
     float* Pp = a.partials + ((size_t)b * g.S + s) * NPART * g.D;
 #pragma unroll
@@ -1359,15 +1447,46 @@ m3_status m3scan_plan(const m3_dims* dims, m3_dtype act, m3_plan* out) {
   return M3_OK;
 }
 
-m3_status m3scan_fwd(const m3_dims* dims, m3_dtype act, const void* x, const void* delta_raw,
-                     const void* z, const void* Bm, const void* Cm, const float* conv_w,
-                     const float* conv_b, const float* dt_bias, const float* a_log, const float* D,
-                     void* gated, void* y_dbg, float* ckpt, void* workspace, size_t workspace_bytes,
-                     m3_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// A window with no steps: the state outputs are the state inputs (zero when
+// absent), and the state-input gradients are the upstream gradients.
+m3_status pass_state(const void* in, void* out, size_t bytes, cudaStream_t s) {
+  if (!out || bytes == 0) return M3_OK;
+  const cudaError_t e = in ? cudaMemcpyAsync(out, in, bytes, cudaMemcpyDeviceToDevice, s)
+                           : cudaMemsetAsync(out, 0, bytes, s);
+  return note(e) == cudaSuccess ? M3_OK : M3_ERR_CUDA;
+}
+
+// Alignment of the carried-state pointers: f32 arrays 4 bytes, activation
+// arrays one element.
+bool state_aligned(const void* f32a, const void* f32b, const void* acta, const void* actb,
+                   m3_dtype act) {
+  const size_t ea = act == M3_BF16 ? 2 : 4;
+  return aligned(f32a, 4) && aligned(f32b, 4) && aligned(acta, ea) && aligned(actb, ea);
+}
+
+m3_status fwd_impl(const m3_dims* dims, m3_dtype act, const void* x, const void* delta_raw,
+                   const void* z, const void* Bm, const void* Cm, const float* conv_w,
+                   const float* conv_b, const float* dt_bias, const float* a_log, const float* D,
+                   void* gated, void* y_dbg, float* ckpt, const m3_fwd_state* state,
+                   void* workspace, size_t workspace_bytes, m3_stream_t stream) {
   Plan p;
   m3_status st = make_plan(dims, act, &p);
   if (st != M3_OK) return st;
-  if ((size_t)p.B * p.T * p.D == 0) return M3_OK;
+  const m3_fwd_state none{};
+  const m3_fwd_state& sv = state ? *state : none;
+  if (!state_aligned(sv.ssm_state, sv.ssm_state_out, sv.conv_state, sv.conv_state_out, act))
+    return M3_ERR_ALIGN;
+  if ((size_t)p.B * p.T * p.D == 0) {
+    const size_t bd = (size_t)p.B * p.D;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    st = pass_state(sv.ssm_state, sv.ssm_state_out, bd * NS * 4, s);
+    if (st == M3_OK) st = pass_state(sv.conv_state, sv.conv_state_out, bd * 3 * (act == M3_BF16 ? 2 : 4), s);
+    return st;
+  }
   if (!x || !delta_raw || !z || !Bm || !Cm || !conv_w || !conv_b || !dt_bias || !a_log || !D ||
       !gated || !ckpt)
     return M3_ERR_NULL;
@@ -1392,22 +1511,34 @@ m3_status m3scan_fwd(const m3_dims* dims, m3_dtype act, const void* x, const voi
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   a.agg_h = p.Sf > 1 ? reinterpret_cast<float*>(ws + p.f_aggh) : nullptr;
   a.agg_s = p.Sf > 1 ? reinterpret_cast<float*>(ws + p.f_aggs) : nullptr;
+  a.h_in = sv.ssm_state; a.conv_in = sv.conv_state;
+  a.h_out = sv.ssm_state_out; a.conv_out = sv.conv_state_out;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   return act == M3_BF16 ? launch_fwd<__nv_bfloat16>(p, a, s) : launch_fwd<float>(p, a, s);
 }
 
-m3_status m3scan_bwd(const m3_dims* dims, m3_dtype act, const void* x, const void* delta_raw,
-                     const void* z, const void* Bm, const void* Cm, const float* conv_w,
-                     const float* conv_b, const float* dt_bias, const float* a_log, const float* D,
-                     const float* ckpt, const void* d_gated, void* d_x, void* d_delta_raw, void* dz,
-                     void* du_dbg, float* dB, float* dC, float* d_conv_w, float* d_conv_b,
-                     float* d_dt_bias, float* d_a_log, float* dD, void* workspace,
-                     size_t workspace_bytes, m3_stream_t stream) {
+m3_status bwd_impl(const m3_dims* dims, m3_dtype act, const void* x, const void* delta_raw,
+                   const void* z, const void* Bm, const void* Cm, const float* conv_w,
+                   const float* conv_b, const float* dt_bias, const float* a_log, const float* D,
+                   const float* ckpt, const void* d_gated, void* d_x, void* d_delta_raw, void* dz,
+                   void* du_dbg, float* dB, float* dC, float* d_conv_w, float* d_conv_b,
+                   float* d_dt_bias, float* d_a_log, float* dD, const m3_bwd_state* state,
+                   void* workspace, size_t workspace_bytes, m3_stream_t stream) {
   Plan p;
   m3_status st = make_plan(dims, act, &p);
   if (st != M3_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const m3_bwd_state none{};
+  const m3_bwd_state& sv = state ? *state : none;
+  if (!state_aligned(sv.d_ssm_state_out, sv.d_ssm_state, sv.conv_state, sv.d_conv_state_out, act) ||
+      !aligned(sv.d_conv_state, act == M3_BF16 ? 2 : 4))
+    return M3_ERR_ALIGN;
   if ((size_t)p.B * p.T * p.D == 0) {
+    const size_t bd = (size_t)p.B * p.D;
+    st = pass_state(sv.d_ssm_state_out, sv.d_ssm_state, bd * NS * 4, s);
+    if (st == M3_OK)
+      st = pass_state(sv.d_conv_state_out, sv.d_conv_state, bd * 3 * (act == M3_BF16 ? 2 : 4), s);
+    if (st != M3_OK) return st;
     // no elements: parameter grads are zero (or unchanged when accumulating)
     if (p.D > 0 && !dims->accumulate_param_grads) {
       if (!d_conv_w || !d_conv_b || !d_dt_bias || !d_a_log || !dD) return M3_ERR_NULL;
@@ -1457,10 +1588,63 @@ m3_status m3scan_bwd(const m3_dims* dims, m3_dtype act, const void* x, const voi
   a.d_conv_w = d_conv_w; a.d_conv_b = d_conv_b; a.d_dt_bias = d_dt_bias; a.d_a_log = d_a_log;
   a.dD = dD;
   a.accumulate = dims->accumulate_param_grads ? 1 : 0;
+  a.conv_in = sv.conv_state; a.g_h = sv.d_ssm_state_out; a.g_conv = sv.d_conv_state_out;
+  a.d_h_in = sv.d_ssm_state; a.d_conv_in = sv.d_conv_state;
   m3_status r = act == M3_BF16 ? launch_bwd<__nv_bfloat16>(p, a, s, smem_sm)
                                 : launch_bwd<float>(p, a, s, smem_sm);
   if (r != M3_OK) cudaGetLastError();
   return r;
+}
+
+}  // namespace
+
+extern "C" {
+
+m3_status m3scan_fwd(const m3_dims* dims, m3_dtype act, const void* x, const void* delta_raw,
+                     const void* z, const void* Bm, const void* Cm, const float* conv_w,
+                     const float* conv_b, const float* dt_bias, const float* a_log, const float* D,
+                     void* gated, void* y_dbg, float* ckpt, void* workspace, size_t workspace_bytes,
+                     m3_stream_t stream) {
+  return fwd_impl(dims, act, x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D, gated,
+                  y_dbg, ckpt, nullptr, workspace, workspace_bytes, stream);
+}
+
+m3_status m3scan_fwd_state(const m3_dims* dims, m3_dtype act, const void* x,
+                           const void* delta_raw, const void* z, const void* Bm, const void* Cm,
+                           const float* conv_w, const float* conv_b, const float* dt_bias,
+                           const float* a_log, const float* D, void* gated, void* y_dbg,
+                           float* ckpt, const m3_fwd_state* state, void* workspace,
+                           size_t workspace_bytes, m3_stream_t stream) {
+  if (!state) return M3_ERR_NULL;
+  return fwd_impl(dims, act, x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D, gated,
+                  y_dbg, ckpt, state, workspace, workspace_bytes, stream);
+}
+
+m3_status m3scan_bwd(const m3_dims* dims, m3_dtype act, const void* x, const void* delta_raw,
+                     const void* z, const void* Bm, const void* Cm, const float* conv_w,
+                     const float* conv_b, const float* dt_bias, const float* a_log, const float* D,
+                     const float* ckpt, const void* d_gated, void* d_x, void* d_delta_raw, void* dz,
+                     void* du_dbg, float* dB, float* dC, float* d_conv_w, float* d_conv_b,
+                     float* d_dt_bias, float* d_a_log, float* dD, void* workspace,
+                     size_t workspace_bytes, m3_stream_t stream) {
+  return bwd_impl(dims, act, x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D, ckpt,
+                  d_gated, d_x, d_delta_raw, dz, du_dbg, dB, dC, d_conv_w, d_conv_b, d_dt_bias,
+                  d_a_log, dD, nullptr, workspace, workspace_bytes, stream);
+}
+
+m3_status m3scan_bwd_state(const m3_dims* dims, m3_dtype act, const void* x,
+                           const void* delta_raw, const void* z, const void* Bm, const void* Cm,
+                           const float* conv_w, const float* conv_b, const float* dt_bias,
+                           const float* a_log, const float* D, const float* ckpt,
+                           const void* d_gated, void* d_x, void* d_delta_raw, void* dz,
+                           void* du_dbg, float* dB, float* dC, float* d_conv_w, float* d_conv_b,
+                           float* d_dt_bias, float* d_a_log, float* dD,
+                           const m3_bwd_state* state, void* workspace, size_t workspace_bytes,
+                           m3_stream_t stream) {
+  if (!state) return M3_ERR_NULL;
+  return bwd_impl(dims, act, x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D, ckpt,
+                  d_gated, d_x, d_delta_raw, dz, du_dbg, dB, dC, d_conv_w, d_conv_b, d_dt_bias,
+                  d_a_log, dD, state, workspace, workspace_bytes, stream);
 }
 
 

@@ -170,3 +170,45 @@ def test_bwd_rejects_bad_arguments_before_any_launch(lib):
     assert _bwd(dims, workspace_bytes=255) == "M3_ERR_WORKSPACE"
     assert _bwd(dims, workspace=A + 128) == "M3_ERR_ALIGN"
     assert _bwd(binding.make_dims(2, 64, 64, d_state=32, segments=1)) == "M3_ERR_UNSUPPORTED"
+
+
+def _fwd_state(dims, state, act=binding.M3_BF16, **over):
+    a = dict(x=A, delta_raw=A, z=A, Bm=A, Cm=A, conv_w=A, conv_b=A, dt_bias=A, a_log=A, D=A,
+             gated=A, y_dbg=None, ckpt=A)
+    a.update(over)
+    return binding.STATUS[binding.raw_fwd_state(dims, act, *a.values(), state, A, 1 << 30,
+                                                None)]
+
+
+def _bwd_state(dims, state, act=binding.M3_BF16):
+    a = dict(x=A, delta_raw=A, z=A, Bm=A, Cm=A, conv_w=A, conv_b=A, dt_bias=A, a_log=A, D=A,
+             ckpt=A, d_gated=A, d_x=A, d_delta_raw=A, dz=A, du_dbg=None, dB=A, dC=A,
+             d_conv_w=A, d_conv_b=A, d_dt_bias=A, d_a_log=A, dD=A)
+    return binding.STATUS[binding.raw_bwd_state(dims, act, *a.values(), state, A, 1 << 30, None)]
+
+
+def test_state_entry_points_validate_before_any_launch(lib):
+    dims = binding.make_dims(2, 64, 64, chunk=16, segments=2)
+    # the state struct itself is required by the _state entry points
+    assert _fwd_state(dims, None) == "M3_ERR_NULL"
+    assert _bwd_state(dims, None) == "M3_ERR_NULL"
+    # float32 state 4-byte aligned, activation-dtype state aligned to its element
+    assert _fwd_state(dims, binding.M3FwdState(A + 2, None, None, None)) == "M3_ERR_ALIGN"
+    assert _fwd_state(dims, binding.M3FwdState(None, None, None, A + 1)) == "M3_ERR_ALIGN"
+    assert _fwd_state(dims, binding.M3FwdState(None, A + 2, None, None),
+                      act=binding.M3_F32) == "M3_ERR_ALIGN"
+    assert _bwd_state(dims, binding.M3BwdState(None, A + 2, None, None, None)) == "M3_ERR_ALIGN"
+    assert _bwd_state(dims, binding.M3BwdState(None, None, None, None, A + 1)) == "M3_ERR_ALIGN"
+    # the other arguments are still checked
+    assert _fwd_state(dims, binding.M3FwdState(A, A + 2, A, A + 2), x=None) == "M3_ERR_NULL"
+
+
+def test_state_structs_match_the_header_layout():
+    assert ctypes.sizeof(binding.M3FwdState) == 4 * ctypes.sizeof(ctypes.c_void_p)
+    assert ctypes.sizeof(binding.M3BwdState) == 5 * ctypes.sizeof(ctypes.c_void_p)
+    src = open(os.path.join(ROOT, "include", "m3scan.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    for struct, cls in (("m3_fwd_state", binding.M3FwdState), ("m3_bwd_state", binding.M3BwdState)):
+        body = re.search(r"typedef struct \{([^{}]*)\}\s*" + struct + ";", src).group(1)
+        names = re.findall(r"(\w+);", body)
+        assert names == [f for f, _ in cls._fields_], struct
