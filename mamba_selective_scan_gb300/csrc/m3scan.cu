@@ -151,6 +151,14 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float2 (&v)[NS / 2]) {
         "=f"(v[3].x), "=f"(v[3].y), "=f"(v[4].x), "=f"(v[4].y), "=f"(v[5].x), "=f"(v[5].y),
         "=f"(v[6].x), "=f"(v[6].y), "=f"(v[7].x), "=f"(v[7].y) : "r"(taddr) : "memory");
 }
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start while the kernel before it in the stream is still
+// running; grid_dep_wait() returns once that kernel has completed and its
+// memory is visible (immediately when there is no such dependency).
+// grid_dep_trigger() lets the next such kernel start launching.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
@@ -346,6 +354,7 @@ __global__ void __launch_bounds__(GF) m3_fwd_kernel(FwdArgs a) {
     cp_async_commit();
   };
   stage(t_begin, 0);  // first tile in flight while the parameters and carries load
+  if (!FINAL) grid_dep_trigger();
 
   float2 a2[NS / 2];  // A log2(e) for lanes (2i, 2i+1)
 #pragma unroll
@@ -369,6 +378,7 @@ __global__ void __launch_bounds__(GF) m3_fwd_kernel(FwdArgs a) {
     for (int i = 0; i < NS / 2; ++i) h[i] = make_float2(h0[(size_t)(2 * i) * g.D], h0[(size_t)(2 * i + 1) * g.D]);
   }
   if (FINAL && s > 0) {
+    grid_dep_wait();  // the aggregate pass's outputs
     // The scan is linear in the state: chain the earlier segments' local end
     // states with their decays, start(s'+1) = exp(A sum delta_s') start(s') +
     // local_end(s'), to get this segment's true start state.
@@ -565,6 +575,7 @@ __global__ void __launch_bounds__(GB) m3_bwd_agg_kernel(BwdArgs a) {
   };
 
   stage(0, 0);  // first tile in flight while the parameters load
+  grid_dep_trigger();
 
   float2 a2[NS / 2];
 #pragma unroll
@@ -678,7 +689,9 @@ __device__ __forceinline__ float warp_sum16_rotated(float (&v)[NS], int lane) {
   return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 16);
 }
 
-template <typename T>
+// ST: compiled with the carried-state terms; the plain entry points run the
+// instance without them.
+template <typename T, bool ST>
 __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(BwdArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   const Geo g = a.g;
@@ -735,7 +748,7 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(BwdArgs a) {
   float2 carry[NS / 2];
 #pragma unroll
   for (int i = 0; i < NS / 2; ++i) carry[i] = make_float2(0.f, 0.f);
-  if (a.g_h && active) {  // the gradient of the state output enters after the last step
+  if (ST && a.g_h && active) {  // the gradient of the state output enters after the last step
     const float* gh = a.g_h + (size_t)b * NS * g.D + d;
 #pragma unroll
     for (int i = 0; i < NS / 2; ++i) {
@@ -743,6 +756,27 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(BwdArgs a) {
       carry[i] = make_float2(gh[(size_t)n * g.D], gh[(size_t)(n + 1) * g.D]);
     }
   }
+  const T* xg = static_cast<const T*>(a.x);
+  auto stage = [&](int c, int buf) {
+    unsigned char* base = smem + (size_t)buf * L.tile;
+    const int t0 = c * K;
+    stage_rows<T, GB, GB>(reinterpret_cast<T*>(base + L.x), xg, b, t0 - 3, K + 3, g.T, g.T, g.D, d0, tid);
+    stage_rows<T, GB, GB>(reinterpret_cast<T*>(base + L.dr), static_cast<const T*>(a.dr), b, t0, K, g.T, g.T, g.D, d0, tid);
+    stage_rows<T, GB, GB>(reinterpret_cast<T*>(base + L.z), static_cast<const T*>(a.z), b, t0, K, g.T, g.T, g.D, d0, tid);
+    stage_rows<T, GB, GB>(reinterpret_cast<T*>(base + L.dg), static_cast<const T*>(a.dg), b, t0, K, g.T, g.T, g.D, d0, tid);
+    stage_bc<T, GB>(reinterpret_cast<T*>(base + L.Bt), static_cast<const T*>(a.Bm), b, t0, K, g.T, g.T, tid);
+    stage_bc<T, GB>(reinterpret_cast<T*>(base + L.Ct), static_cast<const T*>(a.Cm), b, t0, K, g.T, g.T, tid);
+    // chunk start state: 16 rows of GB floats from ckpt[b, c, :, d0:d0+GB]
+    stage_rows<float, GB, GB>(reinterpret_cast<float*>(base + L.ck), a.ckpt + ((size_t)b * g.nc + c) * NS * g.D,
+                              0, 0, NS, NS, NS, g.D, d0, tid);
+    cp_async_commit();
+  };
+
+  stage(c_end - 1, 0);  // last chunk in flight while the carries load
+  grid_dep_trigger();
+  // the aggregate kernel's carries, and its clearing of dB and dC before
+  // this kernel's reductions into them
+  grid_dep_wait();
   if (s + 1 < g.S) {
     // chain the later segments right to left: in(s'-1) = exp(A sum delta_s')
     // in(s') + local(s'), with in(S-1) = 0
@@ -767,23 +801,6 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(BwdArgs a) {
   float dcw[WC] = {0.f, 0.f, 0.f, 0.f};
   float dc1 = 0.f, dc2 = 0.f, dc3 = 0.f;  // conv-input gradient at t+1, t+2, t+3
 
-  const T* xg = static_cast<const T*>(a.x);
-  auto stage = [&](int c, int buf) {
-    unsigned char* base = smem + (size_t)buf * L.tile;
-    const int t0 = c * K;
-    stage_rows<T, GB, GB>(reinterpret_cast<T*>(base + L.x), xg, b, t0 - 3, K + 3, g.T, g.T, g.D, d0, tid);
-    stage_rows<T, GB, GB>(reinterpret_cast<T*>(base + L.dr), static_cast<const T*>(a.dr), b, t0, K, g.T, g.T, g.D, d0, tid);
-    stage_rows<T, GB, GB>(reinterpret_cast<T*>(base + L.z), static_cast<const T*>(a.z), b, t0, K, g.T, g.T, g.D, d0, tid);
-    stage_rows<T, GB, GB>(reinterpret_cast<T*>(base + L.dg), static_cast<const T*>(a.dg), b, t0, K, g.T, g.T, g.D, d0, tid);
-    stage_bc<T, GB>(reinterpret_cast<T*>(base + L.Bt), static_cast<const T*>(a.Bm), b, t0, K, g.T, g.T, tid);
-    stage_bc<T, GB>(reinterpret_cast<T*>(base + L.Ct), static_cast<const T*>(a.Cm), b, t0, K, g.T, g.T, tid);
-    // chunk start state: 16 rows of GB floats from ckpt[b, c, :, d0:d0+GB]
-    stage_rows<float, GB, GB>(reinterpret_cast<float*>(base + L.ck), a.ckpt + ((size_t)b * g.nc + c) * NS * g.D,
-                              0, 0, NS, NS, NS, g.D, d0, tid);
-    cp_async_commit();
-  };
-
-  stage(c_end - 1, 0);
   for (int c = c_end - 1; c >= c_begin; --c) {
     const int buf = (c_end - 1 - c) & 1;
     if (c - 1 >= c_begin) {
@@ -794,7 +811,7 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(BwdArgs a) {
     }
     __syncthreads();
     const unsigned char* base = smem + (size_t)buf * L.tile;
-    if (a.conv_in && c * K < 3 && active) {
+    if (ST && a.conv_in && c * K < 3 && active) {
       // halo rows before step 0 (staged as zeros): the carried conv inputs.
       // Only this thread reads its column of the x tile.
       T* xw = reinterpret_cast<T*>(smem + (size_t)buf * L.tile + L.x);
@@ -970,7 +987,7 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(BwdArgs a) {
 #pragma unroll
         for (int k = 0; k < WC; ++k) dcw[k] = fmaf(dc, Act<T>::ld(xt + (j + k) * GB + tid), dcw[k]);
         float dxv = fmaf(dc, w[3], fmaf(dc1, w[2], fmaf(dc2, w[1], dc3 * w[0])));
-        if (a.g_conv && t >= g.T - 3 && active)  // x[t] is also a conv-state output
+        if (ST && a.g_conv && t >= g.T - 3 && active)  // x[t] is also a conv-state output
           dxv += Act<T>::ld(static_cast<const T*>(a.g_conv) + ((size_t)b * 3 + t - (g.T - 3)) * g.D + d);
         dc3 = dc2;
         dc2 = dc1;
@@ -1001,7 +1018,7 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(BwdArgs a) {
     __syncthreads();
   }
 
-  if (s == 0 && active) {
+  if (ST && s == 0 && active) {
     if (a.d_h_in) {  // carry = exp(delta_0 A) dL/dh_0 = dL/dh_{-1}
       float* dh0 = a.d_h_in + (size_t)b * NS * g.D + d;
 #pragma unroll
@@ -1050,14 +1067,14 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(BwdArgs a) {
 
 // The backward's last kernel, two roles by block index.
 //  - blocks [0, nfin): parameter gradients, the per-(batch, segment) partials
-//    summed in a fixed order (one thread per output, consecutive threads on
-//    consecutive channels so the row reads coalesce), so the result is
-//    deterministic;
+//    summed in a fixed order (32 outputs per block, rows split over its 8
+//    warps and combined in a fixed tree), so the result is deterministic;
 //  - blocks [nfin, ...): d_x at the last three steps of each segment but the
 //    last, which needs the conv gradient of the next segment's first steps.
 template <typename T>
 __global__ void m3_bwd_tail_kernel(BwdArgs a, int rows, int nfin) {
   const Geo g = a.g;
+  grid_dep_wait();  // the main kernel's partials and boundary terms
   if ((int)blockIdx.x >= nfin) {
     const size_t idx = (size_t)(blockIdx.x - nfin) * blockDim.x + threadIdx.x;
     const size_t total = (size_t)g.B * (g.S - 1) * 3 * g.D;
@@ -1080,25 +1097,33 @@ __global__ void m3_bwd_tail_kernel(BwdArgs a, int rows, int nfin) {
     Act<T>::st(static_cast<T*>(a.dx) + ((size_t)b * g.T + t) * g.D + d, v);
     return;
   }
-  const int oidx = (int)((size_t)blockIdx.x * blockDim.x + threadIdx.x);
-  if (oidx >= 23 * g.D) return;
+  // 32 consecutive outputs per block (coalesced row reads), rows split over
+  // the block's 8 warps: warp w sums rows w, w + 8, ... in order, then warp
+  // 0 adds the 8 partial sums in a fixed order.
+  __shared__ float part[8][33];
+  const int cx = threadIdx.x & 31, ry = threadIdx.x >> 5;
+  const int oidx = blockIdx.x * 32 + cx;
+  const bool ok = oidx < 23 * g.D;
   const int jj = oidx / g.D, d = oidx - jj * g.D;
-  const float* __restrict__ P = a.partials + (size_t)jj * g.D + d;
-  const size_t stride = (size_t)NPART * g.D;
-  // four accumulators over rows r = 0 mod 4, 1 mod 4, ...; combined in a
-  // fixed order
-  float v0 = 0.f, v1 = 0.f, v2 = 0.f, v3 = 0.f;
-  int r = 0;
-  for (; r + 3 < rows; r += 4) {
-    v0 += P[(size_t)r * stride];
-    v1 += P[(size_t)(r + 1) * stride];
-    v2 += P[(size_t)(r + 2) * stride];
-    v3 += P[(size_t)(r + 3) * stride];
+  {
+    float v0 = 0.f, v1 = 0.f;
+    if (ok) {
+      const float* __restrict__ P = a.partials + (size_t)jj * g.D + d;
+      const size_t stride = (size_t)NPART * g.D;
+      int r = ry;
+#pragma unroll 4
+      for (; r + 8 < rows; r += 16) {
+        v0 += P[(size_t)r * stride];
+        v1 += P[(size_t)(r + 8) * stride];
+      }
+      if (r < rows) v0 += P[(size_t)r * stride];
+    }
+    part[ry][cx] = v0 + v1;
   }
-  if (r < rows) v0 += P[(size_t)r * stride];
-  if (r + 1 < rows) v1 += P[(size_t)(r + 1) * stride];
-  if (r + 2 < rows) v2 += P[(size_t)(r + 2) * stride];
-  float v = (v0 + v1) + (v2 + v3);
+  __syncthreads();
+  if (ry != 0 || !ok) return;
+  float v = ((part[0][cx] + part[1][cx]) + (part[2][cx] + part[3][cx])) +
+            ((part[4][cx] + part[5][cx]) + (part[6][cx] + part[7][cx]));
   float* dst;
   if (jj < NS) {
     v *= -expf(a.a_log[(size_t)d * NS + jj]);  // dL/da_log = dL/dA * A
@@ -1191,9 +1216,13 @@ cudaError_t set_attrs() {
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(m3_bwd_agg_kernel<T>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(m3_bwd_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_CAP);
+    e = cudaFuncSetAttribute(m3_bwd_kernel<T, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_CAP);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(m3_bwd_kernel<T>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    e = cudaFuncSetAttribute(m3_bwd_kernel<T, false>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(m3_bwd_kernel<T, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_CAP);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(m3_bwd_kernel<T, true>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   return e;
 }
 
@@ -1225,13 +1254,13 @@ cudaError_t device_info(int chunk, int ai, int* sms, int* occ_f, int* occ_b, int
       e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&of, m3_fwd_kernel<__nv_bfloat16, true>, GF,
                                                         fwd_smem(2).total);
       if (e == cudaSuccess)
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ob, m3_bwd_kernel<__nv_bfloat16>, GB,
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ob, m3_bwd_kernel<__nv_bfloat16, false>, GB,
                                                           bwd_launch_smem(chunk, 2, di.smem_per_sm));
     } else {
       e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&of, m3_fwd_kernel<float, true>, GF,
                                                         fwd_smem(4).total);
       if (e == cudaSuccess)
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ob, m3_bwd_kernel<float>, GB,
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ob, m3_bwd_kernel<float, false>, GB,
                                                           bwd_launch_smem(chunk, 4, di.smem_per_sm));
     }
     if (e != cudaSuccess) return e;
@@ -1372,33 +1401,65 @@ m3_status make_plan(const m3_dims* dm, m3_dtype act, Plan* p) {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// Launch with programmatic stream serialization when `pdl`: the kernel may
+// begin while the previous kernel of the same call runs, and waits for it
+// (grid_dep_wait) before reading its results.  The first kernel of a call
+// is launched without it, so it starts after everything before it.
+template <typename... Args, typename... Vals>
+cudaError_t launch_k(void (*kern)(Args...), dim3 grid, unsigned block, size_t smem,
+                     cudaStream_t st, bool pdl, Vals... vals) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, vals...);
+}
+
 template <typename T>
 m3_status launch_fwd(const Plan& p, FwdArgs a, cudaStream_t st) {
   const int groups = (p.D + GF - 1) / GF;
   const size_t smem = fwd_smem(sizeof(T)).total;
   a.g = Geo{p.B, p.T, p.D, p.K, p.nc, p.Sf, p.mf};
-  if (p.Sf > 1) m3_fwd_kernel<T, false><<<dim3(groups, p.Sf - 1, p.B), GF, smem, st>>>(a);
-  m3_fwd_kernel<T, true><<<dim3(groups, p.Sf, p.B), GF, smem, st>>>(a);
-  return note(cudaGetLastError()) == cudaSuccess ? M3_OK : M3_ERR_CUDA;
+  cudaError_t e = cudaSuccess;
+  if (p.Sf > 1) e = launch_k(m3_fwd_kernel<T, false>, dim3(groups, p.Sf - 1, p.B), GF, smem, st, false, a);
+  if (e == cudaSuccess)
+    e = launch_k(m3_fwd_kernel<T, true>, dim3(groups, p.Sf, p.B), GF, smem, st, p.Sf > 1, a);
+  if (e == cudaSuccess) e = cudaGetLastError();
+  return note(e) == cudaSuccess ? M3_OK : M3_ERR_CUDA;
 }
 
 template <typename T>
 m3_status launch_bwd(const Plan& p, BwdArgs a, cudaStream_t st, int smem_per_sm) {
   const int groups = (p.D + GB - 1) / GB;
   a.g = Geo{p.B, p.T, p.D, p.K, p.nc, p.Sb, p.mb};
+  cudaError_t e = cudaSuccess;
   if (p.Sb > 1) {
     // also clears dB and dC before the main kernel's reductions into them
-    m3_bwd_agg_kernel<T><<<dim3(groups, p.Sb - 1, p.B), GB, agg_smem(sizeof(T)).total, st>>>(a);
+    e = launch_k(m3_bwd_agg_kernel<T>, dim3(groups, p.Sb - 1, p.B), GB, agg_smem(sizeof(T)).total,
+                 st, false, a);
+    if (note(e) != cudaSuccess) return M3_ERR_CUDA;
   } else {
     if (note(cudaMemsetAsync(a.dB, 0, (size_t)p.B * p.T * NS * 4, st)) != cudaSuccess) return M3_ERR_CUDA;
     if (note(cudaMemsetAsync(a.dC, 0, (size_t)p.B * p.T * NS * 4, st)) != cudaSuccess) return M3_ERR_CUDA;
   }
   a.tcols = tmem_cols_for(p.K);
-  m3_bwd_kernel<T><<<dim3(groups, p.Sb, p.B), GB, bwd_launch_smem(p.K, sizeof(T), smem_per_sm), st>>>(a);
-  const size_t nfin = ((size_t)23 * p.D + 255) / 256;                  // one thread per output
+  const size_t smem = bwd_launch_smem(p.K, sizeof(T), smem_per_sm);
+  const bool with_state = a.conv_in || a.g_h || a.g_conv || a.d_h_in || a.d_conv_in;
+  e = launch_k(with_state ? m3_bwd_kernel<T, true> : m3_bwd_kernel<T, false>,
+               dim3(groups, p.Sb, p.B), GB, smem, st, p.Sb > 1, a);
+  const size_t nfin = ((size_t)23 * p.D + 31) / 32;                   // 32 outputs per block
   const size_t nfix = p.Sb > 1 ? ((size_t)p.B * (p.Sb - 1) * 3 * p.D + 255) / 256 : 0;
-  m3_bwd_tail_kernel<T><<<(unsigned)(nfin + nfix), 256, 0, st>>>(a, p.B * p.Sb, (int)nfin);
-  return note(cudaGetLastError()) == cudaSuccess ? M3_OK : M3_ERR_CUDA;
+  if (e == cudaSuccess)
+    e = launch_k(m3_bwd_tail_kernel<T>, dim3((unsigned)(nfin + nfix)), 256, 0, st, true, a,
+                 p.B * p.Sb, (int)nfin);
+  if (e == cudaSuccess) e = cudaGetLastError();
+  return note(e) == cudaSuccess ? M3_OK : M3_ERR_CUDA;
 }
 
 // The device must have this library's kernels registered: fail early and
