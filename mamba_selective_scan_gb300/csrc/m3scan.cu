@@ -441,6 +441,7 @@ __global__ void __launch_bounds__(GF) m3_fwd_kernel(FwdArgs a) {
     for (int j0 = 0; j0 < steps; j0 += SUB) {
       const int ns = min(SUB, steps - j0);
       // scalar pass: independent per step (conv, SiLU, softplus, gate factor)
+#pragma unroll 4
       for (int j = 0; j < ns; ++j) {
         const float xv = Act<T>::ld(xt + (j0 + j) * GF + tid);
         const float cpre = fmaf(w[0], xm3, fmaf(w[1], xm2, fmaf(w[2], xm1, fmaf(w[3], xv, cb))));
@@ -459,6 +460,7 @@ __global__ void __launch_bounds__(GF) m3_fwd_kernel(FwdArgs a) {
         scs[j * GF] = make_float4(delta, delta * u, Dd * u, gz);
       }
       // state pass: the only loop-carried dependence is h
+#pragma unroll 4
       for (int j = 0; j < ns; ++j) {
         if (FINAL) {
           if (kc == 0) {
@@ -621,6 +623,7 @@ __global__ void __launch_bounds__(GB) m3_bwd_agg_kernel(BwdArgs a) {
     const T* zt = reinterpret_cast<const T*>(base + L.z);
     const T* dgt = reinterpret_cast<const T*>(base + L.dg);
     float2* scs = reinterpret_cast<float2*>(smem + L.sc) + tid;  // thread-private, stride GB
+#pragma unroll 4
     for (int j = 0; j < steps; ++j) {  // scalar pass
       const float zv = Act<T>::ld(zt + j * GB + tid);
       const float dy = Act<T>::ld(dgt + j * GB + tid) * zv * sigmoid_f(zv);
@@ -628,6 +631,7 @@ __global__ void __launch_bounds__(GB) m3_bwd_agg_kernel(BwdArgs a) {
       sdelta += delta;
       scs[j * GB] = make_float2(delta, dy);
     }
+#pragma unroll 4
     for (int j = steps - 1; j >= 0; --j) {  // state pass
       const float2 v = scs[j * GB];
       const float2 dl2 = f2b(v.x);
@@ -851,6 +855,7 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(BwdArgs a) {
         float xm3 = Act<T>::ld(xt + 0 * GB + tid);
         float xm2 = Act<T>::ld(xt + 1 * GB + tid);
         float xm1 = Act<T>::ld(xt + 2 * GB + tid);
+#pragma unroll 2
         for (int j = 0; j < nst; ++j) {
           const float xv = Act<T>::ld(xt + (j + 3) * GB + tid);
           const float cpre = fmaf(w[0], xm3, fmaf(w[1], xm2, fmaf(w[2], xm1, fmaf(w[3], xv, cb))));
@@ -880,6 +885,7 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(BwdArgs a) {
           const int n = lane_of(i);
           h[i] = make_float2(ckt[n * GB + tid], ckt[(n + 1) * GB + tid]);
         }
+#pragma unroll 2
         for (int j = 0; j < nst; ++j) {
           const float4 v0 = s0[j * GB];
           const float2 dl2 = f2b(v0.x);
@@ -971,6 +977,7 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(BwdArgs a) {
       }
 
       // ---- scalar pass: du, d delta, softplus, SiLU and conv backward ----
+#pragma unroll 2
       for (int j = nst - 1; j >= 0; --j) {
         const int t = c * K + j;
         const float4 v0 = s0[j * GB];
