@@ -225,6 +225,35 @@ m3_status m3scan_bwd_state(const m3_dims* dims, m3_dtype act,
                            m3_stream_t stream);
 
 /*
+ * Decode: the forward of a short window -- typically one new token per
+ * sequence (dims->seq_len == 1) -- from the carried state, which is
+ * updated in place: on return ssm_state holds h after the window's last
+ * step and conv_state the conv inputs of the window's last d_conv-1 steps
+ * (the m3_fwd_state layouts; the mamba-rs trainer carries the same two
+ * states between calls, see m3_fwd_state above).  Same arithmetic as
+ * m3scan_fwd_state with both state pointers given and the outputs written
+ * over the inputs; no checkpoints are written, no workspace is used and
+ * time is not split, so the cost grows with seq_len step by step: use it
+ * for decoding and short verification windows, and m3scan_fwd_state for
+ * long prompts.
+ *
+ * dims->d_state may be 16, 32 or 64 here (a_log [d_inner, d_state],
+ * Bm/Cm [batch, seq_len, d_state], ssm_state [batch, d_state, d_inner]);
+ * dims->chunk, segments and accumulate_param_grads are ignored; d_inner
+ * may be any size.  Activation pointers (x, delta_raw, z, Bm, Cm,
+ * conv_state, gated, y_dbg) must be aligned to their element, float32
+ * pointers to 4 bytes.  seq_len == 0 leaves the state unchanged.
+ */
+m3_status m3scan_decode(const m3_dims* dims, m3_dtype act,
+                        const void* x, const void* delta_raw, const void* z,
+                        const void* Bm, const void* Cm,
+                        const float* conv_w, const float* conv_b,
+                        const float* dt_bias, const float* a_log, const float* D,
+                        float* ssm_state, void* conv_state,
+                        void* gated, void* y_dbg,
+                        m3_stream_t stream);
+
+/*
  * Size in bytes of the scratch array the library keeps on every GPU that
  * loads it, for m3scan_bwd_noalloc.
  */

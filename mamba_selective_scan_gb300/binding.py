@@ -29,7 +29,7 @@ STATUS = {
 
 # every symbol include/m3scan.h declares
 EXPORTS = ("m3scan_plan", "m3scan_fwd", "m3scan_bwd", "m3scan_fwd_state", "m3scan_bwd_state",
-           "m3scan_bwd_noalloc", "m3scan_status_string", "m3scan_last_cuda_error",
+           "m3scan_decode", "m3scan_bwd_noalloc", "m3scan_status_string", "m3scan_last_cuda_error",
            "m3scan_version")
 
 # size of the library's own scratch array used by m3scan_bwd_noalloc
@@ -118,6 +118,9 @@ def _lib_handle(build_if_missing: bool = True):
                                              + [_fp] * 5 + [_fp, _vp] + [_vp] * 4 + [_fp] * 2
                                              + [_fp] * 5 + [ctypes.POINTER(M3BwdState)]
                                              + [_vp, ctypes.c_size_t, _vp])
+            lib.m3scan_decode.restype = ctypes.c_int
+            lib.m3scan_decode.argtypes = ([ctypes.POINTER(M3Dims), ctypes.c_int] + [_vp] * 5
+                                          + [_fp] * 5 + [_fp, _vp, _vp, _vp, _vp])
             lib.m3scan_bwd_noalloc.restype = ctypes.c_int
             lib.m3scan_bwd_noalloc.argtypes = ([ctypes.POINTER(M3Dims), ctypes.c_int] + [_vp] * 5
                                                + [_fp] * 5 + [_fp, _vp] + [_vp] * 4
@@ -199,6 +202,14 @@ def raw_bwd_state(dims, act, x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a
                                           d_delta_raw, dz, du_dbg, dB, dC, d_conv_w, d_conv_b,
                                           d_dt_bias, d_a_log, dD, sp, workspace,
                                           int(workspace_bytes), stream)
+
+
+def raw_decode(dims, act, x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D,
+               ssm_state, conv_state, gated, y_dbg, stream) -> int:
+    """Call m3scan_decode with integer addresses; returns the status code."""
+    return _lib_handle().m3scan_decode(ctypes.byref(dims), int(act), x, delta_raw, z, Bm, Cm,
+                                       conv_w, conv_b, dt_bias, a_log, D, ssm_state, conv_state,
+                                       gated, y_dbg, stream)
 
 
 def raw_bwd_noalloc(dims, act, x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D,
@@ -423,3 +434,32 @@ def _bwd(x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D, ckpt, d_gat
     if st != 0:
         raise M3Error(st, "m3scan_bwd" if state is None else "m3scan_bwd_state")
     return o
+
+
+def m3scan_decode(x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D, ssm_state,
+                  conv_state, *, gated=None, y_dbg=None, want_y=False, stream=None):
+    """Forward of a short window (x [B, T, D], typically T = 1) from the
+    carried state, updating ``ssm_state`` [B, N, D] (f32) and ``conv_state``
+    [B, 3, D] (activation dtype) in place.  Returns (gated, y_dbg or None)."""
+    torch = _torch()
+    act = x.dtype
+    dev = x.device
+    for n, t in (("x", x), ("delta_raw", delta_raw), ("z", z), ("B", Bm), ("C", Cm),
+                 ("conv_state", conv_state)):
+        _check(t, n, act, dev)
+    for n, t in (("conv_w", conv_w), ("conv_b", conv_b), ("dt_bias", dt_bias),
+                 ("a_log", a_log), ("D", D), ("ssm_state", ssm_state)):
+        _check(t, n, torch.float32, dev)
+    Bsz, T, Dn = x.shape
+    dims = make_dims(Bsz, T, Dn, d_state=Bm.shape[-1], d_conv=conv_w.shape[-1])
+    if gated is None:
+        gated = torch.empty_like(x)
+    if want_y and y_dbg is None:
+        y_dbg = torch.empty_like(x)
+    st = raw_decode(dims, _act_code(x), _ptr(x), _ptr(delta_raw), _ptr(z), _ptr(Bm), _ptr(Cm),
+                    _ptr(conv_w), _ptr(conv_b), _ptr(dt_bias), _ptr(a_log), _ptr(D),
+                    _ptr(ssm_state), _ptr(conv_state), _ptr(gated), _ptr(y_dbg),
+                    _stream_handle(stream))
+    if st != 0:
+        raise M3Error(st, "m3scan_decode")
+    return gated, y_dbg

@@ -1148,6 +1148,177 @@ __global__ void m3_bwd_tail_kernel(BwdArgs a, int rows, int nfin) {
 }
 
 // ---------------------------------------------------------------------------
+// decode: the forward of a short window (typically one token per sequence)
+// from the carried state, updating that state in place; no checkpoints, no
+// time split.  One thread per channel keeps its N state lanes in registers;
+// B_t and C_t of each step are staged in shared memory for the block.
+// ---------------------------------------------------------------------------
+
+struct DecArgs {
+  int B, T, D;
+  const void *x, *dr, *z, *Bm, *Cm;
+  const float *conv_w, *conv_b, *dt_bias, *a_log, *Dp;
+  float* h;    // [B, N, D] f32, in and out
+  void* conv;  // [B, 3, D] act, in and out
+  void *gated, *y_dbg;
+};
+
+constexpr int GD = 128;  // decode: channels (= threads) per block
+
+// Each channel's N lanes are split over G = N / 16 neighbouring threads of
+// a warp (16 lanes each; y is summed over the G threads with shuffles), so
+// every d_state keeps 16 state lanes per thread.  R batch rows per thread
+// (two when the grid is large enough) keep more loads in flight.  Each step
+// issues all of its global loads before its barrier; B and C of the next
+// step are staged into the other half of a double buffer.
+template <typename T, int N, int R>
+__global__ void __launch_bounds__(GD) m3_decode_kernel(DecArgs a) {
+  constexpr int G = N / 16;       // threads per channel
+  constexpr int CH = GD / G;      // channels per block
+  constexpr int NB = 2 * N * R;   // B and C values of one step
+  __shared__ float sBC[2][R][2 * N];
+  __shared__ float sA[8][GD][2];  // A log2(e) of this thread's lanes
+  const int tid = threadIdx.x;
+  const int q = tid % G;          // this thread's lanes: 16 q .. 16 q + 15
+  const int d = blockIdx.x * CH + tid / G;
+  const bool active = d < a.D;
+  const size_t D = (size_t)a.D;
+  int rb[R];
+  bool ron[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    rb[r] = blockIdx.y * R + r;
+    ron[r] = active && rb[r] < a.B;
+  }
+  auto stage = [&](int t, int buf) {
+    for (int i = tid; i < NB; i += GD) {
+      const int sr = i / (2 * N), sn = i % (2 * N);
+      const int sb = blockIdx.y * R + sr;
+      if (sb < a.B) {
+        const T* src = static_cast<const T*>(sn < N ? a.Bm : a.Cm);
+        sBC[buf][sr][sn] = Act<T>::ld(src + ((size_t)sb * a.T + t) * N + (sn & (N - 1)));
+      }
+    }
+  };
+  if (a.T > 0) stage(0, 0);
+
+  float2 h[R][8];
+  float w[WC] = {0.f, 0.f, 0.f, 0.f};
+  float xm3[R], xm2[R], xm1[R];
+  float cb = 0.f, dtb = 0.f, Dd = 0.f;
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    xm3[r] = xm2[r] = xm1[r] = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) h[r][i] = make_float2(0.f, 0.f);
+  }
+  // every load of the first step is issued before the first use of any
+  float xn[R], dn[R], zn[R];  // x, delta_raw, z of the next step
+  auto prefetch = [&](int t) {
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      xn[r] = dn[r] = zn[r] = 0.f;
+      if (ron[r]) {
+        const size_t i = ((size_t)rb[r] * a.T + t) * D + d;
+        xn[r] = Act<T>::ld(static_cast<const T*>(a.x) + i);
+        dn[r] = Act<T>::ld(static_cast<const T*>(a.dr) + i);
+        zn[r] = Act<T>::ld(static_cast<const T*>(a.z) + i);
+      }
+    }
+  };
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    if (!ron[r]) continue;
+    const float* hp = a.h + ((size_t)rb[r] * N + 16 * q) * D + d;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) h[r][i] = make_float2(hp[(size_t)(2 * i) * D], hp[(size_t)(2 * i + 1) * D]);
+    const T* cp = static_cast<const T*>(a.conv) + (size_t)rb[r] * 3 * D + d;
+    xm3[r] = Act<T>::ld(cp);
+    xm2[r] = Act<T>::ld(cp + D);
+    xm1[r] = Act<T>::ld(cp + 2 * D);
+  }
+  if (a.T > 0) prefetch(0);
+  if (active) {
+#pragma unroll
+    for (int k = 0; k < WC; ++k) w[k] = a.conv_w[(size_t)d * WC + k];
+    cb = a.conv_b[d];
+    dtb = a.dt_bias[d];
+    Dd = a.Dp[d];
+    const float* al = a.a_log + (size_t)d * N + 16 * q;  // 4-byte aligned only
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      sA[i][tid][0] = -expf(al[2 * i]) * LOG2E;
+      sA[i][tid][1] = -expf(al[2 * i + 1]) * LOG2E;
+    }
+  }
+
+#pragma unroll 1
+  for (int t = 0; t < a.T; ++t) {
+    float xv[R], dr[R], zv[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      xv[r] = xn[r];
+      dr[r] = dn[r];
+      zv[r] = zn[r];
+    }
+    if (t + 1 < a.T) {
+      prefetch(t + 1);
+      stage(t + 1, (t + 1) & 1);
+    }
+    __syncthreads();  // step t's B and C (and, at t = 0, A) are visible
+    const int buf = t & 1;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const float cpre = fmaf(w[0], xm3[r], fmaf(w[1], xm2[r], fmaf(w[2], xm1[r], fmaf(w[3], xv[r], cb))));
+      xm3[r] = xm2[r];
+      xm2[r] = xm1[r];
+      xm1[r] = xv[r];
+      const float u = cpre * sigmoid_f(cpre);
+      const float delta = softplus_f(dr[r] + dtb);
+      const float2 dl2 = f2b(delta);
+      const float2 du2 = f2b(delta * u);
+      float2 y2 = make_float2(0.f, 0.f);
+      const float* bc = sBC[buf][r] + 16 * q;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float2 bb = *reinterpret_cast<const float2*>(bc + 2 * k);
+        const float2 cc = *reinterpret_cast<const float2*>(bc + N + 2 * k);
+        const float2 a2 = *reinterpret_cast<const float2*>(sA[k][tid]);
+        h[r][k] = __ffma2_rn(ex2x2(__fmul2_rn(dl2, a2)), h[r][k], __fmul2_rn(du2, bb));
+        y2 = __ffma2_rn(cc, h[r][k], y2);
+      }
+      float ys = y2.x + y2.y;
+#pragma unroll
+      for (int o = 1; o < G; o <<= 1) ys += __shfl_xor_sync(0xffffffffu, ys, o);
+      if (ron[r] && q == 0) {
+        const size_t i = ((size_t)rb[r] * a.T + t) * D + d;
+        const float y = ys + Dd * u;
+        Act<T>::st(static_cast<T*>(a.gated) + i, y * (zv[r] * sigmoid_f(zv[r])));
+        if (a.y_dbg) Act<T>::st(static_cast<T*>(a.y_dbg) + i, y);
+      }
+    }
+    __syncthreads();  // step t's buffer is free for step t + 2
+  }
+  if (a.T == 0) return;
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    if (!ron[r]) continue;
+    float* hp = a.h + ((size_t)rb[r] * N + 16 * q) * D + d;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      hp[(size_t)(2 * i) * D] = h[r][i].x;
+      hp[(size_t)(2 * i + 1) * D] = h[r][i].y;
+    }
+    if (q == 0) {
+      T* cp = static_cast<T*>(a.conv) + (size_t)rb[r] * 3 * D + d;
+      Act<T>::st(cp, xm3[r]);
+      Act<T>::st(cp + D, xm2[r]);
+      Act<T>::st(cp + 2 * D, xm1[r]);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
 
@@ -1773,6 +1944,81 @@ m3_status m3scan_bwd_noalloc(const m3_dims* dims, m3_dtype act, const void* x,
   return m3scan_bwd(dims, act, x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D, ckpt,
                     d_gated, d_x, d_delta_raw, dz, du_dbg, dB, dC, d_conv_w, d_conv_b, d_dt_bias,
                     d_a_log, dD, ws, (size_t)M3SCAN_NOALLOC_SCRATCH_BYTES, stream);
+}
+
+}  // extern "C"
+
+namespace {
+
+template <typename T, int N, int R>
+cudaError_t launch_decode_r(const DecArgs& a, cudaStream_t st) {
+  constexpr int CH = GD / (N / 16);
+  m3_decode_kernel<T, N, R>
+      <<<dim3((unsigned)((a.D + CH - 1) / CH), (unsigned)((a.B + R - 1) / R)), GD, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+// Two batch rows per thread when there are still enough blocks to give
+// every SM several (a small batch keeps one row per thread, for more blocks).
+template <typename T, int N>
+cudaError_t launch_decode(const DecArgs& a, cudaStream_t st, int sms) {
+  constexpr int CH = GD / (N / 16);
+  const int64_t blocks2 = (int64_t)((a.D + CH - 1) / CH) * ((a.B + 1) / 2);
+  if (blocks2 >= 4 * (int64_t)sms) return launch_decode_r<T, N, 2>(a, st);
+  return launch_decode_r<T, N, 1>(a, st);
+}
+
+template <typename T>
+cudaError_t launch_decode_n(int n, const DecArgs& a, cudaStream_t st, int sms) {
+  if (n == 16) return launch_decode<T, 16>(a, st, sms);
+  if (n == 32) return launch_decode<T, 32>(a, st, sms);
+  return launch_decode<T, 64>(a, st, sms);
+}
+
+}  // namespace
+
+extern "C" {
+
+// The forward of a short window from the carried state, updating the state
+// in place (no checkpoints, no workspace).
+m3_status m3scan_decode(const m3_dims* dims, m3_dtype act, const void* x, const void* delta_raw,
+                        const void* z, const void* Bm, const void* Cm, const float* conv_w,
+                        const float* conv_b, const float* dt_bias, const float* a_log,
+                        const float* D, float* ssm_state, void* conv_state, void* gated,
+                        void* y_dbg, m3_stream_t stream) {
+  if (!dims) return M3_ERR_NULL;
+  if (act != M3_F32 && act != M3_BF16) return M3_ERR_UNSUPPORTED;
+  if (dims->batch < 0 || dims->seq_len < 0 || dims->d_inner < 0) return M3_ERR_DIMS;
+  if ((dims->d_state != 16 && dims->d_state != 32 && dims->d_state != 64) || dims->d_conv != WC)
+    return M3_ERR_UNSUPPORTED;
+  if (dims->batch > 65535 || dims->seq_len > ((int64_t)1 << 30) || dims->d_inner > ((int64_t)1 << 24))
+    return M3_ERR_DIMS;
+  if (dims->batch * dims->seq_len * dims->d_inner == 0) return M3_OK;
+  if (!x || !delta_raw || !z || !Bm || !Cm || !conv_w || !conv_b || !dt_bias || !a_log || !D ||
+      !ssm_state || !conv_state || !gated)
+    return M3_ERR_NULL;
+  const size_t es = act == M3_BF16 ? 2 : 4;
+  const void* act_ptrs[] = {x, delta_raw, z, Bm, Cm, conv_state, gated, y_dbg};
+  for (const void* q : act_ptrs)
+    if (!aligned(q, es)) return M3_ERR_ALIGN;
+  const void* f_ptrs[] = {conv_w, conv_b, dt_bias, a_log, D, ssm_state};
+  for (const void* q : f_ptrs)
+    if (!aligned(q, 4)) return M3_ERR_ALIGN;
+  DecArgs a{};
+  a.B = (int)dims->batch;
+  a.T = (int)dims->seq_len;
+  a.D = (int)dims->d_inner;
+  a.x = x; a.dr = delta_raw; a.z = z; a.Bm = Bm; a.Cm = Cm;
+  a.conv_w = conv_w; a.conv_b = conv_b; a.dt_bias = dt_bias; a.a_log = a_log; a.Dp = D;
+  a.h = ssm_state; a.conv = conv_state; a.gated = gated; a.y_dbg = y_dbg;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int n = (int)dims->d_state;
+  int sms = 0, of = 0, ob = 0;
+  if (note(device_info(KDEF, act == M3_BF16 ? 1 : 0, &sms, &of, &ob)) != cudaSuccess)
+    return M3_ERR_CUDA;
+  const cudaError_t e = act == M3_BF16 ? launch_decode_n<__nv_bfloat16>(n, a, s, sms)
+                                       : launch_decode_n<float>(n, a, s, sms);
+  return note(e) == cudaSuccess ? M3_OK : M3_ERR_CUDA;
 }
 
 }  // extern "C"

@@ -212,3 +212,29 @@ def test_state_structs_match_the_header_layout():
         body = re.search(r"typedef struct \{([^{}]*)\}\s*" + struct + ";", src).group(1)
         names = re.findall(r"(\w+);", body)
         assert names == [f for f, _ in cls._fields_], struct
+
+
+def _decode(dims, act=binding.M3_BF16, **over):
+    a = dict(x=A, delta_raw=A, z=A, Bm=A, Cm=A, conv_w=A, conv_b=A, dt_bias=A, a_log=A, D=A,
+             ssm_state=A, conv_state=A, gated=A, y_dbg=None, stream=None)
+    a.update(over)
+    return binding.STATUS[binding.raw_decode(dims, act, *a.values())]
+
+
+def test_decode_validates_before_any_launch(lib):
+    for n in (16, 32, 64):
+        assert _decode(binding.make_dims(2, 1, 64, d_state=n), x=None) == "M3_ERR_NULL"
+    assert _decode(binding.make_dims(2, 1, 64, d_state=24)) == "M3_ERR_UNSUPPORTED"
+    assert _decode(binding.make_dims(2, 1, 64, d_state=128)) == "M3_ERR_UNSUPPORTED"
+    assert _decode(binding.make_dims(2, 1, 64, d_conv=3)) == "M3_ERR_UNSUPPORTED"
+    assert _decode(binding.make_dims(2, 1, 64), act=7) == "M3_ERR_UNSUPPORTED"
+    assert _decode(binding.make_dims(-1, 1, 64)) == "M3_ERR_DIMS"
+    assert _decode(binding.make_dims(2, 1, 64), ssm_state=None) == "M3_ERR_NULL"
+    assert _decode(binding.make_dims(2, 1, 64), conv_state=None) == "M3_ERR_NULL"
+    assert _decode(binding.make_dims(2, 1, 64), ssm_state=A + 2) == "M3_ERR_ALIGN"
+    assert _decode(binding.make_dims(2, 1, 64), x=A + 1) == "M3_ERR_ALIGN"
+    assert _decode(binding.make_dims(2, 1, 64), x=A + 2, act=binding.M3_F32) == "M3_ERR_ALIGN"
+    # element alignment is enough for bf16; any d_inner is accepted
+    assert _decode(binding.make_dims(2, 0, 60), x=A + 2) == "M3_OK"
+    # nothing to do: no pointer is needed
+    assert _decode(binding.make_dims(2, 0, 64), x=None, ssm_state=None) == "M3_OK"

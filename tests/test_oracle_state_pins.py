@@ -252,3 +252,29 @@ def test_checkpoint_zero_is_the_carried_state():
     a, st = _case(1, 10, 4, N=4, seed=70)
     f = oracle.forward(a, ckpt_chunk=4, ssm_state=st["ssm_state"], conv_state=st["conv_state"])
     assert np.array_equal(f["ckpt"][:, 0], st["ssm_state"])
+
+
+@pytest.mark.parametrize("N", [32, 64])
+def test_one_step_windows_chain_for_wider_states(N):
+    """d_state 32 and 64 (the decode path): stepping one token at a time from
+    the carried state equals one window, and the state after it is the
+    brute-force sum h_{T-1} = exp(A S_{T-1}) h_{-1}
+    + sum_s exp(A (S_{T-1} - S_s)) delta_s B_s u_s."""
+    a, st = _case(1, 6, 3, N=N, seed=80 + N)
+    full = oracle.forward(a, ssm_state=st["ssm_state"], conv_state=st["conv_state"])
+    h, c = st["ssm_state"], st["conv_state"]
+    ys = []
+    for t in range(6):
+        f = oracle.forward(_slice_t(a, t, t + 1), ssm_state=h, conv_state=c)
+        ys.append(f["gated"])
+        h, c = f["ssm_state_out"], f["conv_state_out"]
+    assert np.allclose(np.concatenate(ys, axis=1), full["gated"], rtol=1e-12, atol=1e-13)
+    for d in range(3):
+        u, delta = full["u"][0, :, d], full["delta"][0, :, d]
+        S = np.cumsum(delta)
+        A = -np.exp(a["a_log"][d])
+        want = np.exp(A * S[-1]) * st["ssm_state"][0, :, d]
+        for s in range(6):
+            want = want + np.exp(A * (S[-1] - S[s])) * delta[s] * a["B"][0, s] * u[s]
+        assert np.allclose(full["ssm_state_out"][0, :, d], want, rtol=1e-11, atol=1e-12)
+        assert np.allclose(h[0, :, d], want, rtol=1e-11, atol=1e-12)
