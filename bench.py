@@ -522,6 +522,64 @@ def extras(torch, binding, device, args, flush, stream):
         torch.cuda.empty_cache()
     if not args.no_stack:
         out["m2p8b_stack24"] = stack24(torch, binding, device, args, stream)
+    out["decode"] = decode_extras(torch, binding, device, flush)
+    return out
+
+
+# one-token decode (m3scan_decode): batch 64 sequences of the Mamba-2.8B-like
+# layer (d_inner 5120), bf16 activations, d_state 16, 32 and 64
+DECODE_CONFIGS = ((64, 5120, 16), (64, 5120, 32), (64, 5120, 64))
+
+
+def decode_bytes(B, D, N, es):
+    """Bytes one decode step must move: the f32 state read and written, the
+    conv state read and written, x, delta_raw, z read and gated written, B and
+    C, and the per-channel parameters once."""
+    return B * D * (2 * 4 * N + 2 * 3 * es + 4 * es) + 2 * B * N * es + D * (4 * N + 4 * 4 + 3 * 4)
+
+
+def decode_extras(torch, binding, device, flush, steps=20):
+    out = {}
+    for (B, D, N) in DECODE_CONFIGS:
+        g = torch.Generator(device=device)
+        g.manual_seed(1000 + N)
+        bf = torch.bfloat16
+        rn = lambda *shape, dt=bf: torch.randn(*shape, device=device, generator=g).to(dt)
+        x, z = rn(B, 1, D), rn(B, 1, D)
+        dr = (0.5 * torch.randn(B, 1, D, device=device, generator=g)).to(bf)
+        Bm, Cm = rn(B, 1, N), rn(B, 1, N)
+        cw = torch.rand(D, 4, device=device, generator=g) - 0.5
+        cb = torch.zeros(D, device=device)
+        u = torch.rand(D, device=device, generator=g) * 0.099 + 0.001
+        dtb = torch.log(torch.expm1(u))
+        alog = torch.log(torch.arange(1, N + 1, device=device, dtype=torch.float32)).repeat(D, 1)
+        Dp = torch.ones(D, device=device)
+        h = rn(B, N, D, dt=torch.float32)
+        c = rn(B, 3, D)
+        gated = torch.empty_like(x)
+        dims = binding.make_dims(B, 1, D, d_state=N)
+        s = torch.cuda.current_stream()
+        alog = alog.contiguous()
+        args = (dims, binding.M3_BF16, x.data_ptr(), dr.data_ptr(), z.data_ptr(), Bm.data_ptr(),
+                Cm.data_ptr(), cw.data_ptr(), cb.data_ptr(), dtb.data_ptr(), alog.data_ptr(),
+                Dp.data_ptr(), h.data_ptr(), c.data_ptr(), gated.data_ptr(), None, s.cuda_stream)
+        for _ in range(3):
+            assert binding.raw_decode(*args) == 0
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        for e0, e1 in ev:
+            flush.zero_()
+            e0.record(s)
+            binding.raw_decode(*args)
+            e1.record(s)
+        torch.cuda.synchronize()
+        ms = sorted(e0.elapsed_time(e1) for e0, e1 in ev)[steps // 2]
+        byt = decode_bytes(B, D, N, 2)
+        peak, kind = measured_peaks()
+        gbs = byt / (ms * 1e-3) / 1e9
+        out[f"b{B}_d{D}_n{N}"] = {"us_per_token_step": round(ms * 1e3, 2), "gbs": round(gbs, 1),
+                                  "frac_of_hbm": round(gbs / peak, 3), "hbm_peak_kind": kind,
+                                  "bytes": int(byt)}
     return out
 
 
