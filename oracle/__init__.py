@@ -56,7 +56,7 @@ def _load():
                                         + [_i64] + [_dp] * 4)
             lib.m3o_backward.restype = ctypes.c_int
             lib.m3o_backward.argtypes = ([_i64] * 5 + [_dp] * 11 + [_u8p, _i64]
-                                         + [_dp] * 11 + [_dp] * 6)
+                                         + [_dp] * 11 + [_dp] * 7)
             _lib = lib
     return _lib
 
@@ -146,10 +146,14 @@ STATE_GRAD_NAMES = ("d_ssm_state", "d_conv_state")
 
 
 def backward(inp, d_gated=None, chan_mask=None, chunk: int = 0, ssm_state=None,
-             conv_state=None, d_ssm_state_out=None, d_conv_state_out=None):
+             conv_state=None, d_ssm_state_out=None, d_conv_state_out=None, d_u_extra=None):
     """Oracle backward of
     L = sum(gated * d_gated) + sum(ssm_state_out * d_ssm_state_out)
-        + sum(conv_state_out * d_conv_state_out).
+        + sum(conv_state_out * d_conv_state_out) + sum(u * d_u_extra).
+
+    ``d_u_extra`` [B,T,D] is a gradient reaching u from outside the layer
+    core (the x_proj path); ``du`` stays dL/du through the D skip and the
+    recurrence only.
 
     ``chunk`` = 0 keeps every state (sequential); ``chunk`` > 0 recomputes
     states chunk by chunk from chunk-start states.  The carried-state
@@ -161,6 +165,7 @@ def backward(inp, d_gated=None, chan_mask=None, chunk: int = 0, ssm_state=None,
     g = _c64(inp["d_gated"] if d_gated is None else d_gated)
     h0, c0 = _opt64(ssm_state), _opt64(conv_state)
     gh, gc = _opt64(d_ssm_state_out), _opt64(d_conv_state_out)
+    gu = _opt64(d_u_extra)
     out = {k: np.zeros((Bsz, T, D)) for k in ("d_x", "d_delta_raw", "dz", "du")}
     out["dB"] = np.zeros((Bsz, T, N))
     out["dC"] = np.zeros((Bsz, T, N))
@@ -178,14 +183,14 @@ def backward(inp, d_gated=None, chan_mask=None, chunk: int = 0, ssm_state=None,
                           _ptr(a["a_log"]), _ptr(a["D"]), _ptr(g), mp, int(chunk),
                           *[_ptr(out[k]) for k in GRAD_NAMES],
                           _ptr(h0), _ptr(c0), _ptr(gh), _ptr(gc),
-                          _ptr(out["d_ssm_state"]), _ptr(out["d_conv_state"]))
+                          _ptr(out["d_ssm_state"]), _ptr(out["d_conv_state"]), _ptr(gu))
     if rc != 0:
         raise MemoryError("oracle backward: allocation failed")
     return out
 
 
 def loss(inp, d_gated=None, ssm_state=None, conv_state=None, d_ssm_state_out=None,
-         d_conv_state_out=None) -> float:
+         d_conv_state_out=None, d_u_extra=None) -> float:
     """The scalar whose gradient ``backward`` gives (see ``backward``)."""
     g = _c64(inp["d_gated"] if d_gated is None else d_gated)
     f = forward(inp, ssm_state=ssm_state, conv_state=conv_state)
@@ -194,6 +199,8 @@ def loss(inp, d_gated=None, ssm_state=None, conv_state=None, d_ssm_state_out=Non
         L += float(np.sum(f["ssm_state_out"] * _c64(d_ssm_state_out)))
     if d_conv_state_out is not None:
         L += float(np.sum(f["conv_state_out"] * _c64(d_conv_state_out)))
+    if d_u_extra is not None:
+        L += float(np.sum(f["u"] * _c64(d_u_extra)))
     return L
 
 

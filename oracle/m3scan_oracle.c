@@ -210,6 +210,13 @@ int m3o_forward(int64_t B, int64_t T, int64_t D, int64_t N, int64_t W,
  *        + sum conv_state_out * d_conv_state_out,
  * (d_ssm_state_out, d_conv_state_out nullable = zero), and d_ssm_state,
  * d_conv_state (nullable) receive dL/d ssm_state and dL/d conv_state.
+ *
+ * d_u_extra ([B,T,D], nullable = zero) is a gradient reaching u from
+ * outside the layer core -- in the mamba-rs backward the x_proj GEMM's
+ * input gradient, which the page adds into d_u before the SiLU and conv1d
+ * backward -- so the loss gains sum u * d_u_extra.  It changes d_x,
+ * d_conv_w, d_conv_b and d_conv_state; du_out stays dL/du through the D
+ * skip and the recurrence only.
  */
 int m3o_backward(int64_t B, int64_t T, int64_t D, int64_t N, int64_t W,
                  const double* x, const double* delta_raw, const double* z,
@@ -222,7 +229,7 @@ int m3o_backward(int64_t B, int64_t T, int64_t D, int64_t N, int64_t W,
                  double* d_dt_bias, double* d_a_log, double* dD,
                  const double* ssm_state, const double* conv_state,
                  const double* d_ssm_state_out, const double* d_conv_state_out,
-                 double* d_ssm_state, double* d_conv_state) {
+                 double* d_ssm_state, double* d_conv_state, const double* d_u_extra) {
     int64_t Tm = T > 0 ? T : 1;
     int64_t span = (K > 0) ? K : Tm;         /* states held at once */
     int64_t nc = (K > 0) ? (T + K - 1) / K : 1;
@@ -312,8 +319,9 @@ int m3o_backward(int64_t B, int64_t T, int64_t D, int64_t N, int64_t W,
                     double ddr = ddelta * sigmoid(delta_raw[i] + dt_bias[d]);
                     d_delta_raw[i] = ddr;
                     ddtb_acc += ddr;
-                    /* u = silu(c) */
-                    dc[t] = du * silu_grad(c[t]);
+                    /* u = silu(c); u also feeds the x_proj path */
+                    double du_total = du + (d_u_extra ? d_u_extra[i] : 0.0);
+                    dc[t] = du_total * silu_grad(c[t]);
                 }
             }
 
