@@ -84,6 +84,16 @@ typedef struct {
     /* 1: param grads are added to the output buffers; 0: overwritten. */
     int32_t accumulate_param_grads;
     int32_t reserved;
+    /* Row strides, in elements, between consecutive (batch, step) rows of
+       Bm and Cm, and of dB and dC; 0 = d_state (dense).  A stride > d_state
+       lets Bm/Cm be column slices of the x_proj output [batch, seq_len,
+       dt_rank + 2 d_state] and dB/dC slices of its gradient, with no copy
+       (the x_proj step F4b of forward_mixed.rs splits one GEMM output into
+       dt_low, B and C).  bc_stride times the activation size must be a
+       multiple of 16 bytes (M3_ERR_ALIGN otherwise).  Only the d_state
+       columns of each row are read or written. */
+    int64_t bc_stride;
+    int64_t dbc_stride;
 } m3_dims;
 
 typedef struct {
@@ -223,6 +233,54 @@ m3_status m3scan_bwd_state(const m3_dims* dims, m3_dtype act,
                            const m3_bwd_state* state,
                            void* workspace, size_t workspace_bytes,
                            m3_stream_t stream);
+
+/*
+ * Two-phase backward, for a layer whose u also feeds the x_proj GEMM.  In
+ * the mamba-rs backward (forward_mixed.rs 0.3.1, GpuMambaMixedTrainScratch)
+ * the x_proj input gradient is added into d_u before the SiLU and conv1d
+ * backward; that gradient needs dB, dC and d_delta_raw (through dt_proj)
+ * of this same backward, so the layer core's backward runs in two calls
+ * with the caller's GEMMs between them:
+ *
+ *   1. m3scan_bwd_scan: everything of m3scan_bwd_state up to u -- dz,
+ *      d_delta_raw, dB, dC, d_dt_bias, d_a_log, dD, d_ssm_state -- and du
+ *      (dL/du through the D skip and the recurrence, activation dtype,
+ *      required).  d_x, d_conv_w, d_conv_b and d_conv_state are not
+ *      touched.  From the state struct it reads conv_state and
+ *      d_ssm_state_out and writes d_ssm_state.
+ *   2. the caller forms d_x_dbl = [d_delta_raw W_dt, dB, dC] and
+ *      du_extra = d_x_dbl W_xproj (its GEMMs);
+ *   3. m3scan_conv_bwd: dc = (du + du_extra) silu'(c) with c recomputed
+ *      from x (and conv_state), then d_x, d_conv_w, d_conv_b (written or
+ *      added per dims->accumulate_param_grads) and, from the state struct,
+ *      d_conv_state (using conv_state and d_conv_state_out).  du_extra may
+ *      be NULL (zero).
+ *
+ * With du_extra = NULL the two calls give the results of m3scan_bwd_state.
+ * Both take the same dims (the plan's workspace_bytes covers either call;
+ * one workspace may serve both, in stream order).  Pointer rules as in
+ * m3scan_bwd; state may be NULL.
+ */
+m3_status m3scan_bwd_scan(const m3_dims* dims, m3_dtype act,
+                          const void* x, const void* delta_raw, const void* z,
+                          const void* Bm, const void* Cm,
+                          const float* conv_w, const float* conv_b,
+                          const float* dt_bias, const float* a_log, const float* D,
+                          const float* ckpt, const void* d_gated,
+                          void* du, void* d_delta_raw, void* dz,
+                          float* dB, float* dC,
+                          float* d_dt_bias, float* d_a_log, float* dD,
+                          const m3_bwd_state* state,
+                          void* workspace, size_t workspace_bytes,
+                          m3_stream_t stream);
+
+m3_status m3scan_conv_bwd(const m3_dims* dims, m3_dtype act,
+                          const void* x, const float* conv_w, const float* conv_b,
+                          const void* du, const void* du_extra,
+                          void* d_x, float* d_conv_w, float* d_conv_b,
+                          const m3_bwd_state* state,
+                          void* workspace, size_t workspace_bytes,
+                          m3_stream_t stream);
 
 /*
  * Decode: the forward of a short window -- typically one new token per

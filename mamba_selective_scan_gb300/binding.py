@@ -29,7 +29,7 @@ STATUS = {
 
 # every symbol include/m3scan.h declares
 EXPORTS = ("m3scan_plan", "m3scan_fwd", "m3scan_bwd", "m3scan_fwd_state", "m3scan_bwd_state",
-           "m3scan_decode", "m3scan_bwd_noalloc", "m3scan_status_string", "m3scan_last_cuda_error",
+           "m3scan_bwd_scan", "m3scan_conv_bwd", "m3scan_decode", "m3scan_bwd_noalloc", "m3scan_status_string", "m3scan_last_cuda_error",
            "m3scan_version")
 
 # size of the library's own scratch array used by m3scan_bwd_noalloc
@@ -51,7 +51,8 @@ class M3Dims(ctypes.Structure):
                 ("d_conv", ctypes.c_int64), ("chunk", ctypes.c_int64),
                 ("segments", ctypes.c_int64),
                 ("accumulate_param_grads", ctypes.c_int32),
-                ("reserved", ctypes.c_int32)]
+                ("reserved", ctypes.c_int32),
+                ("bc_stride", ctypes.c_int64), ("dbc_stride", ctypes.c_int64)]
 
 
 class M3Plan(ctypes.Structure):
@@ -118,6 +119,16 @@ def _lib_handle(build_if_missing: bool = True):
                                              + [_fp] * 5 + [_fp, _vp] + [_vp] * 4 + [_fp] * 2
                                              + [_fp] * 5 + [ctypes.POINTER(M3BwdState)]
                                              + [_vp, ctypes.c_size_t, _vp])
+            lib.m3scan_bwd_scan.restype = ctypes.c_int
+            lib.m3scan_bwd_scan.argtypes = ([ctypes.POINTER(M3Dims), ctypes.c_int] + [_vp] * 5
+                                            + [_fp] * 5 + [_fp, _vp] + [_vp] * 3 + [_fp] * 5
+                                            + [ctypes.POINTER(M3BwdState)]
+                                            + [_vp, ctypes.c_size_t, _vp])
+            lib.m3scan_conv_bwd.restype = ctypes.c_int
+            lib.m3scan_conv_bwd.argtypes = ([ctypes.POINTER(M3Dims), ctypes.c_int, _vp, _fp, _fp,
+                                             _vp, _vp, _vp, _fp, _fp,
+                                             ctypes.POINTER(M3BwdState),
+                                             _vp, ctypes.c_size_t, _vp])
             lib.m3scan_decode.restype = ctypes.c_int
             lib.m3scan_decode.argtypes = ([ctypes.POINTER(M3Dims), ctypes.c_int] + [_vp] * 5
                                           + [_fp] * 5 + [_fp, _vp, _vp, _vp, _vp])
@@ -141,9 +152,10 @@ def load():
 
 
 def make_dims(batch, seq_len, d_inner, d_state=16, d_conv=4, chunk=0, segments=0,
-              accumulate_param_grads=False) -> M3Dims:
+              accumulate_param_grads=False, bc_stride=0, dbc_stride=0) -> M3Dims:
     return M3Dims(int(batch), int(seq_len), int(d_inner), int(d_state), int(d_conv),
-                  int(chunk), int(segments), int(bool(accumulate_param_grads)), 0)
+                  int(chunk), int(segments), int(bool(accumulate_param_grads)), 0,
+                  int(bc_stride), int(dbc_stride))
 
 
 def m3scan_plan(dims: M3Dims, act: int) -> M3Plan:
@@ -202,6 +214,28 @@ def raw_bwd_state(dims, act, x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a
                                           d_delta_raw, dz, du_dbg, dB, dC, d_conv_w, d_conv_b,
                                           d_dt_bias, d_a_log, dD, sp, workspace,
                                           int(workspace_bytes), stream)
+
+
+def raw_bwd_scan(dims, act, x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D, ckpt,
+                 d_gated, du, d_delta_raw, dz, dB, dC, d_dt_bias, d_a_log, dD, state, workspace,
+                 workspace_bytes, stream) -> int:
+    """Call m3scan_bwd_scan (``state`` an M3BwdState or None); returns the
+    status code."""
+    sp = ctypes.byref(state) if state is not None else None
+    return _lib_handle().m3scan_bwd_scan(ctypes.byref(dims), int(act), x, delta_raw, z, Bm, Cm,
+                                         conv_w, conv_b, dt_bias, a_log, D, ckpt, d_gated, du,
+                                         d_delta_raw, dz, dB, dC, d_dt_bias, d_a_log, dD, sp,
+                                         workspace, int(workspace_bytes), stream)
+
+
+def raw_conv_bwd(dims, act, x, conv_w, conv_b, du, du_extra, d_x, d_conv_w, d_conv_b, state,
+                 workspace, workspace_bytes, stream) -> int:
+    """Call m3scan_conv_bwd (``state`` an M3BwdState or None); returns the
+    status code."""
+    sp = ctypes.byref(state) if state is not None else None
+    return _lib_handle().m3scan_conv_bwd(ctypes.byref(dims), int(act), x, conv_w, conv_b, du,
+                                         du_extra, d_x, d_conv_w, d_conv_b, sp, workspace,
+                                         int(workspace_bytes), stream)
 
 
 def raw_decode(dims, act, x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D,
@@ -463,3 +497,55 @@ def m3scan_decode(x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D, ss
     if st != 0:
         raise M3Error(st, "m3scan_decode")
     return gated, y_dbg
+
+
+def m3scan_bwd_two_phase(x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D, ckpt,
+                         d_gated, du_extra_fn=None, *, conv_state=None, d_ssm_state_out=None,
+                         d_conv_state_out=None, chunk=0, segments=0, bc_stride=0, dbc_stride=0,
+                         dB=None, dC=None, accumulate_param_grads=False, stream=None):
+    """The two-phase backward: m3scan_bwd_scan, then ``du_extra_fn(grads)``
+    (the caller's x_proj/dt_proj GEMMs, given the scan's gradients; may
+    return None), then m3scan_conv_bwd.  ``Bm``/``Cm`` may be column views
+    of one x_proj output (``bc_stride`` its row length), ``dB``/``dC``
+    column views of its gradient (``dbc_stride``).  Returns the gradient
+    dict (with ``du`` and, when states are involved, ``d_ssm_state`` and
+    ``d_conv_state``)."""
+    torch = _torch()
+    act = x.dtype
+    dev = x.device
+    Bsz, T, Dn = x.shape
+    N, W = 16, conv_w.shape[-1]
+    dims = make_dims(Bsz, T, Dn, d_state=N, d_conv=W, chunk=chunk, segments=segments,
+                     accumulate_param_grads=accumulate_param_grads, bc_stride=bc_stride,
+                     dbc_stride=dbc_stride)
+    code = _act_code(x)
+    pl = m3scan_plan(dims, code)
+    ws = Workspace(pl.workspace_bytes, dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    o = {"du": torch.empty_like(x), "d_delta_raw": torch.empty_like(x), "dz": torch.empty_like(x),
+         "dB": dB if dB is not None else torch.empty((Bsz, T, N), **f32),
+         "dC": dC if dC is not None else torch.empty((Bsz, T, N), **f32),
+         "d_dt_bias": torch.zeros((Dn,), **f32), "d_a_log": torch.zeros((Dn, N), **f32),
+         "dD": torch.zeros((Dn,), **f32), "d_x": torch.empty_like(x),
+         "d_conv_w": torch.zeros((Dn, W), **f32), "d_conv_b": torch.zeros((Dn,), **f32),
+         "d_ssm_state": torch.empty((Bsz, N, Dn), **f32),
+         "d_conv_state": torch.empty((Bsz, W - 1, Dn), dtype=act, device=dev)}
+    st = M3BwdState(_ptr(conv_state), _ptr(d_ssm_state_out), _ptr(d_conv_state_out),
+                    _ptr(o["d_ssm_state"]), _ptr(o["d_conv_state"]))
+    h = _stream_handle(stream)
+    r = raw_bwd_scan(dims, code, _ptr(x), _ptr(delta_raw), _ptr(z), _ptr(Bm), _ptr(Cm),
+                     _ptr(conv_w), _ptr(conv_b), _ptr(dt_bias), _ptr(a_log), _ptr(D), _ptr(ckpt),
+                     _ptr(d_gated), _ptr(o["du"]), _ptr(o["d_delta_raw"]), _ptr(o["dz"]),
+                     o["dB"].data_ptr(), o["dC"].data_ptr(), _ptr(o["d_dt_bias"]),
+                     _ptr(o["d_a_log"]), _ptr(o["dD"]), st, ws.ptr, ws.nbytes, h)
+    if r != 0:
+        raise M3Error(r, "m3scan_bwd_scan")
+    du_extra = du_extra_fn(o) if du_extra_fn is not None else None
+    if du_extra is not None:
+        _check(du_extra, "du_extra", act, dev)
+    r = raw_conv_bwd(dims, code, _ptr(x), _ptr(conv_w), _ptr(conv_b), _ptr(o["du"]),
+                     _ptr(du_extra), _ptr(o["d_x"]), _ptr(o["d_conv_w"]), _ptr(o["d_conv_b"]),
+                     st, ws.ptr, ws.nbytes, h)
+    if r != 0:
+        raise M3Error(r, "m3scan_conv_bwd")
+    return o

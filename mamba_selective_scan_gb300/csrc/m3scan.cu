@@ -180,11 +180,12 @@ __device__ __forceinline__ void stage_rows(T* dst, const T* src, int b, int t_fi
   }
 }
 
-// Stage rows [t_first, t_first + rows) of a [B, T_, 16] tensor into
-// dst[rows][16]; rows outside [0, t_limit) read as zero.
+// Stage rows [t_first, t_first + rows) of a [B, T_, 16] tensor whose rows
+// are ld elements apart into dst[rows][16]; rows outside [0, t_limit) read
+// as zero.
 template <typename T, int NT>
 __device__ __forceinline__ void stage_bc(T* dst, const T* src, int b, int t_first, int rows,
-                                         int T_, int t_limit, int tid) {
+                                         int T_, int t_limit, int ld, int tid) {
   constexpr int EPC = 16 / sizeof(T);
   constexpr int CPR = NS / EPC;
   const int n = rows * CPR;
@@ -192,7 +193,7 @@ __device__ __forceinline__ void stage_bc(T* dst, const T* src, int b, int t_firs
     const int r = i / CPR, cc = i - r * CPR;
     const int t = t_first + r;
     const bool ok = (t >= 0) && (t < t_limit);
-    const T* g = ok ? src + ((size_t)b * T_ + t) * NS + cc * EPC : src;
+    const T* g = ok ? src + ((size_t)b * T_ + t) * ld + cc * EPC : src;
     cp_async16(dst + r * NS + cc * EPC, g, ok);
   }
 }
@@ -203,6 +204,7 @@ __device__ __forceinline__ void stage_bc(T* dst, const T* src, int b, int t_firs
 
 struct Geo {
   int B, T, D, K, nc, S, m;  // S segments of m chunks (the last may be short)
+  int ldbc, lddbc;           // row strides (elements) of Bm/Cm and of dB/dC
 };
 
 __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -346,10 +348,10 @@ __global__ void __launch_bounds__(GF) m3_fwd_kernel(FwdArgs a) {
     unsigned char* base = smem + (size_t)buf * L.tile;
     stage_rows<T, GF, GF>(reinterpret_cast<T*>(base + L.x), xg, b, t0, TT, g.T, t_end, g.D, d0, tid);
     stage_rows<T, GF, GF>(reinterpret_cast<T*>(base + L.dr), drg, b, t0, TT, g.T, t_end, g.D, d0, tid);
-    stage_bc<T, GF>(reinterpret_cast<T*>(base + L.Bt), Bg, b, t0, TT, g.T, t_end, tid);
+    stage_bc<T, GF>(reinterpret_cast<T*>(base + L.Bt), Bg, b, t0, TT, g.T, t_end, g.ldbc, tid);
     if (FINAL) {
       stage_rows<T, GF, GF>(reinterpret_cast<T*>(base + L.z), zg, b, t0, TT, g.T, t_end, g.D, d0, tid);
-      stage_bc<T, GF>(reinterpret_cast<T*>(base + L.Ct), Cg, b, t0, TT, g.T, t_end, tid);
+      stage_bc<T, GF>(reinterpret_cast<T*>(base + L.Ct), Cg, b, t0, TT, g.T, t_end, g.ldbc, tid);
     }
     cp_async_commit();
   };
@@ -572,7 +574,7 @@ __global__ void __launch_bounds__(GB) m3_bwd_agg_kernel(BwdArgs a) {
     stage_rows<T, GB, GB>(reinterpret_cast<T*>(base + L.dr), static_cast<const T*>(a.dr), b, t0, rows, g.T, g.T, g.D, d0, tid);
     stage_rows<T, GB, GB>(reinterpret_cast<T*>(base + L.z), static_cast<const T*>(a.z), b, t0, rows, g.T, g.T, g.D, d0, tid);
     stage_rows<T, GB, GB>(reinterpret_cast<T*>(base + L.dg), static_cast<const T*>(a.dg), b, t0, rows, g.T, g.T, g.D, d0, tid);
-    stage_bc<T, GB>(reinterpret_cast<T*>(base + L.Ct), static_cast<const T*>(a.Cm), b, t0, rows, g.T, g.T, tid);
+    stage_bc<T, GB>(reinterpret_cast<T*>(base + L.Ct), static_cast<const T*>(a.Cm), b, t0, rows, g.T, g.T, g.ldbc, tid);
     cp_async_commit();
   };
 
@@ -598,8 +600,9 @@ __global__ void __launch_bounds__(GB) m3_bwd_agg_kernel(BwdArgs a) {
     const size_t cid = blockIdx.x + (size_t)gridDim.x * (blockIdx.y + (size_t)gridDim.y * blockIdx.z);
     const size_t total = (size_t)g.B * g.T * NS;
     for (size_t i = cid * GB + tid; i < total; i += ncta * GB) {
-      a.dB[i] = 0.f;
-      a.dC[i] = 0.f;
+      const size_t o = (i / NS) * g.lddbc + (i % NS);
+      a.dB[o] = 0.f;
+      a.dC[o] = 0.f;
     }
   }
   for (int i = 0; i < ntiles; ++i) {
@@ -694,8 +697,10 @@ __device__ __forceinline__ float warp_sum16_rotated(float (&v)[NS], int lane) {
 }
 
 // ST: compiled with the carried-state terms; the plain entry points run the
-// instance without them.
-template <typename T, bool ST>
+// instance without them.  SCAN: stop at du (written out) -- the SiLU and
+// conv backward then run in m3_conv_bwd_kernel with du plus any gradient
+// reaching u from outside the layer core.
+template <typename T, bool ST, bool SCAN>
 __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(BwdArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   const Geo g = a.g;
@@ -768,8 +773,8 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(BwdArgs a) {
     stage_rows<T, GB, GB>(reinterpret_cast<T*>(base + L.dr), static_cast<const T*>(a.dr), b, t0, K, g.T, g.T, g.D, d0, tid);
     stage_rows<T, GB, GB>(reinterpret_cast<T*>(base + L.z), static_cast<const T*>(a.z), b, t0, K, g.T, g.T, g.D, d0, tid);
     stage_rows<T, GB, GB>(reinterpret_cast<T*>(base + L.dg), static_cast<const T*>(a.dg), b, t0, K, g.T, g.T, g.D, d0, tid);
-    stage_bc<T, GB>(reinterpret_cast<T*>(base + L.Bt), static_cast<const T*>(a.Bm), b, t0, K, g.T, g.T, tid);
-    stage_bc<T, GB>(reinterpret_cast<T*>(base + L.Ct), static_cast<const T*>(a.Cm), b, t0, K, g.T, g.T, tid);
+    stage_bc<T, GB>(reinterpret_cast<T*>(base + L.Bt), static_cast<const T*>(a.Bm), b, t0, K, g.T, g.T, g.ldbc, tid);
+    stage_bc<T, GB>(reinterpret_cast<T*>(base + L.Ct), static_cast<const T*>(a.Cm), b, t0, K, g.T, g.T, g.ldbc, tid);
     // chunk start state: 16 rows of GB floats from ckpt[b, c, :, d0:d0+GB]
     stage_rows<float, GB, GB>(reinterpret_cast<float*>(base + L.ck), a.ckpt + ((size_t)b * g.nc + c) * NS * g.D,
                               0, 0, NS, NS, NS, g.D, d0, tid);
@@ -989,6 +994,13 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(BwdArgs a) {
         const float ddr = fmaf(u, sumB, LN2 * sAq) * sv;
         dD_acc = fmaf(dy, u, dD_acc);
         ddtb_acc += ddr;
+        if constexpr (SCAN) {  // the SiLU and conv backward run later, with du
+          if (active) {
+            Act<T>::st(ddr_c + (size_t)j * g.D, ddr);
+            Act<T>::st(du_c + (size_t)j * g.D, du);
+          }
+          continue;
+        }
         const float dc = du * (sc * fmaf(cpre, 1.f - sc, 1.f));
         dcb_acc += dc;
 #pragma unroll
@@ -1019,7 +1031,7 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(BwdArgs a) {
       float v = 0.f;
 #pragma unroll
       for (int ww = 0; ww < NWB; ++ww) v += red[(j * NWB + ww) * 32 + l];
-      float* dst = (l < NS ? a.dB : a.dC) + ((size_t)b * g.T + c * K + j) * NS + (l & (NS - 1));
+      float* dst = (l < NS ? a.dB : a.dC) + ((size_t)b * g.T + c * K + j) * g.lddbc + (l & (NS - 1));
       atomicAdd(dst, v);
     }
     __syncthreads();
@@ -1035,7 +1047,7 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(BwdArgs a) {
         dh0[(size_t)(n + 1) * g.D] = carry[i].y;
       }
     }
-    if (a.d_conv_in) {
+    if (!SCAN && a.d_conv_in) {
       // conv inputs of steps -1, -2, -3 reach the conv outputs of steps
       // 0..2 (dc1 = dc_0, dc2 = dc_1, dc3 = dc_2; zero past the sequence),
       // and, when T < 3, the conv-state output too
@@ -1079,7 +1091,7 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(BwdArgs a) {
 //  - blocks [nfin, ...): d_x at the last three steps of each segment but the
 //    last, which needs the conv gradient of the next segment's first steps.
 template <typename T>
-__global__ void m3_bwd_tail_kernel(BwdArgs a, int rows, int nfin) {
+__global__ void m3_bwd_tail_kernel(BwdArgs a, int rows, int nfin, int nout) {
   const Geo g = a.g;
   grid_dep_wait();  // the main kernel's partials and boundary terms
   if ((int)blockIdx.x >= nfin) {
@@ -1110,7 +1122,7 @@ __global__ void m3_bwd_tail_kernel(BwdArgs a, int rows, int nfin) {
   __shared__ float part[8][33];
   const int cx = threadIdx.x & 31, ry = threadIdx.x >> 5;
   const int oidx = blockIdx.x * 32 + cx;
-  const bool ok = oidx < 23 * g.D;
+  const bool ok = oidx < nout * g.D;
   const int jj = oidx / g.D, d = oidx - jj * g.D;
   {
     float v0 = 0.f, v1 = 0.f;
@@ -1148,6 +1160,133 @@ __global__ void m3_bwd_tail_kernel(BwdArgs a, int rows, int nfin) {
 }
 
 // ---------------------------------------------------------------------------
+// SiLU and conv backward of the two-phase backward: with du from the scan
+// backward and a gradient reaching u from outside the layer core (the x_proj
+// path), dc = (du + du_extra) silu'(c) and d_x[s] = sum_k dc[s+3-k] w[k];
+// per-(batch, tile) partials of d_conv_b and d_conv_w.  One thread per
+// channel over a tile of steps, plus the three steps after it, whose dc
+// reaches the tile's last d_x.  Plain coalesced loads: every value is read
+// by one thread.
+// ---------------------------------------------------------------------------
+
+struct ConvArgs {
+  int B, T, D, tile, ntiles;
+  const void *x, *du, *du_extra;  // [B, T, D] act (du_extra nullable)
+  const float *conv_w, *conv_b;
+  void* dx;                       // [B, T, D] act
+  float* part;                    // [B * ntiles, 5, D]: d_conv_b, d_conv_w[0..3]
+  const void* conv_in;            // [B, 3, D] act, nullable
+  const void* g_conv;             // [B, 3, D] act, nullable
+  void* d_conv_in;                // [B, 3, D] act, nullable
+  float *d_conv_w, *d_conv_b;
+  int accumulate;
+};
+
+template <typename T>
+__global__ void __launch_bounds__(128) m3_conv_bwd_kernel(ConvArgs a) {
+  const int d = blockIdx.x * 128 + threadIdx.x;
+  const int tile = blockIdx.y, b = blockIdx.z;
+  if (d >= a.D) return;  // no barriers below
+  const size_t D = (size_t)a.D;
+  const int t0 = tile * a.tile;
+  const int t1 = min(t0 + a.tile, a.T);
+  const int t2 = min(t1 + 3, a.T);
+  const T* xg = static_cast<const T*>(a.x) + (size_t)b * a.T * D + d;
+  const T* dug = static_cast<const T*>(a.du) + (size_t)b * a.T * D + d;
+  const T* deg = a.du_extra ? static_cast<const T*>(a.du_extra) + (size_t)b * a.T * D + d : nullptr;
+  float w[WC];
+#pragma unroll
+  for (int k = 0; k < WC; ++k) w[k] = a.conv_w[(size_t)d * WC + k];
+  const float cb = a.conv_b[d];
+  auto x_at = [&](int t) -> float {
+    if (t >= 0) return Act<T>::ld(xg + (size_t)t * D);
+    if (a.conv_in) return Act<T>::ld(static_cast<const T*>(a.conv_in) + ((size_t)b * 3 + t + 3) * D + d);
+    return 0.f;
+  };
+  float xm3 = x_at(t0 - 3), xm2 = x_at(t0 - 2), xm1 = x_at(t0 - 1);
+  float dc1 = 0.f, dc2 = 0.f, dc3 = 0.f;  // dc one, two and three steps back
+  float dcb = 0.f, dcw[WC] = {0.f, 0.f, 0.f, 0.f};
+  float first[3] = {0.f, 0.f, 0.f};     // dc at steps 0, 1, 2
+#pragma unroll 4
+  for (int t = t0; t < t1 + 3; ++t) {
+    float dc = 0.f;
+    if (t < t2) {
+      const float xv = Act<T>::ld(xg + (size_t)t * D);
+      float gu = Act<T>::ld(dug + (size_t)t * D);
+      if (deg) gu += Act<T>::ld(deg + (size_t)t * D);
+      const float c = fmaf(w[0], xm3, fmaf(w[1], xm2, fmaf(w[2], xm1, fmaf(w[3], xv, cb))));
+      const float sc = sigmoid_f(c);
+      dc = gu * (sc * fmaf(c, 1.f - sc, 1.f));
+      if (t < t1) {
+        dcb += dc;
+        dcw[0] = fmaf(dc, xm3, dcw[0]);
+        dcw[1] = fmaf(dc, xm2, dcw[1]);
+        dcw[2] = fmaf(dc, xm1, dcw[2]);
+        dcw[3] = fmaf(dc, xv, dcw[3]);
+      }
+      if (t < 3) first[t] = dc;
+      xm3 = xm2;
+      xm2 = xm1;
+      xm1 = xv;
+    }
+    const int sx = t - 3;  // d_x[sx] needs dc[sx .. sx + 3]
+    if (sx >= t0) {
+      float v = fmaf(dc3, w[3], fmaf(dc2, w[2], fmaf(dc1, w[1], dc * w[0])));
+      if (a.g_conv && sx >= a.T - 3)  // x[sx] is also a conv-state output
+        v += Act<T>::ld(static_cast<const T*>(a.g_conv) + ((size_t)b * 3 + sx - (a.T - 3)) * D + d);
+      Act<T>::st(static_cast<T*>(a.dx) + ((size_t)b * a.T + sx) * D + d, v);
+    }
+    dc3 = dc2;
+    dc2 = dc1;
+    dc1 = dc;
+  }
+  if (tile == 0 && a.d_conv_in) {
+    // conv inputs of steps -3, -2, -1 (rows 0..2) reach dc of steps 0..2
+    float v[3];
+    v[0] = first[0] * w[0];
+    v[1] = fmaf(first[1], w[0], first[0] * w[1]);
+    v[2] = fmaf(first[2], w[0], fmaf(first[1], w[1], first[0] * w[2]));
+    T* dci = static_cast<T*>(a.d_conv_in) + (size_t)b * 3 * D + d;
+#pragma unroll
+    for (int r = 0; r < 3; ++r) {
+      const int ro = r - a.T;  // row of the conv-state output holding step r - 3
+      if (a.g_conv && ro >= 0)
+        v[r] += Act<T>::ld(static_cast<const T*>(a.g_conv) + ((size_t)b * 3 + ro) * D + d);
+      Act<T>::st(dci + (size_t)r * D, v[r]);
+    }
+  }
+  float* P = a.part + ((size_t)b * a.ntiles + tile) * 5 * D + d;
+  P[0] = dcb;
+#pragma unroll
+  for (int k = 0; k < WC; ++k) P[(size_t)(1 + k) * D] = dcw[k];
+}
+
+// d_conv_b and d_conv_w from the per-(batch, tile) partials, summed in a
+// fixed order (32 outputs per block, rows split over 8 warps).
+__global__ void m3_conv_fin_kernel(ConvArgs a) {
+  grid_dep_wait();  // the conv backward's partials
+  __shared__ float part[8][33];
+  const int cx = threadIdx.x & 31, ry = threadIdx.x >> 5;
+  const int oidx = blockIdx.x * 32 + cx;
+  const bool ok = oidx < 5 * a.D;
+  const int j = ok ? oidx / a.D : 0, d = oidx - j * a.D;
+  const int rows = a.B * a.ntiles;
+  float v0 = 0.f;
+  if (ok) {
+    const float* __restrict__ P = a.part + (size_t)j * a.D + d;
+    const size_t stride = (size_t)5 * a.D;
+    for (int r = ry; r < rows; r += 8) v0 += P[(size_t)r * stride];
+  }
+  part[ry][cx] = v0;
+  __syncthreads();
+  if (ry != 0 || !ok) return;
+  const float v = ((part[0][cx] + part[1][cx]) + (part[2][cx] + part[3][cx])) +
+                  ((part[4][cx] + part[5][cx]) + (part[6][cx] + part[7][cx]));
+  float* dst = j == 0 ? a.d_conv_b + d : a.d_conv_w + (size_t)d * WC + (j - 1);
+  *dst = a.accumulate ? *dst + v : v;
+}
+
+// ---------------------------------------------------------------------------
 // decode: the forward of a short window (typically one token per sequence)
 // from the carried state, updating that state in place; no checkpoints, no
 // time split.  One thread per channel keeps its N state lanes in registers;
@@ -1156,6 +1295,7 @@ __global__ void m3_bwd_tail_kernel(BwdArgs a, int rows, int nfin) {
 
 struct DecArgs {
   int B, T, D;
+  int ldbc;  // row stride (elements) of Bm and Cm
   const void *x, *dr, *z, *Bm, *Cm;
   const float *conv_w, *conv_b, *dt_bias, *a_log, *Dp;
   float* h;    // [B, N, D] f32, in and out
@@ -1196,7 +1336,7 @@ __global__ void __launch_bounds__(GD) m3_decode_kernel(DecArgs a) {
       const int sb = blockIdx.y * R + sr;
       if (sb < a.B) {
         const T* src = static_cast<const T*>(sn < N ? a.Bm : a.Cm);
-        sBC[buf][sr][sn] = Act<T>::ld(src + ((size_t)sb * a.T + t) * N + (sn & (N - 1)));
+        sBC[buf][sr][sn] = Act<T>::ld(src + ((size_t)sb * a.T + t) * a.ldbc + (sn & (N - 1)));
       }
     }
   };
@@ -1393,14 +1533,13 @@ cudaError_t set_attrs() {
                              (int)agg_smem(es).total);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(m3_bwd_agg_kernel<T>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(m3_bwd_kernel<T, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_CAP);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(m3_bwd_kernel<T, false>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(m3_bwd_kernel<T, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_CAP);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(m3_bwd_kernel<T, true>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+  void (*const bwd_kernels[4])(BwdArgs) = {m3_bwd_kernel<T, false, false>, m3_bwd_kernel<T, true, false>,
+                                            m3_bwd_kernel<T, false, true>, m3_bwd_kernel<T, true, true>};
+  for (auto k : bwd_kernels) {
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_CAP);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+  }
   return e;
 }
 
@@ -1432,13 +1571,13 @@ cudaError_t device_info(int chunk, int ai, int* sms, int* occ_f, int* occ_b, int
       e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&of, m3_fwd_kernel<__nv_bfloat16, true>, GF,
                                                         fwd_smem(2).total);
       if (e == cudaSuccess)
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ob, m3_bwd_kernel<__nv_bfloat16, false>, GB,
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ob, m3_bwd_kernel<__nv_bfloat16, false, false>, GB,
                                                           bwd_launch_smem(chunk, 2, di.smem_per_sm));
     } else {
       e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&of, m3_fwd_kernel<float, true>, GF,
                                                         fwd_smem(4).total);
       if (e == cudaSuccess)
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ob, m3_bwd_kernel<float, false>, GB,
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ob, m3_bwd_kernel<float, false, false>, GB,
                                                           bwd_launch_smem(chunk, 4, di.smem_per_sm));
     }
     if (e != cudaSuccess) return e;
@@ -1456,11 +1595,14 @@ cudaError_t device_info(int chunk, int ai, int* sms, int* occ_f, int* occ_b, int
 
 struct Plan {
   int B, T, D, K, nc;
+  int ldbc, lddbc;
   int Sf, mf, Sb, mb;
   size_t ckpt_bytes, ws_bytes;
   // workspace offsets (bytes)
   size_t f_aggh, f_aggs;
   size_t b_part, b_q, b_sd, b_dxpart, b_dchead;
+  int ctile, cntiles;  // conv backward: steps per tile, tiles per sequence
+  size_t c_part;
   int fwd_launches, bwd_launches;
 };
 
@@ -1512,6 +1654,13 @@ m3_status validate_dims(const m3_dims* dm, m3_dtype act) {
     return M3_ERR_DIMS;
   if (dm->segments > 65535) return M3_ERR_DIMS;
   if (dm->batch * dm->d_inner > ((int64_t)1 << 27)) return M3_ERR_DIMS;  // 1-D grid of the tail kernel
+  // row strides of Bm/Cm (16-byte copies: a multiple of 16 bytes) and dB/dC
+  if (dm->bc_stride < 0 || dm->dbc_stride < 0 || dm->bc_stride > ((int64_t)1 << 20) ||
+      dm->dbc_stride > ((int64_t)1 << 20))
+    return M3_ERR_DIMS;
+  if (dm->bc_stride != 0 && dm->bc_stride < NS) return M3_ERR_DIMS;
+  if (dm->dbc_stride != 0 && dm->dbc_stride < NS) return M3_ERR_DIMS;
+  if (dm->bc_stride * (act == M3_BF16 ? 2 : 4) % 16 != 0) return M3_ERR_ALIGN;
   return M3_OK;
 }
 
@@ -1523,6 +1672,8 @@ m3_status make_plan(const m3_dims* dm, m3_dtype act, Plan* p) {
   p->D = (int)dm->d_inner;
   p->K = dm->chunk ? (int)dm->chunk : KDEF;
   p->nc = (p->T + p->K - 1) / p->K;
+  p->ldbc = dm->bc_stride ? (int)dm->bc_stride : NS;
+  p->lddbc = dm->dbc_stride ? (int)dm->dbc_stride : NS;
   const int groups_f = (p->D + GF - 1) / GF;
   const int groups_b = (p->D + GB - 1) / GB;
   int want_f = 1, want_b = 1;
@@ -1569,6 +1720,19 @@ m3_status make_plan(const m3_dims* dm, m3_dtype act, Plan* p) {
     p->b_dchead = take(B * p->Sb * 3 * D * 4);
   }
   size_t bwd_total = off;
+  // conv backward of the two-phase backward (its own call): 128-step tiles,
+  // or 32-step ones when that leaves fewer than four blocks per SM of a
+  // 152-SM GPU
+  {
+    const int64_t groups = (p->D + 127) / 128;
+    p->ctile = 128;
+    if ((int64_t)p->B * groups * ((p->T + 127) / 128) < 4 * 152) p->ctile = 32;
+    p->cntiles = (p->T + p->ctile - 1) / p->ctile;
+  }
+  off = 0;
+  p->c_part = take(B * (size_t)p->cntiles * 5 * D * 4);
+  const size_t conv_total = off;
+  if (conv_total > bwd_total) bwd_total = conv_total;
   p->ws_bytes = fwd_total > bwd_total ? fwd_total : bwd_total;
   if (p->ws_bytes < 256) p->ws_bytes = 256;
   const bool empty = (size_t)p->B * p->T * p->D == 0;
@@ -1603,7 +1767,7 @@ template <typename T>
 m3_status launch_fwd(const Plan& p, FwdArgs a, cudaStream_t st) {
   const int groups = (p.D + GF - 1) / GF;
   const size_t smem = fwd_smem(sizeof(T)).total;
-  a.g = Geo{p.B, p.T, p.D, p.K, p.nc, p.Sf, p.mf};
+  a.g = Geo{p.B, p.T, p.D, p.K, p.nc, p.Sf, p.mf, p.ldbc, p.lddbc};
   cudaError_t e = cudaSuccess;
   if (p.Sf > 1) e = launch_k(m3_fwd_kernel<T, false>, dim3(groups, p.Sf - 1, p.B), GF, smem, st, false, a);
   if (e == cudaSuccess)
@@ -1612,10 +1776,11 @@ m3_status launch_fwd(const Plan& p, FwdArgs a, cudaStream_t st) {
   return note(e) == cudaSuccess ? M3_OK : M3_ERR_CUDA;
 }
 
+// scan: stop at du (m3scan_bwd_scan); the conv side runs in launch_conv_bwd.
 template <typename T>
-m3_status launch_bwd(const Plan& p, BwdArgs a, cudaStream_t st, int smem_per_sm) {
+m3_status launch_bwd(const Plan& p, BwdArgs a, cudaStream_t st, int smem_per_sm, bool scan) {
   const int groups = (p.D + GB - 1) / GB;
-  a.g = Geo{p.B, p.T, p.D, p.K, p.nc, p.Sb, p.mb};
+  a.g = Geo{p.B, p.T, p.D, p.K, p.nc, p.Sb, p.mb, p.ldbc, p.lddbc};
   cudaError_t e = cudaSuccess;
   if (p.Sb > 1) {
     // also clears dB and dC before the main kernel's reductions into them
@@ -1623,19 +1788,24 @@ m3_status launch_bwd(const Plan& p, BwdArgs a, cudaStream_t st, int smem_per_sm)
                  st, false, a);
     if (note(e) != cudaSuccess) return M3_ERR_CUDA;
   } else {
-    if (note(cudaMemsetAsync(a.dB, 0, (size_t)p.B * p.T * NS * 4, st)) != cudaSuccess) return M3_ERR_CUDA;
-    if (note(cudaMemsetAsync(a.dC, 0, (size_t)p.B * p.T * NS * 4, st)) != cudaSuccess) return M3_ERR_CUDA;
+    // only the 16 columns of each (batch, step) row belong to dB and dC
+    const size_t pitch = (size_t)p.lddbc * 4, rows = (size_t)p.B * p.T;
+    if (note(cudaMemset2DAsync(a.dB, pitch, 0, NS * 4, rows, st)) != cudaSuccess) return M3_ERR_CUDA;
+    if (note(cudaMemset2DAsync(a.dC, pitch, 0, NS * 4, rows, st)) != cudaSuccess) return M3_ERR_CUDA;
   }
   a.tcols = tmem_cols_for(p.K);
   const size_t smem = bwd_launch_smem(p.K, sizeof(T), smem_per_sm);
   const bool with_state = a.conv_in || a.g_h || a.g_conv || a.d_h_in || a.d_conv_in;
-  e = launch_k(with_state ? m3_bwd_kernel<T, true> : m3_bwd_kernel<T, false>,
-               dim3(groups, p.Sb, p.B), GB, smem, st, p.Sb > 1, a);
-  const size_t nfin = ((size_t)23 * p.D + 31) / 32;                   // 32 outputs per block
-  const size_t nfix = p.Sb > 1 ? ((size_t)p.B * (p.Sb - 1) * 3 * p.D + 255) / 256 : 0;
+  void (*kern)(BwdArgs) = scan ? (with_state ? m3_bwd_kernel<T, true, true> : m3_bwd_kernel<T, false, true>)
+                               : (with_state ? m3_bwd_kernel<T, true, false> : m3_bwd_kernel<T, false, false>);
+  e = launch_k(kern, dim3(groups, p.Sb, p.B), GB, smem, st, p.Sb > 1, a);
+  // parameter outputs: 16 d_a_log, dD, d_dt_bias (+ d_conv_b, 4 d_conv_w)
+  const int nout = scan ? 18 : 23;
+  const size_t nfin = ((size_t)nout * p.D + 31) / 32;                 // 32 outputs per block
+  const size_t nfix = (!scan && p.Sb > 1) ? ((size_t)p.B * (p.Sb - 1) * 3 * p.D + 255) / 256 : 0;
   if (e == cudaSuccess)
     e = launch_k(m3_bwd_tail_kernel<T>, dim3((unsigned)(nfin + nfix)), 256, 0, st, true, a,
-                 p.B * p.Sb, (int)nfin);
+                 p.B * p.Sb, (int)nfin, nout);
   if (e == cudaSuccess) e = cudaGetLastError();
   return note(e) == cudaSuccess ? M3_OK : M3_ERR_CUDA;
 }
@@ -1762,7 +1932,7 @@ m3_status bwd_impl(const m3_dims* dims, m3_dtype act, const void* x, const void*
                    const float* ckpt, const void* d_gated, void* d_x, void* d_delta_raw, void* dz,
                    void* du_dbg, float* dB, float* dC, float* d_conv_w, float* d_conv_b,
                    float* d_dt_bias, float* d_a_log, float* dD, const m3_bwd_state* state,
-                   void* workspace, size_t workspace_bytes, m3_stream_t stream) {
+                   void* workspace, size_t workspace_bytes, m3_stream_t stream, bool scan) {
   Plan p;
   m3_status st = make_plan(dims, act, &p);
   if (st != M3_OK) return st;
@@ -1780,10 +1950,10 @@ m3_status bwd_impl(const m3_dims* dims, m3_dtype act, const void* x, const void*
     if (st != M3_OK) return st;
     // no elements: parameter grads are zero (or unchanged when accumulating)
     if (p.D > 0 && !dims->accumulate_param_grads) {
-      if (!d_conv_w || !d_conv_b || !d_dt_bias || !d_a_log || !dD) return M3_ERR_NULL;
+      if ((!scan && (!d_conv_w || !d_conv_b)) || !d_dt_bias || !d_a_log || !dD) return M3_ERR_NULL;
       const size_t D_ = p.D;
-      if (cudaMemsetAsync(d_conv_w, 0, D_ * WC * 4, s) != cudaSuccess ||
-          cudaMemsetAsync(d_conv_b, 0, D_ * 4, s) != cudaSuccess ||
+      if ((!scan && (cudaMemsetAsync(d_conv_w, 0, D_ * WC * 4, s) != cudaSuccess ||
+                     cudaMemsetAsync(d_conv_b, 0, D_ * 4, s) != cudaSuccess)) ||
           cudaMemsetAsync(d_dt_bias, 0, D_ * 4, s) != cudaSuccess ||
           cudaMemsetAsync(d_a_log, 0, D_ * NS * 4, s) != cudaSuccess ||
           cudaMemsetAsync(dD, 0, D_ * 4, s) != cudaSuccess) {
@@ -1794,9 +1964,9 @@ m3_status bwd_impl(const m3_dims* dims, m3_dtype act, const void* x, const void*
     return M3_OK;
   }
   if (!x || !delta_raw || !z || !Bm || !Cm || !conv_w || !conv_b || !dt_bias || !a_log || !D ||
-      !ckpt || !d_gated || !d_x || !d_delta_raw || !dz || !dB || !dC || !d_conv_w || !d_conv_b ||
-      !d_dt_bias || !d_a_log || !dD)
+      !ckpt || !d_gated || !d_delta_raw || !dz || !dB || !dC || !d_dt_bias || !d_a_log || !dD)
     return M3_ERR_NULL;
+  if (scan ? !du_dbg : (!d_x || !d_conv_w || !d_conv_b)) return M3_ERR_NULL;
   const void* act_ptrs[] = {x, delta_raw, z, Bm, Cm, d_gated, d_x, d_delta_raw, dz, du_dbg};
   for (const void* q : act_ptrs)
     if (q && !aligned(q, 16)) return M3_ERR_ALIGN;
@@ -1829,8 +1999,8 @@ m3_status bwd_impl(const m3_dims* dims, m3_dtype act, const void* x, const void*
   a.accumulate = dims->accumulate_param_grads ? 1 : 0;
   a.conv_in = sv.conv_state; a.g_h = sv.d_ssm_state_out; a.g_conv = sv.d_conv_state_out;
   a.d_h_in = sv.d_ssm_state; a.d_conv_in = sv.d_conv_state;
-  m3_status r = act == M3_BF16 ? launch_bwd<__nv_bfloat16>(p, a, s, smem_sm)
-                                : launch_bwd<float>(p, a, s, smem_sm);
+  m3_status r = act == M3_BF16 ? launch_bwd<__nv_bfloat16>(p, a, s, smem_sm, scan)
+                                : launch_bwd<float>(p, a, s, smem_sm, scan);
   if (r != M3_OK) cudaGetLastError();
   return r;
 }
@@ -1868,7 +2038,7 @@ m3_status m3scan_bwd(const m3_dims* dims, m3_dtype act, const void* x, const voi
                      size_t workspace_bytes, m3_stream_t stream) {
   return bwd_impl(dims, act, x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D, ckpt,
                   d_gated, d_x, d_delta_raw, dz, du_dbg, dB, dC, d_conv_w, d_conv_b, d_dt_bias,
-                  d_a_log, dD, nullptr, workspace, workspace_bytes, stream);
+                  d_a_log, dD, nullptr, workspace, workspace_bytes, stream, false);
 }
 
 m3_status m3scan_bwd_state(const m3_dims* dims, m3_dtype act, const void* x,
@@ -1883,7 +2053,69 @@ m3_status m3scan_bwd_state(const m3_dims* dims, m3_dtype act, const void* x,
   if (!state) return M3_ERR_NULL;
   return bwd_impl(dims, act, x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D, ckpt,
                   d_gated, d_x, d_delta_raw, dz, du_dbg, dB, dC, d_conv_w, d_conv_b, d_dt_bias,
-                  d_a_log, dD, state, workspace, workspace_bytes, stream);
+                  d_a_log, dD, state, workspace, workspace_bytes, stream, false);
+}
+
+m3_status m3scan_bwd_scan(const m3_dims* dims, m3_dtype act, const void* x, const void* delta_raw,
+                          const void* z, const void* Bm, const void* Cm, const float* conv_w,
+                          const float* conv_b, const float* dt_bias, const float* a_log,
+                          const float* D, const float* ckpt, const void* d_gated, void* du,
+                          void* d_delta_raw, void* dz, float* dB, float* dC, float* d_dt_bias,
+                          float* d_a_log, float* dD, const m3_bwd_state* state, void* workspace,
+                          size_t workspace_bytes, m3_stream_t stream) {
+  return bwd_impl(dims, act, x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D, ckpt,
+                  d_gated, nullptr, d_delta_raw, dz, du, dB, dC, nullptr, nullptr, d_dt_bias,
+                  d_a_log, dD, state, workspace, workspace_bytes, stream, true);
+}
+
+m3_status m3scan_conv_bwd(const m3_dims* dims, m3_dtype act, const void* x, const float* conv_w,
+                          const float* conv_b, const void* du, const void* du_extra, void* d_x,
+                          float* d_conv_w, float* d_conv_b, const m3_bwd_state* state,
+                          void* workspace, size_t workspace_bytes, m3_stream_t stream) {
+  Plan p;
+  m3_status st = make_plan(dims, act, &p);
+  if (st != M3_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const m3_bwd_state none{};
+  const m3_bwd_state& sv = state ? *state : none;
+  const size_t es = act == M3_BF16 ? 2 : 4;
+  if (!aligned(sv.conv_state, es) || !aligned(sv.d_conv_state_out, es) || !aligned(sv.d_conv_state, es))
+    return M3_ERR_ALIGN;
+  if ((size_t)p.B * p.T * p.D == 0) {
+    st = pass_state(sv.d_conv_state_out, sv.d_conv_state, (size_t)p.B * p.D * 3 * es, s);
+    if (st != M3_OK) return st;
+    if (p.D > 0 && !dims->accumulate_param_grads) {
+      if (!d_conv_w || !d_conv_b) return M3_ERR_NULL;
+      if (note(cudaMemsetAsync(d_conv_w, 0, (size_t)p.D * WC * 4, s)) != cudaSuccess ||
+          note(cudaMemsetAsync(d_conv_b, 0, (size_t)p.D * 4, s)) != cudaSuccess)
+        return M3_ERR_CUDA;
+    }
+    return M3_OK;
+  }
+  if (!x || !conv_w || !conv_b || !du || !d_x || !d_conv_w || !d_conv_b) return M3_ERR_NULL;
+  const void* act_ptrs[] = {x, du, du_extra, d_x};
+  for (const void* q : act_ptrs)
+    if (q && !aligned(q, 16)) return M3_ERR_ALIGN;
+  const void* f_ptrs[] = {conv_w, conv_b, d_conv_w, d_conv_b};
+  for (const void* q : f_ptrs)
+    if (!aligned(q, 4)) return M3_ERR_ALIGN;
+  if (!workspace || workspace_bytes < p.ws_bytes) return M3_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return M3_ERR_ALIGN;
+  ConvArgs a{};
+  a.B = p.B; a.T = p.T; a.D = p.D; a.tile = p.ctile; a.ntiles = p.cntiles;
+  a.x = x; a.du = du; a.du_extra = du_extra; a.conv_w = conv_w; a.conv_b = conv_b; a.dx = d_x;
+  a.part = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) + p.c_part);
+  a.conv_in = sv.conv_state; a.g_conv = sv.d_conv_state_out; a.d_conv_in = sv.d_conv_state;
+  a.d_conv_w = d_conv_w; a.d_conv_b = d_conv_b;
+  a.accumulate = dims->accumulate_param_grads ? 1 : 0;
+  const dim3 grid((unsigned)((p.D + 127) / 128), (unsigned)p.cntiles, (unsigned)p.B);
+  cudaError_t e = act == M3_BF16
+                      ? launch_k(m3_conv_bwd_kernel<__nv_bfloat16>, grid, 128, 0, s, false, a)
+                      : launch_k(m3_conv_bwd_kernel<float>, grid, 128, 0, s, false, a);
+  if (e == cudaSuccess)
+    e = launch_k(m3_conv_fin_kernel, dim3((unsigned)((5 * (size_t)p.D + 31) / 32)), 256, 0, s, true, a);
+  if (e == cudaSuccess) e = cudaGetLastError();
+  return note(e) == cudaSuccess ? M3_OK : M3_ERR_CUDA;
 }
 
 
@@ -1993,6 +2225,9 @@ m3_status m3scan_decode(const m3_dims* dims, m3_dtype act, const void* x, const 
     return M3_ERR_UNSUPPORTED;
   if (dims->batch > 65535 || dims->seq_len > ((int64_t)1 << 30) || dims->d_inner > ((int64_t)1 << 24))
     return M3_ERR_DIMS;
+  if (dims->bc_stride < 0 || dims->bc_stride > ((int64_t)1 << 20) ||
+      (dims->bc_stride != 0 && dims->bc_stride < dims->d_state))
+    return M3_ERR_DIMS;
   if (dims->batch * dims->seq_len * dims->d_inner == 0) return M3_OK;
   if (!x || !delta_raw || !z || !Bm || !Cm || !conv_w || !conv_b || !dt_bias || !a_log || !D ||
       !ssm_state || !conv_state || !gated)
@@ -2008,6 +2243,7 @@ m3_status m3scan_decode(const m3_dims* dims, m3_dtype act, const void* x, const 
   a.B = (int)dims->batch;
   a.T = (int)dims->seq_len;
   a.D = (int)dims->d_inner;
+  a.ldbc = dims->bc_stride ? (int)dims->bc_stride : (int)dims->d_state;
   a.x = x; a.dr = delta_raw; a.z = z; a.Bm = Bm; a.Cm = Cm;
   a.conv_w = conv_w; a.conv_b = conv_b; a.dt_bias = dt_bias; a.a_log = a_log; a.Dp = D;
   a.h = ssm_state; a.conv = conv_state; a.gated = gated; a.y_dbg = y_dbg;

@@ -238,3 +238,62 @@ def test_decode_validates_before_any_launch(lib):
     assert _decode(binding.make_dims(2, 0, 60), x=A + 2) == "M3_OK"
     # nothing to do: no pointer is needed
     assert _decode(binding.make_dims(2, 0, 64), x=None, ssm_state=None) == "M3_OK"
+
+
+def _struct_fields(name):
+    src = open(os.path.join(ROOT, "include", "m3scan.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    body = re.search(r"typedef struct \{([^{}]*)\}\s*" + name + ";", src).group(1)
+    names = []
+    for decl in body.split(";"):
+        decl = decl.strip()
+        if not decl:
+            continue
+        parts = decl.split(",")
+        names.append(re.findall(r"(\w+)\s*$", parts[0])[0])
+        names += [p.strip() for p in parts[1:]]
+    return names
+
+
+def test_dims_and_plan_structs_match_the_header():
+    assert _struct_fields("m3_dims") == [f for f, _ in binding.M3Dims._fields_]
+    assert _struct_fields("m3_plan") == [f for f, _ in binding.M3Plan._fields_]
+    assert ctypes.sizeof(binding.M3Dims) == 8 * 7 + 4 * 2 + 8 * 2
+
+
+def test_row_strides_are_validated(lib):
+    out = binding.M3Plan()
+    def plan(**kw):
+        d = binding.make_dims(2, 64, 64, segments=1, **kw)
+        return binding.STATUS[lib.m3scan_plan(ctypes.byref(d), binding.M3_BF16, ctypes.byref(out))]
+    assert plan(bc_stride=48, dbc_stride=48) == "M3_OK"      # dt_rank 16 + 2 x 16
+    assert plan(bc_stride=8) == "M3_ERR_DIMS"                 # narrower than d_state
+    assert plan(dbc_stride=15) == "M3_ERR_DIMS"
+    assert plan(bc_stride=-16) == "M3_ERR_DIMS"
+    assert plan(bc_stride=20) == "M3_ERR_ALIGN"               # 40 bytes: not a multiple of 16
+    assert plan(dbc_stride=17) == "M3_OK"                     # dB/dC take any stride
+
+
+def test_two_phase_entry_points_validate_before_any_launch(lib):
+    dims = binding.make_dims(2, 64, 64, chunk=16, segments=2)
+    a = dict(x=A, delta_raw=A, z=A, Bm=A, Cm=A, conv_w=A, conv_b=A, dt_bias=A, a_log=A, D=A,
+             ckpt=A, d_gated=A, du=A, d_delta_raw=A, dz=A, dB=A, dC=A, d_dt_bias=A, d_a_log=A,
+             dD=A)
+    def scan(**over):
+        b = dict(a)
+        b.update(over)
+        return binding.STATUS[binding.raw_bwd_scan(dims, binding.M3_BF16, *b.values(), None, A,
+                                                   1 << 30, None)]
+    assert scan(du=None) == "M3_ERR_NULL"
+    assert scan(dD=None) == "M3_ERR_NULL"
+    assert scan(du=A + 2) == "M3_ERR_ALIGN"
+    def conv(**over):
+        c = dict(x=A, conv_w=A, conv_b=A, du=A, du_extra=None, d_x=A, d_conv_w=A, d_conv_b=A)
+        c.update(over)
+        ws = c.pop("ws", 1 << 30)
+        return binding.STATUS[binding.raw_conv_bwd(dims, binding.M3_BF16, *c.values(), None, A,
+                                                   ws, None)]
+    assert conv(du=None) == "M3_ERR_NULL"
+    assert conv(d_x=None) == "M3_ERR_NULL"
+    assert conv(du_extra=A + 2) == "M3_ERR_ALIGN"
+    assert conv(ws=16) == "M3_ERR_WORKSPACE"
