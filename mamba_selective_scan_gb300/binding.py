@@ -51,7 +51,7 @@ class M3Dims(ctypes.Structure):
                 ("d_conv", ctypes.c_int64), ("chunk", ctypes.c_int64),
                 ("segments", ctypes.c_int64),
                 ("accumulate_param_grads", ctypes.c_int32),
-                ("reserved", ctypes.c_int32),
+                ("bwd_threads_per_channel", ctypes.c_int32),
                 ("bc_stride", ctypes.c_int64), ("dbc_stride", ctypes.c_int64)]
 
 
@@ -59,7 +59,8 @@ class M3Plan(ctypes.Structure):
     _fields_ = [("chunk", ctypes.c_int64), ("n_chunks", ctypes.c_int64),
                 ("fwd_segments", ctypes.c_int64), ("bwd_segments", ctypes.c_int64),
                 ("ckpt_bytes", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64),
-                ("fwd_launches", ctypes.c_int32), ("bwd_launches", ctypes.c_int32)]
+                ("fwd_launches", ctypes.c_int32), ("bwd_launches", ctypes.c_int32),
+                ("bwd_threads_per_channel", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
     def as_dict(self):
         return {k: getattr(self, k) for k, _ in self._fields_}
@@ -152,10 +153,11 @@ def load():
 
 
 def make_dims(batch, seq_len, d_inner, d_state=16, d_conv=4, chunk=0, segments=0,
-              accumulate_param_grads=False, bc_stride=0, dbc_stride=0) -> M3Dims:
+              accumulate_param_grads=False, bc_stride=0, dbc_stride=0,
+              bwd_threads_per_channel=0) -> M3Dims:
     return M3Dims(int(batch), int(seq_len), int(d_inner), int(d_state), int(d_conv),
-                  int(chunk), int(segments), int(bool(accumulate_param_grads)), 0,
-                  int(bc_stride), int(dbc_stride))
+                  int(chunk), int(segments), int(bool(accumulate_param_grads)),
+                  int(bwd_threads_per_channel), int(bc_stride), int(dbc_stride))
 
 
 def m3scan_plan(dims: M3Dims, act: int) -> M3Plan:
@@ -389,16 +391,17 @@ def _fwd(x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D, chunk, segm
 
 def m3scan_bwd(x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D, ckpt, d_gated, *,
                chunk=0, segments=0, want_du=False, accumulate_param_grads=False, out=None,
-               workspace=None, stream=None):
+               workspace=None, stream=None, bwd_threads_per_channel=0):
     """Backward of the layer core.  Returns a dict of gradients (tensors)."""
     return _bwd(x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D, ckpt, d_gated,
-                chunk, segments, want_du, accumulate_param_grads, out, workspace, stream, None)
+                chunk, segments, want_du, accumulate_param_grads, out, workspace, stream, None,
+                bwd_threads_per_channel)
 
 
 def m3scan_bwd_state(x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D, ckpt, d_gated,
                      *, conv_state=None, d_ssm_state_out=None, d_conv_state_out=None, chunk=0,
                      segments=0, want_du=False, accumulate_param_grads=False, out=None,
-                     workspace=None, stream=None):
+                     workspace=None, stream=None, bwd_threads_per_channel=0):
     """Backward of one window made by ``m3scan_fwd_state``.  Returns the
     gradients of ``m3scan_bwd`` plus ``d_ssm_state`` [B,16,D] f32 and
     ``d_conv_state`` [B,3,D] (activation dtype)."""
@@ -416,11 +419,12 @@ def m3scan_bwd_state(x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D,
     st = M3BwdState(_ptr(conv_state), _ptr(d_ssm_state_out), _ptr(d_conv_state_out),
                     _ptr(o["d_ssm_state"]), _ptr(o["d_conv_state"]))
     return _bwd(x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D, ckpt, d_gated,
-                chunk, segments, want_du, accumulate_param_grads, o, workspace, stream, st)
+                chunk, segments, want_du, accumulate_param_grads, o, workspace, stream, st,
+                bwd_threads_per_channel)
 
 
 def _bwd(x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D, ckpt, d_gated, chunk,
-         segments, want_du, accumulate_param_grads, out, workspace, stream, state):
+         segments, want_du, accumulate_param_grads, out, workspace, stream, state, tpc=0):
     torch = _torch()
     act = x.dtype
     dev = x.device
@@ -434,7 +438,7 @@ def _bwd(x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D, ckpt, d_gat
     N = Bm.shape[-1]
     W = conv_w.shape[-1]
     dims = make_dims(Bsz, T, Dn, d_state=N, d_conv=W, chunk=chunk, segments=segments,
-                     accumulate_param_grads=accumulate_param_grads)
+                     accumulate_param_grads=accumulate_param_grads, bwd_threads_per_channel=tpc)
     code = _act_code(x)
     pl = m3scan_plan(dims, code)
     o = dict(out or {})
@@ -502,7 +506,8 @@ def m3scan_decode(x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D, ss
 def m3scan_bwd_two_phase(x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D, ckpt,
                          d_gated, du_extra_fn=None, *, conv_state=None, d_ssm_state_out=None,
                          d_conv_state_out=None, chunk=0, segments=0, bc_stride=0, dbc_stride=0,
-                         dB=None, dC=None, accumulate_param_grads=False, stream=None):
+                         dB=None, dC=None, accumulate_param_grads=False, stream=None,
+                         bwd_threads_per_channel=0):
     """The two-phase backward: m3scan_bwd_scan, then ``du_extra_fn(grads)``
     (the caller's x_proj/dt_proj GEMMs, given the scan's gradients; may
     return None), then m3scan_conv_bwd.  ``Bm``/``Cm`` may be column views
@@ -517,7 +522,7 @@ def m3scan_bwd_two_phase(x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log
     N, W = 16, conv_w.shape[-1]
     dims = make_dims(Bsz, T, Dn, d_state=N, d_conv=W, chunk=chunk, segments=segments,
                      accumulate_param_grads=accumulate_param_grads, bc_stride=bc_stride,
-                     dbc_stride=dbc_stride)
+                     dbc_stride=dbc_stride, bwd_threads_per_channel=bwd_threads_per_channel)
     code = _act_code(x)
     pl = m3scan_plan(dims, code)
     ws = Workspace(pl.workspace_bytes, dev)

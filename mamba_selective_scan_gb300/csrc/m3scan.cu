@@ -151,6 +151,18 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float2 (&v)[NS / 2]) {
         "=f"(v[3].x), "=f"(v[3].y), "=f"(v[4].x), "=f"(v[4].y), "=f"(v[5].x), "=f"(v[5].y),
         "=f"(v[6].x), "=f"(v[6].y), "=f"(v[7].x), "=f"(v[7].y) : "r"(taddr) : "memory");
 }
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const float2 (&v)[4]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
+      ::"r"(taddr), "f"(v[0].x), "f"(v[0].y), "f"(v[1].x), "f"(v[1].y), "f"(v[2].x), "f"(v[2].y),
+      "f"(v[3].x), "f"(v[3].y) : "memory");
+}
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float2 (&v)[4]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+      : "=f"(v[0].x), "=f"(v[0].y), "=f"(v[1].x), "=f"(v[1].y), "=f"(v[2].x), "=f"(v[2].y),
+        "=f"(v[3].x), "=f"(v[3].y) : "r"(taddr) : "memory");
+}
 // Programmatic dependent launch: a kernel launched with programmatic stream
 // serialization may start while the kernel before it in the stream is still
 // running; grid_dep_wait() returns once that kernel has completed and its
@@ -293,6 +305,34 @@ __host__ __device__ inline BwdSmem bwd_smem(int K, int es) {
   s.scal = s.fC + (size_t)K * NS * 4;
   s.red = s.scal + (size_t)2 * K * GB * 16;
   s.total = s.red + (size_t)K * NWB * 32 * 4;
+  return s;
+}
+
+// Backward with two threads per channel (64 channels per block): the same
+// staging buffers for 64 channels; per-step scalars s0/s1 [K][64] float4
+// shared by the two threads of a channel; the conv-input gradient of the
+// chunk's steps and of the next chunk's first three, dcs[K+3][64]; per-warp
+// dB/dC sums red[K][4][32].
+constexpr int GP = 64;  // channels per block in the two-thread backward
+struct Bwd2Smem {
+  size_t x, dr, z, dg, Bt, Ct, ck, tile, fB, fC, scal, dcs, red, total;
+};
+__host__ __device__ inline Bwd2Smem bwd2_smem(int K, int es) {
+  Bwd2Smem s;
+  s.x = 0;
+  s.dr = s.x + align_up((size_t)(K + 3) * GP * es, 128);
+  s.z = s.dr + align_up((size_t)K * GP * es, 128);
+  s.dg = s.z + align_up((size_t)K * GP * es, 128);
+  s.Bt = s.dg + align_up((size_t)K * GP * es, 128);
+  s.Ct = s.Bt + align_up((size_t)K * NS * es, 128);
+  s.ck = s.Ct + align_up((size_t)K * NS * es, 128);
+  s.tile = s.ck + (size_t)NS * GP * 4;
+  s.fB = 2 * s.tile;
+  s.fC = s.fB + (size_t)K * NS * 4;
+  s.scal = s.fC + (size_t)K * NS * 4;
+  s.dcs = s.scal + (size_t)2 * K * GP * 16;
+  s.red = s.dcs + align_up((size_t)(K + 3) * GP * 4, 128);
+  s.total = s.red + (size_t)K * 4 * 32 * 4;
   return s;
 }
 
@@ -1084,6 +1124,392 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(BwdArgs a) {
   if (warp == 0) tmem_dealloc(tmem_slot, a.tcols);
 }
 
+// ---------------------------------------------------------------------------
+// backward main kernel, two threads per channel (64 channels per block): the
+// thread pair of a channel splits its 16 state lanes (8 each) and takes the
+// per-step scalar work of alternate steps, so each thread runs about half
+// the per-step instructions and a block holds twice the warps per channel.
+// Same results as m3_bwd_kernel up to the order of f32 sums.
+// ---------------------------------------------------------------------------
+
+// Sum over the 16 channels of a warp (the lanes with the same lane & 1) of
+// 8 values held as 4 pairs, pair P holding this thread's lane pair
+// P ^ ((lane >> 3) & 3); returns the total for pair (lane >> 3) & 3, element
+// (lane >> 2) & 1 (lanes differing only in bit 1 return the same total).
+__device__ __forceinline__ float warp_sum8_rotated(float2 (&v)[4], int lane) {
+  v[0].x += __shfl_xor_sync(0xffffffffu, v[2].x, 16);
+  v[0].y += __shfl_xor_sync(0xffffffffu, v[2].y, 16);
+  v[1].x += __shfl_xor_sync(0xffffffffu, v[3].x, 16);
+  v[1].y += __shfl_xor_sync(0xffffffffu, v[3].y, 16);
+  v[0].x += __shfl_xor_sync(0xffffffffu, v[1].x, 8);
+  v[0].y += __shfl_xor_sync(0xffffffffu, v[1].y, 8);
+  const bool up = (lane & 4) != 0;
+  const float send = up ? v[0].x : v[0].y;
+  const float keep = up ? v[0].y : v[0].x;
+  const float r = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+  return r + __shfl_xor_sync(0xffffffffu, r, 2);
+}
+
+template <typename T, bool ST, bool SCAN>
+__global__ void __launch_bounds__(128, 4) m3_bwd2_kernel(BwdArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const Geo g = a.g;
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  const int hf = tid & 1;            // this thread's state lanes: 8 hf .. 8 hf + 7
+  const int ch = tid >> 1;           // channel within the block
+  const int prot = (lane >> 3) & 3;  // pair rotation for the warp reduction
+  const int d0 = blockIdx.x * GP;
+  const int s = blockIdx.y;
+  const int b = blockIdx.z;
+  const int d = d0 + ch;
+  const bool active = d < g.D;
+  const int c_begin = s * g.m;
+  const int c_end = min(c_begin + g.m, g.nc);
+  const int t_begin = c_begin * g.K;
+  const int t_end = min(c_end * g.K, g.T);
+  const int K = g.K;
+  const Bwd2Smem L = bwd2_smem(K, sizeof(T));
+  float* fB = reinterpret_cast<float*>(smem + L.fB);
+  float* fC = reinterpret_cast<float*>(smem + L.fC);
+  float* red = reinterpret_cast<float*>(smem + L.red);
+  float* dcs = reinterpret_cast<float*>(smem + L.dcs);  // [K + 3][GP]
+  // state lane of register pair P
+  auto lane_of = [&](int P) { return 8 * hf + 2 * (P ^ prot); };
+
+  // recomputed states of a chunk: row j of this thread = TMEM columns
+  // [8 j, 8 j + 8) of its lane; warp 0 allocates, every exit deallocates
+  __shared__ uint32_t tmem_slot;
+  if (warp == 0) tmem_alloc(&tmem_slot, a.tcols);
+  tmem_fence_before_sync();
+  __syncthreads();
+  tmem_fence_after_sync();
+  const uint32_t trow = tmem_slot + ((uint32_t)(warp * 32) << 16);
+
+  float2 a2[4];
+  float w[WC];
+  float cb = 0.f, dtb = 0.f, Dd = 0.f;
+#pragma unroll
+  for (int P = 0; P < 4; ++P) {
+    const int n = lane_of(P);
+    a2[P].x = active ? -expf(a.a_log[(size_t)d * NS + n]) * LOG2E : 0.f;
+    a2[P].y = active ? -expf(a.a_log[(size_t)d * NS + n + 1]) * LOG2E : 0.f;
+  }
+#pragma unroll
+  for (int k = 0; k < WC; ++k) w[k] = active ? a.conv_w[(size_t)d * WC + k] : 0.f;
+  if (active) {
+    cb = a.conv_b[d];
+    dtb = a.dt_bias[d];
+    Dd = a.Dp[d];
+  }
+  float2 carry[4];
+#pragma unroll
+  for (int P = 0; P < 4; ++P) carry[P] = make_float2(0.f, 0.f);
+  if (ST && a.g_h && active) {
+    const float* gh = a.g_h + (size_t)b * NS * g.D + d;
+#pragma unroll
+    for (int P = 0; P < 4; ++P) {
+      const int n = lane_of(P);
+      carry[P] = make_float2(gh[(size_t)n * g.D], gh[(size_t)(n + 1) * g.D]);
+    }
+  }
+  const T* xg = static_cast<const T*>(a.x);
+  auto stage = [&](int c, int buf) {
+    unsigned char* base = smem + (size_t)buf * L.tile;
+    const int t0 = c * K;
+    stage_rows<T, GP, 128>(reinterpret_cast<T*>(base + L.x), xg, b, t0 - 3, K + 3, g.T, g.T, g.D, d0, tid);
+    stage_rows<T, GP, 128>(reinterpret_cast<T*>(base + L.dr), static_cast<const T*>(a.dr), b, t0, K, g.T, g.T, g.D, d0, tid);
+    stage_rows<T, GP, 128>(reinterpret_cast<T*>(base + L.z), static_cast<const T*>(a.z), b, t0, K, g.T, g.T, g.D, d0, tid);
+    stage_rows<T, GP, 128>(reinterpret_cast<T*>(base + L.dg), static_cast<const T*>(a.dg), b, t0, K, g.T, g.T, g.D, d0, tid);
+    stage_bc<T, 128>(reinterpret_cast<T*>(base + L.Bt), static_cast<const T*>(a.Bm), b, t0, K, g.T, g.T, g.ldbc, tid);
+    stage_bc<T, 128>(reinterpret_cast<T*>(base + L.Ct), static_cast<const T*>(a.Cm), b, t0, K, g.T, g.T, g.ldbc, tid);
+    stage_rows<float, GP, 128>(reinterpret_cast<float*>(base + L.ck), a.ckpt + ((size_t)b * g.nc + c) * NS * g.D,
+                               0, 0, NS, NS, NS, g.D, d0, tid);
+    cp_async_commit();
+  };
+  stage(c_end - 1, 0);
+  grid_dep_trigger();
+  grid_dep_wait();
+  if (s + 1 < g.S) {
+    const float* __restrict__ sd = a.sd;
+    const float* __restrict__ q = a.q;
+#pragma unroll 2
+    for (int sp = g.S - 1; sp > s; --sp) {
+      const size_t bs = (size_t)b * g.S + sp;
+      const float2 dl2 = f2b(active ? sd[bs * g.D + d] : 0.f);
+#pragma unroll
+      for (int P = 0; P < 4; ++P) {
+        const float* qq = q + (bs * NS + lane_of(P)) * g.D + d;
+        const float2 loc = active ? make_float2(qq[0], qq[g.D]) : make_float2(0.f, 0.f);
+        carry[P] = __ffma2_rn(ex2x2(__fmul2_rn(dl2, a2[P])), carry[P], loc);
+      }
+    }
+  }
+  float2 dAp[4];
+#pragma unroll
+  for (int P = 0; P < 4; ++P) dAp[P] = make_float2(0.f, 0.f);
+  float dD_acc = 0.f, ddtb_acc = 0.f, dcb_acc = 0.f;
+  float dcw[WC] = {0.f, 0.f, 0.f, 0.f};
+  for (int i = tid; i < (K + 3) * GP; i += 128) dcs[i] = 0.f;  // ordered by the loop's first barrier
+
+  for (int c = c_end - 1; c >= c_begin; --c) {
+    const int buf = (c_end - 1 - c) & 1;
+    if (c - 1 >= c_begin) {
+      stage(c - 1, buf ^ 1);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();
+    const unsigned char* base = smem + (size_t)buf * L.tile;
+    if (ST && a.conv_in && c * K < 3 && active && hf == 0) {
+      T* xw = reinterpret_cast<T*>(smem + (size_t)buf * L.tile + L.x);
+      const T* ci = static_cast<const T*>(a.conv_in) + (size_t)b * 3 * g.D + d;
+      for (int r = 0; r < 3 - c * K; ++r) xw[r * GP + ch] = ci[(size_t)(c * K + r) * g.D];
+    }
+    {
+      const T* Bt = reinterpret_cast<const T*>(base + L.Bt);
+      const T* Ct = reinterpret_cast<const T*>(base + L.Ct);
+      for (int i = tid; i < K * NS; i += 128) {
+        fB[i] = Act<T>::ld(Bt + i);
+        fC[i] = Act<T>::ld(Ct + i);
+      }
+    }
+    __syncthreads();
+    const T* xt = reinterpret_cast<const T*>(base + L.x);  // row r is step c*K - 3 + r
+    const T* drt = reinterpret_cast<const T*>(base + L.dr);
+    const T* zt = reinterpret_cast<const T*>(base + L.z);
+    const T* dgt = reinterpret_cast<const T*>(base + L.dg);
+    const float* ckt = reinterpret_cast<const float*>(base + L.ck);
+    const int steps = min(K, g.T - c * K);
+    float4* s0 = reinterpret_cast<float4*>(smem + L.scal) + ch;  // shared by the pair, stride GP
+    float4* s1 = s0 + (size_t)K * GP;
+    const size_t row0 = ((size_t)b * g.T + (size_t)c * K) * g.D + d;
+
+    // ---- scalar pass, steps of this thread's parity ----
+    for (int j = hf; j < steps; j += 2) {
+      const float xm3 = Act<T>::ld(xt + j * GP + ch);
+      const float xm2 = Act<T>::ld(xt + (j + 1) * GP + ch);
+      const float xm1 = Act<T>::ld(xt + (j + 2) * GP + ch);
+      const float xv = Act<T>::ld(xt + (j + 3) * GP + ch);
+      const float cpre = fmaf(w[0], xm3, fmaf(w[1], xm2, fmaf(w[2], xm1, fmaf(w[3], xv, cb))));
+      const float sc = sigmoid_f(cpre);
+      const float u = cpre * sc;
+      const float v = Act<T>::ld(drt + j * GP + ch) + dtb;
+      const float delta = softplus_f(v);
+      const float sv = sigmoid_f(v);
+      const float zv = Act<T>::ld(zt + j * GP + ch);
+      const float gv = Act<T>::ld(dgt + j * GP + ch);
+      const float sz = sigmoid_f(zv);
+      s0[j * GP] = make_float4(delta, delta * u, gv * zv * sz, gv * (sz * fmaf(zv, 1.f - sz, 1.f)));
+      s1[j * GP] = make_float4(Dd * u, sv, sc, cpre);
+    }
+    __syncwarp();
+
+    // ---- recompute this thread's 8 lanes of the chunk's states ----
+    {
+      float2 h[4];
+#pragma unroll
+      for (int P = 0; P < 4; ++P) {
+        const int n = lane_of(P);
+        h[P] = make_float2(ckt[n * GP + ch], ckt[(n + 1) * GP + ch]);
+      }
+#pragma unroll 2
+      for (int j = 0; j < steps; ++j) {
+        const float4 v0 = s0[j * GP];
+        const float2 dl2 = f2b(v0.x);
+        const float2 du2 = f2b(v0.y);
+#pragma unroll
+        for (int P = 0; P < 4; ++P) {
+          const float2 bb = *reinterpret_cast<const float2*>(fB + j * NS + lane_of(P));
+          h[P] = __ffma2_rn(ex2x2(__fmul2_rn(dl2, a2[P])), h[P], __fmul2_rn(du2, bb));
+        }
+        tmem_st8(trow + 8u * (uint32_t)j, h);
+      }
+      tmem_wait_st();
+    }
+
+    // ---- reverse-time pass ----
+    {
+      float2 hn[4];
+      tmem_ld8(trow + 8u * (uint32_t)(steps - 1), hn);
+      tmem_wait_ld();
+#pragma unroll 2
+      for (int j = steps - 1; j >= 0; --j) {
+        const float4 v0 = s0[j * GP];
+        const float Du = reinterpret_cast<const float*>(s1 + j * GP)[0];
+        const float2 dl2 = f2b(v0.x);
+        const float2 du2 = f2b(v0.y);
+        const float2 dy2 = f2b(v0.z);
+        float2 sB = make_float2(0.f, 0.f), sAq = make_float2(0.f, 0.f), y2 = make_float2(0.f, 0.f);
+        float2 pB[4], pC[4], hp[4];
+        if (j > 0) {
+          tmem_ld8(trow + 8u * (uint32_t)(j - 1), hp);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int P = 0; P < 4; ++P) {
+            const int n = lane_of(P);
+            hp[P] = make_float2(ckt[n * GP + ch], ckt[(n + 1) * GP + ch]);
+          }
+        }
+#pragma unroll
+        for (int P = 0; P < 4; ++P) {
+          const float2 bb = *reinterpret_cast<const float2*>(fB + j * NS + lane_of(P));
+          const float2 cc = *reinterpret_cast<const float2*>(fC + j * NS + lane_of(P));
+          y2 = __ffma2_rn(cc, hn[P], y2);
+          const float2 dh = __ffma2_rn(dy2, cc, carry[P]);
+          pC[P] = __fmul2_rn(dy2, hn[P]);
+          pB[P] = __fmul2_rn(dh, du2);
+          sB = __ffma2_rn(dh, bb, sB);
+          carry[P] = __fmul2_rn(ex2x2(__fmul2_rn(dl2, a2[P])), dh);
+          const float2 qv = __fmul2_rn(carry[P], hp[P]);
+          dAp[P] = __ffma2_rn(dl2, qv, dAp[P]);
+          sAq = __ffma2_rn(a2[P], qv, sAq);
+        }
+#pragma unroll
+        for (int P = 0; P < 4; ++P) hn[P] = hp[P];
+        float ys = y2.x + y2.y, sBs = sB.x + sB.y, sAs = sAq.x + sAq.y;
+        ys += __shfl_xor_sync(0xffffffffu, ys, 1);
+        sBs += __shfl_xor_sync(0xffffffffu, sBs, 1);
+        sAs += __shfl_xor_sync(0xffffffffu, sAs, 1);
+        if (hf == (j & 1)) {
+          if (active) Act<T>::st(static_cast<T*>(a.dz) + row0 + (size_t)j * g.D, (ys + Du) * v0.w);
+          reinterpret_cast<float*>(s0 + j * GP)[3] = sAs;
+          reinterpret_cast<float*>(s1 + j * GP)[0] = sBs;
+        }
+        const float rb = warp_sum8_rotated(pB, lane);
+        const float rc = warp_sum8_rotated(pC, lane);
+        if ((lane & 2) == 0) {
+          const int n = 8 * hf + 2 * prot + ((lane >> 2) & 1);
+          red[(j * 4 + warp) * 32 + n] = rb;
+          red[(j * 4 + warp) * 32 + 16 + n] = rc;
+        }
+      }
+    }
+    __syncwarp();
+
+    // ---- du, d delta, softplus and (unless SCAN) SiLU backward, this thread's steps ----
+    for (int j = hf; j < steps; j += 2) {
+      const int t = c * K + j;
+      const float4 v0 = s0[j * GP];
+      const float4 v1 = s1[j * GP];
+      const float delta = v0.x, dy = v0.z, sAq = v0.w;
+      const float sumB = v1.x, sv = v1.y, sc = v1.z, cpre = v1.w;
+      const float u = cpre * sc;
+      const float du = fmaf(dy, Dd, delta * sumB);
+      const float ddr = fmaf(u, sumB, LN2 * sAq) * sv;
+      dD_acc = fmaf(dy, u, dD_acc);
+      ddtb_acc += ddr;
+      if (active) {
+        Act<T>::st(static_cast<T*>(a.ddr) + row0 + (size_t)j * g.D, ddr);
+        if (a.du_dbg) Act<T>::st(static_cast<T*>(a.du_dbg) + row0 + (size_t)j * g.D, du);
+      }
+      if constexpr (SCAN) continue;
+      const float dc = du * (sc * fmaf(cpre, 1.f - sc, 1.f));
+      dcb_acc += dc;
+#pragma unroll
+      for (int k = 0; k < WC; ++k) dcw[k] = fmaf(dc, Act<T>::ld(xt + (j + k) * GP + ch), dcw[k]);
+      dcs[j * GP + ch] = dc;
+      if (active && s > 0 && t < t_begin + 3)
+        a.dchead[(((size_t)b * g.S + s) * 3 + (t - t_begin)) * g.D + d] = dc;
+    }
+    if constexpr (!SCAN) {
+      __syncwarp();
+      // ---- conv backward: d_x from the conv-input gradient of this and the next 3 steps ----
+      for (int j = hf; j < steps; j += 2) {
+        const int t = c * K + j;
+        float dxv = fmaf(dcs[j * GP + ch], w[3], fmaf(dcs[(j + 1) * GP + ch], w[2],
+                         fmaf(dcs[(j + 2) * GP + ch], w[1], dcs[(j + 3) * GP + ch] * w[0])));
+        if (ST && a.g_conv && t >= g.T - 3 && active)
+          dxv += Act<T>::ld(static_cast<const T*>(a.g_conv) + ((size_t)b * 3 + t - (g.T - 3)) * g.D + d);
+        if (active) {
+          if (s + 1 < g.S && t >= t_end - 3)
+            a.dxpart[(((size_t)b * g.S + s) * 3 + (t - (t_end - 3))) * g.D + d] = dxv;
+          else
+            Act<T>::st(static_cast<T*>(a.dx) + row0 + (size_t)j * g.D, dxv);
+        }
+      }
+      __syncwarp();
+      // the next chunk processed (the one before in time) reads the dc of
+      // this chunk's first three steps: rows 0..2 of this chunk followed by
+      // the carried rows (a chunk may be shorter than three steps), all
+      // read before any is overwritten
+      if (hf == 0) {
+        const float v0 = dcs[ch], v1 = dcs[GP + ch], v2 = dcs[2 * GP + ch];
+        dcs[K * GP + ch] = v0;
+        dcs[(K + 1) * GP + ch] = v1;
+        dcs[(K + 2) * GP + ch] = v2;
+      }
+    }
+
+    __syncthreads();
+    for (int i = tid; i < steps * 32; i += 128) {
+      const int j = i >> 5, l = i & 31;
+      float v = 0.f;
+#pragma unroll
+      for (int ww = 0; ww < 4; ++ww) v += red[(j * 4 + ww) * 32 + l];
+      float* dst = (l < NS ? a.dB : a.dC) + ((size_t)b * g.T + c * K + j) * g.lddbc + (l & (NS - 1));
+      atomicAdd(dst, v);
+    }
+    __syncthreads();
+  }
+
+  if (ST && s == 0 && active) {
+    if (a.d_h_in) {
+      float* dh0 = a.d_h_in + (size_t)b * NS * g.D + d;
+#pragma unroll
+      for (int P = 0; P < 4; ++P) {
+        const int n = lane_of(P);
+        dh0[(size_t)n * g.D] = carry[P].x;
+        dh0[(size_t)(n + 1) * g.D] = carry[P].y;
+      }
+    }
+    if (!SCAN && a.d_conv_in && hf == 0) {
+      // dc of steps 0, 1, 2 (zero past the sequence), kept in rows K.. K+2
+      const float f0 = dcs[K * GP + ch], f1 = dcs[(K + 1) * GP + ch], f2 = dcs[(K + 2) * GP + ch];
+      float v[3];
+      v[2] = fmaf(f0, w[2], fmaf(f1, w[1], f2 * w[0]));
+      v[1] = fmaf(f0, w[1], f1 * w[0]);
+      v[0] = f0 * w[0];
+      T* dci = static_cast<T*>(a.d_conv_in) + (size_t)b * 3 * g.D + d;
+#pragma unroll
+      for (int r = 0; r < 3; ++r) {
+        const int ro = r - g.T;
+        if (a.g_conv && ro >= 0)
+          v[r] += Act<T>::ld(static_cast<const T*>(a.g_conv) + ((size_t)b * 3 + ro) * g.D + d);
+        Act<T>::st(dci + (size_t)r * g.D, v[r]);
+      }
+    }
+  }
+  // the pair's per-step partial sums: each thread summed its own steps
+  dD_acc += __shfl_xor_sync(0xffffffffu, dD_acc, 1);
+  ddtb_acc += __shfl_xor_sync(0xffffffffu, ddtb_acc, 1);
+  dcb_acc += __shfl_xor_sync(0xffffffffu, dcb_acc, 1);
+#pragma unroll
+  for (int k = 0; k < WC; ++k) dcw[k] += __shfl_xor_sync(0xffffffffu, dcw[k], 1);
+  if (active) {
+    float* Pp = a.partials + ((size_t)b * g.S + s) * NPART * g.D;
+#pragma unroll
+    for (int P = 0; P < 4; ++P) {
+      const int n = lane_of(P);
+      Pp[(size_t)n * g.D + d] = dAp[P].x;
+      Pp[(size_t)(n + 1) * g.D + d] = dAp[P].y;
+    }
+    if (hf == 0) {
+      Pp[(size_t)16 * g.D + d] = dD_acc;
+      Pp[(size_t)17 * g.D + d] = ddtb_acc;
+      Pp[(size_t)18 * g.D + d] = dcb_acc;
+#pragma unroll
+      for (int k = 0; k < WC; ++k) Pp[(size_t)(19 + k) * g.D + d] = dcw[k];
+    }
+  }
+  tmem_fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem_slot, a.tcols);
+}
+
 // The backward's last kernel, two roles by block index.
 //  - blocks [0, nfin): parameter gradients, the per-(batch, segment) partials
 //    summed in a fixed order (32 outputs per block, rows split over its 8
@@ -1473,6 +1899,13 @@ __host__ inline uint32_t tmem_cols_for(int K) {
   return c;
 }
 
+// Tensor-memory columns of a two-thread-per-channel backward CTA: 8 per step.
+__host__ inline uint32_t tmem_cols2_for(int K) {
+  uint32_t c = 32;
+  while (c < (uint32_t)K * 8) c <<= 1;
+  return c;
+}
+
 // Largest chunk whose backward fits: 16 K tensor-memory columns <= 512 and
 // the shared-memory footprint within one block's limit.
 __host__ inline int kmax_for(int es) {
@@ -1488,6 +1921,15 @@ __host__ inline size_t bwd_launch_smem(int K, int es, int smem_per_sm) {
   const int max_ctas = 512 / (int)tmem_cols_for(K);
   size_t need = bwd_smem(K, es).total;
   const size_t floor_bytes = (size_t)smem_per_sm / (max_ctas + 1) + 1;  // > 1/(max+1) of the SM
+  if (need < floor_bytes) need = floor_bytes;
+  return align_up(need, 128);
+}
+
+// The same residency cap for the two-thread backward.
+__host__ inline size_t bwd2_launch_smem(int K, int es, int smem_per_sm) {
+  const int max_ctas = 512 / (int)tmem_cols2_for(K);
+  size_t need = bwd2_smem(K, es).total;
+  const size_t floor_bytes = (size_t)smem_per_sm / (max_ctas + 1) + 1;
   if (need < floor_bytes) need = floor_bytes;
   return align_up(need, 128);
 }
@@ -1533,8 +1975,10 @@ cudaError_t set_attrs() {
                              (int)agg_smem(es).total);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(m3_bwd_agg_kernel<T>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-  void (*const bwd_kernels[4])(BwdArgs) = {m3_bwd_kernel<T, false, false>, m3_bwd_kernel<T, true, false>,
-                                            m3_bwd_kernel<T, false, true>, m3_bwd_kernel<T, true, true>};
+  void (*const bwd_kernels[8])(BwdArgs) = {
+      m3_bwd_kernel<T, false, false>, m3_bwd_kernel<T, true, false>, m3_bwd_kernel<T, false, true>,
+      m3_bwd_kernel<T, true, true>, m3_bwd2_kernel<T, false, false>, m3_bwd2_kernel<T, true, false>,
+      m3_bwd2_kernel<T, false, true>, m3_bwd2_kernel<T, true, true>};
   for (auto k : bwd_kernels) {
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_CAP);
@@ -1604,6 +2048,7 @@ struct Plan {
   int ctile, cntiles;  // conv backward: steps per tile, tiles per sequence
   size_t c_part;
   int fwd_launches, bwd_launches;
+  int bwd_tpc;  // threads per channel in the backward's main kernel
 };
 
 // Segments of whole chunks; every segment but the last spans >= 4 steps so
@@ -1661,6 +2106,7 @@ m3_status validate_dims(const m3_dims* dm, m3_dtype act) {
   if (dm->bc_stride != 0 && dm->bc_stride < NS) return M3_ERR_DIMS;
   if (dm->dbc_stride != 0 && dm->dbc_stride < NS) return M3_ERR_DIMS;
   if (dm->bc_stride * (act == M3_BF16 ? 2 : 4) % 16 != 0) return M3_ERR_ALIGN;
+  if (dm->bwd_threads_per_channel < 0 || dm->bwd_threads_per_channel > 2) return M3_ERR_UNSUPPORTED;
   return M3_OK;
 }
 
@@ -1677,6 +2123,7 @@ m3_status make_plan(const m3_dims* dm, m3_dtype act, Plan* p) {
   const int groups_f = (p->D + GF - 1) / GF;
   const int groups_b = (p->D + GB - 1) / GB;
   int want_f = 1, want_b = 1;
+  int64_t wave_b = 3 * 152;  // one-thread backward blocks resident at once
   if (dm->segments > 0) {
     want_f = want_b = (int)dm->segments;
   } else if ((int64_t)p->B * p->T * p->D > 0) {
@@ -1685,6 +2132,8 @@ m3_status make_plan(const m3_dims* dm, m3_dtype act, Plan* p) {
       return M3_ERR_CUDA;
     want_f = choose_segments(p->nc, p->K, (int64_t)p->B * groups_f, (int64_t)sms * of, 2);
     want_b = choose_segments(p->nc, p->K, (int64_t)p->B * groups_b, (int64_t)sms * ob, 8);
+    wave_b = (int64_t)sms * 3;  // three resident one-thread blocks per SM (measured; the
+                                // occupancy query reports fewer)
   }
   if (p->nc == 0) {
     p->Sf = p->Sb = 1;
@@ -1736,6 +2185,13 @@ m3_status make_plan(const m3_dims* dm, m3_dtype act, Plan* p) {
   p->ws_bytes = fwd_total > bwd_total ? fwd_total : bwd_total;
   if (p->ws_bytes < 256) p->ws_bytes = 256;
   const bool empty = (size_t)p->B * p->T * p->D == 0;
+  // two threads per channel when the one-thread grid fills less than one
+  // wave (three blocks per SM on a 152-SM GPU, or the device's measured
+  // figure when the segments were chosen for it)
+  p->bwd_tpc = dm->bwd_threads_per_channel;
+  if (p->bwd_tpc == 0) {
+    p->bwd_tpc = (int64_t)p->B * groups_b * p->Sb <= wave_b ? 2 : 1;
+  }
   p->fwd_launches = empty ? 0 : (p->Sf > 1 ? 2 : 1);
   p->bwd_launches = empty ? 0 : (p->Sb > 1 ? 3 : 2);
   return M3_OK;
@@ -1793,12 +2249,20 @@ m3_status launch_bwd(const Plan& p, BwdArgs a, cudaStream_t st, int smem_per_sm,
     if (note(cudaMemset2DAsync(a.dB, pitch, 0, NS * 4, rows, st)) != cudaSuccess) return M3_ERR_CUDA;
     if (note(cudaMemset2DAsync(a.dC, pitch, 0, NS * 4, rows, st)) != cudaSuccess) return M3_ERR_CUDA;
   }
-  a.tcols = tmem_cols_for(p.K);
-  const size_t smem = bwd_launch_smem(p.K, sizeof(T), smem_per_sm);
   const bool with_state = a.conv_in || a.g_h || a.g_conv || a.d_h_in || a.d_conv_in;
-  void (*kern)(BwdArgs) = scan ? (with_state ? m3_bwd_kernel<T, true, true> : m3_bwd_kernel<T, false, true>)
-                               : (with_state ? m3_bwd_kernel<T, true, false> : m3_bwd_kernel<T, false, false>);
-  e = launch_k(kern, dim3(groups, p.Sb, p.B), GB, smem, st, p.Sb > 1, a);
+  if (p.bwd_tpc == 2) {
+    a.tcols = tmem_cols2_for(p.K);
+    const size_t smem = bwd2_launch_smem(p.K, sizeof(T), smem_per_sm);
+    void (*kern)(BwdArgs) = scan ? (with_state ? m3_bwd2_kernel<T, true, true> : m3_bwd2_kernel<T, false, true>)
+                                 : (with_state ? m3_bwd2_kernel<T, true, false> : m3_bwd2_kernel<T, false, false>);
+    e = launch_k(kern, dim3((p.D + GP - 1) / GP, p.Sb, p.B), 128, smem, st, p.Sb > 1, a);
+  } else {
+    a.tcols = tmem_cols_for(p.K);
+    const size_t smem = bwd_launch_smem(p.K, sizeof(T), smem_per_sm);
+    void (*kern)(BwdArgs) = scan ? (with_state ? m3_bwd_kernel<T, true, true> : m3_bwd_kernel<T, false, true>)
+                                 : (with_state ? m3_bwd_kernel<T, true, false> : m3_bwd_kernel<T, false, false>);
+    e = launch_k(kern, dim3(groups, p.Sb, p.B), GB, smem, st, p.Sb > 1, a);
+  }
   // parameter outputs: 16 d_a_log, dD, d_dt_bias (+ d_conv_b, 4 d_conv_w)
   const int nout = scan ? 18 : 23;
   const size_t nfin = ((size_t)nout * p.D + 31) / 32;                 // 32 outputs per block
@@ -1853,6 +2317,8 @@ m3_status m3scan_plan(const m3_dims* dims, m3_dtype act, m3_plan* out) {
   out->workspace_bytes = (int64_t)p.ws_bytes;
   out->fwd_launches = p.fwd_launches;
   out->bwd_launches = p.bwd_launches;
+  out->bwd_threads_per_channel = p.bwd_tpc;
+  out->reserved = 0;
   return M3_OK;
 }
 

@@ -28,10 +28,10 @@ def _need_gpu():
     build.build()
 
 
-def _case(batch, T, D, act, seed, chunk=0, segments=0, fwd_segments=None, slow=False):
+def _case(batch, T, D, act, seed, chunk=0, segments=0, fwd_segments=None, slow=False, tpc=0):
     inp = make_inputs(batch, T, D, act=act, seed=seed, slow_delta=slow)
     dev = to_device(inp)
-    gpu = run_gpu(dev, chunk=chunk, segments=segments, fwd_segments=fwd_segments)
+    gpu = run_gpu(dev, chunk=chunk, segments=segments, fwd_segments=fwd_segments, tpc=tpc)
     ref = run_oracle(inp)
     return inp, gpu, ref
 
@@ -56,10 +56,13 @@ SMALL = [
 
 
 @pytest.mark.parametrize("batch,T,D,act,chunk,segments", SMALL)
-def test_small_cases_match_oracle(batch, T, D, act, chunk, segments):
+@pytest.mark.parametrize("tpc", [1, 2])
+def test_small_cases_match_oracle(batch, T, D, act, chunk, segments, tpc):
+    """Both backward main kernels (one and two threads per channel)."""
     inp, gpu, ref = _case(batch, T, D, act, seed=batch * 1000 + T + D, chunk=chunk,
-                          segments=segments)
-    assert_close(compare(gpu, ref, act), f"B={batch} T={T} D={D} {act} K={chunk} S={segments}")
+                          segments=segments, tpc=tpc)
+    assert_close(compare(gpu, ref, act),
+                 f"B={batch} T={T} D={D} {act} K={chunk} S={segments} tpc={tpc}")
 
 
 def test_forward_checkpoints_match_oracle_states():

@@ -45,7 +45,7 @@ def _state_to_device(st, act):
 
 
 def _gpu(dev, sd, chunk, segments, use=("ssm_state", "conv_state", "d_ssm_state_out",
-                                         "d_conv_state_out")):
+                                         "d_conv_state_out"), tpc=0):
     s = {k: (sd[k] if k in use else None) for k in sd}
     gated, ckpt, y, h_out, c_out = binding.m3scan_fwd_state(
         dev["x"], dev["delta_raw"], dev["z"], dev["B"], dev["C"], dev["conv_w"], dev["conv_b"],
@@ -55,7 +55,7 @@ def _gpu(dev, sd, chunk, segments, use=("ssm_state", "conv_state", "d_ssm_state_
         dev["x"], dev["delta_raw"], dev["z"], dev["B"], dev["C"], dev["conv_w"], dev["conv_b"],
         dev["dt_bias"], dev["a_log"], dev["D"], ckpt, dev["d_gated"], conv_state=s["conv_state"],
         d_ssm_state_out=s["d_ssm_state_out"], d_conv_state_out=s["d_conv_state_out"],
-        chunk=chunk, segments=segments, want_du=True)
+        chunk=chunk, segments=segments, want_du=True, bwd_threads_per_channel=tpc)
     torch.cuda.synchronize()
     res = {"gated": to_np(gated), "y": to_np(y), "ssm_state_out": to_np(h_out),
            "conv_state_out": to_np(c_out), "ckpt": to_np(ckpt)}
@@ -98,14 +98,15 @@ CASES = [
 ]
 
 
+@pytest.mark.parametrize("tpc", [1, 2])
 @pytest.mark.parametrize("batch,T,D,act,chunk,segments", CASES)
-def test_state_in_and_out_match_oracle(batch, T, D, act, chunk, segments):
+def test_state_in_and_out_match_oracle(batch, T, D, act, chunk, segments, tpc):
     seed = 7 * batch + T + D
     inp = make_inputs(batch, T, D, act=act, seed=seed)
     st = make_state_inputs(batch, D, act=act, seed=seed)
-    gpu = _gpu(to_device(inp), _state_to_device(st, act), chunk, segments)
+    gpu = _gpu(to_device(inp), _state_to_device(st, act), chunk, segments, tpc=tpc)
     ref = _oracle(inp, st, ALL)
-    _check(gpu, ref, act, f"B{batch} T{T} D{D} {act} K{chunk} S{segments}")
+    _check(gpu, ref, act, f"B{batch} T{T} D{D} {act} K{chunk} S{segments} tpc{tpc}")
     assert np.array_equal(gpu["ckpt"][:, 0], st["ssm_state"])
 
 

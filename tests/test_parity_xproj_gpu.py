@@ -90,7 +90,8 @@ def test_strided_b_c_and_gradients_match_oracle(act, R, segments):
     (1, 2, 8, "f32", 0, 0, True),           # shorter than the conv
     (3, 37, 72, "bf16", 2, 4, True),
 ])
-def test_two_phase_backward_matches_oracle(batch, T, D, act, chunk, segments, state):
+@pytest.mark.parametrize("tpc", [1, 2])
+def test_two_phase_backward_matches_oracle(batch, T, D, act, chunk, segments, state, tpc):
     seed = batch + T + D + chunk
     inp = make_inputs(batch, T, D, act=act, seed=seed)
     dev = to_device(inp)
@@ -118,7 +119,8 @@ def test_two_phase_backward_matches_oracle(batch, T, D, act, chunk, segments, st
     o = binding.m3scan_bwd_two_phase(dev["x"], dev["delta_raw"], dev["z"], dev["B"], dev["C"],
                                      dev["conv_w"], dev["conv_b"], dev["dt_bias"], dev["a_log"],
                                      dev["D"], ckpt, dev["d_gated"], lambda g: du_extra_t,
-                                     chunk=chunk, segments=segments, **kw)
+                                     chunk=chunk, segments=segments,
+                                     bwd_threads_per_channel=tpc, **kw)
     torch.cuda.synchronize()
     okw = {}
     if state:
