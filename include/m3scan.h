@@ -83,11 +83,12 @@ typedef struct {
     int64_t segments;
     /* 1: param grads are added to the output buffers; 0: overwritten. */
     int32_t accumulate_param_grads;
-    /* Threads per channel in the backward's main kernel: 1 (16 state lanes
-       per thread, the most channels per SM), 2 (8 lanes per thread: half
-       the per-thread work, for grids that fill less than one wave), or 0 =
-       chosen from the grid size.  Same results up to the order of f32 sums. */
-    int32_t bwd_threads_per_channel;
+    /* Threads per channel in the forward's and the backward's main
+       kernels: 1 (16 state lanes per thread, the most channels per SM), 2
+       (8 lanes per thread: half the per-thread work, for grids that fill
+       less than one wave), or 0 = chosen per kernel from its grid size.
+       Same results up to the order of f32 sums. */
+    int32_t threads_per_channel;
     /* Row strides, in elements, between consecutive (batch, step) rows of
        Bm and Cm, and of dB and dC; 0 = d_state (dense).  A stride > d_state
        lets Bm/Cm be column slices of the x_proj output [batch, seq_len,
@@ -109,8 +110,8 @@ typedef struct {
     int64_t workspace_bytes;    /* size of the workspace both calls need */
     int32_t fwd_launches;       /* kernels one m3scan_fwd enqueues */
     int32_t bwd_launches;       /* kernels one m3scan_bwd enqueues (memsets excluded) */
-    int32_t bwd_threads_per_channel;  /* 1 or 2, as resolved */
-    int32_t reserved;
+    int32_t fwd_threads_per_channel;  /* 1 or 2, as resolved */
+    int32_t bwd_threads_per_channel;
 } m3_plan;
 
 /*

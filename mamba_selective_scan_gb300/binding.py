@@ -51,7 +51,7 @@ class M3Dims(ctypes.Structure):
                 ("d_conv", ctypes.c_int64), ("chunk", ctypes.c_int64),
                 ("segments", ctypes.c_int64),
                 ("accumulate_param_grads", ctypes.c_int32),
-                ("bwd_threads_per_channel", ctypes.c_int32),
+                ("threads_per_channel", ctypes.c_int32),
                 ("bc_stride", ctypes.c_int64), ("dbc_stride", ctypes.c_int64)]
 
 
@@ -60,7 +60,8 @@ class M3Plan(ctypes.Structure):
                 ("fwd_segments", ctypes.c_int64), ("bwd_segments", ctypes.c_int64),
                 ("ckpt_bytes", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64),
                 ("fwd_launches", ctypes.c_int32), ("bwd_launches", ctypes.c_int32),
-                ("bwd_threads_per_channel", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("fwd_threads_per_channel", ctypes.c_int32),
+                ("bwd_threads_per_channel", ctypes.c_int32)]
 
     def as_dict(self):
         return {k: getattr(self, k) for k, _ in self._fields_}
@@ -154,10 +155,10 @@ def load():
 
 def make_dims(batch, seq_len, d_inner, d_state=16, d_conv=4, chunk=0, segments=0,
               accumulate_param_grads=False, bc_stride=0, dbc_stride=0,
-              bwd_threads_per_channel=0) -> M3Dims:
+              threads_per_channel=0) -> M3Dims:
     return M3Dims(int(batch), int(seq_len), int(d_inner), int(d_state), int(d_conv),
                   int(chunk), int(segments), int(bool(accumulate_param_grads)),
-                  int(bwd_threads_per_channel), int(bc_stride), int(dbc_stride))
+                  int(threads_per_channel), int(bc_stride), int(dbc_stride))
 
 
 def m3scan_plan(dims: M3Dims, act: int) -> M3Plan:
@@ -322,16 +323,16 @@ def plan_for(x, chunk=0, segments=0):
 
 def m3scan_fwd(x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D, *, chunk=0,
                segments=0, gated=None, y_dbg=None, want_y=False, ckpt=None, workspace=None,
-               stream=None):
+               stream=None, threads_per_channel=0):
     """Forward of the layer core.  Returns (gated, ckpt, y_dbg or None)."""
     return _fwd(x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D, chunk, segments,
-                gated, y_dbg, want_y, ckpt, workspace, stream, None)[:3]
+                gated, y_dbg, want_y, ckpt, workspace, stream, None, threads_per_channel)[:3]
 
 
 def m3scan_fwd_state(x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D, *,
                      ssm_state=None, conv_state=None, chunk=0, segments=0, gated=None,
                      y_dbg=None, want_y=False, ckpt=None, ssm_state_out=None,
-                     conv_state_out=None, workspace=None, stream=None):
+                     conv_state_out=None, workspace=None, stream=None, threads_per_channel=0):
     """Forward of one window from a carried state (None = zero).  Returns
     (gated, ckpt, y_dbg or None, ssm_state_out [B,16,D] f32,
     conv_state_out [B,3,D] activation dtype)."""
@@ -349,12 +350,13 @@ def m3scan_fwd_state(x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D,
     st = M3FwdState(_ptr(ssm_state), _ptr(conv_state), _ptr(ssm_state_out),
                     _ptr(conv_state_out))
     gated, ckpt, y_dbg = _fwd(x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D, chunk,
-                              segments, gated, y_dbg, want_y, ckpt, workspace, stream, st)[:3]
+                              segments, gated, y_dbg, want_y, ckpt, workspace, stream, st,
+                              threads_per_channel)[:3]
     return gated, ckpt, y_dbg, ssm_state_out, conv_state_out
 
 
 def _fwd(x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D, chunk, segments, gated,
-         y_dbg, want_y, ckpt, workspace, stream, state):
+         y_dbg, want_y, ckpt, workspace, stream, state, tpc=0):
     torch = _torch()
     act = x.dtype
     dev = x.device
@@ -365,7 +367,7 @@ def _fwd(x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D, chunk, segm
         _check(t, n, torch.float32, dev)
     Bsz, T, Dn = x.shape
     dims = make_dims(Bsz, T, Dn, d_state=Bm.shape[-1], d_conv=conv_w.shape[-1], chunk=chunk,
-                     segments=segments)
+                     segments=segments, threads_per_channel=tpc)
     code = _act_code(x)
     pl = m3scan_plan(dims, code)
     if gated is None:
@@ -391,17 +393,17 @@ def _fwd(x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D, chunk, segm
 
 def m3scan_bwd(x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D, ckpt, d_gated, *,
                chunk=0, segments=0, want_du=False, accumulate_param_grads=False, out=None,
-               workspace=None, stream=None, bwd_threads_per_channel=0):
+               workspace=None, stream=None, threads_per_channel=0):
     """Backward of the layer core.  Returns a dict of gradients (tensors)."""
     return _bwd(x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D, ckpt, d_gated,
                 chunk, segments, want_du, accumulate_param_grads, out, workspace, stream, None,
-                bwd_threads_per_channel)
+                threads_per_channel)
 
 
 def m3scan_bwd_state(x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D, ckpt, d_gated,
                      *, conv_state=None, d_ssm_state_out=None, d_conv_state_out=None, chunk=0,
                      segments=0, want_du=False, accumulate_param_grads=False, out=None,
-                     workspace=None, stream=None, bwd_threads_per_channel=0):
+                     workspace=None, stream=None, threads_per_channel=0):
     """Backward of one window made by ``m3scan_fwd_state``.  Returns the
     gradients of ``m3scan_bwd`` plus ``d_ssm_state`` [B,16,D] f32 and
     ``d_conv_state`` [B,3,D] (activation dtype)."""
@@ -420,7 +422,7 @@ def m3scan_bwd_state(x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D,
                     _ptr(o["d_ssm_state"]), _ptr(o["d_conv_state"]))
     return _bwd(x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D, ckpt, d_gated,
                 chunk, segments, want_du, accumulate_param_grads, o, workspace, stream, st,
-                bwd_threads_per_channel)
+                threads_per_channel)
 
 
 def _bwd(x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D, ckpt, d_gated, chunk,
@@ -438,7 +440,7 @@ def _bwd(x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D, ckpt, d_gat
     N = Bm.shape[-1]
     W = conv_w.shape[-1]
     dims = make_dims(Bsz, T, Dn, d_state=N, d_conv=W, chunk=chunk, segments=segments,
-                     accumulate_param_grads=accumulate_param_grads, bwd_threads_per_channel=tpc)
+                     accumulate_param_grads=accumulate_param_grads, threads_per_channel=tpc)
     code = _act_code(x)
     pl = m3scan_plan(dims, code)
     o = dict(out or {})
@@ -507,7 +509,7 @@ def m3scan_bwd_two_phase(x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log
                          d_gated, du_extra_fn=None, *, conv_state=None, d_ssm_state_out=None,
                          d_conv_state_out=None, chunk=0, segments=0, bc_stride=0, dbc_stride=0,
                          dB=None, dC=None, accumulate_param_grads=False, stream=None,
-                         bwd_threads_per_channel=0):
+                         threads_per_channel=0):
     """The two-phase backward: m3scan_bwd_scan, then ``du_extra_fn(grads)``
     (the caller's x_proj/dt_proj GEMMs, given the scan's gradients; may
     return None), then m3scan_conv_bwd.  ``Bm``/``Cm`` may be column views
@@ -522,7 +524,7 @@ def m3scan_bwd_two_phase(x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log
     N, W = 16, conv_w.shape[-1]
     dims = make_dims(Bsz, T, Dn, d_state=N, d_conv=W, chunk=chunk, segments=segments,
                      accumulate_param_grads=accumulate_param_grads, bc_stride=bc_stride,
-                     dbc_stride=dbc_stride, bwd_threads_per_channel=bwd_threads_per_channel)
+                     dbc_stride=dbc_stride, threads_per_channel=threads_per_channel)
     code = _act_code(x)
     pl = m3scan_plan(dims, code)
     ws = Workspace(pl.workspace_bytes, dev)

@@ -279,6 +279,28 @@ __host__ __device__ inline FwdSmem fwd_smem(int es) {
   return s;
 }
 
+// Two-thread forward shared memory: two staging buffers {x: [TT+3][GP]
+// (three halo rows), delta_raw, z: [TT][GP]; B, C: [TT][16]}, float B and C
+// of the tile, and per-step scalars sc[SUB][GP] float4 shared by a pair.
+constexpr int GP = 64;  // channels per block of the two-thread kernels
+struct Fwd2Smem {
+  size_t x, dr, z, Bt, Ct, tile, fB, fC, sc, total;
+};
+__host__ __device__ inline Fwd2Smem fwd2_smem(int es) {
+  Fwd2Smem s;
+  s.x = 0;
+  s.dr = s.x + align_up((size_t)(TT + 3) * GP * es, 128);
+  s.z = s.dr + align_up((size_t)TT * GP * es, 128);
+  s.Bt = s.z + align_up((size_t)TT * GP * es, 128);
+  s.Ct = s.Bt + align_up((size_t)TT * NS * es, 128);
+  s.tile = s.Ct + align_up((size_t)TT * NS * es, 128);
+  s.fB = 2 * s.tile;
+  s.fC = s.fB + (size_t)TT * NS * 4;
+  s.sc = s.fC + (size_t)TT * NS * 4;
+  s.total = s.sc + (size_t)SUB * GP * 16;
+  return s;
+}
+
 // Backward shared memory: two staging buffers {x: [K+3][GB] (three halo rows
 // before the chunk), delta_raw, z, d_gated: [K][GB] act; B, C: [K][16] act;
 // the chunk's start state ck: [16][GB] f32}; B and C of the current chunk as
@@ -313,7 +335,6 @@ __host__ __device__ inline BwdSmem bwd_smem(int K, int es) {
 // shared by the two threads of a channel; the conv-input gradient of the
 // chunk's steps and of the next chunk's first three, dcs[K+3][64]; per-warp
 // dB/dC sums red[K][4][32].
-constexpr int GP = 64;  // channels per block in the two-thread backward
 struct Bwd2Smem {
   size_t x, dr, z, dg, Bt, Ct, ck, tile, fB, fC, scal, dcs, red, total;
 };
@@ -581,6 +602,228 @@ __global__ void __launch_bounds__(GF) m3_fwd_kernel(FwdArgs a) {
       ah[(size_t)(2 * i + 1) * g.D] = h[i].y;
     }
     a.agg_s[((size_t)b * g.S + s) * g.D + d] = sdelta;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// forward with two threads per channel (64 channels per block): the pair of
+// a channel splits its 16 state lanes (8 each), takes alternate steps of the
+// scalar pass and sums y with one shuffle.  For grids that fill less than
+// one wave; same results as m3_fwd_kernel up to the order of f32 sums.
+// ---------------------------------------------------------------------------
+
+template <typename T, bool FINAL>
+__global__ void __launch_bounds__(128) m3_fwd2_kernel(FwdArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const Geo g = a.g;
+  const int tid = threadIdx.x;
+  const int hf = tid & 1;   // this thread's state lanes: 8 hf .. 8 hf + 7
+  const int ch = tid >> 1;  // channel within the block
+  const int d0 = blockIdx.x * GP;
+  const int s = blockIdx.y;
+  const int b = blockIdx.z;
+  const int d = d0 + ch;
+  const bool active = d < g.D;
+  const int c_begin = s * g.m;
+  const int c_end = min(c_begin + g.m, g.nc);
+  const int t_begin = c_begin * g.K;
+  const int t_end = min(c_end * g.K, g.T);
+  const Fwd2Smem L = fwd2_smem(sizeof(T));
+  const T* xg = static_cast<const T*>(a.x);
+  float* fB = reinterpret_cast<float*>(smem + L.fB);
+  float* fC = reinterpret_cast<float*>(smem + L.fC);
+
+  // x is staged with the three steps before the tile (row r = step t0 - 3 + r)
+  auto stage = [&](int t0, int buf) {
+    unsigned char* base = smem + (size_t)buf * L.tile;
+    stage_rows<T, GP, 128>(reinterpret_cast<T*>(base + L.x), xg, b, t0 - 3, TT + 3, g.T, t_end, g.D, d0, tid);
+    stage_rows<T, GP, 128>(reinterpret_cast<T*>(base + L.dr), static_cast<const T*>(a.dr), b, t0, TT, g.T, t_end, g.D, d0, tid);
+    stage_bc<T, 128>(reinterpret_cast<T*>(base + L.Bt), static_cast<const T*>(a.Bm), b, t0, TT, g.T, t_end, g.ldbc, tid);
+    if (FINAL) {
+      stage_rows<T, GP, 128>(reinterpret_cast<T*>(base + L.z), static_cast<const T*>(a.z), b, t0, TT, g.T, t_end, g.D, d0, tid);
+      stage_bc<T, 128>(reinterpret_cast<T*>(base + L.Ct), static_cast<const T*>(a.Cm), b, t0, TT, g.T, t_end, g.ldbc, tid);
+    }
+    cp_async_commit();
+  };
+  stage(t_begin, 0);
+  if (!FINAL) grid_dep_trigger();
+
+  float2 a2[4];  // A log2(e) of lanes (8 hf + 2 P, 8 hf + 2 P + 1)
+#pragma unroll
+  for (int P = 0; P < 4; ++P) {
+    const int n = 8 * hf + 2 * P;
+    a2[P].x = active ? -expf(a.a_log[(size_t)d * NS + n]) * LOG2E : 0.f;
+    a2[P].y = active ? -expf(a.a_log[(size_t)d * NS + n + 1]) * LOG2E : 0.f;
+  }
+  float w[WC];
+#pragma unroll
+  for (int k = 0; k < WC; ++k) w[k] = active ? a.conv_w[(size_t)d * WC + k] : 0.f;
+  const float cb = active ? a.conv_b[d] : 0.f;
+  const float dtb = active ? a.dt_bias[d] : 0.f;
+  const float Dd = active ? a.Dp[d] : 0.f;
+
+  float2 h[4];
+#pragma unroll
+  for (int P = 0; P < 4; ++P) h[P] = make_float2(0.f, 0.f);
+  if (FINAL && a.h_in && active) {
+    const float* h0 = a.h_in + (size_t)b * NS * g.D + d;
+#pragma unroll
+    for (int P = 0; P < 4; ++P) {
+      const int n = 8 * hf + 2 * P;
+      h[P] = make_float2(h0[(size_t)n * g.D], h0[(size_t)(n + 1) * g.D]);
+    }
+  }
+  if (FINAL && s > 0) {
+    grid_dep_wait();  // the aggregate pass's outputs
+#pragma unroll 2
+    for (int sp = 0; sp < s; ++sp) {
+      const size_t bs = (size_t)b * g.S + sp;
+      const float2 dl2 = f2b(active ? a.agg_s[bs * g.D + d] : 0.f);
+#pragma unroll
+      for (int P = 0; P < 4; ++P) {
+        const float* ah = a.agg_h + (bs * NS + 8 * hf + 2 * P) * g.D + d;
+        const float2 loc = active ? make_float2(ah[0], ah[g.D]) : make_float2(0.f, 0.f);
+        h[P] = __ffma2_rn(ex2x2(__fmul2_rn(dl2, a2[P])), h[P], loc);
+      }
+    }
+  }
+  float sdelta = 0.f;
+  float4* scs = reinterpret_cast<float4*>(smem + L.sc) + ch;  // shared by the pair, stride GP
+  int kc = 0;  // steps left until the next checkpoint
+  for (int t0 = t_begin, it = 0; t0 < t_end; t0 += TT, ++it) {
+    const int buf = it & 1;
+    if (t0 + TT < t_end) {
+      stage(t0 + TT, buf ^ 1);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();
+    unsigned char* base = smem + (size_t)buf * L.tile;
+    if (a.conv_in && t0 < 3 && active && hf == 0) {
+      // halo rows before step 0 (staged as zeros): the carried conv inputs
+      T* xw = reinterpret_cast<T*>(base + L.x);
+      const T* ci = static_cast<const T*>(a.conv_in) + (size_t)b * 3 * g.D + d;
+      for (int r = 0; r < 3 - t0; ++r) xw[r * GP + ch] = ci[(size_t)(t0 + r) * g.D];
+    }
+    {
+      const T* Bt = reinterpret_cast<const T*>(base + L.Bt);
+      const T* Ct = reinterpret_cast<const T*>(base + L.Ct);
+      for (int i = tid; i < TT * NS; i += 128) {
+        fB[i] = Act<T>::ld(Bt + i);
+        if (FINAL) fC[i] = Act<T>::ld(Ct + i);
+      }
+    }
+    __syncthreads();
+    const T* xt = reinterpret_cast<const T*>(base + L.x);
+    const T* drt = reinterpret_cast<const T*>(base + L.dr);
+    const T* zt = reinterpret_cast<const T*>(base + L.z);
+    const int steps = min(TT, t_end - t0);
+    for (int j0 = 0; j0 < steps; j0 += SUB) {
+      const int ns = min(SUB, steps - j0);
+      // scalar pass, this thread's steps (alternate)
+#pragma unroll 2
+      for (int j = hf; j < ns; j += 2) {
+        const int r = j0 + j;
+        const float xm3 = Act<T>::ld(xt + r * GP + ch);
+        const float xm2 = Act<T>::ld(xt + (r + 1) * GP + ch);
+        const float xm1 = Act<T>::ld(xt + (r + 2) * GP + ch);
+        const float xv = Act<T>::ld(xt + (r + 3) * GP + ch);
+        const float cpre = fmaf(w[0], xm3, fmaf(w[1], xm2, fmaf(w[2], xm1, fmaf(w[3], xv, cb))));
+        const float u = cpre * sigmoid_f(cpre);
+        const float delta = softplus_f(Act<T>::ld(drt + r * GP + ch) + dtb);
+        float gz = 0.f;
+        if (FINAL) {
+          const float zv = Act<T>::ld(zt + r * GP + ch);
+          gz = zv * sigmoid_f(zv);
+        }
+        scs[j * GP] = make_float4(delta, delta * u, Dd * u, gz);
+      }
+      __syncwarp();
+      // state pass, both threads
+#pragma unroll 4
+      for (int j = 0; j < ns; ++j) {
+        if (FINAL) {
+          if (kc == 0) {
+            const int t = t0 + j0 + j;
+            if (active) {
+              float* ck = a.ckpt + (((size_t)b * g.nc + t / g.K) * NS + 8 * hf) * g.D + d;
+#pragma unroll
+              for (int P = 0; P < 4; ++P) {
+                ck[(size_t)(2 * P) * g.D] = h[P].x;
+                ck[(size_t)(2 * P + 1) * g.D] = h[P].y;
+              }
+            }
+            kc = g.K;
+          }
+          --kc;
+        }
+        const float4 v = scs[j * GP];
+        const float2 dl2 = f2b(v.x);
+        const float2 du2 = f2b(v.y);
+        const float* Bj = fB + (j0 + j) * NS + 8 * hf;
+        if (FINAL) {
+          const float* Cj = fC + (j0 + j) * NS + 8 * hf;
+          float2 y2 = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int P = 0; P < 4; ++P) {
+            const float2 bb = *reinterpret_cast<const float2*>(Bj + 2 * P);
+            const float2 cc = *reinterpret_cast<const float2*>(Cj + 2 * P);
+            h[P] = __ffma2_rn(ex2x2(__fmul2_rn(dl2, a2[P])), h[P], __fmul2_rn(du2, bb));
+            y2 = __ffma2_rn(cc, h[P], y2);
+          }
+          float y = y2.x + y2.y;
+          y += __shfl_xor_sync(0xffffffffu, y, 1);
+          y += v.z;
+          if (active && hf == (j & 1)) {
+            const size_t i = ((size_t)b * g.T + t0 + j0 + j) * g.D + d;
+            Act<T>::st(static_cast<T*>(a.gated) + i, y * v.w);
+            if (a.y_dbg) Act<T>::st(static_cast<T*>(a.y_dbg) + i, y);
+          }
+        } else {
+          sdelta += v.x;
+#pragma unroll
+          for (int P = 0; P < 4; ++P) {
+            const float2 bb = *reinterpret_cast<const float2*>(Bj + 2 * P);
+            h[P] = __ffma2_rn(ex2x2(__fmul2_rn(dl2, a2[P])), h[P], __fmul2_rn(du2, bb));
+          }
+        }
+      }
+      __syncwarp();  // this sub-tile's slots are read; the next one overwrites them
+    }
+    __syncthreads();
+  }
+  if (FINAL && s == g.S - 1 && active) {
+    if (a.h_out) {
+      float* ho = a.h_out + ((size_t)b * NS + 8 * hf) * g.D + d;
+#pragma unroll
+      for (int P = 0; P < 4; ++P) {
+        ho[(size_t)(2 * P) * g.D] = h[P].x;
+        ho[(size_t)(2 * P + 1) * g.D] = h[P].y;
+      }
+    }
+    if (a.conv_out && hf == 0) {  // the conv inputs of steps T-3 .. T-1
+      T* co = static_cast<T*>(a.conv_out) + (size_t)b * 3 * g.D + d;
+#pragma unroll
+      for (int r = 0; r < 3; ++r) {
+        const int t = g.T - 3 + r;
+        float v = 0.f;
+        if (t >= 0)
+          v = Act<T>::ld(xg + ((size_t)b * g.T + t) * g.D + d);
+        else if (a.conv_in)
+          v = Act<T>::ld(static_cast<const T*>(a.conv_in) + ((size_t)b * 3 + t + 3) * g.D + d);
+        Act<T>::st(co + (size_t)r * g.D, v);
+      }
+    }
+  }
+  if (!FINAL && active) {
+    float* ah = a.agg_h + (((size_t)b * g.S + s) * NS + 8 * hf) * g.D + d;
+#pragma unroll
+    for (int P = 0; P < 4; ++P) {
+      ah[(size_t)(2 * P) * g.D] = h[P].x;
+      ah[(size_t)(2 * P + 1) * g.D] = h[P].y;
+    }
+    if (hf == 0) a.agg_s[((size_t)b * g.S + s) * g.D + d] = sdelta;
   }
 }
 
@@ -2048,7 +2291,7 @@ struct Plan {
   int ctile, cntiles;  // conv backward: steps per tile, tiles per sequence
   size_t c_part;
   int fwd_launches, bwd_launches;
-  int bwd_tpc;  // threads per channel in the backward's main kernel
+  int fwd_tpc, bwd_tpc;  // threads per channel in the forward's and backward's main kernels
 };
 
 // Segments of whole chunks; every segment but the last spans >= 4 steps so
@@ -2106,7 +2349,7 @@ m3_status validate_dims(const m3_dims* dm, m3_dtype act) {
   if (dm->bc_stride != 0 && dm->bc_stride < NS) return M3_ERR_DIMS;
   if (dm->dbc_stride != 0 && dm->dbc_stride < NS) return M3_ERR_DIMS;
   if (dm->bc_stride * (act == M3_BF16 ? 2 : 4) % 16 != 0) return M3_ERR_ALIGN;
-  if (dm->bwd_threads_per_channel < 0 || dm->bwd_threads_per_channel > 2) return M3_ERR_UNSUPPORTED;
+  if (dm->threads_per_channel < 0 || dm->threads_per_channel > 2) return M3_ERR_UNSUPPORTED;
   return M3_OK;
 }
 
@@ -2124,6 +2367,7 @@ m3_status make_plan(const m3_dims* dm, m3_dtype act, Plan* p) {
   const int groups_b = (p->D + GB - 1) / GB;
   int want_f = 1, want_b = 1;
   int64_t wave_b = 3 * 152;  // one-thread backward blocks resident at once
+  int64_t wave_f = 5 * 152;  // one-thread forward blocks resident at once
   if (dm->segments > 0) {
     want_f = want_b = (int)dm->segments;
   } else if ((int64_t)p->B * p->T * p->D > 0) {
@@ -2134,6 +2378,7 @@ m3_status make_plan(const m3_dims* dm, m3_dtype act, Plan* p) {
     want_b = choose_segments(p->nc, p->K, (int64_t)p->B * groups_b, (int64_t)sms * ob, 8);
     wave_b = (int64_t)sms * 3;  // three resident one-thread blocks per SM (measured; the
                                 // occupancy query reports fewer)
+    wave_f = (int64_t)sms * of;
   }
   if (p->nc == 0) {
     p->Sf = p->Sb = 1;
@@ -2188,10 +2433,9 @@ m3_status make_plan(const m3_dims* dm, m3_dtype act, Plan* p) {
   // two threads per channel when the one-thread grid fills less than one
   // wave (three blocks per SM on a 152-SM GPU, or the device's measured
   // figure when the segments were chosen for it)
-  p->bwd_tpc = dm->bwd_threads_per_channel;
-  if (p->bwd_tpc == 0) {
-    p->bwd_tpc = (int64_t)p->B * groups_b * p->Sb <= wave_b ? 2 : 1;
-  }
+  p->fwd_tpc = p->bwd_tpc = dm->threads_per_channel;
+  if (p->fwd_tpc == 0) p->fwd_tpc = (int64_t)p->B * groups_f * p->Sf <= wave_f ? 2 : 1;
+  if (p->bwd_tpc == 0) p->bwd_tpc = (int64_t)p->B * groups_b * p->Sb <= wave_b ? 2 : 1;
   p->fwd_launches = empty ? 0 : (p->Sf > 1 ? 2 : 1);
   p->bwd_launches = empty ? 0 : (p->Sb > 1 ? 3 : 2);
   return M3_OK;
@@ -2225,6 +2469,15 @@ m3_status launch_fwd(const Plan& p, FwdArgs a, cudaStream_t st) {
   const size_t smem = fwd_smem(sizeof(T)).total;
   a.g = Geo{p.B, p.T, p.D, p.K, p.nc, p.Sf, p.mf, p.ldbc, p.lddbc};
   cudaError_t e = cudaSuccess;
+  if (p.fwd_tpc == 2) {
+    const int groups2 = (p.D + GP - 1) / GP;
+    const size_t smem2 = fwd2_smem(sizeof(T)).total;
+    if (p.Sf > 1) e = launch_k(m3_fwd2_kernel<T, false>, dim3(groups2, p.Sf - 1, p.B), 128, smem2, st, false, a);
+    if (e == cudaSuccess)
+      e = launch_k(m3_fwd2_kernel<T, true>, dim3(groups2, p.Sf, p.B), 128, smem2, st, p.Sf > 1, a);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    return note(e) == cudaSuccess ? M3_OK : M3_ERR_CUDA;
+  }
   if (p.Sf > 1) e = launch_k(m3_fwd_kernel<T, false>, dim3(groups, p.Sf - 1, p.B), GF, smem, st, false, a);
   if (e == cudaSuccess)
     e = launch_k(m3_fwd_kernel<T, true>, dim3(groups, p.Sf, p.B), GF, smem, st, p.Sf > 1, a);
@@ -2317,8 +2570,8 @@ m3_status m3scan_plan(const m3_dims* dims, m3_dtype act, m3_plan* out) {
   out->workspace_bytes = (int64_t)p.ws_bytes;
   out->fwd_launches = p.fwd_launches;
   out->bwd_launches = p.bwd_launches;
+  out->fwd_threads_per_channel = p.fwd_tpc;
   out->bwd_threads_per_channel = p.bwd_tpc;
-  out->reserved = 0;
   return M3_OK;
 }
 

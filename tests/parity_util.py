@@ -46,12 +46,12 @@ def run_gpu(dev, chunk=0, segments=0, want_debug=True, d_gated=None, fwd_segment
     gated, ckpt, y = binding.m3scan_fwd(dev["x"], dev["delta_raw"], dev["z"], dev["B"], dev["C"],
                                         dev["conv_w"], dev["conv_b"], dev["dt_bias"],
                                         dev["a_log"], dev["D"], chunk=chunk, segments=seg_f,
-                                        want_y=want_debug)
+                                        want_y=want_debug, threads_per_channel=tpc)
     g = dev["d_gated"] if d_gated is None else d_gated
     grads = binding.m3scan_bwd(dev["x"], dev["delta_raw"], dev["z"], dev["B"], dev["C"],
                                dev["conv_w"], dev["conv_b"], dev["dt_bias"], dev["a_log"],
                                dev["D"], ckpt, g, chunk=chunk, segments=segments,
-                               want_du=want_debug, bwd_threads_per_channel=tpc)
+                               want_du=want_debug, threads_per_channel=tpc)
     torch.cuda.synchronize()
     res = {"gated": to_np(gated), "ckpt": to_np(ckpt)}
     if y is not None:

@@ -299,15 +299,18 @@ def test_two_phase_entry_points_validate_before_any_launch(lib):
     assert conv(ws=16) == "M3_ERR_WORKSPACE"
 
 
-def test_backward_threads_per_channel_is_resolved_from_the_grid(lib):
+def test_threads_per_channel_are_resolved_from_the_grid(lib):
     def tpc(batch, T, D, seg, want=0, chunk=8):
         out = binding.M3Plan()
-        d = binding.make_dims(batch, T, D, chunk=chunk, segments=seg, bwd_threads_per_channel=want)
+        d = binding.make_dims(batch, T, D, chunk=chunk, segments=seg, threads_per_channel=want)
         st = lib.m3scan_plan(ctypes.byref(d), binding.M3_BF16, ctypes.byref(out))
-        return binding.STATUS[st] if st else out.bwd_threads_per_channel
-    # fewer one-thread blocks than one wave (3 x 152): two threads per channel
-    assert tpc(8, 128, 512, 8) == 2                 # 8 x 4 groups x 8 segments = 256 blocks
-    assert tpc(8, 2048, 1536, 12) == 1              # 8 x 12 x 12 = 1152 blocks
-    assert tpc(8, 2048, 1536, 12, want=2) == 2      # explicit choice wins
-    assert tpc(8, 128, 512, 8, want=1) == 1
+        return binding.STATUS[st] if st else (out.fwd_threads_per_channel,
+                                              out.bwd_threads_per_channel)
+    # grids under one wave of the one-thread kernels (5 forward, 3 backward
+    # blocks per SM of a 152-SM GPU) take two threads per channel
+    assert tpc(8, 128, 512, 8) == (2, 2)            # 8 x 4 groups x 8 segments = 256 blocks
+    assert tpc(8, 2048, 1536, 12) == (1, 1)         # 8 x 12 x 12 = 1152 blocks
+    assert tpc(8, 2048, 1536, 6) == (2, 1)          # 576 blocks: one forward wave, not backward
+    assert tpc(8, 2048, 1536, 12, want=2) == (2, 2)  # an explicit choice wins
+    assert tpc(8, 128, 512, 8, want=1) == (1, 1)
     assert tpc(8, 128, 512, 8, want=3) == "M3_ERR_UNSUPPORTED"

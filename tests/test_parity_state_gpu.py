@@ -50,12 +50,13 @@ def _gpu(dev, sd, chunk, segments, use=("ssm_state", "conv_state", "d_ssm_state_
     gated, ckpt, y, h_out, c_out = binding.m3scan_fwd_state(
         dev["x"], dev["delta_raw"], dev["z"], dev["B"], dev["C"], dev["conv_w"], dev["conv_b"],
         dev["dt_bias"], dev["a_log"], dev["D"], ssm_state=s["ssm_state"],
-        conv_state=s["conv_state"], chunk=chunk, segments=segments, want_y=True)
+        conv_state=s["conv_state"], chunk=chunk, segments=segments, want_y=True,
+        threads_per_channel=tpc)
     g = binding.m3scan_bwd_state(
         dev["x"], dev["delta_raw"], dev["z"], dev["B"], dev["C"], dev["conv_w"], dev["conv_b"],
         dev["dt_bias"], dev["a_log"], dev["D"], ckpt, dev["d_gated"], conv_state=s["conv_state"],
         d_ssm_state_out=s["d_ssm_state_out"], d_conv_state_out=s["d_conv_state_out"],
-        chunk=chunk, segments=segments, want_du=True, bwd_threads_per_channel=tpc)
+        chunk=chunk, segments=segments, want_du=True, threads_per_channel=tpc)
     torch.cuda.synchronize()
     res = {"gated": to_np(gated), "y": to_np(y), "ssm_state_out": to_np(h_out),
            "conv_state_out": to_np(c_out), "ckpt": to_np(ckpt)}

@@ -120,7 +120,7 @@ def test_two_phase_backward_matches_oracle(batch, T, D, act, chunk, segments, st
                                      dev["conv_w"], dev["conv_b"], dev["dt_bias"], dev["a_log"],
                                      dev["D"], ckpt, dev["d_gated"], lambda g: du_extra_t,
                                      chunk=chunk, segments=segments,
-                                     bwd_threads_per_channel=tpc, **kw)
+                                     threads_per_channel=tpc, **kw)
     torch.cuda.synchronize()
     okw = {}
     if state:
