@@ -834,15 +834,22 @@ __global__ void __launch_bounds__(128) m3_fwd2_kernel(FwdArgs a) {
 // and the summed step size (the segment's total decay).
 // ---------------------------------------------------------------------------
 
-template <typename T>
+// TPC threads per channel (1 or 2): with two, a block covers 64 channels,
+// each thread carries 8 of a channel's 16 lanes and the scalar pass of
+// alternate steps.
+template <typename T, int TPC>
 __global__ void __launch_bounds__(GB) m3_bwd_agg_kernel(BwdArgs a) {
+  constexpr int G = GB / TPC;        // channels per block
+  constexpr int NL = NS / TPC;       // state lanes per thread
   extern __shared__ __align__(128) unsigned char smem[];
   const Geo g = a.g;
   const int tid = threadIdx.x;
-  const int d0 = blockIdx.x * GB;
+  const int hf = tid % TPC;
+  const int ch = tid / TPC;
+  const int d0 = blockIdx.x * G;
   const int s = blockIdx.y + 1;
   const int b = blockIdx.z;
-  const int d = d0 + tid;
+  const int d = d0 + ch;
   const bool active = d < g.D;
   const int t_begin = s * g.m * g.K;
   const int t_end = min((s + 1) * g.m * g.K, g.T);
@@ -854,9 +861,9 @@ __global__ void __launch_bounds__(GB) m3_bwd_agg_kernel(BwdArgs a) {
     unsigned char* base = smem + (size_t)buf * L.tile;
     const int t0 = tile_start(i);
     const int rows = (t_end - i * TT) - t0;
-    stage_rows<T, GB, GB>(reinterpret_cast<T*>(base + L.dr), static_cast<const T*>(a.dr), b, t0, rows, g.T, g.T, g.D, d0, tid);
-    stage_rows<T, GB, GB>(reinterpret_cast<T*>(base + L.z), static_cast<const T*>(a.z), b, t0, rows, g.T, g.T, g.D, d0, tid);
-    stage_rows<T, GB, GB>(reinterpret_cast<T*>(base + L.dg), static_cast<const T*>(a.dg), b, t0, rows, g.T, g.T, g.D, d0, tid);
+    stage_rows<T, G, GB>(reinterpret_cast<T*>(base + L.dr), static_cast<const T*>(a.dr), b, t0, rows, g.T, g.T, g.D, d0, tid);
+    stage_rows<T, G, GB>(reinterpret_cast<T*>(base + L.z), static_cast<const T*>(a.z), b, t0, rows, g.T, g.T, g.D, d0, tid);
+    stage_rows<T, G, GB>(reinterpret_cast<T*>(base + L.dg), static_cast<const T*>(a.dg), b, t0, rows, g.T, g.T, g.D, d0, tid);
     stage_bc<T, GB>(reinterpret_cast<T*>(base + L.Ct), static_cast<const T*>(a.Cm), b, t0, rows, g.T, g.T, g.ldbc, tid);
     cp_async_commit();
   };
@@ -864,16 +871,17 @@ __global__ void __launch_bounds__(GB) m3_bwd_agg_kernel(BwdArgs a) {
   stage(0, 0);  // first tile in flight while the parameters load
   grid_dep_trigger();
 
-  float2 a2[NS / 2];
+  float2 a2[NL / 2];
 #pragma unroll
-  for (int i = 0; i < NS / 2; ++i) {
-    a2[i].x = active ? -expf(a.a_log[(size_t)d * NS + 2 * i]) * LOG2E : 0.f;
-    a2[i].y = active ? -expf(a.a_log[(size_t)d * NS + 2 * i + 1]) * LOG2E : 0.f;
+  for (int i = 0; i < NL / 2; ++i) {
+    const int n = NL * hf + 2 * i;
+    a2[i].x = active ? -expf(a.a_log[(size_t)d * NS + n]) * LOG2E : 0.f;
+    a2[i].y = active ? -expf(a.a_log[(size_t)d * NS + n + 1]) * LOG2E : 0.f;
   }
   const float dtb = active ? a.dt_bias[d] : 0.f;
-  float2 carry[NS / 2];
+  float2 carry[NL / 2];
 #pragma unroll
-  for (int i = 0; i < NS / 2; ++i) carry[i] = make_float2(0.f, 0.f);
+  for (int i = 0; i < NL / 2; ++i) carry[i] = make_float2(0.f, 0.f);
   float sdelta = 0.f;
 
   {
@@ -908,28 +916,25 @@ __global__ void __launch_bounds__(GB) m3_bwd_agg_kernel(BwdArgs a) {
     const T* drt = reinterpret_cast<const T*>(base + L.dr);
     const T* zt = reinterpret_cast<const T*>(base + L.z);
     const T* dgt = reinterpret_cast<const T*>(base + L.dg);
-    float2* scs = reinterpret_cast<float2*>(smem + L.sc) + tid;  // thread-private, stride GB
+    float2* scs = reinterpret_cast<float2*>(smem + L.sc) + ch;  // per channel, stride G
 #pragma unroll 4
-    for (int j = 0; j < steps; ++j) {  // scalar pass
-      const float zv = Act<T>::ld(zt + j * GB + tid);
-      const float dy = Act<T>::ld(dgt + j * GB + tid) * zv * sigmoid_f(zv);
-      const float delta = softplus_f(Act<T>::ld(drt + j * GB + tid) + dtb);
-      sdelta += delta;
-      scs[j * GB] = make_float2(delta, dy);
+    for (int j = hf; j < steps; j += TPC) {  // scalar pass
+      const float zv = Act<T>::ld(zt + j * G + ch);
+      const float dy = Act<T>::ld(dgt + j * G + ch) * zv * sigmoid_f(zv);
+      const float delta = softplus_f(Act<T>::ld(drt + j * G + ch) + dtb);
+      scs[j * G] = make_float2(delta, dy);
     }
+    if (TPC > 1) __syncwarp();
 #pragma unroll 4
     for (int j = steps - 1; j >= 0; --j) {  // state pass
-      const float2 v = scs[j * GB];
+      const float2 v = scs[j * G];
+      sdelta += v.x;
       const float2 dl2 = f2b(v.x);
       const float2 dy2 = f2b(v.y);
-      const float4* C4 = reinterpret_cast<const float4*>(fC + j * NS);
+      const float2* C2 = reinterpret_cast<const float2*>(fC + j * NS + NL * hf);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float4 c4 = C4[q];
-        carry[2 * q] = __fmul2_rn(ex2x2(__fmul2_rn(dl2, a2[2 * q])),
-                                  __ffma2_rn(dy2, make_float2(c4.x, c4.y), carry[2 * q]));
-        carry[2 * q + 1] = __fmul2_rn(ex2x2(__fmul2_rn(dl2, a2[2 * q + 1])),
-                                      __ffma2_rn(dy2, make_float2(c4.z, c4.w), carry[2 * q + 1]));
+      for (int q = 0; q < NL / 2; ++q) {
+        carry[q] = __fmul2_rn(ex2x2(__fmul2_rn(dl2, a2[q])), __ffma2_rn(dy2, C2[q], carry[q]));
       }
     }
     __syncthreads();
@@ -937,11 +942,11 @@ __global__ void __launch_bounds__(GB) m3_bwd_agg_kernel(BwdArgs a) {
   if (active) {
     const size_t bs = (size_t)b * g.S + s;
 #pragma unroll
-    for (int i = 0; i < NS / 2; ++i) {
-      a.q[(bs * NS + 2 * i) * g.D + d] = carry[i].x;
-      a.q[(bs * NS + 2 * i + 1) * g.D + d] = carry[i].y;
+    for (int i = 0; i < NL / 2; ++i) {
+      a.q[(bs * NS + NL * hf + 2 * i) * g.D + d] = carry[i].x;
+      a.q[(bs * NS + NL * hf + 2 * i + 1) * g.D + d] = carry[i].y;
     }
-    a.sd[bs * g.D + d] = sdelta;
+    if (hf == 0) a.sd[bs * g.D + d] = sdelta;
   }
 }
 
@@ -2214,10 +2219,15 @@ cudaError_t set_attrs() {
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(m3_fwd_kernel<T, false>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(m3_bwd_agg_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(m3_bwd_agg_kernel<T, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)agg_smem(es).total);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(m3_bwd_agg_kernel<T>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    e = cudaFuncSetAttribute(m3_bwd_agg_kernel<T, 1>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(m3_bwd_agg_kernel<T, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)agg_smem(es).total);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(m3_bwd_agg_kernel<T, 2>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   void (*const bwd_kernels[8])(BwdArgs) = {
       m3_bwd_kernel<T, false, false>, m3_bwd_kernel<T, true, false>, m3_bwd_kernel<T, false, true>,
       m3_bwd_kernel<T, true, true>, m3_bwd2_kernel<T, false, false>, m3_bwd2_kernel<T, true, false>,
@@ -2493,8 +2503,12 @@ m3_status launch_bwd(const Plan& p, BwdArgs a, cudaStream_t st, int smem_per_sm,
   cudaError_t e = cudaSuccess;
   if (p.Sb > 1) {
     // also clears dB and dC before the main kernel's reductions into them
-    e = launch_k(m3_bwd_agg_kernel<T>, dim3(groups, p.Sb - 1, p.B), GB, agg_smem(sizeof(T)).total,
-                 st, false, a);
+    if (p.bwd_tpc == 2)
+      e = launch_k(m3_bwd_agg_kernel<T, 2>, dim3((p.D + GP - 1) / GP, p.Sb - 1, p.B), GB,
+                   agg_smem(sizeof(T)).total, st, false, a);
+    else
+      e = launch_k(m3_bwd_agg_kernel<T, 1>, dim3(groups, p.Sb - 1, p.B), GB, agg_smem(sizeof(T)).total,
+                   st, false, a);
     if (note(e) != cudaSuccess) return M3_ERR_CUDA;
   } else {
     // only the 16 columns of each (batch, step) row belong to dB and dC
