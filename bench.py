@@ -432,54 +432,93 @@ def gpu_arm(args):
         print(json.dumps(line), flush=True)
 
 
+def _packed(torch, shapes, device, pin):
+    """One buffer holding every tensor of ``shapes`` (name -> (shape, dtype))
+    at 256-byte aligned offsets, and a view per name."""
+    offs, off = {}, 0
+    for k, (shape, dt) in shapes.items():
+        offs[k] = off
+        n = int(torch.Size(shape).numel()) * torch.empty((), dtype=dt).element_size()
+        off = (off + n + 255) // 256 * 256
+    buf = torch.empty(off, dtype=torch.uint8, device=device, pin_memory=pin)
+    views = {}
+    for k, (shape, dt) in shapes.items():
+        n = int(torch.Size(shape).numel()) * torch.empty((), dtype=dt).element_size()
+        views[k] = buf[offs[k]:offs[k] + n].view(dt).view(shape)
+    return buf, views
+
+
 def e2e_measure(torch, binding, layer, tensors, steps, device):
     """Same step through the public binding, with the step's inputs copied
-    from pinned host memory and its results copied back inside the events."""
+    from pinned host memory and its results copied back inside the events.
+    The inputs sit in one pinned host buffer (as a data loader would hand
+    over a batch) and the outputs come back into one, so a step is one
+    host-to-device copy, the forward and backward, and one device-to-host
+    copy.  Reported two ways: the step captured once as a CUDA graph and
+    replayed -- how a loop over small layers runs -- and the same calls
+    issued eagerly from Python every step."""
     ins = ("x", "delta_raw", "z", "B", "C", "d_gated", "conv_w", "conv_b", "dt_bias",
            "a_log", "D")
     outs = ("gated", "d_x", "d_delta_raw", "dz", "dB", "dC", "d_conv_w", "d_conv_b",
             "d_dt_bias", "d_a_log", "dD")
-    h_in = {k: tensors[k].cpu().pin_memory() for k in ins}
-    d_in = {k: torch.empty_like(tensors[k]) for k in ins}
-    h_out = {k: torch.empty(layer.o[k].shape, dtype=layer.o[k].dtype, pin_memory=True)
-             for k in outs}
-    bi = sum(v.numel() * v.element_size() for v in h_in.values())
-    bo = sum(v.numel() * v.element_size() for v in h_out.values())
+    in_shapes = {k: (tuple(tensors[k].shape), tensors[k].dtype) for k in ins}
+    out_shapes = {k: (tuple(layer.o[k].shape), layer.o[k].dtype) for k in outs}
+    h_in_buf, h_in = _packed(torch, in_shapes, "cpu", True)
+    d_in_buf, d_in = _packed(torch, in_shapes, device, False)
+    h_out_buf, _ = _packed(torch, out_shapes, "cpu", True)
+    d_out_buf, d_out = _packed(torch, out_shapes, device, False)
+    for k in ins:
+        h_in[k].copy_(tensors[k].cpu())
+    bi = h_in_buf.numel()
+    bo = h_out_buf.numel()
     ws = layer.ws
-    s = torch.cuda.current_stream()
     E = layer.shape[0] * layer.shape[1] * layer.shape[2]
 
-    def step():
-        for k in ins:
-            d_in[k].copy_(h_in[k], non_blocking=True)
-        gated, ckpt, _ = binding.m3scan_fwd(
+    def step(s):
+        d_in_buf.copy_(h_in_buf, non_blocking=True)
+        binding.m3scan_fwd(
             d_in["x"], d_in["delta_raw"], d_in["z"], d_in["B"], d_in["C"], d_in["conv_w"],
             d_in["conv_b"], d_in["dt_bias"], d_in["a_log"], d_in["D"], chunk=int(layer.plan.chunk),
-            gated=layer.o["gated"], ckpt=layer.o["ckpt"],
-            workspace=_WS(ws), stream=s)
-        g = binding.m3scan_bwd(
+            gated=d_out["gated"], ckpt=layer.o["ckpt"], workspace=_WS(ws), stream=s)
+        binding.m3scan_bwd(
             d_in["x"], d_in["delta_raw"], d_in["z"], d_in["B"], d_in["C"], d_in["conv_w"],
-            d_in["conv_b"], d_in["dt_bias"], d_in["a_log"], d_in["D"], ckpt, d_in["d_gated"],
-            chunk=int(layer.plan.chunk), out={k: layer.o[k] for k in outs if k != "gated"},
-            workspace=_WS(ws), stream=s)
-        h_out["gated"].copy_(gated, non_blocking=True)
-        for k in outs[1:]:
-            h_out[k].copy_(g[k], non_blocking=True)
+            d_in["conv_b"], d_in["dt_bias"], d_in["a_log"], d_in["D"], layer.o["ckpt"],
+            d_in["d_gated"], chunk=int(layer.plan.chunk),
+            out={k: d_out[k] for k in outs if k != "gated"}, workspace=_WS(ws), stream=s)
+        h_out_buf.copy_(d_out_buf, non_blocking=True)
 
-    for _ in range(3):
-        step()
+    def timed(run):
+        s = torch.cuda.current_stream()
+        for _ in range(3):
+            run()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for _ in range(steps):
+            run()
+        e1.record(s)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps
+
+    ms_eager = timed(lambda: step(torch.cuda.current_stream()))
+    side = torch.cuda.Stream(device)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        step(side)  # warm the plan cache on the capture stream
     torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(s)
-    for _ in range(steps):
-        step()
-    e1.record(s)
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1)
-    return {"value": round(E * steps / (ms * 1e-3) / 1e9, 3), "unit": UNIT,
+    with torch.cuda.graph(graph, stream=side):
+        step(side)
+    ms = timed(graph.replay)
+    return {"value": round(E / (ms * 1e-3) / 1e9, 3), "unit": UNIT,
             "h2d_bytes_per_step": int(bi), "d2h_bytes_per_step": int(bo),
-            "ms_per_step": round(ms / steps, 5), "steps": steps}
+            "ms_per_step": round(ms, 5), "steps": steps,
+            "how": "inputs in one pinned host buffer copied in, fwd + bwd through the binding, "
+                   "all outputs copied back into one pinned buffer; the step captured once as a "
+                   "CUDA graph and replayed",
+            "eager": {"value": round(E / (ms_eager * 1e-3) / 1e9, 3),
+                      "ms_per_step": round(ms_eager, 5),
+                      "how": "the same calls issued from Python every step"}}
 
 
 class _WS:
