@@ -144,9 +144,12 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float2 (&v)[NS /
       "f"(v[3].x), "f"(v[3].y), "f"(v[4].x), "f"(v[4].y), "f"(v[5].x), "f"(v[5].y), "f"(v[6].x),
       "f"(v[6].y), "f"(v[7].x), "f"(v[7].y) : "memory");
 }
+// Load and wait in one statement, so no use of the registers can be placed
+// between the asynchronous load and its completion.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float2 (&v)[NS / 2]) {
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
       : "=f"(v[0].x), "=f"(v[0].y), "=f"(v[1].x), "=f"(v[1].y), "=f"(v[2].x), "=f"(v[2].y),
         "=f"(v[3].x), "=f"(v[3].y), "=f"(v[4].x), "=f"(v[4].y), "=f"(v[5].x), "=f"(v[5].y),
         "=f"(v[6].x), "=f"(v[6].y), "=f"(v[7].x), "=f"(v[7].y) : "r"(taddr) : "memory");
@@ -159,7 +162,8 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const float2 (&v)[4]) {
 }
 __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float2 (&v)[4]) {
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
       : "=f"(v[0].x), "=f"(v[0].y), "=f"(v[1].x), "=f"(v[1].y), "=f"(v[2].x), "=f"(v[2].y),
         "=f"(v[3].x), "=f"(v[3].y) : "r"(taddr) : "memory");
 }
@@ -172,7 +176,6 @@ __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.w
 __device__ __forceinline__ void grid_dep_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // Stage rows [t_first, t_first + rows) x channels [d0, d0 + G) of a
 // [B, T_, D] tensor of element type T into dst[rows][G]; rows outside
@@ -1201,7 +1204,6 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(BwdArgs a) {
       {
         float2 hn[NS / 2];  // h_t (state after step t)
         tmem_ld16(trow + 16u * (uint32_t)(nst - 1), hn);
-        tmem_wait_ld();
 #pragma unroll 2
         for (int j = nst - 1; j >= 0; --j) {
           const float4 v0 = s0[j * GB];
@@ -1215,7 +1217,6 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(BwdArgs a) {
           float2 hp[NS / 2];  // h_{t-1}
           if (j > 0) {
             tmem_ld16(trow + 16u * (uint32_t)(j - 1), hp);
-            tmem_wait_ld();
           } else {
 #pragma unroll
             for (int i = 0; i < NS / 2; ++i) {
@@ -1582,7 +1583,6 @@ __global__ void __launch_bounds__(128, 4) m3_bwd2_kernel(BwdArgs a) {
     {
       float2 hn[4];
       tmem_ld8(trow + 8u * (uint32_t)(steps - 1), hn);
-      tmem_wait_ld();
 #pragma unroll 2
       for (int j = steps - 1; j >= 0; --j) {
         const float4 v0 = s0[j * GP];
@@ -1594,7 +1594,6 @@ __global__ void __launch_bounds__(128, 4) m3_bwd2_kernel(BwdArgs a) {
         float2 pB[4], pC[4], hp[4];
         if (j > 0) {
           tmem_ld8(trow + 8u * (uint32_t)(j - 1), hp);
-          tmem_wait_ld();
         } else {
 #pragma unroll
           for (int P = 0; P < 4; ++P) {
