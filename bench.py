@@ -181,13 +181,14 @@ class ClockSampler:
 class Layer:
     """Device buffers, plan and captured graphs for one layer-core instance."""
 
-    def __init__(self, torch, binding, tensors, chunk=0, segments=0):
+    def __init__(self, torch, binding, tensors, chunk=0, segments=0, threads_per_channel=0):
         self.t = tensors
         x = tensors["x"]
         self.act = binding.M3_BF16 if x.dtype == torch.bfloat16 else binding.M3_F32
         Bsz, T, D = x.shape
         self.shape = (Bsz, T, D)
-        self.dims = binding.make_dims(Bsz, T, D, chunk=chunk, segments=segments)
+        self.dims = binding.make_dims(Bsz, T, D, chunk=chunk, segments=segments,
+                                      threads_per_channel=threads_per_channel)
         self.plan = binding.m3scan_plan(self.dims, self.act)
         dev = x.device
         f32 = dict(dtype=torch.float32, device=dev)
@@ -743,9 +744,19 @@ def main():
     ap.add_argument("--no-stack", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--decode-only", action="store_true",
+                    help="run only the one-token decode measurements (for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.decode_only:
+        import torch
+        from mamba_selective_scan_gb300 import binding, build
+        build.build()
+        dev = torch.device("cuda", 0)
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        print(json.dumps({"decode": decode_extras(torch, binding, dev, flush, steps=args.steps)}))
+        return
     if args.impl == "reference":
         reference_arm(args)
     else:

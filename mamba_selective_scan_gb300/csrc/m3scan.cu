@@ -1855,70 +1855,100 @@ struct ConvArgs {
   int accumulate;
 };
 
+// Steps per conv-backward tile: rows [t0 - 3, t0 + CT + 3) of x and
+// [t0, t0 + CT + 3) of du and du_extra are staged in shared memory by 16-byte
+// copies, so each thread's walk over the tile reads no global memory.
+constexpr int CT = 32;
+struct ConvSmem {
+  size_t x, du, de, total;
+};
+__host__ __device__ inline ConvSmem conv_smem(int es) {
+  ConvSmem s;
+  s.x = 0;
+  s.du = align_up((size_t)(CT + 6) * 128 * es, 128);
+  s.de = s.du + align_up((size_t)(CT + 3) * 128 * es, 128);
+  s.total = s.de + align_up((size_t)(CT + 3) * 128 * es, 128);
+  return s;
+}
+
 template <typename T>
 __global__ void __launch_bounds__(128) m3_conv_bwd_kernel(ConvArgs a) {
-  const int d = blockIdx.x * 128 + threadIdx.x;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int tid = threadIdx.x;
+  const int d0 = blockIdx.x * 128;
+  const int d = d0 + tid;
   const int tile = blockIdx.y, b = blockIdx.z;
-  if (d >= a.D) return;  // no barriers below
   const size_t D = (size_t)a.D;
-  const int t0 = tile * a.tile;
-  const int t1 = min(t0 + a.tile, a.T);
-  const int t2 = min(t1 + 3, a.T);
-  const T* xg = static_cast<const T*>(a.x) + (size_t)b * a.T * D + d;
-  const T* dug = static_cast<const T*>(a.du) + (size_t)b * a.T * D + d;
-  const T* deg = a.du_extra ? static_cast<const T*>(a.du_extra) + (size_t)b * a.T * D + d : nullptr;
-  float w[WC];
+  const int t0 = tile * CT;
+  const int t1 = min(t0 + CT, a.T);
+  const ConvSmem L = conv_smem(sizeof(T));
+  T* xs = reinterpret_cast<T*>(smem + L.x);    // row r: step t0 - 3 + r
+  T* us = reinterpret_cast<T*>(smem + L.du);   // row r: step t0 + r
+  T* es = reinterpret_cast<T*>(smem + L.de);
+  stage_rows<T, 128, 128>(xs, static_cast<const T*>(a.x), b, t0 - 3, CT + 6, a.T, a.T, a.D, d0, tid);
+  stage_rows<T, 128, 128>(us, static_cast<const T*>(a.du), b, t0, CT + 3, a.T, a.T, a.D, d0, tid);
+  if (a.du_extra)
+    stage_rows<T, 128, 128>(es, static_cast<const T*>(a.du_extra), b, t0, CT + 3, a.T, a.T, a.D, d0, tid);
+  cp_async_commit();
+  const bool active = d < a.D;
+  float w[WC] = {0.f, 0.f, 0.f, 0.f};
+  float cb = 0.f;
+  if (active) {
 #pragma unroll
-  for (int k = 0; k < WC; ++k) w[k] = a.conv_w[(size_t)d * WC + k];
-  const float cb = a.conv_b[d];
-  auto x_at = [&](int t) -> float {
-    if (t >= 0) return Act<T>::ld(xg + (size_t)t * D);
-    if (a.conv_in) return Act<T>::ld(static_cast<const T*>(a.conv_in) + ((size_t)b * 3 + t + 3) * D + d);
-    return 0.f;
-  };
-  float xm3 = x_at(t0 - 3), xm2 = x_at(t0 - 2), xm1 = x_at(t0 - 1);
-  float dc1 = 0.f, dc2 = 0.f, dc3 = 0.f;  // dc one, two and three steps back
+    for (int k = 0; k < WC; ++k) w[k] = a.conv_w[(size_t)d * WC + k];
+    cb = a.conv_b[d];
+  }
+  cp_async_wait<0>();
+  __syncthreads();
+  if (!active) return;  // no barriers below
+  if (a.conv_in && t0 < 3) {
+    // halo rows before step 0 (staged as zeros): the carried conv inputs
+    const T* ci = static_cast<const T*>(a.conv_in) + (size_t)b * 3 * D + d;
+    for (int r = 0; r < 3 - t0; ++r) xs[r * 128 + tid] = ci[(size_t)(t0 + r) * D];
+  }
+  // dc of steps t0 .. t1 + 2 (zero from step T on), then d_x of the tile
+  float dcs[CT + 3];
   float dcb = 0.f, dcw[WC] = {0.f, 0.f, 0.f, 0.f};
-  float first[3] = {0.f, 0.f, 0.f};     // dc at steps 0, 1, 2
-#pragma unroll 4
-  for (int t = t0; t < t1 + 3; ++t) {
+#pragma unroll
+  for (int j = 0; j < CT + 3; ++j) {
+    const int t = t0 + j;
     float dc = 0.f;
-    if (t < t2) {
-      const float xv = Act<T>::ld(xg + (size_t)t * D);
-      float gu = Act<T>::ld(dug + (size_t)t * D);
-      if (deg) gu += Act<T>::ld(deg + (size_t)t * D);
+    if (t < a.T) {
+      const float xm3 = Act<T>::ld(xs + j * 128 + tid);
+      const float xm2 = Act<T>::ld(xs + (j + 1) * 128 + tid);
+      const float xm1 = Act<T>::ld(xs + (j + 2) * 128 + tid);
+      const float xv = Act<T>::ld(xs + (j + 3) * 128 + tid);
+      float gu = Act<T>::ld(us + j * 128 + tid);
+      if (a.du_extra) gu += Act<T>::ld(es + j * 128 + tid);
       const float c = fmaf(w[0], xm3, fmaf(w[1], xm2, fmaf(w[2], xm1, fmaf(w[3], xv, cb))));
       const float sc = sigmoid_f(c);
       dc = gu * (sc * fmaf(c, 1.f - sc, 1.f));
-      if (t < t1) {
+      if (j < CT && t < t1) {
         dcb += dc;
         dcw[0] = fmaf(dc, xm3, dcw[0]);
         dcw[1] = fmaf(dc, xm2, dcw[1]);
         dcw[2] = fmaf(dc, xm1, dcw[2]);
         dcw[3] = fmaf(dc, xv, dcw[3]);
       }
-      if (t < 3) first[t] = dc;
-      xm3 = xm2;
-      xm2 = xm1;
-      xm1 = xv;
     }
-    const int sx = t - 3;  // d_x[sx] needs dc[sx .. sx + 3]
-    if (sx >= t0) {
-      float v = fmaf(dc3, w[3], fmaf(dc2, w[2], fmaf(dc1, w[1], dc * w[0])));
-      if (a.g_conv && sx >= a.T - 3)  // x[sx] is also a conv-state output
-        v += Act<T>::ld(static_cast<const T*>(a.g_conv) + ((size_t)b * 3 + sx - (a.T - 3)) * D + d);
-      Act<T>::st(static_cast<T*>(a.dx) + ((size_t)b * a.T + sx) * D + d, v);
+    dcs[j] = dc;
+  }
+#pragma unroll
+  for (int j = 0; j < CT; ++j) {
+    const int t = t0 + j;
+    if (t < t1) {
+      float v = fmaf(dcs[j], w[3], fmaf(dcs[j + 1], w[2], fmaf(dcs[j + 2], w[1], dcs[j + 3] * w[0])));
+      if (a.g_conv && t >= a.T - 3)  // x[t] is also a conv-state output
+        v += Act<T>::ld(static_cast<const T*>(a.g_conv) + ((size_t)b * 3 + t - (a.T - 3)) * D + d);
+      Act<T>::st(static_cast<T*>(a.dx) + ((size_t)b * a.T + t) * D + d, v);
     }
-    dc3 = dc2;
-    dc2 = dc1;
-    dc1 = dc;
   }
   if (tile == 0 && a.d_conv_in) {
     // conv inputs of steps -3, -2, -1 (rows 0..2) reach dc of steps 0..2
     float v[3];
-    v[0] = first[0] * w[0];
-    v[1] = fmaf(first[1], w[0], first[0] * w[1]);
-    v[2] = fmaf(first[2], w[0], fmaf(first[1], w[1], first[0] * w[2]));
+    v[0] = dcs[0] * w[0];
+    v[1] = fmaf(dcs[1], w[0], dcs[0] * w[1]);
+    v[2] = fmaf(dcs[2], w[0], fmaf(dcs[1], w[1], dcs[0] * w[2]));
     T* dci = static_cast<T*>(a.d_conv_in) + (size_t)b * 3 * D + d;
 #pragma unroll
     for (int r = 0; r < 3; ++r) {
@@ -1948,7 +1978,15 @@ __global__ void m3_conv_fin_kernel(ConvArgs a) {
   if (ok) {
     const float* __restrict__ P = a.part + (size_t)j * a.D + d;
     const size_t stride = (size_t)5 * a.D;
-    for (int r = ry; r < rows; r += 8) v0 += P[(size_t)r * stride];
+    float v1 = 0.f;
+    int r = ry;
+#pragma unroll 4
+    for (; r + 8 < rows; r += 16) {
+      v0 += P[(size_t)r * stride];
+      v1 += P[(size_t)(r + 8) * stride];
+    }
+    if (r < rows) v0 += P[(size_t)r * stride];
+    v0 += v1;
   }
   part[ry][cx] = v0;
   __syncthreads();
@@ -2236,6 +2274,9 @@ cudaError_t set_attrs() {
       e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_CAP);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   }
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(m3_conv_bwd_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)conv_smem(es).total);
   return e;
 }
 
@@ -2423,15 +2464,9 @@ m3_status make_plan(const m3_dims* dm, m3_dtype act, Plan* p) {
     p->b_dchead = take(B * p->Sb * 3 * D * 4);
   }
   size_t bwd_total = off;
-  // conv backward of the two-phase backward (its own call): 128-step tiles,
-  // or 32-step ones when that leaves fewer than four blocks per SM of a
-  // 152-SM GPU
-  {
-    const int64_t groups = (p->D + 127) / 128;
-    p->ctile = 128;
-    if ((int64_t)p->B * groups * ((p->T + 127) / 128) < 4 * 152) p->ctile = 32;
-    p->cntiles = (p->T + p->ctile - 1) / p->ctile;
-  }
+  // conv backward of the two-phase backward (its own call): CT-step tiles
+  p->ctile = CT;
+  p->cntiles = (p->T + CT - 1) / CT;
   off = 0;
   p->c_part = take(B * (size_t)p->cntiles * 5 * D * 4);
   const size_t conv_total = off;
@@ -2833,6 +2868,8 @@ m3_status m3scan_conv_bwd(const m3_dims* dims, m3_dtype act, const void* x, cons
     if (!aligned(q, 4)) return M3_ERR_ALIGN;
   if (!workspace || workspace_bytes < p.ws_bytes) return M3_ERR_WORKSPACE;
   if (!aligned(workspace, 256)) return M3_ERR_ALIGN;
+  int smem_sm = 0;
+  if (ensure_device(p.K, act == M3_BF16 ? 1 : 0, &smem_sm) != M3_OK) return M3_ERR_CUDA;
   ConvArgs a{};
   a.B = p.B; a.T = p.T; a.D = p.D; a.tile = p.ctile; a.ntiles = p.cntiles;
   a.x = x; a.du = du; a.du_extra = du_extra; a.conv_w = conv_w; a.conv_b = conv_b; a.dx = d_x;
@@ -2842,8 +2879,8 @@ m3_status m3scan_conv_bwd(const m3_dims* dims, m3_dtype act, const void* x, cons
   a.accumulate = dims->accumulate_param_grads ? 1 : 0;
   const dim3 grid((unsigned)((p.D + 127) / 128), (unsigned)p.cntiles, (unsigned)p.B);
   cudaError_t e = act == M3_BF16
-                      ? launch_k(m3_conv_bwd_kernel<__nv_bfloat16>, grid, 128, 0, s, false, a)
-                      : launch_k(m3_conv_bwd_kernel<float>, grid, 128, 0, s, false, a);
+                      ? launch_k(m3_conv_bwd_kernel<__nv_bfloat16>, grid, 128, conv_smem(2).total, s, false, a)
+                      : launch_k(m3_conv_bwd_kernel<float>, grid, 128, conv_smem(4).total, s, false, a);
   if (e == cudaSuccess)
     e = launch_k(m3_conv_fin_kernel, dim3((unsigned)((5 * (size_t)p.D + 31) / 32)), 256, 0, s, true, a);
   if (e == cudaSuccess) e = cudaGetLastError();
