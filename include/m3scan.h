@@ -66,7 +66,7 @@ typedef enum {
     M3_OK = 0,
     M3_ERR_NULL = 1,        /* a required pointer is NULL */
     M3_ERR_DIMS = 2,        /* a size is negative or out of range */
-    M3_ERR_UNSUPPORTED = 3, /* d_state != 16, d_conv != 4, d_inner % 8 != 0, dtype */
+    M3_ERR_UNSUPPORTED = 3, /* d_state not 16/32/64, d_conv != 4, d_inner % 8 != 0, dtype */
     M3_ERR_ALIGN = 4,       /* a pointer is not aligned as required */
     M3_ERR_WORKSPACE = 5,   /* workspace missing or smaller than planned */
     M3_ERR_CUDA = 6         /* a CUDA runtime call or launch failed */
@@ -83,11 +83,14 @@ typedef struct {
     int64_t segments;
     /* 1: param grads are added to the output buffers; 0: overwritten. */
     int32_t accumulate_param_grads;
-    /* Threads per channel in the forward's and the backward's main
-       kernels: 1 (16 state lanes per thread, the most channels per SM), 2
-       (8 lanes per thread: half the per-thread work, for grids that fill
-       less than one wave), or 0 = chosen per kernel from its grid size.
-       Same results up to the order of f32 sums. */
+    /* Kernel variant of the forward's and the backward's main passes:
+       1 = one thread per channel (16 state lanes each, the most channels per
+       SM; d_state 16 only), 2 = the split kernels (8 lanes per thread,
+       d_state / 8 threads per channel: half the per-thread work at d_state
+       16, for grids that fill less than one wave), 0 = chosen per pass
+       (d_state 32 and 64 always take the split kernels).  The plan reports
+       the threads per channel chosen.  Same results up to the order of f32
+       sums. */
     int32_t threads_per_channel;
     /* Row strides, in elements, between consecutive (batch, step) rows of
        Bm and Cm, and of dB and dC; 0 = d_state (dense).  A stride > d_state

@@ -521,7 +521,7 @@ def m3scan_bwd_two_phase(x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log
     act = x.dtype
     dev = x.device
     Bsz, T, Dn = x.shape
-    N, W = 16, conv_w.shape[-1]
+    N, W = Bm.shape[-1], conv_w.shape[-1]
     dims = make_dims(Bsz, T, Dn, d_state=N, d_conv=W, chunk=chunk, segments=segments,
                      accumulate_param_grads=accumulate_param_grads, bc_stride=bc_stride,
                      dbc_stride=dbc_stride, threads_per_channel=threads_per_channel)

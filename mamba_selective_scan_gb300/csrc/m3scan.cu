@@ -195,21 +195,21 @@ __device__ __forceinline__ void stage_rows(T* dst, const T* src, int b, int t_fi
   }
 }
 
-// Stage rows [t_first, t_first + rows) of a [B, T_, 16] tensor whose rows
-// are ld elements apart into dst[rows][16]; rows outside [0, t_limit) read
+// Stage rows [t_first, t_first + rows) of a [B, T_, NN] tensor whose rows
+// are ld elements apart into dst[rows][NN]; rows outside [0, t_limit) read
 // as zero.
-template <typename T, int NT>
+template <typename T, int NT, int NN = NS>
 __device__ __forceinline__ void stage_bc(T* dst, const T* src, int b, int t_first, int rows,
                                          int T_, int t_limit, int ld, int tid) {
   constexpr int EPC = 16 / sizeof(T);
-  constexpr int CPR = NS / EPC;
+  constexpr int CPR = NN / EPC;
   const int n = rows * CPR;
   for (int i = tid; i < n; i += NT) {
     const int r = i / CPR, cc = i - r * CPR;
     const int t = t_first + r;
     const bool ok = (t >= 0) && (t < t_limit);
     const T* g = ok ? src + ((size_t)b * T_ + t) * ld + cc * EPC : src;
-    cp_async16(dst + r * NS + cc * EPC, g, ok);
+    cp_async16(dst + r * NN + cc * EPC, g, ok);
   }
 }
 
@@ -282,25 +282,26 @@ __host__ __device__ inline FwdSmem fwd_smem(int es) {
   return s;
 }
 
-// Two-thread forward shared memory: two staging buffers {x: [TT+3][GP]
-// (three halo rows), delta_raw, z: [TT][GP]; B, C: [TT][16]}, float B and C
-// of the tile, and per-step scalars sc[SUB][GP] float4 shared by a pair.
-constexpr int GP = 64;  // channels per block of the two-thread kernels
+// Split forward shared memory (CH = 128 / (N / 8) channels): two staging
+// buffers {x: [TT+3][CH] (three halo rows), delta_raw, z: [TT][CH]; B, C:
+// [TT][N]}, float B and C of the tile, and per-step scalars sc[SUB][CH]
+// float4 shared by the threads of a channel.
 struct Fwd2Smem {
   size_t x, dr, z, Bt, Ct, tile, fB, fC, sc, total;
 };
-__host__ __device__ inline Fwd2Smem fwd2_smem(int es) {
+__host__ __device__ inline Fwd2Smem fwd2_smem(int es, int N) {
+  const int CH = 128 / (N / 8);  // channels per block
   Fwd2Smem s;
   s.x = 0;
-  s.dr = s.x + align_up((size_t)(TT + 3) * GP * es, 128);
-  s.z = s.dr + align_up((size_t)TT * GP * es, 128);
-  s.Bt = s.z + align_up((size_t)TT * GP * es, 128);
-  s.Ct = s.Bt + align_up((size_t)TT * NS * es, 128);
-  s.tile = s.Ct + align_up((size_t)TT * NS * es, 128);
+  s.dr = s.x + align_up((size_t)(TT + 3) * CH * es, 128);
+  s.z = s.dr + align_up((size_t)TT * CH * es, 128);
+  s.Bt = s.z + align_up((size_t)TT * CH * es, 128);
+  s.Ct = s.Bt + align_up((size_t)TT * N * es, 128);
+  s.tile = s.Ct + align_up((size_t)TT * N * es, 128);
   s.fB = 2 * s.tile;
-  s.fC = s.fB + (size_t)TT * NS * 4;
-  s.sc = s.fC + (size_t)TT * NS * 4;
-  s.total = s.sc + (size_t)SUB * GP * 16;
+  s.fC = s.fB + (size_t)TT * N * 4;
+  s.sc = s.fC + (size_t)TT * N * 4;
+  s.total = s.sc + (size_t)SUB * CH * 16;
   return s;
 }
 
@@ -333,30 +334,31 @@ __host__ __device__ inline BwdSmem bwd_smem(int K, int es) {
   return s;
 }
 
-// Backward with two threads per channel (64 channels per block): the same
-// staging buffers for 64 channels; per-step scalars s0/s1 [K][64] float4
-// shared by the two threads of a channel; the conv-input gradient of the
-// chunk's steps and of the next chunk's first three, dcs[K+3][64]; per-warp
-// dB/dC sums red[K][4][32].
+// Split backward (CH = 128 / (N / 8) channels per block): the same staging
+// buffers for CH channels and N-wide B and C; per-step scalars s0/s1
+// [K][CH] float4 shared by the threads of a channel; the conv-input gradient
+// of the chunk's steps and of the next chunk's first three, dcs[K+3][CH];
+// per-warp dB/dC sums red[K][4][2N].
 struct Bwd2Smem {
   size_t x, dr, z, dg, Bt, Ct, ck, tile, fB, fC, scal, dcs, red, total;
 };
-__host__ __device__ inline Bwd2Smem bwd2_smem(int K, int es) {
+__host__ __device__ inline Bwd2Smem bwd2_smem(int K, int es, int N) {
+  const int CH = 128 / (N / 8);  // channels per block
   Bwd2Smem s;
   s.x = 0;
-  s.dr = s.x + align_up((size_t)(K + 3) * GP * es, 128);
-  s.z = s.dr + align_up((size_t)K * GP * es, 128);
-  s.dg = s.z + align_up((size_t)K * GP * es, 128);
-  s.Bt = s.dg + align_up((size_t)K * GP * es, 128);
-  s.Ct = s.Bt + align_up((size_t)K * NS * es, 128);
-  s.ck = s.Ct + align_up((size_t)K * NS * es, 128);
-  s.tile = s.ck + (size_t)NS * GP * 4;
+  s.dr = s.x + align_up((size_t)(K + 3) * CH * es, 128);
+  s.z = s.dr + align_up((size_t)K * CH * es, 128);
+  s.dg = s.z + align_up((size_t)K * CH * es, 128);
+  s.Bt = s.dg + align_up((size_t)K * CH * es, 128);
+  s.Ct = s.Bt + align_up((size_t)K * N * es, 128);
+  s.ck = s.Ct + align_up((size_t)K * N * es, 128);
+  s.tile = s.ck + (size_t)N * CH * 4;
   s.fB = 2 * s.tile;
-  s.fC = s.fB + (size_t)K * NS * 4;
-  s.scal = s.fC + (size_t)K * NS * 4;
-  s.dcs = s.scal + (size_t)2 * K * GP * 16;
-  s.red = s.dcs + align_up((size_t)(K + 3) * GP * 4, 128);
-  s.total = s.red + (size_t)K * 4 * 32 * 4;
+  s.fC = s.fB + (size_t)K * N * 4;
+  s.scal = s.fC + (size_t)K * N * 4;
+  s.dcs = s.scal + (size_t)2 * K * CH * 16;
+  s.red = s.dcs + align_up((size_t)(K + 3) * CH * 4, 128);
+  s.total = s.red + (size_t)K * 4 * 2 * N * 4;
   return s;
 }
 
@@ -365,15 +367,15 @@ __host__ __device__ inline Bwd2Smem bwd2_smem(int K, int es) {
 struct AggSmem {
   size_t dr, z, dg, Ct, tile, fC, sc, total;
 };
-__host__ __device__ inline AggSmem agg_smem(int es) {
+__host__ __device__ inline AggSmem agg_smem(int es, int N = NS) {
   AggSmem s;
   s.dr = 0;
   s.z = s.dr + align_up((size_t)TT * GB * es, 128);
   s.dg = s.z + align_up((size_t)TT * GB * es, 128);
   s.Ct = s.dg + align_up((size_t)TT * GB * es, 128);
-  s.tile = s.Ct + align_up((size_t)TT * NS * es, 128);
+  s.tile = s.Ct + align_up((size_t)TT * N * es, 128);
   s.fC = 2 * s.tile;
-  s.sc = s.fC + (size_t)TT * NS * 4;
+  s.sc = s.fC + (size_t)TT * N * 4;
   s.total = s.sc + (size_t)TT * GB * 8;
   return s;
 }
@@ -609,20 +611,23 @@ __global__ void __launch_bounds__(GF) m3_fwd_kernel(FwdArgs a) {
 }
 
 // ---------------------------------------------------------------------------
-// forward with two threads per channel (64 channels per block): the pair of
-// a channel splits its 16 state lanes (8 each), takes alternate steps of the
-// scalar pass and sums y with one shuffle.  For grids that fill less than
-// one wave; same results as m3_fwd_kernel up to the order of f32 sums.
+// forward with the lanes split over N / 8 threads per channel (8 lanes
+// each; 128 / (N / 8) channels per block): the threads of a channel take the
+// scalar pass of every (N / 8)-th step and sum y with shuffles.  For d_state
+// 32 and 64, and for d_state-16 grids that fill less than one wave; the same
+// results as m3_fwd_kernel up to the order of f32 sums.
 // ---------------------------------------------------------------------------
 
-template <typename T, bool FINAL>
+template <typename T, bool FINAL, int N>
 __global__ void __launch_bounds__(128) m3_fwd2_kernel(FwdArgs a) {
+  constexpr int G = N / 8;     // threads per channel
+  constexpr int CH = 128 / G;  // channels per block
   extern __shared__ __align__(128) unsigned char smem[];
   const Geo g = a.g;
   const int tid = threadIdx.x;
-  const int hf = tid & 1;   // this thread's state lanes: 8 hf .. 8 hf + 7
-  const int ch = tid >> 1;  // channel within the block
-  const int d0 = blockIdx.x * GP;
+  const int hf = tid % G;   // this thread's state lanes: 8 hf .. 8 hf + 7
+  const int ch = tid / G;   // channel within the block
+  const int d0 = blockIdx.x * CH;
   const int s = blockIdx.y;
   const int b = blockIdx.z;
   const int d = d0 + ch;
@@ -631,7 +636,7 @@ __global__ void __launch_bounds__(128) m3_fwd2_kernel(FwdArgs a) {
   const int c_end = min(c_begin + g.m, g.nc);
   const int t_begin = c_begin * g.K;
   const int t_end = min(c_end * g.K, g.T);
-  const Fwd2Smem L = fwd2_smem(sizeof(T));
+  const Fwd2Smem L = fwd2_smem(sizeof(T), N);
   const T* xg = static_cast<const T*>(a.x);
   float* fB = reinterpret_cast<float*>(smem + L.fB);
   float* fC = reinterpret_cast<float*>(smem + L.fC);
@@ -639,12 +644,12 @@ __global__ void __launch_bounds__(128) m3_fwd2_kernel(FwdArgs a) {
   // x is staged with the three steps before the tile (row r = step t0 - 3 + r)
   auto stage = [&](int t0, int buf) {
     unsigned char* base = smem + (size_t)buf * L.tile;
-    stage_rows<T, GP, 128>(reinterpret_cast<T*>(base + L.x), xg, b, t0 - 3, TT + 3, g.T, t_end, g.D, d0, tid);
-    stage_rows<T, GP, 128>(reinterpret_cast<T*>(base + L.dr), static_cast<const T*>(a.dr), b, t0, TT, g.T, t_end, g.D, d0, tid);
-    stage_bc<T, 128>(reinterpret_cast<T*>(base + L.Bt), static_cast<const T*>(a.Bm), b, t0, TT, g.T, t_end, g.ldbc, tid);
+    stage_rows<T, CH, 128>(reinterpret_cast<T*>(base + L.x), xg, b, t0 - 3, TT + 3, g.T, t_end, g.D, d0, tid);
+    stage_rows<T, CH, 128>(reinterpret_cast<T*>(base + L.dr), static_cast<const T*>(a.dr), b, t0, TT, g.T, t_end, g.D, d0, tid);
+    stage_bc<T, 128, N>(reinterpret_cast<T*>(base + L.Bt), static_cast<const T*>(a.Bm), b, t0, TT, g.T, t_end, g.ldbc, tid);
     if (FINAL) {
-      stage_rows<T, GP, 128>(reinterpret_cast<T*>(base + L.z), static_cast<const T*>(a.z), b, t0, TT, g.T, t_end, g.D, d0, tid);
-      stage_bc<T, 128>(reinterpret_cast<T*>(base + L.Ct), static_cast<const T*>(a.Cm), b, t0, TT, g.T, t_end, g.ldbc, tid);
+      stage_rows<T, CH, 128>(reinterpret_cast<T*>(base + L.z), static_cast<const T*>(a.z), b, t0, TT, g.T, t_end, g.D, d0, tid);
+      stage_bc<T, 128, N>(reinterpret_cast<T*>(base + L.Ct), static_cast<const T*>(a.Cm), b, t0, TT, g.T, t_end, g.ldbc, tid);
     }
     cp_async_commit();
   };
@@ -655,8 +660,8 @@ __global__ void __launch_bounds__(128) m3_fwd2_kernel(FwdArgs a) {
 #pragma unroll
   for (int P = 0; P < 4; ++P) {
     const int n = 8 * hf + 2 * P;
-    a2[P].x = active ? -expf(a.a_log[(size_t)d * NS + n]) * LOG2E : 0.f;
-    a2[P].y = active ? -expf(a.a_log[(size_t)d * NS + n + 1]) * LOG2E : 0.f;
+    a2[P].x = active ? -expf(a.a_log[(size_t)d * N + n]) * LOG2E : 0.f;
+    a2[P].y = active ? -expf(a.a_log[(size_t)d * N + n + 1]) * LOG2E : 0.f;
   }
   float w[WC];
 #pragma unroll
@@ -669,7 +674,7 @@ __global__ void __launch_bounds__(128) m3_fwd2_kernel(FwdArgs a) {
 #pragma unroll
   for (int P = 0; P < 4; ++P) h[P] = make_float2(0.f, 0.f);
   if (FINAL && a.h_in && active) {
-    const float* h0 = a.h_in + (size_t)b * NS * g.D + d;
+    const float* h0 = a.h_in + (size_t)b * N * g.D + d;
 #pragma unroll
     for (int P = 0; P < 4; ++P) {
       const int n = 8 * hf + 2 * P;
@@ -684,14 +689,14 @@ __global__ void __launch_bounds__(128) m3_fwd2_kernel(FwdArgs a) {
       const float2 dl2 = f2b(active ? a.agg_s[bs * g.D + d] : 0.f);
 #pragma unroll
       for (int P = 0; P < 4; ++P) {
-        const float* ah = a.agg_h + (bs * NS + 8 * hf + 2 * P) * g.D + d;
+        const float* ah = a.agg_h + (bs * N + 8 * hf + 2 * P) * g.D + d;
         const float2 loc = active ? make_float2(ah[0], ah[g.D]) : make_float2(0.f, 0.f);
         h[P] = __ffma2_rn(ex2x2(__fmul2_rn(dl2, a2[P])), h[P], loc);
       }
     }
   }
   float sdelta = 0.f;
-  float4* scs = reinterpret_cast<float4*>(smem + L.sc) + ch;  // shared by the pair, stride GP
+  float4* scs = reinterpret_cast<float4*>(smem + L.sc) + ch;  // shared by the channel's threads, stride CH
   int kc = 0;  // steps left until the next checkpoint
   for (int t0 = t_begin, it = 0; t0 < t_end; t0 += TT, ++it) {
     const int buf = it & 1;
@@ -707,12 +712,12 @@ __global__ void __launch_bounds__(128) m3_fwd2_kernel(FwdArgs a) {
       // halo rows before step 0 (staged as zeros): the carried conv inputs
       T* xw = reinterpret_cast<T*>(base + L.x);
       const T* ci = static_cast<const T*>(a.conv_in) + (size_t)b * 3 * g.D + d;
-      for (int r = 0; r < 3 - t0; ++r) xw[r * GP + ch] = ci[(size_t)(t0 + r) * g.D];
+      for (int r = 0; r < 3 - t0; ++r) xw[r * CH + ch] = ci[(size_t)(t0 + r) * g.D];
     }
     {
       const T* Bt = reinterpret_cast<const T*>(base + L.Bt);
       const T* Ct = reinterpret_cast<const T*>(base + L.Ct);
-      for (int i = tid; i < TT * NS; i += 128) {
+      for (int i = tid; i < TT * N; i += 128) {
         fB[i] = Act<T>::ld(Bt + i);
         if (FINAL) fC[i] = Act<T>::ld(Ct + i);
       }
@@ -724,23 +729,23 @@ __global__ void __launch_bounds__(128) m3_fwd2_kernel(FwdArgs a) {
     const int steps = min(TT, t_end - t0);
     for (int j0 = 0; j0 < steps; j0 += SUB) {
       const int ns = min(SUB, steps - j0);
-      // scalar pass, this thread's steps (alternate)
+      // scalar pass, this thread's steps (every G-th)
 #pragma unroll 2
-      for (int j = hf; j < ns; j += 2) {
+      for (int j = hf; j < ns; j += G) {
         const int r = j0 + j;
-        const float xm3 = Act<T>::ld(xt + r * GP + ch);
-        const float xm2 = Act<T>::ld(xt + (r + 1) * GP + ch);
-        const float xm1 = Act<T>::ld(xt + (r + 2) * GP + ch);
-        const float xv = Act<T>::ld(xt + (r + 3) * GP + ch);
+        const float xm3 = Act<T>::ld(xt + r * CH + ch);
+        const float xm2 = Act<T>::ld(xt + (r + 1) * CH + ch);
+        const float xm1 = Act<T>::ld(xt + (r + 2) * CH + ch);
+        const float xv = Act<T>::ld(xt + (r + 3) * CH + ch);
         const float cpre = fmaf(w[0], xm3, fmaf(w[1], xm2, fmaf(w[2], xm1, fmaf(w[3], xv, cb))));
         const float u = cpre * sigmoid_f(cpre);
-        const float delta = softplus_f(Act<T>::ld(drt + r * GP + ch) + dtb);
+        const float delta = softplus_f(Act<T>::ld(drt + r * CH + ch) + dtb);
         float gz = 0.f;
         if (FINAL) {
-          const float zv = Act<T>::ld(zt + r * GP + ch);
+          const float zv = Act<T>::ld(zt + r * CH + ch);
           gz = zv * sigmoid_f(zv);
         }
-        scs[j * GP] = make_float4(delta, delta * u, Dd * u, gz);
+        scs[j * CH] = make_float4(delta, delta * u, Dd * u, gz);
       }
       __syncwarp();
       // state pass, both threads
@@ -750,7 +755,7 @@ __global__ void __launch_bounds__(128) m3_fwd2_kernel(FwdArgs a) {
           if (kc == 0) {
             const int t = t0 + j0 + j;
             if (active) {
-              float* ck = a.ckpt + (((size_t)b * g.nc + t / g.K) * NS + 8 * hf) * g.D + d;
+              float* ck = a.ckpt + (((size_t)b * g.nc + t / g.K) * N + 8 * hf) * g.D + d;
 #pragma unroll
               for (int P = 0; P < 4; ++P) {
                 ck[(size_t)(2 * P) * g.D] = h[P].x;
@@ -761,12 +766,12 @@ __global__ void __launch_bounds__(128) m3_fwd2_kernel(FwdArgs a) {
           }
           --kc;
         }
-        const float4 v = scs[j * GP];
+        const float4 v = scs[j * CH];
         const float2 dl2 = f2b(v.x);
         const float2 du2 = f2b(v.y);
-        const float* Bj = fB + (j0 + j) * NS + 8 * hf;
+        const float* Bj = fB + (j0 + j) * N + 8 * hf;
         if (FINAL) {
-          const float* Cj = fC + (j0 + j) * NS + 8 * hf;
+          const float* Cj = fC + (j0 + j) * N + 8 * hf;
           float2 y2 = make_float2(0.f, 0.f);
 #pragma unroll
           for (int P = 0; P < 4; ++P) {
@@ -776,9 +781,10 @@ __global__ void __launch_bounds__(128) m3_fwd2_kernel(FwdArgs a) {
             y2 = __ffma2_rn(cc, h[P], y2);
           }
           float y = y2.x + y2.y;
-          y += __shfl_xor_sync(0xffffffffu, y, 1);
+#pragma unroll
+          for (int o = 1; o < G; o <<= 1) y += __shfl_xor_sync(0xffffffffu, y, o);
           y += v.z;
-          if (active && hf == (j & 1)) {
+          if (active && hf == j % G) {
             const size_t i = ((size_t)b * g.T + t0 + j0 + j) * g.D + d;
             Act<T>::st(static_cast<T*>(a.gated) + i, y * v.w);
             if (a.y_dbg) Act<T>::st(static_cast<T*>(a.y_dbg) + i, y);
@@ -798,7 +804,7 @@ __global__ void __launch_bounds__(128) m3_fwd2_kernel(FwdArgs a) {
   }
   if (FINAL && s == g.S - 1 && active) {
     if (a.h_out) {
-      float* ho = a.h_out + ((size_t)b * NS + 8 * hf) * g.D + d;
+      float* ho = a.h_out + ((size_t)b * N + 8 * hf) * g.D + d;
 #pragma unroll
       for (int P = 0; P < 4; ++P) {
         ho[(size_t)(2 * P) * g.D] = h[P].x;
@@ -820,7 +826,7 @@ __global__ void __launch_bounds__(128) m3_fwd2_kernel(FwdArgs a) {
     }
   }
   if (!FINAL && active) {
-    float* ah = a.agg_h + (((size_t)b * g.S + s) * NS + 8 * hf) * g.D + d;
+    float* ah = a.agg_h + (((size_t)b * g.S + s) * N + 8 * hf) * g.D + d;
 #pragma unroll
     for (int P = 0; P < 4; ++P) {
       ah[(size_t)(2 * P) * g.D] = h[P].x;
@@ -837,13 +843,13 @@ __global__ void __launch_bounds__(128) m3_fwd2_kernel(FwdArgs a) {
 // and the summed step size (the segment's total decay).
 // ---------------------------------------------------------------------------
 
-// TPC threads per channel (1 or 2): with two, a block covers 64 channels,
-// each thread carries 8 of a channel's 16 lanes and the scalar pass of
-// alternate steps.
-template <typename T, int TPC>
+// TPC threads per channel: one (16 lanes each, d_state 16) or d_state / 8
+// (8 lanes each, 128 / TPC channels per block), the threads of a channel
+// taking the scalar pass of every TPC-th step.
+template <typename T, int TPC, int N>
 __global__ void __launch_bounds__(GB) m3_bwd_agg_kernel(BwdArgs a) {
   constexpr int G = GB / TPC;        // channels per block
-  constexpr int NL = NS / TPC;       // state lanes per thread
+  constexpr int NL = N / TPC;        // state lanes per thread
   extern __shared__ __align__(128) unsigned char smem[];
   const Geo g = a.g;
   const int tid = threadIdx.x;
@@ -856,7 +862,7 @@ __global__ void __launch_bounds__(GB) m3_bwd_agg_kernel(BwdArgs a) {
   const bool active = d < g.D;
   const int t_begin = s * g.m * g.K;
   const int t_end = min((s + 1) * g.m * g.K, g.T);
-  const AggSmem L = agg_smem(sizeof(T));
+  const AggSmem L = agg_smem(sizeof(T), N);
   float* fC = reinterpret_cast<float*>(smem + L.fC);
   const int ntiles = (t_end - t_begin + TT - 1) / TT;
   auto tile_start = [&](int i) { return max(t_begin, t_end - (i + 1) * TT); };
@@ -867,7 +873,7 @@ __global__ void __launch_bounds__(GB) m3_bwd_agg_kernel(BwdArgs a) {
     stage_rows<T, G, GB>(reinterpret_cast<T*>(base + L.dr), static_cast<const T*>(a.dr), b, t0, rows, g.T, g.T, g.D, d0, tid);
     stage_rows<T, G, GB>(reinterpret_cast<T*>(base + L.z), static_cast<const T*>(a.z), b, t0, rows, g.T, g.T, g.D, d0, tid);
     stage_rows<T, G, GB>(reinterpret_cast<T*>(base + L.dg), static_cast<const T*>(a.dg), b, t0, rows, g.T, g.T, g.D, d0, tid);
-    stage_bc<T, GB>(reinterpret_cast<T*>(base + L.Ct), static_cast<const T*>(a.Cm), b, t0, rows, g.T, g.T, g.ldbc, tid);
+    stage_bc<T, GB, N>(reinterpret_cast<T*>(base + L.Ct), static_cast<const T*>(a.Cm), b, t0, rows, g.T, g.T, g.ldbc, tid);
     cp_async_commit();
   };
 
@@ -878,8 +884,8 @@ __global__ void __launch_bounds__(GB) m3_bwd_agg_kernel(BwdArgs a) {
 #pragma unroll
   for (int i = 0; i < NL / 2; ++i) {
     const int n = NL * hf + 2 * i;
-    a2[i].x = active ? -expf(a.a_log[(size_t)d * NS + n]) * LOG2E : 0.f;
-    a2[i].y = active ? -expf(a.a_log[(size_t)d * NS + n + 1]) * LOG2E : 0.f;
+    a2[i].x = active ? -expf(a.a_log[(size_t)d * N + n]) * LOG2E : 0.f;
+    a2[i].y = active ? -expf(a.a_log[(size_t)d * N + n + 1]) * LOG2E : 0.f;
   }
   const float dtb = active ? a.dt_bias[d] : 0.f;
   float2 carry[NL / 2];
@@ -892,9 +898,9 @@ __global__ void __launch_bounds__(GB) m3_bwd_agg_kernel(BwdArgs a) {
     // kernel): this kernel runs before it, so it clears them.
     const size_t ncta = (size_t)gridDim.x * gridDim.y * gridDim.z;
     const size_t cid = blockIdx.x + (size_t)gridDim.x * (blockIdx.y + (size_t)gridDim.y * blockIdx.z);
-    const size_t total = (size_t)g.B * g.T * NS;
+    const size_t total = (size_t)g.B * g.T * N;
     for (size_t i = cid * GB + tid; i < total; i += ncta * GB) {
-      const size_t o = (i / NS) * g.lddbc + (i % NS);
+      const size_t o = (i / N) * g.lddbc + (i % N);
       a.dB[o] = 0.f;
       a.dC[o] = 0.f;
     }
@@ -913,7 +919,7 @@ __global__ void __launch_bounds__(GB) m3_bwd_agg_kernel(BwdArgs a) {
     const int steps = (t_end - i * TT) - t0;
     {
       const T* Ct = reinterpret_cast<const T*>(base + L.Ct);
-      for (int k = tid; k < steps * NS; k += GB) fC[k] = Act<T>::ld(Ct + k);
+      for (int k = tid; k < steps * N; k += GB) fC[k] = Act<T>::ld(Ct + k);
     }
     __syncthreads();
     const T* drt = reinterpret_cast<const T*>(base + L.dr);
@@ -934,7 +940,7 @@ __global__ void __launch_bounds__(GB) m3_bwd_agg_kernel(BwdArgs a) {
       sdelta += v.x;
       const float2 dl2 = f2b(v.x);
       const float2 dy2 = f2b(v.y);
-      const float2* C2 = reinterpret_cast<const float2*>(fC + j * NS + NL * hf);
+      const float2* C2 = reinterpret_cast<const float2*>(fC + j * N + NL * hf);
 #pragma unroll
       for (int q = 0; q < NL / 2; ++q) {
         carry[q] = __fmul2_rn(ex2x2(__fmul2_rn(dl2, a2[q])), __ffma2_rn(dy2, C2[q], carry[q]));
@@ -946,8 +952,8 @@ __global__ void __launch_bounds__(GB) m3_bwd_agg_kernel(BwdArgs a) {
     const size_t bs = (size_t)b * g.S + s;
 #pragma unroll
     for (int i = 0; i < NL / 2; ++i) {
-      a.q[(bs * NS + NL * hf + 2 * i) * g.D + d] = carry[i].x;
-      a.q[(bs * NS + NL * hf + 2 * i + 1) * g.D + d] = carry[i].y;
+      a.q[(bs * N + NL * hf + 2 * i) * g.D + d] = carry[i].x;
+      a.q[(bs * N + NL * hf + 2 * i + 1) * g.D + d] = carry[i].y;
     }
     if (hf == 0) a.sd[bs * g.D + d] = sdelta;
   }
@@ -1374,42 +1380,57 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(BwdArgs a) {
 }
 
 // ---------------------------------------------------------------------------
-// backward main kernel, two threads per channel (64 channels per block): the
-// thread pair of a channel splits its 16 state lanes (8 each) and takes the
-// per-step scalar work of alternate steps, so each thread runs about half
-// the per-step instructions and a block holds twice the warps per channel.
-// Same results as m3_bwd_kernel up to the order of f32 sums.
+// backward main kernel with the lanes split over G = N / 8 threads per
+// channel (8 lanes each, 128 / G channels per block); the threads of a
+// channel take the per-step scalar work of every G-th step.  For d_state 32
+// and 64, and for d_state-16 grids that fill less than one wave (each thread
+// then runs about half the per-step instructions of m3_bwd_kernel and a
+// block holds twice the warps per channel).  Same results as m3_bwd_kernel
+// up to the order of f32 sums.
 // ---------------------------------------------------------------------------
 
-// Sum over the 16 channels of a warp (the lanes with the same lane & 1) of
-// 8 values held as 4 pairs, pair P holding this thread's lane pair
-// P ^ ((lane >> 3) & 3); returns the total for pair (lane >> 3) & 3, element
-// (lane >> 2) & 1 (lanes differing only in bit 1 return the same total).
-__device__ __forceinline__ float warp_sum8_rotated(float2 (&v)[4], int lane) {
+// Sum over the channels of a warp (the lanes with the same lane % G) of 8
+// values held as 4 pairs, pair P holding this thread's lane pair
+// P ^ ((lane >> 3) & 3).  The channel bits of a lane are its bits log2(G)
+// and up; the sum runs over them:
+//   G = 2: returns (in .x) the total for pair (lane >> 3) & 3, element
+//          (lane >> 2) & 1 (lanes differing only in bit 1 return the same);
+//   G = 4: the same total, every lane distinct;
+//   G = 8: returns both elements of pair (lane >> 3) & 3.
+template <int G>
+__device__ __forceinline__ float2 warp_sum8_rotated(float2 (&v)[4], int lane) {
   v[0].x += __shfl_xor_sync(0xffffffffu, v[2].x, 16);
   v[0].y += __shfl_xor_sync(0xffffffffu, v[2].y, 16);
   v[1].x += __shfl_xor_sync(0xffffffffu, v[3].x, 16);
   v[1].y += __shfl_xor_sync(0xffffffffu, v[3].y, 16);
   v[0].x += __shfl_xor_sync(0xffffffffu, v[1].x, 8);
   v[0].y += __shfl_xor_sync(0xffffffffu, v[1].y, 8);
-  const bool up = (lane & 4) != 0;
-  const float send = up ? v[0].x : v[0].y;
-  const float keep = up ? v[0].y : v[0].x;
-  const float r = keep + __shfl_xor_sync(0xffffffffu, send, 4);
-  return r + __shfl_xor_sync(0xffffffffu, r, 2);
+  if constexpr (G == 8) {
+    return v[0];
+  } else {
+    const bool up = (lane & 4) != 0;
+    const float send = up ? v[0].x : v[0].y;
+    const float keep = up ? v[0].y : v[0].x;
+    float r = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+    if constexpr (G == 2) r += __shfl_xor_sync(0xffffffffu, r, 2);
+    return make_float2(r, 0.f);
+  }
 }
 
-template <typename T, bool ST, bool SCAN>
+template <typename T, bool ST, bool SCAN, int N>
 __global__ void __launch_bounds__(128, 4) m3_bwd2_kernel(BwdArgs a) {
+  constexpr int G = N / 8;     // threads per channel
+  constexpr int CH = 128 / G;  // channels per block
+  constexpr int NP = N + 8;    // per-channel parameter partials
   extern __shared__ __align__(128) unsigned char smem[];
   const Geo g = a.g;
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
-  const int hf = tid & 1;            // this thread's state lanes: 8 hf .. 8 hf + 7
-  const int ch = tid >> 1;           // channel within the block
+  const int hf = tid % G;            // this thread's state lanes: 8 hf .. 8 hf + 7
+  const int ch = tid / G;            // channel within the block
   const int prot = (lane >> 3) & 3;  // pair rotation for the warp reduction
-  const int d0 = blockIdx.x * GP;
+  const int d0 = blockIdx.x * CH;
   const int s = blockIdx.y;
   const int b = blockIdx.z;
   const int d = d0 + ch;
@@ -1419,11 +1440,11 @@ __global__ void __launch_bounds__(128, 4) m3_bwd2_kernel(BwdArgs a) {
   const int t_begin = c_begin * g.K;
   const int t_end = min(c_end * g.K, g.T);
   const int K = g.K;
-  const Bwd2Smem L = bwd2_smem(K, sizeof(T));
+  const Bwd2Smem L = bwd2_smem(K, sizeof(T), N);
   float* fB = reinterpret_cast<float*>(smem + L.fB);
   float* fC = reinterpret_cast<float*>(smem + L.fC);
   float* red = reinterpret_cast<float*>(smem + L.red);
-  float* dcs = reinterpret_cast<float*>(smem + L.dcs);  // [K + 3][GP]
+  float* dcs = reinterpret_cast<float*>(smem + L.dcs);  // [K + 3][CH]
   // state lane of register pair P
   auto lane_of = [&](int P) { return 8 * hf + 2 * (P ^ prot); };
 
@@ -1442,8 +1463,8 @@ __global__ void __launch_bounds__(128, 4) m3_bwd2_kernel(BwdArgs a) {
 #pragma unroll
   for (int P = 0; P < 4; ++P) {
     const int n = lane_of(P);
-    a2[P].x = active ? -expf(a.a_log[(size_t)d * NS + n]) * LOG2E : 0.f;
-    a2[P].y = active ? -expf(a.a_log[(size_t)d * NS + n + 1]) * LOG2E : 0.f;
+    a2[P].x = active ? -expf(a.a_log[(size_t)d * N + n]) * LOG2E : 0.f;
+    a2[P].y = active ? -expf(a.a_log[(size_t)d * N + n + 1]) * LOG2E : 0.f;
   }
 #pragma unroll
   for (int k = 0; k < WC; ++k) w[k] = active ? a.conv_w[(size_t)d * WC + k] : 0.f;
@@ -1456,7 +1477,7 @@ __global__ void __launch_bounds__(128, 4) m3_bwd2_kernel(BwdArgs a) {
 #pragma unroll
   for (int P = 0; P < 4; ++P) carry[P] = make_float2(0.f, 0.f);
   if (ST && a.g_h && active) {
-    const float* gh = a.g_h + (size_t)b * NS * g.D + d;
+    const float* gh = a.g_h + (size_t)b * N * g.D + d;
 #pragma unroll
     for (int P = 0; P < 4; ++P) {
       const int n = lane_of(P);
@@ -1467,14 +1488,14 @@ __global__ void __launch_bounds__(128, 4) m3_bwd2_kernel(BwdArgs a) {
   auto stage = [&](int c, int buf) {
     unsigned char* base = smem + (size_t)buf * L.tile;
     const int t0 = c * K;
-    stage_rows<T, GP, 128>(reinterpret_cast<T*>(base + L.x), xg, b, t0 - 3, K + 3, g.T, g.T, g.D, d0, tid);
-    stage_rows<T, GP, 128>(reinterpret_cast<T*>(base + L.dr), static_cast<const T*>(a.dr), b, t0, K, g.T, g.T, g.D, d0, tid);
-    stage_rows<T, GP, 128>(reinterpret_cast<T*>(base + L.z), static_cast<const T*>(a.z), b, t0, K, g.T, g.T, g.D, d0, tid);
-    stage_rows<T, GP, 128>(reinterpret_cast<T*>(base + L.dg), static_cast<const T*>(a.dg), b, t0, K, g.T, g.T, g.D, d0, tid);
-    stage_bc<T, 128>(reinterpret_cast<T*>(base + L.Bt), static_cast<const T*>(a.Bm), b, t0, K, g.T, g.T, g.ldbc, tid);
-    stage_bc<T, 128>(reinterpret_cast<T*>(base + L.Ct), static_cast<const T*>(a.Cm), b, t0, K, g.T, g.T, g.ldbc, tid);
-    stage_rows<float, GP, 128>(reinterpret_cast<float*>(base + L.ck), a.ckpt + ((size_t)b * g.nc + c) * NS * g.D,
-                               0, 0, NS, NS, NS, g.D, d0, tid);
+    stage_rows<T, CH, 128>(reinterpret_cast<T*>(base + L.x), xg, b, t0 - 3, K + 3, g.T, g.T, g.D, d0, tid);
+    stage_rows<T, CH, 128>(reinterpret_cast<T*>(base + L.dr), static_cast<const T*>(a.dr), b, t0, K, g.T, g.T, g.D, d0, tid);
+    stage_rows<T, CH, 128>(reinterpret_cast<T*>(base + L.z), static_cast<const T*>(a.z), b, t0, K, g.T, g.T, g.D, d0, tid);
+    stage_rows<T, CH, 128>(reinterpret_cast<T*>(base + L.dg), static_cast<const T*>(a.dg), b, t0, K, g.T, g.T, g.D, d0, tid);
+    stage_bc<T, 128, N>(reinterpret_cast<T*>(base + L.Bt), static_cast<const T*>(a.Bm), b, t0, K, g.T, g.T, g.ldbc, tid);
+    stage_bc<T, 128, N>(reinterpret_cast<T*>(base + L.Ct), static_cast<const T*>(a.Cm), b, t0, K, g.T, g.T, g.ldbc, tid);
+    stage_rows<float, CH, 128>(reinterpret_cast<float*>(base + L.ck), a.ckpt + ((size_t)b * g.nc + c) * N * g.D,
+                               0, 0, N, N, N, g.D, d0, tid);
     cp_async_commit();
   };
   stage(c_end - 1, 0);
@@ -1489,7 +1510,7 @@ __global__ void __launch_bounds__(128, 4) m3_bwd2_kernel(BwdArgs a) {
       const float2 dl2 = f2b(active ? sd[bs * g.D + d] : 0.f);
 #pragma unroll
       for (int P = 0; P < 4; ++P) {
-        const float* qq = q + (bs * NS + lane_of(P)) * g.D + d;
+        const float* qq = q + (bs * N + lane_of(P)) * g.D + d;
         const float2 loc = active ? make_float2(qq[0], qq[g.D]) : make_float2(0.f, 0.f);
         carry[P] = __ffma2_rn(ex2x2(__fmul2_rn(dl2, a2[P])), carry[P], loc);
       }
@@ -1500,7 +1521,7 @@ __global__ void __launch_bounds__(128, 4) m3_bwd2_kernel(BwdArgs a) {
   for (int P = 0; P < 4; ++P) dAp[P] = make_float2(0.f, 0.f);
   float dD_acc = 0.f, ddtb_acc = 0.f, dcb_acc = 0.f;
   float dcw[WC] = {0.f, 0.f, 0.f, 0.f};
-  for (int i = tid; i < (K + 3) * GP; i += 128) dcs[i] = 0.f;  // ordered by the loop's first barrier
+  for (int i = tid; i < (K + 3) * CH; i += 128) dcs[i] = 0.f;  // ordered by the loop's first barrier
 
   for (int c = c_end - 1; c >= c_begin; --c) {
     const int buf = (c_end - 1 - c) & 1;
@@ -1515,12 +1536,12 @@ __global__ void __launch_bounds__(128, 4) m3_bwd2_kernel(BwdArgs a) {
     if (ST && a.conv_in && c * K < 3 && active && hf == 0) {
       T* xw = reinterpret_cast<T*>(smem + (size_t)buf * L.tile + L.x);
       const T* ci = static_cast<const T*>(a.conv_in) + (size_t)b * 3 * g.D + d;
-      for (int r = 0; r < 3 - c * K; ++r) xw[r * GP + ch] = ci[(size_t)(c * K + r) * g.D];
+      for (int r = 0; r < 3 - c * K; ++r) xw[r * CH + ch] = ci[(size_t)(c * K + r) * g.D];
     }
     {
       const T* Bt = reinterpret_cast<const T*>(base + L.Bt);
       const T* Ct = reinterpret_cast<const T*>(base + L.Ct);
-      for (int i = tid; i < K * NS; i += 128) {
+      for (int i = tid; i < K * N; i += 128) {
         fB[i] = Act<T>::ld(Bt + i);
         fC[i] = Act<T>::ld(Ct + i);
       }
@@ -1532,27 +1553,27 @@ __global__ void __launch_bounds__(128, 4) m3_bwd2_kernel(BwdArgs a) {
     const T* dgt = reinterpret_cast<const T*>(base + L.dg);
     const float* ckt = reinterpret_cast<const float*>(base + L.ck);
     const int steps = min(K, g.T - c * K);
-    float4* s0 = reinterpret_cast<float4*>(smem + L.scal) + ch;  // shared by the pair, stride GP
-    float4* s1 = s0 + (size_t)K * GP;
+    float4* s0 = reinterpret_cast<float4*>(smem + L.scal) + ch;  // shared by the channel's threads, stride CH
+    float4* s1 = s0 + (size_t)K * CH;
     const size_t row0 = ((size_t)b * g.T + (size_t)c * K) * g.D + d;
 
-    // ---- scalar pass, steps of this thread's parity ----
-    for (int j = hf; j < steps; j += 2) {
-      const float xm3 = Act<T>::ld(xt + j * GP + ch);
-      const float xm2 = Act<T>::ld(xt + (j + 1) * GP + ch);
-      const float xm1 = Act<T>::ld(xt + (j + 2) * GP + ch);
-      const float xv = Act<T>::ld(xt + (j + 3) * GP + ch);
+    // ---- scalar pass, every G-th step ----
+    for (int j = hf; j < steps; j += G) {
+      const float xm3 = Act<T>::ld(xt + j * CH + ch);
+      const float xm2 = Act<T>::ld(xt + (j + 1) * CH + ch);
+      const float xm1 = Act<T>::ld(xt + (j + 2) * CH + ch);
+      const float xv = Act<T>::ld(xt + (j + 3) * CH + ch);
       const float cpre = fmaf(w[0], xm3, fmaf(w[1], xm2, fmaf(w[2], xm1, fmaf(w[3], xv, cb))));
       const float sc = sigmoid_f(cpre);
       const float u = cpre * sc;
-      const float v = Act<T>::ld(drt + j * GP + ch) + dtb;
+      const float v = Act<T>::ld(drt + j * CH + ch) + dtb;
       const float delta = softplus_f(v);
       const float sv = sigmoid_f(v);
-      const float zv = Act<T>::ld(zt + j * GP + ch);
-      const float gv = Act<T>::ld(dgt + j * GP + ch);
+      const float zv = Act<T>::ld(zt + j * CH + ch);
+      const float gv = Act<T>::ld(dgt + j * CH + ch);
       const float sz = sigmoid_f(zv);
-      s0[j * GP] = make_float4(delta, delta * u, gv * zv * sz, gv * (sz * fmaf(zv, 1.f - sz, 1.f)));
-      s1[j * GP] = make_float4(Dd * u, sv, sc, cpre);
+      s0[j * CH] = make_float4(delta, delta * u, gv * zv * sz, gv * (sz * fmaf(zv, 1.f - sz, 1.f)));
+      s1[j * CH] = make_float4(Dd * u, sv, sc, cpre);
     }
     __syncwarp();
 
@@ -1562,16 +1583,16 @@ __global__ void __launch_bounds__(128, 4) m3_bwd2_kernel(BwdArgs a) {
 #pragma unroll
       for (int P = 0; P < 4; ++P) {
         const int n = lane_of(P);
-        h[P] = make_float2(ckt[n * GP + ch], ckt[(n + 1) * GP + ch]);
+        h[P] = make_float2(ckt[n * CH + ch], ckt[(n + 1) * CH + ch]);
       }
 #pragma unroll 2
       for (int j = 0; j < steps; ++j) {
-        const float4 v0 = s0[j * GP];
+        const float4 v0 = s0[j * CH];
         const float2 dl2 = f2b(v0.x);
         const float2 du2 = f2b(v0.y);
 #pragma unroll
         for (int P = 0; P < 4; ++P) {
-          const float2 bb = *reinterpret_cast<const float2*>(fB + j * NS + lane_of(P));
+          const float2 bb = *reinterpret_cast<const float2*>(fB + j * N + lane_of(P));
           h[P] = __ffma2_rn(ex2x2(__fmul2_rn(dl2, a2[P])), h[P], __fmul2_rn(du2, bb));
         }
         tmem_st8(trow + 8u * (uint32_t)j, h);
@@ -1585,8 +1606,8 @@ __global__ void __launch_bounds__(128, 4) m3_bwd2_kernel(BwdArgs a) {
       tmem_ld8(trow + 8u * (uint32_t)(steps - 1), hn);
 #pragma unroll 2
       for (int j = steps - 1; j >= 0; --j) {
-        const float4 v0 = s0[j * GP];
-        const float Du = reinterpret_cast<const float*>(s1 + j * GP)[0];
+        const float4 v0 = s0[j * CH];
+        const float Du = reinterpret_cast<const float*>(s1 + j * CH)[0];
         const float2 dl2 = f2b(v0.x);
         const float2 du2 = f2b(v0.y);
         const float2 dy2 = f2b(v0.z);
@@ -1598,13 +1619,13 @@ __global__ void __launch_bounds__(128, 4) m3_bwd2_kernel(BwdArgs a) {
 #pragma unroll
           for (int P = 0; P < 4; ++P) {
             const int n = lane_of(P);
-            hp[P] = make_float2(ckt[n * GP + ch], ckt[(n + 1) * GP + ch]);
+            hp[P] = make_float2(ckt[n * CH + ch], ckt[(n + 1) * CH + ch]);
           }
         }
 #pragma unroll
         for (int P = 0; P < 4; ++P) {
-          const float2 bb = *reinterpret_cast<const float2*>(fB + j * NS + lane_of(P));
-          const float2 cc = *reinterpret_cast<const float2*>(fC + j * NS + lane_of(P));
+          const float2 bb = *reinterpret_cast<const float2*>(fB + j * N + lane_of(P));
+          const float2 cc = *reinterpret_cast<const float2*>(fC + j * N + lane_of(P));
           y2 = __ffma2_rn(cc, hn[P], y2);
           const float2 dh = __ffma2_rn(dy2, cc, carry[P]);
           pC[P] = __fmul2_rn(dy2, hn[P]);
@@ -1618,30 +1639,40 @@ __global__ void __launch_bounds__(128, 4) m3_bwd2_kernel(BwdArgs a) {
 #pragma unroll
         for (int P = 0; P < 4; ++P) hn[P] = hp[P];
         float ys = y2.x + y2.y, sBs = sB.x + sB.y, sAs = sAq.x + sAq.y;
-        ys += __shfl_xor_sync(0xffffffffu, ys, 1);
-        sBs += __shfl_xor_sync(0xffffffffu, sBs, 1);
-        sAs += __shfl_xor_sync(0xffffffffu, sAs, 1);
-        if (hf == (j & 1)) {
-          if (active) Act<T>::st(static_cast<T*>(a.dz) + row0 + (size_t)j * g.D, (ys + Du) * v0.w);
-          reinterpret_cast<float*>(s0 + j * GP)[3] = sAs;
-          reinterpret_cast<float*>(s1 + j * GP)[0] = sBs;
+#pragma unroll
+        for (int o = 1; o < G; o <<= 1) {
+          ys += __shfl_xor_sync(0xffffffffu, ys, o);
+          sBs += __shfl_xor_sync(0xffffffffu, sBs, o);
+          sAs += __shfl_xor_sync(0xffffffffu, sAs, o);
         }
-        const float rb = warp_sum8_rotated(pB, lane);
-        const float rc = warp_sum8_rotated(pC, lane);
-        if ((lane & 2) == 0) {
+        if (hf == j % G) {
+          if (active) Act<T>::st(static_cast<T*>(a.dz) + row0 + (size_t)j * g.D, (ys + Du) * v0.w);
+          reinterpret_cast<float*>(s0 + j * CH)[3] = sAs;
+          reinterpret_cast<float*>(s1 + j * CH)[0] = sBs;
+        }
+        const float2 rb = warp_sum8_rotated<G>(pB, lane);
+        const float2 rc = warp_sum8_rotated<G>(pC, lane);
+        float* rj = red + (j * 4 + warp) * 2 * N;  // [dB: N][dC: N]
+        if constexpr (G == 8) {
+          const int n = 8 * hf + 2 * prot;
+          rj[n] = rb.x;
+          rj[n + 1] = rb.y;
+          rj[N + n] = rc.x;
+          rj[N + n + 1] = rc.y;
+        } else if (G == 4 || (lane & 2) == 0) {
           const int n = 8 * hf + 2 * prot + ((lane >> 2) & 1);
-          red[(j * 4 + warp) * 32 + n] = rb;
-          red[(j * 4 + warp) * 32 + 16 + n] = rc;
+          rj[n] = rb.x;
+          rj[N + n] = rc.x;
         }
       }
     }
     __syncwarp();
 
-    // ---- du, d delta, softplus and (unless SCAN) SiLU backward, this thread's steps ----
-    for (int j = hf; j < steps; j += 2) {
+    // ---- du, d delta, softplus and (unless SCAN) SiLU backward, every G-th step ----
+    for (int j = hf; j < steps; j += G) {
       const int t = c * K + j;
-      const float4 v0 = s0[j * GP];
-      const float4 v1 = s1[j * GP];
+      const float4 v0 = s0[j * CH];
+      const float4 v1 = s1[j * CH];
       const float delta = v0.x, dy = v0.z, sAq = v0.w;
       const float sumB = v1.x, sv = v1.y, sc = v1.z, cpre = v1.w;
       const float u = cpre * sc;
@@ -1657,18 +1688,18 @@ __global__ void __launch_bounds__(128, 4) m3_bwd2_kernel(BwdArgs a) {
       const float dc = du * (sc * fmaf(cpre, 1.f - sc, 1.f));
       dcb_acc += dc;
 #pragma unroll
-      for (int k = 0; k < WC; ++k) dcw[k] = fmaf(dc, Act<T>::ld(xt + (j + k) * GP + ch), dcw[k]);
-      dcs[j * GP + ch] = dc;
+      for (int k = 0; k < WC; ++k) dcw[k] = fmaf(dc, Act<T>::ld(xt + (j + k) * CH + ch), dcw[k]);
+      dcs[j * CH + ch] = dc;
       if (active && s > 0 && t < t_begin + 3)
         a.dchead[(((size_t)b * g.S + s) * 3 + (t - t_begin)) * g.D + d] = dc;
     }
     if constexpr (!SCAN) {
       __syncwarp();
       // ---- conv backward: d_x from the conv-input gradient of this and the next 3 steps ----
-      for (int j = hf; j < steps; j += 2) {
+      for (int j = hf; j < steps; j += G) {
         const int t = c * K + j;
-        float dxv = fmaf(dcs[j * GP + ch], w[3], fmaf(dcs[(j + 1) * GP + ch], w[2],
-                         fmaf(dcs[(j + 2) * GP + ch], w[1], dcs[(j + 3) * GP + ch] * w[0])));
+        float dxv = fmaf(dcs[j * CH + ch], w[3], fmaf(dcs[(j + 1) * CH + ch], w[2],
+                         fmaf(dcs[(j + 2) * CH + ch], w[1], dcs[(j + 3) * CH + ch] * w[0])));
         if (ST && a.g_conv && t >= g.T - 3 && active)
           dxv += Act<T>::ld(static_cast<const T*>(a.g_conv) + ((size_t)b * 3 + t - (g.T - 3)) * g.D + d);
         if (active) {
@@ -1684,20 +1715,20 @@ __global__ void __launch_bounds__(128, 4) m3_bwd2_kernel(BwdArgs a) {
       // the carried rows (a chunk may be shorter than three steps), all
       // read before any is overwritten
       if (hf == 0) {
-        const float v0 = dcs[ch], v1 = dcs[GP + ch], v2 = dcs[2 * GP + ch];
-        dcs[K * GP + ch] = v0;
-        dcs[(K + 1) * GP + ch] = v1;
-        dcs[(K + 2) * GP + ch] = v2;
+        const float v0 = dcs[ch], v1 = dcs[CH + ch], v2 = dcs[2 * CH + ch];
+        dcs[K * CH + ch] = v0;
+        dcs[(K + 1) * CH + ch] = v1;
+        dcs[(K + 2) * CH + ch] = v2;
       }
     }
 
     __syncthreads();
-    for (int i = tid; i < steps * 32; i += 128) {
-      const int j = i >> 5, l = i & 31;
+    for (int i = tid; i < steps * 2 * N; i += 128) {
+      const int j = i / (2 * N), l = i % (2 * N);
       float v = 0.f;
 #pragma unroll
-      for (int ww = 0; ww < 4; ++ww) v += red[(j * 4 + ww) * 32 + l];
-      float* dst = (l < NS ? a.dB : a.dC) + ((size_t)b * g.T + c * K + j) * g.lddbc + (l & (NS - 1));
+      for (int ww = 0; ww < 4; ++ww) v += red[(j * 4 + ww) * 2 * N + l];
+      float* dst = (l < N ? a.dB : a.dC) + ((size_t)b * g.T + c * K + j) * g.lddbc + (l & (N - 1));
       atomicAdd(dst, v);
     }
     __syncthreads();
@@ -1705,7 +1736,7 @@ __global__ void __launch_bounds__(128, 4) m3_bwd2_kernel(BwdArgs a) {
 
   if (ST && s == 0 && active) {
     if (a.d_h_in) {
-      float* dh0 = a.d_h_in + (size_t)b * NS * g.D + d;
+      float* dh0 = a.d_h_in + (size_t)b * N * g.D + d;
 #pragma unroll
       for (int P = 0; P < 4; ++P) {
         const int n = lane_of(P);
@@ -1715,7 +1746,7 @@ __global__ void __launch_bounds__(128, 4) m3_bwd2_kernel(BwdArgs a) {
     }
     if (!SCAN && a.d_conv_in && hf == 0) {
       // dc of steps 0, 1, 2 (zero past the sequence), kept in rows K.. K+2
-      const float f0 = dcs[K * GP + ch], f1 = dcs[(K + 1) * GP + ch], f2 = dcs[(K + 2) * GP + ch];
+      const float f0 = dcs[K * CH + ch], f1 = dcs[(K + 1) * CH + ch], f2 = dcs[(K + 2) * CH + ch];
       float v[3];
       v[2] = fmaf(f0, w[2], fmaf(f1, w[1], f2 * w[0]));
       v[1] = fmaf(f0, w[1], f1 * w[0]);
@@ -1730,14 +1761,17 @@ __global__ void __launch_bounds__(128, 4) m3_bwd2_kernel(BwdArgs a) {
       }
     }
   }
-  // the pair's per-step partial sums: each thread summed its own steps
-  dD_acc += __shfl_xor_sync(0xffffffffu, dD_acc, 1);
-  ddtb_acc += __shfl_xor_sync(0xffffffffu, ddtb_acc, 1);
-  dcb_acc += __shfl_xor_sync(0xffffffffu, dcb_acc, 1);
+  // the per-step partial sums: each thread of a channel summed its own steps
 #pragma unroll
-  for (int k = 0; k < WC; ++k) dcw[k] += __shfl_xor_sync(0xffffffffu, dcw[k], 1);
+  for (int o = 1; o < G; o <<= 1) {
+    dD_acc += __shfl_xor_sync(0xffffffffu, dD_acc, o);
+    ddtb_acc += __shfl_xor_sync(0xffffffffu, ddtb_acc, o);
+    dcb_acc += __shfl_xor_sync(0xffffffffu, dcb_acc, o);
+#pragma unroll
+    for (int k = 0; k < WC; ++k) dcw[k] += __shfl_xor_sync(0xffffffffu, dcw[k], o);
+  }
   if (active) {
-    float* Pp = a.partials + ((size_t)b * g.S + s) * NPART * g.D;
+    float* Pp = a.partials + ((size_t)b * g.S + s) * NP * g.D;
 #pragma unroll
     for (int P = 0; P < 4; ++P) {
       const int n = lane_of(P);
@@ -1745,11 +1779,11 @@ __global__ void __launch_bounds__(128, 4) m3_bwd2_kernel(BwdArgs a) {
       Pp[(size_t)(n + 1) * g.D + d] = dAp[P].y;
     }
     if (hf == 0) {
-      Pp[(size_t)16 * g.D + d] = dD_acc;
-      Pp[(size_t)17 * g.D + d] = ddtb_acc;
-      Pp[(size_t)18 * g.D + d] = dcb_acc;
+      Pp[(size_t)N * g.D + d] = dD_acc;
+      Pp[(size_t)(N + 1) * g.D + d] = ddtb_acc;
+      Pp[(size_t)(N + 2) * g.D + d] = dcb_acc;
 #pragma unroll
-      for (int k = 0; k < WC; ++k) Pp[(size_t)(19 + k) * g.D + d] = dcw[k];
+      for (int k = 0; k < WC; ++k) Pp[(size_t)(N + 3 + k) * g.D + d] = dcw[k];
     }
   }
   tmem_fence_before_sync();
@@ -1763,8 +1797,10 @@ __global__ void __launch_bounds__(128, 4) m3_bwd2_kernel(BwdArgs a) {
 //    warps and combined in a fixed tree), so the result is deterministic;
 //  - blocks [nfin, ...): d_x at the last three steps of each segment but the
 //    last, which needs the conv gradient of the next segment's first steps.
+// N = d_state: partial rows per channel are N + 8 (N of dA, then dD,
+// d_dt_bias, d_conv_b, d_conv_w[0..3]); nout of them are finalized.
 template <typename T>
-__global__ void m3_bwd_tail_kernel(BwdArgs a, int rows, int nfin, int nout) {
+__global__ void m3_bwd_tail_kernel(BwdArgs a, int rows, int nfin, int nout, int N) {
   const Geo g = a.g;
   grid_dep_wait();  // the main kernel's partials and boundary terms
   if ((int)blockIdx.x >= nfin) {
@@ -1801,7 +1837,7 @@ __global__ void m3_bwd_tail_kernel(BwdArgs a, int rows, int nfin, int nout) {
     float v0 = 0.f, v1 = 0.f;
     if (ok) {
       const float* __restrict__ P = a.partials + (size_t)jj * g.D + d;
-      const size_t stride = (size_t)NPART * g.D;
+      const size_t stride = (size_t)(N + 8) * g.D;
       int r = ry;
 #pragma unroll 4
       for (; r + 8 < rows; r += 16) {
@@ -1817,17 +1853,17 @@ __global__ void m3_bwd_tail_kernel(BwdArgs a, int rows, int nfin, int nout) {
   float v = ((part[0][cx] + part[1][cx]) + (part[2][cx] + part[3][cx])) +
             ((part[4][cx] + part[5][cx]) + (part[6][cx] + part[7][cx]));
   float* dst;
-  if (jj < NS) {
-    v *= -expf(a.a_log[(size_t)d * NS + jj]);  // dL/da_log = dL/dA * A
-    dst = a.d_a_log + (size_t)d * NS + jj;
-  } else if (jj == 16) {
+  if (jj < N) {
+    v *= -expf(a.a_log[(size_t)d * N + jj]);  // dL/da_log = dL/dA * A
+    dst = a.d_a_log + (size_t)d * N + jj;
+  } else if (jj == N) {
     dst = a.dD + d;
-  } else if (jj == 17) {
+  } else if (jj == N + 1) {
     dst = a.d_dt_bias + d;
-  } else if (jj == 18) {
+  } else if (jj == N + 2) {
     dst = a.d_conv_b + d;
   } else {
-    dst = a.d_conv_w + (size_t)d * WC + (jj - 19);
+    dst = a.d_conv_w + (size_t)d * WC + (jj - N - 3);
   }
   *dst = a.accumulate ? *dst + v : v;
 }
@@ -2211,9 +2247,9 @@ __host__ inline size_t bwd_launch_smem(int K, int es, int smem_per_sm) {
 }
 
 // The same residency cap for the two-thread backward.
-__host__ inline size_t bwd2_launch_smem(int K, int es, int smem_per_sm) {
+__host__ inline size_t bwd2_launch_smem(int K, int es, int N, int smem_per_sm) {
   const int max_ctas = 512 / (int)tmem_cols2_for(K);
-  size_t need = bwd2_smem(K, es).total;
+  size_t need = bwd2_smem(K, es, N).total;
   const size_t floor_bytes = (size_t)smem_per_sm / (max_ctas + 1) + 1;
   if (need < floor_bytes) need = floor_bytes;
   return align_up(need, 128);
@@ -2240,6 +2276,19 @@ inline cudaError_t note(cudaError_t e) {
   return e;
 }
 
+// the split kernels for d_state N
+template <typename T, bool ST, bool SCAN>
+void (*bwd2_for(int N))(BwdArgs) {
+  return N == 16 ? m3_bwd2_kernel<T, ST, SCAN, 16>
+       : N == 32 ? m3_bwd2_kernel<T, ST, SCAN, 32> : m3_bwd2_kernel<T, ST, SCAN, 64>;
+}
+template <typename T>
+void (*agg_for(bool split, int N))(BwdArgs) {
+  if (!split) return m3_bwd_agg_kernel<T, 1, 16>;
+  return N == 16 ? m3_bwd_agg_kernel<T, 2, 16>
+       : N == 32 ? m3_bwd_agg_kernel<T, 4, 32> : m3_bwd_agg_kernel<T, 8, 64>;
+}
+
 template <typename T>
 cudaError_t set_attrs() {
   const int es = sizeof(T);
@@ -2255,20 +2304,34 @@ cudaError_t set_attrs() {
                              (int)fwd_smem(es).total);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(m3_fwd_kernel<T, false>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(m3_bwd_agg_kernel<T, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)agg_smem(es).total);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(m3_bwd_agg_kernel<T, 1>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(m3_bwd_agg_kernel<T, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)agg_smem(es).total);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(m3_bwd_agg_kernel<T, 2>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-  void (*const bwd_kernels[8])(BwdArgs) = {
+  const bool splits[4] = {false, true, true, true};
+  const int ns[4] = {16, 16, 32, 64};
+  for (int i = 0; i < 4; ++i) {
+    void (*k)(BwdArgs) = agg_for<T>(splits[i], ns[i]);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)agg_smem(es, ns[i]).total);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+  }
+  for (int N : {16, 32, 64}) {
+    void (*fk[2])(FwdArgs) = {N == 16 ? m3_fwd2_kernel<T, false, 16> : N == 32 ? m3_fwd2_kernel<T, false, 32>
+                                                                                : m3_fwd2_kernel<T, false, 64>,
+                              N == 16 ? m3_fwd2_kernel<T, true, 16> : N == 32 ? m3_fwd2_kernel<T, true, 32>
+                                                                               : m3_fwd2_kernel<T, true, 64>};
+    for (auto k : fk) {
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fwd2_smem(es, N).total);
+      if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    }
+  }
+  void (*const bwd_kernels[16])(BwdArgs) = {
       m3_bwd_kernel<T, false, false>, m3_bwd_kernel<T, true, false>, m3_bwd_kernel<T, false, true>,
-      m3_bwd_kernel<T, true, true>, m3_bwd2_kernel<T, false, false>, m3_bwd2_kernel<T, true, false>,
-      m3_bwd2_kernel<T, false, true>, m3_bwd2_kernel<T, true, true>};
+      m3_bwd_kernel<T, true, true>,
+      bwd2_for<T, false, false>(16), bwd2_for<T, true, false>(16), bwd2_for<T, false, true>(16),
+      bwd2_for<T, true, true>(16),
+      bwd2_for<T, false, false>(32), bwd2_for<T, true, false>(32), bwd2_for<T, false, true>(32),
+      bwd2_for<T, true, true>(32),
+      bwd2_for<T, false, false>(64), bwd2_for<T, true, false>(64), bwd2_for<T, false, true>(64),
+      bwd2_for<T, true, true>(64)};
   for (auto k : bwd_kernels) {
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_CAP);
@@ -2332,6 +2395,7 @@ cudaError_t device_info(int chunk, int ai, int* sms, int* occ_f, int* occ_b, int
 
 struct Plan {
   int B, T, D, K, nc;
+  int N;  // d_state
   int ldbc, lddbc;
   int Sf, mf, Sb, mb;
   size_t ckpt_bytes, ws_bytes;
@@ -2384,7 +2448,10 @@ m3_status validate_dims(const m3_dims* dm, m3_dtype act) {
   if (act != M3_F32 && act != M3_BF16) return M3_ERR_UNSUPPORTED;
   if (dm->batch < 0 || dm->seq_len < 0 || dm->d_inner < 0 || dm->chunk < 0 || dm->segments < 0)
     return M3_ERR_DIMS;
-  if (dm->d_state != NS || dm->d_conv != WC) return M3_ERR_UNSUPPORTED;
+  if ((dm->d_state != 16 && dm->d_state != 32 && dm->d_state != 64) || dm->d_conv != WC)
+    return M3_ERR_UNSUPPORTED;
+  // only the split kernels carry more than 16 lanes per channel
+  if (dm->d_state != NS && dm->threads_per_channel == 1) return M3_ERR_UNSUPPORTED;
   if (dm->d_inner % 8 != 0) return M3_ERR_UNSUPPORTED;
   if (dm->chunk > KMAX) return M3_ERR_DIMS;
   if (dm->chunk > kmax_for(act == M3_BF16 ? 2 : 4)) return M3_ERR_UNSUPPORTED;
@@ -2396,8 +2463,8 @@ m3_status validate_dims(const m3_dims* dm, m3_dtype act) {
   if (dm->bc_stride < 0 || dm->dbc_stride < 0 || dm->bc_stride > ((int64_t)1 << 20) ||
       dm->dbc_stride > ((int64_t)1 << 20))
     return M3_ERR_DIMS;
-  if (dm->bc_stride != 0 && dm->bc_stride < NS) return M3_ERR_DIMS;
-  if (dm->dbc_stride != 0 && dm->dbc_stride < NS) return M3_ERR_DIMS;
+  if (dm->bc_stride != 0 && dm->bc_stride < dm->d_state) return M3_ERR_DIMS;
+  if (dm->dbc_stride != 0 && dm->dbc_stride < dm->d_state) return M3_ERR_DIMS;
   if (dm->bc_stride * (act == M3_BF16 ? 2 : 4) % 16 != 0) return M3_ERR_ALIGN;
   if (dm->threads_per_channel < 0 || dm->threads_per_channel > 2) return M3_ERR_UNSUPPORTED;
   return M3_OK;
@@ -2409,10 +2476,11 @@ m3_status make_plan(const m3_dims* dm, m3_dtype act, Plan* p) {
   p->B = (int)dm->batch;
   p->T = (int)dm->seq_len;
   p->D = (int)dm->d_inner;
+  p->N = (int)dm->d_state;
   p->K = dm->chunk ? (int)dm->chunk : KDEF;
   p->nc = (p->T + p->K - 1) / p->K;
-  p->ldbc = dm->bc_stride ? (int)dm->bc_stride : NS;
-  p->lddbc = dm->dbc_stride ? (int)dm->dbc_stride : NS;
+  p->ldbc = dm->bc_stride ? (int)dm->bc_stride : p->N;
+  p->lddbc = dm->dbc_stride ? (int)dm->dbc_stride : p->N;
   const int groups_f = (p->D + GF - 1) / GF;
   const int groups_b = (p->D + GB - 1) / GB;
   int want_f = 1, want_b = 1;
@@ -2438,7 +2506,8 @@ m3_status make_plan(const m3_dims* dm, m3_dtype act, Plan* p) {
     fix_segments(p->nc, p->K, want_b, &p->Sb, &p->mb);
   }
   const size_t B = p->B, D = p->D;
-  p->ckpt_bytes = B * p->nc * NS * D * 4;
+  const size_t N = p->N;
+  p->ckpt_bytes = B * p->nc * N * D * 4;
   size_t off = 0;
   auto take = [&](size_t bytes) {
     size_t o = off;
@@ -2449,16 +2518,16 @@ m3_status make_plan(const m3_dims* dm, m3_dtype act, Plan* p) {
   off = 0;
   p->f_aggh = p->f_aggs = 0;
   if (p->Sf > 1) {
-    p->f_aggh = take(B * p->Sf * NS * D * 4);
+    p->f_aggh = take(B * p->Sf * N * D * 4);
     p->f_aggs = take(B * p->Sf * D * 4);
   }
   size_t fwd_total = off;
   // backward section (reuses the same bytes)
   off = 0;
-  p->b_part = take(B * p->Sb * NPART * D * 4);
+  p->b_part = take(B * p->Sb * (N + 8) * D * 4);
   p->b_q = p->b_sd = p->b_dxpart = p->b_dchead = 0;
   if (p->Sb > 1) {
-    p->b_q = take(B * p->Sb * NS * D * 4);
+    p->b_q = take(B * p->Sb * N * D * 4);
     p->b_sd = take(B * p->Sb * D * 4);
     p->b_dxpart = take(B * p->Sb * 3 * D * 4);
     p->b_dchead = take(B * p->Sb * 3 * D * 4);
@@ -2474,12 +2543,17 @@ m3_status make_plan(const m3_dims* dm, m3_dtype act, Plan* p) {
   p->ws_bytes = fwd_total > bwd_total ? fwd_total : bwd_total;
   if (p->ws_bytes < 256) p->ws_bytes = 256;
   const bool empty = (size_t)p->B * p->T * p->D == 0;
-  // two threads per channel when the one-thread grid fills less than one
-  // wave (three blocks per SM on a 152-SM GPU, or the device's measured
-  // figure when the segments were chosen for it)
+  // d_state 16: the split kernels (two threads per channel) when the
+  // one-thread grid fills less than one wave (three backward, five forward
+  // blocks per SM on a 152-SM GPU, or the device's figures when the
+  // segments were chosen for it); wider states: always the split kernels,
+  // d_state / 8 threads per channel
   p->fwd_tpc = p->bwd_tpc = dm->threads_per_channel;
   if (p->fwd_tpc == 0) p->fwd_tpc = (int64_t)p->B * groups_f * p->Sf <= wave_f ? 2 : 1;
   if (p->bwd_tpc == 0) p->bwd_tpc = (int64_t)p->B * groups_b * p->Sb <= wave_b ? 2 : 1;
+  if (p->N != NS) p->fwd_tpc = p->bwd_tpc = 2;
+  if (p->fwd_tpc == 2) p->fwd_tpc = p->N / 8;
+  if (p->bwd_tpc == 2) p->bwd_tpc = p->N / 8;
   p->fwd_launches = empty ? 0 : (p->Sf > 1 ? 2 : 1);
   p->bwd_launches = empty ? 0 : (p->Sb > 1 ? 3 : 2);
   return M3_OK;
@@ -2513,12 +2587,16 @@ m3_status launch_fwd(const Plan& p, FwdArgs a, cudaStream_t st) {
   const size_t smem = fwd_smem(sizeof(T)).total;
   a.g = Geo{p.B, p.T, p.D, p.K, p.nc, p.Sf, p.mf, p.ldbc, p.lddbc};
   cudaError_t e = cudaSuccess;
-  if (p.fwd_tpc == 2) {
-    const int groups2 = (p.D + GP - 1) / GP;
-    const size_t smem2 = fwd2_smem(sizeof(T)).total;
-    if (p.Sf > 1) e = launch_k(m3_fwd2_kernel<T, false>, dim3(groups2, p.Sf - 1, p.B), 128, smem2, st, false, a);
-    if (e == cudaSuccess)
-      e = launch_k(m3_fwd2_kernel<T, true>, dim3(groups2, p.Sf, p.B), 128, smem2, st, p.Sf > 1, a);
+  if (p.fwd_tpc != 1) {  // split kernels, N / 8 threads per channel
+    const int ch = 128 / (p.N / 8);
+    const dim3 ga((p.D + ch - 1) / ch, p.Sf - 1, p.B), gf((p.D + ch - 1) / ch, p.Sf, p.B);
+    const size_t smem2 = fwd2_smem(sizeof(T), p.N).total;
+    void (*agg)(FwdArgs) = p.N == 16 ? m3_fwd2_kernel<T, false, 16>
+                         : p.N == 32 ? m3_fwd2_kernel<T, false, 32> : m3_fwd2_kernel<T, false, 64>;
+    void (*fin)(FwdArgs) = p.N == 16 ? m3_fwd2_kernel<T, true, 16>
+                         : p.N == 32 ? m3_fwd2_kernel<T, true, 32> : m3_fwd2_kernel<T, true, 64>;
+    if (p.Sf > 1) e = launch_k(agg, ga, 128, smem2, st, false, a);
+    if (e == cudaSuccess) e = launch_k(fin, gf, 128, smem2, st, p.Sf > 1, a);
     if (e == cudaSuccess) e = cudaGetLastError();
     return note(e) == cudaSuccess ? M3_OK : M3_ERR_CUDA;
   }
@@ -2537,26 +2615,25 @@ m3_status launch_bwd(const Plan& p, BwdArgs a, cudaStream_t st, int smem_per_sm,
   cudaError_t e = cudaSuccess;
   if (p.Sb > 1) {
     // also clears dB and dC before the main kernel's reductions into them
-    if (p.bwd_tpc == 2)
-      e = launch_k(m3_bwd_agg_kernel<T, 2>, dim3((p.D + GP - 1) / GP, p.Sb - 1, p.B), GB,
-                   agg_smem(sizeof(T)).total, st, false, a);
-    else
-      e = launch_k(m3_bwd_agg_kernel<T, 1>, dim3(groups, p.Sb - 1, p.B), GB, agg_smem(sizeof(T)).total,
-                   st, false, a);
+    const bool split = p.bwd_tpc != 1;
+    const int ch = split ? 128 / (p.N / 8) : GB;
+    e = launch_k(agg_for<T>(split, p.N), dim3((p.D + ch - 1) / ch, p.Sb - 1, p.B), GB,
+                 agg_smem(sizeof(T), p.N).total, st, false, a);
     if (note(e) != cudaSuccess) return M3_ERR_CUDA;
   } else {
-    // only the 16 columns of each (batch, step) row belong to dB and dC
+    // only the d_state columns of each (batch, step) row belong to dB and dC
     const size_t pitch = (size_t)p.lddbc * 4, rows = (size_t)p.B * p.T;
-    if (note(cudaMemset2DAsync(a.dB, pitch, 0, NS * 4, rows, st)) != cudaSuccess) return M3_ERR_CUDA;
-    if (note(cudaMemset2DAsync(a.dC, pitch, 0, NS * 4, rows, st)) != cudaSuccess) return M3_ERR_CUDA;
+    if (note(cudaMemset2DAsync(a.dB, pitch, 0, (size_t)p.N * 4, rows, st)) != cudaSuccess) return M3_ERR_CUDA;
+    if (note(cudaMemset2DAsync(a.dC, pitch, 0, (size_t)p.N * 4, rows, st)) != cudaSuccess) return M3_ERR_CUDA;
   }
   const bool with_state = a.conv_in || a.g_h || a.g_conv || a.d_h_in || a.d_conv_in;
-  if (p.bwd_tpc == 2) {
+  if (p.bwd_tpc != 1) {
     a.tcols = tmem_cols2_for(p.K);
-    const size_t smem = bwd2_launch_smem(p.K, sizeof(T), smem_per_sm);
-    void (*kern)(BwdArgs) = scan ? (with_state ? m3_bwd2_kernel<T, true, true> : m3_bwd2_kernel<T, false, true>)
-                                 : (with_state ? m3_bwd2_kernel<T, true, false> : m3_bwd2_kernel<T, false, false>);
-    e = launch_k(kern, dim3((p.D + GP - 1) / GP, p.Sb, p.B), 128, smem, st, p.Sb > 1, a);
+    const size_t smem = bwd2_launch_smem(p.K, sizeof(T), p.N, smem_per_sm);
+    void (*kern)(BwdArgs) = scan ? (with_state ? bwd2_for<T, true, true>(p.N) : bwd2_for<T, false, true>(p.N))
+                                 : (with_state ? bwd2_for<T, true, false>(p.N) : bwd2_for<T, false, false>(p.N));
+    const int ch = 128 / (p.N / 8);
+    e = launch_k(kern, dim3((p.D + ch - 1) / ch, p.Sb, p.B), 128, smem, st, p.Sb > 1, a);
   } else {
     a.tcols = tmem_cols_for(p.K);
     const size_t smem = bwd_launch_smem(p.K, sizeof(T), smem_per_sm);
@@ -2564,13 +2641,13 @@ m3_status launch_bwd(const Plan& p, BwdArgs a, cudaStream_t st, int smem_per_sm,
                                  : (with_state ? m3_bwd_kernel<T, true, false> : m3_bwd_kernel<T, false, false>);
     e = launch_k(kern, dim3(groups, p.Sb, p.B), GB, smem, st, p.Sb > 1, a);
   }
-  // parameter outputs: 16 d_a_log, dD, d_dt_bias (+ d_conv_b, 4 d_conv_w)
-  const int nout = scan ? 18 : 23;
+  // parameter outputs: N d_a_log, dD, d_dt_bias (+ d_conv_b, 4 d_conv_w)
+  const int nout = scan ? p.N + 2 : p.N + 7;
   const size_t nfin = ((size_t)nout * p.D + 31) / 32;                 // 32 outputs per block
   const size_t nfix = (!scan && p.Sb > 1) ? ((size_t)p.B * (p.Sb - 1) * 3 * p.D + 255) / 256 : 0;
   if (e == cudaSuccess)
     e = launch_k(m3_bwd_tail_kernel<T>, dim3((unsigned)(nfin + nfix)), 256, 0, st, true, a,
-                 p.B * p.Sb, (int)nfin, nout);
+                 p.B * p.Sb, (int)nfin, nout, p.N);
   if (e == cudaSuccess) e = cudaGetLastError();
   return note(e) == cudaSuccess ? M3_OK : M3_ERR_CUDA;
 }
@@ -2593,7 +2670,7 @@ const char* m3scan_status_string(m3_status s) {
     case M3_ERR_NULL: return "M3_ERR_NULL: a required pointer is NULL";
     case M3_ERR_DIMS: return "M3_ERR_DIMS: a size is negative or out of range";
     case M3_ERR_UNSUPPORTED:
-      return "M3_ERR_UNSUPPORTED: needs d_state 16, d_conv 4, d_inner % 8 == 0, dtype f32 or bf16";
+      return "M3_ERR_UNSUPPORTED: needs d_state 16, 32 or 64, d_conv 4, d_inner % 8 == 0, dtype f32 or bf16";
     case M3_ERR_ALIGN: return "M3_ERR_ALIGN: a pointer is not aligned as required";
     case M3_ERR_WORKSPACE: return "M3_ERR_WORKSPACE: workspace missing or too small";
     case M3_ERR_CUDA: return "M3_ERR_CUDA: a CUDA call or kernel launch failed";
@@ -2659,7 +2736,7 @@ m3_status fwd_impl(const m3_dims* dims, m3_dtype act, const void* x, const void*
   if ((size_t)p.B * p.T * p.D == 0) {
     const size_t bd = (size_t)p.B * p.D;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    st = pass_state(sv.ssm_state, sv.ssm_state_out, bd * NS * 4, s);
+    st = pass_state(sv.ssm_state, sv.ssm_state_out, bd * p.N * 4, s);
     if (st == M3_OK) st = pass_state(sv.conv_state, sv.conv_state_out, bd * 3 * (act == M3_BF16 ? 2 : 4), s);
     return st;
   }
@@ -2711,7 +2788,7 @@ m3_status bwd_impl(const m3_dims* dims, m3_dtype act, const void* x, const void*
     return M3_ERR_ALIGN;
   if ((size_t)p.B * p.T * p.D == 0) {
     const size_t bd = (size_t)p.B * p.D;
-    st = pass_state(sv.d_ssm_state_out, sv.d_ssm_state, bd * NS * 4, s);
+    st = pass_state(sv.d_ssm_state_out, sv.d_ssm_state, bd * p.N * 4, s);
     if (st == M3_OK)
       st = pass_state(sv.d_conv_state_out, sv.d_conv_state, bd * 3 * (act == M3_BF16 ? 2 : 4), s);
     if (st != M3_OK) return st;
@@ -2722,7 +2799,7 @@ m3_status bwd_impl(const m3_dims* dims, m3_dtype act, const void* x, const void*
       if ((!scan && (cudaMemsetAsync(d_conv_w, 0, D_ * WC * 4, s) != cudaSuccess ||
                      cudaMemsetAsync(d_conv_b, 0, D_ * 4, s) != cudaSuccess)) ||
           cudaMemsetAsync(d_dt_bias, 0, D_ * 4, s) != cudaSuccess ||
-          cudaMemsetAsync(d_a_log, 0, D_ * NS * 4, s) != cudaSuccess ||
+          cudaMemsetAsync(d_a_log, 0, D_ * p.N * 4, s) != cudaSuccess ||
           cudaMemsetAsync(dD, 0, D_ * 4, s) != cudaSuccess) {
         note(cudaGetLastError());
         return M3_ERR_CUDA;

@@ -169,7 +169,10 @@ def test_bwd_rejects_bad_arguments_before_any_launch(lib):
     assert _bwd(dims, workspace=None) == "M3_ERR_WORKSPACE"
     assert _bwd(dims, workspace_bytes=255) == "M3_ERR_WORKSPACE"
     assert _bwd(dims, workspace=A + 128) == "M3_ERR_ALIGN"
-    assert _bwd(binding.make_dims(2, 64, 64, d_state=32, segments=1)) == "M3_ERR_UNSUPPORTED"
+    assert _bwd(binding.make_dims(2, 64, 64, d_state=24, segments=1)) == "M3_ERR_UNSUPPORTED"
+    # wider states run on the split kernels only
+    assert _bwd(binding.make_dims(2, 64, 64, d_state=32, segments=1,
+                                  threads_per_channel=1)) == "M3_ERR_UNSUPPORTED"
 
 
 def _fwd_state(dims, state, act=binding.M3_BF16, **over):
@@ -314,3 +317,12 @@ def test_threads_per_channel_are_resolved_from_the_grid(lib):
     assert tpc(8, 2048, 1536, 12, want=2) == (2, 2)  # an explicit choice wins
     assert tpc(8, 128, 512, 8, want=1) == (1, 1)
     assert tpc(8, 128, 512, 8, want=3) == "M3_ERR_UNSUPPORTED"
+
+
+def test_wider_states_resolve_to_the_split_kernels(lib):
+    for n, tpc in ((32, 4), (64, 8)):
+        out = binding.M3Plan()
+        d = binding.make_dims(2, 256, 512, d_state=n, chunk=8, segments=2)
+        assert lib.m3scan_plan(ctypes.byref(d), binding.M3_BF16, ctypes.byref(out)) == 0
+        assert (out.fwd_threads_per_channel, out.bwd_threads_per_channel) == (tpc, tpc)
+        assert out.ckpt_bytes == 2 * 32 * n * 512 * 4

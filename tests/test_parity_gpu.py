@@ -161,3 +161,23 @@ def test_workload_full_size_sampled(name):
 def oracle_masked_dbdc(inp, mask):
     import oracle
     return oracle.backward(inp, chan_mask=mask)
+
+
+WIDE = [
+    # batch, T, D, act, chunk, segments, d_state
+    (2, 100, 64, "f32", 8, 3, 32),
+    (2, 97, 48, "bf16", 16, 2, 64),
+    (1, 40, 24, "f32", 2, 4, 64),
+    (3, 33, 136, "bf16", 0, 0, 32),
+    (1, 3, 8, "f32", 1, 0, 64),
+]
+
+
+@pytest.mark.parametrize("batch,T,D,act,chunk,segments,N", WIDE)
+def test_wider_states_match_oracle(batch, T, D, act, chunk, segments, N):
+    """d_state 32 and 64 (the split kernels, d_state / 8 threads per channel)."""
+    inp = make_inputs(batch, T, D, act=act, seed=batch * 100 + T + N, d_state=N)
+    dev = to_device(inp)
+    gpu = run_gpu(dev, chunk=chunk, segments=segments)
+    ref = run_oracle(inp)
+    assert_close(compare(gpu, ref, act), f"B={batch} T={T} D={D} {act} K={chunk} S={segments} N={N}")

@@ -197,3 +197,13 @@ def test_two_gpu_windows_equal_one_gpu_window():
         assert norm_err(to_np(b1[k]) + to_np(b2[k]), full[k]) <= tol[k], k
     for k in ("d_ssm_state", "d_conv_state"):
         assert norm_err(to_np(b1[k]), full[k]) <= 1e-4, k
+
+
+@pytest.mark.parametrize("N", [32, 64])
+def test_wider_state_windows_match_oracle(N):
+    batch, T, D, act = 2, 50, 40, "bf16"
+    inp = make_inputs(batch, T, D, act=act, seed=N, d_state=N)
+    st = make_state_inputs(batch, D, act=act, seed=N, d_state=N)
+    gpu = _gpu(to_device(inp), _state_to_device(st, act), 8, 3)
+    ref = _oracle(inp, st, ALL)
+    _check(gpu, ref, act, f"N={N}")

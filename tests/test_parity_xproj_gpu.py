@@ -160,3 +160,21 @@ def test_two_phase_without_extra_equals_one_call_backward():
     # are added in another order
     for k in ("d_x", "dB", "dC", "d_conv_w", "d_conv_b"):
         assert norm_err(to_np(two[k]), to_np(one[k])) <= 1e-6, k
+
+
+def test_two_phase_backward_with_wider_state():
+    batch, T, D, act, N = 2, 60, 40, "f32", 32
+    inp = make_inputs(batch, T, D, act=act, seed=21, d_state=N)
+    dev = to_device(inp)
+    du_extra = np.random.default_rng(21).standard_normal((batch, T, D)).astype(np.float32)
+    gated, ckpt, _ = binding.m3scan_fwd(dev["x"], dev["delta_raw"], dev["z"], dev["B"], dev["C"],
+                                        dev["conv_w"], dev["conv_b"], dev["dt_bias"],
+                                        dev["a_log"], dev["D"], chunk=8, segments=2)
+    o = binding.m3scan_bwd_two_phase(dev["x"], dev["delta_raw"], dev["z"], dev["B"], dev["C"],
+                                     dev["conv_w"], dev["conv_b"], dev["dt_bias"], dev["a_log"],
+                                     dev["D"], ckpt, dev["d_gated"], lambda g: _act(du_extra, act),
+                                     chunk=8, segments=2)
+    torch.cuda.synchronize()
+    ref = oracle.backward(inp, d_u_extra=du_extra)
+    for k in ("du", "dB", "dC", "d_a_log", "d_x", "d_conv_w"):
+        assert norm_err(to_np(o[k]), ref[k]) <= TOL[act][k], k
