@@ -91,8 +91,11 @@ def alu_peak_gops():
 
 def source_hash():
     h = hashlib.sha256()
-    with open(os.path.join(ROOT, "mamba_selective_scan_gb300", "csrc", "m3scan.cu"), "rb") as f:
-        h.update(f.read())
+    csrc = os.path.join(ROOT, "mamba_selective_scan_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(f.read())
     return h.hexdigest()[:16]
 
 

@@ -2,14 +2,16 @@
 
 from __future__ import annotations
 
+import glob
 import os
 import shutil
 import subprocess
 import sys
+from concurrent.futures import ThreadPoolExecutor
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
-SRC = os.path.join(HERE, "csrc", "m3scan.cu")
+CSRC = os.path.join(HERE, "csrc")
 HEADER = os.path.join(ROOT, "include", "m3scan.h")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libm3scan.so")
@@ -26,29 +28,58 @@ def nvcc_path() -> str:
     raise RuntimeError("nvcc not found: the CUDA toolkit is required to build libm3scan")
 
 
+def sources():
+    """The translation units of the library (compiled in parallel)."""
+    return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+
+
+def _inputs():
+    return sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + [HEADER, __file__]
+
+
 def _stale() -> bool:
     if not os.path.exists(LIB_PATH):
         return True
     t = os.path.getmtime(LIB_PATH)
-    return any(os.path.getmtime(f) > t for f in (SRC, HEADER, __file__))
+    return any(os.path.getmtime(f) > t for f in _inputs())
+
+
+def _run(cmd, verbose):
+    res = subprocess.run(cmd, capture_output=True, text=True)
+    if res.returncode != 0:
+        raise RuntimeError(f"nvcc failed ({res.returncode}): {' '.join(cmd)}\n{res.stdout}\n{res.stderr}")
+    if verbose:
+        sys.stderr.write(res.stderr)
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile csrc/m3scan.cu into _build/libm3scan.so (static cudart)."""
+    """Compile csrc/*.cu (in parallel) and link _build/libm3scan.so (static
+    cudart)."""
     if not force and not _stale():
         return LIB_PATH
     os.makedirs(BUILD_DIR, exist_ok=True)
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
-    cmd = [nvcc_path(), *ARCH_FLAGS, "-O3", "-lineinfo", "-std=c++17",
-           "-Xcompiler", "-fPIC", "-shared", "-o", tmp, SRC]
-    if verbose:
-        cmd.insert(1, "-Xptxas=-v")
-    res = subprocess.run(cmd, capture_output=True, text=True)
-    if res.returncode != 0:
-        raise RuntimeError(f"nvcc failed ({res.returncode}):\n{res.stdout}\n{res.stderr}")
-    if verbose:
-        sys.stderr.write(res.stderr)
-    os.replace(tmp, LIB_PATH)
+    nvcc = nvcc_path()
+    tag = f".tmp{os.getpid()}"
+    objs = []
+    cmds = []
+    for src in sources():
+        obj = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + tag + ".o")
+        objs.append(obj)
+        cmd = [nvcc, *ARCH_FLAGS, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
+               "-c", "-o", obj, src]
+        if verbose:
+            cmd.insert(1, "-Xptxas=-v")
+        cmds.append(cmd)
+    try:
+        with ThreadPoolExecutor(max_workers=len(cmds)) as ex:
+            list(ex.map(lambda c: _run(c, verbose), cmds))
+        tmp = LIB_PATH + tag
+        _run([nvcc, *ARCH_FLAGS, "-shared", "-o", tmp, *objs], verbose)
+        os.replace(tmp, LIB_PATH)
+    finally:
+        for o in objs:
+            if os.path.exists(o):
+                os.remove(o)
     return LIB_PATH
 
 

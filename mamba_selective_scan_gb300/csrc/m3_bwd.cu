@@ -1,0 +1,1139 @@
+// m3_bwd.cu -- the backward kernels (segment carries, the one-thread and
+// split main kernels, the parameter-gradient tail) and their launch.
+#include "m3_common.cuh"
+
+namespace m3 {
+
+// ---------------------------------------------------------------------------
+// backward aggregate (segments 1..S-1): the adjoint carry a segment passes to
+// its predecessor when nothing enters it from the right,
+//   carry_t = exp(delta_t A) * (dy_t C_t + carry_{t+1}),
+// and the summed step size (the segment's total decay).
+// ---------------------------------------------------------------------------
+
+// TPC threads per channel: one (16 lanes each, d_state 16) or d_state / 8
+// (8 lanes each, 128 / TPC channels per block), the threads of a channel
+// taking the scalar pass of every TPC-th step.
+template <typename T, int TPC, int N>
+__global__ void __launch_bounds__(GB) m3_bwd_agg_kernel(BwdArgs a) {
+  constexpr int G = GB / TPC;        // channels per block
+  constexpr int NL = N / TPC;        // state lanes per thread
+  extern __shared__ __align__(128) unsigned char smem[];
+  const Geo g = a.g;
+  const int tid = threadIdx.x;
+  const int hf = tid % TPC;
+  const int ch = tid / TPC;
+  const int d0 = blockIdx.x * G;
+  const int s = blockIdx.y + 1;
+  const int b = blockIdx.z;
+  const int d = d0 + ch;
+  const bool active = d < g.D;
+  const int t_begin = s * g.m * g.K;
+  const int t_end = min((s + 1) * g.m * g.K, g.T);
+  const AggSmem L = agg_smem(sizeof(T), N);
+  float* fC = reinterpret_cast<float*>(smem + L.fC);
+  const int ntiles = (t_end - t_begin + TT - 1) / TT;
+  auto tile_start = [&](int i) { return max(t_begin, t_end - (i + 1) * TT); };
+  auto stage = [&](int i, int buf) {
+    unsigned char* base = smem + (size_t)buf * L.tile;
+    const int t0 = tile_start(i);
+    const int rows = (t_end - i * TT) - t0;
+    stage_rows<T, G, GB>(reinterpret_cast<T*>(base + L.dr), static_cast<const T*>(a.dr), b, t0, rows, g.T, g.T, g.D, d0, tid);
+    stage_rows<T, G, GB>(reinterpret_cast<T*>(base + L.z), static_cast<const T*>(a.z), b, t0, rows, g.T, g.T, g.D, d0, tid);
+    stage_rows<T, G, GB>(reinterpret_cast<T*>(base + L.dg), static_cast<const T*>(a.dg), b, t0, rows, g.T, g.T, g.D, d0, tid);
+    stage_bc<T, GB, N>(reinterpret_cast<T*>(base + L.Ct), static_cast<const T*>(a.Cm), b, t0, rows, g.T, g.T, g.ldbc, tid);
+    cp_async_commit();
+  };
+
+  stage(0, 0);  // first tile in flight while the parameters load
+  grid_dep_trigger();
+
+  float2 a2[NL / 2];
+#pragma unroll
+  for (int i = 0; i < NL / 2; ++i) {
+    const int n = NL * hf + 2 * i;
+    a2[i].x = active ? -expf(a.a_log[(size_t)d * N + n]) * LOG2E : 0.f;
+    a2[i].y = active ? -expf(a.a_log[(size_t)d * N + n + 1]) * LOG2E : 0.f;
+  }
+  const float dtb = active ? a.dt_bias[d] : 0.f;
+  float2 carry[NL / 2];
+#pragma unroll
+  for (int i = 0; i < NL / 2; ++i) carry[i] = make_float2(0.f, 0.f);
+  float sdelta = 0.f;
+
+  {
+    // dB and dC are sums over channel groups (global reductions in the main
+    // kernel): this kernel runs before it, so it clears them.
+    const size_t ncta = (size_t)gridDim.x * gridDim.y * gridDim.z;
+    const size_t cid = blockIdx.x + (size_t)gridDim.x * (blockIdx.y + (size_t)gridDim.y * blockIdx.z);
+    const size_t total = (size_t)g.B * g.T * N;
+    for (size_t i = cid * GB + tid; i < total; i += ncta * GB) {
+      const size_t o = (i / N) * g.lddbc + (i % N);
+      a.dB[o] = 0.f;
+      a.dC[o] = 0.f;
+    }
+  }
+  for (int i = 0; i < ntiles; ++i) {
+    const int buf = i & 1;
+    if (i + 1 < ntiles) {
+      stage(i + 1, buf ^ 1);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();
+    const unsigned char* base = smem + (size_t)buf * L.tile;
+    const int t0 = tile_start(i);
+    const int steps = (t_end - i * TT) - t0;
+    {
+      const T* Ct = reinterpret_cast<const T*>(base + L.Ct);
+      for (int k = tid; k < steps * N; k += GB) fC[k] = Act<T>::ld(Ct + k);
+    }
+    __syncthreads();
+    const T* drt = reinterpret_cast<const T*>(base + L.dr);
+    const T* zt = reinterpret_cast<const T*>(base + L.z);
+    const T* dgt = reinterpret_cast<const T*>(base + L.dg);
+    float2* scs = reinterpret_cast<float2*>(smem + L.sc) + ch;  // per channel, stride G
+#pragma unroll 4
+    for (int j = hf; j < steps; j += TPC) {  // scalar pass
+      const float zv = Act<T>::ld(zt + j * G + ch);
+      const float dy = Act<T>::ld(dgt + j * G + ch) * zv * sigmoid_f(zv);
+      const float delta = softplus_f(Act<T>::ld(drt + j * G + ch) + dtb);
+      scs[j * G] = make_float2(delta, dy);
+    }
+    if (TPC > 1) __syncwarp();
+#pragma unroll 4
+    for (int j = steps - 1; j >= 0; --j) {  // state pass
+      const float2 v = scs[j * G];
+      sdelta += v.x;
+      const float2 dl2 = f2b(v.x);
+      const float2 dy2 = f2b(v.y);
+      const float2* C2 = reinterpret_cast<const float2*>(fC + j * N + NL * hf);
+#pragma unroll
+      for (int q = 0; q < NL / 2; ++q) {
+        carry[q] = __fmul2_rn(ex2x2(__fmul2_rn(dl2, a2[q])), __ffma2_rn(dy2, C2[q], carry[q]));
+      }
+    }
+    __syncthreads();
+  }
+  if (active) {
+    const size_t bs = (size_t)b * g.S + s;
+#pragma unroll
+    for (int i = 0; i < NL / 2; ++i) {
+      a.q[(bs * N + NL * hf + 2 * i) * g.D + d] = carry[i].x;
+      a.q[(bs * N + NL * hf + 2 * i + 1) * g.D + d] = carry[i].y;
+    }
+    if (hf == 0) a.sd[bs * g.D + d] = sdelta;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// backward main kernel
+//
+// Each thread keeps its 16 state lanes in 4 quads whose order is rotated by
+// the lane's two low bits: register quad qs holds state quad qs ^ (lane & 3).
+// The dB/dC sum over the warp's 32 channels then starts with two
+// butterfly levels that need no selects (partners hold the same state lane
+// in the same register), as the reduce-scatter below relies on.
+// ---------------------------------------------------------------------------
+
+// Sum over the 32 lanes of v[0..15] (v[s] holds state lane
+// 4 * ((s >> 2) ^ (lane & 3)) + (s & 3)); returns the total for state lane
+// 4 * (lane & 3) + 2 * ((lane >> 3) & 1) + ((lane >> 2) & 1).
+__device__ __forceinline__ float warp_sum16_rotated(float (&v)[NS], int lane) {
+#pragma unroll
+  for (int s = 0; s < 8; ++s) v[s] += __shfl_xor_sync(0xffffffffu, v[s + 8], 2);
+#pragma unroll
+  for (int s = 0; s < 4; ++s) v[s] += __shfl_xor_sync(0xffffffffu, v[s + 4], 1);
+  {
+    const bool up = (lane & 8) != 0;
+    const float s0 = up ? v[0] : v[2], s1 = up ? v[1] : v[3];
+    const float k0 = up ? v[2] : v[0], k1 = up ? v[3] : v[1];
+    v[0] = k0 + __shfl_xor_sync(0xffffffffu, s0, 8);
+    v[1] = k1 + __shfl_xor_sync(0xffffffffu, s1, 8);
+  }
+  {
+    const bool up = (lane & 4) != 0;
+    const float s0 = up ? v[0] : v[1];
+    const float k0 = up ? v[1] : v[0];
+    v[0] = k0 + __shfl_xor_sync(0xffffffffu, s0, 4);
+  }
+  return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 16);
+}
+
+// ST: compiled with the carried-state terms; the plain entry points run the
+// instance without them.  SCAN: stop at du (written out) -- the SiLU and
+// conv backward then run in m3_conv_bwd_kernel with du plus any gradient
+// reaching u from outside the layer core.
+template <typename T, bool ST, bool SCAN>
+__global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(BwdArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const Geo g = a.g;
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  const int rot = lane & 3;
+  const int d0 = blockIdx.x * GB;
+  const int s = blockIdx.y;
+  const int b = blockIdx.z;
+  const int d = d0 + tid;
+  const bool active = d < g.D;
+  const int c_begin = s * g.m;
+  const int c_end = min(c_begin + g.m, g.nc);
+  const int t_begin = c_begin * g.K;
+  const int t_end = min(c_end * g.K, g.T);
+  const int K = g.K;
+  const BwdSmem L = bwd_smem(K, sizeof(T));
+  float* fB = reinterpret_cast<float*>(smem + L.fB);
+  float* fC = reinterpret_cast<float*>(smem + L.fC);
+  float* red = reinterpret_cast<float*>(smem + L.red);
+  // state lane of register slot 2*i (pair i): quad (i >> 1) ^ rot, offset 2*(i & 1)
+  auto lane_of = [&](int i) { return 4 * ((i >> 1) ^ rot) + 2 * (i & 1); };
+
+  // The recomputed states of a chunk (K rows of 16 f32 per channel) live in
+  // tensor memory: row j of this thread = columns [16 j, 16 j + 16) of its
+  // lane.  Warp 0 allocates for the CTA; every exit path below deallocates.
+  __shared__ uint32_t tmem_slot;
+  if (warp == 0) tmem_alloc(&tmem_slot, a.tcols);
+  tmem_fence_before_sync();
+  __syncthreads();
+  tmem_fence_after_sync();
+  const uint32_t trow = tmem_slot + ((uint32_t)(warp * 32) << 16);
+
+  float2 a2[NS / 2];
+  float w[WC];
+  float cb = 0.f, dtb = 0.f, Dd = 0.f;
+#pragma unroll
+  for (int i = 0; i < NS / 2; ++i) {
+    const int n = lane_of(i);
+    a2[i].x = active ? -expf(a.a_log[(size_t)d * NS + n]) * LOG2E : 0.f;
+    a2[i].y = active ? -expf(a.a_log[(size_t)d * NS + n + 1]) * LOG2E : 0.f;
+  }
+#pragma unroll
+  for (int k = 0; k < WC; ++k) w[k] = active ? a.conv_w[(size_t)d * WC + k] : 0.f;
+  if (active) {
+    cb = a.conv_b[d];
+    dtb = a.dt_bias[d];
+    Dd = a.Dp[d];
+  }
+
+  // adjoint carry entering the segment's last step from the right:
+  // exp(delta_{t+1} A) dh_{t+1}
+  float2 carry[NS / 2];
+#pragma unroll
+  for (int i = 0; i < NS / 2; ++i) carry[i] = make_float2(0.f, 0.f);
+  if (ST && a.g_h && active) {  // the gradient of the state output enters after the last step
+    const float* gh = a.g_h + (size_t)b * NS * g.D + d;
+#pragma unroll
+    for (int i = 0; i < NS / 2; ++i) {
+      const int n = lane_of(i);
+      carry[i] = make_float2(gh[(size_t)n * g.D], gh[(size_t)(n + 1) * g.D]);
+    }
+  }
+  const T* xg = static_cast<const T*>(a.x);
+  auto stage = [&](int c, int buf) {
+    unsigned char* base = smem + (size_t)buf * L.tile;
+    const int t0 = c * K;
+    stage_rows<T, GB, GB>(reinterpret_cast<T*>(base + L.x), xg, b, t0 - 3, K + 3, g.T, g.T, g.D, d0, tid);
+    stage_rows<T, GB, GB>(reinterpret_cast<T*>(base + L.dr), static_cast<const T*>(a.dr), b, t0, K, g.T, g.T, g.D, d0, tid);
+    stage_rows<T, GB, GB>(reinterpret_cast<T*>(base + L.z), static_cast<const T*>(a.z), b, t0, K, g.T, g.T, g.D, d0, tid);
+    stage_rows<T, GB, GB>(reinterpret_cast<T*>(base + L.dg), static_cast<const T*>(a.dg), b, t0, K, g.T, g.T, g.D, d0, tid);
+    stage_bc<T, GB>(reinterpret_cast<T*>(base + L.Bt), static_cast<const T*>(a.Bm), b, t0, K, g.T, g.T, g.ldbc, tid);
+    stage_bc<T, GB>(reinterpret_cast<T*>(base + L.Ct), static_cast<const T*>(a.Cm), b, t0, K, g.T, g.T, g.ldbc, tid);
+    // chunk start state: 16 rows of GB floats from ckpt[b, c, :, d0:d0+GB]
+    stage_rows<float, GB, GB>(reinterpret_cast<float*>(base + L.ck), a.ckpt + ((size_t)b * g.nc + c) * NS * g.D,
+                              0, 0, NS, NS, NS, g.D, d0, tid);
+    cp_async_commit();
+  };
+
+  stage(c_end - 1, 0);  // last chunk in flight while the carries load
+  grid_dep_trigger();
+  // the aggregate kernel's carries, and its clearing of dB and dC before
+  // this kernel's reductions into them
+  grid_dep_wait();
+  if (s + 1 < g.S) {
+    // chain the later segments right to left: in(s'-1) = exp(A sum delta_s')
+    // in(s') + local(s'), with in(S-1) = 0
+    const float* __restrict__ sd = a.sd;
+    const float* __restrict__ q = a.q;
+#pragma unroll 2
+    for (int sp = g.S - 1; sp > s; --sp) {
+      const size_t bs = (size_t)b * g.S + sp;
+      const float2 dl2 = f2b(active ? sd[bs * g.D + d] : 0.f);
+#pragma unroll
+      for (int i = 0; i < NS / 2; ++i) {
+        const float* qq = q + (bs * NS + lane_of(i)) * g.D + d;
+        const float2 loc = active ? make_float2(qq[0], qq[g.D]) : make_float2(0.f, 0.f);
+        carry[i] = __ffma2_rn(ex2x2(__fmul2_rn(dl2, a2[i])), carry[i], loc);
+      }
+    }
+  }
+  float2 dAp[NS / 2];  // dL/dA per lane
+#pragma unroll
+  for (int i = 0; i < NS / 2; ++i) dAp[i] = make_float2(0.f, 0.f);
+  float dD_acc = 0.f, ddtb_acc = 0.f, dcb_acc = 0.f;
+  float dcw[WC] = {0.f, 0.f, 0.f, 0.f};
+  float dc1 = 0.f, dc2 = 0.f, dc3 = 0.f;  // conv-input gradient at t+1, t+2, t+3
+
+  for (int c = c_end - 1; c >= c_begin; --c) {
+    const int buf = (c_end - 1 - c) & 1;
+    if (c - 1 >= c_begin) {
+      stage(c - 1, buf ^ 1);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();
+    const unsigned char* base = smem + (size_t)buf * L.tile;
+    if (ST && a.conv_in && c * K < 3 && active) {
+      // halo rows before step 0 (staged as zeros): the carried conv inputs.
+      // Only this thread reads its column of the x tile.
+      T* xw = reinterpret_cast<T*>(smem + (size_t)buf * L.tile + L.x);
+      const T* ci = static_cast<const T*>(a.conv_in) + (size_t)b * 3 * g.D + d;
+      for (int r = 0; r < 3 - c * K; ++r) xw[r * GB + tid] = ci[(size_t)(c * K + r) * g.D];
+    }
+    {
+      const T* Bt = reinterpret_cast<const T*>(base + L.Bt);
+      const T* Ct = reinterpret_cast<const T*>(base + L.Ct);
+      for (int i = tid; i < K * NS; i += GB) {
+        fB[i] = Act<T>::ld(Bt + i);
+        fC[i] = Act<T>::ld(Ct + i);
+      }
+    }
+    __syncthreads();
+    const T* xt = reinterpret_cast<const T*>(base + L.x);  // row r is step c*K - 3 + r
+    const T* drt = reinterpret_cast<const T*>(base + L.dr);
+    const T* zt = reinterpret_cast<const T*>(base + L.z);
+    const T* dgt = reinterpret_cast<const T*>(base + L.dg);
+    const float* ckt = reinterpret_cast<const float*>(base + L.ck);
+    const int steps = min(K, g.T - c * K);
+
+    float4* s0 = reinterpret_cast<float4*>(smem + L.scal) + tid;  // thread-private, stride GB
+    float4* s1 = s0 + (size_t)K * GB;
+    T* const dz_c = static_cast<T*>(a.dz) + ((size_t)b * g.T + (size_t)c * K) * g.D + d;
+    T* const ddr_c = static_cast<T*>(a.ddr) + ((size_t)b * g.T + (size_t)c * K) * g.D + d;
+    T* const dx_c = static_cast<T*>(a.dx) + ((size_t)b * g.T + (size_t)c * K) * g.D + d;
+    T* const du_c = a.du_dbg ? static_cast<T*>(a.du_dbg) + ((size_t)b * g.T + (size_t)c * K) * g.D + d
+                             : nullptr;
+
+    // The four passes over the chunk.
+    {
+      const int nst = steps;
+
+      // ---- scalar pass: everything per step that does not need the state ----
+      {
+        float xm3 = Act<T>::ld(xt + 0 * GB + tid);
+        float xm2 = Act<T>::ld(xt + 1 * GB + tid);
+        float xm1 = Act<T>::ld(xt + 2 * GB + tid);
+#pragma unroll 2
+        for (int j = 0; j < nst; ++j) {
+          const float xv = Act<T>::ld(xt + (j + 3) * GB + tid);
+          const float cpre = fmaf(w[0], xm3, fmaf(w[1], xm2, fmaf(w[2], xm1, fmaf(w[3], xv, cb))));
+          xm3 = xm2;
+          xm2 = xm1;
+          xm1 = xv;
+          const float sc = sigmoid_f(cpre);
+          const float u = cpre * sc;
+          const float v = Act<T>::ld(drt + j * GB + tid) + dtb;
+          const float delta = softplus_f(v);
+          const float sv = sigmoid_f(v);
+          const float zv = Act<T>::ld(zt + j * GB + tid);
+          const float gv = Act<T>::ld(dgt + j * GB + tid);
+          const float sz = sigmoid_f(zv);
+          const float dy = gv * zv * sz;                           // dL/dy
+          const float dzf = gv * (sz * fmaf(zv, 1.f - sz, 1.f));    // dL/dz = y * dzf
+          s0[j * GB] = make_float4(delta, delta * u, dy, dzf);
+          s1[j * GB] = make_float4(Dd * u, sv, sc, cpre);
+        }
+      }
+
+      // ---- recompute the chunk's states from its start state ----
+      {
+        float2 h[NS / 2];
+#pragma unroll
+        for (int i = 0; i < NS / 2; ++i) {
+          const int n = lane_of(i);
+          h[i] = make_float2(ckt[n * GB + tid], ckt[(n + 1) * GB + tid]);
+        }
+#pragma unroll 2
+        for (int j = 0; j < nst; ++j) {
+          const float4 v0 = s0[j * GB];
+          const float2 dl2 = f2b(v0.x);
+          const float2 du2 = f2b(v0.y);
+          const float4* B4 = reinterpret_cast<const float4*>(fB + j * NS);
+#pragma unroll
+          for (int qs = 0; qs < 4; ++qs) {
+            const float4 bv = B4[qs ^ rot];
+            const float2 dA0 = ex2x2(__fmul2_rn(dl2, a2[2 * qs]));
+            const float2 dA1 = ex2x2(__fmul2_rn(dl2, a2[2 * qs + 1]));
+            h[2 * qs] = __ffma2_rn(dA0, h[2 * qs], __fmul2_rn(du2, make_float2(bv.x, bv.y)));
+            h[2 * qs + 1] = __ffma2_rn(dA1, h[2 * qs + 1], __fmul2_rn(du2, make_float2(bv.z, bv.w)));
+          }
+          tmem_st16(trow + 16u * (uint32_t)j, h);
+        }
+        tmem_wait_st();
+      }
+
+      // ---- reverse-time pass: y and dz, adjoint state, dA, dB/dC ----
+      {
+        float2 hn[NS / 2];  // h_t (state after step t)
+        tmem_ld16(trow + 16u * (uint32_t)(nst - 1), hn);
+#pragma unroll 2
+        for (int j = nst - 1; j >= 0; --j) {
+          const float4 v0 = s0[j * GB];
+          const float Du = reinterpret_cast<const float*>(s1 + j * GB)[0];
+          const float2 dl2 = f2b(v0.x);
+          const float2 du2 = f2b(v0.y);
+          const float2 dy2 = f2b(v0.z);
+          float2 sB = make_float2(0.f, 0.f), sAq = make_float2(0.f, 0.f);
+          float2 y01 = make_float2(0.f, 0.f), y23 = make_float2(0.f, 0.f);
+          float2 pB[NS / 2], pC[NS / 2];
+          float2 hp[NS / 2];  // h_{t-1}
+          if (j > 0) {
+            tmem_ld16(trow + 16u * (uint32_t)(j - 1), hp);
+          } else {
+#pragma unroll
+            for (int i = 0; i < NS / 2; ++i) {
+              const int n = lane_of(i);
+              hp[i] = make_float2(ckt[n * GB + tid], ckt[(n + 1) * GB + tid]);
+            }
+          }
+          const float4* B4 = reinterpret_cast<const float4*>(fB + j * NS);
+          const float4* C4 = reinterpret_cast<const float4*>(fC + j * NS);
+#pragma unroll
+          for (int qs = 0; qs < 4; ++qs) {
+            const float4 bv = B4[qs ^ rot];
+            const float4 cv = C4[qs ^ rot];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int i = 2 * qs + e;
+              const float2 bb = e ? make_float2(bv.z, bv.w) : make_float2(bv.x, bv.y);
+              const float2 cc = e ? make_float2(cv.z, cv.w) : make_float2(cv.x, cv.y);
+              if (e) y23 = __ffma2_rn(cc, hn[i], y23); else y01 = __ffma2_rn(cc, hn[i], y01);
+              const float2 dh = __ffma2_rn(dy2, cc, carry[i]);            // dL/dh_t
+              pC[i] = __fmul2_rn(dy2, hn[i]);                              // dC partial
+              pB[i] = __fmul2_rn(dh, du2);                                 // dB partial
+              sB = __ffma2_rn(dh, bb, sB);
+              carry[i] = __fmul2_rn(ex2x2(__fmul2_rn(dl2, a2[i])), dh);    // exp(delta A) dh
+              const float2 qv = __fmul2_rn(carry[i], hp[i]);               // dh exp(delta A) h_{t-1}
+              dAp[i] = __ffma2_rn(dl2, qv, dAp[i]);
+              sAq = __ffma2_rn(a2[i], qv, sAq);
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < NS / 2; ++i) hn[i] = hp[i];
+          const float y = ((y01.x + y01.y) + (y23.x + y23.y)) + Du;
+          if (active) Act<T>::st(dz_c + (size_t)j * g.D, y * v0.w);
+          // the scalar pass below reads these two sums
+          reinterpret_cast<float*>(s0 + j * GB)[3] = sAq.x + sAq.y;
+          reinterpret_cast<float*>(s1 + j * GB)[0] = sB.x + sB.y;
+          // Channels past d_inner run on zero-filled inputs and parameters, so
+          // their partials are exactly zero and need no masking.
+          float vb[NS], vc[NS];
+#pragma unroll
+          for (int i = 0; i < NS / 2; ++i) {
+            vb[2 * i] = pB[i].x;
+            vb[2 * i + 1] = pB[i].y;
+            vc[2 * i] = pC[i].x;
+            vc[2 * i + 1] = pC[i].y;
+          }
+          const float rb = warp_sum16_rotated(vb, lane);
+          const float rc = warp_sum16_rotated(vc, lane);
+          const int nf = 4 * rot + 2 * ((lane >> 3) & 1) + ((lane >> 2) & 1);
+          red[(j * NWB + warp) * 32 + (lane < 16 ? nf : 16 + nf)] = lane < 16 ? rb : rc;
+        }
+      }
+
+      // ---- scalar pass: du, d delta, softplus, SiLU and conv backward ----
+#pragma unroll 2
+      for (int j = nst - 1; j >= 0; --j) {
+        const int t = c * K + j;
+        const float4 v0 = s0[j * GB];
+        const float4 v1 = s1[j * GB];
+        const float delta = v0.x, dy = v0.z, sAq = v0.w;
+        const float sumB = v1.x, sv = v1.y, sc = v1.z, cpre = v1.w;
+        const float u = cpre * sc;
+        const float du = fmaf(dy, Dd, delta * sumB);
+        const float ddr = fmaf(u, sumB, LN2 * sAq) * sv;
+        dD_acc = fmaf(dy, u, dD_acc);
+        ddtb_acc += ddr;
+        if constexpr (SCAN) {  // the SiLU and conv backward run later, with du
+          if (active) {
+            Act<T>::st(ddr_c + (size_t)j * g.D, ddr);
+            Act<T>::st(du_c + (size_t)j * g.D, du);
+          }
+          continue;
+        }
+        const float dc = du * (sc * fmaf(cpre, 1.f - sc, 1.f));
+        dcb_acc += dc;
+#pragma unroll
+        for (int k = 0; k < WC; ++k) dcw[k] = fmaf(dc, Act<T>::ld(xt + (j + k) * GB + tid), dcw[k]);
+        float dxv = fmaf(dc, w[3], fmaf(dc1, w[2], fmaf(dc2, w[1], dc3 * w[0])));
+        if (ST && a.g_conv && t >= g.T - 3 && active)  // x[t] is also a conv-state output
+          dxv += Act<T>::ld(static_cast<const T*>(a.g_conv) + ((size_t)b * 3 + t - (g.T - 3)) * g.D + d);
+        dc3 = dc2;
+        dc2 = dc1;
+        dc1 = dc;
+        if (active) {
+          Act<T>::st(ddr_c + (size_t)j * g.D, ddr);
+          if (du_c) Act<T>::st(du_c + (size_t)j * g.D, du);
+          if (s + 1 < g.S && t >= t_end - 3)
+            a.dxpart[(((size_t)b * g.S + s) * 3 + (t - (t_end - 3))) * g.D + d] = dxv;
+          else
+            Act<T>::st(dx_c + (size_t)j * g.D, dxv);
+          if (s > 0 && t < t_begin + 3)
+            a.dchead[(((size_t)b * g.S + s) * 3 + (t - t_begin)) * g.D + d] = dc;
+        }
+      }
+    }
+
+    __syncthreads();
+    // one global reduction per (t, n) per block for dB and dC
+    for (int i = tid; i < steps * 32; i += GB) {
+      const int j = i >> 5, l = i & 31;
+      float v = 0.f;
+#pragma unroll
+      for (int ww = 0; ww < NWB; ++ww) v += red[(j * NWB + ww) * 32 + l];
+      float* dst = (l < NS ? a.dB : a.dC) + ((size_t)b * g.T + c * K + j) * g.lddbc + (l & (NS - 1));
+      atomicAdd(dst, v);
+    }
+    __syncthreads();
+  }
+
+  if (ST && s == 0 && active) {
+    if (a.d_h_in) {  // carry = exp(delta_0 A) dL/dh_0 = dL/dh_{-1}
+      float* dh0 = a.d_h_in + (size_t)b * NS * g.D + d;
+#pragma unroll
+      for (int i = 0; i < NS / 2; ++i) {
+        const int n = lane_of(i);
+        dh0[(size_t)n * g.D] = carry[i].x;
+        dh0[(size_t)(n + 1) * g.D] = carry[i].y;
+      }
+    }
+    if (!SCAN && a.d_conv_in) {
+      // conv inputs of steps -1, -2, -3 reach the conv outputs of steps
+      // 0..2 (dc1 = dc_0, dc2 = dc_1, dc3 = dc_2; zero past the sequence),
+      // and, when T < 3, the conv-state output too
+      float v[3];
+      v[2] = fmaf(dc1, w[2], fmaf(dc2, w[1], dc3 * w[0]));
+      v[1] = fmaf(dc1, w[1], dc2 * w[0]);
+      v[0] = dc1 * w[0];
+      T* dci = static_cast<T*>(a.d_conv_in) + (size_t)b * 3 * g.D + d;
+#pragma unroll
+      for (int r = 0; r < 3; ++r) {
+        const int ro = r - g.T;  // row of the conv-state output holding step r - 3
+        if (a.g_conv && ro >= 0)
+          v[r] += Act<T>::ld(static_cast<const T*>(a.g_conv) + ((size_t)b * 3 + ro) * g.D + d);
+        Act<T>::st(dci + (size_t)r * g.D, v[r]);
+      }
+    }
+  }
+  if (active) {
+    float* Pp = a.partials + ((size_t)b * g.S + s) * NPART * g.D;
+#pragma unroll
+    for (int i = 0; i < NS / 2; ++i) {
+      const int n = lane_of(i);
+      Pp[(size_t)n * g.D + d] = dAp[i].x;
+      Pp[(size_t)(n + 1) * g.D + d] = dAp[i].y;
+    }
+    Pp[(size_t)16 * g.D + d] = dD_acc;
+    Pp[(size_t)17 * g.D + d] = ddtb_acc;
+    Pp[(size_t)18 * g.D + d] = dcb_acc;
+#pragma unroll
+    for (int k = 0; k < WC; ++k) Pp[(size_t)(19 + k) * g.D + d] = dcw[k];
+  }
+  tmem_fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem_slot, a.tcols);
+}
+
+// ---------------------------------------------------------------------------
+// backward main kernel with the lanes split over G = N / 8 threads per
+// channel (8 lanes each, 128 / G channels per block); the threads of a
+// channel take the per-step scalar work of every G-th step.  For d_state 32
+// and 64, and for d_state-16 grids that fill less than one wave (each thread
+// then runs about half the per-step instructions of m3_bwd_kernel and a
+// block holds twice the warps per channel).  Same results as m3_bwd_kernel
+// up to the order of f32 sums.
+// ---------------------------------------------------------------------------
+
+// Sum over the channels of a warp (the lanes with the same lane % G) of 8
+// values held as 4 pairs, pair P holding this thread's lane pair
+// P ^ ((lane >> 3) & 3).  The channel bits of a lane are its bits log2(G)
+// and up; the sum runs over them:
+//   G = 2: returns (in .x) the total for pair (lane >> 3) & 3, element
+//          (lane >> 2) & 1 (lanes differing only in bit 1 return the same);
+//   G = 4: the same total, every lane distinct;
+//   G = 8: returns both elements of pair (lane >> 3) & 3.
+template <int G>
+__device__ __forceinline__ float2 warp_sum8_rotated(float2 (&v)[4], int lane) {
+  v[0].x += __shfl_xor_sync(0xffffffffu, v[2].x, 16);
+  v[0].y += __shfl_xor_sync(0xffffffffu, v[2].y, 16);
+  v[1].x += __shfl_xor_sync(0xffffffffu, v[3].x, 16);
+  v[1].y += __shfl_xor_sync(0xffffffffu, v[3].y, 16);
+  v[0].x += __shfl_xor_sync(0xffffffffu, v[1].x, 8);
+  v[0].y += __shfl_xor_sync(0xffffffffu, v[1].y, 8);
+  if constexpr (G == 8) {
+    return v[0];
+  } else {
+    const bool up = (lane & 4) != 0;
+    const float send = up ? v[0].x : v[0].y;
+    const float keep = up ? v[0].y : v[0].x;
+    float r = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+    if constexpr (G == 2) r += __shfl_xor_sync(0xffffffffu, r, 2);
+    return make_float2(r, 0.f);
+  }
+}
+
+template <typename T, bool ST, bool SCAN, int N>
+__global__ void __launch_bounds__(128, 4) m3_bwd2_kernel(BwdArgs a) {
+  constexpr int G = N / 8;     // threads per channel
+  constexpr int CH = 128 / G;  // channels per block
+  constexpr int NP = N + 8;    // per-channel parameter partials
+  extern __shared__ __align__(128) unsigned char smem[];
+  const Geo g = a.g;
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  const int hf = tid % G;            // this thread's state lanes: 8 hf .. 8 hf + 7
+  const int ch = tid / G;            // channel within the block
+  const int prot = (lane >> 3) & 3;  // pair rotation for the warp reduction
+  const int d0 = blockIdx.x * CH;
+  const int s = blockIdx.y;
+  const int b = blockIdx.z;
+  const int d = d0 + ch;
+  const bool active = d < g.D;
+  const int c_begin = s * g.m;
+  const int c_end = min(c_begin + g.m, g.nc);
+  const int t_begin = c_begin * g.K;
+  const int t_end = min(c_end * g.K, g.T);
+  const int K = g.K;
+  const Bwd2Smem L = bwd2_smem(K, sizeof(T), N);
+  float* fB = reinterpret_cast<float*>(smem + L.fB);
+  float* fC = reinterpret_cast<float*>(smem + L.fC);
+  float* red = reinterpret_cast<float*>(smem + L.red);
+  float* dcs = reinterpret_cast<float*>(smem + L.dcs);  // [K + 3][CH]
+  // state lane of register pair P
+  auto lane_of = [&](int P) { return 8 * hf + 2 * (P ^ prot); };
+
+  // recomputed states of a chunk: row j of this thread = TMEM columns
+  // [8 j, 8 j + 8) of its lane; warp 0 allocates, every exit deallocates
+  __shared__ uint32_t tmem_slot;
+  if (warp == 0) tmem_alloc(&tmem_slot, a.tcols);
+  tmem_fence_before_sync();
+  __syncthreads();
+  tmem_fence_after_sync();
+  const uint32_t trow = tmem_slot + ((uint32_t)(warp * 32) << 16);
+
+  float2 a2[4];
+  float w[WC];
+  float cb = 0.f, dtb = 0.f, Dd = 0.f;
+#pragma unroll
+  for (int P = 0; P < 4; ++P) {
+    const int n = lane_of(P);
+    a2[P].x = active ? -expf(a.a_log[(size_t)d * N + n]) * LOG2E : 0.f;
+    a2[P].y = active ? -expf(a.a_log[(size_t)d * N + n + 1]) * LOG2E : 0.f;
+  }
+#pragma unroll
+  for (int k = 0; k < WC; ++k) w[k] = active ? a.conv_w[(size_t)d * WC + k] : 0.f;
+  if (active) {
+    cb = a.conv_b[d];
+    dtb = a.dt_bias[d];
+    Dd = a.Dp[d];
+  }
+  float2 carry[4];
+#pragma unroll
+  for (int P = 0; P < 4; ++P) carry[P] = make_float2(0.f, 0.f);
+  if (ST && a.g_h && active) {
+    const float* gh = a.g_h + (size_t)b * N * g.D + d;
+#pragma unroll
+    for (int P = 0; P < 4; ++P) {
+      const int n = lane_of(P);
+      carry[P] = make_float2(gh[(size_t)n * g.D], gh[(size_t)(n + 1) * g.D]);
+    }
+  }
+  const T* xg = static_cast<const T*>(a.x);
+  auto stage = [&](int c, int buf) {
+    unsigned char* base = smem + (size_t)buf * L.tile;
+    const int t0 = c * K;
+    stage_rows<T, CH, 128>(reinterpret_cast<T*>(base + L.x), xg, b, t0 - 3, K + 3, g.T, g.T, g.D, d0, tid);
+    stage_rows<T, CH, 128>(reinterpret_cast<T*>(base + L.dr), static_cast<const T*>(a.dr), b, t0, K, g.T, g.T, g.D, d0, tid);
+    stage_rows<T, CH, 128>(reinterpret_cast<T*>(base + L.z), static_cast<const T*>(a.z), b, t0, K, g.T, g.T, g.D, d0, tid);
+    stage_rows<T, CH, 128>(reinterpret_cast<T*>(base + L.dg), static_cast<const T*>(a.dg), b, t0, K, g.T, g.T, g.D, d0, tid);
+    stage_bc<T, 128, N>(reinterpret_cast<T*>(base + L.Bt), static_cast<const T*>(a.Bm), b, t0, K, g.T, g.T, g.ldbc, tid);
+    stage_bc<T, 128, N>(reinterpret_cast<T*>(base + L.Ct), static_cast<const T*>(a.Cm), b, t0, K, g.T, g.T, g.ldbc, tid);
+    stage_rows<float, CH, 128>(reinterpret_cast<float*>(base + L.ck), a.ckpt + ((size_t)b * g.nc + c) * N * g.D,
+                               0, 0, N, N, N, g.D, d0, tid);
+    cp_async_commit();
+  };
+  stage(c_end - 1, 0);
+  grid_dep_trigger();
+  grid_dep_wait();
+  if (s + 1 < g.S) {
+    const float* __restrict__ sd = a.sd;
+    const float* __restrict__ q = a.q;
+#pragma unroll 2
+    for (int sp = g.S - 1; sp > s; --sp) {
+      const size_t bs = (size_t)b * g.S + sp;
+      const float2 dl2 = f2b(active ? sd[bs * g.D + d] : 0.f);
+#pragma unroll
+      for (int P = 0; P < 4; ++P) {
+        const float* qq = q + (bs * N + lane_of(P)) * g.D + d;
+        const float2 loc = active ? make_float2(qq[0], qq[g.D]) : make_float2(0.f, 0.f);
+        carry[P] = __ffma2_rn(ex2x2(__fmul2_rn(dl2, a2[P])), carry[P], loc);
+      }
+    }
+  }
+  float2 dAp[4];
+#pragma unroll
+  for (int P = 0; P < 4; ++P) dAp[P] = make_float2(0.f, 0.f);
+  float dD_acc = 0.f, ddtb_acc = 0.f, dcb_acc = 0.f;
+  float dcw[WC] = {0.f, 0.f, 0.f, 0.f};
+  for (int i = tid; i < (K + 3) * CH; i += 128) dcs[i] = 0.f;  // ordered by the loop's first barrier
+
+  for (int c = c_end - 1; c >= c_begin; --c) {
+    const int buf = (c_end - 1 - c) & 1;
+    if (c - 1 >= c_begin) {
+      stage(c - 1, buf ^ 1);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();
+    const unsigned char* base = smem + (size_t)buf * L.tile;
+    if (ST && a.conv_in && c * K < 3 && active && hf == 0) {
+      T* xw = reinterpret_cast<T*>(smem + (size_t)buf * L.tile + L.x);
+      const T* ci = static_cast<const T*>(a.conv_in) + (size_t)b * 3 * g.D + d;
+      for (int r = 0; r < 3 - c * K; ++r) xw[r * CH + ch] = ci[(size_t)(c * K + r) * g.D];
+    }
+    {
+      const T* Bt = reinterpret_cast<const T*>(base + L.Bt);
+      const T* Ct = reinterpret_cast<const T*>(base + L.Ct);
+      for (int i = tid; i < K * N; i += 128) {
+        fB[i] = Act<T>::ld(Bt + i);
+        fC[i] = Act<T>::ld(Ct + i);
+      }
+    }
+    __syncthreads();
+    const T* xt = reinterpret_cast<const T*>(base + L.x);  // row r is step c*K - 3 + r
+    const T* drt = reinterpret_cast<const T*>(base + L.dr);
+    const T* zt = reinterpret_cast<const T*>(base + L.z);
+    const T* dgt = reinterpret_cast<const T*>(base + L.dg);
+    const float* ckt = reinterpret_cast<const float*>(base + L.ck);
+    const int steps = min(K, g.T - c * K);
+    float4* s0 = reinterpret_cast<float4*>(smem + L.scal) + ch;  // shared by the channel's threads, stride CH
+    float4* s1 = s0 + (size_t)K * CH;
+    const size_t row0 = ((size_t)b * g.T + (size_t)c * K) * g.D + d;
+
+    // ---- scalar pass, every G-th step ----
+    for (int j = hf; j < steps; j += G) {
+      const float xm3 = Act<T>::ld(xt + j * CH + ch);
+      const float xm2 = Act<T>::ld(xt + (j + 1) * CH + ch);
+      const float xm1 = Act<T>::ld(xt + (j + 2) * CH + ch);
+      const float xv = Act<T>::ld(xt + (j + 3) * CH + ch);
+      const float cpre = fmaf(w[0], xm3, fmaf(w[1], xm2, fmaf(w[2], xm1, fmaf(w[3], xv, cb))));
+      const float sc = sigmoid_f(cpre);
+      const float u = cpre * sc;
+      const float v = Act<T>::ld(drt + j * CH + ch) + dtb;
+      const float delta = softplus_f(v);
+      const float sv = sigmoid_f(v);
+      const float zv = Act<T>::ld(zt + j * CH + ch);
+      const float gv = Act<T>::ld(dgt + j * CH + ch);
+      const float sz = sigmoid_f(zv);
+      s0[j * CH] = make_float4(delta, delta * u, gv * zv * sz, gv * (sz * fmaf(zv, 1.f - sz, 1.f)));
+      s1[j * CH] = make_float4(Dd * u, sv, sc, cpre);
+    }
+    __syncwarp();
+
+    // ---- recompute this thread's 8 lanes of the chunk's states ----
+    {
+      float2 h[4];
+#pragma unroll
+      for (int P = 0; P < 4; ++P) {
+        const int n = lane_of(P);
+        h[P] = make_float2(ckt[n * CH + ch], ckt[(n + 1) * CH + ch]);
+      }
+#pragma unroll 2
+      for (int j = 0; j < steps; ++j) {
+        const float4 v0 = s0[j * CH];
+        const float2 dl2 = f2b(v0.x);
+        const float2 du2 = f2b(v0.y);
+#pragma unroll
+        for (int P = 0; P < 4; ++P) {
+          const float2 bb = *reinterpret_cast<const float2*>(fB + j * N + lane_of(P));
+          h[P] = __ffma2_rn(ex2x2(__fmul2_rn(dl2, a2[P])), h[P], __fmul2_rn(du2, bb));
+        }
+        tmem_st8(trow + 8u * (uint32_t)j, h);
+      }
+      tmem_wait_st();
+    }
+
+    // ---- reverse-time pass ----
+    {
+      float2 hn[4];
+      tmem_ld8(trow + 8u * (uint32_t)(steps - 1), hn);
+#pragma unroll 2
+      for (int j = steps - 1; j >= 0; --j) {
+        const float4 v0 = s0[j * CH];
+        const float Du = reinterpret_cast<const float*>(s1 + j * CH)[0];
+        const float2 dl2 = f2b(v0.x);
+        const float2 du2 = f2b(v0.y);
+        const float2 dy2 = f2b(v0.z);
+        float2 sB = make_float2(0.f, 0.f), sAq = make_float2(0.f, 0.f), y2 = make_float2(0.f, 0.f);
+        float2 pB[4], pC[4], hp[4];
+        if (j > 0) {
+          tmem_ld8(trow + 8u * (uint32_t)(j - 1), hp);
+        } else {
+#pragma unroll
+          for (int P = 0; P < 4; ++P) {
+            const int n = lane_of(P);
+            hp[P] = make_float2(ckt[n * CH + ch], ckt[(n + 1) * CH + ch]);
+          }
+        }
+#pragma unroll
+        for (int P = 0; P < 4; ++P) {
+          const float2 bb = *reinterpret_cast<const float2*>(fB + j * N + lane_of(P));
+          const float2 cc = *reinterpret_cast<const float2*>(fC + j * N + lane_of(P));
+          y2 = __ffma2_rn(cc, hn[P], y2);
+          const float2 dh = __ffma2_rn(dy2, cc, carry[P]);
+          pC[P] = __fmul2_rn(dy2, hn[P]);
+          pB[P] = __fmul2_rn(dh, du2);
+          sB = __ffma2_rn(dh, bb, sB);
+          carry[P] = __fmul2_rn(ex2x2(__fmul2_rn(dl2, a2[P])), dh);
+          const float2 qv = __fmul2_rn(carry[P], hp[P]);
+          dAp[P] = __ffma2_rn(dl2, qv, dAp[P]);
+          sAq = __ffma2_rn(a2[P], qv, sAq);
+        }
+#pragma unroll
+        for (int P = 0; P < 4; ++P) hn[P] = hp[P];
+        float ys = y2.x + y2.y, sBs = sB.x + sB.y, sAs = sAq.x + sAq.y;
+#pragma unroll
+        for (int o = 1; o < G; o <<= 1) {
+          ys += __shfl_xor_sync(0xffffffffu, ys, o);
+          sBs += __shfl_xor_sync(0xffffffffu, sBs, o);
+          sAs += __shfl_xor_sync(0xffffffffu, sAs, o);
+        }
+        if (hf == j % G) {
+          if (active) Act<T>::st(static_cast<T*>(a.dz) + row0 + (size_t)j * g.D, (ys + Du) * v0.w);
+          reinterpret_cast<float*>(s0 + j * CH)[3] = sAs;
+          reinterpret_cast<float*>(s1 + j * CH)[0] = sBs;
+        }
+        const float2 rb = warp_sum8_rotated<G>(pB, lane);
+        const float2 rc = warp_sum8_rotated<G>(pC, lane);
+        float* rj = red + (j * 4 + warp) * 2 * N;  // [dB: N][dC: N]
+        if constexpr (G == 8) {
+          const int n = 8 * hf + 2 * prot;
+          rj[n] = rb.x;
+          rj[n + 1] = rb.y;
+          rj[N + n] = rc.x;
+          rj[N + n + 1] = rc.y;
+        } else if (G == 4 || (lane & 2) == 0) {
+          const int n = 8 * hf + 2 * prot + ((lane >> 2) & 1);
+          rj[n] = rb.x;
+          rj[N + n] = rc.x;
+        }
+      }
+    }
+    __syncwarp();
+
+    // ---- du, d delta, softplus and (unless SCAN) SiLU backward, every G-th step ----
+    for (int j = hf; j < steps; j += G) {
+      const int t = c * K + j;
+      const float4 v0 = s0[j * CH];
+      const float4 v1 = s1[j * CH];
+      const float delta = v0.x, dy = v0.z, sAq = v0.w;
+      const float sumB = v1.x, sv = v1.y, sc = v1.z, cpre = v1.w;
+      const float u = cpre * sc;
+      const float du = fmaf(dy, Dd, delta * sumB);
+      const float ddr = fmaf(u, sumB, LN2 * sAq) * sv;
+      dD_acc = fmaf(dy, u, dD_acc);
+      ddtb_acc += ddr;
+      if (active) {
+        Act<T>::st(static_cast<T*>(a.ddr) + row0 + (size_t)j * g.D, ddr);
+        if (a.du_dbg) Act<T>::st(static_cast<T*>(a.du_dbg) + row0 + (size_t)j * g.D, du);
+      }
+      if constexpr (SCAN) continue;
+      const float dc = du * (sc * fmaf(cpre, 1.f - sc, 1.f));
+      dcb_acc += dc;
+#pragma unroll
+      for (int k = 0; k < WC; ++k) dcw[k] = fmaf(dc, Act<T>::ld(xt + (j + k) * CH + ch), dcw[k]);
+      dcs[j * CH + ch] = dc;
+      if (active && s > 0 && t < t_begin + 3)
+        a.dchead[(((size_t)b * g.S + s) * 3 + (t - t_begin)) * g.D + d] = dc;
+    }
+    if constexpr (!SCAN) {
+      __syncwarp();
+      // ---- conv backward: d_x from the conv-input gradient of this and the next 3 steps ----
+      for (int j = hf; j < steps; j += G) {
+        const int t = c * K + j;
+        float dxv = fmaf(dcs[j * CH + ch], w[3], fmaf(dcs[(j + 1) * CH + ch], w[2],
+                         fmaf(dcs[(j + 2) * CH + ch], w[1], dcs[(j + 3) * CH + ch] * w[0])));
+        if (ST && a.g_conv && t >= g.T - 3 && active)
+          dxv += Act<T>::ld(static_cast<const T*>(a.g_conv) + ((size_t)b * 3 + t - (g.T - 3)) * g.D + d);
+        if (active) {
+          if (s + 1 < g.S && t >= t_end - 3)
+            a.dxpart[(((size_t)b * g.S + s) * 3 + (t - (t_end - 3))) * g.D + d] = dxv;
+          else
+            Act<T>::st(static_cast<T*>(a.dx) + row0 + (size_t)j * g.D, dxv);
+        }
+      }
+      __syncwarp();
+      // the next chunk processed (the one before in time) reads the dc of
+      // this chunk's first three steps: rows 0..2 of this chunk followed by
+      // the carried rows (a chunk may be shorter than three steps), all
+      // read before any is overwritten
+      if (hf == 0) {
+        const float v0 = dcs[ch], v1 = dcs[CH + ch], v2 = dcs[2 * CH + ch];
+        dcs[K * CH + ch] = v0;
+        dcs[(K + 1) * CH + ch] = v1;
+        dcs[(K + 2) * CH + ch] = v2;
+      }
+    }
+
+    __syncthreads();
+    for (int i = tid; i < steps * 2 * N; i += 128) {
+      const int j = i / (2 * N), l = i % (2 * N);
+      float v = 0.f;
+#pragma unroll
+      for (int ww = 0; ww < 4; ++ww) v += red[(j * 4 + ww) * 2 * N + l];
+      float* dst = (l < N ? a.dB : a.dC) + ((size_t)b * g.T + c * K + j) * g.lddbc + (l & (N - 1));
+      atomicAdd(dst, v);
+    }
+    __syncthreads();
+  }
+
+  if (ST && s == 0 && active) {
+    if (a.d_h_in) {
+      float* dh0 = a.d_h_in + (size_t)b * N * g.D + d;
+#pragma unroll
+      for (int P = 0; P < 4; ++P) {
+        const int n = lane_of(P);
+        dh0[(size_t)n * g.D] = carry[P].x;
+        dh0[(size_t)(n + 1) * g.D] = carry[P].y;
+      }
+    }
+    if (!SCAN && a.d_conv_in && hf == 0) {
+      // dc of steps 0, 1, 2 (zero past the sequence), kept in rows K.. K+2
+      const float f0 = dcs[K * CH + ch], f1 = dcs[(K + 1) * CH + ch], f2 = dcs[(K + 2) * CH + ch];
+      float v[3];
+      v[2] = fmaf(f0, w[2], fmaf(f1, w[1], f2 * w[0]));
+      v[1] = fmaf(f0, w[1], f1 * w[0]);
+      v[0] = f0 * w[0];
+      T* dci = static_cast<T*>(a.d_conv_in) + (size_t)b * 3 * g.D + d;
+#pragma unroll
+      for (int r = 0; r < 3; ++r) {
+        const int ro = r - g.T;
+        if (a.g_conv && ro >= 0)
+          v[r] += Act<T>::ld(static_cast<const T*>(a.g_conv) + ((size_t)b * 3 + ro) * g.D + d);
+        Act<T>::st(dci + (size_t)r * g.D, v[r]);
+      }
+    }
+  }
+  // the per-step partial sums: each thread of a channel summed its own steps
+#pragma unroll
+  for (int o = 1; o < G; o <<= 1) {
+    dD_acc += __shfl_xor_sync(0xffffffffu, dD_acc, o);
+    ddtb_acc += __shfl_xor_sync(0xffffffffu, ddtb_acc, o);
+    dcb_acc += __shfl_xor_sync(0xffffffffu, dcb_acc, o);
+#pragma unroll
+    for (int k = 0; k < WC; ++k) dcw[k] += __shfl_xor_sync(0xffffffffu, dcw[k], o);
+  }
+  if (active) {
+    float* Pp = a.partials + ((size_t)b * g.S + s) * NP * g.D;
+#pragma unroll
+    for (int P = 0; P < 4; ++P) {
+      const int n = lane_of(P);
+      Pp[(size_t)n * g.D + d] = dAp[P].x;
+      Pp[(size_t)(n + 1) * g.D + d] = dAp[P].y;
+    }
+    if (hf == 0) {
+      Pp[(size_t)N * g.D + d] = dD_acc;
+      Pp[(size_t)(N + 1) * g.D + d] = ddtb_acc;
+      Pp[(size_t)(N + 2) * g.D + d] = dcb_acc;
+#pragma unroll
+      for (int k = 0; k < WC; ++k) Pp[(size_t)(N + 3 + k) * g.D + d] = dcw[k];
+    }
+  }
+  tmem_fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem_slot, a.tcols);
+}
+
+// The backward's last kernel, two roles by block index.
+//  - blocks [0, nfin): parameter gradients, the per-(batch, segment) partials
+//    summed in a fixed order (32 outputs per block, rows split over its 8
+//    warps and combined in a fixed tree), so the result is deterministic;
+//  - blocks [nfin, ...): d_x at the last three steps of each segment but the
+//    last, which needs the conv gradient of the next segment's first steps.
+// N = d_state: partial rows per channel are N + 8 (N of dA, then dD,
+// d_dt_bias, d_conv_b, d_conv_w[0..3]); nout of them are finalized.
+template <typename T>
+__global__ void m3_bwd_tail_kernel(BwdArgs a, int rows, int nfin, int nout, int N) {
+  const Geo g = a.g;
+  grid_dep_wait();  // the main kernel's partials and boundary terms
+  if ((int)blockIdx.x >= nfin) {
+    const size_t idx = (size_t)(blockIdx.x - nfin) * blockDim.x + threadIdx.x;
+    const size_t total = (size_t)g.B * (g.S - 1) * 3 * g.D;
+    if (idx >= total) return;
+    const int d = (int)(idx % g.D);
+    size_t rest = idx / g.D;
+    const int j = (int)(rest % 3);
+    rest /= 3;
+    const int s = (int)(rest % (g.S - 1));
+    const int b = (int)(rest / (g.S - 1));
+    const int t_end = min((s + 1) * g.m * g.K, g.T);
+    const int t = t_end - 3 + j;
+    float v = a.dxpart[(((size_t)b * g.S + s) * 3 + j) * g.D + d];
+    for (int k = 0; k < WC; ++k) {
+      const int tp = t + 3 - k;
+      if (tp >= t_end && tp < g.T)
+        v = fmaf(a.dchead[(((size_t)b * g.S + s + 1) * 3 + (tp - t_end)) * g.D + d],
+                 a.conv_w[(size_t)d * WC + k], v);
+    }
+    Act<T>::st(static_cast<T*>(a.dx) + ((size_t)b * g.T + t) * g.D + d, v);
+    return;
+  }
+  // 32 consecutive outputs per block (coalesced row reads), rows split over
+  // the block's 8 warps: warp w sums rows w, w + 8, ... in order, then warp
+  // 0 adds the 8 partial sums in a fixed order.
+  __shared__ float part[8][33];
+  const int cx = threadIdx.x & 31, ry = threadIdx.x >> 5;
+  const int oidx = blockIdx.x * 32 + cx;
+  const bool ok = oidx < nout * g.D;
+  const int jj = oidx / g.D, d = oidx - jj * g.D;
+  {
+    float v0 = 0.f, v1 = 0.f;
+    if (ok) {
+      const float* __restrict__ P = a.partials + (size_t)jj * g.D + d;
+      const size_t stride = (size_t)(N + 8) * g.D;
+      int r = ry;
+#pragma unroll 4
+      for (; r + 8 < rows; r += 16) {
+        v0 += P[(size_t)r * stride];
+        v1 += P[(size_t)(r + 8) * stride];
+      }
+      if (r < rows) v0 += P[(size_t)r * stride];
+    }
+    part[ry][cx] = v0 + v1;
+  }
+  __syncthreads();
+  if (ry != 0 || !ok) return;
+  float v = ((part[0][cx] + part[1][cx]) + (part[2][cx] + part[3][cx])) +
+            ((part[4][cx] + part[5][cx]) + (part[6][cx] + part[7][cx]));
+  float* dst;
+  if (jj < N) {
+    v *= -expf(a.a_log[(size_t)d * N + jj]);  // dL/da_log = dL/dA * A
+    dst = a.d_a_log + (size_t)d * N + jj;
+  } else if (jj == N) {
+    dst = a.dD + d;
+  } else if (jj == N + 1) {
+    dst = a.d_dt_bias + d;
+  } else if (jj == N + 2) {
+    dst = a.d_conv_b + d;
+  } else {
+    dst = a.d_conv_w + (size_t)d * WC + (jj - N - 3);
+  }
+  *dst = a.accumulate ? *dst + v : v;
+}
+
+// the split kernels for d_state N
+template <typename T, bool ST, bool SCAN>
+void (*bwd2_for(int N))(BwdArgs) {
+  return N == 16 ? m3_bwd2_kernel<T, ST, SCAN, 16>
+       : N == 32 ? m3_bwd2_kernel<T, ST, SCAN, 32> : m3_bwd2_kernel<T, ST, SCAN, 64>;
+}
+template <typename T>
+void (*agg_for(bool split, int N))(BwdArgs) {
+  if (!split) return m3_bwd_agg_kernel<T, 1, 16>;
+  return N == 16 ? m3_bwd_agg_kernel<T, 2, 16>
+       : N == 32 ? m3_bwd_agg_kernel<T, 4, 32> : m3_bwd_agg_kernel<T, 8, 64>;
+}
+
+// scan: stop at du (m3scan_bwd_scan); the conv side runs in launch_conv_bwd.
+template <typename T>
+m3_status launch_bwd(const Plan& p, BwdArgs a, cudaStream_t st, int smem_per_sm, bool scan) {
+  const int groups = (p.D + GB - 1) / GB;
+  a.g = Geo{p.B, p.T, p.D, p.K, p.nc, p.Sb, p.mb, p.ldbc, p.lddbc};
+  cudaError_t e = cudaSuccess;
+  if (p.Sb > 1) {
+    // also clears dB and dC before the main kernel's reductions into them
+    const bool split = p.bwd_tpc != 1;
+    const int ch = split ? 128 / (p.N / 8) : GB;
+    e = launch_k(agg_for<T>(split, p.N), dim3((p.D + ch - 1) / ch, p.Sb - 1, p.B), GB,
+                 agg_smem(sizeof(T), p.N).total, st, false, a);
+    if (note(e) != cudaSuccess) return M3_ERR_CUDA;
+  } else {
+    // only the d_state columns of each (batch, step) row belong to dB and dC
+    const size_t pitch = (size_t)p.lddbc * 4, rows = (size_t)p.B * p.T;
+    if (note(cudaMemset2DAsync(a.dB, pitch, 0, (size_t)p.N * 4, rows, st)) != cudaSuccess) return M3_ERR_CUDA;
+    if (note(cudaMemset2DAsync(a.dC, pitch, 0, (size_t)p.N * 4, rows, st)) != cudaSuccess) return M3_ERR_CUDA;
+  }
+  const bool with_state = a.conv_in || a.g_h || a.g_conv || a.d_h_in || a.d_conv_in;
+  if (p.bwd_tpc != 1) {
+    a.tcols = tmem_cols2_for(p.K);
+    const size_t smem = bwd2_launch_smem(p.K, sizeof(T), p.N, smem_per_sm);
+    void (*kern)(BwdArgs) = scan ? (with_state ? bwd2_for<T, true, true>(p.N) : bwd2_for<T, false, true>(p.N))
+                                 : (with_state ? bwd2_for<T, true, false>(p.N) : bwd2_for<T, false, false>(p.N));
+    const int ch = 128 / (p.N / 8);
+    e = launch_k(kern, dim3((p.D + ch - 1) / ch, p.Sb, p.B), 128, smem, st, p.Sb > 1, a);
+  } else {
+    a.tcols = tmem_cols_for(p.K);
+    const size_t smem = bwd_launch_smem(p.K, sizeof(T), smem_per_sm);
+    void (*kern)(BwdArgs) = scan ? (with_state ? m3_bwd_kernel<T, true, true> : m3_bwd_kernel<T, false, true>)
+                                 : (with_state ? m3_bwd_kernel<T, true, false> : m3_bwd_kernel<T, false, false>);
+    e = launch_k(kern, dim3(groups, p.Sb, p.B), GB, smem, st, p.Sb > 1, a);
+  }
+  // parameter outputs: N d_a_log, dD, d_dt_bias (+ d_conv_b, 4 d_conv_w)
+  const int nout = scan ? p.N + 2 : p.N + 7;
+  const size_t nfin = ((size_t)nout * p.D + 31) / 32;                 // 32 outputs per block
+  const size_t nfix = (!scan && p.Sb > 1) ? ((size_t)p.B * (p.Sb - 1) * 3 * p.D + 255) / 256 : 0;
+  if (e == cudaSuccess)
+    e = launch_k(m3_bwd_tail_kernel<T>, dim3((unsigned)(nfin + nfix)), 256, 0, st, true, a,
+                 p.B * p.Sb, (int)nfin, nout, p.N);
+  if (e == cudaSuccess) e = cudaGetLastError();
+  return note(e) == cudaSuccess ? M3_OK : M3_ERR_CUDA;
+}
+
+template <typename T>
+cudaError_t set_bwd_attrs() {
+  const int es = sizeof(T);
+  cudaError_t e = cudaSuccess;
+  const bool splits[4] = {false, true, true, true};
+  const int ns[4] = {16, 16, 32, 64};
+  for (int i = 0; i < 4; ++i) {
+    void (*k)(BwdArgs) = agg_for<T>(splits[i], ns[i]);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)agg_smem(es, ns[i]).total);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+  }
+  void (*const bwd_kernels[16])(BwdArgs) = {
+      m3_bwd_kernel<T, false, false>, m3_bwd_kernel<T, true, false>, m3_bwd_kernel<T, false, true>,
+      m3_bwd_kernel<T, true, true>,
+      bwd2_for<T, false, false>(16), bwd2_for<T, true, false>(16), bwd2_for<T, false, true>(16),
+      bwd2_for<T, true, true>(16),
+      bwd2_for<T, false, false>(32), bwd2_for<T, true, false>(32), bwd2_for<T, false, true>(32),
+      bwd2_for<T, true, true>(32),
+      bwd2_for<T, false, false>(64), bwd2_for<T, true, false>(64), bwd2_for<T, false, true>(64),
+      bwd2_for<T, true, true>(64)};
+  for (auto k : bwd_kernels) {
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_CAP);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+  }
+  return e;
+}
+
+template <typename T>
+cudaError_t bwd_occupancy(int chunk, int smem_per_sm, int* blocks) {
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, m3_bwd_kernel<T, false, false>, GB,
+                                                       bwd_launch_smem(chunk, sizeof(T), smem_per_sm));
+}
+
+template m3_status launch_bwd<float>(const Plan&, BwdArgs, cudaStream_t, int, bool);
+template m3_status launch_bwd<__nv_bfloat16>(const Plan&, BwdArgs, cudaStream_t, int, bool);
+template cudaError_t set_bwd_attrs<float>();
+template cudaError_t set_bwd_attrs<__nv_bfloat16>();
+template cudaError_t bwd_occupancy<float>(int, int, int*);
+template cudaError_t bwd_occupancy<__nv_bfloat16>(int, int, int*);
+
+}  // namespace m3

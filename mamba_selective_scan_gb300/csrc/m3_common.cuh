@@ -1,0 +1,516 @@
+// m3_common.cuh -- selective-scan layer core (Mamba-1) for sm_103a.
+// Shared by the library's translation units: constants, device helpers,
+// kernel argument structs, shared-memory layouts, the launch plan and the
+// entry points each unit provides to the others.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/m3scan.h"
+
+namespace m3 {
+
+constexpr int NS = 16;        // d_state lanes per channel
+constexpr int WC = 4;         // conv taps
+constexpr int GF = 128;       // forward: channels (= threads) per block
+constexpr int GB = 128;       // backward: channels (= threads) per block = 4 warps,
+                              // one per tensor-memory lane quadrant
+constexpr int NWB = GB / 32;  // backward warps per block
+constexpr int TT = 16;        // forward / aggregate staging tile (steps)
+constexpr int SUB = 8;        // forward scalar sub-tile (steps)
+constexpr int KMAX = 64;      // largest chunk (the backward may allow less)
+constexpr int KDEF = 8;       // default chunk
+constexpr int NPART = 24;     // per-channel parameter partials (23 used)
+constexpr float LOG2E = 1.4426950408889634f;
+constexpr float LN2 = 0.6931471805599453f;
+
+// ---------------------------------------------------------------------------
+// small device helpers
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ float ex2(float v) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
+  return r;
+}
+__device__ __forceinline__ float rcp_a(float v) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
+  return r;
+}
+__device__ __forceinline__ float lg2_a(float v) {
+  float r;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
+  return r;
+}
+__device__ __forceinline__ float2 ex2x2(float2 v) { return make_float2(ex2(v.x), ex2(v.y)); }
+__device__ __forceinline__ float2 f2b(float v) { return make_float2(v, v); }
+
+// 1 / (1 + e^-v)
+__device__ __forceinline__ float sigmoid_f(float v) { return rcp_a(1.0f + ex2(-v * LOG2E)); }
+
+// log(1 + e^v) = max(v, 0) + log1p(e^-|v|); log1p(e) for e in (0, 1] from
+// the series e - e^2/2 + e^3/3 below 2^-6 (truncation < e^3/4 relative),
+// else log2(1 + e) ln 2.
+__device__ __forceinline__ float softplus_f(float v) {
+  const float e = ex2(-fabsf(v) * LOG2E);
+  const float series = e * fmaf(e, fmaf(e, 0.33333334f, -0.5f), 1.0f);
+  const float lg = lg2_a(1.0f + e) * LN2;
+  return fmaxf(v, 0.0f) + (e < 0.015625f ? series : lg);
+}
+
+template <typename T> struct Act;
+template <> struct Act<float> {
+  static __device__ __forceinline__ float ld(const float* p) { return *p; }
+  static __device__ __forceinline__ void st(float* p, float v) { *p = v; }
+};
+template <> struct Act<__nv_bfloat16> {
+  static __device__ __forceinline__ float ld(const __nv_bfloat16* p) {
+    return __bfloat162float(*p);
+  }
+  static __device__ __forceinline__ void st(__nv_bfloat16* p, float v) {
+    *p = __float2bfloat16_rn(v);
+  }
+};
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, bool valid) {
+  unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+  int n = valid ? 16 : 0;  // 0 bytes read: the 16 bytes are zero-filled
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(s), "l"(gmem), "r"(n));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+template <int N> __device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
+}
+
+// ---- tensor memory (tcgen05): per-thread row storage ----
+// A CTA of 4 warps owns tensor-memory lanes 0..127 (warp w: lanes 32w..32w+31,
+// one lane per thread).  32x32b accesses move 16 consecutive 32-bit columns
+// of the calling thread's lane.
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {  // whole warp
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)),
+               "r"(ncols) : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {  // whole warp
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tmem_fence_before_sync() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_fence_after_sync() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float2 (&v)[NS / 2]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+      ::"r"(taddr), "f"(v[0].x), "f"(v[0].y), "f"(v[1].x), "f"(v[1].y), "f"(v[2].x), "f"(v[2].y),
+      "f"(v[3].x), "f"(v[3].y), "f"(v[4].x), "f"(v[4].y), "f"(v[5].x), "f"(v[5].y), "f"(v[6].x),
+      "f"(v[6].y), "f"(v[7].x), "f"(v[7].y) : "memory");
+}
+// Load and wait in one statement, so no use of the registers can be placed
+// between the asynchronous load and its completion.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float2 (&v)[NS / 2]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=f"(v[0].x), "=f"(v[0].y), "=f"(v[1].x), "=f"(v[1].y), "=f"(v[2].x), "=f"(v[2].y),
+        "=f"(v[3].x), "=f"(v[3].y), "=f"(v[4].x), "=f"(v[4].y), "=f"(v[5].x), "=f"(v[5].y),
+        "=f"(v[6].x), "=f"(v[6].y), "=f"(v[7].x), "=f"(v[7].y) : "r"(taddr) : "memory");
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const float2 (&v)[4]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
+      ::"r"(taddr), "f"(v[0].x), "f"(v[0].y), "f"(v[1].x), "f"(v[1].y), "f"(v[2].x), "f"(v[2].y),
+      "f"(v[3].x), "f"(v[3].y) : "memory");
+}
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float2 (&v)[4]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=f"(v[0].x), "=f"(v[0].y), "=f"(v[1].x), "=f"(v[1].y), "=f"(v[2].x), "=f"(v[2].y),
+        "=f"(v[3].x), "=f"(v[3].y) : "r"(taddr) : "memory");
+}
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start while the kernel before it in the stream is still
+// running; grid_dep_wait() returns once that kernel has completed and its
+// memory is visible (immediately when there is no such dependency).
+// grid_dep_trigger() lets the next such kernel start launching.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Stage rows [t_first, t_first + rows) x channels [d0, d0 + G) of a
+// [B, T_, D] tensor of element type T into dst[rows][G]; rows outside
+// [0, t_limit) and channels >= D read as zero.  NT threads cooperate.
+template <typename T, int G, int NT>
+__device__ __forceinline__ void stage_rows(T* dst, const T* src, int b, int t_first, int rows,
+                                           int T_, int t_limit, int D, int d0, int tid) {
+  constexpr int EPC = 16 / sizeof(T);
+  constexpr int CPR = G / EPC;
+  const int n = rows * CPR;
+  for (int i = tid; i < n; i += NT) {
+    const int r = i / CPR, cc = i - r * CPR;
+    const int t = t_first + r, dd = d0 + cc * EPC;
+    const bool ok = (t >= 0) && (t < t_limit) && (dd < D);
+    const T* g = ok ? src + ((size_t)b * T_ + t) * D + dd : src;
+    cp_async16(dst + r * G + cc * EPC, g, ok);
+  }
+}
+
+// Stage rows [t_first, t_first + rows) of a [B, T_, NN] tensor whose rows
+// are ld elements apart into dst[rows][NN]; rows outside [0, t_limit) read
+// as zero.
+template <typename T, int NT, int NN = NS>
+__device__ __forceinline__ void stage_bc(T* dst, const T* src, int b, int t_first, int rows,
+                                         int T_, int t_limit, int ld, int tid) {
+  constexpr int EPC = 16 / sizeof(T);
+  constexpr int CPR = NN / EPC;
+  const int n = rows * CPR;
+  for (int i = tid; i < n; i += NT) {
+    const int r = i / CPR, cc = i - r * CPR;
+    const int t = t_first + r;
+    const bool ok = (t >= 0) && (t < t_limit);
+    const T* g = ok ? src + ((size_t)b * T_ + t) * ld + cc * EPC : src;
+    cp_async16(dst + r * NN + cc * EPC, g, ok);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// geometry and kernel arguments
+// ---------------------------------------------------------------------------
+
+struct Geo {
+  int B, T, D, K, nc, S, m;  // S segments of m chunks (the last may be short)
+  int ldbc, lddbc;           // row strides (elements) of Bm/Cm and of dB/dC
+};
+
+__host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+struct FwdArgs {
+  Geo g;
+  const void *x, *dr, *z, *Bm, *Cm;
+  const float *conv_w, *conv_b, *dt_bias, *a_log, *Dp;
+  void *gated, *y_dbg;
+  float* ckpt;
+  float *agg_h, *agg_s;
+  // carried state (all nullable): h before step 0 [B, 16, D] f32, the conv
+  // inputs of steps -3..-1 [B, 3, D] act, and the same two after the window
+  const float* h_in;
+  const void* conv_in;
+  float* h_out;
+  void* conv_out;
+};
+
+struct BwdArgs {
+  Geo g;
+  const void *x, *dr, *z, *Bm, *Cm, *dg;
+  const float *conv_w, *conv_b, *dt_bias, *a_log, *Dp, *ckpt;
+  void *dx, *ddr, *dz, *du_dbg;
+  float *dB, *dC;
+  float *q, *sd, *dxpart, *dchead, *partials;
+  float *d_conv_w, *d_conv_b, *d_dt_bias, *d_a_log, *dD;
+  // carried state (all nullable): the forward's conv inputs of steps -3..-1
+  // [B, 3, D] act; upstream gradients of the window's state outputs
+  // (g_h [B, 16, D] f32, g_conv [B, 3, D] act); gradients of the state
+  // inputs (d_h_in f32, d_conv_in act)
+  const void* conv_in;
+  const float* g_h;
+  const void* g_conv;
+  float* d_h_in;
+  void* d_conv_in;
+  int accumulate;
+  uint32_t tcols;  // tensor-memory columns per CTA for the state history
+};
+
+// Forward shared memory: two staging buffers {x, delta_raw, z: [TT][GF]
+// act; B, C: [TT][16] act}, B and C of the current tile as float [TT][16],
+// and per-step scalars of one sub-tile sc[SUB][GF] float4 (thread-private
+// slots: delta, delta*u, D*u, silu(z)).
+struct FwdSmem {
+  size_t x, dr, z, Bt, Ct, tile, fB, fC, sc, total;
+};
+__host__ __device__ inline FwdSmem fwd_smem(int es) {
+  FwdSmem s;
+  s.x = 0;
+  s.dr = s.x + align_up((size_t)TT * GF * es, 128);
+  s.z = s.dr + align_up((size_t)TT * GF * es, 128);
+  s.Bt = s.z + align_up((size_t)TT * GF * es, 128);
+  s.Ct = s.Bt + align_up((size_t)TT * NS * es, 128);
+  s.tile = s.Ct + align_up((size_t)TT * NS * es, 128);
+  s.fB = 2 * s.tile;
+  s.fC = s.fB + (size_t)TT * NS * 4;
+  s.sc = s.fC + (size_t)TT * NS * 4;
+  s.total = s.sc + (size_t)SUB * GF * 16;
+  return s;
+}
+
+// Split forward shared memory (CH = 128 / (N / 8) channels): two staging
+// buffers {x: [TT+3][CH] (three halo rows), delta_raw, z: [TT][CH]; B, C:
+// [TT][N]}, float B and C of the tile, and per-step scalars sc[SUB][CH]
+// float4 shared by the threads of a channel.
+struct Fwd2Smem {
+  size_t x, dr, z, Bt, Ct, tile, fB, fC, sc, total;
+};
+__host__ __device__ inline Fwd2Smem fwd2_smem(int es, int N) {
+  const int CH = 128 / (N / 8);  // channels per block
+  Fwd2Smem s;
+  s.x = 0;
+  s.dr = s.x + align_up((size_t)(TT + 3) * CH * es, 128);
+  s.z = s.dr + align_up((size_t)TT * CH * es, 128);
+  s.Bt = s.z + align_up((size_t)TT * CH * es, 128);
+  s.Ct = s.Bt + align_up((size_t)TT * N * es, 128);
+  s.tile = s.Ct + align_up((size_t)TT * N * es, 128);
+  s.fB = 2 * s.tile;
+  s.fC = s.fB + (size_t)TT * N * 4;
+  s.sc = s.fC + (size_t)TT * N * 4;
+  s.total = s.sc + (size_t)SUB * CH * 16;
+  return s;
+}
+
+// Backward shared memory: two staging buffers {x: [K+3][GB] (three halo rows
+// before the chunk), delta_raw, z, d_gated: [K][GB] act; B, C: [K][16] act;
+// the chunk's start state ck: [16][GB] f32}; B and C of the current chunk as
+// float (the recomputed states live in tensor memory, see m3_bwd_kernel);
+// per-step scalars, two thread-private float4 slots per step: s0[K][GB] =
+// (delta, delta*u, dy, dz factor -> sum_n A dh exp(delta A) h_{t-1}) and
+// s1[K][GB] = (D*u -> sum_n dh B, sigmoid(delta_raw + dt_bias), sigmoid(c),
+// c); per-warp dB/dC sums red[K][NWB][32].
+struct BwdSmem {
+  size_t x, dr, z, dg, Bt, Ct, ck, tile, fB, fC, scal, red, total;
+};
+__host__ __device__ inline BwdSmem bwd_smem(int K, int es) {
+  BwdSmem s;
+  s.x = 0;
+  s.dr = s.x + align_up((size_t)(K + 3) * GB * es, 128);
+  s.z = s.dr + align_up((size_t)K * GB * es, 128);
+  s.dg = s.z + align_up((size_t)K * GB * es, 128);
+  s.Bt = s.dg + align_up((size_t)K * GB * es, 128);
+  s.Ct = s.Bt + align_up((size_t)K * NS * es, 128);
+  s.ck = s.Ct + align_up((size_t)K * NS * es, 128);
+  s.tile = s.ck + (size_t)NS * GB * 4;
+  s.fB = 2 * s.tile;
+  s.fC = s.fB + (size_t)K * NS * 4;
+  s.scal = s.fC + (size_t)K * NS * 4;
+  s.red = s.scal + (size_t)2 * K * GB * 16;
+  s.total = s.red + (size_t)K * NWB * 32 * 4;
+  return s;
+}
+
+// Split backward (CH = 128 / (N / 8) channels per block): the same staging
+// buffers for CH channels and N-wide B and C; per-step scalars s0/s1
+// [K][CH] float4 shared by the threads of a channel; the conv-input gradient
+// of the chunk's steps and of the next chunk's first three, dcs[K+3][CH];
+// per-warp dB/dC sums red[K][4][2N].
+struct Bwd2Smem {
+  size_t x, dr, z, dg, Bt, Ct, ck, tile, fB, fC, scal, dcs, red, total;
+};
+__host__ __device__ inline Bwd2Smem bwd2_smem(int K, int es, int N) {
+  const int CH = 128 / (N / 8);  // channels per block
+  Bwd2Smem s;
+  s.x = 0;
+  s.dr = s.x + align_up((size_t)(K + 3) * CH * es, 128);
+  s.z = s.dr + align_up((size_t)K * CH * es, 128);
+  s.dg = s.z + align_up((size_t)K * CH * es, 128);
+  s.Bt = s.dg + align_up((size_t)K * CH * es, 128);
+  s.Ct = s.Bt + align_up((size_t)K * N * es, 128);
+  s.ck = s.Ct + align_up((size_t)K * N * es, 128);
+  s.tile = s.ck + (size_t)N * CH * 4;
+  s.fB = 2 * s.tile;
+  s.fC = s.fB + (size_t)K * N * 4;
+  s.scal = s.fC + (size_t)K * N * 4;
+  s.dcs = s.scal + (size_t)2 * K * CH * 16;
+  s.red = s.dcs + align_up((size_t)(K + 3) * CH * 4, 128);
+  s.total = s.red + (size_t)K * 4 * 2 * N * 4;
+  return s;
+}
+
+// Backward aggregate shared memory: two buffers {delta_raw, z, d_gated:
+// [TT][GB]; C: [TT][16]}, float C and per-step (delta, dy) [TT][GB] float2.
+struct AggSmem {
+  size_t dr, z, dg, Ct, tile, fC, sc, total;
+};
+__host__ __device__ inline AggSmem agg_smem(int es, int N = NS) {
+  AggSmem s;
+  s.dr = 0;
+  s.z = s.dr + align_up((size_t)TT * GB * es, 128);
+  s.dg = s.z + align_up((size_t)TT * GB * es, 128);
+  s.Ct = s.dg + align_up((size_t)TT * GB * es, 128);
+  s.tile = s.Ct + align_up((size_t)TT * N * es, 128);
+  s.fC = 2 * s.tile;
+  s.sc = s.fC + (size_t)TT * N * 4;
+  s.total = s.sc + (size_t)TT * GB * 8;
+  return s;
+}
+
+// ---------------------------------------------------------------------------
+// SiLU and conv backward of the two-phase backward: with du from the scan
+// backward and a gradient reaching u from outside the layer core (the x_proj
+// path), dc = (du + du_extra) silu'(c) and d_x[s] = sum_k dc[s+3-k] w[k];
+// per-(batch, tile) partials of d_conv_b and d_conv_w.  One thread per
+// channel over a tile of steps, plus the three steps after it, whose dc
+// reaches the tile's last d_x.  Plain coalesced loads: every value is read
+// by one thread.
+// ---------------------------------------------------------------------------
+
+struct ConvArgs {
+  int B, T, D, tile, ntiles;
+  const void *x, *du, *du_extra;  // [B, T, D] act (du_extra nullable)
+  const float *conv_w, *conv_b;
+  void* dx;                       // [B, T, D] act
+  float* part;                    // [B * ntiles, 5, D]: d_conv_b, d_conv_w[0..3]
+  const void* conv_in;            // [B, 3, D] act, nullable
+  const void* g_conv;             // [B, 3, D] act, nullable
+  void* d_conv_in;                // [B, 3, D] act, nullable
+  float *d_conv_w, *d_conv_b;
+  int accumulate;
+};
+
+// Steps per conv-backward tile: rows [t0 - 3, t0 + CT + 3) of x and
+// [t0, t0 + CT + 3) of du and du_extra are staged in shared memory by 16-byte
+// copies, so each thread's walk over the tile reads no global memory.
+constexpr int CT = 32;
+struct ConvSmem {
+  size_t x, du, de, total;
+};
+__host__ __device__ inline ConvSmem conv_smem(int es) {
+  ConvSmem s;
+  s.x = 0;
+  s.du = align_up((size_t)(CT + 6) * 128 * es, 128);
+  s.de = s.du + align_up((size_t)(CT + 3) * 128 * es, 128);
+  s.total = s.de + align_up((size_t)(CT + 3) * 128 * es, 128);
+  return s;
+}
+
+
+// ---------------------------------------------------------------------------
+// decode: the forward of a short window (typically one token per sequence)
+// from the carried state, updating that state in place; no checkpoints, no
+// time split.  One thread per channel keeps its N state lanes in registers;
+// B_t and C_t of each step are staged in shared memory for the block.
+// ---------------------------------------------------------------------------
+
+struct DecArgs {
+  int B, T, D;
+  int ldbc;  // row stride (elements) of Bm and Cm
+  const void *x, *dr, *z, *Bm, *Cm;
+  const float *conv_w, *conv_b, *dt_bias, *a_log, *Dp;
+  float* h;    // [B, N, D] f32, in and out
+  void* conv;  // [B, 3, D] act, in and out
+  void *gated, *y_dbg;
+};
+
+constexpr int GD = 128;  // decode: channels (= threads) per block
+
+
+// ---------------------------------------------------------------------------
+// host side: sizes, the plan, launching
+// ---------------------------------------------------------------------------
+
+// opt-in shared memory per block, less 1 KB kept for static shared memory
+constexpr size_t SMEM_CAP = 227 * 1024 - 1024;
+
+// Tensor-memory columns a backward CTA allocates for K rows of 16 states:
+// a power of two >= 32 (the allocation granularity), at most 512.
+__host__ inline uint32_t tmem_cols_for(int K) {
+  uint32_t c = 32;
+  while (c < (uint32_t)K * NS) c <<= 1;
+  return c;
+}
+
+// Tensor-memory columns of a two-thread-per-channel backward CTA: 8 per step.
+__host__ inline uint32_t tmem_cols2_for(int K) {
+  uint32_t c = 32;
+  while (c < (uint32_t)K * 8) c <<= 1;
+  return c;
+}
+
+// Largest chunk whose backward fits: 16 K tensor-memory columns <= 512 and
+// the shared-memory footprint within one block's limit.
+__host__ inline int kmax_for(int es) {
+  int k = KMAX;
+  while (k > 1 && (bwd_smem(k, es).total > SMEM_CAP || tmem_cols_for(k) > 512)) --k;
+  return k;
+}
+
+// Shared memory to request per backward CTA: its footprint, raised if needed
+// so that no more CTAs fit on one SM than tensor memory can serve at once
+// (512 columns / tcols), so no allocation ever has to wait.
+__host__ inline size_t bwd_launch_smem(int K, int es, int smem_per_sm) {
+  const int max_ctas = 512 / (int)tmem_cols_for(K);
+  size_t need = bwd_smem(K, es).total;
+  const size_t floor_bytes = (size_t)smem_per_sm / (max_ctas + 1) + 1;  // > 1/(max+1) of the SM
+  if (need < floor_bytes) need = floor_bytes;
+  return align_up(need, 128);
+}
+
+// The same residency cap for the two-thread backward.
+__host__ inline size_t bwd2_launch_smem(int K, int es, int N, int smem_per_sm) {
+  const int max_ctas = 512 / (int)tmem_cols2_for(K);
+  size_t need = bwd2_smem(K, es, N).total;
+  const size_t floor_bytes = (size_t)smem_per_sm / (max_ctas + 1) + 1;
+  if (need < floor_bytes) need = floor_bytes;
+  return align_up(need, 128);
+}
+
+struct Plan {
+  int B, T, D, K, nc;
+  int N;  // d_state
+  int ldbc, lddbc;
+  int Sf, mf, Sb, mb;
+  size_t ckpt_bytes, ws_bytes;
+  // workspace offsets (bytes)
+  size_t f_aggh, f_aggs;
+  size_t b_part, b_q, b_sd, b_dxpart, b_dchead;
+  int ctile, cntiles;  // conv backward: steps per tile, tiles per sequence
+  size_t c_part;
+  int fwd_launches, bwd_launches;
+  int fwd_tpc, bwd_tpc;  // threads per channel in the forward's and backward's main kernels
+};
+
+inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Record a failed CUDA call for m3scan_last_cuda_error (m3_api.cu).
+cudaError_t note(cudaError_t e);
+
+// Launch with programmatic stream serialization when `pdl`: the kernel may
+// begin while the previous kernel of the same call runs, and waits for it
+// (grid_dep_wait) before reading its results.  The first kernel of a call
+// is launched without it, so it starts after everything before it.
+template <typename... Args, typename... Vals>
+cudaError_t launch_k(void (*kern)(Args...), dim3 grid, unsigned block, size_t smem,
+                     cudaStream_t st, bool pdl, Vals... vals) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, vals...);
+}
+
+// Provided by m3_fwd.cu, m3_bwd.cu and m3_aux.cu for T = float and
+// __nv_bfloat16.
+template <typename T> m3_status launch_fwd(const Plan& p, FwdArgs a, cudaStream_t st);
+template <typename T>
+m3_status launch_bwd(const Plan& p, BwdArgs a, cudaStream_t st, int smem_per_sm, bool scan);
+template <typename T> cudaError_t launch_conv_bwd(const ConvArgs& a, dim3 grid, cudaStream_t st);
+template <typename T> cudaError_t launch_decode_n(int n, const DecArgs& a, cudaStream_t st, int sms);
+// kernel attributes (once per device) and occupancy of the one-thread kernels
+template <typename T> cudaError_t set_fwd_attrs();
+template <typename T> cudaError_t set_bwd_attrs();
+template <typename T> cudaError_t set_aux_attrs();
+template <typename T> cudaError_t fwd_occupancy(int* blocks);
+template <typename T> cudaError_t bwd_occupancy(int chunk, int smem_per_sm, int* blocks);
+
+}  // namespace m3
