@@ -254,19 +254,8 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(BwdArgs a) {
   if (s + 1 < g.S) {
     // chain the later segments right to left: in(s'-1) = exp(A sum delta_s')
     // in(s') + local(s'), with in(S-1) = 0
-    const float* __restrict__ sd = a.sd;
-    const float* __restrict__ q = a.q;
-#pragma unroll 2
-    for (int sp = g.S - 1; sp > s; --sp) {
-      const size_t bs = (size_t)b * g.S + sp;
-      const float2 dl2 = f2b(active ? sd[bs * g.D + d] : 0.f);
-#pragma unroll
-      for (int i = 0; i < NS / 2; ++i) {
-        const float* qq = q + (bs * NS + lane_of(i)) * g.D + d;
-        const float2 loc = active ? make_float2(qq[0], qq[g.D]) : make_float2(0.f, 0.f);
-        carry[i] = __ffma2_rn(ex2x2(__fmul2_rn(dl2, a2[i])), carry[i], loc);
-      }
-    }
+    chain_segments<NS / 2, 2>(carry, a2, a.sd, a.q, NS, (size_t)b * g.S, g.S - 1, -1, g.S - 1 - s,
+                              g.D, d, active, lane_of);
   }
   float2 dAp[NS / 2];  // dL/dA per lane
 #pragma unroll
@@ -670,19 +659,8 @@ __global__ void __launch_bounds__(128, 4) m3_bwd2_kernel(BwdArgs a) {
   grid_dep_trigger();
   grid_dep_wait();
   if (s + 1 < g.S) {
-    const float* __restrict__ sd = a.sd;
-    const float* __restrict__ q = a.q;
-#pragma unroll 2
-    for (int sp = g.S - 1; sp > s; --sp) {
-      const size_t bs = (size_t)b * g.S + sp;
-      const float2 dl2 = f2b(active ? sd[bs * g.D + d] : 0.f);
-#pragma unroll
-      for (int P = 0; P < 4; ++P) {
-        const float* qq = q + (bs * N + lane_of(P)) * g.D + d;
-        const float2 loc = active ? make_float2(qq[0], qq[g.D]) : make_float2(0.f, 0.f);
-        carry[P] = __ffma2_rn(ex2x2(__fmul2_rn(dl2, a2[P])), carry[P], loc);
-      }
-    }
+    chain_segments<4, 4>(carry, a2, a.sd, a.q, N, (size_t)b * g.S, g.S - 1, -1, g.S - 1 - s, g.D, d,
+                         active, lane_of);
   }
   float2 dAp[4];
 #pragma unroll

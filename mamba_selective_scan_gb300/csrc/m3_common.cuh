@@ -182,6 +182,43 @@ __device__ __forceinline__ void stage_bc(T* dst, const T* src, int b, int t_firs
   }
 }
 
+// Chain segment aggregates into v (NP lane pairs): for cnt segments
+// sp = first, first + step, ...:  v = exp2(sum_delta(sp) a2) v + local(sp),
+// with sum_delta at sums[(bS + sp) D + d] and the local lane pair P at
+// locs[((bS + sp) N + lane(P)) D + d] (and the next row).  The loads of CB
+// segments are issued before their multiply-adds, so a chain of cnt
+// segments waits for about cnt / CB memory round trips, not cnt.
+template <int NP, int CB, typename Lane>
+__device__ __forceinline__ void chain_segments(float2 (&v)[NP], const float2 (&a2)[NP],
+                                               const float* __restrict__ sums,
+                                               const float* __restrict__ locs, int N, size_t bS,
+                                               int first, int step, int cnt, int D, int d,
+                                               bool active, Lane lane) {
+  for (int i0 = 0; i0 < cnt; i0 += CB) {
+    float dl[CB];
+    float2 loc[CB][NP];
+#pragma unroll
+    for (int k = 0; k < CB; ++k) {
+      const bool ok = active && i0 + k < cnt;
+      const size_t bs = bS + (ok ? first + (i0 + k) * step : 0);
+      dl[k] = ok ? sums[bs * D + d] : 0.f;
+#pragma unroll
+      for (int P = 0; P < NP; ++P) {
+        const float* l = locs + (bs * N + lane(P)) * D + d;
+        loc[k][P] = ok ? make_float2(l[0], l[D]) : make_float2(0.f, 0.f);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < CB; ++k) {
+      if (i0 + k < cnt) {
+        const float2 dl2 = f2b(dl[k]);
+#pragma unroll
+        for (int P = 0; P < NP; ++P) v[P] = __ffma2_rn(ex2x2(__fmul2_rn(dl2, a2[P])), v[P], loc[k][P]);
+      }
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------
 // geometry and kernel arguments
 // ---------------------------------------------------------------------------

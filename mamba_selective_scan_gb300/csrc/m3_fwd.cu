@@ -74,19 +74,8 @@ __global__ void __launch_bounds__(GF) m3_fwd_kernel(FwdArgs a) {
     // The scan is linear in the state: chain the earlier segments' local end
     // states with their decays, start(s'+1) = exp(A sum delta_s') start(s') +
     // local_end(s'), to get this segment's true start state.
-    const float* __restrict__ agg_s = a.agg_s;
-    const float* __restrict__ agg_h = a.agg_h;
-#pragma unroll 4
-    for (int sp = 0; sp < s; ++sp) {
-      const size_t bs = (size_t)b * g.S + sp;
-      const float2 dl2 = f2b(active ? agg_s[bs * g.D + d] : 0.f);
-#pragma unroll
-      for (int i = 0; i < NS / 2; ++i) {
-        const float* ah = agg_h + (bs * NS + 2 * i) * g.D + d;
-        const float2 loc = active ? make_float2(ah[0], ah[g.D]) : make_float2(0.f, 0.f);
-        h[i] = __ffma2_rn(ex2x2(__fmul2_rn(dl2, a2[i])), h[i], loc);
-      }
-    }
+    chain_segments<NS / 2, 1>(h, a2, a.agg_s, a.agg_h, NS, (size_t)b * g.S, 0, 1, s, g.D, d, active,
+                              [](int i) { return 2 * i; });
   }
 
   // conv window x[t-3], x[t-2], x[t-1]; steps before 0 come from the
@@ -307,17 +296,8 @@ __global__ void __launch_bounds__(128) m3_fwd2_kernel(FwdArgs a) {
   }
   if (FINAL && s > 0) {
     grid_dep_wait();  // the aggregate pass's outputs
-#pragma unroll 2
-    for (int sp = 0; sp < s; ++sp) {
-      const size_t bs = (size_t)b * g.S + sp;
-      const float2 dl2 = f2b(active ? a.agg_s[bs * g.D + d] : 0.f);
-#pragma unroll
-      for (int P = 0; P < 4; ++P) {
-        const float* ah = a.agg_h + (bs * N + 8 * hf + 2 * P) * g.D + d;
-        const float2 loc = active ? make_float2(ah[0], ah[g.D]) : make_float2(0.f, 0.f);
-        h[P] = __ffma2_rn(ex2x2(__fmul2_rn(dl2, a2[P])), h[P], loc);
-      }
-    }
+    chain_segments<4, 2>(h, a2, a.agg_s, a.agg_h, N, (size_t)b * g.S, 0, 1, s, g.D, d, active,
+                         [hf](int P) { return 8 * hf + 2 * P; });
   }
   float sdelta = 0.f;
   float4* scs = reinterpret_cast<float4*>(smem + L.sc) + ch;  // shared by the channel's threads, stride CH
