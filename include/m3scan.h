@@ -376,6 +376,14 @@ const char* m3scan_last_cuda_error(void);
 /* Library version as major * 10000 + minor * 100 + patch. */
 int32_t m3scan_version(void);
 
+/* Device-side status of the calling thread's current device since the last
+ * query, then cleared: *out = 0 if every kernel ran normally; nonzero if a
+ * kernel gave up waiting for a tile copy into shared memory (each such wait
+ * is bounded to about a second so the GPU cannot hang; that call's outputs
+ * are then incomplete).  Synchronous: it waits for the device's queued
+ * work.  Returns M3_ERR_NULL for a NULL out, M3_ERR_CUDA if reading fails. */
+m3_status m3scan_device_status(int32_t* out);
+
 #ifdef __cplusplus
 }
 #endif

@@ -57,6 +57,38 @@ cudaError_t note(cudaError_t e) {
   return e;
 }
 
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                                  CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                  CUtensorMapFloatOOBfill);
+
+bool encode_tile_map(CUtensorMap* map, int es, int rank, const void* ptr, const uint64_t* dims,
+                     const uint64_t* strides, const uint32_t* box) {
+  static EncodeTiledFn fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      f = nullptr;
+    return reinterpret_cast<EncodeTiledFn>(f);
+  }();
+  if (!fn || rank < 1 || rank > 5) return false;
+  cuuint64_t gd[5], gs[4];
+  cuuint32_t bx[5], es1[5];
+  for (int i = 0; i < rank; ++i) {
+    gd[i] = dims[i];
+    bx[i] = box[i];
+    es1[i] = 1;
+    if (i + 1 < rank) gs[i] = strides[i];
+  }
+  const CUresult r = fn(map, es == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                        (cuuint32_t)rank, const_cast<void*>(ptr), gd, gs, bx, es1, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 template <typename T>
 cudaError_t set_attrs() {
   cudaError_t e = set_fwd_attrs<T>();
@@ -289,6 +321,15 @@ const char* m3scan_status_string(m3_status s) {
 }
 
 int32_t m3scan_version(void) { return 100; }
+
+m3_status m3scan_device_status(int32_t* out) {
+  if (!out) return M3_ERR_NULL;
+  unsigned vf = 0, vb = 0;
+  if (note(take_fwd_status(&vf)) != cudaSuccess || note(take_bwd_status(&vb)) != cudaSuccess)
+    return M3_ERR_CUDA;
+  *out = (int32_t)(vf | vb);
+  return M3_OK;
+}
 
 const char* m3scan_last_cuda_error(void) { return cudaGetErrorName(g_last_cuda); }
 

@@ -4,6 +4,20 @@
 
 namespace m3 {
 
+// nonzero once a kernel here gave up waiting for a tile copy
+__device__ unsigned int g_bwd_status;
+
+cudaError_t take_bwd_status(unsigned* out) {
+  unsigned v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_bwd_status, sizeof(v));
+  if (e == cudaSuccess && v) {
+    const unsigned zero = 0;
+    e = cudaMemcpyToSymbol(g_bwd_status, &zero, sizeof(zero));
+  }
+  *out = v;
+  return e;
+}
+
 // ---------------------------------------------------------------------------
 // backward aggregate (segments 1..S-1): the adjoint carry a segment passes to
 // its predecessor when nothing enters it from the right,
@@ -15,7 +29,7 @@ namespace m3 {
 // (8 lanes each, 128 / TPC channels per block), the threads of a channel
 // taking the scalar pass of every TPC-th step.
 template <typename T, int TPC, int N>
-__global__ void __launch_bounds__(GB) m3_bwd_agg_kernel(BwdArgs a) {
+__global__ void __launch_bounds__(GB) m3_bwd_agg_kernel(const __grid_constant__ BwdArgs a) {
   constexpr int G = GB / TPC;        // channels per block
   constexpr int NL = N / TPC;        // state lanes per thread
   extern __shared__ __align__(128) unsigned char smem[];
@@ -34,15 +48,29 @@ __global__ void __launch_bounds__(GB) m3_bwd_agg_kernel(BwdArgs a) {
   float* fC = reinterpret_cast<float*>(smem + L.fC);
   const int ntiles = (t_end - t_begin + TT - 1) / TT;
   auto tile_start = [&](int i) { return max(t_begin, t_end - (i + 1) * TT); };
+  // Tiles of TT rows (the first one, at the segment's start, overlaps rows
+  // already covered; only its own rows are read) by tensor-map copies
+  // issued by thread 0.
+  __shared__ __align__(8) uint64_t tbar[2];  // tile copies into staging buffer 0 / 1
+  if (tid == 0) {
+    mbar_init(&tbar[0], 1);
+    mbar_init(&tbar[1], 1);
+    mbar_init_fence();
+  }
+  __syncthreads();
+  const bool misaligned = (smem_u32(smem) & 127u) != 0;  // tile copies need 128-byte aligned buffers
+  const uint32_t tile_bytes = (uint32_t)((3 * TT * G + TT * N) * sizeof(T));
   auto stage = [&](int i, int buf) {
-    unsigned char* base = smem + (size_t)buf * L.tile;
-    const int t0 = tile_start(i);
-    const int rows = (t_end - i * TT) - t0;
-    stage_rows<T, G, GB>(reinterpret_cast<T*>(base + L.dr), static_cast<const T*>(a.dr), b, t0, rows, g.T, g.T, g.D, d0, tid);
-    stage_rows<T, G, GB>(reinterpret_cast<T*>(base + L.z), static_cast<const T*>(a.z), b, t0, rows, g.T, g.T, g.D, d0, tid);
-    stage_rows<T, G, GB>(reinterpret_cast<T*>(base + L.dg), static_cast<const T*>(a.dg), b, t0, rows, g.T, g.T, g.D, d0, tid);
-    stage_bc<T, GB, N>(reinterpret_cast<T*>(base + L.Ct), static_cast<const T*>(a.Cm), b, t0, rows, g.T, g.T, g.ldbc, tid);
-    cp_async_commit();
+    if (tid == 0 && !misaligned) {
+      unsigned char* base = smem + (size_t)buf * L.tile;
+      const int t0 = tile_start(i);
+      fence_proxy_async();
+      mbar_expect_tx(&tbar[buf], tile_bytes);
+      tma_load_3d(base + L.dr, &a.tm[TM_ADR], d0, t0, b, &tbar[buf]);
+      tma_load_3d(base + L.z, &a.tm[TM_AZ], d0, t0, b, &tbar[buf]);
+      tma_load_3d(base + L.dg, &a.tm[TM_ADG], d0, t0, b, &tbar[buf]);
+      tma_load_3d(base + L.Ct, &a.tm[TM_AC], 0, t0, b, &tbar[buf]);
+    }
   };
 
   stage(0, 0);  // first tile in flight while the parameters load
@@ -75,13 +103,16 @@ __global__ void __launch_bounds__(GB) m3_bwd_agg_kernel(BwdArgs a) {
   }
   for (int i = 0; i < ntiles; ++i) {
     const int buf = i & 1;
-    if (i + 1 < ntiles) {
-      stage(i + 1, buf ^ 1);
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
+    if (i + 1 < ntiles) stage(i + 1, buf ^ 1);
+    const bool landed = !misaligned && mbar_wait(&tbar[buf], (i >> 1) & 1);
+    if (__syncthreads_or(!landed)) {
+      // a tile did not arrive: report it, let the copy issued above drain, leave
+      if (tid == 0) {
+        atomicOr(&g_bwd_status, 1u);
+        if (!misaligned && i + 1 < ntiles) mbar_wait(&tbar[buf ^ 1], ((i + 1) >> 1) & 1);
+      }
+      return;
     }
-    __syncthreads();
     const unsigned char* base = smem + (size_t)buf * L.tile;
     const int t0 = tile_start(i);
     const int steps = (t_end - i * TT) - t0;
@@ -166,7 +197,7 @@ __device__ __forceinline__ float warp_sum16_rotated(float (&v)[NS], int lane) {
 // conv backward then run in m3_conv_bwd_kernel with du plus any gradient
 // reaching u from outside the layer core.
 template <typename T, bool ST, bool SCAN>
-__global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(BwdArgs a) {
+__global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(const __grid_constant__ BwdArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   const Geo g = a.g;
   const int tid = threadIdx.x;
@@ -194,7 +225,13 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(BwdArgs a) {
   // tensor memory: row j of this thread = columns [16 j, 16 j + 16) of its
   // lane.  Warp 0 allocates for the CTA; every exit path below deallocates.
   __shared__ uint32_t tmem_slot;
+  __shared__ __align__(8) uint64_t tbar[2];  // tile copies into staging buffer 0 / 1
   if (warp == 0) tmem_alloc(&tmem_slot, a.tcols);
+  if (tid == 32) {
+    mbar_init(&tbar[0], 1);
+    mbar_init(&tbar[1], 1);
+    mbar_init_fence();
+  }
   tmem_fence_before_sync();
   __syncthreads();
   tmem_fence_after_sync();
@@ -230,20 +267,26 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(BwdArgs a) {
       carry[i] = make_float2(gh[(size_t)n * g.D], gh[(size_t)(n + 1) * g.D]);
     }
   }
-  const T* xg = static_cast<const T*>(a.x);
+  // A chunk's tiles arrive by tensor-map copies issued by thread 0: x with
+  // its three halo rows before the chunk, delta_raw, z, d_gated, B, C and
+  // the chunk's start state (16 rows of GB floats); rows outside [0, T) and
+  // channels past d_inner arrive as zeros.
+  const uint32_t tile_bytes = (uint32_t)((4 * K + 3) * GB * sizeof(T) + 2 * K * NS * sizeof(T) + NS * GB * 4);
+  const bool misaligned = (smem_u32(smem) & 127u) != 0;  // tile copies need 128-byte aligned buffers
   auto stage = [&](int c, int buf) {
-    unsigned char* base = smem + (size_t)buf * L.tile;
-    const int t0 = c * K;
-    stage_rows<T, GB, GB>(reinterpret_cast<T*>(base + L.x), xg, b, t0 - 3, K + 3, g.T, g.T, g.D, d0, tid);
-    stage_rows<T, GB, GB>(reinterpret_cast<T*>(base + L.dr), static_cast<const T*>(a.dr), b, t0, K, g.T, g.T, g.D, d0, tid);
-    stage_rows<T, GB, GB>(reinterpret_cast<T*>(base + L.z), static_cast<const T*>(a.z), b, t0, K, g.T, g.T, g.D, d0, tid);
-    stage_rows<T, GB, GB>(reinterpret_cast<T*>(base + L.dg), static_cast<const T*>(a.dg), b, t0, K, g.T, g.T, g.D, d0, tid);
-    stage_bc<T, GB>(reinterpret_cast<T*>(base + L.Bt), static_cast<const T*>(a.Bm), b, t0, K, g.T, g.T, g.ldbc, tid);
-    stage_bc<T, GB>(reinterpret_cast<T*>(base + L.Ct), static_cast<const T*>(a.Cm), b, t0, K, g.T, g.T, g.ldbc, tid);
-    // chunk start state: 16 rows of GB floats from ckpt[b, c, :, d0:d0+GB]
-    stage_rows<float, GB, GB>(reinterpret_cast<float*>(base + L.ck), a.ckpt + ((size_t)b * g.nc + c) * NS * g.D,
-                              0, 0, NS, NS, NS, g.D, d0, tid);
-    cp_async_commit();
+    if (tid == 0 && !misaligned) {
+      unsigned char* base = smem + (size_t)buf * L.tile;
+      const int t0 = c * K;
+      fence_proxy_async();
+      mbar_expect_tx(&tbar[buf], tile_bytes);
+      tma_load_3d(base + L.x, &a.tm[TM_X], d0, t0 - 3, b, &tbar[buf]);
+      tma_load_3d(base + L.dr, &a.tm[TM_DR], d0, t0, b, &tbar[buf]);
+      tma_load_3d(base + L.z, &a.tm[TM_Z], d0, t0, b, &tbar[buf]);
+      tma_load_3d(base + L.dg, &a.tm[TM_DG], d0, t0, b, &tbar[buf]);
+      tma_load_3d(base + L.Bt, &a.tm[TM_B], 0, t0, b, &tbar[buf]);
+      tma_load_3d(base + L.Ct, &a.tm[TM_C], 0, t0, b, &tbar[buf]);
+      tma_load_4d(base + L.ck, &a.tm[TM_CK], d0, 0, c, b, &tbar[buf]);
+    }
   };
 
   stage(c_end - 1, 0);  // last chunk in flight while the carries load
@@ -264,15 +307,21 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(BwdArgs a) {
   float dcw[WC] = {0.f, 0.f, 0.f, 0.f};
   float dc1 = 0.f, dc2 = 0.f, dc3 = 0.f;  // conv-input gradient at t+1, t+2, t+3
 
+  bool aborted = false;
   for (int c = c_end - 1; c >= c_begin; --c) {
-    const int buf = (c_end - 1 - c) & 1;
-    if (c - 1 >= c_begin) {
-      stage(c - 1, buf ^ 1);
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
+    const int it = c_end - 1 - c;  // buffer it & 1, its (it >> 1)-th use
+    const int buf = it & 1;
+    if (c - 1 >= c_begin) stage(c - 1, buf ^ 1);
+    const bool landed = !misaligned && mbar_wait(&tbar[buf], (it >> 1) & 1);
+    if (__syncthreads_or(!landed)) {
+      // a tile did not arrive: report it, let the copy issued above drain, leave
+      if (tid == 0) {
+        atomicOr(&g_bwd_status, 1u);
+        if (!misaligned && c - 1 >= c_begin) mbar_wait(&tbar[buf ^ 1], ((it + 1) >> 1) & 1);
+      }
+      aborted = true;
+      break;
     }
-    __syncthreads();
     const unsigned char* base = smem + (size_t)buf * L.tile;
     if (ST && a.conv_in && c * K < 3 && active) {
       // halo rows before step 0 (staged as zeros): the carried conv inputs.
@@ -434,6 +483,9 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(BwdArgs a) {
       }
 
       // ---- scalar pass: du, d delta, softplus, SiLU and conv backward ----
+      // conv inputs of steps t-2, t-1, t (tile rows j+1 .. j+3), slid down a row per step
+      float xw1 = Act<T>::ld(xt + nst * GB + tid), xw2 = Act<T>::ld(xt + (nst + 1) * GB + tid),
+            xw3 = Act<T>::ld(xt + (nst + 2) * GB + tid);
 #pragma unroll 2
       for (int j = nst - 1; j >= 0; --j) {
         const int t = c * K + j;
@@ -455,8 +507,14 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(BwdArgs a) {
         }
         const float dc = du * (sc * fmaf(cpre, 1.f - sc, 1.f));
         dcb_acc += dc;
-#pragma unroll
-        for (int k = 0; k < WC; ++k) dcw[k] = fmaf(dc, Act<T>::ld(xt + (j + k) * GB + tid), dcw[k]);
+        const float xw0 = Act<T>::ld(xt + j * GB + tid);
+        dcw[0] = fmaf(dc, xw0, dcw[0]);
+        dcw[1] = fmaf(dc, xw1, dcw[1]);
+        dcw[2] = fmaf(dc, xw2, dcw[2]);
+        dcw[3] = fmaf(dc, xw3, dcw[3]);
+        xw3 = xw2;
+        xw2 = xw1;
+        xw1 = xw0;
         float dxv = fmaf(dc, w[3], fmaf(dc1, w[2], fmaf(dc2, w[1], dc3 * w[0])));
         if (ST && a.g_conv && t >= g.T - 3 && active)  // x[t] is also a conv-state output
           dxv += Act<T>::ld(static_cast<const T*>(a.g_conv) + ((size_t)b * 3 + t - (g.T - 3)) * g.D + d);
@@ -489,47 +547,49 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(BwdArgs a) {
     __syncthreads();
   }
 
-  if (ST && s == 0 && active) {
-    if (a.d_h_in) {  // carry = exp(delta_0 A) dL/dh_0 = dL/dh_{-1}
-      float* dh0 = a.d_h_in + (size_t)b * NS * g.D + d;
-#pragma unroll
+  if (!aborted) {
+    if (ST && s == 0 && active) {
+      if (a.d_h_in) {  // carry = exp(delta_0 A) dL/dh_0 = dL/dh_{-1}
+        float* dh0 = a.d_h_in + (size_t)b * NS * g.D + d;
+  #pragma unroll
+        for (int i = 0; i < NS / 2; ++i) {
+          const int n = lane_of(i);
+          dh0[(size_t)n * g.D] = carry[i].x;
+          dh0[(size_t)(n + 1) * g.D] = carry[i].y;
+        }
+      }
+      if (!SCAN && a.d_conv_in) {
+        // conv inputs of steps -1, -2, -3 reach the conv outputs of steps
+        // 0..2 (dc1 = dc_0, dc2 = dc_1, dc3 = dc_2; zero past the sequence),
+        // and, when T < 3, the conv-state output too
+        float v[3];
+        v[2] = fmaf(dc1, w[2], fmaf(dc2, w[1], dc3 * w[0]));
+        v[1] = fmaf(dc1, w[1], dc2 * w[0]);
+        v[0] = dc1 * w[0];
+        T* dci = static_cast<T*>(a.d_conv_in) + (size_t)b * 3 * g.D + d;
+  #pragma unroll
+        for (int r = 0; r < 3; ++r) {
+          const int ro = r - g.T;  // row of the conv-state output holding step r - 3
+          if (a.g_conv && ro >= 0)
+            v[r] += Act<T>::ld(static_cast<const T*>(a.g_conv) + ((size_t)b * 3 + ro) * g.D + d);
+          Act<T>::st(dci + (size_t)r * g.D, v[r]);
+        }
+      }
+    }
+    if (active) {
+      float* Pp = a.partials + ((size_t)b * g.S + s) * NPART * g.D;
+  #pragma unroll
       for (int i = 0; i < NS / 2; ++i) {
         const int n = lane_of(i);
-        dh0[(size_t)n * g.D] = carry[i].x;
-        dh0[(size_t)(n + 1) * g.D] = carry[i].y;
+        Pp[(size_t)n * g.D + d] = dAp[i].x;
+        Pp[(size_t)(n + 1) * g.D + d] = dAp[i].y;
       }
+      Pp[(size_t)16 * g.D + d] = dD_acc;
+      Pp[(size_t)17 * g.D + d] = ddtb_acc;
+      Pp[(size_t)18 * g.D + d] = dcb_acc;
+  #pragma unroll
+      for (int k = 0; k < WC; ++k) Pp[(size_t)(19 + k) * g.D + d] = dcw[k];
     }
-    if (!SCAN && a.d_conv_in) {
-      // conv inputs of steps -1, -2, -3 reach the conv outputs of steps
-      // 0..2 (dc1 = dc_0, dc2 = dc_1, dc3 = dc_2; zero past the sequence),
-      // and, when T < 3, the conv-state output too
-      float v[3];
-      v[2] = fmaf(dc1, w[2], fmaf(dc2, w[1], dc3 * w[0]));
-      v[1] = fmaf(dc1, w[1], dc2 * w[0]);
-      v[0] = dc1 * w[0];
-      T* dci = static_cast<T*>(a.d_conv_in) + (size_t)b * 3 * g.D + d;
-#pragma unroll
-      for (int r = 0; r < 3; ++r) {
-        const int ro = r - g.T;  // row of the conv-state output holding step r - 3
-        if (a.g_conv && ro >= 0)
-          v[r] += Act<T>::ld(static_cast<const T*>(a.g_conv) + ((size_t)b * 3 + ro) * g.D + d);
-        Act<T>::st(dci + (size_t)r * g.D, v[r]);
-      }
-    }
-  }
-  if (active) {
-    float* Pp = a.partials + ((size_t)b * g.S + s) * NPART * g.D;
-#pragma unroll
-    for (int i = 0; i < NS / 2; ++i) {
-      const int n = lane_of(i);
-      Pp[(size_t)n * g.D + d] = dAp[i].x;
-      Pp[(size_t)(n + 1) * g.D + d] = dAp[i].y;
-    }
-    Pp[(size_t)16 * g.D + d] = dD_acc;
-    Pp[(size_t)17 * g.D + d] = ddtb_acc;
-    Pp[(size_t)18 * g.D + d] = dcb_acc;
-#pragma unroll
-    for (int k = 0; k < WC; ++k) Pp[(size_t)(19 + k) * g.D + d] = dcw[k];
   }
   tmem_fence_before_sync();
   __syncthreads();
@@ -575,7 +635,7 @@ __device__ __forceinline__ float2 warp_sum8_rotated(float2 (&v)[4], int lane) {
 }
 
 template <typename T, bool ST, bool SCAN, int N>
-__global__ void __launch_bounds__(128, 4) m3_bwd2_kernel(BwdArgs a) {
+__global__ void __launch_bounds__(128, 4) m3_bwd2_kernel(const __grid_constant__ BwdArgs a) {
   constexpr int G = N / 8;     // threads per channel
   constexpr int CH = 128 / G;  // channels per block
   constexpr int NP = N + 8;    // per-channel parameter partials
@@ -604,11 +664,20 @@ __global__ void __launch_bounds__(128, 4) m3_bwd2_kernel(BwdArgs a) {
   float* dcs = reinterpret_cast<float*>(smem + L.dcs);  // [K + 3][CH]
   // state lane of register pair P
   auto lane_of = [&](int P) { return 8 * hf + 2 * (P ^ prot); };
+  // this thread's copy of B and C: its 8 lanes in register order
+  const float* fBr = fB + prot * K * N + 8 * hf;
+  const float* fCr = fC + prot * K * N + 8 * hf;
 
   // recomputed states of a chunk: row j of this thread = TMEM columns
   // [8 j, 8 j + 8) of its lane; warp 0 allocates, every exit deallocates
   __shared__ uint32_t tmem_slot;
+  __shared__ __align__(8) uint64_t tbar[2];  // tile copies into staging buffer 0 / 1
   if (warp == 0) tmem_alloc(&tmem_slot, a.tcols);
+  if (tid == 32) {
+    mbar_init(&tbar[0], 1);
+    mbar_init(&tbar[1], 1);
+    mbar_init_fence();
+  }
   tmem_fence_before_sync();
   __syncthreads();
   tmem_fence_after_sync();
@@ -641,19 +710,27 @@ __global__ void __launch_bounds__(128, 4) m3_bwd2_kernel(BwdArgs a) {
       carry[P] = make_float2(gh[(size_t)n * g.D], gh[(size_t)(n + 1) * g.D]);
     }
   }
-  const T* xg = static_cast<const T*>(a.x);
+  // A chunk's tiles arrive by tensor-map copies issued by thread 0: x with
+  // its three halo rows before the chunk, delta_raw, z, d_gated, B, C and
+  // the chunk's start state; rows outside [0, T) and channels past d_inner
+  // arrive as zeros.
+  const uint32_t tile_bytes =
+      (uint32_t)((4 * K + 3) * CH * sizeof(T) + 2 * K * N * sizeof(T) + (size_t)N * CH * 4);
+  const bool misaligned = (smem_u32(smem) & 127u) != 0;  // tile copies need 128-byte aligned buffers
   auto stage = [&](int c, int buf) {
-    unsigned char* base = smem + (size_t)buf * L.tile;
-    const int t0 = c * K;
-    stage_rows<T, CH, 128>(reinterpret_cast<T*>(base + L.x), xg, b, t0 - 3, K + 3, g.T, g.T, g.D, d0, tid);
-    stage_rows<T, CH, 128>(reinterpret_cast<T*>(base + L.dr), static_cast<const T*>(a.dr), b, t0, K, g.T, g.T, g.D, d0, tid);
-    stage_rows<T, CH, 128>(reinterpret_cast<T*>(base + L.z), static_cast<const T*>(a.z), b, t0, K, g.T, g.T, g.D, d0, tid);
-    stage_rows<T, CH, 128>(reinterpret_cast<T*>(base + L.dg), static_cast<const T*>(a.dg), b, t0, K, g.T, g.T, g.D, d0, tid);
-    stage_bc<T, 128, N>(reinterpret_cast<T*>(base + L.Bt), static_cast<const T*>(a.Bm), b, t0, K, g.T, g.T, g.ldbc, tid);
-    stage_bc<T, 128, N>(reinterpret_cast<T*>(base + L.Ct), static_cast<const T*>(a.Cm), b, t0, K, g.T, g.T, g.ldbc, tid);
-    stage_rows<float, CH, 128>(reinterpret_cast<float*>(base + L.ck), a.ckpt + ((size_t)b * g.nc + c) * N * g.D,
-                               0, 0, N, N, N, g.D, d0, tid);
-    cp_async_commit();
+    if (tid == 0 && !misaligned) {
+      unsigned char* base = smem + (size_t)buf * L.tile;
+      const int t0 = c * K;
+      fence_proxy_async();
+      mbar_expect_tx(&tbar[buf], tile_bytes);
+      tma_load_3d(base + L.x, &a.tm[TM_X], d0, t0 - 3, b, &tbar[buf]);
+      tma_load_3d(base + L.dr, &a.tm[TM_DR], d0, t0, b, &tbar[buf]);
+      tma_load_3d(base + L.z, &a.tm[TM_Z], d0, t0, b, &tbar[buf]);
+      tma_load_3d(base + L.dg, &a.tm[TM_DG], d0, t0, b, &tbar[buf]);
+      tma_load_3d(base + L.Bt, &a.tm[TM_B], 0, t0, b, &tbar[buf]);
+      tma_load_3d(base + L.Ct, &a.tm[TM_C], 0, t0, b, &tbar[buf]);
+      tma_load_4d(base + L.ck, &a.tm[TM_CK], d0, 0, c, b, &tbar[buf]);
+    }
   };
   stage(c_end - 1, 0);
   grid_dep_trigger();
@@ -669,15 +746,21 @@ __global__ void __launch_bounds__(128, 4) m3_bwd2_kernel(BwdArgs a) {
   float dcw[WC] = {0.f, 0.f, 0.f, 0.f};
   for (int i = tid; i < (K + 3) * CH; i += 128) dcs[i] = 0.f;  // ordered by the loop's first barrier
 
+  bool aborted = false;
   for (int c = c_end - 1; c >= c_begin; --c) {
-    const int buf = (c_end - 1 - c) & 1;
-    if (c - 1 >= c_begin) {
-      stage(c - 1, buf ^ 1);
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
+    const int it = c_end - 1 - c;  // buffer it & 1, its (it >> 1)-th use
+    const int buf = it & 1;
+    if (c - 1 >= c_begin) stage(c - 1, buf ^ 1);
+    const bool landed = !misaligned && mbar_wait(&tbar[buf], (it >> 1) & 1);
+    if (__syncthreads_or(!landed)) {
+      // a tile did not arrive: report it, let the copy issued above drain, leave
+      if (tid == 0) {
+        atomicOr(&g_bwd_status, 1u);
+        if (!misaligned && c - 1 >= c_begin) mbar_wait(&tbar[buf ^ 1], ((it + 1) >> 1) & 1);
+      }
+      aborted = true;
+      break;
     }
-    __syncthreads();
     const unsigned char* base = smem + (size_t)buf * L.tile;
     if (ST && a.conv_in && c * K < 3 && active && hf == 0) {
       T* xw = reinterpret_cast<T*>(smem + (size_t)buf * L.tile + L.x);
@@ -687,9 +770,16 @@ __global__ void __launch_bounds__(128, 4) m3_bwd2_kernel(BwdArgs a) {
     {
       const T* Bt = reinterpret_cast<const T*>(base + L.Bt);
       const T* Ct = reinterpret_cast<const T*>(base + L.Ct);
+      // copy r, row j: position 8 h + 2 P + e holds state lane 8 h + 2 (P ^ r) + e
       for (int i = tid; i < K * N; i += 128) {
-        fB[i] = Act<T>::ld(Bt + i);
-        fC[i] = Act<T>::ld(Ct + i);
+        const float bv = Act<T>::ld(Bt + i), cv = Act<T>::ld(Ct + i);
+        const int j = i / N, n = i % N;
+#pragma unroll
+        for (int r = 0; r < NROT; ++r) {
+          const int o = (r * K + j) * N + (n & ~7) + 2 * (((n >> 1) & 3) ^ r) + (n & 1);
+          fB[o] = bv;
+          fC[o] = cv;
+        }
       }
     }
     __syncthreads();
@@ -738,7 +828,7 @@ __global__ void __launch_bounds__(128, 4) m3_bwd2_kernel(BwdArgs a) {
         const float2 du2 = f2b(v0.y);
 #pragma unroll
         for (int P = 0; P < 4; ++P) {
-          const float2 bb = *reinterpret_cast<const float2*>(fB + j * N + lane_of(P));
+          const float2 bb = *reinterpret_cast<const float2*>(fBr + j * N + 2 * P);
           h[P] = __ffma2_rn(ex2x2(__fmul2_rn(dl2, a2[P])), h[P], __fmul2_rn(du2, bb));
         }
         tmem_st8(trow + 8u * (uint32_t)j, h);
@@ -770,8 +860,8 @@ __global__ void __launch_bounds__(128, 4) m3_bwd2_kernel(BwdArgs a) {
         }
 #pragma unroll
         for (int P = 0; P < 4; ++P) {
-          const float2 bb = *reinterpret_cast<const float2*>(fB + j * N + lane_of(P));
-          const float2 cc = *reinterpret_cast<const float2*>(fC + j * N + lane_of(P));
+          const float2 bb = *reinterpret_cast<const float2*>(fBr + j * N + 2 * P);
+          const float2 cc = *reinterpret_cast<const float2*>(fCr + j * N + 2 * P);
           y2 = __ffma2_rn(cc, hn[P], y2);
           const float2 dh = __ffma2_rn(dy2, cc, carry[P]);
           pC[P] = __fmul2_rn(dy2, hn[P]);
@@ -880,56 +970,58 @@ __global__ void __launch_bounds__(128, 4) m3_bwd2_kernel(BwdArgs a) {
     __syncthreads();
   }
 
-  if (ST && s == 0 && active) {
-    if (a.d_h_in) {
-      float* dh0 = a.d_h_in + (size_t)b * N * g.D + d;
-#pragma unroll
+  if (!aborted) {
+    if (ST && s == 0 && active) {
+      if (a.d_h_in) {
+        float* dh0 = a.d_h_in + (size_t)b * N * g.D + d;
+  #pragma unroll
+        for (int P = 0; P < 4; ++P) {
+          const int n = lane_of(P);
+          dh0[(size_t)n * g.D] = carry[P].x;
+          dh0[(size_t)(n + 1) * g.D] = carry[P].y;
+        }
+      }
+      if (!SCAN && a.d_conv_in && hf == 0) {
+        // dc of steps 0, 1, 2 (zero past the sequence), kept in rows K.. K+2
+        const float f0 = dcs[K * CH + ch], f1 = dcs[(K + 1) * CH + ch], f2 = dcs[(K + 2) * CH + ch];
+        float v[3];
+        v[2] = fmaf(f0, w[2], fmaf(f1, w[1], f2 * w[0]));
+        v[1] = fmaf(f0, w[1], f1 * w[0]);
+        v[0] = f0 * w[0];
+        T* dci = static_cast<T*>(a.d_conv_in) + (size_t)b * 3 * g.D + d;
+  #pragma unroll
+        for (int r = 0; r < 3; ++r) {
+          const int ro = r - g.T;
+          if (a.g_conv && ro >= 0)
+            v[r] += Act<T>::ld(static_cast<const T*>(a.g_conv) + ((size_t)b * 3 + ro) * g.D + d);
+          Act<T>::st(dci + (size_t)r * g.D, v[r]);
+        }
+      }
+    }
+    // the per-step partial sums: each thread of a channel summed its own steps
+  #pragma unroll
+    for (int o = 1; o < G; o <<= 1) {
+      dD_acc += __shfl_xor_sync(0xffffffffu, dD_acc, o);
+      ddtb_acc += __shfl_xor_sync(0xffffffffu, ddtb_acc, o);
+      dcb_acc += __shfl_xor_sync(0xffffffffu, dcb_acc, o);
+  #pragma unroll
+      for (int k = 0; k < WC; ++k) dcw[k] += __shfl_xor_sync(0xffffffffu, dcw[k], o);
+    }
+    if (active) {
+      float* Pp = a.partials + ((size_t)b * g.S + s) * NP * g.D;
+  #pragma unroll
       for (int P = 0; P < 4; ++P) {
         const int n = lane_of(P);
-        dh0[(size_t)n * g.D] = carry[P].x;
-        dh0[(size_t)(n + 1) * g.D] = carry[P].y;
+        Pp[(size_t)n * g.D + d] = dAp[P].x;
+        Pp[(size_t)(n + 1) * g.D + d] = dAp[P].y;
       }
-    }
-    if (!SCAN && a.d_conv_in && hf == 0) {
-      // dc of steps 0, 1, 2 (zero past the sequence), kept in rows K.. K+2
-      const float f0 = dcs[K * CH + ch], f1 = dcs[(K + 1) * CH + ch], f2 = dcs[(K + 2) * CH + ch];
-      float v[3];
-      v[2] = fmaf(f0, w[2], fmaf(f1, w[1], f2 * w[0]));
-      v[1] = fmaf(f0, w[1], f1 * w[0]);
-      v[0] = f0 * w[0];
-      T* dci = static_cast<T*>(a.d_conv_in) + (size_t)b * 3 * g.D + d;
-#pragma unroll
-      for (int r = 0; r < 3; ++r) {
-        const int ro = r - g.T;
-        if (a.g_conv && ro >= 0)
-          v[r] += Act<T>::ld(static_cast<const T*>(a.g_conv) + ((size_t)b * 3 + ro) * g.D + d);
-        Act<T>::st(dci + (size_t)r * g.D, v[r]);
+      if (hf == 0) {
+        Pp[(size_t)N * g.D + d] = dD_acc;
+        Pp[(size_t)(N + 1) * g.D + d] = ddtb_acc;
+        Pp[(size_t)(N + 2) * g.D + d] = dcb_acc;
+  #pragma unroll
+        for (int k = 0; k < WC; ++k) Pp[(size_t)(N + 3 + k) * g.D + d] = dcw[k];
       }
-    }
-  }
-  // the per-step partial sums: each thread of a channel summed its own steps
-#pragma unroll
-  for (int o = 1; o < G; o <<= 1) {
-    dD_acc += __shfl_xor_sync(0xffffffffu, dD_acc, o);
-    ddtb_acc += __shfl_xor_sync(0xffffffffu, ddtb_acc, o);
-    dcb_acc += __shfl_xor_sync(0xffffffffu, dcb_acc, o);
-#pragma unroll
-    for (int k = 0; k < WC; ++k) dcw[k] += __shfl_xor_sync(0xffffffffu, dcw[k], o);
-  }
-  if (active) {
-    float* Pp = a.partials + ((size_t)b * g.S + s) * NP * g.D;
-#pragma unroll
-    for (int P = 0; P < 4; ++P) {
-      const int n = lane_of(P);
-      Pp[(size_t)n * g.D + d] = dAp[P].x;
-      Pp[(size_t)(n + 1) * g.D + d] = dAp[P].y;
-    }
-    if (hf == 0) {
-      Pp[(size_t)N * g.D + d] = dD_acc;
-      Pp[(size_t)(N + 1) * g.D + d] = ddtb_acc;
-      Pp[(size_t)(N + 2) * g.D + d] = dcb_acc;
-#pragma unroll
-      for (int k = 0; k < WC; ++k) Pp[(size_t)(N + 3 + k) * g.D + d] = dcw[k];
     }
   }
   tmem_fence_before_sync();
@@ -1028,11 +1120,37 @@ void (*agg_for(bool split, int N))(BwdArgs) {
 }
 
 // scan: stop at du (m3scan_bwd_scan); the conv side runs in launch_conv_bwd.
+// Tensor maps of the backward's tiles (boxes of ch channels).
+template <typename T>
+bool encode_bwd_maps(const Plan& p, int ch, BwdArgs& a) {
+  const uint64_t es = sizeof(T), D = p.D, T_ = p.T, B = p.B, N = p.N, ld = p.ldbc, nc = p.nc;
+  const uint32_t K = (uint32_t)p.K, c = (uint32_t)ch, n = (uint32_t)p.N;
+  const uint64_t adim[3] = {D, T_, B}, astr[2] = {D * es, T_ * D * es};
+  const uint64_t bdim[3] = {N, T_, B}, bstr[2] = {ld * es, T_ * ld * es};
+  const uint64_t cdim[4] = {D, N, nc, B}, cstr[3] = {D * 4, N * D * 4, nc * N * D * 4};
+  const uint32_t box_x[3] = {c, K + 3, 1}, box_a[3] = {c, K, 1}, box_b[3] = {n, K, 1}, box_c[4] = {c, n, 1, 1};
+  const uint32_t box_ta[3] = {c, TT, 1}, box_tb[3] = {n, TT, 1};
+  const bool ok = encode_tile_map(&a.tm[TM_X], (int)es, 3, a.x, adim, astr, box_x) &&
+                  encode_tile_map(&a.tm[TM_DR], (int)es, 3, a.dr, adim, astr, box_a) &&
+                  encode_tile_map(&a.tm[TM_Z], (int)es, 3, a.z, adim, astr, box_a) &&
+                  encode_tile_map(&a.tm[TM_DG], (int)es, 3, a.dg, adim, astr, box_a) &&
+                  encode_tile_map(&a.tm[TM_B], (int)es, 3, a.Bm, bdim, bstr, box_b) &&
+                  encode_tile_map(&a.tm[TM_C], (int)es, 3, a.Cm, bdim, bstr, box_b) &&
+                  encode_tile_map(&a.tm[TM_CK], 4, 4, a.ckpt, cdim, cstr, box_c) &&
+                  encode_tile_map(&a.tm[TM_ADR], (int)es, 3, a.dr, adim, astr, box_ta) &&
+                  encode_tile_map(&a.tm[TM_AZ], (int)es, 3, a.z, adim, astr, box_ta) &&
+                  encode_tile_map(&a.tm[TM_ADG], (int)es, 3, a.dg, adim, astr, box_ta) &&
+                  encode_tile_map(&a.tm[TM_AC], (int)es, 3, a.Cm, bdim, bstr, box_tb);
+  if (!ok) note(cudaErrorInvalidValue);
+  return ok;
+}
+
 template <typename T>
 m3_status launch_bwd(const Plan& p, BwdArgs a, cudaStream_t st, int smem_per_sm, bool scan) {
   const int groups = (p.D + GB - 1) / GB;
   a.g = Geo{p.B, p.T, p.D, p.K, p.nc, p.Sb, p.mb, p.ldbc, p.lddbc};
   cudaError_t e = cudaSuccess;
+  if (!encode_bwd_maps<T>(p, p.bwd_tpc != 1 ? 128 / (p.N / 8) : GB, a)) return M3_ERR_CUDA;
   if (p.Sb > 1) {
     // also clears dB and dC before the main kernel's reductions into them
     const bool split = p.bwd_tpc != 1;

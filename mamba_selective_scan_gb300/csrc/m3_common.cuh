@@ -4,6 +4,7 @@
 // entry points each unit provides to the others.
 #pragma once
 
+#include <cuda.h>  // CUtensorMap (the driver function that fills one is looked up at run time)
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -146,6 +147,64 @@ __device__ __forceinline__ void grid_dep_trigger() { asm volatile("griddepcontro
 
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// ---- tile copies by the tensor memory accelerator ----
+// One thread issues cp.async.bulk.tensor copies of whole tiles into shared
+// memory; they complete on a shared-memory mbarrier whose transaction count
+// the issuing thread raised by the tiles' bytes.  Elements outside the
+// tensor (negative or too-large coordinates) arrive as zeros.
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+// makes initialised mbarriers visible to the copy engine (before a block barrier)
+__device__ __forceinline__ void mbar_init_fence() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Wait until the phase of the given parity has completed.  Gives up and
+// returns false after about one second, so a copy that never lands cannot
+// hang the GPU; the caller then reports the failure and leaves.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  const uint32_t a = smem_u32(bar);
+  uint64_t t0 = 0;
+  for (uint32_t i = 0;; ++i) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done) : "r"(a), "r"(parity) : "memory");
+    if (done) return true;
+    if (i == 0) t0 = global_ns();
+    else if (global_ns() - t0 > 1000000000ull) return false;
+  }
+}
+// orders this thread's view of earlier generic-proxy shared-memory accesses
+// (made visible to it by a block barrier) before its next tile copies
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1, int c2,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, int c0, int c1, int c2, int c3,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];"
+      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+        "r"(smem_u32(bar))
+      : "memory");
+}
+
 // Stage rows [t_first, t_first + rows) x channels [d0, d0 + G) of a
 // [B, T_, D] tensor of element type T into dst[rows][G]; rows outside
 // [0, t_limit) and channels >= D read as zero.  NT threads cooperate.
@@ -243,7 +302,13 @@ struct FwdArgs {
   const void* conv_in;
   float* h_out;
   void* conv_out;
+  // tile maps of the forward's staging (see TF_* below)
+  CUtensorMap tm[5];
 };
+// tensor maps of FwdArgs::tm: activations [B, T, D] with boxes of the
+// block's channels x TT rows (x: TT + 3 rows in the split kernels, which
+// stage the conv halo); B and C [B, T, ld] with boxes of N x TT
+enum { TF_X = 0, TF_DR, TF_Z, TF_B, TF_C };
 
 struct BwdArgs {
   Geo g;
@@ -264,7 +329,14 @@ struct BwdArgs {
   void* d_conv_in;
   int accumulate;
   uint32_t tcols;  // tensor-memory columns per CTA for the state history
+  // tile maps of the backward's staging (see TM_* below)
+  CUtensorMap tm[11];
 };
+// tensor maps of BwdArgs::tm, boxes of the block's channels (128 / threads
+// per channel): main kernels -- activations [B, T, D] x (K + 3) rows (x)
+// or K rows, B and C [B, T, ld] N x K, checkpoints [B, nc, N, D] f32
+// channels x N; aggregate kernel -- delta_raw, z, d_gated TT rows, C N x TT
+enum { TM_X = 0, TM_DR, TM_Z, TM_DG, TM_B, TM_C, TM_CK, TM_ADR, TM_AZ, TM_ADG, TM_AC };
 
 // Forward shared memory: two staging buffers {x, delta_raw, z: [TT][GF]
 // act; B, C: [TT][16] act}, B and C of the current tile as float [TT][16],
@@ -344,7 +416,11 @@ __host__ __device__ inline BwdSmem bwd_smem(int K, int es) {
 // buffers for CH channels and N-wide B and C; per-step scalars s0/s1
 // [K][CH] float4 shared by the threads of a channel; the conv-input gradient
 // of the chunk's steps and of the next chunk's first three, dcs[K+3][CH];
-// per-warp dB/dC sums red[K][4][2N].
+// per-warp dB/dC sums red[K][4][2N].  B and C of the current chunk are kept
+// as float in NROT = 4 copies whose lane pairs are permuted the way the
+// threads' state registers are (see m3_bwd2_kernel), so every thread reads
+// its copy in register order at fixed offsets.
+constexpr int NROT = 4;
 struct Bwd2Smem {
   size_t x, dr, z, dg, Bt, Ct, ck, tile, fB, fC, scal, dcs, red, total;
 };
@@ -360,8 +436,8 @@ __host__ __device__ inline Bwd2Smem bwd2_smem(int K, int es, int N) {
   s.ck = s.Ct + align_up((size_t)K * N * es, 128);
   s.tile = s.ck + (size_t)N * CH * 4;
   s.fB = 2 * s.tile;
-  s.fC = s.fB + (size_t)K * N * 4;
-  s.scal = s.fC + (size_t)K * N * 4;
+  s.fC = s.fB + (size_t)NROT * K * N * 4;
+  s.scal = s.fC + (size_t)NROT * K * N * 4;
   s.dcs = s.scal + (size_t)2 * K * CH * 16;
   s.red = s.dcs + align_up((size_t)(K + 3) * CH * 4, 128);
   s.total = s.red + (size_t)K * 4 * 2 * N * 4;
@@ -469,10 +545,13 @@ __host__ inline uint32_t tmem_cols2_for(int K) {
 }
 
 // Largest chunk whose backward fits: 16 K tensor-memory columns <= 512 and
-// the shared-memory footprint within one block's limit.
+// the shared-memory footprints of the one-thread kernel and of the split
+// kernel at its widest state (d_state 64) within one block's limit.
 __host__ inline int kmax_for(int es) {
   int k = KMAX;
-  while (k > 1 && (bwd_smem(k, es).total > SMEM_CAP || tmem_cols_for(k) > 512)) --k;
+  while (k > 1 && (bwd_smem(k, es).total > SMEM_CAP || bwd2_smem(k, es, 64).total > SMEM_CAP ||
+                   tmem_cols_for(k) > 512))
+    --k;
   return k;
 }
 
@@ -535,6 +614,16 @@ cudaError_t launch_k(void (*kern)(Args...), dim3 grid, unsigned block, size_t sm
   cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kern, vals...);
 }
+
+// Fill a tiled tensor map (host; the driver function is found at run time):
+// rank 3 or 4, dims innermost first, strides in bytes of dims 1.., box in
+// elements; es = 2 (bf16) or 4 (f32).  False if the driver refuses it.
+bool encode_tile_map(CUtensorMap* map, int es, int rank, const void* ptr, const uint64_t* dims,
+                     const uint64_t* strides, const uint32_t* box);
+// Per-unit device status word: nonzero once a kernel of that unit gave up
+// waiting for a tile copy.  take_*_status reads and clears it (synchronous).
+cudaError_t take_bwd_status(unsigned* out);
+cudaError_t take_fwd_status(unsigned* out);
 
 // Provided by m3_fwd.cu, m3_bwd.cu and m3_aux.cu for T = float and
 // __nv_bfloat16.

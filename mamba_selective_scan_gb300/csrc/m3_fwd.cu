@@ -4,6 +4,35 @@
 
 namespace m3 {
 
+// nonzero once a kernel here gave up waiting for a tile copy
+__device__ unsigned int g_fwd_status;
+
+cudaError_t take_fwd_status(unsigned* out) {
+  unsigned v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_fwd_status, sizeof(v));
+  if (e == cudaSuccess && v) {
+    const unsigned zero = 0;
+    e = cudaMemcpyToSymbol(g_fwd_status, &zero, sizeof(zero));
+  }
+  *out = v;
+  return e;
+}
+
+// Wait for the tiles of staging buffer buf (its (it >> 1)-th use).  On a
+// timeout every thread of the block learns it at the block barrier; thread
+// 0 reports it and lets the copy it issued into the other buffer (if any)
+// drain, and the caller leaves.  Returns false then.
+__device__ __forceinline__ bool fwd_tiles_landed(uint64_t* tbar, int it, bool misaligned, bool other_in_flight) {
+  const int buf = it & 1;
+  const bool landed = !misaligned && mbar_wait(&tbar[buf], (it >> 1) & 1);
+  if (!__syncthreads_or(!landed)) return true;
+  if (threadIdx.x == 0) {
+    atomicOr(&g_fwd_status, 1u);
+    if (!misaligned && other_in_flight) mbar_wait(&tbar[buf ^ 1], ((it + 1) >> 1) & 1);
+  }
+  return false;
+}
+
 // ---------------------------------------------------------------------------
 // forward: FINAL = run each segment from its true start state, write gated
 // (+y) and a checkpoint every K steps; !FINAL = local pass from zero over
@@ -12,7 +41,7 @@ namespace m3 {
 // ---------------------------------------------------------------------------
 
 template <typename T, bool FINAL>
-__global__ void __launch_bounds__(GF) m3_fwd_kernel(FwdArgs a) {
+__global__ void __launch_bounds__(GF) m3_fwd_kernel(const __grid_constant__ FwdArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   const Geo g = a.g;
   const int tid = threadIdx.x;
@@ -27,23 +56,34 @@ __global__ void __launch_bounds__(GF) m3_fwd_kernel(FwdArgs a) {
   const int t_end = min(c_end * g.K, g.T);
   const FwdSmem L = fwd_smem(sizeof(T));
   const T* xg = static_cast<const T*>(a.x);
-  const T* drg = static_cast<const T*>(a.dr);
-  const T* zg = static_cast<const T*>(a.z);
-  const T* Bg = static_cast<const T*>(a.Bm);
-  const T* Cg = static_cast<const T*>(a.Cm);
   float* fB = reinterpret_cast<float*>(smem + L.fB);
   float* fC = reinterpret_cast<float*>(smem + L.fC);
 
+  // A tile's x, delta_raw, B (and z, C) rows arrive by tensor-map copies
+  // issued by thread 0; rows past the sequence and channels past d_inner
+  // arrive as zeros (rows past the segment are never read).
+  __shared__ __align__(8) uint64_t tbar[2];  // tile copies into staging buffer 0 / 1
+  if (tid == 0) {
+    mbar_init(&tbar[0], 1);
+    mbar_init(&tbar[1], 1);
+    mbar_init_fence();
+  }
+  __syncthreads();
+  const bool misaligned = (smem_u32(smem) & 127u) != 0;  // tile copies need 128-byte aligned buffers
+  const uint32_t tile_bytes = (uint32_t)(((FINAL ? 3 : 2) * TT * GF + (FINAL ? 2 : 1) * TT * NS) * sizeof(T));
   auto stage = [&](int t0, int buf) {
-    unsigned char* base = smem + (size_t)buf * L.tile;
-    stage_rows<T, GF, GF>(reinterpret_cast<T*>(base + L.x), xg, b, t0, TT, g.T, t_end, g.D, d0, tid);
-    stage_rows<T, GF, GF>(reinterpret_cast<T*>(base + L.dr), drg, b, t0, TT, g.T, t_end, g.D, d0, tid);
-    stage_bc<T, GF>(reinterpret_cast<T*>(base + L.Bt), Bg, b, t0, TT, g.T, t_end, g.ldbc, tid);
-    if (FINAL) {
-      stage_rows<T, GF, GF>(reinterpret_cast<T*>(base + L.z), zg, b, t0, TT, g.T, t_end, g.D, d0, tid);
-      stage_bc<T, GF>(reinterpret_cast<T*>(base + L.Ct), Cg, b, t0, TT, g.T, t_end, g.ldbc, tid);
+    if (tid == 0 && !misaligned) {
+      unsigned char* base = smem + (size_t)buf * L.tile;
+      fence_proxy_async();
+      mbar_expect_tx(&tbar[buf], tile_bytes);
+      tma_load_3d(base + L.x, &a.tm[TF_X], d0, t0, b, &tbar[buf]);
+      tma_load_3d(base + L.dr, &a.tm[TF_DR], d0, t0, b, &tbar[buf]);
+      tma_load_3d(base + L.Bt, &a.tm[TF_B], 0, t0, b, &tbar[buf]);
+      if (FINAL) {
+        tma_load_3d(base + L.z, &a.tm[TF_Z], d0, t0, b, &tbar[buf]);
+        tma_load_3d(base + L.Ct, &a.tm[TF_C], 0, t0, b, &tbar[buf]);
+      }
     }
-    cp_async_commit();
   };
   stage(t_begin, 0);  // first tile in flight while the parameters and carries load
   if (!FINAL) grid_dep_trigger();
@@ -98,13 +138,8 @@ __global__ void __launch_bounds__(GF) m3_fwd_kernel(FwdArgs a) {
   int kc = 0;  // steps left until the next checkpoint
   for (int t0 = t_begin, it = 0; t0 < t_end; t0 += TT, ++it) {
     const int buf = it & 1;
-    if (t0 + TT < t_end) {
-      stage(t0 + TT, buf ^ 1);
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
-    __syncthreads();
+    if (t0 + TT < t_end) stage(t0 + TT, buf ^ 1);
+    if (!fwd_tiles_landed(tbar, it, misaligned, t0 + TT < t_end)) return;
     const unsigned char* base = smem + (size_t)buf * L.tile;
     {
       const T* Bt = reinterpret_cast<const T*>(base + L.Bt);
@@ -232,7 +267,7 @@ __global__ void __launch_bounds__(GF) m3_fwd_kernel(FwdArgs a) {
 // ---------------------------------------------------------------------------
 
 template <typename T, bool FINAL, int N>
-__global__ void __launch_bounds__(128) m3_fwd2_kernel(FwdArgs a) {
+__global__ void __launch_bounds__(128) m3_fwd2_kernel(const __grid_constant__ FwdArgs a) {
   constexpr int G = N / 8;     // threads per channel
   constexpr int CH = 128 / G;  // channels per block
   extern __shared__ __align__(128) unsigned char smem[];
@@ -254,17 +289,32 @@ __global__ void __launch_bounds__(128) m3_fwd2_kernel(FwdArgs a) {
   float* fB = reinterpret_cast<float*>(smem + L.fB);
   float* fC = reinterpret_cast<float*>(smem + L.fC);
 
-  // x is staged with the three steps before the tile (row r = step t0 - 3 + r)
+  // x arrives with the three steps before the tile (row r = step t0 - 3 + r);
+  // tiles come by tensor-map copies issued by thread 0, zeros outside the
+  // tensor (rows past the segment are never read)
+  __shared__ __align__(8) uint64_t tbar[2];  // tile copies into staging buffer 0 / 1
+  if (tid == 0) {
+    mbar_init(&tbar[0], 1);
+    mbar_init(&tbar[1], 1);
+    mbar_init_fence();
+  }
+  __syncthreads();
+  const bool misaligned = (smem_u32(smem) & 127u) != 0;  // tile copies need 128-byte aligned buffers
+  const uint32_t tile_bytes =
+      (uint32_t)((((FINAL ? 3 : 2) * TT + 3) * CH + (FINAL ? 2 : 1) * TT * N) * sizeof(T));
   auto stage = [&](int t0, int buf) {
-    unsigned char* base = smem + (size_t)buf * L.tile;
-    stage_rows<T, CH, 128>(reinterpret_cast<T*>(base + L.x), xg, b, t0 - 3, TT + 3, g.T, t_end, g.D, d0, tid);
-    stage_rows<T, CH, 128>(reinterpret_cast<T*>(base + L.dr), static_cast<const T*>(a.dr), b, t0, TT, g.T, t_end, g.D, d0, tid);
-    stage_bc<T, 128, N>(reinterpret_cast<T*>(base + L.Bt), static_cast<const T*>(a.Bm), b, t0, TT, g.T, t_end, g.ldbc, tid);
-    if (FINAL) {
-      stage_rows<T, CH, 128>(reinterpret_cast<T*>(base + L.z), static_cast<const T*>(a.z), b, t0, TT, g.T, t_end, g.D, d0, tid);
-      stage_bc<T, 128, N>(reinterpret_cast<T*>(base + L.Ct), static_cast<const T*>(a.Cm), b, t0, TT, g.T, t_end, g.ldbc, tid);
+    if (tid == 0 && !misaligned) {
+      unsigned char* base = smem + (size_t)buf * L.tile;
+      fence_proxy_async();
+      mbar_expect_tx(&tbar[buf], tile_bytes);
+      tma_load_3d(base + L.x, &a.tm[TF_X], d0, t0 - 3, b, &tbar[buf]);
+      tma_load_3d(base + L.dr, &a.tm[TF_DR], d0, t0, b, &tbar[buf]);
+      tma_load_3d(base + L.Bt, &a.tm[TF_B], 0, t0, b, &tbar[buf]);
+      if (FINAL) {
+        tma_load_3d(base + L.z, &a.tm[TF_Z], d0, t0, b, &tbar[buf]);
+        tma_load_3d(base + L.Ct, &a.tm[TF_C], 0, t0, b, &tbar[buf]);
+      }
     }
-    cp_async_commit();
   };
   stage(t_begin, 0);
   if (!FINAL) grid_dep_trigger();
@@ -304,13 +354,8 @@ __global__ void __launch_bounds__(128) m3_fwd2_kernel(FwdArgs a) {
   int kc = 0;  // steps left until the next checkpoint
   for (int t0 = t_begin, it = 0; t0 < t_end; t0 += TT, ++it) {
     const int buf = it & 1;
-    if (t0 + TT < t_end) {
-      stage(t0 + TT, buf ^ 1);
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
-    __syncthreads();
+    if (t0 + TT < t_end) stage(t0 + TT, buf ^ 1);
+    if (!fwd_tiles_landed(tbar, it, misaligned, t0 + TT < t_end)) return;
     unsigned char* base = smem + (size_t)buf * L.tile;
     if (a.conv_in && t0 < 3 && active && hf == 0) {
       // halo rows before step 0 (staged as zeros): the carried conv inputs
@@ -440,6 +485,24 @@ __global__ void __launch_bounds__(128) m3_fwd2_kernel(FwdArgs a) {
   }
 }
 
+// Tensor maps of the forward's tiles: boxes of ch channels x TT rows (x:
+// TT + halo rows) and N x TT for B and C.
+template <typename T>
+bool encode_fwd_maps(const Plan& p, int ch, int halo, FwdArgs& a) {
+  const uint64_t es = sizeof(T), D = p.D, T_ = p.T, B = p.B, N = p.N, ld = p.ldbc;
+  const uint32_t c = (uint32_t)ch, n = (uint32_t)p.N;
+  const uint64_t adim[3] = {D, T_, B}, astr[2] = {D * es, T_ * D * es};
+  const uint64_t bdim[3] = {N, T_, B}, bstr[2] = {ld * es, T_ * ld * es};
+  const uint32_t box_x[3] = {c, (uint32_t)(TT + halo), 1}, box_a[3] = {c, TT, 1}, box_b[3] = {n, TT, 1};
+  const bool ok = encode_tile_map(&a.tm[TF_X], (int)es, 3, a.x, adim, astr, box_x) &&
+                  encode_tile_map(&a.tm[TF_DR], (int)es, 3, a.dr, adim, astr, box_a) &&
+                  encode_tile_map(&a.tm[TF_Z], (int)es, 3, a.z, adim, astr, box_a) &&
+                  encode_tile_map(&a.tm[TF_B], (int)es, 3, a.Bm, bdim, bstr, box_b) &&
+                  encode_tile_map(&a.tm[TF_C], (int)es, 3, a.Cm, bdim, bstr, box_b);
+  if (!ok) note(cudaErrorInvalidValue);
+  return ok;
+}
+
 template <typename T>
 m3_status launch_fwd(const Plan& p, FwdArgs a, cudaStream_t st) {
   const int groups = (p.D + GF - 1) / GF;
@@ -450,6 +513,7 @@ m3_status launch_fwd(const Plan& p, FwdArgs a, cudaStream_t st) {
     const int ch = 128 / (p.N / 8);
     const dim3 ga((p.D + ch - 1) / ch, p.Sf - 1, p.B), gf((p.D + ch - 1) / ch, p.Sf, p.B);
     const size_t smem2 = fwd2_smem(sizeof(T), p.N).total;
+    if (!encode_fwd_maps<T>(p, ch, 3, a)) return M3_ERR_CUDA;
     void (*agg)(FwdArgs) = p.N == 16 ? m3_fwd2_kernel<T, false, 16>
                          : p.N == 32 ? m3_fwd2_kernel<T, false, 32> : m3_fwd2_kernel<T, false, 64>;
     void (*fin)(FwdArgs) = p.N == 16 ? m3_fwd2_kernel<T, true, 16>
@@ -459,6 +523,7 @@ m3_status launch_fwd(const Plan& p, FwdArgs a, cudaStream_t st) {
     if (e == cudaSuccess) e = cudaGetLastError();
     return note(e) == cudaSuccess ? M3_OK : M3_ERR_CUDA;
   }
+  if (!encode_fwd_maps<T>(p, GF, 0, a)) return M3_ERR_CUDA;
   if (p.Sf > 1) e = launch_k(m3_fwd_kernel<T, false>, dim3(groups, p.Sf - 1, p.B), GF, smem, st, false, a);
   if (e == cudaSuccess)
     e = launch_k(m3_fwd_kernel<T, true>, dim3(groups, p.Sf, p.B), GF, smem, st, p.Sf > 1, a);

@@ -11,6 +11,7 @@ the sampled channels so that the oracle's sampled sums are the exact answer.
 import numpy as np
 import pytest
 
+from mamba_selective_scan_gb300 import binding
 from mamba_selective_scan_gb300.inputs import (WORKLOADS, make_inputs,
                                                make_workload_inputs)
 from parity_util import assert_close, compare, run_gpu, run_oracle, to_device
@@ -181,3 +182,13 @@ def test_wider_states_match_oracle(batch, T, D, act, chunk, segments, N):
     gpu = run_gpu(dev, chunk=chunk, segments=segments)
     ref = run_oracle(inp)
     assert_close(compare(gpu, ref, act), f"B={batch} T={T} D={D} {act} K={chunk} S={segments} N={N}")
+
+
+def test_device_status_stays_clear():
+    """Every tile copy of the split backward lands: the library's device
+    status word reads zero after runs that use those kernels."""
+    binding.m3scan_device_status()  # clear whatever earlier tests left
+    for act, chunk, seg in (("bf16", 8, 3), ("f32", 16, 0)):
+        inp, gpu, ref = _case(2, 130, 136, act, seed=77, chunk=chunk, segments=seg, tpc=2)
+        assert_close(compare(gpu, ref, act), f"status case {act} K={chunk}")
+    assert binding.m3scan_device_status() == 0
