@@ -176,6 +176,37 @@ int choose_segments(int nc, int K, int64_t groups, int64_t cap, int waves) {
   return S;
 }
 
+// Backward segment count by wave fill: per_seg blocks per segment, W blocks
+// resident at once.  Among splits with at least two chunks per segment and
+// at most six waves of blocks, take the one whose last wave is fullest
+// (blocks / (waves * W)), less 0.01 per wave.  Measured on GB300: the
+// backward's time follows the filled fraction of its waves closely (a
+// nearly empty last wave costs as much as a full one) and grows slowly with
+// the number of segments.
+int best_bwd_segments(int nc, int K, int64_t per_seg, int64_t W) {
+  if (per_seg < 1) per_seg = 1;
+  if (W < 1) W = 1;
+  int64_t s_max = 6 * W / per_seg;
+  const int64_t two_chunks = (nc + 1) / 2;
+  if (s_max > two_chunks) s_max = two_chunks;
+  if (s_max > 65535) s_max = 65535;
+  if (s_max < 1) s_max = 1;
+  int best_S = 1;
+  double best = -1.0;
+  for (int64_t want = 1; want <= s_max; ++want) {
+    int S = 1, m = 1;
+    fix_segments(nc, K, (int)want, &S, &m);
+    const int64_t n = per_seg * S;
+    const int64_t waves = (n + W - 1) / W;
+    const double score = (double)n / (double)(waves * W) - 0.01 * (double)waves;
+    if (score > best + 1e-9) {
+      best = score;
+      best_S = S;
+    }
+  }
+  return best_S;
+}
+
 m3_status validate_dims(const m3_dims* dm, m3_dtype act) {
   if (!dm) return M3_ERR_NULL;
   if (act != M3_F32 && act != M3_BF16) return M3_ERR_UNSUPPORTED;
@@ -219,6 +250,7 @@ m3_status make_plan(const m3_dims* dm, m3_dtype act, Plan* p) {
   int want_f = 1, want_b = 1;
   int64_t wave_b = 3 * 152;  // one-thread backward blocks resident at once
   int64_t wave_f = 5 * 152;  // one-thread forward blocks resident at once
+  bool auto_split_b = false;  // backward kernel variant decided with its segments
   if (dm->segments > 0) {
     want_f = want_b = (int)dm->segments;
   } else if ((int64_t)p->B * p->T * p->D > 0) {
@@ -226,10 +258,25 @@ m3_status make_plan(const m3_dims* dm, m3_dtype act, Plan* p) {
     if (note(device_info(p->K, act == M3_BF16 ? 1 : 0, &sms, &of, &ob)) != cudaSuccess)
       return M3_ERR_CUDA;
     want_f = choose_segments(p->nc, p->K, (int64_t)p->B * groups_f, (int64_t)sms * of, 2);
-    want_b = choose_segments(p->nc, p->K, (int64_t)p->B * groups_b, (int64_t)sms * ob, 8);
     wave_b = (int64_t)sms * 3;  // three resident one-thread blocks per SM (measured; the
                                 // occupancy query reports fewer)
     wave_f = (int64_t)sms * of;
+    // backward: the one-thread kernels (three blocks per SM) unless even
+    // their best split leaves the GPU less than one wave, then the split
+    // kernels (four blocks per SM, 128 / (d_state / 8) channels per block)
+    const int tpc = (int)dm->threads_per_channel;
+    bool split = p->N != NS || tpc == 2;
+    if (!split) {
+      want_b = best_bwd_segments(p->nc, p->K, (int64_t)p->B * groups_b, wave_b);
+      int Sb1 = 1, mb1 = 1;
+      fix_segments(p->nc, p->K, want_b, &Sb1, &mb1);
+      split = tpc == 0 && (int64_t)p->B * groups_b * Sb1 <= wave_b;
+      auto_split_b = split;
+    }
+    if (split) {
+      const int ch = 128 / (p->N / 8);
+      want_b = best_bwd_segments(p->nc, p->K, (int64_t)p->B * ((p->D + ch - 1) / ch), (int64_t)sms * 4);
+    }
   }
   if (p->nc == 0) {
     p->Sf = p->Sb = 1;
@@ -283,7 +330,8 @@ m3_status make_plan(const m3_dims* dm, m3_dtype act, Plan* p) {
   // d_state / 8 threads per channel
   p->fwd_tpc = p->bwd_tpc = dm->threads_per_channel;
   if (p->fwd_tpc == 0) p->fwd_tpc = (int64_t)p->B * groups_f * p->Sf <= wave_f ? 2 : 1;
-  if (p->bwd_tpc == 0) p->bwd_tpc = (int64_t)p->B * groups_b * p->Sb <= wave_b ? 2 : 1;
+  if (p->bwd_tpc == 0)
+    p->bwd_tpc = (auto_split_b || (dm->segments > 0 && (int64_t)p->B * groups_b * p->Sb <= wave_b)) ? 2 : 1;
   if (p->N != NS) p->fwd_tpc = p->bwd_tpc = 2;
   if (p->fwd_tpc == 2) p->fwd_tpc = p->N / 8;
   if (p->bwd_tpc == 2) p->bwd_tpc = p->N / 8;
