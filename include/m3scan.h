@@ -384,6 +384,12 @@ int32_t m3scan_version(void);
  * work.  Returns M3_ERR_NULL for a NULL out, M3_ERR_CUDA if reading fails. */
 m3_status m3scan_device_status(int32_t* out);
 
+/* Diagnostic of the bounded waits: enqueues one block on `stream` that waits
+ * for a tile copy it never issues.  The wait gives up after about a second
+ * and the block sets the device status word, so m3scan_device_status then
+ * reports nonzero (and clears it).  Nothing else is touched. */
+m3_status m3scan_selftest_wait_timeout(m3_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -30,7 +30,7 @@ STATUS = {
 # every symbol include/m3scan.h declares
 EXPORTS = ("m3scan_plan", "m3scan_fwd", "m3scan_bwd", "m3scan_fwd_state", "m3scan_bwd_state",
            "m3scan_bwd_scan", "m3scan_conv_bwd", "m3scan_decode", "m3scan_bwd_noalloc", "m3scan_status_string", "m3scan_last_cuda_error",
-           "m3scan_version", "m3scan_device_status")
+           "m3scan_version", "m3scan_device_status", "m3scan_selftest_wait_timeout")
 
 # size of the library's own scratch array used by m3scan_bwd_noalloc
 NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -146,6 +146,8 @@ def _lib_handle(build_if_missing: bool = True):
             lib.m3scan_version.argtypes = []
             lib.m3scan_device_status.restype = ctypes.c_int
             lib.m3scan_device_status.argtypes = [ctypes.POINTER(ctypes.c_int32)]
+            lib.m3scan_selftest_wait_timeout.restype = ctypes.c_int
+            lib.m3scan_selftest_wait_timeout.argtypes = [ctypes.c_void_p]
             _LIB = lib
     return _LIB
 
@@ -177,6 +179,13 @@ def m3scan_status_string(status: int) -> str:
 
 def m3scan_version() -> int:
     return int(_lib_handle().m3scan_version())
+
+
+def m3scan_selftest_wait_timeout(stream: int = 0) -> None:
+    """Enqueue the diagnostic block whose tile wait never completes."""
+    st = _lib_handle().m3scan_selftest_wait_timeout(ctypes.c_void_p(stream))
+    if st != 0:
+        raise M3Error(st, "m3scan_selftest_wait_timeout")
 
 
 def m3scan_device_status() -> int:

@@ -370,6 +370,11 @@ const char* m3scan_status_string(m3_status s) {
 
 int32_t m3scan_version(void) { return 100; }
 
+m3_status m3scan_selftest_wait_timeout(m3_stream_t stream) {
+  if (note(launch_wait_timeout(reinterpret_cast<cudaStream_t>(stream))) != cudaSuccess) return M3_ERR_CUDA;
+  return M3_OK;
+}
+
 m3_status m3scan_device_status(int32_t* out) {
   if (!out) return M3_ERR_NULL;
   unsigned vf = 0, vb = 0;

@@ -18,6 +18,26 @@ cudaError_t take_bwd_status(unsigned* out) {
   return e;
 }
 
+// Diagnostic: one block raises an mbarrier's transaction count but issues no
+// copy, so the phase never completes; the bounded wait must give up and the
+// failure must reach the status word, as in the scan kernels.
+__global__ void m3_wait_timeout_kernel() {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    mbar_init_fence();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_expect_tx(&bar, 16);
+  const bool landed = mbar_wait(&bar, 0);
+  if (__syncthreads_or(!landed) && threadIdx.x == 0) atomicOr(&g_bwd_status, 1u);
+}
+
+cudaError_t launch_wait_timeout(cudaStream_t st) {
+  m3_wait_timeout_kernel<<<1, 32, 0, st>>>();
+  return cudaGetLastError();
+}
+
 // ---------------------------------------------------------------------------
 // backward aggregate (segments 1..S-1): the adjoint carry a segment passes to
 // its predecessor when nothing enters it from the right,

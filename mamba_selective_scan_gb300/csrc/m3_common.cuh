@@ -623,6 +623,8 @@ bool encode_tile_map(CUtensorMap* map, int es, int rank, const void* ptr, const 
 // Per-unit device status word: nonzero once a kernel of that unit gave up
 // waiting for a tile copy.  take_*_status reads and clears it (synchronous).
 cudaError_t take_bwd_status(unsigned* out);
+// one block whose tile wait never completes (diagnostic of the bounded waits)
+cudaError_t launch_wait_timeout(cudaStream_t st);
 cudaError_t take_fwd_status(unsigned* out);
 
 // Provided by m3_fwd.cu, m3_bwd.cu and m3_aux.cu for T = float and

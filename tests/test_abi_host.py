@@ -326,3 +326,7 @@ def test_wider_states_resolve_to_the_split_kernels(lib):
         assert lib.m3scan_plan(ctypes.byref(d), binding.M3_BF16, ctypes.byref(out)) == 0
         assert (out.fwd_threads_per_channel, out.bwd_threads_per_channel) == (tpc, tpc)
         assert out.ckpt_bytes == 2 * 32 * n * 512 * 4
+
+
+def test_device_status_rejects_null(lib):
+    assert lib.m3scan_device_status(None) == 1  # M3_ERR_NULL

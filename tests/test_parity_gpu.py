@@ -192,3 +192,19 @@ def test_device_status_stays_clear():
         inp, gpu, ref = _case(2, 130, 136, act, seed=77, chunk=chunk, segments=seg, tpc=2)
         assert_close(compare(gpu, ref, act), f"status case {act} K={chunk}")
     assert binding.m3scan_device_status() == 0
+
+
+def test_bounded_tile_wait_gives_up_and_reports():
+    """A block whose tile copy never lands gives up after about a second,
+    the failure reaches the device status word, reading clears it, and the
+    context stays usable for a normal call afterwards."""
+    import time
+    binding.m3scan_device_status()
+    t0 = time.time()
+    binding.m3scan_selftest_wait_timeout(0)
+    assert binding.m3scan_device_status() != 0
+    assert time.time() - t0 < 30
+    assert binding.m3scan_device_status() == 0
+    inp, gpu, ref = _case(1, 40, 24, "f32", seed=5, chunk=8, segments=2, tpc=2)
+    assert_close(compare(gpu, ref, "f32"), "after the timeout diagnostic")
+    assert binding.m3scan_device_status() == 0
