@@ -685,8 +685,8 @@ __global__ void __launch_bounds__(128, 4) m3_bwd2_kernel(const __grid_constant__
   // state lane of register pair P
   auto lane_of = [&](int P) { return 8 * hf + 2 * (P ^ prot); };
   // this thread's copy of B and C: its 8 lanes in register order
-  const float* fBr = fB + prot * K * N + 8 * hf;
-  const float* fCr = fC + prot * K * N + 8 * hf;
+  const float* fBr = fB + prot * rot_stride(K, N) + 8 * hf;
+  const float* fCr = fC + prot * rot_stride(K, N) + 8 * hf;
 
   // recomputed states of a chunk: row j of this thread = TMEM columns
   // [8 j, 8 j + 8) of its lane; warp 0 allocates, every exit deallocates
@@ -796,7 +796,7 @@ __global__ void __launch_bounds__(128, 4) m3_bwd2_kernel(const __grid_constant__
         const int j = i / N, n = i % N;
 #pragma unroll
         for (int r = 0; r < NROT; ++r) {
-          const int o = (r * K + j) * N + (n & ~7) + 2 * (((n >> 1) & 3) ^ r) + (n & 1);
+          const int o = r * rot_stride(K, N) + j * N + (n & ~7) + 2 * (((n >> 1) & 3) ^ r) + (n & 1);
           fB[o] = bv;
           fC[o] = cv;
         }

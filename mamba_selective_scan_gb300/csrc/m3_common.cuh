@@ -391,6 +391,14 @@ __host__ __device__ inline Fwd2Smem fwd2_smem(int es, int N) {
 // (delta, delta*u, dy, dz factor -> sum_n A dh exp(delta A) h_{t-1}) and
 // s1[K][GB] = (D*u -> sum_n dh B, sigmoid(delta_raw + dt_bias), sigmoid(c),
 // c); per-warp dB/dC sums red[K][NWB][32].
+// The split backward keeps B and C of a chunk as float in NROT = 4 copies
+// whose lane pairs are permuted the way the threads' state registers are
+// (see m3_bwd2_kernel), so every thread reads its copy in register order at
+// fixed offsets.  Copy r starts r * rot_stride(K, N) floats in: 16 bytes
+// past a multiple of 128, so the copies that a warp's threads read at the
+// same offset fall in different banks.
+constexpr int NROT = 4;
+__host__ __device__ inline int rot_stride(int K, int N) { return K * N + 4; }
 struct BwdSmem {
   size_t x, dr, z, dg, Bt, Ct, ck, tile, fB, fC, scal, red, total;
 };
@@ -416,11 +424,7 @@ __host__ __device__ inline BwdSmem bwd_smem(int K, int es) {
 // buffers for CH channels and N-wide B and C; per-step scalars s0/s1
 // [K][CH] float4 shared by the threads of a channel; the conv-input gradient
 // of the chunk's steps and of the next chunk's first three, dcs[K+3][CH];
-// per-warp dB/dC sums red[K][4][2N].  B and C of the current chunk are kept
-// as float in NROT = 4 copies whose lane pairs are permuted the way the
-// threads' state registers are (see m3_bwd2_kernel), so every thread reads
-// its copy in register order at fixed offsets.
-constexpr int NROT = 4;
+// per-warp dB/dC sums red[K][4][2N].
 struct Bwd2Smem {
   size_t x, dr, z, dg, Bt, Ct, ck, tile, fB, fC, scal, dcs, red, total;
 };
@@ -436,8 +440,8 @@ __host__ __device__ inline Bwd2Smem bwd2_smem(int K, int es, int N) {
   s.ck = s.Ct + align_up((size_t)K * N * es, 128);
   s.tile = s.ck + (size_t)N * CH * 4;
   s.fB = 2 * s.tile;
-  s.fC = s.fB + (size_t)NROT * K * N * 4;
-  s.scal = s.fC + (size_t)NROT * K * N * 4;
+  s.fC = s.fB + (size_t)NROT * rot_stride(K, N) * 4;
+  s.scal = s.fC + (size_t)NROT * rot_stride(K, N) * 4;
   s.dcs = s.scal + (size_t)2 * K * CH * 16;
   s.red = s.dcs + align_up((size_t)(K + 3) * CH * 4, 128);
   s.total = s.red + (size_t)K * 4 * 2 * N * 4;
