@@ -377,10 +377,11 @@ m3_status m3scan_selftest_wait_timeout(m3_stream_t stream) {
 
 m3_status m3scan_device_status(int32_t* out) {
   if (!out) return M3_ERR_NULL;
-  unsigned vf = 0, vb = 0;
-  if (note(take_fwd_status(&vf)) != cudaSuccess || note(take_bwd_status(&vb)) != cudaSuccess)
+  unsigned vf = 0, vb = 0, va = 0;
+  if (note(take_fwd_status(&vf)) != cudaSuccess || note(take_bwd_status(&vb)) != cudaSuccess ||
+      note(take_aux_status(&va)) != cudaSuccess)
     return M3_ERR_CUDA;
-  *out = (int32_t)(vf | vb);
+  *out = (int32_t)(vf | vb | va);
   return M3_OK;
 }
 

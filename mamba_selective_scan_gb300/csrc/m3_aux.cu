@@ -4,8 +4,22 @@
 
 namespace m3 {
 
+// nonzero once a kernel here gave up waiting for a tile copy
+__device__ unsigned int g_aux_status;
+
+cudaError_t take_aux_status(unsigned* out) {
+  unsigned v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_aux_status, sizeof(v));
+  if (e == cudaSuccess && v) {
+    const unsigned zero = 0;
+    e = cudaMemcpyToSymbol(g_aux_status, &zero, sizeof(zero));
+  }
+  *out = v;
+  return e;
+}
+
 template <typename T>
-__global__ void __launch_bounds__(128) m3_conv_bwd_kernel(ConvArgs a) {
+__global__ void __launch_bounds__(128) m3_conv_bwd_kernel(const __grid_constant__ ConvArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   const int tid = threadIdx.x;
   const int d0 = blockIdx.x * 128;
@@ -18,11 +32,22 @@ __global__ void __launch_bounds__(128) m3_conv_bwd_kernel(ConvArgs a) {
   T* xs = reinterpret_cast<T*>(smem + L.x);    // row r: step t0 - 3 + r
   T* us = reinterpret_cast<T*>(smem + L.du);   // row r: step t0 + r
   T* es = reinterpret_cast<T*>(smem + L.de);
-  stage_rows<T, 128, 128>(xs, static_cast<const T*>(a.x), b, t0 - 3, CT + 6, a.T, a.T, a.D, d0, tid);
-  stage_rows<T, 128, 128>(us, static_cast<const T*>(a.du), b, t0, CT + 3, a.T, a.T, a.D, d0, tid);
-  if (a.du_extra)
-    stage_rows<T, 128, 128>(es, static_cast<const T*>(a.du_extra), b, t0, CT + 3, a.T, a.T, a.D, d0, tid);
-  cp_async_commit();
+  // the tile's rows arrive by tensor-map copies issued by thread 0 (zeros
+  // outside [0, T) and past d_inner)
+  __shared__ __align__(8) uint64_t tbar;
+  const bool misaligned = (smem_u32(smem) & 127u) != 0;  // tile copies need 128-byte aligned buffers
+  if (tid == 0) {
+    mbar_init(&tbar, 1);
+    mbar_init_fence();
+  }
+  __syncthreads();
+  if (tid == 0 && !misaligned) {
+    const uint32_t bytes = (uint32_t)(((CT + 6) + (a.du_extra ? 2 : 1) * (CT + 3)) * 128 * sizeof(T));
+    mbar_expect_tx(&tbar, bytes);
+    tma_load_3d(xs, &a.tm[0], d0, t0 - 3, b, &tbar);
+    tma_load_3d(us, &a.tm[1], d0, t0, b, &tbar);
+    if (a.du_extra) tma_load_3d(es, &a.tm[2], d0, t0, b, &tbar);
+  }
   const bool active = d < a.D;
   float w[WC] = {0.f, 0.f, 0.f, 0.f};
   float cb = 0.f;
@@ -31,8 +56,11 @@ __global__ void __launch_bounds__(128) m3_conv_bwd_kernel(ConvArgs a) {
     for (int k = 0; k < WC; ++k) w[k] = a.conv_w[(size_t)d * WC + k];
     cb = a.conv_b[d];
   }
-  cp_async_wait<0>();
-  __syncthreads();
+  const bool landed = !misaligned && mbar_wait(&tbar, 0);
+  if (__syncthreads_or(!landed)) {
+    if (tid == 0) atomicOr(&g_aux_status, 1u);
+    return;
+  }
   if (!active) return;  // no barriers below
   if (a.conv_in && t0 < 3) {
     // halo rows before step 0 (staged as zeros): the carried conv inputs
@@ -99,7 +127,7 @@ __global__ void __launch_bounds__(128) m3_conv_bwd_kernel(ConvArgs a) {
 
 // d_conv_b and d_conv_w from the per-(batch, tile) partials, summed in a
 // fixed order (32 outputs per block, rows split over 8 warps).
-__global__ void m3_conv_fin_kernel(ConvArgs a) {
+__global__ void m3_conv_fin_kernel(const __grid_constant__ ConvArgs a) {
   grid_dep_wait();  // the conv backward's partials
   __shared__ float part[8][33];
   const int cx = threadIdx.x & 31, ry = threadIdx.x >> 5;
@@ -309,7 +337,14 @@ cudaError_t launch_decode_n(int n, const DecArgs& a, cudaStream_t st, int sms) {
 }
 
 template <typename T>
-cudaError_t launch_conv_bwd(const ConvArgs& a, dim3 grid, cudaStream_t s) {
+cudaError_t launch_conv_bwd(ConvArgs a, dim3 grid, cudaStream_t s) {
+  const uint64_t es = sizeof(T), D = a.D, T_ = a.T, B = a.B;
+  const uint64_t dim[3] = {D, T_, B}, str[2] = {D * es, T_ * D * es};
+  const uint32_t box_x[3] = {128, CT + 6, 1}, box_u[3] = {128, CT + 3, 1};
+  if (!encode_tile_map(&a.tm[0], (int)es, 3, a.x, dim, str, box_x) ||
+      !encode_tile_map(&a.tm[1], (int)es, 3, a.du, dim, str, box_u) ||
+      (a.du_extra && !encode_tile_map(&a.tm[2], (int)es, 3, a.du_extra, dim, str, box_u)))
+    return cudaErrorInvalidValue;
   cudaError_t e = launch_k(m3_conv_bwd_kernel<T>, grid, 128, conv_smem(sizeof(T)).total, s, false, a);
   if (e == cudaSuccess)
     e = launch_k(m3_conv_fin_kernel, dim3((unsigned)((5 * (size_t)a.D + 31) / 32)), 256, 0, s, true, a);
@@ -326,8 +361,8 @@ cudaError_t set_aux_attrs() {
   return e;
 }
 
-template cudaError_t launch_conv_bwd<float>(const ConvArgs&, dim3, cudaStream_t);
-template cudaError_t launch_conv_bwd<__nv_bfloat16>(const ConvArgs&, dim3, cudaStream_t);
+template cudaError_t launch_conv_bwd<float>(ConvArgs, dim3, cudaStream_t);
+template cudaError_t launch_conv_bwd<__nv_bfloat16>(ConvArgs, dim3, cudaStream_t);
 template cudaError_t launch_decode_n<float>(int, const DecArgs&, cudaStream_t, int);
 template cudaError_t launch_decode_n<__nv_bfloat16>(int, const DecArgs&, cudaStream_t, int);
 template cudaError_t set_aux_attrs<float>();

@@ -487,10 +487,13 @@ struct ConvArgs {
   void* d_conv_in;                // [B, 3, D] act, nullable
   float *d_conv_w, *d_conv_b;
   int accumulate;
+  // tile maps: x [B, T, D] with boxes of 128 channels x (CT + 6) rows, du
+  // and du_extra with 128 x (CT + 3)
+  CUtensorMap tm[3];
 };
 
 // Steps per conv-backward tile: rows [t0 - 3, t0 + CT + 3) of x and
-// [t0, t0 + CT + 3) of du and du_extra are staged in shared memory by 16-byte
+// [t0, t0 + CT + 3) of du and du_extra arrive in shared memory by tensor-map
 // copies, so each thread's walk over the tile reads no global memory.
 constexpr int CT = 32;
 struct ConvSmem {
@@ -630,13 +633,14 @@ cudaError_t take_bwd_status(unsigned* out);
 // one block whose tile wait never completes (diagnostic of the bounded waits)
 cudaError_t launch_wait_timeout(cudaStream_t st);
 cudaError_t take_fwd_status(unsigned* out);
+cudaError_t take_aux_status(unsigned* out);
 
 // Provided by m3_fwd.cu, m3_bwd.cu and m3_aux.cu for T = float and
 // __nv_bfloat16.
 template <typename T> m3_status launch_fwd(const Plan& p, FwdArgs a, cudaStream_t st);
 template <typename T>
 m3_status launch_bwd(const Plan& p, BwdArgs a, cudaStream_t st, int smem_per_sm, bool scan);
-template <typename T> cudaError_t launch_conv_bwd(const ConvArgs& a, dim3 grid, cudaStream_t st);
+template <typename T> cudaError_t launch_conv_bwd(ConvArgs a, dim3 grid, cudaStream_t st);
 template <typename T> cudaError_t launch_decode_n(int n, const DecArgs& a, cudaStream_t st, int sms);
 // kernel attributes (once per device) and occupancy of the one-thread kernels
 template <typename T> cudaError_t set_fwd_attrs();
