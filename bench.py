@@ -178,6 +178,27 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------
+# replicas: combining ranks
+# ---------------------------------------------------------------------------
+
+def max_over_ranks(dist, x, device=None):
+    """The largest of a per-rank float over all ranks (x itself without a
+    process group): the job is as slow as its slowest replica."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gelem_s(world, elems_per_rank_step, steps, total_ms):
+    """Whole-job throughput: the elements every rank processed over the
+    slowest rank's time."""
+    return world * elems_per_rank_step * steps / (total_ms * 1e-3) / 1e9
+
+
+# ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
 
@@ -370,13 +391,9 @@ def gpu_arm(args):
         dist.barrier()
     clocks = sampler.stop()
 
-    total_ms = sum(f_ms) + sum(b_ms)
-    if dist is not None:
-        tt = torch.tensor([total_ms], device=device, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(dist, sum(f_ms) + sum(b_ms), device)
     E = w.elems
-    value = world * E * args.steps / (total_ms * 1e-3) / 1e9
+    value = job_gelem_s(world, E, args.steps, total_ms)
     fwd_avg = sum(f_ms) / len(f_ms)
     bwd_avg = sum(b_ms) / len(b_ms)
     fb, bb = algorithmic_bytes(w.batch, w.seq_len, w.d_inner, es)
@@ -403,9 +420,12 @@ def gpu_arm(args):
            "bwd_gelem_s": round(E / (bwd_avg * 1e-3) / 1e9, 2)}
 
     # end to end through the public binding with pinned host buffers
-    e2e = None
-    if rank == 0 or world > 1:
-        e2e = e2e_measure(torch, binding, layer, tensors, min(args.steps, 50), device)
+    e2e = e2e_measure(torch, binding, layer, tensors, min(args.steps, 50), device)
+    if dist is not None:  # whole-job figures: every replica's elements over the slowest time
+        for part in (e2e, e2e["serial"], e2e["eager"]):
+            ms = max_over_ranks(dist, part["ms_per_step"], device)
+            part["ms_per_step"] = round(ms, 5)
+            part["value"] = round(job_gelem_s(world, E, 1, ms), 3)
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
