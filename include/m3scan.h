@@ -102,6 +102,15 @@ typedef struct {
        columns of each row are read or written. */
     int64_t bc_stride;
     int64_t dbc_stride;
+    /* dB and dC are sums over all channels.  0: each block of channels adds
+       its share with float atomics (fastest; the order of the additions,
+       and so the last bits, may differ between runs).  1: each block writes
+       its share to the workspace and the backward's last kernel adds the
+       blocks in a fixed order, so repeated calls give identical bits (every
+       other output is deterministic either way).  The workspace then also
+       holds batch * seq_len * 2 * d_state floats per channel block. */
+    int32_t deterministic_dbc;
+    int32_t reserved0;  /* must be 0 */
 } m3_dims;
 
 typedef struct {
@@ -113,7 +122,7 @@ typedef struct {
     int64_t workspace_bytes;    /* size of the workspace both calls need */
     int32_t fwd_launches;       /* kernels one m3scan_fwd enqueues */
     int32_t bwd_launches;       /* kernels one m3scan_bwd enqueues (memsets excluded) */
-    int32_t fwd_threads_per_channel;  /* 1 or 2, as resolved */
+    int32_t fwd_threads_per_channel;  /* 1, or d_state / 8 for the split kernels */
     int32_t bwd_threads_per_channel;
 } m3_plan;
 

@@ -231,6 +231,8 @@ m3_status validate_dims(const m3_dims* dm, m3_dtype act) {
   if (dm->dbc_stride != 0 && dm->dbc_stride < dm->d_state) return M3_ERR_DIMS;
   if (dm->bc_stride * (act == M3_BF16 ? 2 : 4) % 16 != 0) return M3_ERR_ALIGN;
   if (dm->threads_per_channel < 0 || dm->threads_per_channel > 2) return M3_ERR_UNSUPPORTED;
+  if (dm->deterministic_dbc != 0 && dm->deterministic_dbc != 1) return M3_ERR_DIMS;
+  if (dm->reserved0 != 0) return M3_ERR_DIMS;
   return M3_OK;
 }
 
@@ -285,6 +287,19 @@ m3_status make_plan(const m3_dims* dm, m3_dtype act, Plan* p) {
     fix_segments(p->nc, p->K, want_f, &p->Sf, &p->mf);
     fix_segments(p->nc, p->K, want_b, &p->Sb, &p->mb);
   }
+  const bool empty = (size_t)p->B * p->T * p->D == 0;
+  // d_state 16: the split kernels (two threads per channel) when the
+  // one-thread grid fills less than one wave (three backward, five forward
+  // blocks per SM on a 152-SM GPU, or the device's figures when the
+  // segments were chosen for it); wider states: always the split kernels,
+  // d_state / 8 threads per channel
+  p->fwd_tpc = p->bwd_tpc = dm->threads_per_channel;
+  if (p->fwd_tpc == 0) p->fwd_tpc = (int64_t)p->B * groups_f * p->Sf <= wave_f ? 2 : 1;
+  if (p->bwd_tpc == 0)
+    p->bwd_tpc = (auto_split_b || (dm->segments > 0 && (int64_t)p->B * groups_b * p->Sb <= wave_b)) ? 2 : 1;
+  if (p->N != NS) p->fwd_tpc = p->bwd_tpc = 2;
+  if (p->fwd_tpc == 2) p->fwd_tpc = p->N / 8;
+  if (p->bwd_tpc == 2) p->bwd_tpc = p->N / 8;
   const size_t B = p->B, D = p->D;
   const size_t N = p->N;
   p->ckpt_bytes = B * p->nc * N * D * 4;
@@ -312,6 +327,11 @@ m3_status make_plan(const m3_dims* dm, m3_dtype act, Plan* p) {
     p->b_dxpart = take(B * p->Sb * 3 * D * 4);
     p->b_dchead = take(B * p->Sb * 3 * D * 4);
   }
+  // deterministic dB/dC: one partial row of 2N floats per (batch, step,
+  // channel block of the backward's main kernel)
+  p->det = dm->deterministic_dbc != 0;
+  p->dblk = (p->D + (p->bwd_tpc != 1 ? 128 / p->bwd_tpc : GB) - 1) / (p->bwd_tpc != 1 ? 128 / p->bwd_tpc : GB);
+  p->b_dbc = p->det ? take(B * (size_t)p->T * p->dblk * 2 * N * 4) : 0;
   size_t bwd_total = off;
   // conv backward of the two-phase backward (its own call): CT-step tiles
   p->ctile = CT;
@@ -322,19 +342,6 @@ m3_status make_plan(const m3_dims* dm, m3_dtype act, Plan* p) {
   if (conv_total > bwd_total) bwd_total = conv_total;
   p->ws_bytes = fwd_total > bwd_total ? fwd_total : bwd_total;
   if (p->ws_bytes < 256) p->ws_bytes = 256;
-  const bool empty = (size_t)p->B * p->T * p->D == 0;
-  // d_state 16: the split kernels (two threads per channel) when the
-  // one-thread grid fills less than one wave (three backward, five forward
-  // blocks per SM on a 152-SM GPU, or the device's figures when the
-  // segments were chosen for it); wider states: always the split kernels,
-  // d_state / 8 threads per channel
-  p->fwd_tpc = p->bwd_tpc = dm->threads_per_channel;
-  if (p->fwd_tpc == 0) p->fwd_tpc = (int64_t)p->B * groups_f * p->Sf <= wave_f ? 2 : 1;
-  if (p->bwd_tpc == 0)
-    p->bwd_tpc = (auto_split_b || (dm->segments > 0 && (int64_t)p->B * groups_b * p->Sb <= wave_b)) ? 2 : 1;
-  if (p->N != NS) p->fwd_tpc = p->bwd_tpc = 2;
-  if (p->fwd_tpc == 2) p->fwd_tpc = p->N / 8;
-  if (p->bwd_tpc == 2) p->bwd_tpc = p->N / 8;
   p->fwd_launches = empty ? 0 : (p->Sf > 1 ? 2 : 1);
   p->bwd_launches = empty ? 0 : (p->Sb > 1 ? 3 : 2);
   return M3_OK;
@@ -537,6 +544,8 @@ m3_status bwd_impl(const m3_dims* dims, m3_dtype act, const void* x, const void*
   a.dB = dB; a.dC = dC;
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   a.partials = reinterpret_cast<float*>(ws + p.b_part);
+  a.dbc_part = p.det ? reinterpret_cast<float*>(ws + p.b_dbc) : nullptr;
+  a.nblk = p.dblk;
   if (p.Sb > 1) {
     a.q = reinterpret_cast<float*>(ws + p.b_q);
     a.sd = reinterpret_cast<float*>(ws + p.b_sd);

@@ -109,7 +109,7 @@ __global__ void __launch_bounds__(GB) m3_bwd_agg_kernel(const __grid_constant__ 
   for (int i = 0; i < NL / 2; ++i) carry[i] = make_float2(0.f, 0.f);
   float sdelta = 0.f;
 
-  {
+  if (!a.dbc_part) {
     // dB and dC are sums over channel groups (global reductions in the main
     // kernel): this kernel runs before it, so it clears them.
     const size_t ncta = (size_t)gridDim.x * gridDim.y * gridDim.z;
@@ -556,13 +556,23 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(const __grid_constant__ B
 
     __syncthreads();
     // one global reduction per (t, n) per block for dB and dC
-    for (int i = tid; i < steps * 32; i += GB) {
-      const int j = i >> 5, l = i & 31;
-      float v = 0.f;
+    if (a.dbc_part) {  // this block's share, summed in a fixed order by the tail kernel
+      for (int i = tid; i < steps * 32; i += GB) {
+        const int j = i >> 5, l = i & 31;
+        float v = 0.f;
 #pragma unroll
-      for (int ww = 0; ww < NWB; ++ww) v += red[(j * NWB + ww) * 32 + l];
-      float* dst = (l < NS ? a.dB : a.dC) + ((size_t)b * g.T + c * K + j) * g.lddbc + (l & (NS - 1));
-      atomicAdd(dst, v);
+        for (int ww = 0; ww < NWB; ++ww) v += red[(j * NWB + ww) * 32 + l];
+        a.dbc_part[(((size_t)b * g.T + c * K + j) * a.nblk + blockIdx.x) * 32 + l] = v;
+      }
+    } else {
+      for (int i = tid; i < steps * 32; i += GB) {
+        const int j = i >> 5, l = i & 31;
+        float v = 0.f;
+#pragma unroll
+        for (int ww = 0; ww < NWB; ++ww) v += red[(j * NWB + ww) * 32 + l];
+        float* dst = (l < NS ? a.dB : a.dC) + ((size_t)b * g.T + c * K + j) * g.lddbc + (l & (NS - 1));
+        atomicAdd(dst, v);
+      }
     }
     __syncthreads();
   }
@@ -979,13 +989,23 @@ __global__ void __launch_bounds__(128, 4) m3_bwd2_kernel(const __grid_constant__
     }
 
     __syncthreads();
-    for (int i = tid; i < steps * 2 * N; i += 128) {
-      const int j = i / (2 * N), l = i % (2 * N);
-      float v = 0.f;
+    if (a.dbc_part) {  // this block's share, summed in a fixed order by the tail kernel
+      for (int i = tid; i < steps * 2 * N; i += 128) {
+        const int j = i / (2 * N), l = i % (2 * N);
+        float v = 0.f;
 #pragma unroll
-      for (int ww = 0; ww < 4; ++ww) v += red[(j * 4 + ww) * 2 * N + l];
-      float* dst = (l < N ? a.dB : a.dC) + ((size_t)b * g.T + c * K + j) * g.lddbc + (l & (N - 1));
-      atomicAdd(dst, v);
+        for (int ww = 0; ww < 4; ++ww) v += red[(j * 4 + ww) * 2 * N + l];
+        a.dbc_part[(((size_t)b * g.T + c * K + j) * a.nblk + blockIdx.x) * 2 * N + l] = v;
+      }
+    } else {
+      for (int i = tid; i < steps * 2 * N; i += 128) {
+        const int j = i / (2 * N), l = i % (2 * N);
+        float v = 0.f;
+#pragma unroll
+        for (int ww = 0; ww < 4; ++ww) v += red[(j * 4 + ww) * 2 * N + l];
+        float* dst = (l < N ? a.dB : a.dC) + ((size_t)b * g.T + c * K + j) * g.lddbc + (l & (N - 1));
+        atomicAdd(dst, v);
+      }
     }
     __syncthreads();
   }
@@ -1058,9 +1078,23 @@ __global__ void __launch_bounds__(128, 4) m3_bwd2_kernel(const __grid_constant__
 // N = d_state: partial rows per channel are N + 8 (N of dA, then dD,
 // d_dt_bias, d_conv_b, d_conv_w[0..3]); nout of them are finalized.
 template <typename T>
-__global__ void m3_bwd_tail_kernel(BwdArgs a, int rows, int nfin, int nout, int N) {
+__global__ void m3_bwd_tail_kernel(const __grid_constant__ BwdArgs a, int rows, int nfin, int nfix,
+                                   int nout, int N) {
   const Geo g = a.g;
   grid_dep_wait();  // the main kernel's partials and boundary terms
+  if ((int)blockIdx.x >= nfin + nfix) {
+    // deterministic dB/dC: the channel blocks' shares of one (batch, step,
+    // lane) summed in block order
+    const size_t idx = (size_t)(blockIdx.x - nfin - nfix) * blockDim.x + threadIdx.x;
+    const size_t bt = idx / (2 * N);
+    const int l = (int)(idx % (2 * N));
+    if (bt >= (size_t)g.B * g.T) return;
+    const float* p = a.dbc_part + bt * a.nblk * 2 * N + l;
+    float v = 0.f;
+    for (int k = 0; k < a.nblk; ++k) v += p[(size_t)k * 2 * N];
+    (l < N ? a.dB : a.dC)[bt * g.lddbc + (l % N)] = v;
+    return;
+  }
   if ((int)blockIdx.x >= nfin) {
     const size_t idx = (size_t)(blockIdx.x - nfin) * blockDim.x + threadIdx.x;
     const size_t total = (size_t)g.B * (g.S - 1) * 3 * g.D;
@@ -1178,7 +1212,7 @@ m3_status launch_bwd(const Plan& p, BwdArgs a, cudaStream_t st, int smem_per_sm,
     e = launch_k(agg_for<T>(split, p.N), dim3((p.D + ch - 1) / ch, p.Sb - 1, p.B), GB,
                  agg_smem(sizeof(T), p.N).total, st, false, a);
     if (note(e) != cudaSuccess) return M3_ERR_CUDA;
-  } else {
+  } else if (!p.det) {
     // only the d_state columns of each (batch, step) row belong to dB and dC
     const size_t pitch = (size_t)p.lddbc * 4, rows = (size_t)p.B * p.T;
     if (note(cudaMemset2DAsync(a.dB, pitch, 0, (size_t)p.N * 4, rows, st)) != cudaSuccess) return M3_ERR_CUDA;
@@ -1203,9 +1237,10 @@ m3_status launch_bwd(const Plan& p, BwdArgs a, cudaStream_t st, int smem_per_sm,
   const int nout = scan ? p.N + 2 : p.N + 7;
   const size_t nfin = ((size_t)nout * p.D + 31) / 32;                 // 32 outputs per block
   const size_t nfix = (!scan && p.Sb > 1) ? ((size_t)p.B * (p.Sb - 1) * 3 * p.D + 255) / 256 : 0;
+  const size_t ndbc = p.det ? ((size_t)p.B * p.T * 2 * p.N + 255) / 256 : 0;
   if (e == cudaSuccess)
-    e = launch_k(m3_bwd_tail_kernel<T>, dim3((unsigned)(nfin + nfix)), 256, 0, st, true, a,
-                 p.B * p.Sb, (int)nfin, nout, p.N);
+    e = launch_k(m3_bwd_tail_kernel<T>, dim3((unsigned)(nfin + nfix + ndbc)), 256, 0, st, true, a,
+                 p.B * p.Sb, (int)nfin, (int)nfix, nout, p.N);
   if (e == cudaSuccess) e = cudaGetLastError();
   return note(e) == cudaSuccess ? M3_OK : M3_ERR_CUDA;
 }

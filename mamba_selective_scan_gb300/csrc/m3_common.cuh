@@ -329,6 +329,10 @@ struct BwdArgs {
   void* d_conv_in;
   int accumulate;
   uint32_t tcols;  // tensor-memory columns per CTA for the state history
+  // deterministic dB/dC: per-(batch, step, channel block) partials
+  // [B * T][nblk][2N], summed by the tail kernel; NULL: float atomics
+  float* dbc_part;
+  int nblk;
   // tile maps of the backward's staging (see TM_* below)
   CUtensorMap tm[11];
 };
@@ -595,6 +599,9 @@ struct Plan {
   size_t c_part;
   int fwd_launches, bwd_launches;
   int fwd_tpc, bwd_tpc;  // threads per channel in the forward's and backward's main kernels
+  bool det;              // dB/dC by fixed-order sums of per-block partials
+  int dblk;              // channel blocks of the backward's main kernel
+  size_t b_dbc;          // workspace offset of those partials [B * T][dblk][2N]
 };
 
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }

@@ -39,7 +39,8 @@ def to_np(t):
     return t.detach().to(torch.float64).cpu().numpy()
 
 
-def run_gpu(dev, chunk=0, segments=0, want_debug=True, d_gated=None, fwd_segments=None, tpc=0):
+def run_gpu(dev, chunk=0, segments=0, want_debug=True, d_gated=None, fwd_segments=None, tpc=0,
+            det=False):
     """Forward then backward through the C ABI.  Returns dict of float64 arrays."""
     import torch
     seg_f = segments if fwd_segments is None else fwd_segments
@@ -51,7 +52,8 @@ def run_gpu(dev, chunk=0, segments=0, want_debug=True, d_gated=None, fwd_segment
     grads = binding.m3scan_bwd(dev["x"], dev["delta_raw"], dev["z"], dev["B"], dev["C"],
                                dev["conv_w"], dev["conv_b"], dev["dt_bias"], dev["a_log"],
                                dev["D"], ckpt, g, chunk=chunk, segments=segments,
-                               want_du=want_debug, threads_per_channel=tpc)
+                               want_du=want_debug, threads_per_channel=tpc,
+                               deterministic_dbc=det)
     torch.cuda.synchronize()
     res = {"gated": to_np(gated), "ckpt": to_np(ckpt)}
     if y is not None:

@@ -261,7 +261,7 @@ def _struct_fields(name):
 def test_dims_and_plan_structs_match_the_header():
     assert _struct_fields("m3_dims") == [f for f, _ in binding.M3Dims._fields_]
     assert _struct_fields("m3_plan") == [f for f, _ in binding.M3Plan._fields_]
-    assert ctypes.sizeof(binding.M3Dims) == 8 * 7 + 4 * 2 + 8 * 2
+    assert ctypes.sizeof(binding.M3Dims) == 8 * 7 + 4 * 2 + 8 * 2 + 4 * 2
 
 
 def test_row_strides_are_validated(lib):
@@ -330,3 +330,20 @@ def test_wider_states_resolve_to_the_split_kernels(lib):
 
 def test_device_status_rejects_null(lib):
     assert lib.m3scan_device_status(None) == 1  # M3_ERR_NULL
+
+
+def test_deterministic_dbc_adds_block_partials_to_the_workspace(lib):
+    base = binding.make_dims(8, 2048, 1536, chunk=8, segments=12, threads_per_channel=1)
+    det = binding.make_dims(8, 2048, 1536, chunk=8, segments=12, threads_per_channel=1,
+                            deterministic_dbc=True)
+    st0, p0 = _plan(base)
+    st1, p1 = _plan(det)
+    assert st0 == 0 and st1 == 0
+    # 12 blocks of 128 channels, one partial row of 2 x 16 floats per (batch, step, block)
+    assert p1.workspace_bytes >= p0.workspace_bytes + 8 * 2048 * 12 * 32 * 4 - 256
+    bad = binding.make_dims(8, 2048, 1536, chunk=8, segments=12)
+    bad.deterministic_dbc = 2
+    assert binding.STATUS[_plan(bad)[0]] == "M3_ERR_DIMS"
+    bad = binding.make_dims(8, 2048, 1536, chunk=8, segments=12)
+    bad.reserved0 = 1
+    assert binding.STATUS[_plan(bad)[0]] == "M3_ERR_DIMS"

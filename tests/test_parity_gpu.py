@@ -208,3 +208,25 @@ def test_bounded_tile_wait_gives_up_and_reports():
     inp, gpu, ref = _case(1, 40, 24, "f32", seed=5, chunk=8, segments=2, tpc=2)
     assert_close(compare(gpu, ref, "f32"), "after the timeout diagnostic")
     assert binding.m3scan_device_status() == 0
+
+
+@pytest.mark.parametrize("tpc", [1, 2])
+@pytest.mark.parametrize("batch,T,D,act,chunk,segments", [
+    (2, 200, 136, "f32", 16, 3),
+    (2, 97, 72, "bf16", 30, 3),
+    (4, 33, 520, "bf16", 16, 2),
+    (1, 130, 200, "f32", 7, 1),
+])
+def test_deterministic_dbc_matches_oracle_and_repeats_bit_for_bit(batch, T, D, act, chunk,
+                                                                  segments, tpc):
+    """dB and dC as fixed-order sums of the channel blocks' shares: within
+    tolerance of the oracle, and two calls give identical bits for every
+    output."""
+    inp = make_inputs(batch, T, D, act=act, seed=batch * 77 + T + D)
+    dev = to_device(inp)
+    a = run_gpu(dev, chunk=chunk, segments=segments, tpc=tpc, det=True)
+    b = run_gpu(dev, chunk=chunk, segments=segments, tpc=tpc, det=True)
+    ref = run_oracle(inp)
+    assert_close(compare(a, ref, act), f"deterministic B={batch} T={T} D={D} {act} tpc={tpc}")
+    for k in a:
+        assert np.array_equal(a[k], b[k]), k
