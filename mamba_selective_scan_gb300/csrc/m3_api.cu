@@ -343,7 +343,7 @@ m3_status make_plan(const m3_dims* dm, m3_dtype act, Plan* p) {
   p->ws_bytes = fwd_total > bwd_total ? fwd_total : bwd_total;
   if (p->ws_bytes < 256) p->ws_bytes = 256;
   p->fwd_launches = empty ? 0 : (p->Sf > 1 ? 2 : 1);
-  p->bwd_launches = empty ? 0 : (p->Sb > 1 ? 3 : 2);
+  p->bwd_launches = empty ? 0 : (p->Sb > 1 ? 3 : 2) + (p->det ? 1 : 0);
   return M3_OK;
 }
 
@@ -384,11 +384,11 @@ m3_status m3scan_selftest_wait_timeout(m3_stream_t stream) {
 
 m3_status m3scan_device_status(int32_t* out) {
   if (!out) return M3_ERR_NULL;
-  unsigned vf = 0, vb = 0, va = 0;
+  unsigned vf = 0, vb = 0, v2 = 0, va = 0;
   if (note(take_fwd_status(&vf)) != cudaSuccess || note(take_bwd_status(&vb)) != cudaSuccess ||
-      note(take_aux_status(&va)) != cudaSuccess)
+      note(take_bwd2_status(&v2)) != cudaSuccess || note(take_aux_status(&va)) != cudaSuccess)
     return M3_ERR_CUDA;
-  *out = (int32_t)(vf | vb | va);
+  *out = (int32_t)(vf | vb | v2 | va);
   return M3_OK;
 }
 

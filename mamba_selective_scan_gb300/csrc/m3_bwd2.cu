@@ -1,0 +1,485 @@
+// m3_bwd2.cu -- the backward main kernel with the lanes split over
+// d_state / 8 threads per channel, compiled apart from the rest of the
+// backward so the two build in parallel.
+#include "m3_common.cuh"
+
+namespace m3 {
+
+// nonzero once a kernel here gave up waiting for a tile copy
+__device__ unsigned int g_bwd2_status;
+
+cudaError_t take_bwd2_status(unsigned* out) {
+  unsigned v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_bwd2_status, sizeof(v));
+  if (e == cudaSuccess && v) {
+    const unsigned zero = 0;
+    e = cudaMemcpyToSymbol(g_bwd2_status, &zero, sizeof(zero));
+  }
+  *out = v;
+  return e;
+}
+
+// ---------------------------------------------------------------------------
+// backward main kernel with the lanes split over G = N / 8 threads per
+// channel (8 lanes each, 128 / G channels per block); the threads of a
+// channel take the per-step scalar work of every G-th step.  For d_state 32
+// and 64, and for d_state-16 grids that fill less than one wave (each thread
+// then runs about half the per-step instructions of m3_bwd_kernel and a
+// block holds twice the warps per channel).  Same results as m3_bwd_kernel
+// up to the order of f32 sums.
+// ---------------------------------------------------------------------------
+
+// Sum over the channels of a warp (the lanes with the same lane % G) of 8
+// values held as 4 pairs, pair P holding this thread's lane pair
+// P ^ ((lane >> 3) & 3).  The channel bits of a lane are its bits log2(G)
+// and up; the sum runs over them:
+//   G = 2: returns (in .x) the total for pair (lane >> 3) & 3, element
+//          (lane >> 2) & 1 (lanes differing only in bit 1 return the same);
+//   G = 4: the same total, every lane distinct;
+//   G = 8: returns both elements of pair (lane >> 3) & 3.
+template <int G>
+__device__ __forceinline__ float2 warp_sum8_rotated(float2 (&v)[4], int lane) {
+  v[0].x += __shfl_xor_sync(0xffffffffu, v[2].x, 16);
+  v[0].y += __shfl_xor_sync(0xffffffffu, v[2].y, 16);
+  v[1].x += __shfl_xor_sync(0xffffffffu, v[3].x, 16);
+  v[1].y += __shfl_xor_sync(0xffffffffu, v[3].y, 16);
+  v[0].x += __shfl_xor_sync(0xffffffffu, v[1].x, 8);
+  v[0].y += __shfl_xor_sync(0xffffffffu, v[1].y, 8);
+  if constexpr (G == 8) {
+    return v[0];
+  } else {
+    const bool up = (lane & 4) != 0;
+    const float send = up ? v[0].x : v[0].y;
+    const float keep = up ? v[0].y : v[0].x;
+    float r = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+    if constexpr (G == 2) r += __shfl_xor_sync(0xffffffffu, r, 2);
+    return make_float2(r, 0.f);
+  }
+}
+
+template <typename T, bool ST, bool SCAN, int N, bool DET>
+__global__ void __launch_bounds__(128, 4) m3_bwd2_kernel(const __grid_constant__ BwdArgs a) {
+  constexpr int G = N / 8;     // threads per channel
+  constexpr int CH = 128 / G;  // channels per block
+  constexpr int NP = N + 8;    // per-channel parameter partials
+  extern __shared__ __align__(128) unsigned char smem[];
+  const Geo g = a.g;
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  const int hf = tid % G;            // this thread's state lanes: 8 hf .. 8 hf + 7
+  const int ch = tid / G;            // channel within the block
+  const int prot = (lane >> 3) & 3;  // pair rotation for the warp reduction
+  const int d0 = blockIdx.x * CH;
+  const int s = blockIdx.y;
+  const int b = blockIdx.z;
+  const int d = d0 + ch;
+  const bool active = d < g.D;
+  const int c_begin = s * g.m;
+  const int c_end = min(c_begin + g.m, g.nc);
+  const int t_begin = c_begin * g.K;
+  const int t_end = min(c_end * g.K, g.T);
+  const int K = g.K;
+  const Bwd2Smem L = bwd2_smem(K, sizeof(T), N);
+  float* fB = reinterpret_cast<float*>(smem + L.fB);
+  float* fC = reinterpret_cast<float*>(smem + L.fC);
+  float* red = reinterpret_cast<float*>(smem + L.red);
+  float* dcs = reinterpret_cast<float*>(smem + L.dcs);  // [K + 3][CH]
+  // state lane of register pair P
+  auto lane_of = [&](int P) { return 8 * hf + 2 * (P ^ prot); };
+  // this thread's copy of B and C: its 8 lanes in register order
+  const float* fBr = fB + prot * rot_stride(K, N) + 8 * hf;
+  const float* fCr = fC + prot * rot_stride(K, N) + 8 * hf;
+
+  // recomputed states of a chunk: row j of this thread = TMEM columns
+  // [8 j, 8 j + 8) of its lane; warp 0 allocates, every exit deallocates
+  __shared__ uint32_t tmem_slot;
+  __shared__ __align__(8) uint64_t tbar[2];  // tile copies into staging buffer 0 / 1
+  if (warp == 0) tmem_alloc(&tmem_slot, a.tcols);
+  if (tid == 32) {
+    mbar_init(&tbar[0], 1);
+    mbar_init(&tbar[1], 1);
+    mbar_init_fence();
+  }
+  tmem_fence_before_sync();
+  __syncthreads();
+  tmem_fence_after_sync();
+  const uint32_t trow = tmem_slot + ((uint32_t)(warp * 32) << 16);
+
+  float2 a2[4];
+  float w[WC];
+  float cb = 0.f, dtb = 0.f, Dd = 0.f;
+#pragma unroll
+  for (int P = 0; P < 4; ++P) {
+    const int n = lane_of(P);
+    a2[P].x = active ? -expf(a.a_log[(size_t)d * N + n]) * LOG2E : 0.f;
+    a2[P].y = active ? -expf(a.a_log[(size_t)d * N + n + 1]) * LOG2E : 0.f;
+  }
+#pragma unroll
+  for (int k = 0; k < WC; ++k) w[k] = active ? a.conv_w[(size_t)d * WC + k] : 0.f;
+  if (active) {
+    cb = a.conv_b[d];
+    dtb = a.dt_bias[d];
+    Dd = a.Dp[d];
+  }
+  float2 carry[4];
+#pragma unroll
+  for (int P = 0; P < 4; ++P) carry[P] = make_float2(0.f, 0.f);
+  if (ST && a.g_h && active) {
+    const float* gh = a.g_h + (size_t)b * N * g.D + d;
+#pragma unroll
+    for (int P = 0; P < 4; ++P) {
+      const int n = lane_of(P);
+      carry[P] = make_float2(gh[(size_t)n * g.D], gh[(size_t)(n + 1) * g.D]);
+    }
+  }
+  // A chunk's tiles arrive by tensor-map copies issued by thread 0: x with
+  // its three halo rows before the chunk, delta_raw, z, d_gated, B, C and
+  // the chunk's start state; rows outside [0, T) and channels past d_inner
+  // arrive as zeros.
+  const uint32_t tile_bytes =
+      (uint32_t)((4 * K + 3) * CH * sizeof(T) + 2 * K * N * sizeof(T) + (size_t)N * CH * 4);
+  const bool misaligned = (smem_u32(smem) & 127u) != 0;  // tile copies need 128-byte aligned buffers
+  auto stage = [&](int c, int buf) {
+    if (tid == 0 && !misaligned) {
+      unsigned char* base = smem + (size_t)buf * L.tile;
+      const int t0 = c * K;
+      fence_proxy_async();
+      mbar_expect_tx(&tbar[buf], tile_bytes);
+      tma_load_3d(base + L.x, &a.tm[TM_X], d0, t0 - 3, b, &tbar[buf]);
+      tma_load_3d(base + L.dr, &a.tm[TM_DR], d0, t0, b, &tbar[buf]);
+      tma_load_3d(base + L.z, &a.tm[TM_Z], d0, t0, b, &tbar[buf]);
+      tma_load_3d(base + L.dg, &a.tm[TM_DG], d0, t0, b, &tbar[buf]);
+      tma_load_3d(base + L.Bt, &a.tm[TM_B], 0, t0, b, &tbar[buf]);
+      tma_load_3d(base + L.Ct, &a.tm[TM_C], 0, t0, b, &tbar[buf]);
+      tma_load_4d(base + L.ck, &a.tm[TM_CK], d0, 0, c, b, &tbar[buf]);
+    }
+  };
+  stage(c_end - 1, 0);
+  grid_dep_trigger();
+  grid_dep_wait();
+  if (s + 1 < g.S) {
+    chain_segments<4, 4>(carry, a2, a.sd, a.q, N, (size_t)b * g.S, g.S - 1, -1, g.S - 1 - s, g.D, d,
+                         active, lane_of);
+  }
+  float2 dAp[4];
+#pragma unroll
+  for (int P = 0; P < 4; ++P) dAp[P] = make_float2(0.f, 0.f);
+  float dD_acc = 0.f, ddtb_acc = 0.f, dcb_acc = 0.f;
+  float dcw[WC] = {0.f, 0.f, 0.f, 0.f};
+  for (int i = tid; i < (K + 3) * CH; i += 128) dcs[i] = 0.f;  // ordered by the loop's first barrier
+
+  bool aborted = false;
+  for (int c = c_end - 1; c >= c_begin; --c) {
+    const int it = c_end - 1 - c;  // buffer it & 1, its (it >> 1)-th use
+    const int buf = it & 1;
+    if (c - 1 >= c_begin) stage(c - 1, buf ^ 1);
+    const bool landed = !misaligned && mbar_wait(&tbar[buf], (it >> 1) & 1);
+    if (__syncthreads_or(!landed)) {
+      // a tile did not arrive: report it, let the copy issued above drain, leave
+      if (tid == 0) {
+        atomicOr(&g_bwd2_status, 1u);
+        if (!misaligned && c - 1 >= c_begin) mbar_wait(&tbar[buf ^ 1], ((it + 1) >> 1) & 1);
+      }
+      aborted = true;
+      break;
+    }
+    const unsigned char* base = smem + (size_t)buf * L.tile;
+    if (ST && a.conv_in && c * K < 3 && active && hf == 0) {
+      T* xw = reinterpret_cast<T*>(smem + (size_t)buf * L.tile + L.x);
+      const T* ci = static_cast<const T*>(a.conv_in) + (size_t)b * 3 * g.D + d;
+      for (int r = 0; r < 3 - c * K; ++r) xw[r * CH + ch] = ci[(size_t)(c * K + r) * g.D];
+    }
+    {
+      const T* Bt = reinterpret_cast<const T*>(base + L.Bt);
+      const T* Ct = reinterpret_cast<const T*>(base + L.Ct);
+      // copy r, row j: position 8 h + 2 P + e holds state lane 8 h + 2 (P ^ r) + e
+      for (int i = tid; i < K * N; i += 128) {
+        const float bv = Act<T>::ld(Bt + i), cv = Act<T>::ld(Ct + i);
+        const int j = i / N, n = i % N;
+#pragma unroll
+        for (int r = 0; r < NROT; ++r) {
+          const int o = r * rot_stride(K, N) + j * N + (n & ~7) + 2 * (((n >> 1) & 3) ^ r) + (n & 1);
+          fB[o] = bv;
+          fC[o] = cv;
+        }
+      }
+    }
+    __syncthreads();
+    const T* xt = reinterpret_cast<const T*>(base + L.x);  // row r is step c*K - 3 + r
+    const T* drt = reinterpret_cast<const T*>(base + L.dr);
+    const T* zt = reinterpret_cast<const T*>(base + L.z);
+    const T* dgt = reinterpret_cast<const T*>(base + L.dg);
+    const float* ckt = reinterpret_cast<const float*>(base + L.ck);
+    const int steps = min(K, g.T - c * K);
+    float4* s0 = reinterpret_cast<float4*>(smem + L.scal) + ch;  // shared by the channel's threads, stride CH
+    float4* s1 = s0 + (size_t)K * CH;
+    const size_t row0 = ((size_t)b * g.T + (size_t)c * K) * g.D + d;
+
+    // ---- scalar pass, every G-th step ----
+    for (int j = hf; j < steps; j += G) {
+      const float xm3 = Act<T>::ld(xt + j * CH + ch);
+      const float xm2 = Act<T>::ld(xt + (j + 1) * CH + ch);
+      const float xm1 = Act<T>::ld(xt + (j + 2) * CH + ch);
+      const float xv = Act<T>::ld(xt + (j + 3) * CH + ch);
+      const float cpre = fmaf(w[0], xm3, fmaf(w[1], xm2, fmaf(w[2], xm1, fmaf(w[3], xv, cb))));
+      const float sc = sigmoid_f(cpre);
+      const float u = cpre * sc;
+      const float v = Act<T>::ld(drt + j * CH + ch) + dtb;
+      const float delta = softplus_f(v);
+      const float sv = sigmoid_f(v);
+      const float zv = Act<T>::ld(zt + j * CH + ch);
+      const float gv = Act<T>::ld(dgt + j * CH + ch);
+      const float sz = sigmoid_f(zv);
+      s0[j * CH] = make_float4(delta, delta * u, gv * zv * sz, gv * (sz * fmaf(zv, 1.f - sz, 1.f)));
+      s1[j * CH] = make_float4(Dd * u, sv, sc, cpre);
+    }
+    __syncwarp();
+
+    // ---- recompute this thread's 8 lanes of the chunk's states ----
+    {
+      float2 h[4];
+#pragma unroll
+      for (int P = 0; P < 4; ++P) {
+        const int n = lane_of(P);
+        h[P] = make_float2(ckt[n * CH + ch], ckt[(n + 1) * CH + ch]);
+      }
+#pragma unroll 2
+      for (int j = 0; j < steps; ++j) {
+        const float4 v0 = s0[j * CH];
+        const float2 dl2 = f2b(v0.x);
+        const float2 du2 = f2b(v0.y);
+#pragma unroll
+        for (int P = 0; P < 4; ++P) {
+          const float2 bb = *reinterpret_cast<const float2*>(fBr + j * N + 2 * P);
+          h[P] = __ffma2_rn(ex2x2(__fmul2_rn(dl2, a2[P])), h[P], __fmul2_rn(du2, bb));
+        }
+        tmem_st8(trow + 8u * (uint32_t)j, h);
+      }
+      tmem_wait_st();
+    }
+
+    // ---- reverse-time pass ----
+    {
+      float2 hn[4];
+      tmem_ld8(trow + 8u * (uint32_t)(steps - 1), hn);
+#pragma unroll 2
+      for (int j = steps - 1; j >= 0; --j) {
+        const float4 v0 = s0[j * CH];
+        const float Du = reinterpret_cast<const float*>(s1 + j * CH)[0];
+        const float2 dl2 = f2b(v0.x);
+        const float2 du2 = f2b(v0.y);
+        const float2 dy2 = f2b(v0.z);
+        float2 sB = make_float2(0.f, 0.f), sAq = make_float2(0.f, 0.f), y2 = make_float2(0.f, 0.f);
+        float2 pB[4], pC[4], hp[4];
+        if (j > 0) {
+          tmem_ld8(trow + 8u * (uint32_t)(j - 1), hp);
+        } else {
+#pragma unroll
+          for (int P = 0; P < 4; ++P) {
+            const int n = lane_of(P);
+            hp[P] = make_float2(ckt[n * CH + ch], ckt[(n + 1) * CH + ch]);
+          }
+        }
+#pragma unroll
+        for (int P = 0; P < 4; ++P) {
+          const float2 bb = *reinterpret_cast<const float2*>(fBr + j * N + 2 * P);
+          const float2 cc = *reinterpret_cast<const float2*>(fCr + j * N + 2 * P);
+          y2 = __ffma2_rn(cc, hn[P], y2);
+          const float2 dh = __ffma2_rn(dy2, cc, carry[P]);
+          pC[P] = __fmul2_rn(dy2, hn[P]);
+          pB[P] = __fmul2_rn(dh, du2);
+          sB = __ffma2_rn(dh, bb, sB);
+          carry[P] = __fmul2_rn(ex2x2(__fmul2_rn(dl2, a2[P])), dh);
+          const float2 qv = __fmul2_rn(carry[P], hp[P]);
+          dAp[P] = __ffma2_rn(dl2, qv, dAp[P]);
+          sAq = __ffma2_rn(a2[P], qv, sAq);
+        }
+#pragma unroll
+        for (int P = 0; P < 4; ++P) hn[P] = hp[P];
+        float ys = y2.x + y2.y, sBs = sB.x + sB.y, sAs = sAq.x + sAq.y;
+#pragma unroll
+        for (int o = 1; o < G; o <<= 1) {
+          ys += __shfl_xor_sync(0xffffffffu, ys, o);
+          sBs += __shfl_xor_sync(0xffffffffu, sBs, o);
+          sAs += __shfl_xor_sync(0xffffffffu, sAs, o);
+        }
+        if (hf == j % G) {
+          if (active) Act<T>::st(static_cast<T*>(a.dz) + row0 + (size_t)j * g.D, (ys + Du) * v0.w);
+          reinterpret_cast<float*>(s0 + j * CH)[3] = sAs;
+          reinterpret_cast<float*>(s1 + j * CH)[0] = sBs;
+        }
+        const float2 rb = warp_sum8_rotated<G>(pB, lane);
+        const float2 rc = warp_sum8_rotated<G>(pC, lane);
+        float* rj = red + (j * 4 + warp) * 2 * N;  // [dB: N][dC: N]
+        if constexpr (G == 8) {
+          const int n = 8 * hf + 2 * prot;
+          rj[n] = rb.x;
+          rj[n + 1] = rb.y;
+          rj[N + n] = rc.x;
+          rj[N + n + 1] = rc.y;
+        } else if (G == 4 || (lane & 2) == 0) {
+          const int n = 8 * hf + 2 * prot + ((lane >> 2) & 1);
+          rj[n] = rb.x;
+          rj[N + n] = rc.x;
+        }
+      }
+    }
+    __syncwarp();
+
+    // ---- du, d delta, softplus and (unless SCAN) SiLU backward, every G-th step ----
+    for (int j = hf; j < steps; j += G) {
+      const int t = c * K + j;
+      const float4 v0 = s0[j * CH];
+      const float4 v1 = s1[j * CH];
+      const float delta = v0.x, dy = v0.z, sAq = v0.w;
+      const float sumB = v1.x, sv = v1.y, sc = v1.z, cpre = v1.w;
+      const float u = cpre * sc;
+      const float du = fmaf(dy, Dd, delta * sumB);
+      const float ddr = fmaf(u, sumB, LN2 * sAq) * sv;
+      dD_acc = fmaf(dy, u, dD_acc);
+      ddtb_acc += ddr;
+      if (active) {
+        Act<T>::st(static_cast<T*>(a.ddr) + row0 + (size_t)j * g.D, ddr);
+        if (a.du_dbg) Act<T>::st(static_cast<T*>(a.du_dbg) + row0 + (size_t)j * g.D, du);
+      }
+      if constexpr (SCAN) continue;
+      const float dc = du * (sc * fmaf(cpre, 1.f - sc, 1.f));
+      dcb_acc += dc;
+#pragma unroll
+      for (int k = 0; k < WC; ++k) dcw[k] = fmaf(dc, Act<T>::ld(xt + (j + k) * CH + ch), dcw[k]);
+      dcs[j * CH + ch] = dc;
+      if (active && s > 0 && t < t_begin + 3)
+        a.dchead[(((size_t)b * g.S + s) * 3 + (t - t_begin)) * g.D + d] = dc;
+    }
+    if constexpr (!SCAN) {
+      __syncwarp();
+      // ---- conv backward: d_x from the conv-input gradient of this and the next 3 steps ----
+      for (int j = hf; j < steps; j += G) {
+        const int t = c * K + j;
+        float dxv = fmaf(dcs[j * CH + ch], w[3], fmaf(dcs[(j + 1) * CH + ch], w[2],
+                         fmaf(dcs[(j + 2) * CH + ch], w[1], dcs[(j + 3) * CH + ch] * w[0])));
+        if (ST && a.g_conv && t >= g.T - 3 && active)
+          dxv += Act<T>::ld(static_cast<const T*>(a.g_conv) + ((size_t)b * 3 + t - (g.T - 3)) * g.D + d);
+        if (active) {
+          if (s + 1 < g.S && t >= t_end - 3)
+            a.dxpart[(((size_t)b * g.S + s) * 3 + (t - (t_end - 3))) * g.D + d] = dxv;
+          else
+            Act<T>::st(static_cast<T*>(a.dx) + row0 + (size_t)j * g.D, dxv);
+        }
+      }
+      __syncwarp();
+      // the next chunk processed (the one before in time) reads the dc of
+      // this chunk's first three steps: rows 0..2 of this chunk followed by
+      // the carried rows (a chunk may be shorter than three steps), all
+      // read before any is overwritten
+      if (hf == 0) {
+        const float v0 = dcs[ch], v1 = dcs[CH + ch], v2 = dcs[2 * CH + ch];
+        dcs[K * CH + ch] = v0;
+        dcs[(K + 1) * CH + ch] = v1;
+        dcs[(K + 2) * CH + ch] = v2;
+      }
+    }
+
+    __syncthreads();
+    if constexpr (DET) {  // this block's share, summed in a fixed order by the tail kernel
+      for (int i = tid; i < steps * 2 * N; i += 128) {
+        const int j = i / (2 * N), l = i % (2 * N);
+        float v = 0.f;
+#pragma unroll
+        for (int ww = 0; ww < 4; ++ww) v += red[(j * 4 + ww) * 2 * N + l];
+        a.dbc_part[(((size_t)b * g.T + c * K + j) * a.nblk + blockIdx.x) * 2 * N + l] = v;
+      }
+    } else {
+      for (int i = tid; i < steps * 2 * N; i += 128) {
+        const int j = i / (2 * N), l = i % (2 * N);
+        float v = 0.f;
+#pragma unroll
+        for (int ww = 0; ww < 4; ++ww) v += red[(j * 4 + ww) * 2 * N + l];
+        float* dst = (l < N ? a.dB : a.dC) + ((size_t)b * g.T + c * K + j) * g.lddbc + (l & (N - 1));
+        atomicAdd(dst, v);
+      }
+    }
+    __syncthreads();
+  }
+
+  if (!aborted) {
+    if (ST && s == 0 && active) {
+      if (a.d_h_in) {
+        float* dh0 = a.d_h_in + (size_t)b * N * g.D + d;
+  #pragma unroll
+        for (int P = 0; P < 4; ++P) {
+          const int n = lane_of(P);
+          dh0[(size_t)n * g.D] = carry[P].x;
+          dh0[(size_t)(n + 1) * g.D] = carry[P].y;
+        }
+      }
+      if (!SCAN && a.d_conv_in && hf == 0) {
+        // dc of steps 0, 1, 2 (zero past the sequence), kept in rows K.. K+2
+        const float f0 = dcs[K * CH + ch], f1 = dcs[(K + 1) * CH + ch], f2 = dcs[(K + 2) * CH + ch];
+        float v[3];
+        v[2] = fmaf(f0, w[2], fmaf(f1, w[1], f2 * w[0]));
+        v[1] = fmaf(f0, w[1], f1 * w[0]);
+        v[0] = f0 * w[0];
+        T* dci = static_cast<T*>(a.d_conv_in) + (size_t)b * 3 * g.D + d;
+  #pragma unroll
+        for (int r = 0; r < 3; ++r) {
+          const int ro = r - g.T;
+          if (a.g_conv && ro >= 0)
+            v[r] += Act<T>::ld(static_cast<const T*>(a.g_conv) + ((size_t)b * 3 + ro) * g.D + d);
+          Act<T>::st(dci + (size_t)r * g.D, v[r]);
+        }
+      }
+    }
+    // the per-step partial sums: each thread of a channel summed its own steps
+  #pragma unroll
+    for (int o = 1; o < G; o <<= 1) {
+      dD_acc += __shfl_xor_sync(0xffffffffu, dD_acc, o);
+      ddtb_acc += __shfl_xor_sync(0xffffffffu, ddtb_acc, o);
+      dcb_acc += __shfl_xor_sync(0xffffffffu, dcb_acc, o);
+  #pragma unroll
+      for (int k = 0; k < WC; ++k) dcw[k] += __shfl_xor_sync(0xffffffffu, dcw[k], o);
+    }
+    if (active) {
+      float* Pp = a.partials + ((size_t)b * g.S + s) * NP * g.D;
+  #pragma unroll
+      for (int P = 0; P < 4; ++P) {
+        const int n = lane_of(P);
+        Pp[(size_t)n * g.D + d] = dAp[P].x;
+        Pp[(size_t)(n + 1) * g.D + d] = dAp[P].y;
+      }
+      if (hf == 0) {
+        Pp[(size_t)N * g.D + d] = dD_acc;
+        Pp[(size_t)(N + 1) * g.D + d] = ddtb_acc;
+        Pp[(size_t)(N + 2) * g.D + d] = dcb_acc;
+  #pragma unroll
+        for (int k = 0; k < WC; ++k) Pp[(size_t)(N + 3 + k) * g.D + d] = dcw[k];
+      }
+    }
+  }
+  tmem_fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem_slot, a.tcols);
+}
+
+
+// the split kernel for (deterministic dB/dC, stop at du, carried state, d_state)
+template <typename T, bool ST, bool SCAN, bool DET>
+void (*bwd2_for(int N))(BwdArgs) {
+  return N == 16 ? m3_bwd2_kernel<T, ST, SCAN, 16, DET>
+       : N == 32 ? m3_bwd2_kernel<T, ST, SCAN, 32, DET> : m3_bwd2_kernel<T, ST, SCAN, 64, DET>;
+}
+template <typename T, bool DET>
+void (*bwd2_pick(bool scan, bool st, int N))(BwdArgs) {
+  return scan ? (st ? bwd2_for<T, true, true, DET>(N) : bwd2_for<T, false, true, DET>(N))
+              : (st ? bwd2_for<T, true, false, DET>(N) : bwd2_for<T, false, false, DET>(N));
+}
+template <typename T>
+void (*bwd2_kernel_for(bool det, bool scan, bool st, int N))(BwdArgs) {
+  return det ? bwd2_pick<T, true>(scan, st, N) : bwd2_pick<T, false>(scan, st, N);
+}
+
+template void (*bwd2_kernel_for<float>(bool, bool, bool, int))(BwdArgs);
+template void (*bwd2_kernel_for<__nv_bfloat16>(bool, bool, bool, int))(BwdArgs);
+
+}  // namespace m3

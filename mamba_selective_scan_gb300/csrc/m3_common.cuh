@@ -637,6 +637,10 @@ bool encode_tile_map(CUtensorMap* map, int es, int rank, const void* ptr, const 
 // Per-unit device status word: nonzero once a kernel of that unit gave up
 // waiting for a tile copy.  take_*_status reads and clears it (synchronous).
 cudaError_t take_bwd_status(unsigned* out);
+cudaError_t take_bwd2_status(unsigned* out);
+// the split backward main kernel for (deterministic dB/dC, stop at du,
+// carried state, d_state); provided by m3_bwd2.cu
+template <typename T> void (*bwd2_kernel_for(bool det, bool scan, bool st, int N))(BwdArgs);
 // one block whose tile wait never completes (diagnostic of the bounded waits)
 cudaError_t launch_wait_timeout(cudaStream_t st);
 cudaError_t take_fwd_status(unsigned* out);
