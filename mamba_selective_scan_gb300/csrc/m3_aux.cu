@@ -127,7 +127,7 @@ __global__ void __launch_bounds__(128) m3_conv_bwd_kernel(const __grid_constant_
 
 // d_conv_b and d_conv_w from the per-(batch, tile) partials, summed in a
 // fixed order (32 outputs per block, rows split over 8 warps).
-__global__ void m3_conv_fin_kernel(const __grid_constant__ ConvArgs a) {
+__global__ void m3_conv_fin_kernel(ConvArgs a) {
   grid_dep_wait();  // the conv backward's partials
   __shared__ float part[8][33];
   const int cx = threadIdx.x & 31, ry = threadIdx.x >> 5;

@@ -628,7 +628,7 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(const __grid_constant__ B
 
 // Deterministic dB/dC (launched after the main kernel when asked for): the
 // channel blocks' shares of one (batch, step, lane) summed in block order.
-__global__ void m3_dbc_sum_kernel(const __grid_constant__ BwdArgs a, int N) {
+__global__ void m3_dbc_sum_kernel(BwdArgs a, int N) {
   const Geo g = a.g;
   grid_dep_wait();  // the main kernel's shares
   const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
