@@ -650,7 +650,7 @@ __global__ void m3_dbc_sum_kernel(BwdArgs a, int N) {
 // N = d_state: partial rows per channel are N + 8 (N of dA, then dD,
 // d_dt_bias, d_conv_b, d_conv_w[0..3]); nout of them are finalized.
 template <typename T>
-__global__ void m3_bwd_tail_kernel(BwdArgs a, int rows, int nfin, int nout, int N) {
+__global__ void m3_bwd_tail_kernel(TailArgs a, int rows, int nfin, int nout, int N) {
   const Geo g = a.g;
   grid_dep_wait();  // the main kernel's partials and boundary terms
   if ((int)blockIdx.x >= nfin) {
@@ -789,9 +789,16 @@ m3_status launch_bwd(const Plan& p, BwdArgs a, cudaStream_t st, int smem_per_sm,
   const size_t nfin = ((size_t)nout * p.D + 31) / 32;                 // 32 outputs per block
   const size_t nfix = (!scan && p.Sb > 1) ? ((size_t)p.B * (p.Sb - 1) * 3 * p.D + 255) / 256 : 0;
   const size_t ndbc = p.det ? ((size_t)p.B * p.T * 2 * p.N + 255) / 256 : 0;
-  if (e == cudaSuccess)
-    e = launch_k(m3_bwd_tail_kernel<T>, dim3((unsigned)(nfin + nfix)), 256, 0, st, true, a,
+  if (e == cudaSuccess) {
+    TailArgs ta;
+    ta.g = a.g;
+    ta.partials = a.partials; ta.dxpart = a.dxpart; ta.dchead = a.dchead;
+    ta.conv_w = a.conv_w; ta.a_log = a.a_log; ta.dx = a.dx;
+    ta.d_a_log = a.d_a_log; ta.dD = a.dD; ta.d_dt_bias = a.d_dt_bias;
+    ta.d_conv_b = a.d_conv_b; ta.d_conv_w = a.d_conv_w; ta.accumulate = a.accumulate;
+    e = launch_k(m3_bwd_tail_kernel<T>, dim3((unsigned)(nfin + nfix)), 256, 0, st, true, ta,
                  p.B * p.Sb, (int)nfin, nout, p.N);
+  }
   if (e == cudaSuccess && p.det)
     e = launch_k(m3_dbc_sum_kernel, dim3((unsigned)ndbc), 256, 0, st, true, a, p.N);
   if (e == cudaSuccess) e = cudaGetLastError();

@@ -336,6 +336,16 @@ struct BwdArgs {
   // tile maps of the backward's staging (see TM_* below)
   CUtensorMap tm[11];
 };
+// The backward's last kernel needs only these (a small argument block keeps
+// its launch cheap).
+struct TailArgs {
+  Geo g;
+  const float *partials, *dxpart, *dchead, *conv_w, *a_log;
+  void* dx;
+  float *d_a_log, *dD, *d_dt_bias, *d_conv_b, *d_conv_w;
+  int accumulate;
+};
+
 // tensor maps of BwdArgs::tm, boxes of the block's channels (128 / threads
 // per channel): main kernels -- activations [B, T, D] x (K + 3) rows (x)
 // or K rows, B and C [B, T, ld] N x K, checkpoints [B, nc, N, D] f32
