@@ -91,7 +91,10 @@ def test_strided_b_c_and_gradients_match_oracle(act, R, segments):
     (3, 37, 72, "bf16", 2, 4, True),
 ])
 @pytest.mark.parametrize("tpc", [1, 2])
-def test_two_phase_backward_matches_oracle(batch, T, D, act, chunk, segments, state, tpc):
+@pytest.mark.parametrize("det", [False, True])
+def test_two_phase_backward_matches_oracle(batch, T, D, act, chunk, segments, state, tpc, det):
+    """det: dB/dC as fixed-order sums (m3_dims.deterministic_dbc), and a
+    second call must repeat every output bit for bit."""
     seed = batch + T + D + chunk
     inp = make_inputs(batch, T, D, act=act, seed=seed)
     dev = to_device(inp)
@@ -116,12 +119,19 @@ def test_two_phase_backward_matches_oracle(batch, T, D, act, chunk, segments, st
                                             dev["C"], dev["conv_w"], dev["conv_b"],
                                             dev["dt_bias"], dev["a_log"], dev["D"], chunk=chunk,
                                             segments=segments)
-    o = binding.m3scan_bwd_two_phase(dev["x"], dev["delta_raw"], dev["z"], dev["B"], dev["C"],
-                                     dev["conv_w"], dev["conv_b"], dev["dt_bias"], dev["a_log"],
-                                     dev["D"], ckpt, dev["d_gated"], lambda g: du_extra_t,
-                                     chunk=chunk, segments=segments,
-                                     threads_per_channel=tpc, **kw)
+    def run():
+        return binding.m3scan_bwd_two_phase(
+            dev["x"], dev["delta_raw"], dev["z"], dev["B"], dev["C"], dev["conv_w"],
+            dev["conv_b"], dev["dt_bias"], dev["a_log"], dev["D"], ckpt, dev["d_gated"],
+            lambda g: du_extra_t, chunk=chunk, segments=segments, threads_per_channel=tpc,
+            deterministic_dbc=det, **kw)
+    o = run()
     torch.cuda.synchronize()
+    if det:
+        o2 = run()
+        torch.cuda.synchronize()
+        for k in o:
+            assert np.array_equal(to_np(o[k]), to_np(o2[k])), k
     okw = {}
     if state:
         okw = {k: st[k] for k in ("ssm_state", "conv_state", "d_ssm_state_out",
