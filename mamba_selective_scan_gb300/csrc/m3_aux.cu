@@ -164,14 +164,31 @@ __global__ void m3_conv_fin_kernel(ConvArgs a) {
 // (two when the grid is large enough) keep more loads in flight.  Each step
 // issues all of its global loads before its barrier; B and C of the next
 // step are staged into the other half of a double buffer.
-template <typename T, int N, int R>
-__global__ void __launch_bounds__(GD) m3_decode_kernel(DecArgs a) {
+// TL: the block's carried states arrive by one tensor-map copy into shared
+// memory (hs[R][N][CH]), issued before the other loads and waited for after
+// them; otherwise each thread loads its own lanes.
+template <typename T, int N, int R, bool TL>
+__global__ void __launch_bounds__(GD) m3_decode_kernel(const __grid_constant__ DecArgs a) {
   constexpr int G = N / 16;       // threads per channel
   constexpr int CH = GD / G;      // channels per block
   constexpr int NB = 2 * N * R;   // B and C values of one step
   __shared__ float sBC[2][R][2 * N];
   __shared__ float sA[8][GD][2];  // A log2(e) of this thread's lanes
+  extern __shared__ __align__(128) unsigned char dsm[];
+  __shared__ __align__(8) uint64_t tbar;
   const int tid = threadIdx.x;
+  const bool misaligned = TL && (smem_u32(dsm) & 127u) != 0;  // tile copies need 128-byte aligned buffers
+  if constexpr (TL) {
+    if (tid == 0) {
+      mbar_init(&tbar, 1);
+      mbar_init_fence();
+    }
+    __syncthreads();
+    if (tid == 0 && !misaligned) {
+      mbar_expect_tx(&tbar, (uint32_t)(R * N * CH * 4));
+      tma_load_3d(dsm, &a.tm_h, blockIdx.x * CH, 0, blockIdx.y * R, &tbar);
+    }
+  }
   const int q = tid % G;          // this thread's lanes: 16 q .. 16 q + 15
   const int d = blockIdx.x * CH + tid / G;
   const bool active = d < a.D;
@@ -222,9 +239,11 @@ __global__ void __launch_bounds__(GD) m3_decode_kernel(DecArgs a) {
 #pragma unroll
   for (int r = 0; r < R; ++r) {
     if (!ron[r]) continue;
-    const float* hp = a.h + ((size_t)rb[r] * N + 16 * q) * D + d;
+    if constexpr (!TL) {
+      const float* hp = a.h + ((size_t)rb[r] * N + 16 * q) * D + d;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) h[r][i] = make_float2(hp[(size_t)(2 * i) * D], hp[(size_t)(2 * i + 1) * D]);
+      for (int i = 0; i < 8; ++i) h[r][i] = make_float2(hp[(size_t)(2 * i) * D], hp[(size_t)(2 * i + 1) * D]);
+    }
     const T* cp = static_cast<const T*>(a.conv) + (size_t)rb[r] * 3 * D + d;
     xm3[r] = Act<T>::ld(cp);
     xm2[r] = Act<T>::ld(cp + D);
@@ -242,6 +261,20 @@ __global__ void __launch_bounds__(GD) m3_decode_kernel(DecArgs a) {
     for (int i = 0; i < 8; ++i) {
       sA[i][tid][0] = -expf(al[2 * i]) * LOG2E;
       sA[i][tid][1] = -expf(al[2 * i + 1]) * LOG2E;
+    }
+  }
+  if constexpr (TL) {
+    const bool landed = !misaligned && mbar_wait(&tbar, 0);
+    if (__syncthreads_or(!landed)) {
+      if (tid == 0) atomicOr(&g_aux_status, 1u);
+      return;
+    }
+    const float* hs = reinterpret_cast<const float*>(dsm) + tid / G;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        h[r][i] = make_float2(hs[((size_t)r * N + 16 * q + 2 * i) * CH], hs[((size_t)r * N + 16 * q + 2 * i + 1) * CH]);
     }
   }
 
@@ -312,10 +345,22 @@ __global__ void __launch_bounds__(GD) m3_decode_kernel(DecArgs a) {
 }
 
 template <typename T, int N, int R>
-cudaError_t launch_decode_r(const DecArgs& a, cudaStream_t st) {
+cudaError_t launch_decode_r(const DecArgs& a0, cudaStream_t st) {
   constexpr int CH = GD / (N / 16);
-  m3_decode_kernel<T, N, R>
-      <<<dim3((unsigned)((a.D + CH - 1) / CH), (unsigned)((a.B + R - 1) / R)), GD, 0, st>>>(a);
+  const dim3 grid((unsigned)((a0.D + CH - 1) / CH), (unsigned)((a0.B + R - 1) / R));
+  // the carried states by tile copies when their layout allows one and the
+  // state is wide (measured: faster for d_state 32 and 64, slower for 16,
+  // where each thread's own loads already keep enough bytes in flight)
+  if (N >= 32 && reinterpret_cast<uintptr_t>(a0.h) % 16 == 0 && a0.D % 4 == 0) {
+    DecArgs a = a0;
+    const uint64_t dim[3] = {(uint64_t)a.D, (uint64_t)N, (uint64_t)a.B};
+    const uint64_t str[2] = {(uint64_t)a.D * 4, (uint64_t)N * a.D * 4};
+    const uint32_t box[3] = {(uint32_t)CH, (uint32_t)N, (uint32_t)R};
+    if (!encode_tile_map(&a.tm_h, 4, 3, a.h, dim, str, box)) return cudaErrorInvalidValue;
+    m3_decode_kernel<T, N, R, true><<<grid, GD, (size_t)R * N * CH * 4, st>>>(a);
+  } else {
+    m3_decode_kernel<T, N, R, false><<<grid, GD, 0, st>>>(a0);
+  }
   return cudaGetLastError();
 }
 

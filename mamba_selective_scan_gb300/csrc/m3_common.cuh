@@ -538,6 +538,9 @@ struct DecArgs {
   float* h;    // [B, N, D] f32, in and out
   void* conv;  // [B, 3, D] act, in and out
   void *gated, *y_dbg;
+  // tile map of h (boxes of the block's channels x N lanes x its batch rows),
+  // used when h is 16-byte aligned and d_inner a multiple of 4
+  CUtensorMap tm_h;
 };
 
 constexpr int GD = 128;  // decode: channels (= threads) per block
