@@ -644,6 +644,7 @@ def extras(torch, binding, device, args, flush, stream):
     if not args.no_stack:
         out["m2p8b_stack24"] = stack24(torch, binding, device, args, stream)
     out["decode"] = decode_extras(torch, binding, device, flush)
+    out["conv_bwd"] = conv_bwd_extras(torch, binding, device, flush)
     return out
 
 
@@ -701,6 +702,49 @@ def decode_extras(torch, binding, device, flush, steps=20):
         out[f"b{B}_d{D}_n{N}"] = {"us_per_token_step": round(ms * 1e3, 2), "gbs": round(gbs, 1),
                                   "frac_of_hbm": round(gbs / peak, 3), "hbm_peak_kind": kind,
                                   "bytes": int(byt)}
+    return out
+
+
+def conv_bwd_extras(torch, binding, device, flush, steps=20):
+    """The second call of the two-phase backward (m3scan_conv_bwd: SiLU and
+    conv backward from du plus an extra input gradient) on the large
+    workloads: its own launches, L2 flushed before each.  Bytes: x, du and
+    du_extra read, d_x written (activation dtype), the parameter partials."""
+    out = {}
+    for name in ("m130m_b8_t2048_d1536", "m2p8b_b4_t4096_d5120"):
+        w = WORKLOADS[name]
+        t = device_inputs(torch, w, device)
+        Bsz, T, D = t["x"].shape
+        es = 2 if w.act == "bf16" else 4
+        act = binding.M3_BF16 if es == 2 else binding.M3_F32
+        dims = binding.make_dims(Bsz, T, D)
+        pl = binding.m3scan_plan(dims, act)
+        ws = binding.Workspace(pl.workspace_bytes, device)
+        du, due, dx = torch.randn_like(t["x"]), torch.randn_like(t["x"]), torch.empty_like(t["x"])
+        dw = torch.empty(D, 4, device=device)
+        db = torch.empty(D, device=device)
+        s = torch.cuda.current_stream()
+        args = (dims, act, t["x"].data_ptr(), t["conv_w"].data_ptr(), t["conv_b"].data_ptr(),
+                du.data_ptr(), due.data_ptr(), dx.data_ptr(), dw.data_ptr(), db.data_ptr(), None,
+                ws.ptr, ws.nbytes, s.cuda_stream)
+        for _ in range(3):
+            assert binding.raw_conv_bwd(*args) == 0
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        for e0, e1 in ev:
+            flush.zero_()
+            e0.record(s)
+            binding.raw_conv_bwd(*args)
+            e1.record(s)
+        torch.cuda.synchronize()
+        ms = sorted(e0.elapsed_time(e1) for e0, e1 in ev)[steps // 2]
+        byt = Bsz * T * D * 4 * es
+        peak, kind = measured_peaks()
+        gbs = byt / (ms * 1e-3) / 1e9
+        out[name] = {"us": round(ms * 1e3, 1), "gbs": round(gbs, 1), "frac_of_hbm": round(gbs / peak, 3),
+                     "hbm_peak_kind": kind, "bytes": int(byt)}
+        del t, du, due, dx, ws
+        torch.cuda.empty_cache()
     return out
 
 
@@ -827,6 +871,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--decode-only", action="store_true",
                     help="run only the one-token decode measurements (for profiling)")
+    ap.add_argument("--conv-only", action="store_true",
+                    help="run only the two-phase conv-backward measurements (for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -837,6 +883,14 @@ def main():
         dev = torch.device("cuda", 0)
         flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
         print(json.dumps({"decode": decode_extras(torch, binding, dev, flush, steps=args.steps)}))
+        return
+    if args.conv_only:
+        import torch
+        from mamba_selective_scan_gb300 import binding, build
+        build.build()
+        dev = torch.device("cuda", 0)
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        print(json.dumps({"conv_bwd": conv_bwd_extras(torch, binding, dev, flush, steps=args.steps)}))
         return
     if args.impl == "reference":
         reference_arm(args)

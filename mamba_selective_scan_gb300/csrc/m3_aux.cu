@@ -67,69 +67,80 @@ __global__ void __launch_bounds__(128) m3_conv_bwd_kernel(const __grid_constant_
     const T* ci = static_cast<const T*>(a.conv_in) + (size_t)b * 3 * D + d;
     for (int r = 0; r < 3 - t0; ++r) xs[r * 128 + tid] = ci[(size_t)(t0 + r) * D];
   }
-  // dc of steps t0 .. t1 + 2 (zero from step T on), then d_x of the tile
-  float dcs[CT + 3];
-  float dcb = 0.f, dcw[WC] = {0.f, 0.f, 0.f, 0.f};
+  // A tile whose steps and three look-ahead steps all lie inside the
+  // sequence (every tile but the last one or two) runs without bounds checks.
+  auto run = [&](auto full_tag) {
+    constexpr bool FULL = decltype(full_tag)::value;
+    // dc of steps t0 .. t1 + 2 (zero from step T on), then d_x of the tile
+    float dcs[CT + 3];
+    float dcb = 0.f, dcw[WC] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-  for (int j = 0; j < CT + 3; ++j) {
-    const int t = t0 + j;
-    float dc = 0.f;
-    if (t < a.T) {
-      const float xm3 = Act<T>::ld(xs + j * 128 + tid);
-      const float xm2 = Act<T>::ld(xs + (j + 1) * 128 + tid);
-      const float xm1 = Act<T>::ld(xs + (j + 2) * 128 + tid);
-      const float xv = Act<T>::ld(xs + (j + 3) * 128 + tid);
-      float gu = Act<T>::ld(us + j * 128 + tid);
-      if (a.du_extra) gu += Act<T>::ld(es + j * 128 + tid);
-      const float c = fmaf(w[0], xm3, fmaf(w[1], xm2, fmaf(w[2], xm1, fmaf(w[3], xv, cb))));
-      const float sc = sigmoid_f(c);
-      dc = gu * (sc * fmaf(c, 1.f - sc, 1.f));
-      if (j < CT && t < t1) {
-        dcb += dc;
-        dcw[0] = fmaf(dc, xm3, dcw[0]);
-        dcw[1] = fmaf(dc, xm2, dcw[1]);
-        dcw[2] = fmaf(dc, xm1, dcw[2]);
-        dcw[3] = fmaf(dc, xv, dcw[3]);
+    for (int j = 0; j < CT + 3; ++j) {
+      const int t = t0 + j;
+      float dc = 0.f;
+      if (FULL || t < a.T) {
+        const float xm3 = Act<T>::ld(xs + j * 128 + tid);
+        const float xm2 = Act<T>::ld(xs + (j + 1) * 128 + tid);
+        const float xm1 = Act<T>::ld(xs + (j + 2) * 128 + tid);
+        const float xv = Act<T>::ld(xs + (j + 3) * 128 + tid);
+        float gu = Act<T>::ld(us + j * 128 + tid);
+        if (a.du_extra) gu += Act<T>::ld(es + j * 128 + tid);
+        const float c = fmaf(w[0], xm3, fmaf(w[1], xm2, fmaf(w[2], xm1, fmaf(w[3], xv, cb))));
+        const float sc = sigmoid_f(c);
+        dc = gu * (sc * fmaf(c, 1.f - sc, 1.f));
+        if (j < CT && (FULL || t < t1)) {
+          dcb += dc;
+          dcw[0] = fmaf(dc, xm3, dcw[0]);
+          dcw[1] = fmaf(dc, xm2, dcw[1]);
+          dcw[2] = fmaf(dc, xm1, dcw[2]);
+          dcw[3] = fmaf(dc, xv, dcw[3]);
+        }
+      }
+      dcs[j] = dc;
+    }
+    T* const dxp = static_cast<T*>(a.dx) + ((size_t)b * a.T + t0) * D + d;
+#pragma unroll
+    for (int j = 0; j < CT; ++j) {
+      const int t = t0 + j;
+      if (FULL || t < t1) {
+        float v = fmaf(dcs[j], w[3], fmaf(dcs[j + 1], w[2], fmaf(dcs[j + 2], w[1], dcs[j + 3] * w[0])));
+        if (!FULL && a.g_conv && t >= a.T - 3)  // x[t] is also a conv-state output
+          v += Act<T>::ld(static_cast<const T*>(a.g_conv) + ((size_t)b * 3 + t - (a.T - 3)) * D + d);
+        Act<T>::st(dxp + (size_t)j * D, v);
       }
     }
-    dcs[j] = dc;
-  }
+    if (tile == 0 && a.d_conv_in) {
+      // conv inputs of steps -3, -2, -1 (rows 0..2) reach dc of steps 0..2
+      float v[3];
+      v[0] = dcs[0] * w[0];
+      v[1] = fmaf(dcs[1], w[0], dcs[0] * w[1]);
+      v[2] = fmaf(dcs[2], w[0], fmaf(dcs[1], w[1], dcs[0] * w[2]));
+      T* dci = static_cast<T*>(a.d_conv_in) + (size_t)b * 3 * D + d;
 #pragma unroll
-  for (int j = 0; j < CT; ++j) {
-    const int t = t0 + j;
-    if (t < t1) {
-      float v = fmaf(dcs[j], w[3], fmaf(dcs[j + 1], w[2], fmaf(dcs[j + 2], w[1], dcs[j + 3] * w[0])));
-      if (a.g_conv && t >= a.T - 3)  // x[t] is also a conv-state output
-        v += Act<T>::ld(static_cast<const T*>(a.g_conv) + ((size_t)b * 3 + t - (a.T - 3)) * D + d);
-      Act<T>::st(static_cast<T*>(a.dx) + ((size_t)b * a.T + t) * D + d, v);
+      for (int r = 0; r < 3; ++r) {
+        const int ro = r - a.T;  // row of the conv-state output holding step r - 3
+        if (a.g_conv && ro >= 0)
+          v[r] += Act<T>::ld(static_cast<const T*>(a.g_conv) + ((size_t)b * 3 + ro) * D + d);
+        Act<T>::st(dci + (size_t)r * D, v[r]);
+      }
     }
-  }
-  if (tile == 0 && a.d_conv_in) {
-    // conv inputs of steps -3, -2, -1 (rows 0..2) reach dc of steps 0..2
-    float v[3];
-    v[0] = dcs[0] * w[0];
-    v[1] = fmaf(dcs[1], w[0], dcs[0] * w[1]);
-    v[2] = fmaf(dcs[2], w[0], fmaf(dcs[1], w[1], dcs[0] * w[2]));
-    T* dci = static_cast<T*>(a.d_conv_in) + (size_t)b * 3 * D + d;
+    float* P = a.part + ((size_t)b * a.ntiles + tile) * 5 * D + d;
+    P[0] = dcb;
 #pragma unroll
-    for (int r = 0; r < 3; ++r) {
-      const int ro = r - a.T;  // row of the conv-state output holding step r - 3
-      if (a.g_conv && ro >= 0)
-        v[r] += Act<T>::ld(static_cast<const T*>(a.g_conv) + ((size_t)b * 3 + ro) * D + d);
-      Act<T>::st(dci + (size_t)r * D, v[r]);
-    }
-  }
-  float* P = a.part + ((size_t)b * a.ntiles + tile) * 5 * D + d;
-  P[0] = dcb;
-#pragma unroll
-  for (int k = 0; k < WC; ++k) P[(size_t)(1 + k) * D] = dcw[k];
+    for (int k = 0; k < WC; ++k) P[(size_t)(1 + k) * D] = dcw[k];
+  };
+  if (t0 + CT + 3 <= a.T)
+    run(std::true_type{});
+  else
+    run(std::false_type{});
 }
 
 // d_conv_b and d_conv_w from the per-(batch, tile) partials, summed in a
-// fixed order (32 outputs per block, rows split over 8 warps).
+// fixed order (32 outputs per block, rows split over 16 warps, so enough
+// loads are in flight to keep this short kernel off the latency floor).
 __global__ void m3_conv_fin_kernel(ConvArgs a) {
   grid_dep_wait();  // the conv backward's partials
-  __shared__ float part[8][33];
+  __shared__ float part[16][33];
   const int cx = threadIdx.x & 31, ry = threadIdx.x >> 5;
   const int oidx = blockIdx.x * 32 + cx;
   const bool ok = oidx < 5 * a.D;
@@ -142,9 +153,9 @@ __global__ void m3_conv_fin_kernel(ConvArgs a) {
     float v1 = 0.f;
     int r = ry;
 #pragma unroll 4
-    for (; r + 8 < rows; r += 16) {
+    for (; r + 16 < rows; r += 32) {
       v0 += P[(size_t)r * stride];
-      v1 += P[(size_t)(r + 8) * stride];
+      v1 += P[(size_t)(r + 16) * stride];
     }
     if (r < rows) v0 += P[(size_t)r * stride];
     v0 += v1;
@@ -152,8 +163,10 @@ __global__ void m3_conv_fin_kernel(ConvArgs a) {
   part[ry][cx] = v0;
   __syncthreads();
   if (ry != 0 || !ok) return;
-  const float v = ((part[0][cx] + part[1][cx]) + (part[2][cx] + part[3][cx])) +
-                  ((part[4][cx] + part[5][cx]) + (part[6][cx] + part[7][cx]));
+  float v = 0.f;
+#pragma unroll
+  for (int k = 0; k < 16; k += 4)
+    v += (part[k][cx] + part[k + 1][cx]) + (part[k + 2][cx] + part[k + 3][cx]);
   float* dst = j == 0 ? a.d_conv_b + d : a.d_conv_w + (size_t)d * WC + (j - 1);
   *dst = a.accumulate ? *dst + v : v;
 }
@@ -392,7 +405,7 @@ cudaError_t launch_conv_bwd(ConvArgs a, dim3 grid, cudaStream_t s) {
     return cudaErrorInvalidValue;
   cudaError_t e = launch_k(m3_conv_bwd_kernel<T>, grid, 128, conv_smem(sizeof(T)).total, s, false, a);
   if (e == cudaSuccess)
-    e = launch_k(m3_conv_fin_kernel, dim3((unsigned)((5 * (size_t)a.D + 31) / 32)), 256, 0, s, true, a);
+    e = launch_k(m3_conv_fin_kernel, dim3((unsigned)((5 * (size_t)a.D + 31) / 32)), 512, 0, s, true, a);
   return e;
 }
 
