@@ -89,13 +89,19 @@ def alu_peak_gops():
     return GB300_SMS * FP32_LANES_PER_SM * mhz * 1e6 / 1e9
 
 
+# The translation units whose kernels (and launch logic) the forward and
+# backward calls run; the decode and conv-backward unit is not among them.
+SCAN_SOURCES = ("m3_api.cu", "m3_bwd.cu", "m3_bwd2.cu", "m3_common.cuh", "m3_fwd.cu")
+
+
 def source_hash():
+    """Hash of the forward/backward kernel sources the ncu traffic figures
+    were taken on."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "mamba_selective_scan_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(f.read())
+    for name in SCAN_SOURCES:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
     return h.hexdigest()[:16]
 
 
