@@ -102,14 +102,19 @@ typedef struct {
        columns of each row are read or written. */
     int64_t bc_stride;
     int64_t dbc_stride;
-    /* dB and dC are sums over all channels.  0: each block of channels adds
-       its share with float atomics (fastest; the order of the additions,
-       and so the last bits, may differ between runs).  1: each block writes
-       its share to the workspace and the backward's last kernel adds the
-       blocks in a fixed order, so repeated calls give identical bits (every
-       other output is deterministic either way).  The workspace then also
-       holds batch * seq_len * 2 * d_state floats per channel block. */
-    int32_t deterministic_dbc;
+    /* dB and dC are sums over all channels, the parameter gradients
+       (d_a_log, dD, d_dt_bias, d_conv_w, d_conv_b) sums over batch and
+       time.  0: blocks add their shares of dB and dC with float atomics,
+       and so do the clusters of the split backward over 2-8 time segments
+       for the parameter gradients (fastest; the order of the additions, and
+       so the last bits of these outputs, may differ between runs).  1: every
+       block writes its shares to the workspace and the backward's last
+       kernels add them in a fixed order, so repeated calls give identical
+       bits for every output.  The workspace then also holds
+       batch * seq_len * 2 * d_state floats per channel block and the
+       per-(batch, segment) parameter partials.  d_x, d_delta_raw, dz and du
+       are the same bits either way. */
+    int32_t deterministic;
     int32_t reserved0;  /* must be 0 */
 } m3_dims;
 

@@ -53,7 +53,7 @@ class M3Dims(ctypes.Structure):
                 ("accumulate_param_grads", ctypes.c_int32),
                 ("threads_per_channel", ctypes.c_int32),
                 ("bc_stride", ctypes.c_int64), ("dbc_stride", ctypes.c_int64),
-                ("deterministic_dbc", ctypes.c_int32), ("reserved0", ctypes.c_int32)]
+                ("deterministic", ctypes.c_int32), ("reserved0", ctypes.c_int32)]
 
 
 class M3Plan(ctypes.Structure):
@@ -160,11 +160,11 @@ def load():
 
 def make_dims(batch, seq_len, d_inner, d_state=16, d_conv=4, chunk=0, segments=0,
               accumulate_param_grads=False, bc_stride=0, dbc_stride=0,
-              threads_per_channel=0, deterministic_dbc=False) -> M3Dims:
+              threads_per_channel=0, deterministic=False) -> M3Dims:
     return M3Dims(int(batch), int(seq_len), int(d_inner), int(d_state), int(d_conv),
                   int(chunk), int(segments), int(bool(accumulate_param_grads)),
                   int(threads_per_channel), int(bc_stride), int(dbc_stride),
-                  int(bool(deterministic_dbc)), 0)
+                  int(bool(deterministic)), 0)
 
 
 def m3scan_plan(dims: M3Dims, act: int) -> M3Plan:
@@ -416,17 +416,17 @@ def _fwd(x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D, chunk, segm
 
 def m3scan_bwd(x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D, ckpt, d_gated, *,
                chunk=0, segments=0, want_du=False, accumulate_param_grads=False, out=None,
-               workspace=None, stream=None, threads_per_channel=0, deterministic_dbc=False):
+               workspace=None, stream=None, threads_per_channel=0, deterministic=False):
     """Backward of the layer core.  Returns a dict of gradients (tensors)."""
     return _bwd(x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D, ckpt, d_gated,
                 chunk, segments, want_du, accumulate_param_grads, out, workspace, stream, None,
-                threads_per_channel, deterministic_dbc)
+                threads_per_channel, deterministic)
 
 
 def m3scan_bwd_state(x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D, ckpt, d_gated,
                      *, conv_state=None, d_ssm_state_out=None, d_conv_state_out=None, chunk=0,
                      segments=0, want_du=False, accumulate_param_grads=False, out=None,
-                     workspace=None, stream=None, threads_per_channel=0, deterministic_dbc=False):
+                     workspace=None, stream=None, threads_per_channel=0, deterministic=False):
     """Backward of one window made by ``m3scan_fwd_state``.  Returns the
     gradients of ``m3scan_bwd`` plus ``d_ssm_state`` [B,16,D] f32 and
     ``d_conv_state`` [B,3,D] (activation dtype)."""
@@ -445,7 +445,7 @@ def m3scan_bwd_state(x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D,
                     _ptr(o["d_ssm_state"]), _ptr(o["d_conv_state"]))
     return _bwd(x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D, ckpt, d_gated,
                 chunk, segments, want_du, accumulate_param_grads, o, workspace, stream, st,
-                threads_per_channel, deterministic_dbc)
+                threads_per_channel, deterministic)
 
 
 def _bwd(x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D, ckpt, d_gated, chunk,
@@ -465,7 +465,7 @@ def _bwd(x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D, ckpt, d_gat
     W = conv_w.shape[-1]
     dims = make_dims(Bsz, T, Dn, d_state=N, d_conv=W, chunk=chunk, segments=segments,
                      accumulate_param_grads=accumulate_param_grads, threads_per_channel=tpc,
-                     deterministic_dbc=det)
+                     deterministic=det)
     code = _act_code(x)
     pl = m3scan_plan(dims, code)
     o = dict(out or {})
@@ -534,7 +534,7 @@ def m3scan_bwd_two_phase(x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log
                          d_gated, du_extra_fn=None, *, conv_state=None, d_ssm_state_out=None,
                          d_conv_state_out=None, chunk=0, segments=0, bc_stride=0, dbc_stride=0,
                          dB=None, dC=None, accumulate_param_grads=False, stream=None,
-                         threads_per_channel=0, deterministic_dbc=False):
+                         threads_per_channel=0, deterministic=False):
     """The two-phase backward: m3scan_bwd_scan, then ``du_extra_fn(grads)``
     (the caller's x_proj/dt_proj GEMMs, given the scan's gradients; may
     return None), then m3scan_conv_bwd.  ``Bm``/``Cm`` may be column views
@@ -550,7 +550,7 @@ def m3scan_bwd_two_phase(x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log
     dims = make_dims(Bsz, T, Dn, d_state=N, d_conv=W, chunk=chunk, segments=segments,
                      accumulate_param_grads=accumulate_param_grads, bc_stride=bc_stride,
                      dbc_stride=dbc_stride, threads_per_channel=threads_per_channel,
-                     deterministic_dbc=deterministic_dbc)
+                     deterministic=deterministic)
     code = _act_code(x)
     pl = m3scan_plan(dims, code)
     ws = Workspace(pl.workspace_bytes, dev)

@@ -21,8 +21,11 @@
 // earlier segments' aggregates to its true start state.  The backward does
 // the same in reverse time for the adjoint state.  dB and dC are sums over
 // channels (warp shuffles, shared memory, one f32 global reduction per
-// (t, n) per block); parameter gradients are per-(batch, segment) partials
-// summed in a fixed order (deterministic).
+// (t, n) per block).  Parameter gradients: the split main kernel over
+// several segments adds each block's sums into the outputs with f32
+// reductions; otherwise (and always when deterministic sums are asked for)
+// they are per-(batch, segment) partials that a tail kernel sums in a fixed
+// order.
 
 #include <mutex>
 
@@ -231,7 +234,7 @@ m3_status validate_dims(const m3_dims* dm, m3_dtype act) {
   if (dm->dbc_stride != 0 && dm->dbc_stride < dm->d_state) return M3_ERR_DIMS;
   if (dm->bc_stride * (act == M3_BF16 ? 2 : 4) % 16 != 0) return M3_ERR_ALIGN;
   if (dm->threads_per_channel < 0 || dm->threads_per_channel > 2) return M3_ERR_UNSUPPORTED;
-  if (dm->deterministic_dbc != 0 && dm->deterministic_dbc != 1) return M3_ERR_DIMS;
+  if (dm->deterministic != 0 && dm->deterministic != 1) return M3_ERR_DIMS;
   if (dm->reserved0 != 0) return M3_ERR_DIMS;
   return M3_OK;
 }
@@ -319,7 +322,11 @@ m3_status make_plan(const m3_dims* dm, m3_dtype act, Plan* p) {
   size_t fwd_total = off;
   // backward section (reuses the same bytes)
   off = 0;
-  p->b_part = take(B * p->Sb * (N + 8) * D * 4);
+  p->det = dm->deterministic != 0;
+  p->fin = !p->det && p->bwd_tpc != 1 && p->Sb > 1 && p->Sb <= FIN_MAX;
+  // per-(batch, segment) parameter partials, unless the main kernel adds
+  // its sums into the outputs
+  p->b_part = p->fin ? 0 : take(B * p->Sb * (N + 8) * D * 4);
   p->b_q = p->b_sd = p->b_dxpart = p->b_dchead = 0;
   if (p->Sb > 1) {
     p->b_q = take(B * p->Sb * N * D * 4);
@@ -329,7 +336,6 @@ m3_status make_plan(const m3_dims* dm, m3_dtype act, Plan* p) {
   }
   // deterministic dB/dC: one partial row of 2N floats per (batch, step,
   // channel block of the backward's main kernel)
-  p->det = dm->deterministic_dbc != 0;
   p->dblk = (p->D + (p->bwd_tpc != 1 ? 128 / p->bwd_tpc : GB) - 1) / (p->bwd_tpc != 1 ? 128 / p->bwd_tpc : GB);
   p->b_dbc = p->det ? take(B * (size_t)p->T * p->dblk * 2 * N * 4) : 0;
   size_t bwd_total = off;
@@ -343,7 +349,7 @@ m3_status make_plan(const m3_dims* dm, m3_dtype act, Plan* p) {
   p->ws_bytes = fwd_total > bwd_total ? fwd_total : bwd_total;
   if (p->ws_bytes < 256) p->ws_bytes = 256;
   p->fwd_launches = empty ? 0 : (p->Sf > 1 ? 2 : 1);
-  p->bwd_launches = empty ? 0 : (p->Sb > 1 ? 3 : 2) + (p->det ? 1 : 0);
+  p->bwd_launches = empty ? 0 : (p->Sb > 1 ? 2 : 1) + (p->fin ? 0 : 1) + (p->det ? 1 : 0);
   return M3_OK;
 }
 
@@ -552,8 +558,10 @@ m3_status bwd_impl(const m3_dims* dims, m3_dtype act, const void* x, const void*
     a.dxpart = reinterpret_cast<float*>(ws + p.b_dxpart);
     a.dchead = reinterpret_cast<float*>(ws + p.b_dchead);
   }
-  a.d_conv_w = d_conv_w; a.d_conv_b = d_conv_b; a.d_dt_bias = d_dt_bias; a.d_a_log = d_a_log;
-  a.dD = dD;
+  a.fin = p.fin ? 1 : 0;
+  // stopping at du leaves the conv parameters' grads alone
+  a.d_conv_w = scan ? nullptr : d_conv_w; a.d_conv_b = scan ? nullptr : d_conv_b;
+  a.d_dt_bias = d_dt_bias; a.d_a_log = d_a_log; a.dD = dD;
   a.accumulate = dims->accumulate_param_grads ? 1 : 0;
   a.conv_in = sv.conv_state; a.g_h = sv.d_ssm_state_out; a.g_conv = sv.d_conv_state_out;
   a.d_h_in = sv.d_ssm_state; a.d_conv_in = sv.d_conv_state;

@@ -120,6 +120,17 @@ __global__ void __launch_bounds__(GB) m3_bwd_agg_kernel(const __grid_constant__ 
       a.dB[o] = 0.f;
       a.dC[o] = 0.f;
     }
+    if (a.fin && !a.accumulate) {
+      // the main kernel adds its parameter sums into the outputs
+      for (size_t i = cid * GB + tid; i < (size_t)g.D * N; i += ncta * GB) a.d_a_log[i] = 0.f;
+      for (size_t i = cid * GB + tid; i < (size_t)g.D; i += ncta * GB) {
+        a.dD[i] = 0.f;
+        a.d_dt_bias[i] = 0.f;
+        if (a.d_conv_b) a.d_conv_b[i] = 0.f;
+      }
+      if (a.d_conv_w)
+        for (size_t i = cid * GB + tid; i < (size_t)g.D * WC; i += ncta * GB) a.d_conv_w[i] = 0.f;
+    }
   }
   for (int i = 0; i < ntiles; ++i) {
     const int buf = i & 1;
@@ -776,7 +787,9 @@ m3_status launch_bwd(const Plan& p, BwdArgs a, cudaStream_t st, int smem_per_sm,
     const size_t smem = bwd2_launch_smem(p.K, sizeof(T), p.N, smem_per_sm);
     void (*kern)(BwdArgs) = bwd2_kernel_for<T>(p.det, scan, with_state, p.N);
     const int ch = 128 / (p.N / 8);
-    e = launch_k(kern, dim3((p.D + ch - 1) / ch, p.Sb, p.B), 128, smem, st, p.Sb > 1, a);
+    const dim3 grid((p.D + ch - 1) / ch, p.Sb, p.B);
+    e = a.fin ? launch_k_cluster_y(kern, grid, 128, smem, st, true, (unsigned)p.Sb, a)
+              : launch_k(kern, grid, 128, smem, st, p.Sb > 1, a);
   } else {
     a.tcols = tmem_cols_for(p.K);
     const size_t smem = bwd_launch_smem(p.K, sizeof(T), smem_per_sm);
@@ -789,7 +802,7 @@ m3_status launch_bwd(const Plan& p, BwdArgs a, cudaStream_t st, int smem_per_sm,
   const size_t nfin = ((size_t)nout * p.D + 31) / 32;                 // 32 outputs per block
   const size_t nfix = (!scan && p.Sb > 1) ? ((size_t)p.B * (p.Sb - 1) * 3 * p.D + 255) / 256 : 0;
   const size_t ndbc = p.det ? ((size_t)p.B * p.T * 2 * p.N + 255) / 256 : 0;
-  if (e == cudaSuccess) {
+  if (e == cudaSuccess && !a.fin) {
     TailArgs ta;
     ta.g = a.g;
     ta.partials = a.partials; ta.dxpart = a.dxpart; ta.dchead = a.dchead;

@@ -440,7 +440,27 @@ __global__ void __launch_bounds__(128, 4) m3_bwd2_kernel(const __grid_constant__
   #pragma unroll
       for (int k = 0; k < WC; ++k) dcw[k] += __shfl_xor_sync(0xffffffffu, dcw[k], o);
     }
-    if (active) {
+    if (!DET && a.fin) {
+      // this block's sums, staged in the outputs' layout (d_a_log [CH][N],
+      // d_conv_w [CH][4], then dD, d_dt_bias, d_conv_b [CH] each) in its tile
+      // buffers, idle now, for the cluster's sum over the segments below
+      float* sA = reinterpret_cast<float*>(smem);
+      float* sW = sA + CH * N;
+      float* sV = sW + CH * WC;
+  #pragma unroll
+      for (int P = 0; P < 4; ++P) {
+        const int n = lane_of(P);  // dL/da_log = dL/dA * A, A = (A log2 e) ln 2
+        sA[ch * N + n] = dAp[P].x * (a2[P].x * LN2);
+        sA[ch * N + n + 1] = dAp[P].y * (a2[P].y * LN2);
+      }
+      if (hf == 0) {
+  #pragma unroll
+        for (int k = 0; k < WC; ++k) sW[ch * WC + k] = dcw[k];
+        sV[ch] = dD_acc;
+        sV[CH + ch] = ddtb_acc;
+        sV[2 * CH + ch] = dcb_acc;
+      }
+    } else if (active) {
       float* Pp = a.partials + ((size_t)b * g.S + s) * NP * g.D;
   #pragma unroll
       for (int P = 0; P < 4; ++P) {
@@ -455,6 +475,81 @@ __global__ void __launch_bounds__(128, 4) m3_bwd2_kernel(const __grid_constant__
   #pragma unroll
         for (int k = 0; k < WC; ++k) Pp[(size_t)(N + 3 + k) * g.D + d] = dcw[k];
       }
+    }
+  }
+  if constexpr (!DET) {
+    if (a.fin) {
+      // The S segments of this (channel block, batch) are one cluster; every
+      // block passes both cluster barriers, aborted or not.
+      cluster_sync_all();
+      if (!aborted) {
+        if constexpr (!SCAN) {
+          // d_x at the last three steps of this segment: its own partial rows
+          // plus the conv-input gradient of the next segment's first three
+          // steps, written by the next block before the barrier
+          if (s + 1 < g.S) {
+            for (int i = tid; i < 3 * CH; i += 128) {
+              const int j = i / CH, dd = d0 + i % CH;
+              if (dd >= g.D) continue;
+              const int t = t_end - 3 + j;
+              float v = __ldcg(a.dxpart + (((size_t)b * g.S + s) * 3 + j) * g.D + dd);
+  #pragma unroll
+              for (int k = 0; k < WC; ++k) {
+                const int tp = t + 3 - k;
+                if (tp >= t_end && tp < g.T)
+                  v = fmaf(__ldcg(a.dchead + (((size_t)b * g.S + s + 1) * 3 + (tp - t_end)) * g.D + dd),
+                           a.conv_w[(size_t)dd * WC + k], v);
+              }
+              Act<T>::st(static_cast<T*>(a.dx) + ((size_t)b * g.T + t) * g.D + dd, v);
+            }
+          }
+        }
+        // parameter sums: four consecutive staged values per thread, summed
+        // over the cluster's blocks in segment order, then added to the
+        // outputs (one float4 atomic where the four are in range and 16-byte
+        // aligned); block s takes every S-th group of 128 quads
+        constexpr int U = CH * (N + 7) / 4;
+        const int nch = min(CH, g.D - d0);
+        const uint32_t sbase = smem_u32(smem);
+        for (int u = s * 128 + tid; u < U; u += g.S * 128) {
+          float4 v = ld_cluster_f4(cluster_addr(sbase + 16u * u, 0));
+          for (int r = 1; r < g.S; ++r) {
+            const float4 w4 = ld_cluster_f4(cluster_addr(sbase + 16u * u, r));
+            v.x += w4.x;
+            v.y += w4.y;
+            v.z += w4.z;
+            v.w += w4.w;
+          }
+          const int i = 4 * u;
+          float* dst;
+          int idx, lim;
+          if (i < CH * N) {
+            dst = a.d_a_log + (size_t)d0 * N;
+            idx = i;
+            lim = nch * N;
+          } else if (i < CH * (N + WC)) {
+            if (SCAN) continue;
+            dst = a.d_conv_w + (size_t)d0 * WC;
+            idx = i - CH * N;
+            lim = nch * WC;
+          } else {
+            const int jv = i - CH * (N + WC), q = jv / CH;
+            if (SCAN && q == 2) continue;
+            dst = (q == 0 ? a.dD : q == 1 ? a.d_dt_bias : a.d_conv_b) + d0;
+            idx = jv - q * CH;
+            lim = nch;
+          }
+          if (idx + 4 <= lim && (reinterpret_cast<uintptr_t>(dst + idx) & 15u) == 0) {
+            atomicAdd(reinterpret_cast<float4*>(dst + idx), v);
+          } else {
+            const float e4[4] = {v.x, v.y, v.z, v.w};
+  #pragma unroll
+            for (int e = 0; e < 4; ++e)
+              if (idx + e < lim) atomicAdd(dst + idx + e, e4[e]);
+          }
+        }
+      }
+      cluster_sync_relaxed();  // no block leaves while the others may read its staging
     }
   }
   tmem_fence_before_sync();

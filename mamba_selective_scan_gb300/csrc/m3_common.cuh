@@ -205,6 +205,31 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
+// Thread-block cluster: a barrier over every thread of every block in the
+// cluster (the release / acquire halves order shared and global memory
+// writes before it against reads after it), and loads from another block's
+// shared memory at the same offset.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// The same without the release half: for a barrier whose only job is that
+// no block leaves before the others have used the values they loaded from
+// its shared memory (a load whose value was consumed has completed).
+__device__ __forceinline__ void cluster_sync_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_addr(uint32_t smem_addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float4 ld_cluster_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr) : "memory");
+  return v;
+}
+
 // Stage rows [t_first, t_first + rows) x channels [d0, d0 + G) of a
 // [B, T_, D] tensor of element type T into dst[rows][G]; rows outside
 // [0, t_limit) and channels >= D read as zero.  NT threads cooperate.
@@ -333,6 +358,11 @@ struct BwdArgs {
   // [B * T][nblk][2N], summed by the tail kernel; NULL: float atomics
   float* dbc_part;
   int nblk;
+  // 1: the split main kernel runs with the S segments of a (channel block,
+  // batch) as one thread-block cluster, which sums its parameter shares over
+  // the segments and adds them into the outputs (cleared by the aggregate
+  // kernel unless accumulating) and finishes d_x at the segment boundaries
+  int fin;
   // tile maps of the backward's staging (see TM_* below)
   CUtensorMap tm[11];
 };
@@ -612,10 +642,15 @@ struct Plan {
   size_t c_part;
   int fwd_launches, bwd_launches;
   int fwd_tpc, bwd_tpc;  // threads per channel in the forward's and backward's main kernels
-  bool det;              // dB/dC by fixed-order sums of per-block partials
+  bool det;              // dB/dC and parameter grads by fixed-order sums of per-block partials
   int dblk;              // channel blocks of the backward's main kernel
   size_t b_dbc;          // workspace offset of those partials [B * T][dblk][2N]
+  // the split backward over 2..FIN_MAX segments, not deterministic: the
+  // segments of a channel block form a cluster that finishes the parameter
+  // gradients and d_x at the boundaries itself (no tail kernel)
+  bool fin;
 };
+constexpr int FIN_MAX = 8;  // portable cluster size
 
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -639,6 +674,26 @@ cudaError_t launch_k(void (*kern)(Args...), dim3 grid, unsigned block, size_t sm
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, vals...);
+}
+// The same with clusters of cy blocks along grid y.
+template <typename... Args, typename... Vals>
+cudaError_t launch_k_cluster_y(void (*kern)(Args...), dim3 grid, unsigned block, size_t smem,
+                               cudaStream_t st, bool pdl, unsigned cy, Vals... vals) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = cy;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, kern, vals...);
 }
 

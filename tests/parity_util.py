@@ -53,7 +53,7 @@ def run_gpu(dev, chunk=0, segments=0, want_debug=True, d_gated=None, fwd_segment
                                dev["conv_w"], dev["conv_b"], dev["dt_bias"], dev["a_log"],
                                dev["D"], ckpt, g, chunk=chunk, segments=segments,
                                want_du=want_debug, threads_per_channel=tpc,
-                               deterministic_dbc=det)
+                               deterministic=det)
     torch.cuda.synchronize()
     res = {"gated": to_np(gated), "ckpt": to_np(ckpt)}
     if y is not None:

@@ -59,7 +59,17 @@ def test_plan_with_explicit_segments_needs_no_device(lib):
     assert p.chunk == 16 and p.n_chunks == 128
     assert p.fwd_segments == 4 and p.bwd_segments == 4
     assert p.ckpt_bytes == 8 * 128 * 16 * 1536 * 4
-    assert p.fwd_launches == 2 and p.bwd_launches == 3
+    # 8 x 12 x 4 blocks fit one wave: the split kernels, whose backward main
+    # kernel finishes the parameter gradients itself (aggregate + main)
+    assert p.bwd_threads_per_channel == 2
+    assert p.fwd_launches == 2 and p.bwd_launches == 2
+    # the one-thread kernels: aggregate + main + parameter-gradient tail
+    st, pt = _plan(binding.make_dims(8, 2048, 1536, chunk=16, segments=4, threads_per_channel=1))
+    assert st == 0 and pt.bwd_launches == 3
+    assert pt.workspace_bytes >= 8 * 4 * 24 * 1536 * 4
+    # deterministic: the tail kernel and the dB/dC sum kernel as well
+    st, pd = _plan(binding.make_dims(8, 2048, 1536, chunk=16, segments=4, deterministic=True))
+    assert st == 0 and pd.bwd_launches == 4
     # one segment: the main kernel plus the parameter-gradient tail kernel
     st, p1 = _plan(binding.make_dims(8, 2048, 1536, chunk=16, segments=1))
     assert st == 0 and p1.fwd_launches == 1 and p1.bwd_launches == 2
@@ -332,17 +342,17 @@ def test_device_status_rejects_null(lib):
     assert lib.m3scan_device_status(None) == 1  # M3_ERR_NULL
 
 
-def test_deterministic_dbc_adds_block_partials_to_the_workspace(lib):
+def test_deterministic_adds_block_partials_to_the_workspace(lib):
     base = binding.make_dims(8, 2048, 1536, chunk=8, segments=12, threads_per_channel=1)
     det = binding.make_dims(8, 2048, 1536, chunk=8, segments=12, threads_per_channel=1,
-                            deterministic_dbc=True)
+                            deterministic=True)
     st0, p0 = _plan(base)
     st1, p1 = _plan(det)
     assert st0 == 0 and st1 == 0
     # 12 blocks of 128 channels, one partial row of 2 x 16 floats per (batch, step, block)
     assert p1.workspace_bytes >= p0.workspace_bytes + 8 * 2048 * 12 * 32 * 4 - 256
     bad = binding.make_dims(8, 2048, 1536, chunk=8, segments=12)
-    bad.deterministic_dbc = 2
+    bad.deterministic = 2
     assert binding.STATUS[_plan(bad)[0]] == "M3_ERR_DIMS"
     bad = binding.make_dims(8, 2048, 1536, chunk=8, segments=12)
     bad.reserved0 = 1

@@ -136,11 +136,11 @@ def test_null_state_matches_plain_entry_points_bit_for_bit():
                            ckpt, dev["d_gated"], chunk=8, segments=3, want_du=True)
     torch.cuda.synchronize()
     assert np.array_equal(a["gated"], to_np(gated))
-    # dB and dC are sums of float atomics: their order may differ between runs
-    for k in ("d_x", "d_delta_raw", "dz", "du", "d_conv_w", "d_conv_b", "d_dt_bias",
-              "d_a_log", "dD"):
+    # dB, dC and (split kernel over several segments) the parameter
+    # gradients are sums of float atomics: their order may differ between runs
+    for k in ("d_x", "d_delta_raw", "dz", "du"):
         assert np.array_equal(a[k], to_np(g[k])), k
-    for k in ("dB", "dC"):
+    for k in ("dB", "dC", "d_conv_w", "d_conv_b", "d_dt_bias", "d_a_log", "dD"):
         assert norm_err(a[k], to_np(g[k])) <= 1e-6, k
 
 

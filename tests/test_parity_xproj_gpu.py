@@ -93,7 +93,7 @@ def test_strided_b_c_and_gradients_match_oracle(act, R, segments):
 @pytest.mark.parametrize("tpc", [1, 2])
 @pytest.mark.parametrize("det", [False, True])
 def test_two_phase_backward_matches_oracle(batch, T, D, act, chunk, segments, state, tpc, det):
-    """det: dB/dC as fixed-order sums (m3_dims.deterministic_dbc), and a
+    """det: dB/dC as fixed-order sums (m3_dims.deterministic), and a
     second call must repeat every output bit for bit."""
     seed = batch + T + D + chunk
     inp = make_inputs(batch, T, D, act=act, seed=seed)
@@ -124,7 +124,7 @@ def test_two_phase_backward_matches_oracle(batch, T, D, act, chunk, segments, st
             dev["x"], dev["delta_raw"], dev["z"], dev["B"], dev["C"], dev["conv_w"],
             dev["conv_b"], dev["dt_bias"], dev["a_log"], dev["D"], ckpt, dev["d_gated"],
             lambda g: du_extra_t, chunk=chunk, segments=segments, threads_per_channel=tpc,
-            deterministic_dbc=det, **kw)
+            deterministic=det, **kw)
     o = run()
     torch.cuda.synchronize()
     if det:
@@ -164,11 +164,11 @@ def test_two_phase_without_extra_equals_one_call_backward():
                                        dev["a_log"], dev["D"], ckpt, dev["d_gated"], None,
                                        chunk=8, segments=4)
     torch.cuda.synchronize()
-    for k in ("du", "dz", "d_delta_raw", "d_dt_bias", "d_a_log", "dD"):
+    for k in ("du", "dz", "d_delta_raw"):
         assert torch.equal(one[k], two[k]), k
-    # d_x at segment boundaries, dB/dC (atomics) and the conv parameter sums
-    # are added in another order
-    for k in ("d_x", "dB", "dC", "d_conv_w", "d_conv_b"):
+    # d_x at segment boundaries, dB/dC and the parameter gradients (float
+    # atomics) are added in another order
+    for k in ("d_x", "dB", "dC", "d_conv_w", "d_conv_b", "d_dt_bias", "d_a_log", "dD"):
         assert norm_err(to_np(two[k]), to_np(one[k])) <= 1e-6, k
 
 
