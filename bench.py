@@ -217,6 +217,7 @@ class Layer:
         self.act = binding.M3_BF16 if x.dtype == torch.bfloat16 else binding.M3_F32
         Bsz, T, D = x.shape
         self.shape = (Bsz, T, D)
+        self.segments, self.tpc = segments, threads_per_channel
         self.dims = binding.make_dims(Bsz, T, D, chunk=chunk, segments=segments,
                                       threads_per_channel=threads_per_channel)
         self.plan = binding.m3scan_plan(self.dims, self.act)
@@ -509,11 +510,13 @@ def e2e_measure(torch, binding, layer, tensors, steps, device):
         binding.m3scan_fwd(
             d_in["x"], d_in["delta_raw"], d_in["z"], d_in["B"], d_in["C"], d_in["conv_w"],
             d_in["conv_b"], d_in["dt_bias"], d_in["a_log"], d_in["D"], chunk=int(layer.plan.chunk),
+            segments=layer.segments, threads_per_channel=layer.tpc,
             gated=d_out["gated"], ckpt=layer.o["ckpt"], workspace=_WS(ws), stream=s)
         binding.m3scan_bwd(
             d_in["x"], d_in["delta_raw"], d_in["z"], d_in["B"], d_in["C"], d_in["conv_w"],
             d_in["conv_b"], d_in["dt_bias"], d_in["a_log"], d_in["D"], layer.o["ckpt"],
-            d_in["d_gated"], chunk=int(layer.plan.chunk),
+            d_in["d_gated"], chunk=int(layer.plan.chunk), segments=layer.segments,
+            threads_per_channel=layer.tpc,
             out={k: d_out[k] for k in outs if k != "gated"}, workspace=_WS(ws), stream=s)
         h_out_buf.copy_(d_out_buf, non_blocking=True)
 
@@ -571,11 +574,13 @@ def e2e_measure(torch, binding, layer, tensors, steps, device):
             binding.m3scan_fwd(
                 di["x"], di["delta_raw"], di["z"], di["B"], di["C"], di["conv_w"],
                 di["conv_b"], di["dt_bias"], di["a_log"], di["D"], chunk=int(layer.plan.chunk),
+                segments=layer.segments, threads_per_channel=layer.tpc,
                 gated=do["gated"], ckpt=layer.o["ckpt"], workspace=_WS(ws), stream=sc)
             binding.m3scan_bwd(
                 di["x"], di["delta_raw"], di["z"], di["B"], di["C"], di["conv_w"],
                 di["conv_b"], di["dt_bias"], di["a_log"], di["D"], layer.o["ckpt"],
-                di["d_gated"], chunk=int(layer.plan.chunk),
+                di["d_gated"], chunk=int(layer.plan.chunk), segments=layer.segments,
+                threads_per_channel=layer.tpc,
                 out={k2: do[k2] for k2 in outs if k2 != "gated"}, workspace=_WS(ws), stream=sc)
             ev["in_free"][b].record(sc)
             ev["out_ready"][b].record(sc)
