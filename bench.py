@@ -412,7 +412,10 @@ def gpu_arm(args):
     # FP32 lane-op rate of the backward call, the dominant launch sequence.
     alu_peak = alu_peak_gops()
     bwd_gops = BWD_FP32_OPS_PER_ELEM * E / (bwd_avg * 1e-3) / 1e9
-    roofline = {"bound": "alu", "kernel": "m3scan_bwd (aggregate + main + tail kernels)",
+    parts = (["aggregate"] if int(layer.plan.bwd_segments) > 1 else []) + ["main"]
+    parts += ["tail", "dB/dC sum"][:max(0, int(layer.plan.bwd_launches) - len(parts))]
+    bwd_kernels = " + ".join(parts) + (" kernels" if len(parts) > 1 else " kernel")
+    roofline = {"bound": "alu", "kernel": f"m3scan_bwd ({bwd_kernels})",
                 "achieved": round(bwd_gops, 1), "peak": round(alu_peak, 1), "unit": "Gop/s",
                 "frac": round(bwd_gops / alu_peak, 4),
                 "peak_kind": "derived: 152 SMs x 128 FP32 lanes x max SM clock",
