@@ -357,3 +357,23 @@ def test_deterministic_adds_block_partials_to_the_workspace(lib):
     bad = binding.make_dims(8, 2048, 1536, chunk=8, segments=12)
     bad.reserved0 = 1
     assert binding.STATUS[_plan(bad)[0]] == "M3_ERR_DIMS"
+
+
+def test_cluster_finish_covers_two_to_eight_backward_segments(lib):
+    """The split backward finishes its sums in a cluster of its segments when
+    there are 2-8 of them (aggregate + main kernel, no partials region);
+    with more segments, one thread per channel, or deterministic sums the
+    tail kernel runs after it."""
+    def plan(**kw):
+        st, p = _plan(binding.make_dims(2, 1024, 256, chunk=8, **kw))
+        assert st == 0
+        return p
+    p8 = plan(segments=8, threads_per_channel=2)
+    assert p8.bwd_segments == 8 and p8.bwd_launches == 2
+    p9 = plan(segments=9, threads_per_channel=2)
+    assert p9.bwd_segments == 9 and p9.bwd_launches == 3
+    # the cluster path needs no per-(batch, segment) partials [B * S, N + 8, D]
+    assert p9.workspace_bytes >= p8.workspace_bytes + 2 * 8 * 24 * 256 * 4 - 256 * 8
+    assert plan(segments=8, threads_per_channel=1).bwd_launches == 3
+    assert plan(segments=8, threads_per_channel=2, deterministic=True).bwd_launches == 4
+    assert plan(segments=1, threads_per_channel=2).bwd_launches == 2  # main + tail
