@@ -283,3 +283,48 @@ def test_split_backward_in_kernel_sums_accumulate_when_asked():
     for k in keys:
         want = g1[k] + prior[k]
         assert (g2[k] - want).abs().max() <= 1e-6 * want.abs().max(), k
+
+
+@pytest.mark.parametrize("segments,tpc,det", [(4, 2, False), (4, 2, True), (3, 1, False)])
+def test_back_to_back_calls_sharing_checkpoints_and_workspace(segments, tpc, det):
+    """Forward/backward pairs of two input sets queued back to back on one
+    stream, sharing the checkpoint and workspace buffers (a kernel that
+    started before the previous call finished would overwrite what that call
+    still reads; inside a call the kernels overlap by programmatic dependent
+    launch), give the same results as the same calls with a synchronisation
+    after each (the same bits, but for float-atomic sums without
+    deterministic mode)."""
+    from parity_util import norm_err, to_np
+    kw = dict(chunk=8, segments=segments, threads_per_channel=tpc)
+    sets = [to_device(make_inputs(2, 96, 136, act="bf16", seed=40 + i)) for i in range(2)]
+    dims = binding.make_dims(2, 96, 136, deterministic=det, **kw)
+    pl = binding.m3scan_plan(dims, binding.M3_BF16)
+    ws = binding.Workspace(pl.workspace_bytes, "cuda:0")
+    ckpt = torch.empty((2, pl.n_chunks, 16, 136), dtype=torch.float32, device="cuda:0")
+
+    def pair(dev, sync):
+        gated, _, _ = binding.m3scan_fwd(dev["x"], dev["delta_raw"], dev["z"], dev["B"], dev["C"],
+                                         dev["conv_w"], dev["conv_b"], dev["dt_bias"],
+                                         dev["a_log"], dev["D"], ckpt=ckpt, workspace=ws, **kw)
+        if sync:
+            torch.cuda.synchronize()
+        g = binding.m3scan_bwd(dev["x"], dev["delta_raw"], dev["z"], dev["B"], dev["C"],
+                               dev["conv_w"], dev["conv_b"], dev["dt_bias"], dev["a_log"],
+                               dev["D"], ckpt, dev["d_gated"], workspace=ws, deterministic=det,
+                               **kw)
+        if sync:
+            torch.cuda.synchronize()
+        return gated, g
+
+    want = [pair(dev, True) for dev in sets]
+    want = [(gt.clone(), {k: v.clone() for k, v in g.items()}) for gt, g in want]
+    for _ in range(3):
+        got = [pair(dev, False) for dev in sets]
+        torch.cuda.synchronize()
+        for (gt, g), (wgt, wg) in zip(got, want):
+            assert torch.equal(gt, wgt)
+            for k in wg:
+                if det or k in ("d_x", "d_delta_raw", "dz"):
+                    assert torch.equal(g[k], wg[k]), k
+                else:
+                    assert norm_err(to_np(g[k]), to_np(wg[k])) <= 1e-6, k
