@@ -1,0 +1,71 @@
+"""The benchmark's one-line JSON contract, read back from a real run: the
+reference arm (the float64 oracle on the host, no GPU) and, on a GPU, the
+CUDA arm with its roofline, CPU baseline, end-to-end, launch count and clock
+record.
+"""
+
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _run(args, timeout):
+    p = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args], cwd=ROOT,
+                       capture_output=True, text=True, timeout=timeout)
+    assert p.returncode == 0, p.stderr[-2000:]
+    lines = [ln for ln in p.stdout.splitlines() if ln.strip().startswith("{")]
+    assert len(lines) == 1, p.stdout[-2000:]
+    return json.loads(lines[0])
+
+
+def _common(d):
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+              "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config", "e2e"):
+        assert k in d, k
+    assert d["unit"] == "Gelem/s" and d["higher_is_better"] is True
+    assert d["n_gpus"] == 1 and d["data"] == "synthetic"
+    assert d["config"]["workload"] == "trainer_b8_t128_d512"
+    assert d["vs_baseline"] is None  # the pages publish no number for this metric
+    assert d["value"] > 0 and d["ms_per_step"] > 0
+
+
+def test_reference_arm_prints_the_contract_line():
+    d = _run(["--impl", "reference", "--steps", "1", "--warmup", "3"], timeout=600)
+    _common(d)
+    assert d["impl"] == "reference" and d["steps"] == 1 and d["warmup"] == 3
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["sample"]
+    assert cb["value"] == d["value"]
+    e = d["e2e"]
+    assert e["value"] == d["value"] and e["unit"] == d["unit"]
+    assert e["h2d_bytes_per_step"] == 0 and e["d2h_bytes_per_step"] == 0
+
+
+@pytest.mark.gpu
+def test_cuda_arm_prints_the_contract_line():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    d = _run(["--steps", "20", "--warmup", "3", "--no-extras", "--cpu-seconds", "2"], timeout=900)
+    _common(d)
+    assert "impl" not in d or d["impl"] != "reference"
+    assert d["scaling"] == "weak" and d["warmup"] >= 3
+    r = d["roofline"]
+    assert r["bound"] in ("alu", "hbm", "tensor")
+    assert abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-3
+    assert 0 < r["frac"] < 1.5
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] > 0
+    e = d["e2e"]
+    assert e["value"] > 0 and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
+    assert e["value"] != d["value"]
+    # four kernels per step on this workload: aggregate + final forward,
+    # aggregate + main backward
+    assert d["gpu_launches"] == 20 * 4
+    c = d["clocks"]
+    assert c["sm_max_mhz"] > 0 and isinstance(c["reasons"], list)
