@@ -22,6 +22,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -94,14 +95,23 @@ def alu_peak_gops():
 SCAN_SOURCES = ("m3_api.cu", "m3_bwd.cu", "m3_bwd2.cu", "m3_common.cuh", "m3_fwd.cu")
 
 
+def code_only(text):
+    """C++/CUDA source with its comments removed and whitespace collapsed, so
+    that an edit to comments alone leaves the hash unchanged (string literals
+    here hold no comment markers)."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def source_hash():
-    """Hash of the forward/backward kernel sources the ncu traffic figures
-    were taken on."""
+    """Hash of the code (comments aside) of the forward/backward kernel
+    sources the ncu traffic figures were taken on."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "mamba_selective_scan_gb300", "csrc")
     for name in SCAN_SOURCES:
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            h.update(code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

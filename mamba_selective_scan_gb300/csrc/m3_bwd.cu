@@ -567,7 +567,7 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(const __grid_constant__ B
 
     __syncthreads();
     // one global reduction per (t, n) per block for dB and dC
-    if (a.dbc_part) {  // this block's share, summed in a fixed order by the tail kernel
+    if (a.dbc_part) {  // this block's share, summed in a fixed order by m3_dbc_sum_kernel
       for (int i = tid; i < steps * 32; i += GB) {
         const int j = i >> 5, l = i & 31;
         float v = 0.f;

@@ -382,7 +382,7 @@ __global__ void __launch_bounds__(128, 4) m3_bwd2_kernel(const __grid_constant__
     }
 
     __syncthreads();
-    if constexpr (DET) {  // this block's share, summed in a fixed order by the tail kernel
+    if constexpr (DET) {  // this block's share, summed in a fixed order by m3_dbc_sum_kernel
       for (int i = tid; i < steps * 2 * N; i += 128) {
         const int j = i / (2 * N), l = i % (2 * N);
         float v = 0.f;

@@ -355,7 +355,7 @@ struct BwdArgs {
   int accumulate;
   uint32_t tcols;  // tensor-memory columns per CTA for the state history
   // deterministic dB/dC: per-(batch, step, channel block) partials
-  // [B * T][nblk][2N], summed by the tail kernel; NULL: float atomics
+  // [B * T][nblk][2N], summed by m3_dbc_sum_kernel; NULL: float atomics
   float* dbc_part;
   int nblk;
   // 1: the split main kernel runs with the S segments of a (channel block,
