@@ -69,3 +69,13 @@ def test_cuda_arm_prints_the_contract_line():
     assert d["gpu_launches"] == 20 * 4
     c = d["clocks"]
     assert c["sm_max_mhz"] > 0 and isinstance(c["reasons"], list)
+
+
+def test_traffic_key_ignores_comments_but_not_code():
+    if ROOT not in sys.path:
+        sys.path.insert(0, ROOT)
+    import bench
+    src = "int f(int a) {  // one\n  return a + 1; /* two\n lines */ }\n"
+    assert bench.code_only(src) == bench.code_only("int f(int a) {\n return a + 1; }")
+    assert bench.code_only(src) != bench.code_only("int f(int a) { return a + 2; }")
+    assert len(bench.source_hash()) == 16
