@@ -417,7 +417,10 @@ def _fwd(x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D, chunk, segm
 def m3scan_bwd(x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D, ckpt, d_gated, *,
                chunk=0, segments=0, want_du=False, accumulate_param_grads=False, out=None,
                workspace=None, stream=None, threads_per_channel=0, deterministic=False):
-    """Backward of the layer core.  Returns a dict of gradients (tensors)."""
+    """Backward of the layer core.  Returns a dict of gradients (tensors).
+    ``deterministic``: dB, dC and the parameter gradients as fixed-order sums
+    (identical bits on every call, a larger workspace) instead of float-atomic
+    sums; the per-element gradients are the same bits either way."""
     return _bwd(x, delta_raw, z, Bm, Cm, conv_w, conv_b, dt_bias, a_log, D, ckpt, d_gated,
                 chunk, segments, want_du, accumulate_param_grads, out, workspace, stream, None,
                 threads_per_channel, deterministic)
