@@ -129,6 +129,43 @@ def ncu_traffic(workload, kernel):
     return d.get("traffic", {}).get(workload, {}).get(kernel)
 
 
+def traffic_from_launch_list(csv_path, workload):
+    """The ncu_traffic.json record from an ncu launch list (the CSV of
+    ``ncu --metrics gpu__time_duration.sum,dram__bytes_read.sum,
+    dram__bytes_write.sum --csv``): DRAM bytes per launch of every m3_ kernel
+    (read + write, averaged over its launches) and their sums over the
+    forward's and the backward's kernels, keyed to the current kernel code."""
+    import csv
+    with open(csv_path, newline="") as f:
+        rows = list(csv.reader(f))
+    hi = next(i for i, r in enumerate(rows) if "Kernel Name" in r)
+    hdr = rows[hi]
+    ki, ii = hdr.index("Kernel Name"), hdr.index("ID")
+    mi, vi, ui = hdr.index("Metric Name"), hdr.index("Metric Value"), hdr.index("Metric Unit")
+    scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}
+    per_launch = {}
+    for r in rows[hi + 1:]:
+        if len(r) <= vi or not r[mi].startswith("dram__bytes_"):
+            continue
+        name = r[ki].split("(")[0].replace("void ", "").strip()
+        if not name.startswith("m3_"):
+            continue
+        key = (name, r[ii])
+        per_launch[key] = per_launch.get(key, 0.0) + float(r[vi].replace(",", "")) * scale[r[ui]]
+    sums = {}
+    for (name, _), v in per_launch.items():
+        tot, n = sums.get(name, (0.0, 0))
+        sums[name] = (tot + v, n + 1)
+    per = {k: int(tot / n) for k, (tot, n) in sums.items()}
+    return {"note": "DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per call, summed "
+                    "over the call's kernels, from one ncu launch list; valid only for the kernel "
+                    "code with this hash",
+            "source_sha256_16": source_hash(),
+            "traffic": {workload: {"bwd": sum(v for k, v in per.items() if "bwd" in k),
+                                   "fwd": sum(v for k, v in per.items() if "fwd" in k)}},
+            "per_kernel_bytes_per_launch": per}
+
+
 # ---------------------------------------------------------------------------
 # clocks
 # ---------------------------------------------------------------------------
@@ -897,7 +934,16 @@ def main():
                     help="run only the one-token decode measurements (for profiling)")
     ap.add_argument("--conv-only", action="store_true",
                     help="run only the two-phase conv-backward measurements (for profiling)")
+    ap.add_argument("--write-traffic", metavar="LAUNCHES_CSV",
+                    help="write profiles/ncu_traffic.json for --workload from an ncu launch list "
+                         "taken on the current kernel code (no GPU needed), then exit")
     args = ap.parse_args()
+    if args.write_traffic:
+        rec = traffic_from_launch_list(args.write_traffic, args.workload)
+        with open(os.path.join(ROOT, "profiles", "ncu_traffic.json"), "w") as f:
+            json.dump(rec, f, indent=1)
+        print(json.dumps(rec["traffic"]))
+        return
     if args.warmup < 3:
         args.warmup = 3
     if args.decode_only:

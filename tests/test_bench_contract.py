@@ -79,3 +79,28 @@ def test_traffic_key_ignores_comments_but_not_code():
     assert bench.code_only(src) == bench.code_only("int f(int a) {\n return a + 1; }")
     assert bench.code_only(src) != bench.code_only("int f(int a) { return a + 2; }")
     assert len(bench.source_hash()) == 16
+
+
+def test_traffic_record_from_a_launch_list(tmp_path):
+    if ROOT not in sys.path:
+        sys.path.insert(0, ROOT)
+    import bench
+    hdr = '"ID","Kernel Name","Metric Name","Metric Unit","Metric Value"\n'
+    rows = []
+    for launch, (name, rd, wr) in enumerate([
+            ("void m3_fwd2_kernel<float, 0, 16>(FwdArgs)", "1.5", "0.5"),
+            ("void m3_fwd2_kernel<float, 1, 16>(FwdArgs)", "4", "2"),
+            ("void m3_bwd2_kernel<float, 0, 0, 16, 0>(BwdArgs)", "10", "0"),
+            ("void m3_fwd2_kernel<float, 0, 16>(FwdArgs)", "2.5", "0.5"),
+            ("void other_kernel(int)", "99", "99")]):
+        rows.append(f'"{launch}","{name}","gpu__time_duration.sum","ns","1,000"\n')
+        rows.append(f'"{launch}","{name}","dram__bytes_read.sum","Mbyte","{rd}"\n')
+        rows.append(f'"{launch}","{name}","dram__bytes_write.sum","Mbyte","{wr}"\n')
+    p = tmp_path / "launches.csv"
+    p.write_text("==PROF== a line before the table\n" + hdr + "".join(rows))
+    rec = bench.traffic_from_launch_list(str(p), "w")
+    per = rec["per_kernel_bytes_per_launch"]
+    assert per == {"m3_fwd2_kernel<float, 0, 16>": 2_500_000, "m3_fwd2_kernel<float, 1, 16>": 6_000_000,
+                   "m3_bwd2_kernel<float, 0, 0, 16, 0>": 10_000_000}
+    assert rec["traffic"] == {"w": {"fwd": 8_500_000, "bwd": 10_000_000}}
+    assert rec["source_sha256_16"] == bench.source_hash()
