@@ -25,6 +25,16 @@ delta* ~ U[0.001, 0.01] in delta_raw's slot and sets
 ``delta_raw = softplus^-1(delta*) - dt_bias`` (then rounds to bf16), so that
 the step size lands near [0.001, 0.01] and decay across chunk checkpoints is
 slow.
+
+``random_params=True`` replaces the three per-channel parameters that the
+recipe fixes (a_log, conv_b, D) with draws that differ per channel, from a
+stream of their own (``default_rng([seed, 2])``, so the other draws are
+unchanged), in this order:
+
+* ``a_log[d, n]`` ~ U(-4, 3): A = -exp(a_log) spans [-20.1, -0.018], so that
+  exp(delta A) reaches both nearly 1 (slow decay) and nearly 0 (no memory);
+* ``conv_b[d]`` ~ U(-0.5, 0.5);
+* ``D[d]`` ~ U(-1.5, 1.5).
 """
 
 from __future__ import annotations
@@ -125,7 +135,7 @@ class Inputs:
 
 
 def make_inputs(batch, seq_len, d_inner, act="bf16", seed=0, d_state=D_STATE,
-                d_conv=D_CONV, slow_delta=False) -> Inputs:
+                d_conv=D_CONV, slow_delta=False, random_params=False) -> Inputs:
     """Draw one seeded input set following the recipe in the module doc."""
     if act not in ("f32", "bf16"):
         raise ValueError(f"act must be 'f32' or 'bf16', got {act!r}")
@@ -149,6 +159,8 @@ def make_inputs(batch, seq_len, d_inner, act="bf16", seed=0, d_state=D_STATE,
     a_log = np.log(np.arange(1, d_state + 1, dtype=np.float64))[None, :].repeat(d_inner, 0)
     a_log = np.ascontiguousarray(a_log, dtype=np.float32)
     Dp = np.ones(d_inner, dtype=np.float32)
+    if random_params:
+        a_log, conv_b, Dp = draw_random_params(d_inner, d_state, seed)
 
     acts = dict(x=x, delta_raw=delta_raw, z=z, B=Bm, C=Cm, d_gated=d_gated)
     if act == "bf16":
@@ -156,6 +168,16 @@ def make_inputs(batch, seq_len, d_inner, act="bf16", seed=0, d_state=D_STATE,
     arrays = dict(acts)
     arrays.update(conv_w=conv_w, conv_b=conv_b, dt_bias=dt_bias, a_log=a_log, D=Dp)
     return Inputs(batch, seq_len, d_inner, d_state, d_conv, act, arrays)
+
+
+def draw_random_params(d_inner, d_state=D_STATE, seed=0):
+    """Per-channel a_log [d_inner, d_state], conv_b and D [d_inner] (float32)
+    drawn as the module doc states for ``random_params=True``."""
+    rng = np.random.default_rng([seed, 2])
+    a_log = rng.uniform(-4.0, 3.0, size=(d_inner, d_state)).astype(np.float32)
+    conv_b = rng.uniform(-0.5, 0.5, size=d_inner).astype(np.float32)
+    Dp = rng.uniform(-1.5, 1.5, size=d_inner).astype(np.float32)
+    return a_log, conv_b, Dp
 
 
 STATE_NAMES = ("ssm_state", "conv_state", "d_ssm_state_out", "d_conv_state_out")
@@ -183,7 +205,7 @@ def make_state_inputs(batch, d_inner, act="bf16", seed=0, d_state=D_STATE,
     return dict(ssm_state=h, conv_state=c, d_ssm_state_out=gh, d_conv_state_out=gc)
 
 
-def make_workload_inputs(name: str) -> Inputs:
+def make_workload_inputs(name: str, random_params=False) -> Inputs:
     w = WORKLOADS[name]
     return make_inputs(w.batch, w.seq_len, w.d_inner, w.act, w.seed,
-                       w.d_state, w.d_conv, w.slow_delta)
+                       w.d_state, w.d_conv, w.slow_delta, random_params)
