@@ -43,6 +43,18 @@
  * validation returns a status and enqueues nothing.  A failed launch
  * returns M3_ERR_CUDA (the CUDA error is cleared with cudaGetLastError).
  * Unsupported shapes return M3_ERR_UNSUPPORTED; there is no fallback path.
+ * (The mamba-rs 0.4.0 page src/mamba3_siso/gpu/backward_mixed.rs states the
+ * same rules in its module header: labelled errors, never a silent
+ * fallback.)  Errors that only the GPU can see -- a kernel that gave up
+ * waiting for a tile copy (every such wait is bounded to about a second, so
+ * the GPU cannot hang) -- are recorded on the device: in the status block at
+ * the start of the call's workspace, read with m3scan_get_status, and in a
+ * per-device word read with m3scan_device_status.
+ *
+ * Workspace status block: the first M3SCAN_STATUS_BYTES of every workspace
+ * belong to the library.  They must be zero when a workspace is first used
+ * (allocate it zeroed, or clear those bytes); kernels only ever set bits in
+ * them, and m3scan_get_status reads and clears them.
  */
 #ifndef M3SCAN_H
 #define M3SCAN_H
@@ -69,8 +81,14 @@ typedef enum {
     M3_ERR_UNSUPPORTED = 3, /* d_state not 16/32/64, d_conv != 4, d_inner % 8 != 0, dtype */
     M3_ERR_ALIGN = 4,       /* a pointer is not aligned as required */
     M3_ERR_WORKSPACE = 5,   /* workspace missing or smaller than planned */
-    M3_ERR_CUDA = 6         /* a CUDA runtime call or launch failed */
+    M3_ERR_CUDA = 6,        /* a CUDA runtime call or launch failed */
+    M3_ERR_TIMEOUT = 7      /* reported by m3scan_get_status: a kernel of an earlier call
+                               gave up waiting for a tile copy; that call's outputs are
+                               incomplete */
 } m3_status;
+
+/* Bytes at the start of every workspace that hold the status block. */
+#define M3SCAN_STATUS_BYTES 256
 
 typedef struct {
     int64_t batch, seq_len, d_inner, d_state, d_conv;
@@ -359,8 +377,11 @@ m3_status m3scan_decode(const m3_dims* dims, m3_dtype act,
  *   (m3scan_plan's workspace_bytes) is rejected with M3_ERR_WORKSPACE before
  *   anything is enqueued; use m3scan_bwd with a workspace for it.
  * - The first call on a device, with that device current, looks up the
- *   array's device address (cudaGetSymbolAddress) and caches it; make that
- *   first call before any stream capture on that device.
+ *   array's device address (cudaGetSymbolAddress) and caches it for that
+ *   device's CUDA context; make that first call before any stream capture on
+ *   that device.  A new context on the device (after cudaDeviceReset) has the
+ *   array elsewhere: the first call in it looks the address up again, so it
+ *   too must come before any capture.
  * - Every call on a device shares the one array, and the array keeps what
  *   the last call left in it (nothing in it needs to start at zero).  Calls
  *   that overlap on the GPU -- on different streams, or from different host
@@ -390,19 +411,36 @@ const char* m3scan_last_cuda_error(void);
 /* Library version as major * 10000 + minor * 100 + patch. */
 int32_t m3scan_version(void);
 
+/* Device-side status of the calls made with `workspace`: waits for `stream`
+ * (the stream those calls were enqueued on), reads the workspace's status
+ * block and clears it (on `stream`).  *device_status = M3_OK if every kernel
+ * of those calls since the last query ran normally, M3_ERR_TIMEOUT if one of
+ * them gave up waiting for a tile copy (its call's outputs are incomplete).
+ * Calls on other workspaces and streams are neither seen nor waited for.
+ * Calls that were given no workspace (a forward over one time segment with
+ * workspace NULL, m3scan_decode) report only to m3scan_device_status.
+ * Returns M3_ERR_NULL for a NULL workspace or device_status, M3_ERR_CUDA if
+ * waiting or reading fails.  Synchronous for the host. */
+m3_status m3scan_get_status(const void* workspace, m3_stream_t stream, m3_status* device_status);
+
 /* Device-side status of the calling thread's current device since the last
  * query, then cleared: *out = 0 if every kernel ran normally; nonzero if a
- * kernel gave up waiting for a tile copy into shared memory (each such wait
- * is bounded to about a second so the GPU cannot hang; that call's outputs
- * are then incomplete).  Synchronous: it waits for the device's queued
- * work.  Returns M3_ERR_NULL for a NULL out, M3_ERR_CUDA if reading fails. */
+ * kernel of any call on that device gave up waiting for a tile copy into
+ * shared memory (each such wait is bounded to about a second so the GPU
+ * cannot hang; that call's outputs are then incomplete).  One word per
+ * device, shared by every caller: prefer m3scan_get_status, which reports
+ * the calls of one workspace only.  Synchronous: it waits for the device's
+ * queued work.  Returns M3_ERR_NULL for a NULL out, M3_ERR_CUDA if reading
+ * fails. */
 m3_status m3scan_device_status(int32_t* out);
 
 /* Diagnostic of the bounded waits: enqueues one block on `stream` that waits
  * for a tile copy it never issues.  The wait gives up after about a second
- * and the block sets the device status word, so m3scan_device_status then
- * reports nonzero (and clears it).  Nothing else is touched. */
-m3_status m3scan_selftest_wait_timeout(m3_stream_t stream);
+ * and the block sets the device status word and, when `workspace` is not
+ * NULL, that workspace's status block, so m3scan_device_status and
+ * m3scan_get_status then report the failure (and clear it).  Nothing else is
+ * touched. */
+m3_status m3scan_selftest_wait_timeout(void* workspace, m3_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -25,12 +25,17 @@ STATUS = {
     4: "M3_ERR_ALIGN",
     5: "M3_ERR_WORKSPACE",
     6: "M3_ERR_CUDA",
+    7: "M3_ERR_TIMEOUT",
 }
+
+# bytes at the start of every workspace that hold the library's status block
+STATUS_BYTES = 256
 
 # every symbol include/m3scan.h declares
 EXPORTS = ("m3scan_plan", "m3scan_fwd", "m3scan_bwd", "m3scan_fwd_state", "m3scan_bwd_state",
            "m3scan_bwd_scan", "m3scan_conv_bwd", "m3scan_decode", "m3scan_bwd_noalloc", "m3scan_status_string", "m3scan_last_cuda_error",
-           "m3scan_version", "m3scan_device_status", "m3scan_selftest_wait_timeout")
+           "m3scan_version", "m3scan_get_status", "m3scan_device_status",
+           "m3scan_selftest_wait_timeout")
 
 # size of the library's own scratch array used by m3scan_bwd_noalloc
 NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -147,8 +152,10 @@ def _lib_handle(build_if_missing: bool = True):
             lib.m3scan_version.argtypes = []
             lib.m3scan_device_status.restype = ctypes.c_int
             lib.m3scan_device_status.argtypes = [ctypes.POINTER(ctypes.c_int32)]
+            lib.m3scan_get_status.restype = ctypes.c_int
+            lib.m3scan_get_status.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_int)]
             lib.m3scan_selftest_wait_timeout.restype = ctypes.c_int
-            lib.m3scan_selftest_wait_timeout.argtypes = [ctypes.c_void_p]
+            lib.m3scan_selftest_wait_timeout.argtypes = [_vp, _vp]
             _LIB = lib
     return _LIB
 
@@ -183,11 +190,25 @@ def m3scan_version() -> int:
     return int(_lib_handle().m3scan_version())
 
 
-def m3scan_selftest_wait_timeout(stream: int = 0) -> None:
-    """Enqueue the diagnostic block whose tile wait never completes."""
-    st = _lib_handle().m3scan_selftest_wait_timeout(ctypes.c_void_p(stream))
+def m3scan_selftest_wait_timeout(stream: int = 0, workspace=None) -> None:
+    """Enqueue the diagnostic block whose tile wait never completes (it
+    reports to the device word and, if given, to ``workspace``'s status
+    block)."""
+    ws = None if workspace is None else workspace.ptr
+    st = _lib_handle().m3scan_selftest_wait_timeout(ws, ctypes.c_void_p(stream))
     if st != 0:
         raise M3Error(st, "m3scan_selftest_wait_timeout")
+
+
+def m3scan_get_status(workspace, stream=None) -> int:
+    """Status of the calls made with ``workspace`` (a ``Workspace``) since the
+    last query, then cleared: 0 (M3_OK) or 7 (M3_ERR_TIMEOUT).  Waits for
+    ``stream`` (default: the current torch stream)."""
+    out = ctypes.c_int(0)
+    st = _lib_handle().m3scan_get_status(workspace.ptr, _stream_handle(stream), ctypes.byref(out))
+    if st != 0:
+        raise M3Error(st, "m3scan_get_status")
+    return int(out.value)
 
 
 def m3scan_device_status() -> int:
@@ -326,12 +347,15 @@ def _stream_handle(stream):
 
 
 class Workspace:
-    """A device workspace sized for a plan (reusable across calls)."""
+    """A device workspace sized for a plan (reusable across calls).  Its
+    status block (the first STATUS_BYTES) starts at zero, as the library
+    requires."""
 
     def __init__(self, nbytes: int, device):
         torch = _torch()
-        self.nbytes = max(int(nbytes), 256)
+        self.nbytes = max(int(nbytes), STATUS_BYTES)
         self.buf = torch.empty(self.nbytes, dtype=torch.uint8, device=device)
+        self.buf[:STATUS_BYTES].zero_()
 
     @property
     def ptr(self):

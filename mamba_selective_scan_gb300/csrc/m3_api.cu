@@ -39,8 +39,42 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[M3SCAN_NOALLOC_
 
 namespace m3 {
 
+// Identity of the calling thread's current CUDA context: 0 when there is
+// none yet or the driver cannot say.  A context that was torn down and
+// created again (cudaDeviceReset) gets a new identity, so the per-device
+// caches below redo their set-up for it instead of reusing what belonged to
+// the old one (function attributes, a symbol's device address).
+unsigned long long current_context_id() {
+  typedef CUresult (*GetCurrentFn)(CUcontext*);
+  typedef CUresult (*GetIdFn)(CUcontext, unsigned long long*);
+  static const GetCurrentFn get_current = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      f = nullptr;
+    return reinterpret_cast<GetCurrentFn>(f);
+  }();
+  static const GetIdFn get_id = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      f = nullptr;
+    return reinterpret_cast<GetIdFn>(f);
+  }();
+  cudaGetLastError();  // a failed lookup leaves no error behind
+  if (!get_current || !get_id) return 0;
+  CUcontext c = nullptr;
+  if (get_current(&c) != CUDA_SUCCESS || !c) return 0;
+  unsigned long long id = 0;
+  if (get_id(c, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
 struct DevInfo {
   bool attrs = false;
+  unsigned long long ctx = 0;  // context the attributes were set in (0: unknown)
   int sms = 0;
   int smem_per_sm = 0;
   int occ_fwd[2][KMAX + 1];  // [dtype][chunk] blocks per SM, 0 = not yet queried
@@ -109,7 +143,9 @@ cudaError_t device_info(int chunk, int ai, int* sms, int* occ_f, int* occ_b, int
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lk(g_mu);
   DevInfo& di = g_dev[dev];
-  if (!di.attrs) {
+  const unsigned long long ctx = current_context_id();
+  if (!di.attrs || (ctx != 0 && di.ctx != 0 && ctx != di.ctx)) {
+    di.attrs = false;
     e = set_attrs<float>();
     if (e != cudaSuccess) return e;
     e = set_attrs<__nv_bfloat16>();
@@ -121,6 +157,7 @@ cudaError_t device_info(int chunk, int ai, int* sms, int* occ_f, int* occ_b, int
     for (int a = 0; a < 2; ++a)
       for (int k = 0; k <= KMAX; ++k) di.occ_fwd[a][k] = di.occ_bwd[a][k] = 0;
     di.attrs = true;
+    di.ctx = current_context_id();  // the set-up above made the context current if it was not
   }
   if (occ_f && di.occ_fwd[ai][chunk] == 0) {
     int of = 0, ob = 0;
@@ -312,8 +349,8 @@ m3_status make_plan(const m3_dims* dm, m3_dtype act, Plan* p) {
     off = align_up(off + bytes, 256);
     return o;
   };
-  // forward section
-  off = 0;
+  // forward section, after the status block
+  off = STATUS_BYTES;
   p->f_aggh = p->f_aggs = 0;
   if (p->Sf > 1) {
     p->f_aggh = take(B * p->Sf * N * D * 4);
@@ -321,7 +358,7 @@ m3_status make_plan(const m3_dims* dm, m3_dtype act, Plan* p) {
   }
   size_t fwd_total = off;
   // backward section (reuses the same bytes)
-  off = 0;
+  off = STATUS_BYTES;
   p->det = dm->deterministic != 0;
   p->fin = !p->det && p->bwd_tpc != 1 && p->Sb > 1 && p->Sb <= FIN_MAX;
   // per-(batch, segment) parameter partials, unless the main kernel adds
@@ -342,12 +379,12 @@ m3_status make_plan(const m3_dims* dm, m3_dtype act, Plan* p) {
   // conv backward of the two-phase backward (its own call): CT-step tiles
   p->ctile = CT;
   p->cntiles = (p->T + CT - 1) / CT;
-  off = 0;
+  off = STATUS_BYTES;
   p->c_part = take(B * (size_t)p->cntiles * 5 * D * 4);
   const size_t conv_total = off;
   if (conv_total > bwd_total) bwd_total = conv_total;
   p->ws_bytes = fwd_total > bwd_total ? fwd_total : bwd_total;
-  if (p->ws_bytes < 256) p->ws_bytes = 256;
+  if (p->ws_bytes < STATUS_BYTES) p->ws_bytes = STATUS_BYTES;
   p->fwd_launches = empty ? 0 : (p->Sf > 1 ? 2 : 1);
   p->bwd_launches = empty ? 0 : (p->Sb > 1 ? 2 : 1) + (p->fin ? 0 : 1) + (p->det ? 1 : 0);
   return M3_OK;
@@ -377,14 +414,33 @@ const char* m3scan_status_string(m3_status s) {
     case M3_ERR_ALIGN: return "M3_ERR_ALIGN: a pointer is not aligned as required";
     case M3_ERR_WORKSPACE: return "M3_ERR_WORKSPACE: workspace missing or too small";
     case M3_ERR_CUDA: return "M3_ERR_CUDA: a CUDA call or kernel launch failed";
+    case M3_ERR_TIMEOUT:
+      return "M3_ERR_TIMEOUT: a kernel gave up waiting for a tile copy; that call's outputs are incomplete";
   }
   return "unknown m3_status";
 }
 
-int32_t m3scan_version(void) { return 100; }
+int32_t m3scan_version(void) { return 10100; }
 
-m3_status m3scan_selftest_wait_timeout(m3_stream_t stream) {
-  if (note(launch_wait_timeout(reinterpret_cast<cudaStream_t>(stream))) != cudaSuccess) return M3_ERR_CUDA;
+m3_status m3scan_selftest_wait_timeout(void* workspace, m3_stream_t stream) {
+  if (workspace && !aligned(workspace, 256)) return M3_ERR_ALIGN;
+  if (note(launch_wait_timeout(static_cast<unsigned*>(workspace), reinterpret_cast<cudaStream_t>(stream))) !=
+      cudaSuccess)
+    return M3_ERR_CUDA;
+  return M3_OK;
+}
+
+m3_status m3scan_get_status(const void* workspace, m3_stream_t stream, m3_status* device_status) {
+  if (!workspace || !device_status) return M3_ERR_NULL;
+  if (!aligned(workspace, 256)) return M3_ERR_ALIGN;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  unsigned word = 0;
+  void* w = const_cast<void*>(workspace);
+  if (note(cudaMemcpyAsync(&word, w, sizeof(word), cudaMemcpyDeviceToHost, s)) != cudaSuccess ||
+      note(cudaStreamSynchronize(s)) != cudaSuccess)
+    return M3_ERR_CUDA;
+  if (word != 0 && note(cudaMemsetAsync(w, 0, sizeof(word), s)) != cudaSuccess) return M3_ERR_CUDA;
+  *device_status = word ? M3_ERR_TIMEOUT : M3_OK;
   return M3_OK;
 }
 
@@ -468,8 +524,10 @@ m3_status fwd_impl(const m3_dims* dims, m3_dtype act, const void* x, const void*
   for (const void* q : f_ptrs)
     if (!aligned(q, 4)) return M3_ERR_ALIGN;
   if (!aligned(ckpt, 16)) return M3_ERR_ALIGN;
-  if (p.Sf > 1) {
-    if (!workspace) return M3_ERR_WORKSPACE;
+  // a workspace is needed over several time segments; one that is given
+  // must be planned-size either way (its status block records failures)
+  if (p.Sf > 1 && !workspace) return M3_ERR_WORKSPACE;
+  if (workspace) {
     if (workspace_bytes < p.ws_bytes) return M3_ERR_WORKSPACE;
     if (!aligned(workspace, 256)) return M3_ERR_ALIGN;
   }
@@ -484,6 +542,7 @@ m3_status fwd_impl(const m3_dims* dims, m3_dtype act, const void* x, const void*
   a.agg_s = p.Sf > 1 ? reinterpret_cast<float*>(ws + p.f_aggs) : nullptr;
   a.h_in = sv.ssm_state; a.conv_in = sv.conv_state;
   a.h_out = sv.ssm_state_out; a.conv_out = sv.conv_state_out;
+  a.status = static_cast<unsigned*>(workspace);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   return act == M3_BF16 ? launch_fwd<__nv_bfloat16>(p, a, s) : launch_fwd<float>(p, a, s);
 }
@@ -565,6 +624,7 @@ m3_status bwd_impl(const m3_dims* dims, m3_dtype act, const void* x, const void*
   a.accumulate = dims->accumulate_param_grads ? 1 : 0;
   a.conv_in = sv.conv_state; a.g_h = sv.d_ssm_state_out; a.g_conv = sv.d_conv_state_out;
   a.d_h_in = sv.d_ssm_state; a.d_conv_in = sv.d_conv_state;
+  a.status = reinterpret_cast<unsigned*>(ws);
   m3_status r = act == M3_BF16 ? launch_bwd<__nv_bfloat16>(p, a, s, smem_sm, scan)
                                 : launch_bwd<float>(p, a, s, smem_sm, scan);
   if (r != M3_OK) cudaGetLastError();
@@ -676,6 +736,7 @@ m3_status m3scan_conv_bwd(const m3_dims* dims, m3_dtype act, const void* x, cons
   a.conv_in = sv.conv_state; a.g_conv = sv.d_conv_state_out; a.d_conv_in = sv.d_conv_state;
   a.d_conv_w = d_conv_w; a.d_conv_b = d_conv_b;
   a.accumulate = dims->accumulate_param_grads ? 1 : 0;
+  a.status = static_cast<unsigned*>(workspace);
   const dim3 grid((unsigned)((p.D + 127) / 128), (unsigned)p.cntiles, (unsigned)p.B);
   cudaError_t e = act == M3_BF16 ? launch_conv_bwd<__nv_bfloat16>(a, grid, s) : launch_conv_bwd<float>(a, grid, s);
   if (e == cudaSuccess) e = cudaGetLastError();
@@ -688,10 +749,17 @@ m3_status m3scan_conv_bwd(const m3_dims* dims, m3_dtype act, const void* x, cons
 namespace {
 
 std::mutex g_noalloc_mu;
-void* g_noalloc_addr[64];  // device address of g_noalloc_scratch, per device
+struct NoallocAddr {
+  void* addr = nullptr;        // device address of g_noalloc_scratch
+  unsigned long long ctx = 0;  // in this context (0: unknown)
+};
+NoallocAddr g_noalloc_addr[64];  // per device
 
-// Set-up for m3scan_bwd_noalloc, once per device with that device current:
-// look up the device address of the library's scratch array.
+// Set-up for m3scan_bwd_noalloc, once per device and context, with that
+// device current: look up the device address of the library's scratch
+// array.  A new context on the device (after cudaDeviceReset the module is
+// loaded again and the array may sit elsewhere) looks it up again; when the
+// driver cannot identify contexts it is looked up on every call.
 m3_status noalloc_scratch(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
@@ -699,16 +767,20 @@ m3_status noalloc_scratch(void** out) {
     return M3_ERR_CUDA;
   }
   std::lock_guard<std::mutex> lk(g_noalloc_mu);
-  if (!g_noalloc_addr[dev]) {
+  NoallocAddr& na = g_noalloc_addr[dev];
+  const unsigned long long ctx = current_context_id();
+  if (!na.addr || ctx == 0 || ctx != na.ctx) {
     void* p = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess || p == nullptr) {
       note(e != cudaSuccess ? e : cudaErrorInvalidSymbol);
+      na.addr = nullptr;
       return M3_ERR_CUDA;
     }
-    g_noalloc_addr[dev] = p;
+    na.addr = p;
+    na.ctx = current_context_id();  // the look-up made the context current if it was not
   }
-  *out = g_noalloc_addr[dev];
+  *out = na.addr;
   return M3_OK;
 }
 

@@ -58,7 +58,7 @@ __global__ void __launch_bounds__(128) m3_conv_bwd_kernel(const __grid_constant_
   }
   const bool landed = !misaligned && mbar_wait(&tbar, 0);
   if (__syncthreads_or(!landed)) {
-    if (tid == 0) atomicOr(&g_aux_status, 1u);
+    if (tid == 0) report_timeout(&g_aux_status, a.status);
     return;
   }
   if (!active) return;  // no barriers below
@@ -279,7 +279,7 @@ __global__ void __launch_bounds__(GD) m3_decode_kernel(const __grid_constant__ D
   if constexpr (TL) {
     const bool landed = !misaligned && mbar_wait(&tbar, 0);
     if (__syncthreads_or(!landed)) {
-      if (tid == 0) atomicOr(&g_aux_status, 1u);
+      if (tid == 0) report_timeout(&g_aux_status, nullptr);  // decode has no workspace
       return;
     }
     const float* hs = reinterpret_cast<const float*>(dsm) + tid / G;

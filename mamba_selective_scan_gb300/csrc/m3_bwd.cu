@@ -21,7 +21,7 @@ cudaError_t take_bwd_status(unsigned* out) {
 // Diagnostic: one block raises an mbarrier's transaction count but issues no
 // copy, so the phase never completes; the bounded wait must give up and the
 // failure must reach the status word, as in the scan kernels.
-__global__ void m3_wait_timeout_kernel() {
+__global__ void m3_wait_timeout_kernel(unsigned* ws_status) {
   __shared__ __align__(8) uint64_t bar;
   if (threadIdx.x == 0) {
     mbar_init(&bar, 1);
@@ -30,11 +30,11 @@ __global__ void m3_wait_timeout_kernel() {
   __syncthreads();
   if (threadIdx.x == 0) mbar_expect_tx(&bar, 16);
   const bool landed = mbar_wait(&bar, 0);
-  if (__syncthreads_or(!landed) && threadIdx.x == 0) atomicOr(&g_bwd_status, 1u);
+  if (__syncthreads_or(!landed) && threadIdx.x == 0) report_timeout(&g_bwd_status, ws_status);
 }
 
-cudaError_t launch_wait_timeout(cudaStream_t st) {
-  m3_wait_timeout_kernel<<<1, 32, 0, st>>>();
+cudaError_t launch_wait_timeout(unsigned* ws_status, cudaStream_t st) {
+  m3_wait_timeout_kernel<<<1, 32, 0, st>>>(ws_status);
   return cudaGetLastError();
 }
 
@@ -139,7 +139,7 @@ __global__ void __launch_bounds__(GB) m3_bwd_agg_kernel(const __grid_constant__ 
     if (__syncthreads_or(!landed)) {
       // a tile did not arrive: report it, let the copy issued above drain, leave
       if (tid == 0) {
-        atomicOr(&g_bwd_status, 1u);
+        report_timeout(&g_bwd_status, a.status);
         if (!misaligned && i + 1 < ntiles) mbar_wait(&tbar[buf ^ 1], ((i + 1) >> 1) & 1);
       }
       return;
@@ -347,7 +347,7 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(const __grid_constant__ B
     if (__syncthreads_or(!landed)) {
       // a tile did not arrive: report it, let the copy issued above drain, leave
       if (tid == 0) {
-        atomicOr(&g_bwd_status, 1u);
+        report_timeout(&g_bwd_status, a.status);
         if (!misaligned && c - 1 >= c_begin) mbar_wait(&tbar[buf ^ 1], ((it + 1) >> 1) & 1);
       }
       aborted = true;

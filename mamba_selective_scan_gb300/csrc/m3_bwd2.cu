@@ -178,7 +178,7 @@ __global__ void __launch_bounds__(128, 4) m3_bwd2_kernel(const __grid_constant__
     if (__syncthreads_or(!landed)) {
       // a tile did not arrive: report it, let the copy issued above drain, leave
       if (tid == 0) {
-        atomicOr(&g_bwd2_status, 1u);
+        report_timeout(&g_bwd2_status, a.status);
         if (!misaligned && c - 1 >= c_begin) mbar_wait(&tbar[buf ^ 1], ((it + 1) >> 1) & 1);
       }
       aborted = true;

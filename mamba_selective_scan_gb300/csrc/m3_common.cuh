@@ -186,6 +186,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
     else if (global_ns() - t0 > 1000000000ull) return false;
   }
 }
+// A kernel that gave up waiting for a tile copy records it in its
+// translation unit's per-device word and, when the call has a workspace, in
+// that workspace's status block (bits are only ever set on the device; the
+// host reads and clears them).
+__device__ __forceinline__ void report_timeout(unsigned* unit_word, unsigned* ws_word) {
+  atomicOr(unit_word, 1u);
+  if (ws_word) atomicOr(ws_word, 1u);
+}
+
 // orders this thread's view of earlier generic-proxy shared-memory accesses
 // (made visible to it by a block barrier) before its next tile copies
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
@@ -327,6 +336,8 @@ struct FwdArgs {
   const void* conv_in;
   float* h_out;
   void* conv_out;
+  // the workspace's status block (nullable: no workspace)
+  unsigned* status;
   // tile maps of the forward's staging (see TF_* below)
   CUtensorMap tm[5];
 };
@@ -363,6 +374,8 @@ struct BwdArgs {
   // the segments and adds them into the outputs (cleared by the aggregate
   // kernel unless accumulating) and finishes d_x at the segment boundaries
   int fin;
+  // the workspace's status block
+  unsigned* status;
   // tile maps of the backward's staging (see TM_* below)
   CUtensorMap tm[11];
 };
@@ -531,6 +544,7 @@ struct ConvArgs {
   void* d_conv_in;                // [B, 3, D] act, nullable
   float *d_conv_w, *d_conv_b;
   int accumulate;
+  unsigned* status;  // the workspace's status block
   // tile maps: x [B, T, D] with boxes of 128 channels x (CT + 6) rows, du
   // and du_extra with 128 x (CT + 3)
   CUtensorMap tm[3];
@@ -579,6 +593,9 @@ constexpr int GD = 128;  // decode: channels (= threads) per block
 // ---------------------------------------------------------------------------
 // host side: sizes, the plan, launching
 // ---------------------------------------------------------------------------
+
+// the workspace's status block (M3SCAN_STATUS_BYTES) comes first
+constexpr size_t STATUS_BYTES = M3SCAN_STATUS_BYTES;
 
 // opt-in shared memory per block, less 1 KB kept for static shared memory
 constexpr size_t SMEM_CAP = 227 * 1024 - 1024;
@@ -710,7 +727,7 @@ cudaError_t take_bwd2_status(unsigned* out);
 // carried state, d_state); provided by m3_bwd2.cu
 template <typename T> void (*bwd2_kernel_for(bool det, bool scan, bool st, int N))(BwdArgs);
 // one block whose tile wait never completes (diagnostic of the bounded waits)
-cudaError_t launch_wait_timeout(cudaStream_t st);
+cudaError_t launch_wait_timeout(unsigned* ws_status, cudaStream_t st);
 cudaError_t take_fwd_status(unsigned* out);
 cudaError_t take_aux_status(unsigned* out);
 

@@ -22,12 +22,13 @@ cudaError_t take_fwd_status(unsigned* out) {
 // timeout every thread of the block learns it at the block barrier; thread
 // 0 reports it and lets the copy it issued into the other buffer (if any)
 // drain, and the caller leaves.  Returns false then.
-__device__ __forceinline__ bool fwd_tiles_landed(uint64_t* tbar, int it, bool misaligned, bool other_in_flight) {
+__device__ __forceinline__ bool fwd_tiles_landed(uint64_t* tbar, int it, bool misaligned, bool other_in_flight,
+                                                 unsigned* ws_status) {
   const int buf = it & 1;
   const bool landed = !misaligned && mbar_wait(&tbar[buf], (it >> 1) & 1);
   if (!__syncthreads_or(!landed)) return true;
   if (threadIdx.x == 0) {
-    atomicOr(&g_fwd_status, 1u);
+    report_timeout(&g_fwd_status, ws_status);
     if (!misaligned && other_in_flight) mbar_wait(&tbar[buf ^ 1], ((it + 1) >> 1) & 1);
   }
   return false;
@@ -139,7 +140,7 @@ __global__ void __launch_bounds__(GF) m3_fwd_kernel(const __grid_constant__ FwdA
   for (int t0 = t_begin, it = 0; t0 < t_end; t0 += TT, ++it) {
     const int buf = it & 1;
     if (t0 + TT < t_end) stage(t0 + TT, buf ^ 1);
-    if (!fwd_tiles_landed(tbar, it, misaligned, t0 + TT < t_end)) return;
+    if (!fwd_tiles_landed(tbar, it, misaligned, t0 + TT < t_end, a.status)) return;
     const unsigned char* base = smem + (size_t)buf * L.tile;
     {
       const T* Bt = reinterpret_cast<const T*>(base + L.Bt);
@@ -355,7 +356,7 @@ __global__ void __launch_bounds__(128) m3_fwd2_kernel(const __grid_constant__ Fw
   for (int t0 = t_begin, it = 0; t0 < t_end; t0 += TT, ++it) {
     const int buf = it & 1;
     if (t0 + TT < t_end) stage(t0 + TT, buf ^ 1);
-    if (!fwd_tiles_landed(tbar, it, misaligned, t0 + TT < t_end)) return;
+    if (!fwd_tiles_landed(tbar, it, misaligned, t0 + TT < t_end, a.status)) return;
     unsigned char* base = smem + (size_t)buf * L.tile;
     if (a.conv_in && t0 < 3 && active && hf == 0) {
       // halo rows before step 0 (staged as zeros): the carried conv inputs

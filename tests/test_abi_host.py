@@ -40,7 +40,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert binding.m3scan_version() == 100
+    assert binding.m3scan_version() == 10100  # 1.1.0
     for code, name in binding.STATUS.items():
         assert binding.m3scan_status_string(code).startswith(name)
     assert "unknown" in binding.m3scan_status_string(99)
@@ -340,6 +340,23 @@ def test_wider_states_resolve_to_the_split_kernels(lib):
 
 def test_device_status_rejects_null(lib):
     assert lib.m3scan_device_status(None) == 1  # M3_ERR_NULL
+
+
+def test_get_status_rejects_null_and_misaligned_before_touching_a_device(lib):
+    out = ctypes.c_int(0)
+    assert binding.STATUS[lib.m3scan_get_status(None, None, ctypes.byref(out))] == "M3_ERR_NULL"
+    assert binding.STATUS[lib.m3scan_get_status(1 << 20, None, None)] == "M3_ERR_NULL"
+    assert binding.STATUS[lib.m3scan_get_status((1 << 20) + 16, None, ctypes.byref(out))] == \
+        "M3_ERR_ALIGN"
+    assert binding.STATUS[lib.m3scan_selftest_wait_timeout((1 << 20) + 16, None)] == "M3_ERR_ALIGN"
+
+
+def test_workspace_begins_with_the_status_block(lib):
+    """Every section of the workspace starts after the status block, and the
+    smallest workspace holds it."""
+    dims = binding.make_dims(1, 8, 8, chunk=8, segments=1)
+    pl = binding.m3scan_plan(dims, binding.M3_F32)
+    assert pl.workspace_bytes >= binding.STATUS_BYTES == 256
 
 
 def test_deterministic_adds_block_partials_to_the_workspace(lib):

@@ -194,18 +194,38 @@ def test_device_status_stays_clear():
         inp, gpu, ref = _case(2, 130, 136, act, seed=77, chunk=chunk, segments=seg, tpc=2)
         assert_close(compare(gpu, ref, act), f"status case {act} K={chunk}")
     assert binding.m3scan_device_status() == 0
+    # the same through a workspace's status block
+    inp = make_inputs(2, 130, 136, act="bf16", seed=78)
+    dev = to_device(inp)
+    dims = binding.make_dims(2, 130, 136, chunk=8, segments=3)
+    ws = binding.Workspace(binding.m3scan_plan(dims, binding.M3_BF16).workspace_bytes, "cuda:0")
+    gated, ckpt, _ = binding.m3scan_fwd(dev["x"], dev["delta_raw"], dev["z"], dev["B"], dev["C"],
+                                        dev["conv_w"], dev["conv_b"], dev["dt_bias"],
+                                        dev["a_log"], dev["D"], chunk=8, segments=3, workspace=ws)
+    binding.m3scan_bwd(dev["x"], dev["delta_raw"], dev["z"], dev["B"], dev["C"], dev["conv_w"],
+                       dev["conv_b"], dev["dt_bias"], dev["a_log"], dev["D"], ckpt,
+                       dev["d_gated"], chunk=8, segments=3, workspace=ws)
+    assert binding.m3scan_get_status(ws) == 0
 
 
 def test_bounded_tile_wait_gives_up_and_reports():
-    """A block whose tile copy never lands gives up after about a second,
-    the failure reaches the device status word, reading clears it, and the
-    context stays usable for a normal call afterwards."""
+    """A block whose tile copy never lands gives up after about a second;
+    the failure reaches the workspace's status block (m3scan_get_status:
+    M3_ERR_TIMEOUT, and reading clears it) and the device status word; and
+    the context stays usable for a normal call afterwards."""
     import time
     binding.m3scan_device_status()
+    ws = binding.Workspace(4096, "cuda:0")
+    other = binding.Workspace(4096, "cuda:0")
+    s = torch.cuda.current_stream()
+    assert binding.m3scan_get_status(ws) == 0
     t0 = time.time()
-    binding.m3scan_selftest_wait_timeout(0)
-    assert binding.m3scan_device_status() != 0
+    binding.m3scan_selftest_wait_timeout(s.cuda_stream, workspace=ws)
+    assert binding.STATUS[binding.m3scan_get_status(ws)] == "M3_ERR_TIMEOUT"
     assert time.time() - t0 < 30
+    assert binding.m3scan_get_status(ws) == 0      # cleared by the read
+    assert binding.m3scan_get_status(other) == 0   # another workspace saw nothing
+    assert binding.m3scan_device_status() != 0
     assert binding.m3scan_device_status() == 0
     inp, gpu, ref = _case(1, 40, 24, "f32", seed=5, chunk=8, segments=2, tpc=2)
     assert_close(compare(gpu, ref, "f32"), "after the timeout diagnostic")

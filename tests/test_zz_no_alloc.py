@@ -37,26 +37,34 @@ def test_noalloc_rejects_shapes_beyond_its_scratch_before_any_launch():
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("act", ["bf16", "f32"])
-def test_noalloc_backward_matches_workspace_backward_twice(act):
+@pytest.mark.parametrize("act,tpc,det", [
+    ("bf16", 0, False), ("f32", 0, False),
+    # the fixed-order sums keep the channel blocks' dB/dC shares in the
+    # scratch as well; the second call must not read the first call's
+    ("bf16", 1, True), ("f32", 2, True),
+    ("bf16", 1, False), ("bf16", 2, False),
+])
+def test_noalloc_backward_matches_workspace_backward_twice(act, tpc, det):
     torch = pytest.importorskip("torch")
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     from parity_util import TOL, norm_err, to_device, to_np
     build.build()
     batch, T, D = 2, 200, 136
-    inp = make_inputs(batch, T, D, act=act, seed=77)
+    # per-channel parameters, so a wrong channel's a_log, conv_b or D shows
+    inp = make_inputs(batch, T, D, act=act, seed=77, random_params=True)
     dev = to_device(inp)
+    kw = dict(chunk=16, segments=3, threads_per_channel=tpc)
     gated, ckpt, _ = binding.m3scan_fwd(dev["x"], dev["delta_raw"], dev["z"], dev["B"],
                                         dev["C"], dev["conv_w"], dev["conv_b"],
-                                        dev["dt_bias"], dev["a_log"], dev["D"], chunk=16,
-                                        segments=3)
+                                        dev["dt_bias"], dev["a_log"], dev["D"], **kw)
     ref = binding.m3scan_bwd(dev["x"], dev["delta_raw"], dev["z"], dev["B"], dev["C"],
                              dev["conv_w"], dev["conv_b"], dev["dt_bias"], dev["a_log"],
-                             dev["D"], ckpt, dev["d_gated"], chunk=16, segments=3, want_du=True)
+                             dev["D"], ckpt, dev["d_gated"], want_du=True, deterministic=det,
+                             **kw)
     torch.cuda.synchronize()
     ref = {k: to_np(v) for k, v in ref.items()}
-    dims = binding.make_dims(batch, T, D, chunk=16, segments=3)
+    dims = binding.make_dims(batch, T, D, deterministic=det, **kw)
     code = binding.M3_BF16 if act == "bf16" else binding.M3_F32
     stream = torch.cuda.current_stream().cuda_stream
     for call in range(2):
@@ -79,5 +87,7 @@ def test_noalloc_backward_matches_workspace_backward_twice(act):
         for k in GRADS:
             got = to_np(out[k])
             assert np.isfinite(got).all(), (call, k)
+            if det:  # fixed-order sums: the same bits as the workspace call
+                assert np.array_equal(got, ref[k]), (call, k)
             err = norm_err(got, ref[k])
             assert err <= TOL[act][k], (call, k, err)
