@@ -36,8 +36,9 @@ from mamba_selective_scan_gb300.inputs import WORKLOADS, make_workload_inputs  #
 
 METRIC = "selective-scan fwd+bwd Gelem/s (B*T*d_inner) and % of GB300 HBM roofline"
 UNIT = "Gelem/s"
-DEFAULT_WORKLOAD = "trainer_b8_t128_d512"
-EXTRA_WORKLOADS = ("m130m_b8_t2048_d1536", "longseq_b1_t65536_d2048", "m2p8b_b4_t4096_d5120")
+# the largest configuration that fits one GPU (134 M elements per step)
+DEFAULT_WORKLOAD = "longseq_b1_t65536_d2048"
+EXTRA_WORKLOADS = ("trainer_b8_t128_d512", "m130m_b8_t2048_d1536", "m2p8b_b4_t4096_d5120")
 HBM_TARGET_GBS = 8000.0  # the roofline bandwidth the metric is defined with
 ROOFLINE_CHUNK = 128     # chunk length of the metric's minimum-bytes formula
 NS = 16
@@ -280,7 +281,8 @@ class Layer:
             "d_dt_bias": torch.empty((D,), **f32), "d_a_log": torch.empty((D, NS), **f32),
             "dD": torch.empty((D,), **f32),
         }
-        self.ws = torch.empty(max(int(self.plan.workspace_bytes), 256), dtype=torch.uint8,
+        # zeroed: the library's status block at its start must begin at zero
+        self.ws = torch.zeros(max(int(self.plan.workspace_bytes), 256), dtype=torch.uint8,
                               device=dev)
         self.binding = binding
 
@@ -450,31 +452,46 @@ def gpu_arm(args):
     value = job_gelem_s(world, E, args.steps, total_ms)
     fwd_avg = sum(f_ms) / len(f_ms)
     bwd_avg = sum(b_ms) / len(b_ms)
+    fwd_med = statistics.median(f_ms)
+    bwd_med = statistics.median(b_ms)
+    step_med = statistics.median([a + b for a, b in zip(f_ms, b_ms)])
     fb, bb = algorithmic_bytes(w.batch, w.seq_len, w.d_inner, es)
     peak, peak_kind = measured_peaks()
     step_s = (fwd_avg + bwd_avg) * 1e-3
+    # The roofline of the metric: the minimum bytes the fused method moves
+    # (checkpoints every 128 steps) over the measured HBM copy bandwidth, for
+    # the dominant call (the backward: aggregate, main and any finishing
+    # kernels of one m3scan_bwd, timed by CUDA events around its graph).
     bwd_achieved = bb / (bwd_avg * 1e-3) / 1e9
-    # The layer core is bound by instruction issue and FP32/MUFU arithmetic,
-    # not by HBM (DRAM is under 20 % busy in every kernel): the roofline is the
-    # FP32 lane-op rate of the backward call, the dominant launch sequence.
     alu_peak = alu_peak_gops()
     bwd_gops = BWD_FP32_OPS_PER_ELEM * E / (bwd_avg * 1e-3) / 1e9
     parts = (["aggregate"] if int(layer.plan.bwd_segments) > 1 else []) + ["main"]
     parts += ["tail", "dB/dC sum"][:max(0, int(layer.plan.bwd_launches) - len(parts))]
     bwd_kernels = " + ".join(parts) + (" kernels" if len(parts) > 1 else " kernel")
-    roofline = {"bound": "alu", "kernel": f"m3scan_bwd ({bwd_kernels})",
-                "achieved": round(bwd_gops, 1), "peak": round(alu_peak, 1), "unit": "Gop/s",
-                "frac": round(bwd_gops / alu_peak, 4),
-                "peak_kind": "derived: 152 SMs x 128 FP32 lanes x max SM clock",
-                "ops_per_element": BWD_FP32_OPS_PER_ELEM,
+    roofline = {"bound": "hbm", "kernel": f"m3scan_bwd ({bwd_kernels})",
+                "achieved": round(bwd_achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(bwd_achieved / peak, 4), "peak_kind": peak_kind,
                 "traffic": ncu_traffic(args.workload, "bwd"),
-                "hbm_achieved_gbs": round(bwd_achieved, 1), "hbm_peak_gbs": peak,
-                "hbm_peak_kind": peak_kind, "algorithmic_bytes_per_launch": bb}
+                "algorithmic_bytes_per_launch": bb,
+                "bytes_per_element": round(bb / E, 3),
+                "time": "mean call time over the timed steps",
+                "median": {"achieved": round(bb / (bwd_med * 1e-3) / 1e9, 1),
+                           "frac": round(bb / (bwd_med * 1e-3) / 1e9 / peak, 4)},
+                # the path's binding resource: FP32 lane operations
+                "alu": {"achieved": round(bwd_gops, 1), "peak": round(alu_peak, 1),
+                        "unit": "Gop/s", "frac": round(bwd_gops / alu_peak, 4),
+                        "ops_per_element": BWD_FP32_OPS_PER_ELEM,
+                        "peak_kind": "derived: 152 SMs x 128 FP32 lanes x max SM clock"}}
     hbm = {"min_bytes_fwd_bwd": fb + bb, "chunk_for_min_bytes": ROOFLINE_CHUNK,
            "frac_of_8TBs": round((fb + bb) / HBM_TARGET_GBS / 1e9 / step_s, 4),
            "frac_of_measured": round((fb + bb) / peak / 1e9 / step_s, 4),
            "fwd_gelem_s": round(E / (fwd_avg * 1e-3) / 1e9, 2),
-           "bwd_gelem_s": round(E / (bwd_avg * 1e-3) / 1e9, 2)}
+           "bwd_gelem_s": round(E / (bwd_avg * 1e-3) / 1e9, 2),
+           "median": {"ms_per_step": round(step_med, 5),
+                      "gelem_s": round(E / (step_med * 1e-3) / 1e9, 3),
+                      "fwd_gelem_s": round(E / (fwd_med * 1e-3) / 1e9, 2),
+                      "bwd_gelem_s": round(E / (bwd_med * 1e-3) / 1e9, 2),
+                      "frac_of_measured": round((fb + bb) / peak / 1e9 / (step_med * 1e-3), 4)}}
 
     # end to end through the public binding with pinned host buffers
     e2e = e2e_measure(torch, binding, layer, tensors, min(args.steps, 50), device)
@@ -493,6 +510,8 @@ def gpu_arm(args):
                    "d_inner": w.d_inner, "d_state": NS, "d_conv": 4, "act_storage": w.act,
                    "chunk": int(layer.plan.chunk), "fwd_segments": int(layer.plan.fwd_segments),
                    "bwd_segments": int(layer.plan.bwd_segments),
+                   "fwd_launches": int(layer.plan.fwd_launches),
+                   "bwd_launches": int(layer.plan.bwd_launches),
                    "l2": "flushed before every step (256 MiB memset outside the events)",
                    "timing": "CUDA graphs (fwd, bwd) per step, CUDA events per graph",
                    "parallelism": f"replicas x{world}"},
@@ -841,19 +860,56 @@ def stack24(torch, binding, device, args, stream):
 # CPU oracle timing (baseline and reference arm)
 # ---------------------------------------------------------------------------
 
-def oracle_sample_rate(inp, channels):
-    """Time the oracle's forward + backward on the first `channels`
-    channels (all batches and steps) of the workload; returns (elements, s)."""
+def channel_sample(inp, channels):
+    """The workload restricted to its first `channels` channels (all batches
+    and steps): every per-channel tensor and parameter sliced, B and C whole.
+    Channels are independent recurrences, so the oracle computes these
+    channels exactly (dB and dC become their sums over the sample)."""
     import numpy as np
+    from mamba_selective_scan_gb300.inputs import Inputs
+    per_elem = ("x", "delta_raw", "z", "d_gated")
+    per_chan = ("conv_w", "conv_b", "dt_bias", "a_log", "D")
+    arrays = {}
+    for k, v in inp.arrays.items():
+        if k in per_elem:
+            arrays[k] = np.ascontiguousarray(v[:, :, :channels])
+        elif k in per_chan:
+            arrays[k] = np.ascontiguousarray(v[:channels])
+        else:
+            arrays[k] = v
+    return Inputs(inp.batch, inp.seq_len, channels, inp.d_state, inp.d_conv, inp.act, arrays)
 
+
+def oracle_sample_rate(inp, channels):
+    """Time the single-threaded oracle's forward + backward on the first
+    `channels` channels (all batches and steps) of the workload; returns
+    (elements, s).  The slicing is outside the timed region."""
     import oracle
-    mask = np.zeros(inp.d_inner, dtype=np.uint8)
-    mask[:channels] = 1
+    sub = channel_sample(inp, channels)
     t0 = time.perf_counter()
-    oracle.forward(inp, chan_mask=mask)
-    oracle.backward(inp, chan_mask=mask)
+    oracle.forward(sub)
+    oracle.backward(sub)
     dt = time.perf_counter() - t0
     return inp.batch * inp.seq_len * channels, dt
+
+
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return "unknown"
 
 
 def pick_channels(inp, seconds):
@@ -870,13 +926,37 @@ def pick_channels(inp, seconds):
 
 
 def cpu_baseline(inp, seconds):
+    """The float64 oracle on the host cores, on a bounded channel sample of
+    the workload: single-threaded (the pinned oracle as it stands), and on
+    every core (the same oracle, one block of channels per OpenMP thread)."""
     import oracle
     oracle.build()
-    ch, _ = pick_channels(inp, seconds)
-    e, dt = oracle_sample_rate(inp, ch)
-    return {"value": round(e / dt / 1e9, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"first {ch} of {inp.d_inner} channels, all batches and steps, "
-                      f"fwd+bwd, float64 C, single thread ({dt:.1f} s)"}
+    host_cores = os.cpu_count() or 1
+    ch1, _ = pick_channels(inp, seconds)
+    e1, t1 = oracle_sample_rate(inp, ch1)
+    single = {"value": round(e1 / t1 / 1e9, 6), "unit": UNIT, "cores": 1,
+              "sample": f"first {ch1} of {inp.d_inner} channels, all batches and steps, "
+                        f"fwd+bwd ({t1:.1f} s)"}
+    try:
+        oracle.build_par()
+    except Exception as e:  # no OpenMP on this host: the single-threaded figure only
+        return {"value": single["value"], "unit": UNIT, "cores": 1, "kind": "oracle",
+                "host_cores": host_cores, "model": cpu_model(),
+                "sample": single["sample"] + ", float64 C oracle, single thread",
+                "single_thread": single, "all_cores": None, "note": f"all-core driver: {e}"}
+    chn = min(inp.d_inner, ch1 * host_cores)
+    sub = channel_sample(inp, chn)
+    t0 = time.perf_counter()
+    _, used = oracle.forward_backward_all_cores(sub, 0)
+    tn = time.perf_counter() - t0
+    en = inp.batch * inp.seq_len * chn
+    return {"value": round(en / tn / 1e9, 6), "unit": UNIT, "cores": used, "kind": "oracle",
+            "host_cores": host_cores, "model": cpu_model(),
+            "sample": f"first {chn} of {inp.d_inner} channels, all batches and steps, fwd+bwd, "
+                      f"float64 C oracle on {used} OpenMP threads, one block of channels each "
+                      f"({tn:.1f} s)",
+            "single_thread": single,
+            "all_cores": {"value": round(en / tn / 1e9, 6), "unit": UNIT, "cores": used}}
 
 
 def reference_arm(args):
@@ -910,7 +990,8 @@ def reference_arm(args):
             "config": {"workload": args.workload, "batch": w.batch, "seq_len": w.seq_len,
                        "d_inner": w.d_inner, "d_state": NS, "d_conv": 4, "act_storage": w.act},
             "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": 1,
-                             "kind": "oracle", "sample": sample},
+                             "kind": "oracle", "sample": sample, "model": cpu_model(),
+                             "host_cores": os.cpu_count()},
             "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)

@@ -204,5 +204,73 @@ def loss(inp, d_gated=None, ssm_state=None, conv_state=None, d_ssm_state_out=Non
     return L
 
 
+# ---------------------------------------------------------------------------
+# All-core timing driver (m3scan_oracle_par.c): the same oracle on every host
+# core, one block of channels per OpenMP thread.  Used by the benchmark's
+# CPU baseline; the tests compare it with the single-threaded functions above.
+# ---------------------------------------------------------------------------
+
+_PAR_SRC = os.path.join(_HERE, "m3scan_oracle_par.c")
+_PAR_LIB_PATH = os.path.join(_BUILD_DIR, "libm3oracle_par.so")
+_par_lib = None
+
+
+def build_par(force: bool = False) -> str:
+    """Compile the all-core driver (the oracle source included unchanged,
+    same float64 flags, plus OpenMP)."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    newest = max(os.path.getmtime(_SRC), os.path.getmtime(_PAR_SRC))
+    if not force and os.path.exists(_PAR_LIB_PATH) and os.path.getmtime(_PAR_LIB_PATH) >= newest:
+        return _PAR_LIB_PATH
+    tmp = _PAR_LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-fPIC", "-shared", "-std=c11", "-fno-fast-math", "-ffp-contract=off",
+           "-fopenmp", "-I", _HERE, "-o", tmp, _PAR_SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _PAR_LIB_PATH)
+    return _PAR_LIB_PATH
+
+
+def _load_par():
+    global _par_lib
+    with _lock:
+        if _par_lib is None:
+            lib = ctypes.CDLL(build_par())
+            lib.m3o_fwd_bwd_par.restype = ctypes.c_int
+            lib.m3o_fwd_bwd_par.argtypes = ([_i64] * 5 + [_dp] * 11 + [ctypes.c_int] + [_dp] * 11
+                                            + [ctypes.POINTER(ctypes.c_int)])
+            _par_lib = lib
+    return _par_lib
+
+
+def forward_backward_all_cores(inp, threads: int = 0):
+    """Forward ``gated`` and the backward of L = sum(gated * d_gated) (no
+    carried state) on ``threads`` OpenMP threads (0 = all cores).  Returns
+    (dict of float64 arrays named as in ``forward``/``backward``, threads
+    used)."""
+    lib = _load_par()
+    (Bsz, T, D, N, W), a = _common(inp)
+    g = _c64(inp["d_gated"])
+    out = {k: np.zeros((Bsz, T, D)) for k in ("gated", "d_x", "d_delta_raw", "dz")}
+    out["dB"] = np.zeros((Bsz, T, N))
+    out["dC"] = np.zeros((Bsz, T, N))
+    out["d_conv_w"] = np.zeros((D, W))
+    out["d_conv_b"] = np.zeros(D)
+    out["d_dt_bias"] = np.zeros(D)
+    out["d_a_log"] = np.zeros((D, N))
+    out["dD"] = np.zeros(D)
+    used = ctypes.c_int(0)
+    rc = lib.m3o_fwd_bwd_par(Bsz, T, D, N, W, _ptr(a["x"]), _ptr(a["delta_raw"]), _ptr(a["z"]),
+                             _ptr(a["B"]), _ptr(a["C"]), _ptr(a["conv_w"]), _ptr(a["conv_b"]),
+                             _ptr(a["dt_bias"]), _ptr(a["a_log"]), _ptr(a["D"]), _ptr(g),
+                             int(threads), _ptr(out["gated"]), _ptr(out["d_x"]),
+                             _ptr(out["d_delta_raw"]), _ptr(out["dz"]), _ptr(out["dB"]),
+                             _ptr(out["dC"]), _ptr(out["d_conv_w"]), _ptr(out["d_conv_b"]),
+                             _ptr(out["d_dt_bias"]), _ptr(out["d_a_log"]), _ptr(out["dD"]),
+                             ctypes.byref(used))
+    if rc != 0:
+        raise MemoryError("oracle (all cores): allocation failed")
+    return out, int(used.value)
+
+
 if __name__ == "__main__":  # pragma: no cover
     print(build(force="--force" in sys.argv))
