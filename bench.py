@@ -413,7 +413,8 @@ def gpu_arm(args):
     es = 2 if w.act == "bf16" else 4
     inp = make_workload_inputs(args.workload)
     tensors = host_inputs_to_device(torch, inp, device)
-    layer = Layer(torch, binding, tensors, chunk=args.chunk, segments=args.segments)
+    layer = Layer(torch, binding, tensors, chunk=args.chunk, segments=args.segments,
+                  threads_per_channel=args.threads_per_channel)
     stream = torch.cuda.Stream(device)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
 
@@ -494,8 +495,9 @@ def gpu_arm(args):
                       "frac_of_measured": round((fb + bb) / peak / 1e9 / (step_med * 1e-3), 4)}}
 
     # end to end through the public binding with pinned host buffers
-    e2e = e2e_measure(torch, binding, layer, tensors, min(args.steps, 50), device)
-    if dist is not None:  # whole-job figures: every replica's elements over the slowest time
+    e2e = None if args.no_e2e else e2e_measure(torch, binding, layer, tensors,
+                                               min(args.steps, 50), device)
+    if dist is not None and e2e is not None:  # whole-job figures: every replica's elements over the slowest time
         for part in (e2e, e2e["serial"], e2e["eager"]):
             ms = max_over_ranks(dist, part["ms_per_step"], device)
             part["ms_per_step"] = round(ms, 5)
@@ -1006,10 +1008,14 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--chunk", type=int, default=0)
     ap.add_argument("--segments", type=int, default=0)
+    ap.add_argument("--threads-per-channel", type=int, default=0,
+                    help="kernel variant (0 = chosen by the plan, 1 or 2)")
     ap.add_argument("--extra-steps", type=int, default=20)
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--no-stack", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true",
+                    help="leave out the end-to-end measurement (kernel sweeps and profiling)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--decode-only", action="store_true",
                     help="run only the one-token decode measurements (for profiling)")

@@ -92,9 +92,14 @@ typedef enum {
 
 typedef struct {
     int64_t batch, seq_len, d_inner, d_state, d_conv;
-    /* Checkpoint interval K in steps; 0 = library default (8).  At most 64,
-       and small enough for the backward's shared memory (30 for bf16
-       activations, 23 for f32); larger values give M3_ERR_UNSUPPORTED. */
+    /* Checkpoint interval K in steps: the forward writes the state before
+       every K-th step, the backward recomputes from there.  0 = library
+       default (8).  1..8, or a multiple of 8 up to 256 (other values:
+       M3_ERR_UNSUPPORTED; above 256: M3_ERR_DIMS).  The backward recomputes
+       at most 8 steps on chip at a time: with K > 8 it first runs each chunk
+       forward from its checkpoint to the start of every 8-step tile, keeping
+       those states in the workspace (m3scan_plan sizes it), so a longer
+       chunk moves fewer checkpoint bytes through HBM for more arithmetic. */
     int64_t chunk;
     /* Number of time segments scanned in parallel (each segment is a run of
        whole chunks); 0 = chosen from the shape and the current device. */

@@ -77,8 +77,8 @@ struct DevInfo {
   unsigned long long ctx = 0;  // context the attributes were set in (0: unknown)
   int sms = 0;
   int smem_per_sm = 0;
-  int occ_fwd[2][KMAX + 1];  // [dtype][chunk] blocks per SM, 0 = not yet queried
-  int occ_bwd[2][KMAX + 1];
+  int occ_fwd[2][KT + 1];  // [dtype][backward tile] blocks per SM, 0 = not yet queried
+  int occ_bwd[2][KT + 1];
 };
 
 std::mutex g_mu;
@@ -135,8 +135,10 @@ cudaError_t set_attrs() {
 }
 
 // Device facts for the current device: kernel attributes are set once per
-// device (with that device current), occupancy is queried once per chunk.
+// device (with that device current), occupancy is queried once per backward
+// tile length (chunk = that tile, at most KT).
 cudaError_t device_info(int chunk, int ai, int* sms, int* occ_f, int* occ_b, int* smem_sm = nullptr) {
+  if (chunk < 1 || chunk > KT) return cudaErrorInvalidValue;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -155,7 +157,7 @@ cudaError_t device_info(int chunk, int ai, int* sms, int* occ_f, int* occ_b, int
     e = cudaDeviceGetAttribute(&di.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
     if (e != cudaSuccess) return e;
     for (int a = 0; a < 2; ++a)
-      for (int k = 0; k <= KMAX; ++k) di.occ_fwd[a][k] = di.occ_bwd[a][k] = 0;
+      for (int k = 0; k <= KT; ++k) di.occ_fwd[a][k] = di.occ_bwd[a][k] = 0;
     di.attrs = true;
     di.ctx = current_context_id();  // the set-up above made the context current if it was not
   }
@@ -247,6 +249,18 @@ int best_bwd_segments(int nc, int K, int64_t per_seg, int64_t W) {
   return best_S;
 }
 
+// The checkpoint interval a call gets when it asks for none.  Measured on
+// GB300 (bf16, long-sequence and Mamba-130M-like layers): 8-step chunks,
+// whose backward recomputes each tile straight from its checkpoint, run
+// fwd+bwd 16-19 % faster than 64- or 128-step chunks, whose backward first
+// recomputes the sub-checkpoints of every chunk; the layer core is bound by
+// instruction issue, not by the 16 bytes per element the 8-step checkpoints
+// add to HBM traffic.
+int default_chunk(int64_t seq_len) {
+  (void)seq_len;
+  return KSHORT;
+}
+
 m3_status validate_dims(const m3_dims* dm, m3_dtype act) {
   if (!dm) return M3_ERR_NULL;
   if (act != M3_F32 && act != M3_BF16) return M3_ERR_UNSUPPORTED;
@@ -258,7 +272,8 @@ m3_status validate_dims(const m3_dims* dm, m3_dtype act) {
   if (dm->d_state != NS && dm->threads_per_channel == 1) return M3_ERR_UNSUPPORTED;
   if (dm->d_inner % 8 != 0) return M3_ERR_UNSUPPORTED;
   if (dm->chunk > KMAX) return M3_ERR_DIMS;
-  if (dm->chunk > kmax_for(act == M3_BF16 ? 2 : 4)) return M3_ERR_UNSUPPORTED;
+  // a chunk longer than the backward's on-chip tile is a whole number of tiles
+  if (dm->chunk > KT && dm->chunk % KT != 0) return M3_ERR_UNSUPPORTED;
   if (dm->batch > 65535 || dm->seq_len > (int64_t)1 << 30 || dm->d_inner > (int64_t)1 << 24)
     return M3_ERR_DIMS;
   if (dm->segments > 65535) return M3_ERR_DIMS;
@@ -283,8 +298,14 @@ m3_status make_plan(const m3_dims* dm, m3_dtype act, Plan* p) {
   p->T = (int)dm->seq_len;
   p->D = (int)dm->d_inner;
   p->N = (int)dm->d_state;
-  p->K = dm->chunk ? (int)dm->chunk : KDEF;
+  // default checkpoint interval
+  p->K = dm->chunk ? (int)dm->chunk : default_chunk(dm->seq_len);
   p->nc = (p->T + p->K - 1) / p->K;
+  p->KS = p->K < KT ? p->K : KT;
+  {
+    const int nt_max = (p->K + p->KS - 1) / p->KS;
+    p->nsk = nt_max > 2 ? nt_max - 2 : 0;
+  }
   p->ldbc = dm->bc_stride ? (int)dm->bc_stride : p->N;
   p->lddbc = dm->dbc_stride ? (int)dm->dbc_stride : p->N;
   const int groups_f = (p->D + GF - 1) / GF;
@@ -297,7 +318,7 @@ m3_status make_plan(const m3_dims* dm, m3_dtype act, Plan* p) {
     want_f = want_b = (int)dm->segments;
   } else if ((int64_t)p->B * p->T * p->D > 0) {
     int sms = 0, of = 0, ob = 0;
-    if (note(device_info(p->K, act == M3_BF16 ? 1 : 0, &sms, &of, &ob)) != cudaSuccess)
+    if (note(device_info(KT, act == M3_BF16 ? 1 : 0, &sms, &of, &ob)) != cudaSuccess)
       return M3_ERR_CUDA;
     want_f = choose_segments(p->nc, p->K, (int64_t)p->B * groups_f, (int64_t)sms * of, 2);
     wave_b = (int64_t)sms * 3;  // three resident one-thread blocks per SM (measured; the
@@ -375,6 +396,13 @@ m3_status make_plan(const m3_dims* dm, m3_dtype act, Plan* p) {
   // channel block of the backward's main kernel)
   p->dblk = (p->D + (p->bwd_tpc != 1 ? 128 / p->bwd_tpc : GB) - 1) / (p->bwd_tpc != 1 ? 128 / p->bwd_tpc : GB);
   p->b_dbc = p->det ? take(B * (size_t)p->T * p->dblk * 2 * N * 4) : 0;
+  // sub-checkpoints: the states before tiles 1 .. nt-2 of the chunk a block
+  // of the main kernel is working on
+  {
+    const size_t ch = p->bwd_tpc != 1 ? 128 / p->bwd_tpc : GB;
+    const size_t blocks = (size_t)p->dblk * p->Sb * B;
+    p->b_sk = p->nsk > 0 && !empty ? take(blocks * p->nsk * N * ch * 4) : 0;
+  }
   size_t bwd_total = off;
   // conv backward of the two-phase backward (its own call): CT-step tiles
   p->ctile = CT;
@@ -532,7 +560,7 @@ m3_status fwd_impl(const m3_dims* dims, m3_dtype act, const void* x, const void*
     if (!aligned(workspace, 256)) return M3_ERR_ALIGN;
   }
   int smem_sm = 0;
-  if (ensure_device(p.K, act == M3_BF16 ? 1 : 0, &smem_sm) != M3_OK) return M3_ERR_CUDA;
+  if (ensure_device(KT, act == M3_BF16 ? 1 : 0, &smem_sm) != M3_OK) return M3_ERR_CUDA;
   FwdArgs a{};
   a.x = x; a.dr = delta_raw; a.z = z; a.Bm = Bm; a.Cm = Cm;
   a.conv_w = conv_w; a.conv_b = conv_b; a.dt_bias = dt_bias; a.a_log = a_log; a.Dp = D;
@@ -600,7 +628,7 @@ m3_status bwd_impl(const m3_dims* dims, m3_dtype act, const void* x, const void*
   if (workspace_bytes < p.ws_bytes) return M3_ERR_WORKSPACE;
   if (!aligned(workspace, 256)) return M3_ERR_ALIGN;
   int smem_sm = 0;
-  if (ensure_device(p.K, act == M3_BF16 ? 1 : 0, &smem_sm) != M3_OK) return M3_ERR_CUDA;
+  if (ensure_device(KT, act == M3_BF16 ? 1 : 0, &smem_sm) != M3_OK) return M3_ERR_CUDA;
   BwdArgs a{};
   a.x = x; a.dr = delta_raw; a.z = z; a.Bm = Bm; a.Cm = Cm; a.dg = d_gated;
   a.conv_w = conv_w; a.conv_b = conv_b; a.dt_bias = dt_bias; a.a_log = a_log; a.Dp = D;
@@ -625,6 +653,7 @@ m3_status bwd_impl(const m3_dims* dims, m3_dtype act, const void* x, const void*
   a.conv_in = sv.conv_state; a.g_h = sv.d_ssm_state_out; a.g_conv = sv.d_conv_state_out;
   a.d_h_in = sv.d_ssm_state; a.d_conv_in = sv.d_conv_state;
   a.status = reinterpret_cast<unsigned*>(ws);
+  a.sk = p.nsk > 0 ? reinterpret_cast<float*>(ws + p.b_sk) : nullptr;
   m3_status r = act == M3_BF16 ? launch_bwd<__nv_bfloat16>(p, a, s, smem_sm, scan)
                                 : launch_bwd<float>(p, a, s, smem_sm, scan);
   if (r != M3_OK) cudaGetLastError();
@@ -728,7 +757,7 @@ m3_status m3scan_conv_bwd(const m3_dims* dims, m3_dtype act, const void* x, cons
   if (!workspace || workspace_bytes < p.ws_bytes) return M3_ERR_WORKSPACE;
   if (!aligned(workspace, 256)) return M3_ERR_ALIGN;
   int smem_sm = 0;
-  if (ensure_device(p.K, act == M3_BF16 ? 1 : 0, &smem_sm) != M3_OK) return M3_ERR_CUDA;
+  if (ensure_device(KT, act == M3_BF16 ? 1 : 0, &smem_sm) != M3_OK) return M3_ERR_CUDA;
   ConvArgs a{};
   a.B = p.B; a.T = p.T; a.D = p.D; a.tile = p.ctile; a.ntiles = p.cntiles;
   a.x = x; a.du = du; a.du_extra = du_extra; a.conv_w = conv_w; a.conv_b = conv_b; a.dx = d_x;
@@ -857,7 +886,7 @@ m3_status m3scan_decode(const m3_dims* dims, m3_dtype act, const void* x, const 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int n = (int)dims->d_state;
   int sms = 0, of = 0, ob = 0;
-  if (note(device_info(KDEF, act == M3_BF16 ? 1 : 0, &sms, &of, &ob)) != cudaSuccess)
+  if (note(device_info(KT, act == M3_BF16 ? 1 : 0, &sms, &of, &ob)) != cudaSuccess)
     return M3_ERR_CUDA;
   const cudaError_t e = act == M3_BF16 ? launch_decode_n<__nv_bfloat16>(n, a, s, sms)
                                        : launch_decode_n<float>(n, a, s, sms);

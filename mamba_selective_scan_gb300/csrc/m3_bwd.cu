@@ -199,34 +199,49 @@ __global__ void __launch_bounds__(GB) m3_bwd_agg_kernel(const __grid_constant__ 
 // in the same register), as the reduce-scatter below relies on.
 // ---------------------------------------------------------------------------
 
-// Sum over the 32 lanes of v[0..15] (v[s] holds state lane
-// 4 * ((s >> 2) ^ (lane & 3)) + (s & 3)); returns the total for state lane
-// 4 * (lane & 3) + 2 * ((lane >> 3) & 1) + ((lane >> 2) & 1).
-__device__ __forceinline__ float warp_sum16_rotated(float (&v)[NS], int lane) {
+// Sum over the 32 lanes of 16 values held as 8 pairs (element e of pair P:
+// state lane 4 * ((P >> 1) ^ (lane & 3)) + 2 * (P & 1) + e); returns the
+// total for state lane 4 * (lane & 3) + 2 * ((lane >> 3) & 1) + ((lane >> 2) & 1).
+__device__ __forceinline__ float warp_sum16_rotated(float2 (&v)[NS / 2], int lane) {
+  constexpr unsigned FULL = 0xffffffffu;
 #pragma unroll
-  for (int s = 0; s < 8; ++s) v[s] += __shfl_xor_sync(0xffffffffu, v[s + 8], 2);
+  for (int P = 0; P < 4; ++P)
+    v[P] = __fadd2_rn(v[P], make_float2(__shfl_xor_sync(FULL, v[P + 4].x, 2), __shfl_xor_sync(FULL, v[P + 4].y, 2)));
 #pragma unroll
-  for (int s = 0; s < 4; ++s) v[s] += __shfl_xor_sync(0xffffffffu, v[s + 4], 1);
+  for (int P = 0; P < 2; ++P)
+    v[P] = __fadd2_rn(v[P], make_float2(__shfl_xor_sync(FULL, v[P + 2].x, 1), __shfl_xor_sync(FULL, v[P + 2].y, 1)));
   {
     const bool up = (lane & 8) != 0;
-    const float s0 = up ? v[0] : v[2], s1 = up ? v[1] : v[3];
-    const float k0 = up ? v[2] : v[0], k1 = up ? v[3] : v[1];
-    v[0] = k0 + __shfl_xor_sync(0xffffffffu, s0, 8);
-    v[1] = k1 + __shfl_xor_sync(0xffffffffu, s1, 8);
+    const float2 send = up ? v[0] : v[1];
+    const float2 keep = up ? v[1] : v[0];
+    v[0] = __fadd2_rn(keep, make_float2(__shfl_xor_sync(FULL, send.x, 8), __shfl_xor_sync(FULL, send.y, 8)));
   }
-  {
-    const bool up = (lane & 4) != 0;
-    const float s0 = up ? v[0] : v[1];
-    const float k0 = up ? v[1] : v[0];
-    v[0] = k0 + __shfl_xor_sync(0xffffffffu, s0, 4);
-  }
-  return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 16);
+  const bool up = (lane & 4) != 0;
+  const float r = (up ? v[0].y : v[0].x) + __shfl_xor_sync(FULL, up ? v[0].x : v[0].y, 4);
+  return r + __shfl_xor_sync(FULL, r, 16);
 }
 
 // ST: compiled with the carried-state terms; the plain entry points run the
 // instance without them.  SCAN: stop at du (written out) -- the SiLU and
 // conv backward then run in m3_conv_bwd_kernel with du plus any gradient
 // reaching u from outside the layer core.
+//
+// Work: a block owns 128 channels of one batch row over one time segment
+// (whole chunks of K steps, K the checkpoint interval) and walks its chunks
+// last to first.  A chunk is split into tiles of KS = min(K, 8) steps, the
+// most whose recomputed states fit the block's tensor memory.  The items of
+// chunk c (nt tiles) are, in order:
+//   items 0 .. nt-2: tiles 0 .. nt-2 forward from the chunk's checkpoint,
+//     leaving the state before tiles 1 .. nt-2 in the workspace (the
+//     sub-checkpoints, written with an L2 keep-resident hint: they are read
+//     back within the same chunk) and the state before tile nt-1 in the
+//     shared memory of the next item;
+//   items nt-1 .. 2nt-2: the backward of tiles nt-1 .. 0, each from its
+//     start state (the chunk's checkpoint for tile 0).
+// Every item's tiles arrive by tensor-map copies into one of two staging
+// buffers while the item before runs.  A backward item writes dz, d_delta_raw
+// and d_x (du in SCAN mode) into the buffer regions its inputs z, delta_raw
+// and d_gated no longer need, and stores them with tile copies.
 template <typename T, bool ST, bool SCAN>
 __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(const __grid_constant__ BwdArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
@@ -244,15 +259,17 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(const __grid_constant__ B
   const int c_end = min(c_begin + g.m, g.nc);
   const int t_begin = c_begin * g.K;
   const int t_end = min(c_end * g.K, g.T);
-  const int K = g.K;
-  const BwdSmem L = bwd_smem(K, sizeof(T));
+  const int K = g.K, KS = g.KS;
+  const BwdSmem L = bwd_smem(KT, sizeof(T));  // laid out for KT-step tiles; a tile may be shorter
   float* fB = reinterpret_cast<float*>(smem + L.fB);
   float* fC = reinterpret_cast<float*>(smem + L.fC);
   float* red = reinterpret_cast<float*>(smem + L.red);
   // state lane of register slot 2*i (pair i): quad (i >> 1) ^ rot, offset 2*(i & 1)
   auto lane_of = [&](int i) { return 4 * ((i >> 1) ^ rot) + 2 * (i & 1); };
+  // this block's sub-checkpoint slot in the workspace
+  auto slot = [&]() { return (int)(blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z)); };
 
-  // The recomputed states of a chunk (K rows of 16 f32 per channel) live in
+  // The recomputed states of a tile (KS rows of 16 f32 per channel) live in
   // tensor memory: row j of this thread = columns [16 j, 16 j + 16) of its
   // lane.  Warp 0 allocates for the CTA; every exit path below deallocates.
   __shared__ uint32_t tmem_slot;
@@ -298,29 +315,43 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(const __grid_constant__ B
       carry[i] = make_float2(gh[(size_t)n * g.D], gh[(size_t)(n + 1) * g.D]);
     }
   }
-  // A chunk's tiles arrive by tensor-map copies issued by thread 0: x with
-  // its three halo rows before the chunk, delta_raw, z, d_gated, B, C and
-  // the chunk's start state (16 rows of GB floats); rows outside [0, T) and
-  // channels past d_inner arrive as zeros.
-  const uint32_t tile_bytes = (uint32_t)((4 * K + 3) * GB * sizeof(T) + 2 * K * NS * sizeof(T) + NS * GB * 4);
+  // The tiles of an item arrive by tensor-map copies issued by thread 0: x
+  // with its three halo rows before the tile, delta_raw and B; for a
+  // backward item also z, d_gated and C; and the start state (16 rows of GB
+  // floats) when it comes from the chunk's checkpoint or a sub-checkpoint.
+  // Rows outside [0, T) and channels past d_inner arrive as zeros.
+  auto tiles_of = [&](int c) { return (min(K, g.T - c * K) + KS - 1) / KS; };
   const bool misaligned = (smem_u32(smem) & 127u) != 0;  // tile copies need 128-byte aligned buffers
-  auto stage = [&](int c, int buf) {
+  auto stage = [&](int c, int q, int buf) {
     if (tid == 0 && !misaligned) {
+      const uint32_t fwd_bytes = (uint32_t)(((2 * KS + 3) * GB + KS * NS) * sizeof(T));
+      const uint32_t bwd_bytes = (uint32_t)(((4 * KS + 3) * GB + 2 * KS * NS) * sizeof(T));
+      const uint32_t ck_bytes = (uint32_t)(NS * GB * 4);
+      const int nt = tiles_of(c);
+      const bool fw = q < nt - 1;
+      const int j = fw ? q : 2 * nt - 2 - q;
+      const int t0 = c * K + j * KS;
+      const bool ck_chunk = j == 0;
+      const bool ck_sub = !fw && j >= 1 && j <= nt - 2;
       unsigned char* base = smem + (size_t)buf * L.tile;
-      const int t0 = c * K;
+      // the tile stores of the item that last used this buffer have read it
+      bulk_wait_read();
       fence_proxy_async();
-      mbar_expect_tx(&tbar[buf], tile_bytes);
+      mbar_expect_tx(&tbar[buf], (fw ? fwd_bytes : bwd_bytes) + (ck_chunk || ck_sub ? ck_bytes : 0u));
       tma_load_3d(base + L.x, &a.tm[TM_X], d0, t0 - 3, b, &tbar[buf]);
       tma_load_3d(base + L.dr, &a.tm[TM_DR], d0, t0, b, &tbar[buf]);
-      tma_load_3d(base + L.z, &a.tm[TM_Z], d0, t0, b, &tbar[buf]);
-      tma_load_3d(base + L.dg, &a.tm[TM_DG], d0, t0, b, &tbar[buf]);
       tma_load_3d(base + L.Bt, &a.tm[TM_B], 0, t0, b, &tbar[buf]);
-      tma_load_3d(base + L.Ct, &a.tm[TM_C], 0, t0, b, &tbar[buf]);
-      tma_load_4d(base + L.ck, &a.tm[TM_CK], d0, 0, c, b, &tbar[buf]);
+      if (!fw) {
+        tma_load_3d(base + L.z, &a.tm[TM_Z], d0, t0, b, &tbar[buf]);
+        tma_load_3d(base + L.dg, &a.tm[TM_DG], d0, t0, b, &tbar[buf]);
+        tma_load_3d(base + L.Ct, &a.tm[TM_C], 0, t0, b, &tbar[buf]);
+      }
+      if (ck_chunk) tma_load_4d(base + L.ck, &a.tm[TM_CK], d0, 0, c, b, &tbar[buf]);
+      if (ck_sub) tma_load_4d(base + L.ck, &a.tm[TM_SK], 0, 0, j - 1, slot(), &tbar[buf]);
     }
   };
 
-  stage(c_end - 1, 0);  // last chunk in flight while the carries load
+  if (c_begin < c_end) stage(c_end - 1, 0, 0);  // first item in flight while the carries load
   grid_dep_trigger();
   // the aggregate kernel's carries, and its clearing of dB and dC before
   // this kernel's reductions into them
@@ -339,54 +370,139 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(const __grid_constant__ B
   float dc1 = 0.f, dc2 = 0.f, dc3 = 0.f;  // conv-input gradient at t+1, t+2, t+3
 
   bool aborted = false;
-  for (int c = c_end - 1; c >= c_begin; --c) {
-    const int it = c_end - 1 - c;  // buffer it & 1, its (it >> 1)-th use
-    const int buf = it & 1;
-    if (c - 1 >= c_begin) stage(c - 1, buf ^ 1);
-    const bool landed = !misaligned && mbar_wait(&tbar[buf], (it >> 1) & 1);
-    if (__syncthreads_or(!landed)) {
-      // a tile did not arrive: report it, let the copy issued above drain, leave
-      if (tid == 0) {
-        report_timeout(&g_bwd_status, a.status);
-        if (!misaligned && c - 1 >= c_begin) mbar_wait(&tbar[buf ^ 1], ((it + 1) >> 1) & 1);
+  int it = 0;  // items so far: buffer it & 1, its (it >> 1)-th use
+  for (int c = c_end - 1; c >= c_begin && !aborted; --c) {
+    const int nt = tiles_of(c);
+    const int nq = 2 * nt - 1;
+    for (int q = 0; q < nq; ++q, ++it) {
+      const int buf = it & 1;
+      const bool more = q + 1 < nq || c - 1 >= c_begin;
+      const bool fw = q < nt - 1;
+      // The next item's tiles: a forward item issues them now; a backward
+      // item after its first scalar pass, by when the tile stores of the item
+      // before (which read the buffer being refilled) have long finished.
+      auto stage_next = [&]() {
+        if (q + 1 < nq) stage(c, q + 1, buf ^ 1);
+        else if (c - 1 >= c_begin) stage(c - 1, 0, buf ^ 1);
+      };
+      if (fw) stage_next();
+      const bool landed = !misaligned && mbar_wait(&tbar[buf], (it >> 1) & 1);
+      if (__syncthreads_or(!landed)) {
+        // a tile did not arrive: report it, let a copy issued above drain, leave
+        if (tid == 0) {
+          report_timeout(&g_bwd_status, a.status);
+          if (!misaligned && fw && more) mbar_wait(&tbar[buf ^ 1], ((it + 1) >> 1) & 1);
+        }
+        aborted = true;
+        break;
       }
-      aborted = true;
-      break;
-    }
-    const unsigned char* base = smem + (size_t)buf * L.tile;
-    if (ST && a.conv_in && c * K < 3 && active) {
-      // halo rows before step 0 (staged as zeros): the carried conv inputs.
-      // Only this thread reads its column of the x tile.
-      T* xw = reinterpret_cast<T*>(smem + (size_t)buf * L.tile + L.x);
-      const T* ci = static_cast<const T*>(a.conv_in) + (size_t)b * 3 * g.D + d;
-      for (int r = 0; r < 3 - c * K; ++r) xw[r * GB + tid] = ci[(size_t)(c * K + r) * g.D];
-    }
-    {
-      const T* Bt = reinterpret_cast<const T*>(base + L.Bt);
-      const T* Ct = reinterpret_cast<const T*>(base + L.Ct);
-      for (int i = tid; i < K * NS; i += GB) {
-        fB[i] = Act<T>::ld(Bt + i);
-        fC[i] = Act<T>::ld(Ct + i);
+      const int j = fw ? q : 2 * nt - 2 - q;  // tile within the chunk
+      const int t0 = c * K + j * KS;          // its first step
+      const int steps = min(KS, min(c * K + K, g.T) - t0);
+      unsigned char* base = smem + (size_t)buf * L.tile;
+      if (ST && a.conv_in && t0 < 3 && active) {
+        // halo rows before step 0 (staged as zeros): the carried conv inputs.
+        // Only this thread reads its column of the x tile.
+        T* xw = reinterpret_cast<T*>(base + L.x);
+        const T* ci = static_cast<const T*>(a.conv_in) + (size_t)b * 3 * g.D + d;
+        for (int r = 0; r < 3 - t0; ++r) xw[r * GB + tid] = ci[(size_t)(t0 + r) * g.D];
       }
-    }
-    __syncthreads();
-    const T* xt = reinterpret_cast<const T*>(base + L.x);  // row r is step c*K - 3 + r
-    const T* drt = reinterpret_cast<const T*>(base + L.dr);
-    const T* zt = reinterpret_cast<const T*>(base + L.z);
-    const T* dgt = reinterpret_cast<const T*>(base + L.dg);
-    const float* ckt = reinterpret_cast<const float*>(base + L.ck);
-    const int steps = min(K, g.T - c * K);
+      {
+        const T* Bt = reinterpret_cast<const T*>(base + L.Bt);
+        const T* Ct = reinterpret_cast<const T*>(base + L.Ct);
+        for (int i = tid; i < KS * NS; i += GB) {
+          fB[i] = Act<T>::ld(Bt + i);
+          if (!fw) fC[i] = Act<T>::ld(Ct + i);
+        }
+      }
+      __syncthreads();
+      const T* xt = reinterpret_cast<const T*>(base + L.x);  // row r is step t0 - 3 + r
+      const T* drt = reinterpret_cast<const T*>(base + L.dr);
+      float* ckt = reinterpret_cast<float*>(base + L.ck);
+      float4* s0 = reinterpret_cast<float4*>(smem + L.scal) + tid;  // thread-private, stride GB
+      float4* s1 = s0 + (size_t)KT * GB;
 
-    float4* s0 = reinterpret_cast<float4*>(smem + L.scal) + tid;  // thread-private, stride GB
-    float4* s1 = s0 + (size_t)K * GB;
-    T* const dz_c = static_cast<T*>(a.dz) + ((size_t)b * g.T + (size_t)c * K) * g.D + d;
-    T* const ddr_c = static_cast<T*>(a.ddr) + ((size_t)b * g.T + (size_t)c * K) * g.D + d;
-    T* const dx_c = static_cast<T*>(a.dx) + ((size_t)b * g.T + (size_t)c * K) * g.D + d;
-    T* const du_c = a.du_dbg ? static_cast<T*>(a.du_dbg) + ((size_t)b * g.T + (size_t)c * K) * g.D + d
-                             : nullptr;
+      if (fw) {
+        // ---- forward item: the states through tile j, from the chunk's
+        // checkpoint (tile 0) or the sub-checkpoint this thread wrote in the
+        // item before ----
+        float2 hs[NS / 2];
+        {
+          const float* h0 = j == 0 ? ckt + tid : a.sk + ((size_t)slot() * g.nsk + (j - 1)) * NS * GB + tid;
+#pragma unroll
+          for (int i = 0; i < NS / 2; ++i) {
+            const int n = lane_of(i);
+            hs[i] = make_float2(h0[n * GB], h0[(n + 1) * GB]);
+          }
+        }
+        {
+          float xm3 = Act<T>::ld(xt + 0 * GB + tid);
+          float xm2 = Act<T>::ld(xt + 1 * GB + tid);
+          float xm1 = Act<T>::ld(xt + 2 * GB + tid);
+#pragma unroll 2
+          for (int jj = 0; jj < steps; ++jj) {
+            const float xv = Act<T>::ld(xt + (jj + 3) * GB + tid);
+            const float cpre = fmaf(w[0], xm3, fmaf(w[1], xm2, fmaf(w[2], xm1, fmaf(w[3], xv, cb))));
+            xm3 = xm2;
+            xm2 = xm1;
+            xm1 = xv;
+            const float u = cpre * sigmoid_f(cpre);
+            const float delta = softplus_f(Act<T>::ld(drt + jj * GB + tid) + dtb);
+            *reinterpret_cast<float2*>(s0 + jj * GB) = make_float2(delta, delta * u);
+          }
+        }
+#pragma unroll 2
+        for (int jj = 0; jj < steps; ++jj) {
+          const float2 v0 = *reinterpret_cast<const float2*>(s0 + jj * GB);
+          const float2 dl2 = f2b(v0.x);
+          const float2 du2 = f2b(v0.y);
+          const float4* B4 = reinterpret_cast<const float4*>(fB + jj * NS);
+#pragma unroll
+          for (int qs = 0; qs < 4; ++qs) {
+            const float4 bv = B4[qs ^ rot];
+            hs[2 * qs] = __ffma2_rn(ex2x2(__fmul2_rn(dl2, a2[2 * qs])), hs[2 * qs],
+                                    __fmul2_rn(du2, make_float2(bv.x, bv.y)));
+            hs[2 * qs + 1] = __ffma2_rn(ex2x2(__fmul2_rn(dl2, a2[2 * qs + 1])), hs[2 * qs + 1],
+                                        __fmul2_rn(du2, make_float2(bv.z, bv.w)));
+          }
+        }
+        if (j + 1 < nt - 1) {
+          // the state before tile j + 1: a sub-checkpoint, read back by the
+          // backward item of that tile with a tile copy
+          float* skp = a.sk + ((size_t)slot() * g.nsk + j) * NS * GB + tid;
+          const uint64_t keep_policy = l2_evict_last_policy();
+#pragma unroll
+          for (int i = 0; i < NS / 2; ++i) {
+            const int n = lane_of(i);
+            st_keep(skp + n * GB, hs[i].x, keep_policy);
+            st_keep(skp + (n + 1) * GB, hs[i].y, keep_policy);
+          }
+          fence_proxy_async_global();
+        } else {
+          // the state before the last tile: the start state of the next item
+          float* ckn = reinterpret_cast<float*>(smem + (size_t)(buf ^ 1) * L.tile + L.ck);
+#pragma unroll
+          for (int i = 0; i < NS / 2; ++i) {
+            const int n = lane_of(i);
+            ckn[n * GB + tid] = hs[i].x;
+            ckn[(n + 1) * GB + tid] = hs[i].y;
+          }
+        }
+        __syncthreads();
+        continue;
+      }
 
-    // The four passes over the chunk.
-    {
+      // ---- backward item: tile j ----
+      const T* zt = reinterpret_cast<const T*>(base + L.z);
+      const T* dgt = reinterpret_cast<const T*>(base + L.dg);
+      // outputs, staged where the inputs no longer needed were: dz over z,
+      // d_delta_raw over delta_raw, d_x (or du when stopping at du) over d_gated
+      T* oz = reinterpret_cast<T*>(base + L.z);
+      T* odr = reinterpret_cast<T*>(base + L.dr);
+      T* odx = reinterpret_cast<T*>(base + L.dg);
+      T* const du_c = (!SCAN && a.du_dbg)
+                          ? static_cast<T*>(a.du_dbg) + ((size_t)b * g.T + (size_t)t0) * g.D + d
+                          : nullptr;
       const int nst = steps;
 
       // ---- scalar pass: everything per step that does not need the state ----
@@ -395,28 +511,29 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(const __grid_constant__ B
         float xm2 = Act<T>::ld(xt + 1 * GB + tid);
         float xm1 = Act<T>::ld(xt + 2 * GB + tid);
 #pragma unroll 2
-        for (int j = 0; j < nst; ++j) {
-          const float xv = Act<T>::ld(xt + (j + 3) * GB + tid);
+        for (int jj = 0; jj < nst; ++jj) {
+          const float xv = Act<T>::ld(xt + (jj + 3) * GB + tid);
           const float cpre = fmaf(w[0], xm3, fmaf(w[1], xm2, fmaf(w[2], xm1, fmaf(w[3], xv, cb))));
           xm3 = xm2;
           xm2 = xm1;
           xm1 = xv;
           const float sc = sigmoid_f(cpre);
           const float u = cpre * sc;
-          const float v = Act<T>::ld(drt + j * GB + tid) + dtb;
-          const float delta = softplus_f(v);
-          const float sv = sigmoid_f(v);
-          const float zv = Act<T>::ld(zt + j * GB + tid);
-          const float gv = Act<T>::ld(dgt + j * GB + tid);
+          const float2 sps = softplus_sigmoid(Act<T>::ld(drt + jj * GB + tid) + dtb);
+          const float delta = sps.x;
+          const float zv = Act<T>::ld(zt + jj * GB + tid);
+          const float gv = Act<T>::ld(dgt + jj * GB + tid);
           const float sz = sigmoid_f(zv);
           const float dy = gv * zv * sz;                           // dL/dy
           const float dzf = gv * (sz * fmaf(zv, 1.f - sz, 1.f));    // dL/dz = y * dzf
-          s0[j * GB] = make_float4(delta, delta * u, dy, dzf);
-          s1[j * GB] = make_float4(Dd * u, sv, sc, cpre);
+          s0[jj * GB] = make_float4(delta, delta * u, dy, dzf);
+          s1[jj * GB] = make_float4(Dd * u, sps.y, sc, cpre);
         }
       }
 
-      // ---- recompute the chunk's states from its start state ----
+      stage_next();
+
+      // ---- recompute the tile's states from its start state ----
       {
         float2 h[NS / 2];
 #pragma unroll
@@ -425,11 +542,11 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(const __grid_constant__ B
           h[i] = make_float2(ckt[n * GB + tid], ckt[(n + 1) * GB + tid]);
         }
 #pragma unroll 2
-        for (int j = 0; j < nst; ++j) {
-          const float4 v0 = s0[j * GB];
+        for (int jj = 0; jj < nst; ++jj) {
+          const float2 v0 = *reinterpret_cast<const float2*>(s0 + jj * GB);
           const float2 dl2 = f2b(v0.x);
           const float2 du2 = f2b(v0.y);
-          const float4* B4 = reinterpret_cast<const float4*>(fB + j * NS);
+          const float4* B4 = reinterpret_cast<const float4*>(fB + jj * NS);
 #pragma unroll
           for (int qs = 0; qs < 4; ++qs) {
             const float4 bv = B4[qs ^ rot];
@@ -438,7 +555,7 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(const __grid_constant__ B
             h[2 * qs] = __ffma2_rn(dA0, h[2 * qs], __fmul2_rn(du2, make_float2(bv.x, bv.y)));
             h[2 * qs + 1] = __ffma2_rn(dA1, h[2 * qs + 1], __fmul2_rn(du2, make_float2(bv.z, bv.w)));
           }
-          tmem_st16(trow + 16u * (uint32_t)j, h);
+          tmem_st16(trow + 16u * (uint32_t)jj, h);
         }
         tmem_wait_st();
       }
@@ -448,9 +565,9 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(const __grid_constant__ B
         float2 hn[NS / 2];  // h_t (state after step t)
         tmem_ld16(trow + 16u * (uint32_t)(nst - 1), hn);
 #pragma unroll 2
-        for (int j = nst - 1; j >= 0; --j) {
-          const float4 v0 = s0[j * GB];
-          const float Du = reinterpret_cast<const float*>(s1 + j * GB)[0];
+        for (int jj = nst - 1; jj >= 0; --jj) {
+          const float4 v0 = s0[jj * GB];
+          const float Du = reinterpret_cast<const float*>(s1 + jj * GB)[0];
           const float2 dl2 = f2b(v0.x);
           const float2 du2 = f2b(v0.y);
           const float2 dy2 = f2b(v0.z);
@@ -458,8 +575,8 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(const __grid_constant__ B
           float2 y01 = make_float2(0.f, 0.f), y23 = make_float2(0.f, 0.f);
           float2 pB[NS / 2], pC[NS / 2];
           float2 hp[NS / 2];  // h_{t-1}
-          if (j > 0) {
-            tmem_ld16(trow + 16u * (uint32_t)(j - 1), hp);
+          if (jj > 0) {
+            tmem_ld16(trow + 16u * (uint32_t)(jj - 1), hp);
           } else {
 #pragma unroll
             for (int i = 0; i < NS / 2; ++i) {
@@ -467,8 +584,8 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(const __grid_constant__ B
               hp[i] = make_float2(ckt[n * GB + tid], ckt[(n + 1) * GB + tid]);
             }
           }
-          const float4* B4 = reinterpret_cast<const float4*>(fB + j * NS);
-          const float4* C4 = reinterpret_cast<const float4*>(fC + j * NS);
+          const float4* B4 = reinterpret_cast<const float4*>(fB + jj * NS);
+          const float4* C4 = reinterpret_cast<const float4*>(fC + jj * NS);
 #pragma unroll
           for (int qs = 0; qs < 4; ++qs) {
             const float4 bv = B4[qs ^ rot];
@@ -492,24 +609,16 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(const __grid_constant__ B
 #pragma unroll
           for (int i = 0; i < NS / 2; ++i) hn[i] = hp[i];
           const float y = ((y01.x + y01.y) + (y23.x + y23.y)) + Du;
-          if (active) Act<T>::st(dz_c + (size_t)j * g.D, y * v0.w);
+          Act<T>::st(oz + jj * GB + tid, y * v0.w);
           // the scalar pass below reads these two sums
-          reinterpret_cast<float*>(s0 + j * GB)[3] = sAq.x + sAq.y;
-          reinterpret_cast<float*>(s1 + j * GB)[0] = sB.x + sB.y;
+          reinterpret_cast<float*>(s0 + jj * GB)[3] = sAq.x + sAq.y;
+          reinterpret_cast<float*>(s1 + jj * GB)[0] = sB.x + sB.y;
           // Channels past d_inner run on zero-filled inputs and parameters, so
           // their partials are exactly zero and need no masking.
-          float vb[NS], vc[NS];
-#pragma unroll
-          for (int i = 0; i < NS / 2; ++i) {
-            vb[2 * i] = pB[i].x;
-            vb[2 * i + 1] = pB[i].y;
-            vc[2 * i] = pC[i].x;
-            vc[2 * i + 1] = pC[i].y;
-          }
-          const float rb = warp_sum16_rotated(vb, lane);
-          const float rc = warp_sum16_rotated(vc, lane);
+          const float rb = warp_sum16_rotated(pB, lane);
+          const float rc = warp_sum16_rotated(pC, lane);
           const int nf = 4 * rot + 2 * ((lane >> 3) & 1) + ((lane >> 2) & 1);
-          red[(j * NWB + warp) * 32 + (lane < 16 ? nf : 16 + nf)] = lane < 16 ? rb : rc;
+          red[(jj * NWB + warp) * 32 + (lane < 16 ? nf : 16 + nf)] = lane < 16 ? rb : rc;
         }
       }
 
@@ -518,10 +627,10 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(const __grid_constant__ B
       float xw1 = Act<T>::ld(xt + nst * GB + tid), xw2 = Act<T>::ld(xt + (nst + 1) * GB + tid),
             xw3 = Act<T>::ld(xt + (nst + 2) * GB + tid);
 #pragma unroll 2
-      for (int j = nst - 1; j >= 0; --j) {
-        const int t = c * K + j;
-        const float4 v0 = s0[j * GB];
-        const float4 v1 = s1[j * GB];
+      for (int jj = nst - 1; jj >= 0; --jj) {
+        const int t = t0 + jj;
+        const float4 v0 = s0[jj * GB];
+        const float4 v1 = s1[jj * GB];
         const float delta = v0.x, dy = v0.z, sAq = v0.w;
         const float sumB = v1.x, sv = v1.y, sc = v1.z, cpre = v1.w;
         const float u = cpre * sc;
@@ -529,16 +638,14 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(const __grid_constant__ B
         const float ddr = fmaf(u, sumB, LN2 * sAq) * sv;
         dD_acc = fmaf(dy, u, dD_acc);
         ddtb_acc += ddr;
+        Act<T>::st(odr + jj * GB + tid, ddr);
         if constexpr (SCAN) {  // the SiLU and conv backward run later, with du
-          if (active) {
-            Act<T>::st(ddr_c + (size_t)j * g.D, ddr);
-            Act<T>::st(du_c + (size_t)j * g.D, du);
-          }
+          Act<T>::st(odx + jj * GB + tid, du);
           continue;
         }
         const float dc = du * (sc * fmaf(cpre, 1.f - sc, 1.f));
         dcb_acc += dc;
-        const float xw0 = Act<T>::ld(xt + j * GB + tid);
+        const float xw0 = Act<T>::ld(xt + jj * GB + tid);
         dcw[0] = fmaf(dc, xw0, dcw[0]);
         dcw[1] = fmaf(dc, xw1, dcw[1]);
         dcw[2] = fmaf(dc, xw2, dcw[2]);
@@ -552,40 +659,48 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(const __grid_constant__ B
         dc3 = dc2;
         dc2 = dc1;
         dc1 = dc;
+        // at the last three steps before a later segment d_x still lacks that
+        // segment's terms: the tail kernel writes those rows again, complete
+        Act<T>::st(odx + jj * GB + tid, dxv);
         if (active) {
-          Act<T>::st(ddr_c + (size_t)j * g.D, ddr);
-          if (du_c) Act<T>::st(du_c + (size_t)j * g.D, du);
+          if (du_c) Act<T>::st(du_c + (size_t)jj * g.D, du);
           if (s + 1 < g.S && t >= t_end - 3)
             a.dxpart[(((size_t)b * g.S + s) * 3 + (t - (t_end - 3))) * g.D + d] = dxv;
-          else
-            Act<T>::st(dx_c + (size_t)j * g.D, dxv);
           if (s > 0 && t < t_begin + 3)
             a.dchead[(((size_t)b * g.S + s) * 3 + (t - t_begin)) * g.D + d] = dc;
         }
       }
-    }
 
-    __syncthreads();
-    // one global reduction per (t, n) per block for dB and dC
-    if (a.dbc_part) {  // this block's share, summed in a fixed order by m3_dbc_sum_kernel
-      for (int i = tid; i < steps * 32; i += GB) {
-        const int j = i >> 5, l = i & 31;
-        float v = 0.f;
-#pragma unroll
-        for (int ww = 0; ww < NWB; ++ww) v += red[(j * NWB + ww) * 32 + l];
-        a.dbc_part[(((size_t)b * g.T + c * K + j) * a.nblk + blockIdx.x) * 32 + l] = v;
+      fence_proxy_async();  // this thread's output rows, before the tile stores read them
+      __syncthreads();
+      if (tid == 0) {
+        // rows past the sequence and channels past d_inner are not written
+        tma_store_3d(&a.tm[TM_ODZ], oz, d0, t0, b);
+        tma_store_3d(&a.tm[TM_ODR], odr, d0, t0, b);
+        tma_store_3d(&a.tm[SCAN ? TM_ODU : TM_ODX], odx, d0, t0, b);
+        bulk_commit();
       }
-    } else {
-      for (int i = tid; i < steps * 32; i += GB) {
-        const int j = i >> 5, l = i & 31;
-        float v = 0.f;
+      // one global reduction per (t, n) per block for dB and dC
+      if (a.dbc_part) {  // this block's share, summed in a fixed order by m3_dbc_sum_kernel
+        for (int i = tid; i < steps * 32; i += GB) {
+          const int jj = i >> 5, l = i & 31;
+          float v = 0.f;
 #pragma unroll
-        for (int ww = 0; ww < NWB; ++ww) v += red[(j * NWB + ww) * 32 + l];
-        float* dst = (l < NS ? a.dB : a.dC) + ((size_t)b * g.T + c * K + j) * g.lddbc + (l & (NS - 1));
-        atomicAdd(dst, v);
+          for (int ww = 0; ww < NWB; ++ww) v += red[(jj * NWB + ww) * 32 + l];
+          a.dbc_part[(((size_t)b * g.T + t0 + jj) * a.nblk + blockIdx.x) * 32 + l] = v;
+        }
+      } else {
+        for (int i = tid; i < steps * 32; i += GB) {
+          const int jj = i >> 5, l = i & 31;
+          float v = 0.f;
+#pragma unroll
+          for (int ww = 0; ww < NWB; ++ww) v += red[(jj * NWB + ww) * 32 + l];
+          float* dst = (l < NS ? a.dB : a.dC) + ((size_t)b * g.T + t0 + jj) * g.lddbc + (l & (NS - 1));
+          atomicAdd(dst, v);
+        }
       }
+      __syncthreads();
     }
-    __syncthreads();
   }
 
   if (!aborted) {
@@ -632,6 +747,7 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(const __grid_constant__ B
       for (int k = 0; k < WC; ++k) Pp[(size_t)(19 + k) * g.D + d] = dcw[k];
     }
   }
+  if (tid == 0) bulk_wait_all();  // the tile stores are done before the block's memory goes
   tmem_fence_before_sync();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem_slot, a.tcols);
@@ -739,15 +855,28 @@ void (*agg_for(bool split, int N))(BwdArgs) {
 // scan: stop at du (m3scan_bwd_scan); the conv side runs in launch_conv_bwd.
 // Tensor maps of the backward's tiles (boxes of ch channels).
 template <typename T>
-bool encode_bwd_maps(const Plan& p, int ch, BwdArgs& a) {
+bool encode_bwd_maps(const Plan& p, int ch, bool scan, BwdArgs& a) {
   const uint64_t es = sizeof(T), D = p.D, T_ = p.T, B = p.B, N = p.N, ld = p.ldbc, nc = p.nc;
-  const uint32_t K = (uint32_t)p.K, c = (uint32_t)ch, n = (uint32_t)p.N;
+  const uint32_t K = (uint32_t)p.KS, c = (uint32_t)ch, n = (uint32_t)p.N;  // tiles of KS steps
   const uint64_t adim[3] = {D, T_, B}, astr[2] = {D * es, T_ * D * es};
   const uint64_t bdim[3] = {N, T_, B}, bstr[2] = {ld * es, T_ * ld * es};
   const uint64_t cdim[4] = {D, N, nc, B}, cstr[3] = {D * 4, N * D * 4, nc * N * D * 4};
   const uint32_t box_x[3] = {c, K + 3, 1}, box_a[3] = {c, K, 1}, box_b[3] = {n, K, 1}, box_c[4] = {c, n, 1, 1};
   const uint32_t box_ta[3] = {c, TT, 1}, box_tb[3] = {n, TT, 1};
-  const bool ok = encode_tile_map(&a.tm[TM_X], (int)es, 3, a.x, adim, astr, box_x) &&
+  bool ok = true;
+  if (p.nsk > 0) {  // sub-checkpoints [blocks][nsk][N][ch]
+    const uint64_t blocks = (uint64_t)((p.D + ch - 1) / ch) * p.Sb * p.B, nsk = p.nsk;
+    const uint64_t sdim[4] = {(uint64_t)ch, N, nsk, blocks};
+    const uint64_t sstr[3] = {(uint64_t)ch * 4, N * ch * 4, nsk * N * ch * 4};
+    ok = encode_tile_map(&a.tm[TM_SK], 4, 4, a.sk, sdim, sstr, box_c);
+  }
+  if (p.bwd_tpc == 1) {  // the one-thread kernel stores its tiles of dz, d_delta_raw, d_x / du
+    ok = ok && encode_tile_map(&a.tm[TM_ODZ], (int)es, 3, a.dz, adim, astr, box_a) &&
+         encode_tile_map(&a.tm[TM_ODR], (int)es, 3, a.ddr, adim, astr, box_a) &&
+         (scan ? encode_tile_map(&a.tm[TM_ODU], (int)es, 3, a.du_dbg, adim, astr, box_a)
+               : encode_tile_map(&a.tm[TM_ODX], (int)es, 3, a.dx, adim, astr, box_a));
+  }
+  ok = ok && encode_tile_map(&a.tm[TM_X], (int)es, 3, a.x, adim, astr, box_x) &&
                   encode_tile_map(&a.tm[TM_DR], (int)es, 3, a.dr, adim, astr, box_a) &&
                   encode_tile_map(&a.tm[TM_Z], (int)es, 3, a.z, adim, astr, box_a) &&
                   encode_tile_map(&a.tm[TM_DG], (int)es, 3, a.dg, adim, astr, box_a) &&
@@ -765,9 +894,9 @@ bool encode_bwd_maps(const Plan& p, int ch, BwdArgs& a) {
 template <typename T>
 m3_status launch_bwd(const Plan& p, BwdArgs a, cudaStream_t st, int smem_per_sm, bool scan) {
   const int groups = (p.D + GB - 1) / GB;
-  a.g = Geo{p.B, p.T, p.D, p.K, p.nc, p.Sb, p.mb, p.ldbc, p.lddbc};
+  a.g = Geo{p.B, p.T, p.D, p.K, p.nc, p.Sb, p.mb, p.ldbc, p.lddbc, p.KS, p.nsk};
   cudaError_t e = cudaSuccess;
-  if (!encode_bwd_maps<T>(p, p.bwd_tpc != 1 ? 128 / (p.N / 8) : GB, a)) return M3_ERR_CUDA;
+  if (!encode_bwd_maps<T>(p, p.bwd_tpc != 1 ? 128 / (p.N / 8) : GB, scan, a)) return M3_ERR_CUDA;
   if (p.Sb > 1) {
     // also clears dB and dC before the main kernel's reductions into them
     const bool split = p.bwd_tpc != 1;
@@ -783,16 +912,16 @@ m3_status launch_bwd(const Plan& p, BwdArgs a, cudaStream_t st, int smem_per_sm,
   }
   const bool with_state = a.conv_in || a.g_h || a.g_conv || a.d_h_in || a.d_conv_in;
   if (p.bwd_tpc != 1) {
-    a.tcols = tmem_cols2_for(p.K);
-    const size_t smem = bwd2_launch_smem(p.K, sizeof(T), p.N, smem_per_sm);
+    a.tcols = tmem_cols2_for(KT);
+    const size_t smem = bwd2_launch_smem(KT, sizeof(T), p.N, smem_per_sm);
     void (*kern)(BwdArgs) = bwd2_kernel_for<T>(p.det, scan, with_state, p.N);
     const int ch = 128 / (p.N / 8);
     const dim3 grid((p.D + ch - 1) / ch, p.Sb, p.B);
     e = a.fin ? launch_k_cluster_y(kern, grid, 128, smem, st, true, (unsigned)p.Sb, a)
               : launch_k(kern, grid, 128, smem, st, p.Sb > 1, a);
   } else {
-    a.tcols = tmem_cols_for(p.K);
-    const size_t smem = bwd_launch_smem(p.K, sizeof(T), smem_per_sm);
+    a.tcols = tmem_cols_for(KT);
+    const size_t smem = bwd_launch_smem(KT, sizeof(T), smem_per_sm);
     void (*kern)(BwdArgs) = scan ? (with_state ? m3_bwd_kernel<T, true, true> : m3_bwd_kernel<T, false, true>)
                                  : (with_state ? m3_bwd_kernel<T, true, false> : m3_bwd_kernel<T, false, false>);
     e = launch_k(kern, dim3(groups, p.Sb, p.B), GB, smem, st, p.Sb > 1, a);

@@ -79,17 +79,19 @@ __global__ void __launch_bounds__(128, 4) m3_bwd2_kernel(const __grid_constant__
   const int c_end = min(c_begin + g.m, g.nc);
   const int t_begin = c_begin * g.K;
   const int t_end = min(c_end * g.K, g.T);
-  const int K = g.K;
-  const Bwd2Smem L = bwd2_smem(K, sizeof(T), N);
+  const int K = g.K, KS = g.KS;  // checkpoint interval; tile
+  const Bwd2Smem L = bwd2_smem(KT, sizeof(T), N);  // laid out for KT-step tiles; a tile may be shorter
   float* fB = reinterpret_cast<float*>(smem + L.fB);
   float* fC = reinterpret_cast<float*>(smem + L.fC);
   float* red = reinterpret_cast<float*>(smem + L.red);
-  float* dcs = reinterpret_cast<float*>(smem + L.dcs);  // [K + 3][CH]
+  float* dcs = reinterpret_cast<float*>(smem + L.dcs);  // [KT + 3][CH]
   // state lane of register pair P
   auto lane_of = [&](int P) { return 8 * hf + 2 * (P ^ prot); };
   // this thread's copy of B and C: its 8 lanes in register order
-  const float* fBr = fB + prot * rot_stride(K, N) + 8 * hf;
-  const float* fCr = fC + prot * rot_stride(K, N) + 8 * hf;
+  const float* fBr = fB + prot * rot_stride(KT, N) + 8 * hf;
+  const float* fCr = fC + prot * rot_stride(KT, N) + 8 * hf;
+  // this block's sub-checkpoint slot in the workspace
+  const int slot = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
 
   // recomputed states of a chunk: row j of this thread = TMEM columns
   // [8 j, 8 j + 8) of its lane; warp 0 allocates, every exit deallocates
@@ -133,29 +135,44 @@ __global__ void __launch_bounds__(128, 4) m3_bwd2_kernel(const __grid_constant__
       carry[P] = make_float2(gh[(size_t)n * g.D], gh[(size_t)(n + 1) * g.D]);
     }
   }
-  // A chunk's tiles arrive by tensor-map copies issued by thread 0: x with
-  // its three halo rows before the chunk, delta_raw, z, d_gated, B, C and
-  // the chunk's start state; rows outside [0, T) and channels past d_inner
-  // arrive as zeros.
-  const uint32_t tile_bytes =
-      (uint32_t)((4 * K + 3) * CH * sizeof(T) + 2 * K * N * sizeof(T) + (size_t)N * CH * 4);
+  // Work items as in m3_bwd_kernel: for chunk c of nt tiles of KS steps,
+  // items 0 .. nt-2 run tiles 0 .. nt-2 forward from the chunk's checkpoint
+  // (sub-checkpoints of tiles 1 .. nt-2 to the workspace, the state before
+  // tile nt-1 to the next item's staging buffer), items nt-1 .. 2nt-2 the
+  // backward of tiles nt-1 .. 0.  An item's tiles arrive by tensor-map copies
+  // issued by thread 0: x with its three halo rows, delta_raw, B; for a
+  // backward item also z, d_gated, C; and the start state when it comes
+  // from the chunk's checkpoint or a sub-checkpoint.  Rows outside [0, T)
+  // and channels past d_inner arrive as zeros.
+  auto tiles_of = [&](int c) { return (min(K, g.T - c * K) + KS - 1) / KS; };
+  const uint32_t fwd_bytes = (uint32_t)(((2 * KS + 3) * CH + KS * N) * sizeof(T));
+  const uint32_t bwd_bytes = (uint32_t)(((4 * KS + 3) * CH + 2 * KS * N) * sizeof(T));
+  const uint32_t ck_bytes = (uint32_t)(N * CH * 4);
   const bool misaligned = (smem_u32(smem) & 127u) != 0;  // tile copies need 128-byte aligned buffers
-  auto stage = [&](int c, int buf) {
+  auto stage = [&](int c, int q, int buf) {
     if (tid == 0 && !misaligned) {
+      const int nt = tiles_of(c);
+      const bool fw = q < nt - 1;
+      const int j = fw ? q : 2 * nt - 2 - q;
+      const int t0 = c * K + j * KS;
+      const bool ck_chunk = j == 0;
+      const bool ck_sub = !fw && j >= 1 && j <= nt - 2;
       unsigned char* base = smem + (size_t)buf * L.tile;
-      const int t0 = c * K;
       fence_proxy_async();
-      mbar_expect_tx(&tbar[buf], tile_bytes);
+      mbar_expect_tx(&tbar[buf], (fw ? fwd_bytes : bwd_bytes) + (ck_chunk || ck_sub ? ck_bytes : 0u));
       tma_load_3d(base + L.x, &a.tm[TM_X], d0, t0 - 3, b, &tbar[buf]);
       tma_load_3d(base + L.dr, &a.tm[TM_DR], d0, t0, b, &tbar[buf]);
-      tma_load_3d(base + L.z, &a.tm[TM_Z], d0, t0, b, &tbar[buf]);
-      tma_load_3d(base + L.dg, &a.tm[TM_DG], d0, t0, b, &tbar[buf]);
       tma_load_3d(base + L.Bt, &a.tm[TM_B], 0, t0, b, &tbar[buf]);
-      tma_load_3d(base + L.Ct, &a.tm[TM_C], 0, t0, b, &tbar[buf]);
-      tma_load_4d(base + L.ck, &a.tm[TM_CK], d0, 0, c, b, &tbar[buf]);
+      if (!fw) {
+        tma_load_3d(base + L.z, &a.tm[TM_Z], d0, t0, b, &tbar[buf]);
+        tma_load_3d(base + L.dg, &a.tm[TM_DG], d0, t0, b, &tbar[buf]);
+        tma_load_3d(base + L.Ct, &a.tm[TM_C], 0, t0, b, &tbar[buf]);
+      }
+      if (ck_chunk) tma_load_4d(base + L.ck, &a.tm[TM_CK], d0, 0, c, b, &tbar[buf]);
+      if (ck_sub) tma_load_4d(base + L.ck, &a.tm[TM_SK], 0, 0, j - 1, slot, &tbar[buf]);
     }
   };
-  stage(c_end - 1, 0);
+  if (c_begin < c_end) stage(c_end - 1, 0, 0);
   grid_dep_trigger();
   grid_dep_wait();
   if (s + 1 < g.S) {
@@ -167,54 +184,123 @@ __global__ void __launch_bounds__(128, 4) m3_bwd2_kernel(const __grid_constant__
   for (int P = 0; P < 4; ++P) dAp[P] = make_float2(0.f, 0.f);
   float dD_acc = 0.f, ddtb_acc = 0.f, dcb_acc = 0.f;
   float dcw[WC] = {0.f, 0.f, 0.f, 0.f};
-  for (int i = tid; i < (K + 3) * CH; i += 128) dcs[i] = 0.f;  // ordered by the loop's first barrier
+  for (int i = tid; i < (KT + 3) * CH; i += 128) dcs[i] = 0.f;  // ordered by the loop's first barrier
 
   bool aborted = false;
-  for (int c = c_end - 1; c >= c_begin; --c) {
-    const int it = c_end - 1 - c;  // buffer it & 1, its (it >> 1)-th use
+  int it = 0;  // items so far: buffer it & 1, its (it >> 1)-th use
+  for (int c = c_end - 1; c >= c_begin && !aborted; --c) {
+   const int nt = tiles_of(c);
+   const int nq = 2 * nt - 1;
+   for (int q = 0; q < nq; ++q, ++it) {
     const int buf = it & 1;
-    if (c - 1 >= c_begin) stage(c - 1, buf ^ 1);
+    const bool more = q + 1 < nq || c - 1 >= c_begin;
+    if (q + 1 < nq) stage(c, q + 1, buf ^ 1);
+    else if (c - 1 >= c_begin) stage(c - 1, 0, buf ^ 1);
     const bool landed = !misaligned && mbar_wait(&tbar[buf], (it >> 1) & 1);
     if (__syncthreads_or(!landed)) {
       // a tile did not arrive: report it, let the copy issued above drain, leave
       if (tid == 0) {
         report_timeout(&g_bwd2_status, a.status);
-        if (!misaligned && c - 1 >= c_begin) mbar_wait(&tbar[buf ^ 1], ((it + 1) >> 1) & 1);
+        if (!misaligned && more) mbar_wait(&tbar[buf ^ 1], ((it + 1) >> 1) & 1);
       }
       aborted = true;
       break;
     }
+    const bool fw = q < nt - 1;
+    const int jt = fw ? q : 2 * nt - 2 - q;  // tile within the chunk
+    const int t0 = c * K + jt * KS;          // its first step
+    const int steps = min(KS, min(c * K + K, g.T) - t0);
     const unsigned char* base = smem + (size_t)buf * L.tile;
-    if (ST && a.conv_in && c * K < 3 && active && hf == 0) {
+    if (ST && a.conv_in && t0 < 3 && active && hf == 0) {
       T* xw = reinterpret_cast<T*>(smem + (size_t)buf * L.tile + L.x);
       const T* ci = static_cast<const T*>(a.conv_in) + (size_t)b * 3 * g.D + d;
-      for (int r = 0; r < 3 - c * K; ++r) xw[r * CH + ch] = ci[(size_t)(c * K + r) * g.D];
+      for (int r = 0; r < 3 - t0; ++r) xw[r * CH + ch] = ci[(size_t)(t0 + r) * g.D];
     }
     {
       const T* Bt = reinterpret_cast<const T*>(base + L.Bt);
       const T* Ct = reinterpret_cast<const T*>(base + L.Ct);
       // copy r, row j: position 8 h + 2 P + e holds state lane 8 h + 2 (P ^ r) + e
-      for (int i = tid; i < K * N; i += 128) {
-        const float bv = Act<T>::ld(Bt + i), cv = Act<T>::ld(Ct + i);
+      for (int i = tid; i < KS * N; i += 128) {
+        const float bv = Act<T>::ld(Bt + i), cv = fw ? 0.f : Act<T>::ld(Ct + i);
         const int j = i / N, n = i % N;
 #pragma unroll
         for (int r = 0; r < NROT; ++r) {
-          const int o = r * rot_stride(K, N) + j * N + (n & ~7) + 2 * (((n >> 1) & 3) ^ r) + (n & 1);
+          const int o = r * rot_stride(KT, N) + j * N + (n & ~7) + 2 * (((n >> 1) & 3) ^ r) + (n & 1);
           fB[o] = bv;
-          fC[o] = cv;
+          if (!fw) fC[o] = cv;
         }
       }
     }
     __syncthreads();
-    const T* xt = reinterpret_cast<const T*>(base + L.x);  // row r is step c*K - 3 + r
+    const T* xt = reinterpret_cast<const T*>(base + L.x);  // row r is step t0 - 3 + r
     const T* drt = reinterpret_cast<const T*>(base + L.dr);
     const T* zt = reinterpret_cast<const T*>(base + L.z);
     const T* dgt = reinterpret_cast<const T*>(base + L.dg);
     const float* ckt = reinterpret_cast<const float*>(base + L.ck);
-    const int steps = min(K, g.T - c * K);
     float4* s0 = reinterpret_cast<float4*>(smem + L.scal) + ch;  // shared by the channel's threads, stride CH
-    float4* s1 = s0 + (size_t)K * CH;
-    const size_t row0 = ((size_t)b * g.T + (size_t)c * K) * g.D + d;
+    float4* s1 = s0 + (size_t)KT * CH;
+    const size_t row0 = ((size_t)b * g.T + (size_t)t0) * g.D + d;
+
+    if (fw) {
+      // ---- forward item: this thread's lanes of the states through tile
+      // jt, from the chunk's checkpoint (tile 0) or the sub-checkpoint this
+      // thread wrote in the item before ----
+      float2 hs[4];
+      {
+        const float* h0 = jt == 0 ? ckt + ch : a.sk + ((size_t)slot * g.nsk + (jt - 1)) * N * CH + ch;
+#pragma unroll
+        for (int P = 0; P < 4; ++P) {
+          const int n = lane_of(P);
+          hs[P] = make_float2(h0[n * CH], h0[(n + 1) * CH]);
+        }
+      }
+      for (int j = hf; j < steps; j += G) {
+        const float xm3 = Act<T>::ld(xt + j * CH + ch);
+        const float xm2 = Act<T>::ld(xt + (j + 1) * CH + ch);
+        const float xm1 = Act<T>::ld(xt + (j + 2) * CH + ch);
+        const float xv = Act<T>::ld(xt + (j + 3) * CH + ch);
+        const float cpre = fmaf(w[0], xm3, fmaf(w[1], xm2, fmaf(w[2], xm1, fmaf(w[3], xv, cb))));
+        const float u = cpre * sigmoid_f(cpre);
+        const float delta = softplus_f(Act<T>::ld(drt + j * CH + ch) + dtb);
+        *reinterpret_cast<float2*>(s0 + j * CH) = make_float2(delta, delta * u);
+      }
+      __syncwarp();
+#pragma unroll 2
+      for (int j = 0; j < steps; ++j) {
+        const float2 v0 = *reinterpret_cast<const float2*>(s0 + j * CH);
+        const float2 dl2 = f2b(v0.x);
+        const float2 du2 = f2b(v0.y);
+#pragma unroll
+        for (int P = 0; P < 4; ++P) {
+          const float2 bb = *reinterpret_cast<const float2*>(fBr + j * N + 2 * P);
+          hs[P] = __ffma2_rn(ex2x2(__fmul2_rn(dl2, a2[P])), hs[P], __fmul2_rn(du2, bb));
+        }
+      }
+      if (jt + 1 < nt - 1) {
+        // the state before tile jt + 1: a sub-checkpoint, read back by the
+        // backward item of that tile with a tile copy
+        float* skp = a.sk + ((size_t)slot * g.nsk + jt) * N * CH + ch;
+        const uint64_t keep_policy = l2_evict_last_policy();
+#pragma unroll
+        for (int P = 0; P < 4; ++P) {
+          const int n = lane_of(P);
+          st_keep(skp + n * CH, hs[P].x, keep_policy);
+          st_keep(skp + (n + 1) * CH, hs[P].y, keep_policy);
+        }
+        fence_proxy_async_global();
+      } else {
+        // the state before the last tile: the start state of the next item
+        float* ckn = reinterpret_cast<float*>(smem + (size_t)(buf ^ 1) * L.tile + L.ck);
+#pragma unroll
+        for (int P = 0; P < 4; ++P) {
+          const int n = lane_of(P);
+          ckn[n * CH + ch] = hs[P].x;
+          ckn[(n + 1) * CH + ch] = hs[P].y;
+        }
+      }
+      __syncthreads();
+      continue;
+    }
 
     // ---- scalar pass, every G-th step ----
     for (int j = hf; j < steps; j += G) {
@@ -329,7 +415,7 @@ __global__ void __launch_bounds__(128, 4) m3_bwd2_kernel(const __grid_constant__
 
     // ---- du, d delta, softplus and (unless SCAN) SiLU backward, every G-th step ----
     for (int j = hf; j < steps; j += G) {
-      const int t = c * K + j;
+      const int t = t0 + j;
       const float4 v0 = s0[j * CH];
       const float4 v1 = s1[j * CH];
       const float delta = v0.x, dy = v0.z, sAq = v0.w;
@@ -356,7 +442,7 @@ __global__ void __launch_bounds__(128, 4) m3_bwd2_kernel(const __grid_constant__
       __syncwarp();
       // ---- conv backward: d_x from the conv-input gradient of this and the next 3 steps ----
       for (int j = hf; j < steps; j += G) {
-        const int t = c * K + j;
+        const int t = t0 + j;
         float dxv = fmaf(dcs[j * CH + ch], w[3], fmaf(dcs[(j + 1) * CH + ch], w[2],
                          fmaf(dcs[(j + 2) * CH + ch], w[1], dcs[(j + 3) * CH + ch] * w[0])));
         if (ST && a.g_conv && t >= g.T - 3 && active)
@@ -375,9 +461,9 @@ __global__ void __launch_bounds__(128, 4) m3_bwd2_kernel(const __grid_constant__
       // read before any is overwritten
       if (hf == 0) {
         const float v0 = dcs[ch], v1 = dcs[CH + ch], v2 = dcs[2 * CH + ch];
-        dcs[K * CH + ch] = v0;
-        dcs[(K + 1) * CH + ch] = v1;
-        dcs[(K + 2) * CH + ch] = v2;
+        dcs[KS * CH + ch] = v0;
+        dcs[(KS + 1) * CH + ch] = v1;
+        dcs[(KS + 2) * CH + ch] = v2;
       }
     }
 
@@ -388,7 +474,7 @@ __global__ void __launch_bounds__(128, 4) m3_bwd2_kernel(const __grid_constant__
         float v = 0.f;
 #pragma unroll
         for (int ww = 0; ww < 4; ++ww) v += red[(j * 4 + ww) * 2 * N + l];
-        a.dbc_part[(((size_t)b * g.T + c * K + j) * a.nblk + blockIdx.x) * 2 * N + l] = v;
+        a.dbc_part[(((size_t)b * g.T + t0 + j) * a.nblk + blockIdx.x) * 2 * N + l] = v;
       }
     } else {
       for (int i = tid; i < steps * 2 * N; i += 128) {
@@ -396,11 +482,12 @@ __global__ void __launch_bounds__(128, 4) m3_bwd2_kernel(const __grid_constant__
         float v = 0.f;
 #pragma unroll
         for (int ww = 0; ww < 4; ++ww) v += red[(j * 4 + ww) * 2 * N + l];
-        float* dst = (l < N ? a.dB : a.dC) + ((size_t)b * g.T + c * K + j) * g.lddbc + (l & (N - 1));
+        float* dst = (l < N ? a.dB : a.dC) + ((size_t)b * g.T + t0 + j) * g.lddbc + (l & (N - 1));
         atomicAdd(dst, v);
       }
     }
     __syncthreads();
+   }
   }
 
   if (!aborted) {
@@ -415,8 +502,8 @@ __global__ void __launch_bounds__(128, 4) m3_bwd2_kernel(const __grid_constant__
         }
       }
       if (!SCAN && a.d_conv_in && hf == 0) {
-        // dc of steps 0, 1, 2 (zero past the sequence), kept in rows K.. K+2
-        const float f0 = dcs[K * CH + ch], f1 = dcs[(K + 1) * CH + ch], f2 = dcs[(K + 2) * CH + ch];
+        // dc of steps 0, 1, 2 (zero past the sequence), kept in rows KS .. KS+2
+        const float f0 = dcs[KS * CH + ch], f1 = dcs[(KS + 1) * CH + ch], f2 = dcs[(KS + 2) * CH + ch];
         float v[3];
         v[2] = fmaf(f0, w[2], fmaf(f1, w[1], f2 * w[0]));
         v[1] = fmaf(f0, w[1], f1 * w[0]);

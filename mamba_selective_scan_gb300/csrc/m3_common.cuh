@@ -21,8 +21,10 @@ constexpr int GB = 128;       // backward: channels (= threads) per block = 4 wa
 constexpr int NWB = GB / 32;  // backward warps per block
 constexpr int TT = 16;        // forward / aggregate staging tile (steps)
 constexpr int SUB = 8;        // forward scalar sub-tile (steps)
-constexpr int KMAX = 64;      // largest chunk (the backward may allow less)
-constexpr int KDEF = 8;       // default chunk
+constexpr int KT = 8;         // backward tile: steps whose states are recomputed on chip at once
+constexpr int KMAX = 256;     // largest checkpoint interval
+constexpr int KLONG = 64;     // default checkpoint interval of long sequences
+constexpr int KSHORT = 8;     // default checkpoint interval of short sequences
 constexpr int NPART = 24;     // per-channel parameter partials (23 used)
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
@@ -51,6 +53,17 @@ __device__ __forceinline__ float2 f2b(float v) { return make_float2(v, v); }
 
 // 1 / (1 + e^-v)
 __device__ __forceinline__ float sigmoid_f(float v) { return rcp_a(1.0f + ex2(-v * LOG2E)); }
+
+// softplus(v) (.x) and sigmoid(v) (.y) from one exponential e = e^-|v|:
+// softplus as in softplus_f below; sigmoid(v) = 1 / (1 + e) for v >= 0 and
+// e / (1 + e) for v < 0.
+__device__ __forceinline__ float2 softplus_sigmoid(float v) {
+  const float e = ex2(-fabsf(v) * LOG2E);
+  const float series = e * fmaf(e, fmaf(e, 0.33333334f, -0.5f), 1.0f);
+  const float lg = lg2_a(1.0f + e) * LN2;
+  const float r = rcp_a(1.0f + e);
+  return make_float2(fmaxf(v, 0.0f) + (e < 0.015625f ? series : lg), v >= 0.0f ? r : e * r);
+}
 
 // log(1 + e^v) = max(v, 0) + log1p(e^-|v|); log1p(e) for e in (0, 1] from
 // the series e - e^2/2 + e^3/3 below 2^-6 (truncation < e^3/4 relative),
@@ -205,6 +218,34 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
       ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
       : "memory");
 }
+// Tile store from shared memory (elements outside the tensor are not
+// written); the issuing thread commits a bulk group after its stores.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];"
+               ::"l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// the shared memory read by every committed bulk store may be overwritten
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// every committed bulk store has completed
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// orders this thread's generic-proxy writes to global memory before later
+// tile copies (async proxy) that read them
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+// A 64-bit L2 cache policy that keeps written lines resident in preference
+// to others (for short-lived workspace data read back soon), and stores
+// that carry it.
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ void st_keep(float* p, float v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(p), "f"(v), "l"(pol) : "memory");
+}
 __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, int c0, int c1, int c2, int c3,
                                             uint64_t* bar) {
   asm volatile(
@@ -319,6 +360,9 @@ __device__ __forceinline__ void chain_segments(float2 (&v)[NP], const float2 (&a
 struct Geo {
   int B, T, D, K, nc, S, m;  // S segments of m chunks (the last may be short)
   int ldbc, lddbc;           // row strides (elements) of Bm/Cm and of dB/dC
+  // backward: tiles of KS = min(K, KT) steps; nsk = sub-checkpoints per chunk
+  // kept in the workspace (the states before tiles 1 .. ceil(K / KS) - 2)
+  int KS, nsk;
 };
 
 __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -376,8 +420,11 @@ struct BwdArgs {
   int fin;
   // the workspace's status block
   unsigned* status;
-  // tile maps of the backward's staging (see TM_* below)
-  CUtensorMap tm[11];
+  // sub-checkpoints of the chunk a block is working on, [blocks][nsk][N][ch]
+  // f32 (block = linear block index; ch = channels per block)
+  float* sk;
+  // tile maps of the backward's staging and stores (see TM_* below)
+  CUtensorMap tm[16];
 };
 // The backward's last kernel needs only these (a small argument block keeps
 // its launch cheap).
@@ -390,10 +437,13 @@ struct TailArgs {
 };
 
 // tensor maps of BwdArgs::tm, boxes of the block's channels (128 / threads
-// per channel): main kernels -- activations [B, T, D] x (K + 3) rows (x)
-// or K rows, B and C [B, T, ld] N x K, checkpoints [B, nc, N, D] f32
-// channels x N; aggregate kernel -- delta_raw, z, d_gated TT rows, C N x TT
-enum { TM_X = 0, TM_DR, TM_Z, TM_DG, TM_B, TM_C, TM_CK, TM_ADR, TM_AZ, TM_ADG, TM_AC };
+// per channel): main kernels -- activations [B, T, D] x (KS + 3) rows (x)
+// or KS rows, B and C [B, T, ld] N x KS, checkpoints [B, nc, N, D] f32
+// channels x N, sub-checkpoints [blocks, nsk, N, ch] f32 ch x N;
+// aggregate kernel -- delta_raw, z, d_gated TT rows, C N x TT; stores of
+// the one-thread main kernel -- dz, d_delta_raw, d_x, du [B, T, D] x KS rows
+enum { TM_X = 0, TM_DR, TM_Z, TM_DG, TM_B, TM_C, TM_CK, TM_ADR, TM_AZ, TM_ADG, TM_AC, TM_SK,
+       TM_ODZ, TM_ODR, TM_ODX, TM_ODU };
 
 // Forward shared memory: two staging buffers {x, delta_raw, z: [TT][GF]
 // act; B, C: [TT][16] act}, B and C of the current tile as float [TT][16],
@@ -440,10 +490,11 @@ __host__ __device__ inline Fwd2Smem fwd2_smem(int es, int N) {
   return s;
 }
 
-// Backward shared memory: two staging buffers {x: [K+3][GB] (three halo rows
-// before the chunk), delta_raw, z, d_gated: [K][GB] act; B, C: [K][16] act;
-// the chunk's start state ck: [16][GB] f32}; B and C of the current chunk as
-// float (the recomputed states live in tensor memory, see m3_bwd_kernel);
+// Backward shared memory for tiles of K steps: two staging buffers {x:
+// [K+3][GB] (three halo rows before the tile), delta_raw, z, d_gated: [K][GB]
+// act; B, C: [K][16] act; the tile's start state ck: [16][GB] f32}; B and C
+// of the current tile as float (the recomputed states live in tensor memory,
+// see m3_bwd_kernel);
 // per-step scalars, two thread-private float4 slots per step: s0[K][GB] =
 // (delta, delta*u, dy, dz factor -> sum_n A dh exp(delta A) h_{t-1}) and
 // s1[K][GB] = (D*u -> sum_n dh B, sigmoid(delta_raw + dt_bias), sigmoid(c),
@@ -615,17 +666,6 @@ __host__ inline uint32_t tmem_cols2_for(int K) {
   return c;
 }
 
-// Largest chunk whose backward fits: 16 K tensor-memory columns <= 512 and
-// the shared-memory footprints of the one-thread kernel and of the split
-// kernel at its widest state (d_state 64) within one block's limit.
-__host__ inline int kmax_for(int es) {
-  int k = KMAX;
-  while (k > 1 && (bwd_smem(k, es).total > SMEM_CAP || bwd2_smem(k, es, 64).total > SMEM_CAP ||
-                   tmem_cols_for(k) > 512))
-    --k;
-  return k;
-}
-
 // Shared memory to request per backward CTA: its footprint, raised if needed
 // so that no more CTAs fit on one SM than tensor memory can serve at once
 // (512 columns / tcols), so no allocation ever has to wait.
@@ -648,6 +688,7 @@ __host__ inline size_t bwd2_launch_smem(int K, int es, int N, int smem_per_sm) {
 
 struct Plan {
   int B, T, D, K, nc;
+  int KS, nsk;  // backward tile (min(K, KT)) and sub-checkpoints per chunk
   int N;  // d_state
   int ldbc, lddbc;
   int Sf, mf, Sb, mb;
@@ -662,6 +703,7 @@ struct Plan {
   bool det;              // dB/dC and parameter grads by fixed-order sums of per-block partials
   int dblk;              // channel blocks of the backward's main kernel
   size_t b_dbc;          // workspace offset of those partials [B * T][dblk][2N]
+  size_t b_sk;           // workspace offset of the sub-checkpoints [blocks][nsk][N][ch]
   // the split backward over 2..FIN_MAX segments, not deterministic: the
   // segments of a channel block form a cluster that finishes the parameter
   // gradients and d_x at the boundaries itself (no tail kernel)

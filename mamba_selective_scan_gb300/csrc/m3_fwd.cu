@@ -508,7 +508,7 @@ template <typename T>
 m3_status launch_fwd(const Plan& p, FwdArgs a, cudaStream_t st) {
   const int groups = (p.D + GF - 1) / GF;
   const size_t smem = fwd_smem(sizeof(T)).total;
-  a.g = Geo{p.B, p.T, p.D, p.K, p.nc, p.Sf, p.mf, p.ldbc, p.lddbc};
+  a.g = Geo{p.B, p.T, p.D, p.K, p.nc, p.Sf, p.mf, p.ldbc, p.lddbc, p.KS, 0};
   cudaError_t e = cudaSuccess;
   if (p.fwd_tpc != 1) {  // split kernels, N / 8 threads per channel
     const int ch = 128 / (p.N / 8);

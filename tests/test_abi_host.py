@@ -91,8 +91,8 @@ def test_segments_are_whole_chunks_of_at_least_four_steps(lib):
     (dict(d_inner=36), "M3_ERR_UNSUPPORTED"),
     (dict(batch=-1), "M3_ERR_DIMS"),
     (dict(seq_len=-5), "M3_ERR_DIMS"),
-    (dict(chunk=65), "M3_ERR_DIMS"),
-    (dict(chunk=64), "M3_ERR_UNSUPPORTED"),  # backward footprint too large
+    (dict(chunk=257), "M3_ERR_DIMS"),
+    (dict(chunk=60), "M3_ERR_UNSUPPORTED"),  # longer than a tile, not a whole number of tiles
     (dict(segments=-1), "M3_ERR_DIMS"),
     (dict(batch=70000), "M3_ERR_DIMS"),
 ])
@@ -109,13 +109,35 @@ def test_plan_rejects_unknown_dtype_and_null(lib):
     assert binding.STATUS[lib.m3scan_plan(None, 1, None)] == "M3_ERR_NULL"
 
 
-def test_chunk_limits_follow_the_backward_shared_memory(lib):
-    def st(chunk, act):
+def test_chunk_is_up_to_a_tile_or_whole_tiles_up_to_256(lib):
+    def st(chunk, act=binding.M3_BF16):
         return binding.STATUS[_plan(binding.make_dims(1, 64, 64, chunk=chunk, segments=1), act)[0]]
-    assert st(30, binding.M3_BF16) == "M3_OK"
-    assert st(31, binding.M3_BF16) == "M3_ERR_UNSUPPORTED"
-    assert st(23, binding.M3_F32) == "M3_OK"
-    assert st(24, binding.M3_F32) == "M3_ERR_UNSUPPORTED"
+    for k in (1, 5, 7, 8, 16, 24, 64, 128, 256):
+        assert st(k) == "M3_OK" and st(k, binding.M3_F32) == "M3_OK", k
+    for k in (9, 30, 63, 100, 250):
+        assert st(k) == "M3_ERR_UNSUPPORTED", k
+    assert st(264) == "M3_ERR_DIMS"
+
+
+def test_default_chunk(lib):
+    for T in (128, 1024, 65536):
+        _, pl = _plan(binding.make_dims(1, T, 64, segments=1))
+        assert pl.chunk == 8, T
+
+
+def test_long_chunks_add_sub_checkpoints_to_the_workspace(lib):
+    """Per block of the backward's main kernel: the states before tiles
+    1 .. K/8 - 2 of its chunk (16 floats x 128 channels each)."""
+    def ws(chunk, segments=3):
+        _, pl = _plan(binding.make_dims(2, 1024, 256, chunk=chunk, segments=segments,
+                                        threads_per_channel=1))
+        return pl.workspace_bytes, pl
+    small, _ = ws(16)      # two tiles: none kept
+    big, pl = ws(64)       # eight tiles: six kept
+    blocks = 2 * 3 * 2     # channel blocks x segments x batch
+    sub = blocks * 6 * 16 * 128 * 4
+    assert small < sub <= big
+    assert pl.chunk == 64 and pl.n_chunks == 16
 
 
 A = 1 << 20  # a 256-byte aligned fake address; never dereferenced

@@ -48,9 +48,14 @@ SMALL = [
     (1, 2, 8, "bf16", 0, 0),
     (3, 3, 16, "f32", 1, 0),
     (1, 7, 64, "f32", 2, 3),
-    (2, 97, 72, "bf16", 28, 2),
-    (2, 97, 72, "f32", 23, 3),
-    (2, 97, 72, "bf16", 30, 3),
+    # chunks longer than the backward's 8-step tile: tiles forward from the
+    # checkpoint, sub-checkpoints in the workspace, ragged last chunk
+    (2, 97, 72, "bf16", 24, 2),
+    (2, 97, 72, "f32", 32, 2),
+    (2, 97, 72, "bf16", 40, 1),
+    (1, 300, 72, "f32", 64, 2),
+    (1, 700, 40, "bf16", 128, 3),
+    (1, 600, 24, "f32", 256, 2),
     (1, 130, 200, "f32", 7, 5),
     (4, 33, 520, "bf16", 16, 2),
     (1, 200, 64, "bf16", 4, 12),  # more segments than a cluster of the split backward takes
@@ -235,9 +240,10 @@ def test_bounded_tile_wait_gives_up_and_reports():
 @pytest.mark.parametrize("tpc", [1, 2])
 @pytest.mark.parametrize("batch,T,D,act,chunk,segments", [
     (2, 200, 136, "f32", 16, 3),
-    (2, 97, 72, "bf16", 30, 3),
+    (2, 97, 72, "bf16", 32, 2),
     (4, 33, 520, "bf16", 16, 2),
     (1, 130, 200, "f32", 7, 1),
+    (2, 300, 72, "f32", 64, 2),
 ])
 def test_deterministic_matches_oracle_and_repeats_bit_for_bit(batch, T, D, act, chunk,
                                                                   segments, tpc):

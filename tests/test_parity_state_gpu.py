@@ -88,7 +88,8 @@ CASES = [
     # batch, T, D, act, chunk, segments
     (2, 200, 136, "f32", 16, 3),
     (2, 200, 136, "bf16", 8, 0),
-    (2, 97, 72, "bf16", 30, 3),
+    (2, 97, 72, "bf16", 32, 2),
+    (1, 300, 40, "f32", 64, 2),
     (1, 130, 200, "f32", 7, 5),
     (3, 40, 24, "f32", 1, 4),     # one-step chunks: halos of chunks 1, 2 reach the carried inputs
     (2, 41, 40, "bf16", 2, 3),    # two-step chunks
