@@ -266,6 +266,14 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(const __grid_constant__ B
   float* red = reinterpret_cast<float*>(smem + L.red);
   // state lane of register slot 2*i (pair i): quad (i >> 1) ^ rot, offset 2*(i & 1)
   auto lane_of = [&](int i) { return 4 * ((i >> 1) ^ rot) + 2 * (i & 1); };
+  // this thread's quads of a row of B or C, in register order
+  const float4* fBq[4];
+  const float4* fCq[4];
+#pragma unroll
+  for (int qs = 0; qs < 4; ++qs) {
+    fBq[qs] = reinterpret_cast<const float4*>(fB) + (qs ^ rot);
+    fCq[qs] = reinterpret_cast<const float4*>(fC) + (qs ^ rot);
+  }
   // this block's sub-checkpoint slot in the workspace
   auto slot = [&]() { return (int)(blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z)); };
 
@@ -439,8 +447,9 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(const __grid_constant__ B
           float xm3 = Act<T>::ld(xt + 0 * GB + tid);
           float xm2 = Act<T>::ld(xt + 1 * GB + tid);
           float xm1 = Act<T>::ld(xt + 2 * GB + tid);
-#pragma unroll 2
-          for (int jj = 0; jj < steps; ++jj) {
+#pragma unroll
+          for (int jj = 0; jj < KT; ++jj) {
+            if (jj >= steps) break;
             const float xv = Act<T>::ld(xt + (jj + 3) * GB + tid);
             const float cpre = fmaf(w[0], xm3, fmaf(w[1], xm2, fmaf(w[2], xm1, fmaf(w[3], xv, cb))));
             xm3 = xm2;
@@ -451,15 +460,15 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(const __grid_constant__ B
             *reinterpret_cast<float2*>(s0 + jj * GB) = make_float2(delta, delta * u);
           }
         }
-#pragma unroll 2
-        for (int jj = 0; jj < steps; ++jj) {
+#pragma unroll
+        for (int jj = 0; jj < KT; ++jj) {
+          if (jj >= steps) break;
           const float2 v0 = *reinterpret_cast<const float2*>(s0 + jj * GB);
           const float2 dl2 = f2b(v0.x);
           const float2 du2 = f2b(v0.y);
-          const float4* B4 = reinterpret_cast<const float4*>(fB + jj * NS);
 #pragma unroll
           for (int qs = 0; qs < 4; ++qs) {
-            const float4 bv = B4[qs ^ rot];
+            const float4 bv = fBq[qs][jj * (NS / 4)];
             hs[2 * qs] = __ffma2_rn(ex2x2(__fmul2_rn(dl2, a2[2 * qs])), hs[2 * qs],
                                     __fmul2_rn(du2, make_float2(bv.x, bv.y)));
             hs[2 * qs + 1] = __ffma2_rn(ex2x2(__fmul2_rn(dl2, a2[2 * qs + 1])), hs[2 * qs + 1],
@@ -511,7 +520,8 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(const __grid_constant__ B
         float xm2 = Act<T>::ld(xt + 1 * GB + tid);
         float xm1 = Act<T>::ld(xt + 2 * GB + tid);
 #pragma unroll 2
-        for (int jj = 0; jj < nst; ++jj) {
+        for (int jj = 0; jj < KT; ++jj) {
+          if (jj >= nst) break;
           const float xv = Act<T>::ld(xt + (jj + 3) * GB + tid);
           const float cpre = fmaf(w[0], xm3, fmaf(w[1], xm2, fmaf(w[2], xm1, fmaf(w[3], xv, cb))));
           xm3 = xm2;
@@ -541,15 +551,15 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(const __grid_constant__ B
           const int n = lane_of(i);
           h[i] = make_float2(ckt[n * GB + tid], ckt[(n + 1) * GB + tid]);
         }
-#pragma unroll 2
-        for (int jj = 0; jj < nst; ++jj) {
+#pragma unroll
+        for (int jj = 0; jj < KT; ++jj) {
+          if (jj >= nst) break;
           const float2 v0 = *reinterpret_cast<const float2*>(s0 + jj * GB);
           const float2 dl2 = f2b(v0.x);
           const float2 du2 = f2b(v0.y);
-          const float4* B4 = reinterpret_cast<const float4*>(fB + jj * NS);
 #pragma unroll
           for (int qs = 0; qs < 4; ++qs) {
-            const float4 bv = B4[qs ^ rot];
+            const float4 bv = fBq[qs][jj * (NS / 4)];
             const float2 dA0 = ex2x2(__fmul2_rn(dl2, a2[2 * qs]));
             const float2 dA1 = ex2x2(__fmul2_rn(dl2, a2[2 * qs + 1]));
             h[2 * qs] = __ffma2_rn(dA0, h[2 * qs], __fmul2_rn(du2, make_float2(bv.x, bv.y)));
@@ -562,10 +572,11 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(const __grid_constant__ B
 
       // ---- reverse-time pass: y and dz, adjoint state, dA, dB/dC ----
       {
-        float2 hn[NS / 2];  // h_t (state after step t)
-        tmem_ld16(trow + 16u * (uint32_t)(nst - 1), hn);
-#pragma unroll 2
-        for (int jj = nst - 1; jj >= 0; --jj) {
+        // this lane's row of the dB/dC sums: lanes 0-15 dB, 16-31 dC
+        float* const red_l = red + warp * 32 +
+                             (lane < 16 ? 0 : 16) + 4 * rot + 2 * ((lane >> 3) & 1) + ((lane >> 2) & 1);
+        // One step: hn = h_t (state after step t = jj), hp receives h_{t-1}.
+        auto rev_step = [&](const int jj, const float2 (&hn)[NS / 2], float2 (&hp)[NS / 2]) {
           const float4 v0 = s0[jj * GB];
           const float Du = reinterpret_cast<const float*>(s1 + jj * GB)[0];
           const float2 dl2 = f2b(v0.x);
@@ -574,7 +585,6 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(const __grid_constant__ B
           float2 sB = make_float2(0.f, 0.f), sAq = make_float2(0.f, 0.f);
           float2 y01 = make_float2(0.f, 0.f), y23 = make_float2(0.f, 0.f);
           float2 pB[NS / 2], pC[NS / 2];
-          float2 hp[NS / 2];  // h_{t-1}
           if (jj > 0) {
             tmem_ld16(trow + 16u * (uint32_t)(jj - 1), hp);
           } else {
@@ -584,12 +594,10 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(const __grid_constant__ B
               hp[i] = make_float2(ckt[n * GB + tid], ckt[(n + 1) * GB + tid]);
             }
           }
-          const float4* B4 = reinterpret_cast<const float4*>(fB + jj * NS);
-          const float4* C4 = reinterpret_cast<const float4*>(fC + jj * NS);
 #pragma unroll
           for (int qs = 0; qs < 4; ++qs) {
-            const float4 bv = B4[qs ^ rot];
-            const float4 cv = C4[qs ^ rot];
+            const float4 bv = fBq[qs][jj * (NS / 4)];
+            const float4 cv = fCq[qs][jj * (NS / 4)];
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
               const int i = 2 * qs + e;
@@ -606,8 +614,6 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(const __grid_constant__ B
               sAq = __ffma2_rn(a2[i], qv, sAq);
             }
           }
-#pragma unroll
-          for (int i = 0; i < NS / 2; ++i) hn[i] = hp[i];
           const float y = ((y01.x + y01.y) + (y23.x + y23.y)) + Du;
           Act<T>::st(oz + jj * GB + tid, y * v0.w);
           // the scalar pass below reads these two sums
@@ -617,8 +623,24 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(const __grid_constant__ B
           // their partials are exactly zero and need no masking.
           const float rb = warp_sum16_rotated(pB, lane);
           const float rc = warp_sum16_rotated(pC, lane);
-          const int nf = 4 * rot + 2 * ((lane >> 3) & 1) + ((lane >> 2) & 1);
-          red[(jj * NWB + warp) * 32 + (lane < 16 ? nf : 16 + nf)] = lane < 16 ? rb : rc;
+          red_l[jj * NWB * 32] = lane < 16 ? rb : rc;
+        };
+        float2 hA[NS / 2], hB[NS / 2];
+        tmem_ld16(trow + 16u * (uint32_t)(nst - 1), hA);
+        if (nst == KT) {
+          // a whole tile: steps in pairs, the two state registers trading roles
+#pragma unroll 1
+          for (int jj = KT - 1; jj > 0; jj -= 2) {
+            rev_step(jj, hA, hB);
+            rev_step(jj - 1, hB, hA);
+          }
+        } else {
+#pragma unroll 1
+          for (int jj = nst - 1; jj >= 0; --jj) {
+            rev_step(jj, hA, hB);
+#pragma unroll
+            for (int i = 0; i < NS / 2; ++i) hA[i] = hB[i];
+          }
         }
       }
 
@@ -626,8 +648,13 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(const __grid_constant__ B
       // conv inputs of steps t-2, t-1, t (tile rows j+1 .. j+3), slid down a row per step
       float xw1 = Act<T>::ld(xt + nst * GB + tid), xw2 = Act<T>::ld(xt + (nst + 1) * GB + tid),
             xw3 = Act<T>::ld(xt + (nst + 2) * GB + tid);
+      // whether any step of this tile writes the optional du, or a segment
+      // boundary term (one test per tile instead of per step)
+      const bool edge = du_c != nullptr || (s + 1 < g.S && t0 + nst > t_end - 3) ||
+                        (s > 0 && t0 < t_begin + 3);
 #pragma unroll 2
-      for (int jj = nst - 1; jj >= 0; --jj) {
+      for (int jj = KT - 1; jj >= 0; --jj) {
+        if (jj >= nst) continue;
         const int t = t0 + jj;
         const float4 v0 = s0[jj * GB];
         const float4 v1 = s1[jj * GB];
@@ -662,7 +689,7 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(const __grid_constant__ B
         // at the last three steps before a later segment d_x still lacks that
         // segment's terms: the tail kernel writes those rows again, complete
         Act<T>::st(odx + jj * GB + tid, dxv);
-        if (active) {
+        if (edge && active) {
           if (du_c) Act<T>::st(du_c + (size_t)jj * g.D, du);
           if (s + 1 < g.S && t >= t_end - 3)
             a.dxpart[(((size_t)b * g.S + s) * 3 + (t - (t_end - 3))) * g.D + d] = dxv;

@@ -137,6 +137,29 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float2 (&v)[NS / 2]) {
         "=f"(v[3].x), "=f"(v[3].y), "=f"(v[4].x), "=f"(v[4].y), "=f"(v[5].x), "=f"(v[5].y),
         "=f"(v[6].x), "=f"(v[6].y), "=f"(v[7].x), "=f"(v[7].y) : "r"(taddr) : "memory");
 }
+// The same load and store split from their waits, with no memory clobber:
+// ordinary loads and stores may be scheduled across them.  The wait names
+// the loaded registers as read-written, so no use of them can move above it.
+__device__ __forceinline__ void tmem_st16_async(uint32_t taddr, const float2 (&v)[NS / 2]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+      ::"r"(taddr), "f"(v[0].x), "f"(v[0].y), "f"(v[1].x), "f"(v[1].y), "f"(v[2].x), "f"(v[2].y),
+      "f"(v[3].x), "f"(v[3].y), "f"(v[4].x), "f"(v[4].y), "f"(v[5].x), "f"(v[5].y), "f"(v[6].x),
+      "f"(v[6].y), "f"(v[7].x), "f"(v[7].y));
+}
+__device__ __forceinline__ void tmem_ld16_async(uint32_t taddr, float2 (&v)[NS / 2]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=f"(v[0].x), "=f"(v[0].y), "=f"(v[1].x), "=f"(v[1].y), "=f"(v[2].x), "=f"(v[2].y),
+        "=f"(v[3].x), "=f"(v[3].y), "=f"(v[4].x), "=f"(v[4].y), "=f"(v[5].x), "=f"(v[5].y),
+        "=f"(v[6].x), "=f"(v[6].y), "=f"(v[7].x), "=f"(v[7].y) : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld16(float2 (&v)[NS / 2]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+f"(v[0].x), "+f"(v[0].y), "+f"(v[1].x), "+f"(v[1].y), "+f"(v[2].x), "+f"(v[2].y),
+                 "+f"(v[3].x), "+f"(v[3].y), "+f"(v[4].x), "+f"(v[4].y), "+f"(v[5].x), "+f"(v[5].y),
+                 "+f"(v[6].x), "+f"(v[6].y), "+f"(v[7].x), "+f"(v[7].y));
+}
 __device__ __forceinline__ void tmem_st8(uint32_t taddr, const float2 (&v)[4]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
