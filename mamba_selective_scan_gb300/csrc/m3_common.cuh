@@ -405,13 +405,14 @@ struct FwdArgs {
   void* conv_out;
   // the workspace's status block (nullable: no workspace)
   unsigned* status;
-  // tile maps of the forward's staging (see TF_* below)
-  CUtensorMap tm[5];
+  // tile maps of the forward's staging and stores (see TF_* below)
+  CUtensorMap tm[7];
 };
 // tensor maps of FwdArgs::tm: activations [B, T, D] with boxes of the
 // block's channels x TT rows (x: TT + 3 rows in the split kernels, which
-// stage the conv halo); B and C [B, T, ld] with boxes of N x TT
-enum { TF_X = 0, TF_DR, TF_Z, TF_B, TF_C };
+// stage the conv halo); B and C [B, T, ld] with boxes of N x TT; stores of
+// the one-thread final pass: gated and y [B, T, D] with boxes of GF x SUB
+enum { TF_X = 0, TF_DR, TF_Z, TF_B, TF_C, TF_OG, TF_OY };
 
 struct BwdArgs {
   Geo g;

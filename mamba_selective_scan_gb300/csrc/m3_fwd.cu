@@ -75,6 +75,7 @@ __global__ void __launch_bounds__(GF) m3_fwd_kernel(const __grid_constant__ FwdA
   auto stage = [&](int t0, int buf) {
     if (tid == 0 && !misaligned) {
       unsigned char* base = smem + (size_t)buf * L.tile;
+      if (FINAL) bulk_wait_read();  // the output stores of the tile that last used this buffer
       fence_proxy_async();
       mbar_expect_tx(&tbar[buf], tile_bytes);
       tma_load_3d(base + L.x, &a.tm[TF_X], d0, t0, b, &tbar[buf]);
@@ -136,12 +137,18 @@ __global__ void __launch_bounds__(GF) m3_fwd_kernel(const __grid_constant__ FwdA
 
 
   float4* scs = reinterpret_cast<float4*>(smem + L.sc) + tid;  // this thread's slots, stride GF
-  int kc = 0;  // steps left until the next checkpoint
+  // The final pass writes gated (and y) of a tile into the staging regions of
+  // z (and delta_raw), which its scalar pass has consumed, and stores each
+  // whole 8-step sub-tile with a tile copy; a sub-tile cut short by the end
+  // of the segment (chunks under 8 steps) is written by the threads.
   for (int t0 = t_begin, it = 0; t0 < t_end; t0 += TT, ++it) {
     const int buf = it & 1;
-    if (t0 + TT < t_end) stage(t0 + TT, buf ^ 1);
-    if (!fwd_tiles_landed(tbar, it, misaligned, t0 + TT < t_end, a.status)) return;
-    const unsigned char* base = smem + (size_t)buf * L.tile;
+    const bool more = t0 + TT < t_end;
+    // the local pass issues the next tile's copies now; the final pass after
+    // its first scalar sub-pass, when the stores that read that buffer are done
+    if (!FINAL && more) stage(t0 + TT, buf ^ 1);
+    if (!fwd_tiles_landed(tbar, it, misaligned, !FINAL && more, a.status)) return;
+    unsigned char* base = smem + (size_t)buf * L.tile;
     {
       const T* Bt = reinterpret_cast<const T*>(base + L.Bt);
       const T* Ct = reinterpret_cast<const T*>(base + L.Ct);
@@ -154,12 +161,15 @@ __global__ void __launch_bounds__(GF) m3_fwd_kernel(const __grid_constant__ FwdA
     const T* xt = reinterpret_cast<const T*>(base + L.x);
     const T* drt = reinterpret_cast<const T*>(base + L.dr);
     const T* zt = reinterpret_cast<const T*>(base + L.z);
+    T* og = reinterpret_cast<T*>(base + L.z);   // gated over z
+    T* oy = reinterpret_cast<T*>(base + L.dr);  // y over delta_raw
     const int steps = min(TT, t_end - t0);
     for (int j0 = 0; j0 < steps; j0 += SUB) {
       const int ns = min(SUB, steps - j0);
       // scalar pass: independent per step (conv, SiLU, softplus, gate factor)
-#pragma unroll 4
-      for (int j = 0; j < ns; ++j) {
+#pragma unroll
+      for (int j = 0; j < SUB; ++j) {
+        if (j >= ns) break;
         const float xv = Act<T>::ld(xt + (j0 + j) * GF + tid);
         const float cpre = fmaf(w[0], xm3, fmaf(w[1], xm2, fmaf(w[2], xm1, fmaf(w[3], xv, cb))));
         xm3 = xm2;
@@ -176,23 +186,26 @@ __global__ void __launch_bounds__(GF) m3_fwd_kernel(const __grid_constant__ FwdA
         }
         scs[j * GF] = make_float4(delta, delta * u, Dd * u, gz);
       }
-      // state pass: the only loop-carried dependence is h
-#pragma unroll 4
-      for (int j = 0; j < ns; ++j) {
-        if (FINAL) {
-          if (kc == 0) {
-            const int t = t0 + j0 + j;
-            if (active) {
-              float* ck = a.ckpt + (((size_t)b * g.nc + t / g.K) * NS) * g.D + d;
+      if (FINAL && j0 == 0 && more) stage(t0 + TT, buf ^ 1);
+      // state pass: the only loop-carried dependence is h.  A checkpoint is
+      // the state before every step t with t % K == 0: the first such step of
+      // this sub-tile is jc, then every K-th.
+      const int tsub = t0 + j0;
+      int jc = FINAL ? (g.K - tsub % g.K) % g.K : SUB;
+      const bool whole = tsub + SUB <= t_end;  // stored by a tile copy
 #pragma unroll
-              for (int i = 0; i < NS / 2; ++i) {
-                ck[(size_t)(2 * i) * g.D] = h[i].x;
-                ck[(size_t)(2 * i + 1) * g.D] = h[i].y;
-              }
+      for (int j = 0; j < SUB; ++j) {
+        if (j >= ns) break;
+        if (FINAL && j == jc) {
+          jc += g.K;
+          if (active) {
+            float* ck = a.ckpt + (((size_t)b * g.nc + (tsub + j) / g.K) * NS) * g.D + d;
+#pragma unroll
+            for (int i = 0; i < NS / 2; ++i) {
+              ck[(size_t)(2 * i) * g.D] = h[i].x;
+              ck[(size_t)(2 * i + 1) * g.D] = h[i].y;
             }
-            kc = g.K;
           }
-          --kc;
         }
         const float4 v = scs[j * GF];
         const float2 dl2 = f2b(v.x);
@@ -213,8 +226,11 @@ __global__ void __launch_bounds__(GF) m3_fwd_kernel(const __grid_constant__ FwdA
             y23 = __ffma2_rn(make_float2(cv.z, cv.w), h[2 * q + 1], y23);
           }
           const float y = ((y01.x + y01.y) + (y23.x + y23.y)) + v.z;
-          if (active) {
-            const size_t i = ((size_t)b * g.T + t0 + j0 + j) * g.D + d;
+          if (whole) {
+            Act<T>::st(og + (j0 + j) * GF + tid, y * v.w);
+            if (a.y_dbg) Act<T>::st(oy + (j0 + j) * GF + tid, y);
+          } else if (active) {
+            const size_t i = ((size_t)b * g.T + tsub + j) * g.D + d;
             Act<T>::st(static_cast<T*>(a.gated) + i, y * v.w);
             if (a.y_dbg) Act<T>::st(static_cast<T*>(a.y_dbg) + i, y);
           }
@@ -230,8 +246,23 @@ __global__ void __launch_bounds__(GF) m3_fwd_kernel(const __grid_constant__ FwdA
         }
       }
     }
-    __syncthreads();
+    if (FINAL) {
+      fence_proxy_async();  // this thread's output rows, before the tile stores read them
+      __syncthreads();
+      if (tid == 0) {
+        // rows past the sequence and channels past d_inner are not written
+        for (int j0 = 0; j0 < steps; j0 += SUB) {
+          if (t0 + j0 + SUB > t_end) break;
+          tma_store_3d(&a.tm[TF_OG], og + j0 * GF, d0, t0 + j0, b);
+          if (a.y_dbg) tma_store_3d(&a.tm[TF_OY], oy + j0 * GF, d0, t0 + j0, b);
+        }
+        bulk_commit();
+      }
+    } else {
+      __syncthreads();
+    }
   }
+  if (FINAL && tid == 0) bulk_wait_all();  // the tile stores are done before the block's memory goes
   if (FINAL && s == g.S - 1 && active) {
     if (a.h_out) {
       float* ho = a.h_out + (size_t)b * NS * g.D + d;
@@ -495,11 +526,16 @@ bool encode_fwd_maps(const Plan& p, int ch, int halo, FwdArgs& a) {
   const uint64_t adim[3] = {D, T_, B}, astr[2] = {D * es, T_ * D * es};
   const uint64_t bdim[3] = {N, T_, B}, bstr[2] = {ld * es, T_ * ld * es};
   const uint32_t box_x[3] = {c, (uint32_t)(TT + halo), 1}, box_a[3] = {c, TT, 1}, box_b[3] = {n, TT, 1};
-  const bool ok = encode_tile_map(&a.tm[TF_X], (int)es, 3, a.x, adim, astr, box_x) &&
-                  encode_tile_map(&a.tm[TF_DR], (int)es, 3, a.dr, adim, astr, box_a) &&
-                  encode_tile_map(&a.tm[TF_Z], (int)es, 3, a.z, adim, astr, box_a) &&
-                  encode_tile_map(&a.tm[TF_B], (int)es, 3, a.Bm, bdim, bstr, box_b) &&
-                  encode_tile_map(&a.tm[TF_C], (int)es, 3, a.Cm, bdim, bstr, box_b);
+  const uint32_t box_o[3] = {c, SUB, 1};
+  bool ok = encode_tile_map(&a.tm[TF_X], (int)es, 3, a.x, adim, astr, box_x) &&
+            encode_tile_map(&a.tm[TF_DR], (int)es, 3, a.dr, adim, astr, box_a) &&
+            encode_tile_map(&a.tm[TF_Z], (int)es, 3, a.z, adim, astr, box_a) &&
+            encode_tile_map(&a.tm[TF_B], (int)es, 3, a.Bm, bdim, bstr, box_b) &&
+            encode_tile_map(&a.tm[TF_C], (int)es, 3, a.Cm, bdim, bstr, box_b);
+  if (ok && halo == 0) {  // the one-thread final pass stores its output sub-tiles
+    ok = encode_tile_map(&a.tm[TF_OG], (int)es, 3, a.gated, adim, astr, box_o) &&
+         (!a.y_dbg || encode_tile_map(&a.tm[TF_OY], (int)es, 3, a.y_dbg, adim, astr, box_o));
+  }
   if (!ok) note(cudaErrorInvalidValue);
   return ok;
 }
