@@ -259,7 +259,8 @@ def job_gelem_s(world, elems_per_rank_step, steps, total_ms):
 class Layer:
     """Device buffers, plan and captured graphs for one layer-core instance."""
 
-    def __init__(self, torch, binding, tensors, chunk=0, segments=0, threads_per_channel=0):
+    def __init__(self, torch, binding, tensors, chunk=0, segments=0, threads_per_channel=0,
+                 deterministic=False):
         self.t = tensors
         x = tensors["x"]
         self.act = binding.M3_BF16 if x.dtype == torch.bfloat16 else binding.M3_F32
@@ -267,7 +268,9 @@ class Layer:
         self.shape = (Bsz, T, D)
         self.segments, self.tpc = segments, threads_per_channel
         self.dims = binding.make_dims(Bsz, T, D, chunk=chunk, segments=segments,
-                                      threads_per_channel=threads_per_channel)
+                                      threads_per_channel=threads_per_channel,
+                                      deterministic=deterministic)
+        self.deterministic = deterministic
         self.plan = binding.m3scan_plan(self.dims, self.act)
         dev = x.device
         f32 = dict(dtype=torch.float32, device=dev)
@@ -414,7 +417,7 @@ def gpu_arm(args):
     inp = make_workload_inputs(args.workload)
     tensors = host_inputs_to_device(torch, inp, device)
     layer = Layer(torch, binding, tensors, chunk=args.chunk, segments=args.segments,
-                  threads_per_channel=args.threads_per_channel)
+                  threads_per_channel=args.threads_per_channel, deterministic=args.deterministic)
     stream = torch.cuda.Stream(device)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
 
@@ -587,7 +590,7 @@ def e2e_measure(torch, binding, layer, tensors, steps, device):
             d_in["x"], d_in["delta_raw"], d_in["z"], d_in["B"], d_in["C"], d_in["conv_w"],
             d_in["conv_b"], d_in["dt_bias"], d_in["a_log"], d_in["D"], layer.o["ckpt"],
             d_in["d_gated"], chunk=int(layer.plan.chunk), segments=layer.segments,
-            threads_per_channel=layer.tpc,
+            threads_per_channel=layer.tpc, deterministic=layer.deterministic,
             out={k: d_out[k] for k in outs if k != "gated"}, workspace=_WS(ws), stream=s)
         h_out_buf.copy_(d_out_buf, non_blocking=True)
 
@@ -651,7 +654,7 @@ def e2e_measure(torch, binding, layer, tensors, steps, device):
                 di["x"], di["delta_raw"], di["z"], di["B"], di["C"], di["conv_w"],
                 di["conv_b"], di["dt_bias"], di["a_log"], di["D"], layer.o["ckpt"],
                 di["d_gated"], chunk=int(layer.plan.chunk), segments=layer.segments,
-                threads_per_channel=layer.tpc,
+                threads_per_channel=layer.tpc, deterministic=layer.deterministic,
                 out={k2: do[k2] for k2 in outs if k2 != "gated"}, workspace=_WS(ws), stream=sc)
             ev["in_free"][b].record(sc)
             ev["out_ready"][b].record(sc)
@@ -1010,6 +1013,8 @@ def main():
     ap.add_argument("--segments", type=int, default=0)
     ap.add_argument("--threads-per-channel", type=int, default=0,
                     help="kernel variant (0 = chosen by the plan, 1 or 2)")
+    ap.add_argument("--deterministic", action="store_true",
+                    help="fixed-order sums for dB, dC and the parameter gradients")
     ap.add_argument("--extra-steps", type=int, default=20)
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--no-stack", action="store_true")

@@ -229,8 +229,11 @@ int best_bwd_segments(int nc, int K, int64_t per_seg, int64_t W) {
   if (per_seg < 1) per_seg = 1;
   if (W < 1) W = 1;
   int64_t s_max = 6 * W / per_seg;
-  const int64_t two_chunks = (nc + 1) / 2;
-  if (s_max > two_chunks) s_max = two_chunks;
+  // at least two chunks per segment, or one chunk once a chunk spans
+  // several tiles (it is then long enough on its own)
+  const int64_t min_chunks = K > KT ? 1 : 2;
+  const int64_t cap = (nc + min_chunks - 1) / min_chunks;
+  if (s_max > cap) s_max = cap;
   if (s_max > 65535) s_max = 65535;
   if (s_max < 1) s_max = 1;
   int best_S = 1;
@@ -333,7 +336,9 @@ m3_status make_plan(const m3_dims* dm, m3_dtype act, Plan* p) {
       want_b = best_bwd_segments(p->nc, p->K, (int64_t)p->B * groups_b, wave_b);
       int Sb1 = 1, mb1 = 1;
       fix_segments(p->nc, p->K, want_b, &Sb1, &mb1);
-      split = tpc == 0 && (int64_t)p->B * groups_b * Sb1 <= wave_b;
+      // (chunks of several tiles keep one thread per channel: the split
+      // kernels' extra per-step work would be paid on every forward item too)
+      split = tpc == 0 && p->K <= KT && (int64_t)p->B * groups_b * Sb1 <= wave_b;
       auto_split_b = split;
     }
     if (split) {

@@ -170,10 +170,16 @@ __global__ void __launch_bounds__(GB) m3_bwd_agg_kernel(const __grid_constant__ 
       sdelta += v.x;
       const float2 dl2 = f2b(v.x);
       const float2 dy2 = f2b(v.y);
-      const float2* C2 = reinterpret_cast<const float2*>(fC + j * N + NL * hf);
+      // this thread's NL lanes of C_t, four at a time (16-byte loads)
+      const float4* C4 = reinterpret_cast<const float4*>(fC + j * N + NL * hf);
 #pragma unroll
-      for (int q = 0; q < NL / 2; ++q) {
-        carry[q] = __fmul2_rn(ex2x2(__fmul2_rn(dl2, a2[q])), __ffma2_rn(dy2, C2[q], carry[q]));
+      for (int q4 = 0; q4 < NL / 4; ++q4) {
+        const float4 cv = C4[q4];
+        const int q = 2 * q4;
+        carry[q] = __fmul2_rn(ex2x2(__fmul2_rn(dl2, a2[q])),
+                              __ffma2_rn(dy2, make_float2(cv.x, cv.y), carry[q]));
+        carry[q + 1] = __fmul2_rn(ex2x2(__fmul2_rn(dl2, a2[q + 1])),
+                                  __ffma2_rn(dy2, make_float2(cv.z, cv.w), carry[q + 1]));
       }
     }
     __syncthreads();
@@ -431,17 +437,14 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(const __grid_constant__ B
       float4* s1 = s0 + (size_t)KT * GB;
 
       if (fw) {
-        // ---- forward item: the states through tile j, from the chunk's
-        // checkpoint (tile 0) or the sub-checkpoint this thread wrote in the
-        // item before ----
+        // ---- forward item: the states through tile j, from the start state
+        // in this buffer (the chunk's checkpoint for tile 0, else left by the
+        // forward item before) ----
         float2 hs[NS / 2];
-        {
-          const float* h0 = j == 0 ? ckt + tid : a.sk + ((size_t)slot() * g.nsk + (j - 1)) * NS * GB + tid;
 #pragma unroll
-          for (int i = 0; i < NS / 2; ++i) {
-            const int n = lane_of(i);
-            hs[i] = make_float2(h0[n * GB], h0[(n + 1) * GB]);
-          }
+        for (int i = 0; i < NS / 2; ++i) {
+          const int n = lane_of(i);
+          hs[i] = make_float2(ckt[n * GB + tid], ckt[(n + 1) * GB + tid]);
         }
         {
           float xm3 = Act<T>::ld(xt + 0 * GB + tid);
@@ -487,8 +490,10 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(const __grid_constant__ B
             st_keep(skp + (n + 1) * GB, hs[i].y, keep_policy);
           }
           fence_proxy_async_global();
-        } else {
-          // the state before the last tile: the start state of the next item
+        }
+        {
+          // and the start state of the next item (the next forward item, or
+          // the backward item of the last tile), whose copies bring none
           float* ckn = reinterpret_cast<float*>(smem + (size_t)(buf ^ 1) * L.tile + L.ck);
 #pragma unroll
           for (int i = 0; i < NS / 2; ++i) {

@@ -243,16 +243,13 @@ __global__ void __launch_bounds__(128, 4) m3_bwd2_kernel(const __grid_constant__
 
     if (fw) {
       // ---- forward item: this thread's lanes of the states through tile
-      // jt, from the chunk's checkpoint (tile 0) or the sub-checkpoint this
-      // thread wrote in the item before ----
+      // jt, from the start state in this buffer (the chunk's checkpoint for
+      // tile 0, else left by the forward item before) ----
       float2 hs[4];
-      {
-        const float* h0 = jt == 0 ? ckt + ch : a.sk + ((size_t)slot * g.nsk + (jt - 1)) * N * CH + ch;
 #pragma unroll
-        for (int P = 0; P < 4; ++P) {
-          const int n = lane_of(P);
-          hs[P] = make_float2(h0[n * CH], h0[(n + 1) * CH]);
-        }
+      for (int P = 0; P < 4; ++P) {
+        const int n = lane_of(P);
+        hs[P] = make_float2(ckt[n * CH + ch], ckt[(n + 1) * CH + ch]);
       }
       for (int j = hf; j < steps; j += G) {
         const float xm3 = Act<T>::ld(xt + j * CH + ch);
@@ -288,8 +285,10 @@ __global__ void __launch_bounds__(128, 4) m3_bwd2_kernel(const __grid_constant__
           st_keep(skp + (n + 1) * CH, hs[P].y, keep_policy);
         }
         fence_proxy_async_global();
-      } else {
-        // the state before the last tile: the start state of the next item
+      }
+      {
+        // and the start state of the next item (the next forward item, or
+        // the backward item of the last tile), whose copies bring none
         float* ckn = reinterpret_cast<float*>(smem + (size_t)(buf ^ 1) * L.tile + L.ck);
 #pragma unroll
         for (int P = 0; P < 4; ++P) {
