@@ -730,6 +730,45 @@ def extras(torch, binding, device, args, flush, stream):
         out["m2p8b_stack24"] = stack24(torch, binding, device, args, stream)
     out["decode"] = decode_extras(torch, binding, device, flush)
     out["conv_bwd"] = conv_bwd_extras(torch, binding, device, flush)
+    out["dt_proj"] = dt_proj_extras(torch, device, flush)
+    return out
+
+
+def dt_proj_extras(torch, device, flush, steps=20):
+    """The low-rank dt_proj that feeds delta_raw (delta_raw = dt_low W_dt^T,
+    dt_rank = d_model / 16), as the unfused path runs it: one bf16 GEMM
+    (cuBLAS) writing delta_raw, L2 flushed before each.  Beside it the
+    least a fold into the scan kernels would add to the forward alone:
+    dt_rank FP32 multiply-adds per element at the GPU's FP32 lane rate (152
+    SMs x 128 lanes x the maximum clock), on kernels already bound by
+    instruction issue."""
+    out = {}
+    for name in ("trainer_b8_t128_d512", "m130m_b8_t2048_d1536", "longseq_b1_t65536_d2048",
+                 "m2p8b_b4_t4096_d5120"):
+        w = WORKLOADS[name]
+        R = (w.d_inner // 2 + 15) // 16  # d_model = d_inner / 2
+        g = torch.Generator(device=device)
+        g.manual_seed(7)
+        low = torch.randn(w.batch * w.seq_len, R, device=device, generator=g).to(torch.bfloat16)
+        W = (torch.randn(R, w.d_inner, device=device, generator=g) * 0.1).to(torch.bfloat16)
+        dr = torch.empty(w.batch * w.seq_len, w.d_inner, device=device, dtype=torch.bfloat16)
+        s = torch.cuda.current_stream()
+        for _ in range(3):
+            torch.matmul(low, W, out=dr)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        for e0, e1 in ev:
+            flush.zero_()
+            e0.record(s)
+            torch.matmul(low, W, out=dr)
+            e1.record(s)
+        torch.cuda.synchronize()
+        ms = sorted(e0.elapsed_time(e1) for e0, e1 in ev)[steps // 2]
+        fold_ms = R * w.elems / (alu_peak_gops() * 1e9) * 1e3
+        out[name] = {"dt_rank": R, "gemm_us": round(ms * 1e3, 1),
+                     "fold_fwd_floor_us": round(fold_ms * 1e3, 1)}
+        del low, W, dr
+        torch.cuda.empty_cache()
     return out
 
 
