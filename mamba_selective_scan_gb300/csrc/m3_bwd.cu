@@ -334,7 +334,9 @@ __global__ void __launch_bounds__(GB, 3) m3_bwd_kernel(const __grid_constant__ B
   // backward item also z, d_gated and C; and the start state (16 rows of GB
   // floats) when it comes from the chunk's checkpoint or a sub-checkpoint.
   // Rows outside [0, T) and channels past d_inner arrive as zeros.
-  auto tiles_of = [&](int c) { return (min(K, g.T - c * K) + KS - 1) / KS; };
+  // tiles of chunk c: one when a chunk is at most a tile, else whole KT-step
+  // tiles (a shift, no division)
+  auto tiles_of = [&](int c) { return K <= KT ? 1 : (min(K, g.T - c * K) + KT - 1) / KT; };
   const bool misaligned = (smem_u32(smem) & 127u) != 0;  // tile copies need 128-byte aligned buffers
   auto stage = [&](int c, int q, int buf) {
     if (tid == 0 && !misaligned) {

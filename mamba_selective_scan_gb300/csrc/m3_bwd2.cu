@@ -144,7 +144,9 @@ __global__ void __launch_bounds__(128, 4) m3_bwd2_kernel(const __grid_constant__
   // backward item also z, d_gated, C; and the start state when it comes
   // from the chunk's checkpoint or a sub-checkpoint.  Rows outside [0, T)
   // and channels past d_inner arrive as zeros.
-  auto tiles_of = [&](int c) { return (min(K, g.T - c * K) + KS - 1) / KS; };
+  // tiles of chunk c: one when a chunk is at most a tile, else whole KT-step
+  // tiles (a shift, no division)
+  auto tiles_of = [&](int c) { return K <= KT ? 1 : (min(K, g.T - c * K) + KT - 1) / KT; };
   const uint32_t fwd_bytes = (uint32_t)(((2 * KS + 3) * CH + KS * N) * sizeof(T));
   const uint32_t bwd_bytes = (uint32_t)(((4 * KS + 3) * CH + 2 * KS * N) * sizeof(T));
   const uint32_t ck_bytes = (uint32_t)(N * CH * 4);

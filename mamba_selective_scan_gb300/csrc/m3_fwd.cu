@@ -137,6 +137,13 @@ __global__ void __launch_bounds__(GF) m3_fwd_kernel(const __grid_constant__ FwdA
 
 
   float4* scs = reinterpret_cast<float4*>(smem + L.sc) + tid;  // this thread's slots, stride GF
+  const bool want_y = a.y_dbg != nullptr;
+  // checkpoints: the state before every step t with t % K == 0; kc = steps
+  // from the current sub-tile's start to the next one, ck = that checkpoint
+  // (running counters: no division per step or sub-tile)
+  int kc = 0;
+  float* ck = a.ckpt + (((size_t)b * g.nc + c_begin) * NS) * g.D + d;
+  const size_t ck_step = (size_t)NS * g.D;
   // The final pass writes gated (and y) of a tile into the staging regions of
   // z (and delta_raw), which its scalar pass has consumed, and stores each
   // whole 8-step sub-tile with a tile copy; a sub-tile cut short by the end
@@ -187,11 +194,10 @@ __global__ void __launch_bounds__(GF) m3_fwd_kernel(const __grid_constant__ FwdA
         scs[j * GF] = make_float4(delta, delta * u, Dd * u, gz);
       }
       if (FINAL && j0 == 0 && more) stage(t0 + TT, buf ^ 1);
-      // state pass: the only loop-carried dependence is h.  A checkpoint is
-      // the state before every step t with t % K == 0: the first such step of
-      // this sub-tile is jc, then every K-th.
+      // state pass: the only loop-carried dependence is h; a checkpoint at
+      // every step jc = kc, kc + K, ... of this sub-tile
       const int tsub = t0 + j0;
-      int jc = FINAL ? (g.K - tsub % g.K) % g.K : SUB;
+      int jc = kc;
       const bool whole = tsub + SUB <= t_end;  // stored by a tile copy
 #pragma unroll
       for (int j = 0; j < SUB; ++j) {
@@ -199,13 +205,13 @@ __global__ void __launch_bounds__(GF) m3_fwd_kernel(const __grid_constant__ FwdA
         if (FINAL && j == jc) {
           jc += g.K;
           if (active) {
-            float* ck = a.ckpt + (((size_t)b * g.nc + (tsub + j) / g.K) * NS) * g.D + d;
 #pragma unroll
             for (int i = 0; i < NS / 2; ++i) {
               ck[(size_t)(2 * i) * g.D] = h[i].x;
               ck[(size_t)(2 * i + 1) * g.D] = h[i].y;
             }
           }
+          ck += ck_step;
         }
         const float4 v = scs[j * GF];
         const float2 dl2 = f2b(v.x);
@@ -228,11 +234,11 @@ __global__ void __launch_bounds__(GF) m3_fwd_kernel(const __grid_constant__ FwdA
           const float y = ((y01.x + y01.y) + (y23.x + y23.y)) + v.z;
           if (whole) {
             Act<T>::st(og + (j0 + j) * GF + tid, y * v.w);
-            if (a.y_dbg) Act<T>::st(oy + (j0 + j) * GF + tid, y);
+            if (want_y) Act<T>::st(oy + (j0 + j) * GF + tid, y);
           } else if (active) {
             const size_t i = ((size_t)b * g.T + tsub + j) * g.D + d;
             Act<T>::st(static_cast<T*>(a.gated) + i, y * v.w);
-            if (a.y_dbg) Act<T>::st(static_cast<T*>(a.y_dbg) + i, y);
+            if (want_y) Act<T>::st(static_cast<T*>(a.y_dbg) + i, y);
           }
         } else {
 #pragma unroll
@@ -245,6 +251,7 @@ __global__ void __launch_bounds__(GF) m3_fwd_kernel(const __grid_constant__ FwdA
           }
         }
       }
+      kc = jc - ns;  // the next checkpoint, from the next sub-tile's start
     }
     if (FINAL) {
       fence_proxy_async();  // this thread's output rows, before the tile stores read them
@@ -254,7 +261,7 @@ __global__ void __launch_bounds__(GF) m3_fwd_kernel(const __grid_constant__ FwdA
         for (int j0 = 0; j0 < steps; j0 += SUB) {
           if (t0 + j0 + SUB > t_end) break;
           tma_store_3d(&a.tm[TF_OG], og + j0 * GF, d0, t0 + j0, b);
-          if (a.y_dbg) tma_store_3d(&a.tm[TF_OY], oy + j0 * GF, d0, t0 + j0, b);
+          if (want_y) tma_store_3d(&a.tm[TF_OY], oy + j0 * GF, d0, t0 + j0, b);
         }
         bulk_commit();
       }
@@ -384,6 +391,9 @@ __global__ void __launch_bounds__(128) m3_fwd2_kernel(const __grid_constant__ Fw
   float sdelta = 0.f;
   float4* scs = reinterpret_cast<float4*>(smem + L.sc) + ch;  // shared by the channel's threads, stride CH
   int kc = 0;  // steps left until the next checkpoint
+  // the next checkpoint's lanes of this thread (a running pointer: no division)
+  float* ck = a.ckpt + (((size_t)b * g.nc + c_begin) * N + 8 * hf) * g.D + d;
+  const size_t ck_step = (size_t)N * g.D;
   for (int t0 = t_begin, it = 0; t0 < t_end; t0 += TT, ++it) {
     const int buf = it & 1;
     if (t0 + TT < t_end) stage(t0 + TT, buf ^ 1);
@@ -434,15 +444,14 @@ __global__ void __launch_bounds__(128) m3_fwd2_kernel(const __grid_constant__ Fw
       for (int j = 0; j < ns; ++j) {
         if (FINAL) {
           if (kc == 0) {
-            const int t = t0 + j0 + j;
             if (active) {
-              float* ck = a.ckpt + (((size_t)b * g.nc + t / g.K) * N + 8 * hf) * g.D + d;
 #pragma unroll
               for (int P = 0; P < 4; ++P) {
                 ck[(size_t)(2 * P) * g.D] = h[P].x;
                 ck[(size_t)(2 * P + 1) * g.D] = h[P].y;
               }
             }
+            ck += ck_step;
             kc = g.K;
           }
           --kc;
