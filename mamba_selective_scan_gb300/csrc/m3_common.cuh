@@ -19,7 +19,8 @@ constexpr int GF = 128;       // forward: channels (= threads) per block
 constexpr int GB = 128;       // backward: channels (= threads) per block = 4 warps,
                               // one per tensor-memory lane quadrant
 constexpr int NWB = GB / 32;  // backward warps per block
-constexpr int TT = 16;        // forward / aggregate staging tile (steps)
+constexpr int TT = 8;         // forward / aggregate staging tile (steps): the small
+                              // staging footprint lets more blocks stay resident
 constexpr int SUB = 8;        // forward scalar sub-tile (steps)
 constexpr int KT = 8;         // backward tile: steps whose states are recomputed on chip at once
 constexpr int KMAX = 256;     // largest checkpoint interval
