@@ -52,6 +52,7 @@ template <typename T, int TPC, int N>
 __global__ void __launch_bounds__(GB) m3_bwd_agg_kernel(const __grid_constant__ BwdArgs a) {
   constexpr int G = GB / TPC;        // channels per block
   constexpr int NL = N / TPC;        // state lanes per thread
+  constexpr int TA = TPC == 1 ? TT : TT2;  // staging tile (steps)
   extern __shared__ __align__(128) unsigned char smem[];
   const Geo g = a.g;
   const int tid = threadIdx.x;
@@ -64,11 +65,11 @@ __global__ void __launch_bounds__(GB) m3_bwd_agg_kernel(const __grid_constant__ 
   const bool active = d < g.D;
   const int t_begin = s * g.m * g.K;
   const int t_end = min((s + 1) * g.m * g.K, g.T);
-  const AggSmem L = agg_smem(sizeof(T), N);
+  const AggSmem L = agg_smem(sizeof(T), N, TA);
   float* fC = reinterpret_cast<float*>(smem + L.fC);
-  const int ntiles = (t_end - t_begin + TT - 1) / TT;
-  auto tile_start = [&](int i) { return max(t_begin, t_end - (i + 1) * TT); };
-  // Tiles of TT rows (the first one, at the segment's start, overlaps rows
+  const int ntiles = (t_end - t_begin + TA - 1) / TA;
+  auto tile_start = [&](int i) { return max(t_begin, t_end - (i + 1) * TA); };
+  // Tiles of TA rows (the first one, at the segment's start, overlaps rows
   // already covered; only its own rows are read) by tensor-map copies
   // issued by thread 0.
   __shared__ __align__(8) uint64_t tbar[2];  // tile copies into staging buffer 0 / 1
@@ -79,7 +80,7 @@ __global__ void __launch_bounds__(GB) m3_bwd_agg_kernel(const __grid_constant__ 
   }
   __syncthreads();
   const bool misaligned = (smem_u32(smem) & 127u) != 0;  // tile copies need 128-byte aligned buffers
-  const uint32_t tile_bytes = (uint32_t)((3 * TT * G + TT * N) * sizeof(T));
+  const uint32_t tile_bytes = (uint32_t)((3 * TA * G + TA * N) * sizeof(T));
   auto stage = [&](int i, int buf) {
     if (tid == 0 && !misaligned) {
       unsigned char* base = smem + (size_t)buf * L.tile;
@@ -146,7 +147,7 @@ __global__ void __launch_bounds__(GB) m3_bwd_agg_kernel(const __grid_constant__ 
     }
     const unsigned char* base = smem + (size_t)buf * L.tile;
     const int t0 = tile_start(i);
-    const int steps = (t_end - i * TT) - t0;
+    const int steps = (t_end - i * TA) - t0;
     {
       const T* Ct = reinterpret_cast<const T*>(base + L.Ct);
       for (int k = tid; k < steps * N; k += GB) fC[k] = Act<T>::ld(Ct + k);
@@ -896,7 +897,8 @@ bool encode_bwd_maps(const Plan& p, int ch, bool scan, BwdArgs& a) {
   const uint64_t bdim[3] = {N, T_, B}, bstr[2] = {ld * es, T_ * ld * es};
   const uint64_t cdim[4] = {D, N, nc, B}, cstr[3] = {D * 4, N * D * 4, nc * N * D * 4};
   const uint32_t box_x[3] = {c, K + 3, 1}, box_a[3] = {c, K, 1}, box_b[3] = {n, K, 1}, box_c[4] = {c, n, 1, 1};
-  const uint32_t box_ta[3] = {c, TT, 1}, box_tb[3] = {n, TT, 1};
+  const uint32_t ta = (uint32_t)(p.bwd_tpc == 1 ? TT : TT2);  // the aggregate kernel's tile
+  const uint32_t box_ta[3] = {c, ta, 1}, box_tb[3] = {n, ta, 1};
   bool ok = true;
   if (p.nsk > 0) {  // sub-checkpoints [blocks][nsk][N][ch]
     const uint64_t blocks = (uint64_t)((p.D + ch - 1) / ch) * p.Sb * p.B, nsk = p.nsk;
@@ -936,7 +938,7 @@ m3_status launch_bwd(const Plan& p, BwdArgs a, cudaStream_t st, int smem_per_sm,
     const bool split = p.bwd_tpc != 1;
     const int ch = split ? 128 / (p.N / 8) : GB;
     e = launch_k(agg_for<T>(split, p.N), dim3((p.D + ch - 1) / ch, p.Sb - 1, p.B), GB,
-                 agg_smem(sizeof(T), p.N).total, st, false, a);
+                 agg_smem(sizeof(T), p.N, split ? TT2 : TT).total, st, false, a);
     if (note(e) != cudaSuccess) return M3_ERR_CUDA;
   } else if (!p.det) {
     // only the d_state columns of each (batch, step) row belong to dB and dC
@@ -990,7 +992,7 @@ cudaError_t set_bwd_attrs() {
   for (int i = 0; i < 4; ++i) {
     void (*k)(BwdArgs) = agg_for<T>(splits[i], ns[i]);
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)agg_smem(es, ns[i]).total);
+      e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)agg_smem(es, ns[i], splits[i] ? TT2 : TT).total);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   }
   void (*bwd_kernels[28])(BwdArgs) = {

@@ -19,8 +19,10 @@ constexpr int GF = 128;       // forward: channels (= threads) per block
 constexpr int GB = 128;       // backward: channels (= threads) per block = 4 warps,
                               // one per tensor-memory lane quadrant
 constexpr int NWB = GB / 32;  // backward warps per block
-constexpr int TT = 8;         // forward / aggregate staging tile (steps): the small
-                              // staging footprint lets more blocks stay resident
+constexpr int TT = 8;         // one-thread forward / aggregate staging tile (steps):
+                              // the small footprint lets more blocks stay resident
+constexpr int TT2 = 16;       // the split kernels' staging tile: they serve grids under
+                              // a wave, where fewer, longer tiles wait less
 constexpr int SUB = 8;        // forward scalar sub-tile (steps)
 constexpr int KT = 8;         // backward tile: steps whose states are recomputed on chip at once
 constexpr int KMAX = 256;     // largest checkpoint interval
@@ -410,8 +412,8 @@ struct FwdArgs {
   CUtensorMap tm[7];
 };
 // tensor maps of FwdArgs::tm: activations [B, T, D] with boxes of the
-// block's channels x TT rows (x: TT + 3 rows in the split kernels, which
-// stage the conv halo); B and C [B, T, ld] with boxes of N x TT; stores of
+// block's channels x TT rows (TT2 in the split kernels, whose x boxes add
+// the three conv halo rows); B and C [B, T, ld] with boxes of N x TT (TT2); stores of
 // the one-thread final pass: gated and y [B, T, D] with boxes of GF x SUB
 enum { TF_X = 0, TF_DR, TF_Z, TF_B, TF_C, TF_OG, TF_OY };
 
@@ -465,7 +467,8 @@ struct TailArgs {
 // per channel): main kernels -- activations [B, T, D] x (KS + 3) rows (x)
 // or KS rows, B and C [B, T, ld] N x KS, checkpoints [B, nc, N, D] f32
 // channels x N, sub-checkpoints [blocks, nsk, N, ch] f32 ch x N;
-// aggregate kernel -- delta_raw, z, d_gated TT rows, C N x TT; stores of
+// aggregate kernel -- delta_raw, z, d_gated TT rows (TT2 for d_state / 8
+// threads per channel), C N x TT (TT2); stores of
 // the one-thread main kernel -- dz, d_delta_raw, d_x, du [B, T, D] x KS rows
 enum { TM_X = 0, TM_DR, TM_Z, TM_DG, TM_B, TM_C, TM_CK, TM_ADR, TM_AZ, TM_ADG, TM_AC, TM_SK,
        TM_ODZ, TM_ODR, TM_ODX, TM_ODU };
@@ -493,8 +496,8 @@ __host__ __device__ inline FwdSmem fwd_smem(int es) {
 }
 
 // Split forward shared memory (CH = 128 / (N / 8) channels): two staging
-// buffers {x: [TT+3][CH] (three halo rows), delta_raw, z: [TT][CH]; B, C:
-// [TT][N]}, float B and C of the tile, and per-step scalars sc[SUB][CH]
+// buffers {x: [TT2+3][CH] (three halo rows), delta_raw, z: [TT2][CH]; B, C:
+// [TT2][N]}, float B and C of the tile, and per-step scalars sc[SUB][CH]
 // float4 shared by the threads of a channel.
 struct Fwd2Smem {
   size_t x, dr, z, Bt, Ct, tile, fB, fC, sc, total;
@@ -503,14 +506,14 @@ __host__ __device__ inline Fwd2Smem fwd2_smem(int es, int N) {
   const int CH = 128 / (N / 8);  // channels per block
   Fwd2Smem s;
   s.x = 0;
-  s.dr = s.x + align_up((size_t)(TT + 3) * CH * es, 128);
-  s.z = s.dr + align_up((size_t)TT * CH * es, 128);
-  s.Bt = s.z + align_up((size_t)TT * CH * es, 128);
-  s.Ct = s.Bt + align_up((size_t)TT * N * es, 128);
-  s.tile = s.Ct + align_up((size_t)TT * N * es, 128);
+  s.dr = s.x + align_up((size_t)(TT2 + 3) * CH * es, 128);
+  s.z = s.dr + align_up((size_t)TT2 * CH * es, 128);
+  s.Bt = s.z + align_up((size_t)TT2 * CH * es, 128);
+  s.Ct = s.Bt + align_up((size_t)TT2 * N * es, 128);
+  s.tile = s.Ct + align_up((size_t)TT2 * N * es, 128);
   s.fB = 2 * s.tile;
-  s.fC = s.fB + (size_t)TT * N * 4;
-  s.sc = s.fC + (size_t)TT * N * 4;
+  s.fC = s.fB + (size_t)TT2 * N * 4;
+  s.sc = s.fC + (size_t)TT2 * N * 4;
   s.total = s.sc + (size_t)SUB * CH * 16;
   return s;
 }
@@ -581,21 +584,22 @@ __host__ __device__ inline Bwd2Smem bwd2_smem(int K, int es, int N) {
   return s;
 }
 
-// Backward aggregate shared memory: two buffers {delta_raw, z, d_gated:
-// [TT][GB]; C: [TT][16]}, float C and per-step (delta, dy) [TT][GB] float2.
+// Backward aggregate shared memory for tiles of tt steps: two buffers
+// {delta_raw, z, d_gated: [tt][GB]; C: [tt][N]}, float C and per-step
+// (delta, dy) [tt][GB] float2.
 struct AggSmem {
   size_t dr, z, dg, Ct, tile, fC, sc, total;
 };
-__host__ __device__ inline AggSmem agg_smem(int es, int N = NS) {
+__host__ __device__ inline AggSmem agg_smem(int es, int N, int tt) {
   AggSmem s;
   s.dr = 0;
-  s.z = s.dr + align_up((size_t)TT * GB * es, 128);
-  s.dg = s.z + align_up((size_t)TT * GB * es, 128);
-  s.Ct = s.dg + align_up((size_t)TT * GB * es, 128);
-  s.tile = s.Ct + align_up((size_t)TT * N * es, 128);
+  s.z = s.dr + align_up((size_t)tt * GB * es, 128);
+  s.dg = s.z + align_up((size_t)tt * GB * es, 128);
+  s.Ct = s.dg + align_up((size_t)tt * GB * es, 128);
+  s.tile = s.Ct + align_up((size_t)tt * N * es, 128);
   s.fC = 2 * s.tile;
-  s.sc = s.fC + (size_t)TT * N * 4;
-  s.total = s.sc + (size_t)TT * GB * 8;
+  s.sc = s.fC + (size_t)tt * N * 4;
+  s.total = s.sc + (size_t)tt * GB * 8;
   return s;
 }
 

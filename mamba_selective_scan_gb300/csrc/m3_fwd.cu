@@ -340,7 +340,7 @@ __global__ void __launch_bounds__(128) m3_fwd2_kernel(const __grid_constant__ Fw
   __syncthreads();
   const bool misaligned = (smem_u32(smem) & 127u) != 0;  // tile copies need 128-byte aligned buffers
   const uint32_t tile_bytes =
-      (uint32_t)((((FINAL ? 3 : 2) * TT + 3) * CH + (FINAL ? 2 : 1) * TT * N) * sizeof(T));
+      (uint32_t)((((FINAL ? 3 : 2) * TT2 + 3) * CH + (FINAL ? 2 : 1) * TT2 * N) * sizeof(T));
   auto stage = [&](int t0, int buf) {
     if (tid == 0 && !misaligned) {
       unsigned char* base = smem + (size_t)buf * L.tile;
@@ -394,10 +394,10 @@ __global__ void __launch_bounds__(128) m3_fwd2_kernel(const __grid_constant__ Fw
   // the next checkpoint's lanes of this thread (a running pointer: no division)
   float* ck = a.ckpt + (((size_t)b * g.nc + c_begin) * N + 8 * hf) * g.D + d;
   const size_t ck_step = (size_t)N * g.D;
-  for (int t0 = t_begin, it = 0; t0 < t_end; t0 += TT, ++it) {
+  for (int t0 = t_begin, it = 0; t0 < t_end; t0 += TT2, ++it) {
     const int buf = it & 1;
-    if (t0 + TT < t_end) stage(t0 + TT, buf ^ 1);
-    if (!fwd_tiles_landed(tbar, it, misaligned, t0 + TT < t_end, a.status)) return;
+    if (t0 + TT2 < t_end) stage(t0 + TT2, buf ^ 1);
+    if (!fwd_tiles_landed(tbar, it, misaligned, t0 + TT2 < t_end, a.status)) return;
     unsigned char* base = smem + (size_t)buf * L.tile;
     if (a.conv_in && t0 < 3 && active && hf == 0) {
       // halo rows before step 0 (staged as zeros): the carried conv inputs
@@ -408,7 +408,7 @@ __global__ void __launch_bounds__(128) m3_fwd2_kernel(const __grid_constant__ Fw
     {
       const T* Bt = reinterpret_cast<const T*>(base + L.Bt);
       const T* Ct = reinterpret_cast<const T*>(base + L.Ct);
-      for (int i = tid; i < TT * N; i += 128) {
+      for (int i = tid; i < TT2 * N; i += 128) {
         fB[i] = Act<T>::ld(Bt + i);
         if (FINAL) fC[i] = Act<T>::ld(Ct + i);
       }
@@ -417,7 +417,7 @@ __global__ void __launch_bounds__(128) m3_fwd2_kernel(const __grid_constant__ Fw
     const T* xt = reinterpret_cast<const T*>(base + L.x);
     const T* drt = reinterpret_cast<const T*>(base + L.dr);
     const T* zt = reinterpret_cast<const T*>(base + L.z);
-    const int steps = min(TT, t_end - t0);
+    const int steps = min(TT2, t_end - t0);
     for (int j0 = 0; j0 < steps; j0 += SUB) {
       const int ns = min(SUB, steps - j0);
       // scalar pass, this thread's steps (every G-th)
@@ -526,15 +526,16 @@ __global__ void __launch_bounds__(128) m3_fwd2_kernel(const __grid_constant__ Fw
   }
 }
 
-// Tensor maps of the forward's tiles: boxes of ch channels x TT rows (x:
-// TT + halo rows) and N x TT for B and C.
+// Tensor maps of the forward's tiles: boxes of ch channels x tt rows (x:
+// tt + halo rows) and N x tt for B and C; tt is the kernel's staging tile.
 template <typename T>
-bool encode_fwd_maps(const Plan& p, int ch, int halo, FwdArgs& a) {
+bool encode_fwd_maps(const Plan& p, int ch, int halo, int tt, FwdArgs& a) {
   const uint64_t es = sizeof(T), D = p.D, T_ = p.T, B = p.B, N = p.N, ld = p.ldbc;
   const uint32_t c = (uint32_t)ch, n = (uint32_t)p.N;
   const uint64_t adim[3] = {D, T_, B}, astr[2] = {D * es, T_ * D * es};
   const uint64_t bdim[3] = {N, T_, B}, bstr[2] = {ld * es, T_ * ld * es};
-  const uint32_t box_x[3] = {c, (uint32_t)(TT + halo), 1}, box_a[3] = {c, TT, 1}, box_b[3] = {n, TT, 1};
+  const uint32_t rows = (uint32_t)tt;
+  const uint32_t box_x[3] = {c, rows + halo, 1}, box_a[3] = {c, rows, 1}, box_b[3] = {n, rows, 1};
   const uint32_t box_o[3] = {c, SUB, 1};
   bool ok = encode_tile_map(&a.tm[TF_X], (int)es, 3, a.x, adim, astr, box_x) &&
             encode_tile_map(&a.tm[TF_DR], (int)es, 3, a.dr, adim, astr, box_a) &&
@@ -559,7 +560,7 @@ m3_status launch_fwd(const Plan& p, FwdArgs a, cudaStream_t st) {
     const int ch = 128 / (p.N / 8);
     const dim3 ga((p.D + ch - 1) / ch, p.Sf - 1, p.B), gf((p.D + ch - 1) / ch, p.Sf, p.B);
     const size_t smem2 = fwd2_smem(sizeof(T), p.N).total;
-    if (!encode_fwd_maps<T>(p, ch, 3, a)) return M3_ERR_CUDA;
+    if (!encode_fwd_maps<T>(p, ch, 3, TT2, a)) return M3_ERR_CUDA;
     void (*agg)(FwdArgs) = p.N == 16 ? m3_fwd2_kernel<T, false, 16>
                          : p.N == 32 ? m3_fwd2_kernel<T, false, 32> : m3_fwd2_kernel<T, false, 64>;
     void (*fin)(FwdArgs) = p.N == 16 ? m3_fwd2_kernel<T, true, 16>
@@ -569,7 +570,7 @@ m3_status launch_fwd(const Plan& p, FwdArgs a, cudaStream_t st) {
     if (e == cudaSuccess) e = cudaGetLastError();
     return note(e) == cudaSuccess ? M3_OK : M3_ERR_CUDA;
   }
-  if (!encode_fwd_maps<T>(p, GF, 0, a)) return M3_ERR_CUDA;
+  if (!encode_fwd_maps<T>(p, GF, 0, TT, a)) return M3_ERR_CUDA;
   if (p.Sf > 1) e = launch_k(m3_fwd_kernel<T, false>, dim3(groups, p.Sf - 1, p.B), GF, smem, st, false, a);
   if (e == cudaSuccess)
     e = launch_k(m3_fwd_kernel<T, true>, dim3(groups, p.Sf, p.B), GF, smem, st, p.Sf > 1, a);
