@@ -315,7 +315,7 @@ m3_status make_plan(const m3_dims* dm, m3_dtype act, Plan* p) {
   const int groups_b = (p->D + GB - 1) / GB;
   int want_f = 1, want_b = 1;
   int64_t wave_b = 3 * 152;  // one-thread backward blocks resident at once
-  int64_t wave_f = 5 * 152;  // one-thread forward blocks resident at once
+  int64_t wave_f = 6 * 152;  // one-thread forward blocks resident at once
   bool auto_split_b = false;  // backward kernel variant decided with its segments
   if (dm->segments > 0) {
     want_f = want_b = (int)dm->segments;
@@ -355,7 +355,7 @@ m3_status make_plan(const m3_dims* dm, m3_dtype act, Plan* p) {
   }
   const bool empty = (size_t)p->B * p->T * p->D == 0;
   // d_state 16: the split kernels (two threads per channel) when the
-  // one-thread grid fills less than one wave (three backward, five forward
+  // one-thread grid fills less than one wave (three backward, six forward
   // blocks per SM on a 152-SM GPU, or the device's figures when the
   // segments were chosen for it); wider states: always the split kernels,
   // d_state / 8 threads per channel

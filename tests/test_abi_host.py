@@ -341,7 +341,7 @@ def test_threads_per_channel_are_resolved_from_the_grid(lib):
         st = lib.m3scan_plan(ctypes.byref(d), binding.M3_BF16, ctypes.byref(out))
         return binding.STATUS[st] if st else (out.fwd_threads_per_channel,
                                               out.bwd_threads_per_channel)
-    # grids under one wave of the one-thread kernels (5 forward, 3 backward
+    # grids under one wave of the one-thread kernels (6 forward, 3 backward
     # blocks per SM of a 152-SM GPU) take two threads per channel
     assert tpc(8, 128, 512, 8) == (2, 2)            # 8 x 4 groups x 8 segments = 256 blocks
     assert tpc(8, 2048, 1536, 12) == (1, 1)         # 8 x 12 x 12 = 1152 blocks
