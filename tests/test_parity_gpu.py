@@ -354,3 +354,33 @@ def test_back_to_back_calls_sharing_checkpoints_and_workspace(segments, tpc, det
                     assert torch.equal(g[k], wg[k]), k
                 else:
                     assert norm_err(to_np(g[k]), to_np(wg[k])) <= 1e-6, k
+
+
+@pytest.mark.parametrize("accumulate", [False, True])
+@pytest.mark.parametrize("act", ["f32", "bf16"])
+def test_empty_sequence_gives_zero_parameter_grads(act, accumulate):
+    # T = 0: L has no terms, so every parameter gradient is zero (or, when
+    # accumulating, the caller's values stay as they were)
+    dt = torch.float32 if act == "f32" else torch.bfloat16
+    dev = torch.device("cuda")
+    Bsz, T, D, N = 2, 0, 16, 16
+    x = torch.zeros((Bsz, T, D), dtype=dt, device=dev)
+    bc = torch.zeros((Bsz, T, N), dtype=dt, device=dev)
+    conv_w = torch.zeros((D, 4), device=dev)
+    p = [torch.zeros(D, device=dev) for _ in range(3)]
+    a_log = torch.zeros((D, N), device=dev)
+    gated, ckpt, _ = binding.m3scan_fwd(x, x, x, bc, bc, conv_w, p[0], p[1], a_log, p[2])
+    assert gated.numel() == 0
+    prior = 7.0 if accumulate else float("nan")
+    out = {"d_conv_w": torch.full((D, 4), prior, device=dev),
+           "d_conv_b": torch.full((D,), prior, device=dev),
+           "d_dt_bias": torch.full((D,), prior, device=dev),
+           "d_a_log": torch.full((D, N), prior, device=dev),
+           "dD": torch.full((D,), prior, device=dev)}
+    g = binding.m3scan_bwd(x, x, x, bc, bc, conv_w, p[0], p[1], a_log, p[2], ckpt, x, out=out,
+                           accumulate_param_grads=accumulate)
+    torch.cuda.synchronize()
+    for k in out:
+        want = torch.full_like(out[k], 7.0) if accumulate else torch.zeros_like(out[k])
+        assert torch.equal(g[k], want), k
+    assert g["dB"].numel() == 0 and g["d_x"].numel() == 0
