@@ -40,6 +40,7 @@ UNIT = "Gelem/s"
 DEFAULT_WORKLOAD = "longseq_b1_t65536_d2048"
 EXTRA_WORKLOADS = ("trainer_b8_t128_d512", "m130m_b8_t2048_d1536", "m2p8b_b4_t4096_d5120")
 HBM_TARGET_GBS = 8000.0  # the roofline bandwidth the metric is defined with
+L2_BYTES = 126 << 20     # GB300 L2 (the 256 MiB flush buffer is twice that)
 ROOFLINE_CHUNK = 128     # chunk length of the metric's minimum-bytes formula
 NS = 16
 
@@ -724,6 +725,15 @@ def extras(torch, binding, device, args, flush, stream):
                      "frac_of_8TBs": round((fb + bb) / HBM_TARGET_GBS / 1e9 / ((fa + ba) * 1e-3), 4),
                      "fwd_segments": int(L.plan.fwd_segments),
                      "bwd_segments": int(L.plan.bwd_segments), "chunk": int(L.plan.chunk)}
+        if (fb + bb) < L2_BYTES // 4:
+            # a step whose data fits in L2 several times over: also timed with
+            # the previous step's lines left in L2, as a training loop over
+            # such small layers runs it
+            wf, wb = time_steps(torch, gf, gb, args.extra_steps, None)
+            wfa, wba = sum(wf) / len(wf), sum(wb) / len(wb)
+            out[name]["warm_l2"] = {"gelem_s": round(E / ((wfa + wba) * 1e-3) / 1e9, 2),
+                                    "fwd_gelem_s": round(E / (wfa * 1e-3) / 1e9, 2),
+                                    "bwd_gelem_s": round(E / (wba * 1e-3) / 1e9, 2)}
         del gf, gb, L, t
         torch.cuda.empty_cache()
     if not args.no_stack:
