@@ -10,7 +10,7 @@ JSON line (rank 0).
 
 Timing: inputs resident in HBM; each step is two CUDA-graph replays (forward
 graph, backward graph) bracketed by CUDA events on the launching stream;
-L2 is flushed (256 MiB memset) between steps, outside the events.  The
+L2 is flushed (256 MiB memset, read back) between steps, outside the events.  The
 end-to-end number repeats the step through the Python binding with inputs
 copied from pinned host memory and results copied back inside the timed
 region.  Multi-GPU runs are independent replicas (weak scaling).
@@ -373,6 +373,14 @@ def capture(torch, layer_list, stream):
     return gf, gb
 
 
+def flush_l2(torch, flush):
+    """Evict L2 before a timed step: write a buffer twice the L2's size, then
+    read it back, so that the lines it leaves in L2 are clean and no
+    write-back of the flush lands inside the timed region."""
+    flush.zero_()
+    torch.amax(flush)
+
+
 def time_steps(torch, gf, gb, steps, flush):
     """Per-step forward and backward device times (ms) with L2 flushed
     before every step."""
@@ -381,7 +389,7 @@ def time_steps(torch, gf, gb, steps, flush):
            torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     for i in range(steps):
         if flush is not None:
-            flush.zero_()
+            flush_l2(torch, flush)
         e0, e1, e2 = ev[i]
         e0.record(s)
         gf.replay()
@@ -518,7 +526,7 @@ def gpu_arm(args):
                    "bwd_segments": int(layer.plan.bwd_segments),
                    "fwd_launches": int(layer.plan.fwd_launches),
                    "bwd_launches": int(layer.plan.bwd_launches),
-                   "l2": "flushed before every step (256 MiB memset outside the events)",
+                   "l2": "flushed before every step (256 MiB memset, then read back so that no write-back of it is timed; outside the events)",
                    "timing": "CUDA graphs (fwd, bwd) per step, CUDA events per graph",
                    "parallelism": f"replicas x{world}"},
         "hbm_roofline": hbm,
@@ -768,7 +776,7 @@ def dt_proj_extras(torch, device, flush, steps=20):
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(steps)]
         for e0, e1 in ev:
-            flush.zero_()
+            flush_l2(torch, flush)
             e0.record(s)
             torch.matmul(low, W, out=dr)
             e1.record(s)
@@ -824,7 +832,7 @@ def decode_extras(torch, binding, device, flush, steps=20):
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(steps)]
         for e0, e1 in ev:
-            flush.zero_()
+            flush_l2(torch, flush)
             e0.record(s)
             binding.raw_decode(*args)
             e1.record(s)
@@ -866,7 +874,7 @@ def conv_bwd_extras(torch, binding, device, flush, steps=20):
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(steps)]
         for e0, e1 in ev:
-            flush.zero_()
+            flush_l2(torch, flush)
             e0.record(s)
             binding.raw_conv_bwd(*args)
             e1.record(s)
