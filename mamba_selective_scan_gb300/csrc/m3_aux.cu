@@ -179,9 +179,13 @@ __global__ void m3_conv_fin_kernel(ConvArgs a) {
 // step are staged into the other half of a double buffer.
 // TL: the block's carried states arrive by one tensor-map copy into shared
 // memory (hs[R][N][CH]), issued before the other loads and waited for after
-// them; otherwise each thread loads its own lanes.
-template <typename T, int N, int R, bool TL>
-__global__ void __launch_bounds__(GD) m3_decode_kernel(const __grid_constant__ DecArgs a) {
+// them; otherwise each thread loads its own lanes.  HS (with TL): the states
+// stay in that shared-memory tile, are updated there and leave by one tile
+// store, so a thread holds none in registers and more blocks fit per SM.
+template <typename T, int N, int R, bool TL, bool HS>
+__global__ void __launch_bounds__(GD, HS ? 8 : 5)  // blocks per SM: HS 8 (64 registers), else 5
+m3_decode_kernel(const __grid_constant__ DecArgs a) {
+  static_assert(!HS || TL, "shared-memory states arrive by the tile copy");
   constexpr int G = N / 16;       // threads per channel
   constexpr int CH = GD / G;      // channels per block
   constexpr int NB = 2 * N * R;   // B and C values of one step
@@ -282,14 +286,19 @@ __global__ void __launch_bounds__(GD) m3_decode_kernel(const __grid_constant__ D
       if (tid == 0) report_timeout(&g_aux_status, nullptr);  // decode has no workspace
       return;
     }
-    const float* hs = reinterpret_cast<const float*>(dsm) + tid / G;
+    if constexpr (!HS) {
+      const float* hs = reinterpret_cast<const float*>(dsm) + tid / G;
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
+      for (int r = 0; r < R; ++r) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
-        h[r][i] = make_float2(hs[((size_t)r * N + 16 * q + 2 * i) * CH], hs[((size_t)r * N + 16 * q + 2 * i + 1) * CH]);
+        for (int i = 0; i < 8; ++i)
+          h[r][i] = make_float2(hs[((size_t)r * N + 16 * q + 2 * i) * CH], hs[((size_t)r * N + 16 * q + 2 * i + 1) * CH]);
+      }
     }
   }
+  // this thread's lane 16 q + 2 i (+1) of row r in the shared-memory tile
+  float* const hsm = reinterpret_cast<float*>(dsm) + (size_t)16 * q * CH + tid / G;
+  auto hs_at = [&](int r, int i) { return hsm + ((size_t)r * N + 2 * i) * CH; };
 
 #pragma unroll 1
   for (int t = 0; t < a.T; ++t) {
@@ -323,8 +332,17 @@ __global__ void __launch_bounds__(GD) m3_decode_kernel(const __grid_constant__ D
         const float2 bb = *reinterpret_cast<const float2*>(bc + 2 * k);
         const float2 cc = *reinterpret_cast<const float2*>(bc + N + 2 * k);
         const float2 a2 = *reinterpret_cast<const float2*>(sA[k][tid]);
-        h[r][k] = __ffma2_rn(ex2x2(__fmul2_rn(dl2, a2)), h[r][k], __fmul2_rn(du2, bb));
-        y2 = __ffma2_rn(cc, h[r][k], y2);
+        if constexpr (HS) {
+          float* hp = hs_at(r, k);
+          const float2 hn = __ffma2_rn(ex2x2(__fmul2_rn(dl2, a2)), make_float2(hp[0], hp[CH]),
+                                       __fmul2_rn(du2, bb));
+          hp[0] = hn.x;
+          hp[CH] = hn.y;
+          y2 = __ffma2_rn(cc, hn, y2);
+        } else {
+          h[r][k] = __ffma2_rn(ex2x2(__fmul2_rn(dl2, a2)), h[r][k], __fmul2_rn(du2, bb));
+          y2 = __ffma2_rn(cc, h[r][k], y2);
+        }
       }
       float ys = y2.x + y2.y;
 #pragma unroll
@@ -339,14 +357,28 @@ __global__ void __launch_bounds__(GD) m3_decode_kernel(const __grid_constant__ D
     __syncthreads();  // step t's buffer is free for step t + 2
   }
   if (a.T == 0) return;
+  if constexpr (HS) {
+    // the updated tile back by one tile store (lanes of channels past
+    // d_inner and rows past the batch are not written); the block's shared
+    // memory stays until the store has read it
+    fence_proxy_async();
+    __syncthreads();
+    if (tid == 0) {
+      tma_store_3d(&a.tm_h, dsm, blockIdx.x * CH, 0, blockIdx.y * R);
+      bulk_commit();
+      bulk_wait_read();
+    }
+  }
 #pragma unroll
   for (int r = 0; r < R; ++r) {
     if (!ron[r]) continue;
-    float* hp = a.h + ((size_t)rb[r] * N + 16 * q) * D + d;
+    if constexpr (!HS) {
+      float* hp = a.h + ((size_t)rb[r] * N + 16 * q) * D + d;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      hp[(size_t)(2 * i) * D] = h[r][i].x;
-      hp[(size_t)(2 * i + 1) * D] = h[r][i].y;
+      for (int i = 0; i < 8; ++i) {
+        hp[(size_t)(2 * i) * D] = h[r][i].x;
+        hp[(size_t)(2 * i + 1) * D] = h[r][i].y;
+      }
     }
     if (q == 0) {
       T* cp = static_cast<T*>(a.conv) + (size_t)rb[r] * 3 * D + d;
@@ -361,18 +393,19 @@ template <typename T, int N, int R>
 cudaError_t launch_decode_r(const DecArgs& a0, cudaStream_t st) {
   constexpr int CH = GD / (N / 16);
   const dim3 grid((unsigned)((a0.D + CH - 1) / CH), (unsigned)((a0.B + R - 1) / R));
-  // the carried states by tile copies when their layout allows one and the
-  // state is wide (measured: faster for d_state 32 and 64, slower for 16,
-  // where each thread's own loads already keep enough bytes in flight)
-  if (N >= 32 && reinterpret_cast<uintptr_t>(a0.h) % 16 == 0 && a0.D % 4 == 0) {
+  // the carried states in and out by tile copies, kept in shared memory in
+  // between, when their layout allows a tile map (measured on GB300, 64
+  // sequences of d_inner 5120: 8 % faster than per-thread loads into
+  // registers for d_state 16, 19-23 % for 32 and 64)
+  if (reinterpret_cast<uintptr_t>(a0.h) % 16 == 0 && a0.D % 4 == 0) {
     DecArgs a = a0;
     const uint64_t dim[3] = {(uint64_t)a.D, (uint64_t)N, (uint64_t)a.B};
     const uint64_t str[2] = {(uint64_t)a.D * 4, (uint64_t)N * a.D * 4};
     const uint32_t box[3] = {(uint32_t)CH, (uint32_t)N, (uint32_t)R};
     if (!encode_tile_map(&a.tm_h, 4, 3, a.h, dim, str, box)) return cudaErrorInvalidValue;
-    m3_decode_kernel<T, N, R, true><<<grid, GD, (size_t)R * N * CH * 4, st>>>(a);
+    m3_decode_kernel<T, N, R, true, true><<<grid, GD, (size_t)R * N * CH * 4, st>>>(a);
   } else {
-    m3_decode_kernel<T, N, R, false><<<grid, GD, 0, st>>>(a0);
+    m3_decode_kernel<T, N, R, false, false><<<grid, GD, 0, st>>>(a0);
   }
   return cudaGetLastError();
 }
